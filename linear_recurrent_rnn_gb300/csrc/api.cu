@@ -1,0 +1,319 @@
+// librglru host layer: argument validation, scratch layouts, and kernel launches on the
+// caller's stream.  No allocation, no synchronisation (except rglru_sync_status, whose job
+// it is).
+#include <stdio.h>
+#include <string.h>
+
+#include "internal.h"
+
+using namespace rglru;
+
+namespace {
+
+int g_spin_limit = 1 << 22;
+int g_drop_tile = -1;
+
+size_t dsize(int dt) { return dt == RGLRU_BF16 ? 2 : 4; }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Validates the shape and fills `d`.
+rglru_status make_dims(const rglru_shape* s, Dims* d) {
+  if (!s) return RGLRU_ERR_INVALID_ARG;
+  if (s->B < 1 || s->T < 1 || s->W < 1 || s->nblk < 1) return RGLRU_ERR_INVALID_ARG;
+  if (s->W % s->nblk) return RGLRU_ERR_INVALID_ARG;
+  if ((s->io != RGLRU_F32 && s->io != RGLRU_BF16) || (s->grad != RGLRU_F32 && s->grad != RGLRU_BF16))
+    return RGLRU_ERR_INVALID_ARG;
+  if (s->mode != RGLRU_CANONICAL && s->mode != RGLRU_RESTRICTED) return RGLRU_ERR_INVALID_ARG;
+  if (s->io == RGLRU_F32 && s->grad != RGLRU_F32) return RGLRU_ERR_UNSUPPORTED;
+  if ((size_t)s->W * dsize(s->io) % 16 || (size_t)s->W * dsize(s->grad) % 16)
+    return RGLRU_ERR_UNSUPPORTED;
+  d->B = s->B;
+  d->T = s->T;
+  d->W = s->W;
+  d->nblk = s->nblk;
+  d->k = s->W / s->nblk;
+  d->nC = (s->T + SC - 1) / SC;
+  d->ng = (s->W + 31) / 32;
+  d->N = (size_t)s->B * s->T * s->W;
+  d->io = s->io;
+  d->grad = s->grad;
+  d->mode = s->mode;
+  // ticket counters are 32-bit
+  if ((double)d->B * d->nC * d->ng >= 4.0e9) return RGLRU_ERR_UNSUPPORTED;
+  return RGLRU_OK;
+}
+
+// Required pointers: non-null and 16-byte aligned.  Optional: null or 16-byte aligned.
+bool req(const void* p) { return p && aligned16(p); }
+bool opt(const void* p) { return !p || aligned16(p); }
+
+rglru_status check_resets(const Dims& d, const uint8_t* rm, const int32_t* sp, const float* h0) {
+  if (!opt(rm) || !opt(sp) || !opt(h0)) return RGLRU_ERR_INVALID_ARG;
+  if (rm && sp) return RGLRU_ERR_INVALID_ARG;
+  if (d.mode == RGLRU_RESTRICTED && (rm || sp || h0)) return RGLRU_ERR_INVALID_ARG;
+  return RGLRU_OK;
+}
+
+rglru_status cuda_status(cudaError_t e) {
+  if (e == cudaSuccess) return RGLRU_OK;
+  fprintf(stderr, "librglru: CUDA error %s\n", cudaGetErrorString(e));
+  return RGLRU_ERR_CUDA;
+}
+
+// Fused layer through the separate kernels (float32 logits kept in `saved`).
+struct ComposedLayout {
+  size_t lr, li, total;  // within `saved`, after the scan layout
+};
+ComposedLayout composed_saved(const Dims& d) {
+  ComposedLayout C;
+  const ScanLayout L = scan_layout(d, false);
+  C.lr = align_up(L.total, 256);
+  C.li = align_up(C.lr + d.N * 4, 256);
+  C.total = align_up(C.li + d.N * 4, 256);
+  return C;
+}
+struct ComposedWs {
+  size_t dxd, dlr, dli, gate, total;  // within `workspace`, after the backward scan layout
+};
+ComposedWs composed_ws(const Dims& d) {
+  ComposedWs C;
+  const ScanLayout L = scan_layout(d, true);
+  C.dxd = align_up(L.total, 256);
+  C.dlr = align_up(C.dxd + d.N * 4, 256);
+  C.dli = align_up(C.dlr + d.N * 4, 256);
+  C.gate = align_up(C.dli + d.N * 4, 256);
+  C.total = align_up(C.gate + gate_bwd_layout(d).total, 256);
+  return C;
+}
+
+ScanFwdArgs fwd_args(const Dims& d, const void* x, const void* lr, const void* li,
+                     const float* Lambda, const uint8_t* rm, const int32_t* sp, const float* h0,
+                     void* y, float* hT, void* saved) {
+  ScanFwdArgs a;
+  a.B = d.B;
+  a.T = d.T;
+  a.W = d.W;
+  a.nC = d.nC;
+  a.ng = d.ng;
+  a.x = x;
+  a.lr = lr;
+  a.li = li;
+  a.Lambda = Lambda;
+  a.reset_mask = rm;
+  a.segment_pos = sp;
+  a.h0 = h0;
+  a.y = y;
+  a.hT = hT;
+  a.scratch = static_cast<uint8_t*>(saved);
+  a.L = scan_layout(d, false);
+  a.spin_limit = g_spin_limit;
+  a.drop_tile = g_drop_tile;
+  return a;
+}
+
+ScanBwdArgs bwd_args(const Dims& d, const void* dy, const float* dhT, const void* x,
+                     const void* lr, const void* li, const float* Lambda, const uint8_t* rm,
+                     const int32_t* sp, const float* h0, const void* saved, void* dx, void* dlr,
+                     void* dli, float* dLambda, float* dh0, void* ws) {
+  ScanBwdArgs a;
+  a.B = d.B;
+  a.T = d.T;
+  a.W = d.W;
+  a.nC = d.nC;
+  a.ng = d.ng;
+  a.dy = dy;
+  a.dhT = dhT;
+  a.x = x;
+  a.lr = lr;
+  a.li = li;
+  a.Lambda = Lambda;
+  a.reset_mask = rm;
+  a.segment_pos = sp;
+  a.h0 = h0;
+  a.fwd_carry = reinterpret_cast<const float*>(static_cast<const uint8_t*>(saved) +
+                                                scan_layout(d, false).carry);
+  a.dx = dx;
+  a.dlr = dlr;
+  a.dli = dli;
+  a.dLambda = dLambda;
+  a.dh0 = dh0;
+  a.scratch = static_cast<uint8_t*>(ws);
+  a.L = scan_layout(d, true);
+  a.spin_limit = g_spin_limit;
+  a.drop_tile = g_drop_tile;
+  return a;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* rglru_status_string(rglru_status s) {
+  switch (s) {
+    case RGLRU_OK: return "ok";
+    case RGLRU_ERR_INVALID_ARG: return "invalid argument";
+    case RGLRU_ERR_UNSUPPORTED: return "unsupported shape or dtype";
+    case RGLRU_ERR_CUDA: return "CUDA error";
+    case RGLRU_ERR_TIMEOUT: return "look-back wait timed out";
+  }
+  return "unknown status";
+}
+
+size_t rglru_saved_bytes(const rglru_shape* shape) {
+  Dims d;
+  if (make_dims(shape, &d) != RGLRU_OK) return 0;
+  const size_t a = scan_layout(d, false).total;
+  const size_t b = composed_saved(d).total;
+  return a > b ? a : b;
+}
+
+size_t rglru_workspace_bytes(const rglru_shape* shape) {
+  Dims d;
+  if (make_dims(shape, &d) != RGLRU_OK) return 0;
+  size_t m = scan_layout(d, true).total;
+  const size_t g = gate_bwd_layout(d).total;
+  const size_t c = composed_ws(d).total;
+  if (g > m) m = g;
+  if (c > m) m = c;
+  return m;
+}
+
+rglru_status rglru_gate_proj(const rglru_shape* shape, const void* x, const void* Wa,
+                             const float* ba, const void* Wx, const float* bx, void* lr, void* li,
+                             rglru_stream stream) {
+  Dims d;
+  rglru_status st = make_dims(shape, &d);
+  if (st != RGLRU_OK) return st;
+  if (!req(x) || !req(Wa) || !req(Wx) || !req(lr) || !req(li) || !opt(ba) || !opt(bx))
+    return RGLRU_ERR_INVALID_ARG;
+  return cuda_status(launch_gate_proj_simt(d, d.io, d.io, x, Wa, ba, Wx, bx, lr, li, stream));
+}
+
+rglru_status rglru_forward(const rglru_shape* shape, const void* x, const void* lr,
+                           const void* li, const float* Lambda, const uint8_t* reset_mask,
+                           const int32_t* segment_pos, const float* h0, void* y, float* hT,
+                           void* saved, rglru_stream stream) {
+  Dims d;
+  rglru_status st = make_dims(shape, &d);
+  if (st != RGLRU_OK) return st;
+  if (!req(x) || !req(lr) || !req(li) || !req(Lambda) || !req(y) || !opt(hT) || !req(saved))
+    return RGLRU_ERR_INVALID_ARG;
+  if ((st = check_resets(d, reset_mask, segment_pos, h0)) != RGLRU_OK) return st;
+  const ScanFwdArgs a = fwd_args(d, x, lr, li, Lambda, reset_mask, segment_pos, h0, y, hT, saved);
+  cudaError_t e = cudaMemsetAsync(saved, 0, a.L.zero_bytes, stream);
+  if (e == cudaSuccess) e = launch_scan_fwd(a, d.io, d.io, d.mode == RGLRU_CANONICAL, stream);
+  return cuda_status(e);
+}
+
+rglru_status rglru_backward(const rglru_shape* shape, const void* dy, const float* dhT,
+                            const void* x, const void* lr, const void* li, const float* Lambda,
+                            const uint8_t* reset_mask, const int32_t* segment_pos,
+                            const float* h0, const void* saved, void* dx, void* dlr, void* dli,
+                            float* dLambda, float* dh0, void* workspace, rglru_stream stream) {
+  Dims d;
+  rglru_status st = make_dims(shape, &d);
+  if (st != RGLRU_OK) return st;
+  if (!req(dy) || !opt(dhT) || !req(x) || !req(lr) || !req(li) || !req(Lambda) || !req(saved) ||
+      !req(dx) || !req(dlr) || !req(dli) || !req(dLambda) || !opt(dh0) || !req(workspace))
+    return RGLRU_ERR_INVALID_ARG;
+  if ((st = check_resets(d, reset_mask, segment_pos, h0)) != RGLRU_OK) return st;
+  const ScanBwdArgs a = bwd_args(d, dy, dhT, x, lr, li, Lambda, reset_mask, segment_pos, h0, saved,
+                                 dx, dlr, dli, dLambda, dh0, workspace);
+  cudaError_t e = cudaMemsetAsync(workspace, 0, a.L.zero_bytes, stream);
+  if (e == cudaSuccess)
+    e = launch_scan_bwd(a, d.io, d.io, d.grad, d.grad, d.mode == RGLRU_CANONICAL, stream);
+  return cuda_status(e);
+}
+
+rglru_status rglru_gate_proj_backward(const rglru_shape* shape, const void* dlr, const void* dli,
+                                      const void* x, const void* Wa, const void* Wx, void* dx,
+                                      float* dWa, float* dba, float* dWx, float* dbx,
+                                      void* workspace, rglru_stream stream) {
+  Dims d;
+  rglru_status st = make_dims(shape, &d);
+  if (st != RGLRU_OK) return st;
+  if (!req(dlr) || !req(dli) || !req(x) || !req(Wa) || !req(Wx) || !req(dx) || !req(dWa) ||
+      !req(dWx) || !opt(dba) || !opt(dbx) || !req(workspace))
+    return RGLRU_ERR_INVALID_ARG;
+  cudaError_t e =
+      launch_gate_dx_simt(d, d.io, d.grad, d.grad, dlr, dli, Wa, Wx, nullptr, dx, stream);
+  if (e == cudaSuccess)
+    e = launch_gate_dw_simt(d, d.io, d.grad, x, dlr, dli, dWa, dba, dWx, dbx,
+                            static_cast<uint8_t*>(workspace), stream);
+  return cuda_status(e);
+}
+
+rglru_status rglru_fused_forward(const rglru_shape* shape, const void* x, const void* Wa,
+                                 const float* ba, const void* Wx, const float* bx,
+                                 const float* Lambda, const uint8_t* reset_mask,
+                                 const int32_t* segment_pos, const float* h0, void* y, float* hT,
+                                 void* saved, rglru_stream stream) {
+  Dims d;
+  rglru_status st = make_dims(shape, &d);
+  if (st != RGLRU_OK) return st;
+  if (!req(x) || !req(Wa) || !req(Wx) || !opt(ba) || !opt(bx) || !req(Lambda) || !req(y) ||
+      !opt(hT) || !req(saved))
+    return RGLRU_ERR_INVALID_ARG;
+  if ((st = check_resets(d, reset_mask, segment_pos, h0)) != RGLRU_OK) return st;
+  uint8_t* sv = static_cast<uint8_t*>(saved);
+  const ComposedLayout C = composed_saved(d);
+  cudaError_t e = launch_gate_proj_simt(d, d.io, DT_F32, x, Wa, ba, Wx, bx, sv + C.lr, sv + C.li,
+                                        stream);
+  const ScanFwdArgs a = fwd_args(d, x, sv + C.lr, sv + C.li, Lambda, reset_mask, segment_pos, h0,
+                                 y, hT, saved);
+  if (e == cudaSuccess) e = cudaMemsetAsync(saved, 0, a.L.zero_bytes, stream);
+  if (e == cudaSuccess) e = launch_scan_fwd(a, d.io, DT_F32, d.mode == RGLRU_CANONICAL, stream);
+  return cuda_status(e);
+}
+
+rglru_status rglru_fused_backward(const rglru_shape* shape, const void* dy, const float* dhT,
+                                  const void* x, const void* Wa, const float* ba, const void* Wx,
+                                  const float* bx, const float* Lambda,
+                                  const uint8_t* reset_mask, const int32_t* segment_pos,
+                                  const float* h0, const void* saved, void* dx, float* dWa,
+                                  float* dba, float* dWx, float* dbx, float* dLambda, float* dh0,
+                                  void* workspace, rglru_stream stream) {
+  Dims d;
+  rglru_status st = make_dims(shape, &d);
+  if (st != RGLRU_OK) return st;
+  if (!req(dy) || !opt(dhT) || !req(x) || !req(Wa) || !req(Wx) || !opt(ba) || !opt(bx) ||
+      !req(Lambda) || !req(saved) || !req(dx) || !req(dWa) || !req(dWx) || !opt(dba) ||
+      !opt(dbx) || !req(dLambda) || !opt(dh0) || !req(workspace))
+    return RGLRU_ERR_INVALID_ARG;
+  if ((st = check_resets(d, reset_mask, segment_pos, h0)) != RGLRU_OK) return st;
+  const uint8_t* sv = static_cast<const uint8_t*>(saved);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  const ComposedLayout C = composed_saved(d);
+  const ComposedWs CW = composed_ws(d);
+  const ScanBwdArgs a = bwd_args(d, dy, dhT, x, sv + C.lr, sv + C.li, Lambda, reset_mask,
+                                 segment_pos, h0, saved, ws + CW.dxd, ws + CW.dlr, ws + CW.dli,
+                                 dLambda, dh0, workspace);
+  // The direct term of dx stays float32 until the projections are added: one rounding.
+  cudaError_t e = cudaMemsetAsync(workspace, 0, a.L.zero_bytes, stream);
+  if (e == cudaSuccess)
+    e = launch_scan_bwd(a, d.io, DT_F32, DT_F32, DT_F32, d.mode == RGLRU_CANONICAL, stream);
+  if (e == cudaSuccess)
+    e = launch_gate_dx_simt(d, d.io, DT_F32, d.grad, ws + CW.dlr, ws + CW.dli, Wa, Wx,
+                            reinterpret_cast<const float*>(ws + CW.dxd), dx, stream);
+  if (e == cudaSuccess)
+    e = launch_gate_dw_simt(d, d.io, DT_F32, x, ws + CW.dlr, ws + CW.dli, dWa, dba, dWx, dbx,
+                            ws + CW.gate, stream);
+  return cuda_status(e);
+}
+
+rglru_status rglru_sync_status(const void* buf, rglru_stream stream) {
+  if (!buf) return RGLRU_ERR_INVALID_ARG;
+  uint32_t word = 0;
+  cudaError_t e = cudaStreamSynchronize(stream);
+  if (e == cudaSuccess) e = cudaMemcpy(&word, buf, sizeof(word), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_status(e);
+  return (word & 1u) ? RGLRU_ERR_TIMEOUT : RGLRU_OK;
+}
+
+void rglru_debug_lookback(int32_t spin_limit, int32_t drop_tile) {
+  g_spin_limit = spin_limit > 0 ? spin_limit : (1 << 22);
+  g_drop_tile = drop_tile;
+}
+
+}  // extern "C"

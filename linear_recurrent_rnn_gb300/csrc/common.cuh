@@ -1,0 +1,114 @@
+// Device helpers shared by the librglru kernels: element access for the two I/O dtypes,
+// the gate and decay arithmetic in float32, and the flag protocol of the cross-chunk
+// look-back.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace rglru {
+
+using bf16 = __nv_bfloat16;
+
+// ---------------------------------------------------------------- element pairs
+// Two adjacent channels per access (4 bytes of bf16, 8 bytes of float).
+template <typename T>
+struct Pair;
+
+template <>
+struct Pair<float> {
+  static __device__ __forceinline__ float2 load(const float* p) {
+    return *reinterpret_cast<const float2*>(p);
+  }
+  static __device__ __forceinline__ void store(float* p, float a, float b) {
+    *reinterpret_cast<float2*>(p) = make_float2(a, b);
+  }
+  static __device__ __forceinline__ float load1(const float* p) { return *p; }
+};
+
+template <>
+struct Pair<bf16> {
+  static __device__ __forceinline__ float2 load(const bf16* p) {
+    return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(p));
+  }
+  static __device__ __forceinline__ void store(bf16* p, float a, float b) {
+    *reinterpret_cast<__nv_bfloat162*>(p) = __floats2bfloat162_rn(a, b);
+  }
+  static __device__ __forceinline__ float load1(const bf16* p) { return __bfloat162float(*p); }
+};
+
+template <typename T>
+__device__ __forceinline__ T from_f32(float v);
+template <>
+__device__ __forceinline__ float from_f32<float>(float v) { return v; }
+template <>
+__device__ __forceinline__ bf16 from_f32<bf16>(float v) { return __float2bfloat16_rn(v); }
+
+template <typename T>
+__device__ __forceinline__ float to_f32(T v);
+template <>
+__device__ __forceinline__ float to_f32<float>(float v) { return v; }
+template <>
+__device__ __forceinline__ float to_f32<bf16>(bf16 v) { return __bfloat162float(v); }
+
+// ---------------------------------------------------------------- gate arithmetic
+// sigmoid(z) = 1 / (1 + e^-z); e^-z overflows to +inf for very negative z, giving 0.
+__device__ __forceinline__ float sigmoid_f(float z) {
+  return __fdividef(1.0f, 1.0f + __expf(-z));
+}
+
+// softplus(z) = log(1 + e^z) in the overflow-free form; once per channel, full precision.
+__device__ __forceinline__ float softplus_f(float z) {
+  return z > 0.0f ? z + log1pf(expf(-z)) : log1pf(expf(z));
+}
+
+// 1 - a^2 for a = e^la, la <= 0, without the cancellation of 1 - a*a as a -> 1.
+__device__ __forceinline__ float one_minus_a2(float la) { return -expm1f(2.0f * la); }
+
+// Reset flag of token (b, t) in canonical mode.
+__device__ __forceinline__ bool is_reset(const uint8_t* reset_mask, const int32_t* segment_pos,
+                                         size_t bt) {
+  if (reset_mask) return reset_mask[bt] != 0;
+  if (segment_pos) return segment_pos[bt] == 0;
+  return false;
+}
+
+// ---------------------------------------------------------------- look-back flags
+// A scan tile publishes FLAG_AGG once its own affine aggregate (A, B) is stored, and
+// FLAG_INCL once its chunk-boundary state (the "inclusive prefix") is stored.  Flags are
+// zeroed before every launch.
+constexpr uint32_t FLAG_AGG = 1u;
+constexpr uint32_t FLAG_INCL = 2u;
+constexpr uint32_t FLAG_TIMEOUT = 0xffffffffu;  // returned by spin_flag only
+constexpr uint32_t STATUS_TIMEOUT = 1u;
+
+__device__ __forceinline__ uint32_t ld_acquire(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void st_release(uint32_t* p, uint32_t v) {
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// Polls `flag` until it reaches `target` (FLAG_AGG or FLAG_INCL), at most `limit` times.  On
+// running out it records the timeout in `status` and returns FLAG_TIMEOUT, so the caller
+// carries on (with a zero carry) and the kernel always terminates.
+__device__ __forceinline__ uint32_t spin_flag(const uint32_t* flag, uint32_t target, int limit,
+                                              uint32_t* status) {
+  uint32_t f = ld_acquire(flag);
+  int it = 0;
+  while (f < target) {
+    if (++it > limit) {
+      atomicOr(status, STATUS_TIMEOUT);
+      return FLAG_TIMEOUT;
+    }
+    __nanosleep(64);
+    f = ld_acquire(flag);
+  }
+  return f;
+}
+
+}  // namespace rglru

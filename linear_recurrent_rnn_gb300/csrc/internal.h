@@ -1,0 +1,140 @@
+// Internal interfaces between librglru's host layer and its kernel translation units:
+// buffer layouts of `saved` / `workspace`, kernel argument blocks and launchers.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/librglru.h"
+
+namespace rglru {
+
+// Tokens per scan chunk of the SIMT scan kernels: a warp owns 32 channels x SC tokens,
+// each lane two channels x SUB tokens.
+constexpr int SC = 16;
+constexpr int SUB = 8;
+// Every ANCHOR-th chunk (counted from the start in the forward, from the end in the
+// backward) publishes its chunk-boundary state; a tile's look-back composes the aggregates of
+// the chunks after the nearest anchor and applies them to that anchor's state.  The carry
+// each tile sees is therefore a fixed expression of the inputs, independent of timing: the
+// scan is bitwise deterministic.
+constexpr int ANCHOR = 8;
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+struct Dims {
+  int B, T, W, nblk, k;
+  int nC;  // scan chunks per row: ceil(T / SC)
+  int ng;  // 32-channel groups: ceil(W / 32)
+  size_t N;
+  int io, grad, mode;
+};
+
+// Scan scratch: [0, zero_bytes) is cleared before each launch (status word, ticket, flags).
+//   header: u32 status, u32 ticket (256 bytes)
+//   flags  u32 [B][nC][ng]
+//   carry  f32 [B][nC+1][W]   forward: state entering chunk c (c = nC: hT)
+//                             backward: carry passed from chunk c to chunk c-1
+//   agg    float2 [B][nC][W]  per-chunk affine aggregate (A, B)
+//   part   f32 [B*nC][W]      backward only: per-chunk dLambda partial sums
+struct ScanLayout {
+  size_t flags, zero_bytes, carry, agg, part, total;
+};
+
+inline ScanLayout scan_layout(const Dims& d, bool backward) {
+  ScanLayout L;
+  const size_t nflags = (size_t)d.B * d.nC * d.ng;
+  L.flags = 256;
+  L.zero_bytes = align_up(L.flags + nflags * 4, 256);
+  L.carry = L.zero_bytes;
+  L.agg = align_up(L.carry + (size_t)d.B * (d.nC + 1) * d.W * 4, 256);
+  L.part = align_up(L.agg + (size_t)d.B * d.nC * d.W * 8, 256);
+  L.total = backward ? align_up(L.part + (size_t)d.B * d.nC * d.W * 4, 256) : L.part;
+  return L;
+}
+
+// Split-K layout of the SIMT projection-weight gradient.
+inline int dw_splits(const Dims& d) {
+  const int tiles = ((d.k + 63) / 64) * ((d.k + 63) / 64) * d.nblk * 2;
+  const long BT = (long)d.B * d.T;
+  long s = (600 + tiles - 1) / tiles;
+  const long smax = (BT + 255) / 256;
+  if (s > smax) s = smax;
+  if (s < 1) s = 1;
+  if (s > 64) s = 64;
+  return (int)s;
+}
+
+struct GateBwdLayout {
+  size_t dw_part, db_part, total;
+};
+
+inline GateBwdLayout gate_bwd_layout(const Dims& d) {
+  GateBwdLayout L;
+  const int S = dw_splits(d);
+  L.dw_part = 0;
+  L.db_part = align_up((size_t)S * 2 * d.nblk * d.k * d.k * 4, 256);
+  L.total = align_up(L.db_part + (size_t)S * 2 * d.W * 4, 256);
+  return L;
+}
+
+// ---------------------------------------------------------------- kernel arguments
+struct ScanFwdArgs {
+  int B, T, W, nC, ng;
+  const void* x;
+  const void* lr;
+  const void* li;
+  const float* Lambda;
+  const uint8_t* reset_mask;
+  const int32_t* segment_pos;
+  const float* h0;
+  void* y;
+  float* hT;
+  uint8_t* scratch;  // `saved`
+  ScanLayout L;
+  int spin_limit, drop_tile;
+};
+
+struct ScanBwdArgs {
+  int B, T, W, nC, ng;
+  const void* dy;
+  const float* dhT;
+  const void* x;
+  const void* lr;
+  const void* li;
+  const float* Lambda;
+  const uint8_t* reset_mask;
+  const int32_t* segment_pos;
+  const float* h0;
+  const float* fwd_carry;  // from `saved`: state entering each chunk
+  void* dx;
+  void* dlr;
+  void* dli;
+  float* dLambda;
+  float* dh0;
+  uint8_t* scratch;  // `workspace`
+  ScanLayout L;
+  int spin_limit, drop_tile;
+};
+
+// dtype codes used by the launchers (io of x/y/dy, of the logits, of dx, of dlr/dli)
+enum { DT_F32 = RGLRU_F32, DT_BF16 = RGLRU_BF16 };
+
+cudaError_t launch_scan_fwd(const ScanFwdArgs& a, int xt, int lt, bool canonical,
+                            cudaStream_t s);
+cudaError_t launch_scan_bwd(const ScanBwdArgs& a, int xt, int lt, int dxt, int dlt,
+                            bool canonical, cudaStream_t s);
+
+// SIMT projections (float32 accumulation).
+cudaError_t launch_gate_proj_simt(const Dims& d, int xt, int ot, const void* x, const void* Wa,
+                                  const float* ba, const void* Wx, const float* bx, void* lr,
+                                  void* li, cudaStream_t s);
+cudaError_t launch_gate_dx_simt(const Dims& d, int wt, int gt, int dxt, const void* dlr,
+                                const void* dli, const void* Wa, const void* Wx,
+                                const float* dx_in, void* dx, cudaStream_t s);
+cudaError_t launch_gate_dw_simt(const Dims& d, int xt, int gt, const void* x, const void* dlr,
+                                const void* dli, float* dWa, float* dba, float* dWx, float* dbx,
+                                uint8_t* ws, cudaStream_t s);
+
+}  // namespace rglru

@@ -1,0 +1,190 @@
+"""Thin ctypes binding of librglru (include/librglru.h).
+
+Argument marshalling only: every function here checks that its tensors are contiguous CUDA
+tensors, passes their device pointers and the current CUDA stream to the C ABI call of the
+same name, and raises ``RglruError`` on a non-OK status.  No arithmetic runs in Python and
+there is no fallback: if the shared library is missing, the first call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Optional
+
+import torch
+
+from . import build as _build
+
+F32, BF16 = 0, 1
+CANONICAL, RESTRICTED = 0, 1
+OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT = range(5)
+
+_DT = {torch.float32: F32, torch.bfloat16: BF16}
+TORCH_DT = {F32: torch.float32, BF16: torch.bfloat16}
+
+
+class RglruError(RuntimeError):
+    def __init__(self, fn, status):
+        self.status = status
+        super().__init__(f"{fn}: {status_string(status)} ({status})")
+
+
+class Shape(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int32), ("T", ctypes.c_int32), ("W", ctypes.c_int32),
+                ("nblk", ctypes.c_int32), ("io", ctypes.c_int32), ("grad", ctypes.c_int32),
+                ("mode", ctypes.c_int32)]
+
+    def __repr__(self):
+        return (f"Shape(B={self.B}, T={self.T}, W={self.W}, nblk={self.nblk}, io={self.io}, "
+                f"grad={self.grad}, mode={self.mode})")
+
+
+_lock = threading.Lock()
+_lib = None
+
+EXPORTS = ("rglru_status_string", "rglru_saved_bytes", "rglru_workspace_bytes",
+           "rglru_gate_proj", "rglru_forward", "rglru_backward", "rglru_gate_proj_backward",
+           "rglru_fused_forward", "rglru_fused_backward", "rglru_sync_status",
+           "rglru_debug_lookback")
+
+
+def library_path() -> str:
+    return os.environ.get("RGLRU_LIBRARY", _build.LIB)
+
+
+def lib():
+    """The loaded shared library (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = library_path()
+            if not os.path.exists(path):
+                raise RuntimeError(f"librglru is not built ({path} missing); call "
+                                   "linear_recurrent_rnn_gb300.build.build() first")
+            L = ctypes.CDLL(path)
+            P, S = ctypes.c_void_p, ctypes.POINTER(Shape)
+            L.rglru_status_string.argtypes = [ctypes.c_int]
+            L.rglru_status_string.restype = ctypes.c_char_p
+            L.rglru_saved_bytes.argtypes = [S]
+            L.rglru_saved_bytes.restype = ctypes.c_size_t
+            L.rglru_workspace_bytes.argtypes = [S]
+            L.rglru_workspace_bytes.restype = ctypes.c_size_t
+            L.rglru_gate_proj.argtypes = [S] + [P] * 8
+            L.rglru_forward.argtypes = [S] + [P] * 11
+            L.rglru_backward.argtypes = [S] + [P] * 17
+            L.rglru_gate_proj_backward.argtypes = [S] + [P] * 12
+            L.rglru_fused_forward.argtypes = [S] + [P] * 13
+            L.rglru_fused_backward.argtypes = [S] + [P] * 21
+            L.rglru_sync_status.argtypes = [P, P]
+            L.rglru_debug_lookback.argtypes = [ctypes.c_int32, ctypes.c_int32]
+            L.rglru_debug_lookback.restype = None
+            for n in ("rglru_gate_proj", "rglru_forward", "rglru_backward",
+                      "rglru_gate_proj_backward", "rglru_fused_forward", "rglru_fused_backward",
+                      "rglru_sync_status"):
+                getattr(L, n).restype = ctypes.c_int
+            _lib = L
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return lib().rglru_status_string(int(status)).decode()
+
+
+def make_shape(B, T, W, nblk, io=BF16, grad=None, mode=CANONICAL) -> Shape:
+    if isinstance(io, torch.dtype):
+        io = _DT[io]
+    if grad is None:
+        grad = io
+    elif isinstance(grad, torch.dtype):
+        grad = _DT[grad]
+    return Shape(int(B), int(T), int(W), int(nblk), int(io), int(grad), int(mode))
+
+
+def saved_bytes(shape: Shape) -> int:
+    return int(lib().rglru_saved_bytes(ctypes.byref(shape)))
+
+
+def workspace_bytes(shape: Shape) -> int:
+    return int(lib().rglru_workspace_bytes(ctypes.byref(shape)))
+
+
+def alloc_saved(shape: Shape, device="cuda") -> torch.Tensor:
+    return torch.empty(max(1, saved_bytes(shape)), dtype=torch.uint8, device=device)
+
+
+def alloc_workspace(shape: Shape, device="cuda") -> torch.Tensor:
+    return torch.empty(max(1, workspace_bytes(shape)), dtype=torch.uint8, device=device)
+
+
+def _p(t: Optional[torch.Tensor]):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("librglru takes CUDA tensors")
+    if not t.is_contiguous():
+        raise ValueError("librglru takes contiguous tensors")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _check(fn, st):
+    if st != OK:
+        raise RglruError(fn, st)
+
+
+def rglru_gate_proj(shape, x, Wa, ba, Wx, bx, lr, li, stream=None):
+    _check("rglru_gate_proj", lib().rglru_gate_proj(
+        ctypes.byref(shape), _p(x), _p(Wa), _p(ba), _p(Wx), _p(bx), _p(lr), _p(li),
+        _stream(stream)))
+
+
+def rglru_forward(shape, x, lr, li, Lambda, reset_mask, segment_pos, h0, y, hT, saved,
+                  stream=None):
+    _check("rglru_forward", lib().rglru_forward(
+        ctypes.byref(shape), _p(x), _p(lr), _p(li), _p(Lambda), _p(reset_mask), _p(segment_pos),
+        _p(h0), _p(y), _p(hT), _p(saved), _stream(stream)))
+
+
+def rglru_backward(shape, dy, dhT, x, lr, li, Lambda, reset_mask, segment_pos, h0, saved, dx,
+                   dlr, dli, dLambda, dh0, workspace, stream=None):
+    _check("rglru_backward", lib().rglru_backward(
+        ctypes.byref(shape), _p(dy), _p(dhT), _p(x), _p(lr), _p(li), _p(Lambda),
+        _p(reset_mask), _p(segment_pos), _p(h0), _p(saved), _p(dx), _p(dlr), _p(dli),
+        _p(dLambda), _p(dh0), _p(workspace), _stream(stream)))
+
+
+def rglru_gate_proj_backward(shape, dlr, dli, x, Wa, Wx, dx, dWa, dba, dWx, dbx, workspace,
+                             stream=None):
+    _check("rglru_gate_proj_backward", lib().rglru_gate_proj_backward(
+        ctypes.byref(shape), _p(dlr), _p(dli), _p(x), _p(Wa), _p(Wx), _p(dx), _p(dWa), _p(dba),
+        _p(dWx), _p(dbx), _p(workspace), _stream(stream)))
+
+
+def rglru_fused_forward(shape, x, Wa, ba, Wx, bx, Lambda, reset_mask, segment_pos, h0, y, hT,
+                        saved, stream=None):
+    _check("rglru_fused_forward", lib().rglru_fused_forward(
+        ctypes.byref(shape), _p(x), _p(Wa), _p(ba), _p(Wx), _p(bx), _p(Lambda), _p(reset_mask),
+        _p(segment_pos), _p(h0), _p(y), _p(hT), _p(saved), _stream(stream)))
+
+
+def rglru_fused_backward(shape, dy, dhT, x, Wa, ba, Wx, bx, Lambda, reset_mask, segment_pos, h0,
+                         saved, dx, dWa, dba, dWx, dbx, dLambda, dh0, workspace, stream=None):
+    _check("rglru_fused_backward", lib().rglru_fused_backward(
+        ctypes.byref(shape), _p(dy), _p(dhT), _p(x), _p(Wa), _p(ba), _p(Wx), _p(bx), _p(Lambda),
+        _p(reset_mask), _p(segment_pos), _p(h0), _p(saved), _p(dx), _p(dWa), _p(dba), _p(dWx),
+        _p(dbx), _p(dLambda), _p(dh0), _p(workspace), _stream(stream)))
+
+
+def rglru_sync_status(buf: torch.Tensor, stream=None) -> int:
+    """Synchronises the stream and returns the status word of a saved/workspace buffer."""
+    return int(lib().rglru_sync_status(_p(buf), _stream(stream)))
+
+
+def rglru_debug_lookback(spin_limit: int, drop_tile: int) -> None:
+    lib().rglru_debug_lookback(int(spin_limit), int(drop_tile))

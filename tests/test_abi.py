@@ -1,0 +1,88 @@
+"""CPU checks of the C ABI: the library builds and loads without a GPU, exports every symbol
+that include/librglru.h declares, sizes its scratch buffers, and rejects invalid arguments on
+the host before touching CUDA."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+from linear_recurrent_rnn_gb300 import build as B_
+from linear_recurrent_rnn_gb300 import librglru as R
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "librglru.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    B_.build()
+    return R.lib()
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(rglru_[a-z_]+)\s*\(", src)))
+
+
+def test_header_declares_the_api():
+    names = declared_functions()
+    for n in ("rglru_gate_proj", "rglru_forward", "rglru_backward", "rglru_gate_proj_backward",
+              "rglru_fused_forward", "rglru_fused_backward", "rglru_saved_bytes",
+              "rglru_workspace_bytes", "rglru_status_string", "rglru_sync_status"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", B_.LIB], capture_output=True, text=True,
+                         check=True).stdout
+    exported = set(re.findall(r"\bT (rglru_\w+)", out))
+    missing = [n for n in declared_functions() if n not in exported]
+    assert not missing, missing
+    for n in declared_functions():
+        assert hasattr(lib, n)
+    assert set(R.EXPORTS) <= set(declared_functions())
+
+
+def test_status_strings(lib):
+    assert R.status_string(R.OK) == "ok"
+    assert "timed out" in R.status_string(R.ERR_TIMEOUT)
+
+
+def test_scratch_sizes(lib):
+    sh = R.make_shape(4, 2048, 2048, 16, R.BF16, R.BF16, R.RESTRICTED)
+    s, w = R.saved_bytes(sh), R.workspace_bytes(sh)
+    # the saved chunk states alone are B*(ceil(T/16)+1)*W float32
+    assert s >= 4 * (2048 // 16 + 1) * 2048 * 4
+    assert w > 0
+    assert R.saved_bytes(R.make_shape(1, 1, 8, 1)) > 0
+    # invalid shapes size to zero
+    assert R.saved_bytes(R.make_shape(0, 1, 8, 1)) == 0
+    assert R.saved_bytes(R.make_shape(1, 1, 10, 3)) == 0          # W % nblk
+    assert R.workspace_bytes(R.make_shape(1, 1, 12, 1)) == 0      # 12 bf16 = 24 bytes, not 16-aligned
+    assert R.saved_bytes(R.make_shape(1, 4, 8, 1, R.F32, R.BF16)) == 0   # f32 io needs f32 grads
+
+
+def _call_forward(lib, sh, x=16, lr=16, li=16, L=16, rm=None, sp=None, h0=None, y=16, saved=16):
+    P = lambda v: None if v is None else ctypes.c_void_p(v)
+    return lib.rglru_forward(ctypes.byref(sh), P(x), P(lr), P(li), P(L), P(rm), P(sp), P(h0),
+                             P(y), None, P(saved), None)
+
+
+def test_host_validation_rejects_before_cuda(lib):
+    """Fake (never dereferenced) addresses: every one of these fails validation on the host."""
+    good = R.make_shape(1, 4, 16, 1, R.BF16, R.BF16, R.CANONICAL)
+    res = R.make_shape(1, 4, 16, 1, R.BF16, R.BF16, R.RESTRICTED)
+    A = 1 << 20
+    assert _call_forward(lib, good, x=None) == R.ERR_INVALID_ARG
+    assert _call_forward(lib, good, x=A + 8) == R.ERR_INVALID_ARG          # misaligned
+    assert _call_forward(lib, good, rm=A, sp=A) == R.ERR_INVALID_ARG       # both reset forms
+    assert _call_forward(lib, res, rm=A) == R.ERR_INVALID_ARG              # restricted + resets
+    assert _call_forward(lib, res, h0=A) == R.ERR_INVALID_ARG              # restricted + h0
+    bad = R.make_shape(1, 4, 12, 1, R.BF16, R.BF16, R.CANONICAL)
+    assert _call_forward(lib, bad) == R.ERR_UNSUPPORTED
+    bad = R.make_shape(1, 0, 16, 1, R.BF16, R.BF16, R.CANONICAL)
+    assert _call_forward(lib, bad) == R.ERR_INVALID_ARG
+    assert lib.rglru_sync_status(None, None) == R.ERR_INVALID_ARG

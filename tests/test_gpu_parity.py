@@ -1,0 +1,284 @@
+"""GPU parity: every librglru entry point against the float64 oracle on identical seeded
+inputs, at sizes the oracle finishes in seconds that still span several scan chunks, warp
+tiles and GEMM tiles, with ragged tails and the method's degenerate cases."""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from helpers import assert_close, dev, host, mode_id, oracle_inputs, shape_for
+from linear_recurrent_rnn_gb300 import build as B_
+from linear_recurrent_rnn_gb300 import librglru as R
+from linear_recurrent_rnn_gb300.inputs import WORKLOADS, Workload, generate
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    B_.build()
+    R.lib()
+
+
+def W_(name, B, T, W, k, io, mode, *args, **kw):
+    return Workload(name, B, T, W, k, io, mode, *args, **kw)
+
+
+SCAN_CASES = [
+    (WORKLOADS[1], 1, None),
+    (W_("f32-res", 2, 37, 64, 64, "f32", "restricted"), 2, None),
+    (W_("bf16-res-ragged", 2, 100, 256, 256, "bf16", "restricted"), 3, None),
+    (W_("bf16-res-ragged-g32", 2, 100, 256, 256, "bf16", "restricted"), 3, "f32"),
+    (W_("bf16-can-W72", 3, 129, 72, 72, "bf16", "canonical", reset_p=0.1, h0_std=1.0), 4, None),
+    (W_("bf16-can-packed", 2, 200, 128, 128, "bf16", "canonical", seg_len=(1, 40),
+        continuation=True, h0_std=0.5), 5, "f32"),
+    (W_("bf16-T1", 3, 1, 64, 64, "bf16", "canonical", h0_std=1.0), 6, None),
+    (W_("bf16-T1-res", 2, 1, 64, 64, "bf16", "restricted"), 7, None),
+    (W_("bf16-W8-T33", 2, 33, 8, 8, "bf16", "canonical", reset_p=0.2, h0_std=1.0), 8, None),
+    (W_("bf16-all-reset", 2, 40, 64, 64, "bf16", "canonical", reset_p=1.0, h0_std=1.0), 9, None),
+    (W_("f32-T17-noreset-h0", 2, 17, 32, 32, "f32", "canonical", h0_std=1.0), 10, None),
+    (W_("bf16-longmem", 1, 600, 96, 96, "bf16", "canonical", (0.99, 0.9999), reset_p=1e-3), 11,
+     "f32"),
+]
+
+
+def _gdt(sh):
+    return R.TORCH_DT[sh.grad]
+
+
+def run_scan_gpu(wl, inp, sh):
+    d = {k: dev(v) for k, v in inp.items()}
+    io = d["x"].dtype
+    y = torch.empty_like(d["x"])
+    hT = torch.empty(wl.B, wl.W, dtype=torch.float32, device="cuda")
+    saved = R.alloc_saved(sh)
+    ws = R.alloc_workspace(sh)
+    R.rglru_forward(sh, d["x"], d["lr"], d["li"], d["Lambda"], d["reset_mask"], d["segment_pos"],
+                    d["h0"], y, hT, saved)
+    gd = _gdt(sh)
+    out = {"y": y, "hT": hT}
+    out["dx"] = torch.empty(d["x"].shape, dtype=gd, device="cuda")
+    out["dlr"] = torch.empty_like(out["dx"])
+    out["dli"] = torch.empty_like(out["dx"])
+    out["dLambda"] = torch.empty(wl.W, dtype=torch.float32, device="cuda")
+    out["dh0"] = torch.empty(wl.B, wl.W, dtype=torch.float32, device="cuda")
+    R.rglru_backward(sh, d["dy"], d["dhT"], d["x"], d["lr"], d["li"], d["Lambda"],
+                     d["reset_mask"], d["segment_pos"], d["h0"], saved, out["dx"], out["dlr"],
+                     out["dli"], out["dLambda"], out["dh0"], ws)
+    assert R.rglru_sync_status(saved) == R.OK
+    assert R.rglru_sync_status(ws) == R.OK
+    return {k: host(v) for k, v in out.items()}
+
+
+@pytest.mark.parametrize("wl,seed,grad", SCAN_CASES, ids=[c[0].name + ("-g" + c[2] if c[2] else "") for c in SCAN_CASES])
+def test_scan_forward_backward(wl, seed, grad):
+    inp = generate(wl, seed, want_logits=True)
+    sh = shape_for(wl, grad)
+    got = run_scan_gpu(wl, inp, sh)
+    o = oracle_inputs(inp)
+    mode = mode_id(wl)
+    y, hT = oracle.forward(mode, o["x"], o["lr"], o["li"], o["Lambda"], o["reset_mask"],
+                           o["segment_pos"], o["h0"])
+    g = oracle.backward(mode, o["x"], o["lr"], o["li"], o["Lambda"], o["dy"], o["dhT"],
+                        o["reset_mask"], o["segment_pos"], o["h0"])
+    gst = "f32" if sh.grad == R.F32 else "bf16"
+    assert_close("y", got["y"], y, io=wl.io, kind="out")
+    assert_close("hT", got["hT"], hT, io=wl.io, kind="out")
+    for k in ("dx", "dlr", "dli"):
+        assert_close(k, got[k], g[k], io=wl.io, kind="grad", stored=gst)
+    assert_close("dLambda", got["dLambda"], g["dLambda"], io=wl.io, kind="grad")
+    assert_close("dh0", got["dh0"], g["dh0"], io=wl.io, kind="grad")
+
+
+GEMM_CASES = [
+    (WORKLOADS[1], 21, None),
+    (W_("bf16-k128", 2, 70, 256, 128, "bf16", "restricted"), 22, None),
+    (W_("bf16-k160", 1, 150, 320, 160, "bf16", "restricted"), 23, "f32"),
+    (W_("bf16-k64", 1, 33, 192, 64, "bf16", "restricted"), 24, None),
+    (W_("bf16-k16-T1", 1, 1, 32, 16, "bf16", "restricted"), 25, None),
+]
+
+
+@pytest.mark.parametrize("wl,seed,grad", GEMM_CASES, ids=[c[0].name for c in GEMM_CASES])
+def test_gate_proj_and_backward(wl, seed, grad):
+    inp = generate(wl, seed, want_dlogits=True)
+    sh = shape_for(wl, grad)
+    d = {k: dev(v) for k, v in inp.items()}
+    lr = torch.empty_like(d["x"])
+    li = torch.empty_like(d["x"])
+    ba = torch.randn(wl.W, generator=torch.Generator().manual_seed(seed)).mul_(0.1)
+    bx = torch.randn(wl.W, generator=torch.Generator().manual_seed(seed + 1)).mul_(0.1)
+    R.rglru_gate_proj(sh, d["x"], d["Wa"], dev(ba), d["Wx"], dev(bx), lr, li)
+    o = oracle_inputs(inp)
+    rl, ri = oracle.gate_proj(o["x"], o["Wa"], ba.double().numpy(), o["Wx"], bx.double().numpy())
+    assert_close("lr", host(lr), rl, io=wl.io, kind="out")
+    assert_close("li", host(li), ri, io=wl.io, kind="out")
+
+    gd = _gdt(sh)
+    dlr = inp["dlr"].to(gd)
+    dli = inp["dli"].to(gd)
+    dx0 = torch.randn(inp["x"].shape, generator=torch.Generator().manual_seed(seed + 2)).to(gd)
+    dx = dev(dx0.clone())
+    dWa = torch.empty(wl.nblk, wl.k, wl.k, dtype=torch.float32, device="cuda")
+    dWx = torch.empty_like(dWa)
+    dba = torch.empty(wl.W, dtype=torch.float32, device="cuda")
+    dbx = torch.empty_like(dba)
+    ws = R.alloc_workspace(sh)
+    R.rglru_gate_proj_backward(sh, dev(dlr), dev(dli), d["x"], d["Wa"], d["Wx"], dx, dWa, dba,
+                               dWx, dbx, ws)
+    torch.cuda.synchronize()
+    p = oracle.gate_proj_backward(o["x"], o["Wa"], o["Wx"], dlr.double().numpy(),
+                                  dli.double().numpy(), dx_in=dx0.double().numpy())
+    gst = "f32" if sh.grad == R.F32 else "bf16"
+    assert_close("dx", host(dx), p["dx"], io=wl.io, kind="grad", stored=gst)
+    for k, v in (("dWa", dWa), ("dWx", dWx), ("dba", dba), ("dbx", dbx)):
+        assert_close(k, host(v), p[k], io=wl.io, kind="grad")
+
+
+FUSED_CASES = [
+    (WORKLOADS[1], 31, None),
+    (W_("bf16-res-k128", 2, 100, 256, 128, "bf16", "restricted"), 32, None),
+    (W_("bf16-res-k128-g32", 2, 100, 256, 128, "bf16", "restricted"), 32, "f32"),
+    (W_("bf16-packed-k160", 2, 150, 320, 160, "bf16", "canonical", seg_len=(1, 60),
+        continuation=True, h0_std=1.0), 33, "f32"),
+    (W_("bf16-T1-k128", 2, 1, 128, 128, "bf16", "canonical", h0_std=1.0), 34, None),
+    (W_("bf16-reset-k64", 1, 70, 128, 64, "bf16", "canonical", reset_p=0.05, reset_t0=True,
+        h0_std=1.0), 35, None),
+]
+
+
+def run_fused_gpu(wl, inp, sh, ba=None, bx=None):
+    d = {k: dev(v) for k, v in inp.items()}
+    ba = d["ba"] if ba is None else dev(ba)
+    bx = d["bx"] if bx is None else dev(bx)
+    y = torch.empty_like(d["x"])
+    hT = torch.empty(wl.B, wl.W, dtype=torch.float32, device="cuda")
+    saved = R.alloc_saved(sh)
+    ws = R.alloc_workspace(sh)
+    R.rglru_fused_forward(sh, d["x"], d["Wa"], ba, d["Wx"], bx, d["Lambda"], d["reset_mask"],
+                          d["segment_pos"], d["h0"], y, hT, saved)
+    out = {"y": y, "hT": hT}
+    out["dx"] = torch.empty(d["x"].shape, dtype=_gdt(sh), device="cuda")
+    for k in ("dWa", "dWx"):
+        out[k] = torch.empty(wl.nblk, wl.k, wl.k, dtype=torch.float32, device="cuda")
+    for k in ("dba", "dbx", "dLambda"):
+        out[k] = torch.empty(wl.W, dtype=torch.float32, device="cuda")
+    out["dh0"] = torch.empty(wl.B, wl.W, dtype=torch.float32, device="cuda")
+    R.rglru_fused_backward(sh, d["dy"], d["dhT"], d["x"], d["Wa"], ba, d["Wx"], bx,
+                           d["Lambda"], d["reset_mask"], d["segment_pos"], d["h0"], saved,
+                           out["dx"], out["dWa"], out["dba"], out["dWx"], out["dbx"],
+                           out["dLambda"], out["dh0"], ws)
+    assert R.rglru_sync_status(saved) == R.OK
+    assert R.rglru_sync_status(ws) == R.OK
+    return out
+
+
+def check_fused(wl, inp, got, gst, ba=None, bx=None, sl=slice(None)):
+    o = oracle_inputs(inp)
+    ba = o["ba"] if ba is None else ba
+    bx = o["bx"] if bx is None else bx
+    mode = mode_id(wl)
+    y, hT = oracle.fused_forward(mode, o["x"], o["Wa"], ba, o["Wx"], bx, o["Lambda"],
+                                 o["reset_mask"], o["segment_pos"], o["h0"])
+    g = oracle.fused_backward(mode, o["x"], o["Wa"], ba, o["Wx"], bx, o["Lambda"], o["dy"],
+                              o["dhT"], o["reset_mask"], o["segment_pos"], o["h0"])
+    assert_close("y", got["y"], y, io=wl.io, kind="out")
+    assert_close("hT", got["hT"], hT, io=wl.io, kind="out")
+    assert_close("dx", got["dx"], g["dx"], io=wl.io, kind="grad", stored=gst)
+    for k in ("dWa", "dWx", "dba", "dbx", "dLambda", "dh0"):
+        assert_close(k, got[k], g[k], io=wl.io, kind="grad")
+
+
+@pytest.mark.parametrize("wl,seed,grad", FUSED_CASES,
+                         ids=[c[0].name + ("-g" + c[2] if c[2] else "") for c in FUSED_CASES])
+def test_fused_forward_backward(wl, seed, grad):
+    inp = generate(wl, seed)
+    sh = shape_for(wl, grad)
+    ba = torch.randn(wl.W, generator=torch.Generator().manual_seed(seed)).mul_(0.1)
+    bx = torch.randn(wl.W, generator=torch.Generator().manual_seed(seed + 1)).mul_(0.1)
+    got = {k: host(v) for k, v in run_fused_gpu(wl, inp, sh, ba, bx).items()}
+    check_fused(wl, inp, got, "f32" if sh.grad == R.F32 else "bf16",
+                ba.double().numpy(), bx.double().numpy())
+
+
+def test_fused_deterministic():
+    wl = W_("det", 2, 300, 256, 128, "bf16", "canonical", reset_p=0.01, h0_std=1.0)
+    inp = generate(wl, 41)
+    sh = shape_for(wl)
+    a = run_fused_gpu(wl, inp, sh)
+    b = run_fused_gpu(wl, inp, sh)
+    for k in a:
+        assert torch.equal(a[k], b[k]), k
+
+
+def test_outputs_stay_in_bounds():
+    """Canary: the elements just past every output buffer are never written."""
+    wl = W_("canary", 1, 45, 72, 72, "bf16", "canonical", reset_p=0.1, h0_std=1.0)
+    inp = generate(wl, 42, want_logits=True)
+    sh = shape_for(wl)
+    d = {k: dev(v) for k, v in inp.items()}
+    N = wl.B * wl.T * wl.W
+    pad = 512
+    sentinel = 12345.0
+
+    def buf(n, dt):
+        t = torch.full((n + pad,), sentinel, dtype=dt, device="cuda")
+        return t, t[:n]
+
+    yb, y = buf(N, torch.bfloat16)
+    hb, hT = buf(wl.B * wl.W, torch.float32)
+    saved = R.alloc_saved(sh)
+    ws = R.alloc_workspace(sh)
+    R.rglru_forward(sh, d["x"], d["lr"], d["li"], d["Lambda"], d["reset_mask"], None, d["h0"],
+                    y, hT, saved)
+    bufs = [buf(N, torch.bfloat16) for _ in range(3)] + [buf(wl.W, torch.float32),
+                                                          buf(wl.B * wl.W, torch.float32)]
+    R.rglru_backward(sh, d["dy"], d["dhT"], d["x"], d["lr"], d["li"], d["Lambda"],
+                     d["reset_mask"], None, d["h0"], saved, bufs[0][1], bufs[1][1], bufs[2][1],
+                     bufs[3][1], bufs[4][1], ws)
+    torch.cuda.synchronize()
+    for full, n in [(yb, N), (hb, wl.B * wl.W)] + [(b[0], b[1].numel()) for b in bufs]:
+        assert torch.all(full[n:] == torch.tensor(sentinel, dtype=full.dtype, device="cuda"))
+
+
+def test_lookback_timeout_is_reported():
+    """A tile that never publishes makes its successor's bounded wait run out; the call still
+    finishes and the status word reports the timeout.  Afterwards the defaults are back."""
+    wl = W_("timeout", 1, 128, 64, 64, "bf16", "restricted")
+    inp = generate(wl, 43, want_logits=True)
+    sh = shape_for(wl)
+    d = {k: dev(v) for k, v in inp.items()}
+    y = torch.empty_like(d["x"])
+    saved = R.alloc_saved(sh)
+    R.rglru_debug_lookback(2000, 5)
+    try:
+        R.rglru_forward(sh, d["x"], d["lr"], d["li"], d["Lambda"], None, None, None, y, None, saved)
+        assert R.rglru_sync_status(saved) == R.ERR_TIMEOUT
+    finally:
+        R.rglru_debug_lookback(0, -1)
+    R.rglru_forward(sh, d["x"], d["lr"], d["li"], d["Lambda"], None, None, None, y, None, saved)
+    assert R.rglru_sync_status(saved) == R.OK
+    o = oracle_inputs(inp)
+    yr, _ = oracle.forward(oracle.RESTRICTED, o["x"], o["lr"], o["li"], o["Lambda"])
+    assert_close("y", host(y), yr, io="bf16", kind="out")
+
+
+def test_invalid_arguments_rejected_on_gpu():
+    wl = W_("bad", 1, 8, 64, 64, "bf16", "restricted")
+    sh = shape_for(wl)
+    x = torch.zeros(1, 8, 64, dtype=torch.bfloat16, device="cuda")
+    L = torch.zeros(64, device="cuda")
+    saved = R.alloc_saved(sh)
+    rm = torch.zeros(1, 8, dtype=torch.uint8, device="cuda")
+    with pytest.raises(R.RglruError) as e:   # restricted mode takes no resets
+        R.rglru_forward(sh, x, x, x, L, rm, None, None, x, None, saved)
+    assert e.value.status == R.ERR_INVALID_ARG
+    P = ctypes.c_void_p
+    st = R.lib().rglru_forward(ctypes.byref(sh), P(x.data_ptr() + 2), P(x.data_ptr()),
+                               P(x.data_ptr()), P(L.data_ptr()), None, None, None, P(x.data_ptr()),
+                               None, P(saved.data_ptr()), None)
+    assert st == R.ERR_INVALID_ARG   # misaligned x
