@@ -1,0 +1,362 @@
+#!/usr/bin/env python
+"""RG-LRU layer benchmark: fused forward + backward tokens/s at B4 T2048 W2048, bf16 I/O with
+a float32 carry, restricted protocol (zero initial state, no resets), 16 gate blocks of 128.
+
+One step = rglru_fused_forward + rglru_fused_backward over one batch of seeded synthetic
+input already resident in HBM: the gate projections, gates, decay, multiplier, write and
+scan, then the reverse scan, pointwise gradients, the on-device Lambda reduction and the
+projection gradients (dx, dWa, dWx, dba, dbx).  L2 is flushed (a 256 MiB write) before every
+timed step; CUDA events bracket each step on the launching stream.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun (N > 1) every rank runs its own batch on its own GPU (weak scaling, no
+collective on the data path); rank 0 prints one JSON line with the max-over-ranks time.
+`--impl reference` times the float64 CPU oracle (the reference arm of this build) on the
+host cores instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "RG-LRU fwd+bwd tokens/s (B4 T2048 W2048 bf16); % of HBM roofline"
+UNIT = "tokens/s"
+
+
+# ------------------------------------------------------------------ process group helpers
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", str(rank)))
+    return rank, world, local
+
+
+def dist_init(world, backend):
+    if world > 1:
+        import torch.distributed as dist
+        if not dist.is_initialized():
+            dist.init_process_group(backend=backend)
+
+
+def dist_barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def dist_max(value: float, world: int, device="cpu") -> float:
+    """Max of a float over ranks (measurement only; nothing on the data path)."""
+    if world <= 1:
+        return float(value)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------ clocks during timing
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"], stdout=self.f,
+                stderr=subprocess.DEVNULL)
+            time.sleep(0.25)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        rows = []
+        for line in open(self.path):
+            p = [x.strip() for x in line.split(",")]
+            if len(p) >= 9:
+                rows.append(p)
+        os.unlink(self.path)
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(rows)}
+
+
+# ------------------------------------------------------------------ workload
+def workload():
+    from linear_recurrent_rnn_gb300.inputs import WORKLOADS
+    return WORKLOADS[2]
+
+
+def algorithmic_bytes(wl):
+    """Compulsory HBM bytes per step: every input read once, every output written once.
+    fwd: x (2N) read, y (2N) written, Wa/Wx, biases, Lambda read, hT written.
+    bwd: x, dy (4N) read, dx (2N) written, Wa/Wx, biases, Lambda read, dWa/dWx (f32), dba,
+    dbx, dLambda written.  Saved chunk states and look-back flags are overhead, not counted."""
+    N = wl.B * wl.T * wl.W
+    wbytes = 2 * wl.nblk * wl.k * wl.k * 2
+    vec = wl.W * 4
+    fwd = 4 * N + wbytes + 3 * vec + wl.B * wl.W * 4
+    bwd = 6 * N + wbytes + 3 * vec + 2 * wl.nblk * wl.k * wl.k * 4 + 3 * vec
+    return fwd, bwd
+
+
+def measured_peaks():
+    try:
+        return json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
+    except Exception:
+        return {}
+
+
+# ncu-measured DRAM traffic per launch of the dominant unit (null until captured for the
+# current kernels; see profiles/).
+TRAFFIC_BYTES = None
+
+
+def run_ours(args, rank, world, local):
+    import torch
+    from linear_recurrent_rnn_gb300 import build as B_
+    from linear_recurrent_rnn_gb300 import librglru as R
+    from linear_recurrent_rnn_gb300.inputs import generate
+
+    torch.cuda.set_device(local)
+    dist_init(world, "nccl")
+    B_.build()
+    R.lib()
+    wl = workload()
+    inp = generate(wl, 2 + rank)
+    dev = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+    sh = R.make_shape(wl.B, wl.T, wl.W, wl.nblk, R.BF16, R.BF16, R.RESTRICTED)
+    x, Wa, Wx, ba, bx, L, dy = (dev[k] for k in ("x", "Wa", "Wx", "ba", "bx", "Lambda", "dy"))
+    y = torch.empty_like(x)
+    hT = torch.empty(wl.B, wl.W, device="cuda")
+    saved, ws = R.alloc_saved(sh), R.alloc_workspace(sh)
+    dx = torch.empty_like(x)
+    dWa = torch.empty(wl.nblk, wl.k, wl.k, device="cuda")
+    dWx = torch.empty_like(dWa)
+    dba, dbx, dL = (torch.empty(wl.W, device="cuda") for _ in range(3))
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def fwd():
+        R.rglru_fused_forward(sh, x, Wa, ba, Wx, bx, L, None, None, None, y, hT, saved, stream)
+
+    def bwd():
+        R.rglru_fused_backward(sh, dy, None, x, Wa, ba, Wx, bx, L, None, None, None, saved, dx,
+                               dWa, dba, dWx, dbx, dL, None, ws, stream)
+
+    for _ in range(args.warmup):
+        fwd()
+        bwd()
+    torch.cuda.synchronize()
+    if R.rglru_sync_status(saved) != R.OK or R.rglru_sync_status(ws) != R.OK:
+        raise RuntimeError("look-back timeout during warm-up")
+
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    clocks = ClockSampler(local)
+    dist_barrier(world)
+    torch.cuda.synchronize()
+    clocks.start()
+    n0 = R.rglru_kernel_launches()
+    for k in range(args.steps):
+        flush.zero_()
+        ev[k][0].record(stream)
+        fwd()
+        ev[k][1].record(stream)
+        bwd()
+        ev[k][2].record(stream)
+    torch.cuda.synchronize()
+    launches = R.rglru_kernel_launches() - n0
+    clk = clocks.stop()
+    dist_barrier(world)
+    if R.rglru_sync_status(saved) != R.OK or R.rglru_sync_status(ws) != R.OK:
+        raise RuntimeError("look-back timeout during the timed region")
+    fwd_ms = [e[0].elapsed_time(e[1]) for e in ev]
+    bwd_ms = [e[1].elapsed_time(e[2]) for e in ev]
+    total_ms = sum(fwd_ms) + sum(bwd_ms)
+    total_ms = dist_max(total_ms, world, device="cuda")
+    tokens = wl.B * wl.T
+    value = tokens * world * args.steps / (total_ms / 1e3)
+
+    # end to end through the C ABI with host buffers: H2D of x and dy from pinned memory, the
+    # step, D2H of the parameter gradients, all inside the events
+    hx = inp["x"].pin_memory()
+    hdy = inp["dy"].pin_memory()
+    hout = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in (dWa, dWx, dba, dbx, dL)]
+    e2e_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
+    for k in range(args.warmup + args.steps):
+        if k >= args.warmup:
+            flush.zero_()
+            e2e_ev[k - args.warmup][0].record(stream)
+        x.copy_(hx, non_blocking=True)
+        dy.copy_(hdy, non_blocking=True)
+        fwd()
+        bwd()
+        for h, d in zip(hout, (dWa, dWx, dba, dbx, dL)):
+            h.copy_(d, non_blocking=True)
+        if k >= args.warmup:
+            e2e_ev[k - args.warmup][1].record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = dist_max(sum(e[0].elapsed_time(e[1]) for e in e2e_ev), world, device="cuda")
+    h2d = hx.numel() * hx.element_size() + hdy.numel() * hdy.element_size()
+    d2h = sum(h.numel() * h.element_size() for h in hout)
+
+    fwd_b, bwd_b = algorithmic_bytes(wl)
+    peaks = measured_peaks()
+    peak = peaks.get("hbm_gbs")
+    bwd_med = statistics.median(bwd_ms)
+    achieved = bwd_b / (bwd_med / 1e3) / 1e9
+    step_ms = total_ms / args.steps
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": wl.name + " fused fwd+bwd", "B": wl.B, "T": wl.T, "W": wl.W,
+                   "k": wl.k, "nblk": wl.nblk, "mode": wl.mode, "grad": "bf16",
+                   "carry": "f32", "seed": "2 + rank",
+                   "l2": "flushed by a 256 MiB write before every timed step",
+                   "parallelism": f"dp{world} (independent batches, no collective)"},
+        "fwd_ms": {"median": statistics.median(fwd_ms), "min": min(fwd_ms), "max": max(fwd_ms),
+                   "mean": statistics.fmean(fwd_ms)},
+        "fwd_bwd_ms": {"median": statistics.median([a + b for a, b in zip(fwd_ms, bwd_ms)]),
+                       "min": min(a + b for a, b in zip(fwd_ms, bwd_ms)),
+                       "max": max(a + b for a, b in zip(fwd_ms, bwd_ms))},
+        "hbm_fraction_of_8TBps": (fwd_b + bwd_b) / (step_ms / 1e3) / 8e12,
+        "roofline": {"bound": "hbm", "unit": "GB/s", "kernel": "rglru_fused_backward",
+                     "achieved": achieved, "peak": peak,
+                     "frac": (achieved / peak) if peak else None, "peak_source": "measured",
+                     "algorithmic_bytes": bwd_b, "traffic": TRAFFIC_BYTES},
+        "e2e": {"value": tokens * world * args.steps / (e2e_ms / 1e3), "unit": UNIT,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches,
+        "clocks": clk,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(wl, T=args.cpu_sample_T)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def oracle_step(wl_sample, inp):
+    import oracle
+    from linear_recurrent_rnn_gb300.inputs import as_f64
+    o = {k: as_f64(v) if v is not None and not isinstance(v, str) else v for k, v in inp.items()}
+    mode = oracle.RESTRICTED if wl_sample.mode == "restricted" else oracle.CANONICAL
+    oracle.fused_forward(mode, o["x"], o["Wa"], o["ba"], o["Wx"], o["bx"], o["Lambda"])
+    oracle.fused_backward(mode, o["x"], o["Wa"], o["ba"], o["Wx"], o["bx"], o["Lambda"], o["dy"])
+
+
+def cpu_cores():
+    n = os.environ.get("OMP_NUM_THREADS")
+    return int(n) if n and n.isdigit() else (os.cpu_count() or 1)
+
+
+def cpu_baseline(wl, T=2048, min_seconds=10.0):
+    """The float64 oracle as it stands, on the host cores, on a bounded sample of the
+    workload: batch row 0, the first T tokens, all W channels (every gate block), repeated
+    until at least `min_seconds` of CPU work have been timed."""
+    from linear_recurrent_rnn_gb300.inputs import generate
+    ws = wl.scaled(B=1, T=T)
+    inp = generate(ws, 2)
+    reps = 0
+    t0 = time.perf_counter()
+    while True:
+        oracle_step(ws, inp)
+        reps += 1
+        dt = time.perf_counter() - t0
+        if dt >= min_seconds:
+            break
+    return {"value": reps * ws.B * ws.T / dt, "unit": UNIT, "cores": cpu_cores(),
+            "kind": "oracle",
+            "sample": f"B1 T{T} W{wl.W} (all {wl.nblk} blocks) fused fwd+bwd, float64, "
+                      f"{reps} repetitions in {dt:.1f} s"}
+
+
+def run_reference(args, rank, world):
+    """Reference arm: the oracle on the host cores, each step a bounded sample."""
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    from linear_recurrent_rnn_gb300.inputs import generate
+    wl = workload()
+    T = args.ref_sample_T
+    ws = wl.scaled(B=1, T=T)
+    inp = generate(ws, 2)
+    for _ in range(args.warmup):
+        oracle_step(ws, inp)
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        oracle_step(ws, inp)
+        times.append(time.perf_counter() - t0)
+    total = sum(times)
+    value = ws.B * ws.T * args.steps / total
+    sample = f"B1 T{T} W{wl.W} (all {wl.nblk} blocks) fused fwd+bwd per step, float64"
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * total / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": wl.name + " fused fwd+bwd", "B": wl.B, "T": wl.T,
+                       "W": wl.W, "k": wl.k, "mode": wl.mode},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cpu_cores(),
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    p = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=20)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--cpu-sample-T", type=int, default=2048)
+    p.add_argument("--ref-sample-T", type=int, default=256)
+    args = p.parse_args(argv)
+    if args.warmup < 3:
+        p.error("--warmup must be >= 3")
+    rank, world, local = dist_env()
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+    else:
+        run_ours(args, rank, world, local)
+
+
+if __name__ == "__main__":
+    main()

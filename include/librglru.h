@@ -156,6 +156,11 @@ rglru_status rglru_sync_status(const void *saved_or_workspace, rglru_stream stre
  * waits run out.  (0, -1) restores the defaults.  Process-wide; not thread-safe. */
 void rglru_debug_lookback(int32_t spin_limit, int32_t drop_tile);
 
+/* Launch accounting (no counterpart on the pages): the number of CUDA kernels this library
+ * has enqueued since the process started (memsets excluded).  Lets a caller count the
+ * kernels behind a timed region.  Process-wide, atomic. */
+uint64_t rglru_kernel_launches(void);
+
 #ifdef __cplusplus
 }
 #endif

@@ -4,12 +4,15 @@
 #include <stdio.h>
 #include <string.h>
 
+#include <atomic>
+
 #include "internal.h"
 
 using namespace rglru;
 
 namespace {
 
+std::atomic<uint64_t> g_launches{0};
 int g_spin_limit = 1 << 22;
 int g_drop_tile = -1;
 
@@ -146,6 +149,10 @@ ScanBwdArgs bwd_args(const Dims& d, const void* dy, const float* dhT, const void
 }
 
 }  // namespace
+
+namespace rglru {
+void note_launches(unsigned n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
+}  // namespace rglru
 
 extern "C" {
 
@@ -310,6 +317,8 @@ rglru_status rglru_sync_status(const void* buf, rglru_stream stream) {
   if (e != cudaSuccess) return cuda_status(e);
   return (word & 1u) ? RGLRU_ERR_TIMEOUT : RGLRU_OK;
 }
+
+uint64_t rglru_kernel_launches(void) { return g_launches.load(std::memory_order_relaxed); }
 
 void rglru_debug_lookback(int32_t spin_limit, int32_t drop_tile) {
   g_spin_limit = spin_limit > 0 ? spin_limit : (1 << 22);

@@ -225,6 +225,7 @@ cudaError_t proj(const Dims& d, const void* x, const void* Wa, const float* ba, 
   dim3 grid((BT + TM - 1) / TM, d.nblk * ((d.k + TN - 1) / TN), 2);
   k_proj<XT, OT><<<grid, 256, 0, s>>>(BT, d.W, d.k, (const XT*)x, (const XT*)Wa, ba,
                                       (const XT*)Wx, bx, (OT*)lr, (OT*)li);
+  note_launches(1);
   return cudaGetLastError();
 }
 
@@ -235,6 +236,7 @@ cudaError_t dxk(const Dims& d, const void* gr, const void* gi, const void* Wa, c
   dim3 grid((BT + TM - 1) / TM, d.nblk * ((d.k + TN - 1) / TN));
   k_dx<WT, GT, DXT><<<grid, 256, 0, s>>>(BT, d.W, d.k, (const GT*)gr, (const GT*)gi,
                                          (const WT*)Wa, (const WT*)Wx, dx_in, (DXT*)dx);
+  note_launches(1);
   return cudaGetLastError();
 }
 
@@ -249,21 +251,29 @@ cudaError_t dwk(const Dims& d, const void* x, const void* gr, const void* gi, fl
   const int nt = (d.k + 63) / 64;
   k_dw_part<XT, GT><<<dim3(nt * nt, d.nblk * 2, S), 256, 0, s>>>(
       BT, d.W, d.k, d.nblk, S, (const XT*)x, (const GT*)gr, (const GT*)gi, part);
+  note_launches(1);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const size_t per_gate = (size_t)d.nblk * d.k * d.k;
   k_sum_splits<<<(unsigned)((per_gate + 255) / 256), 256, 0, s>>>(part, S, per_gate,
                                                                    2 * per_gate, dWa);
+  note_launches(1);
   k_sum_splits<<<(unsigned)((per_gate + 255) / 256), 256, 0, s>>>(part + per_gate, S, per_gate,
                                                                    2 * per_gate, dWx);
+  note_launches(1);
   if (dba || dbx) {
     k_db_part<GT><<<dim3((d.W + 255) / 256, 2, S), 256, 0, s>>>(BT, d.W, S, (const GT*)gr,
                                                                 (const GT*)gi, dbp);
-    if (dba)
+    note_launches(1);
+    if (dba) {
       k_sum_splits<<<(d.W + 255) / 256, 256, 0, s>>>(dbp, S, (size_t)d.W, 2 * (size_t)d.W, dba);
-    if (dbx)
+      note_launches(1);
+    }
+    if (dbx) {
       k_sum_splits<<<(d.W + 255) / 256, 256, 0, s>>>(dbp + d.W, S, (size_t)d.W, 2 * (size_t)d.W,
                                                      dbx);
+      note_launches(1);
+    }
   }
   return cudaGetLastError();
 }

@@ -118,6 +118,9 @@ struct ScanBwdArgs {
   int spin_limit, drop_tile;
 };
 
+// Adds n to the process-wide count of kernels enqueued (rglru_kernel_launches).
+void note_launches(unsigned n);
+
 // dtype codes used by the launchers (io of x/y/dy, of the logits, of dx, of dlr/dli)
 enum { DT_F32 = RGLRU_F32, DT_BF16 = RGLRU_BF16 };
 

@@ -455,6 +455,7 @@ cudaError_t fwd_dispatch_mode(const ScanFwdArgs& a, bool canonical, cudaStream_t
     k_scan_fwd<XT, LT, true><<<grid, 128, 0, s>>>(a);
   else
     k_scan_fwd<XT, LT, false><<<grid, 128, 0, s>>>(a);
+  note_launches(1);
   return cudaGetLastError();
 }
 
@@ -466,10 +467,12 @@ cudaError_t bwd_dispatch_mode(const ScanBwdArgs& a, bool canonical, cudaStream_t
     k_scan_bwd<XT, LT, DXT, DLT, true><<<grid, 128, 0, s>>>(a);
   else
     k_scan_bwd<XT, LT, DXT, DLT, false><<<grid, 128, 0, s>>>(a);
+  note_launches(1);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const float* part = reinterpret_cast<const float*>(a.scratch + a.L.part);
   k_reduce_dlambda<<<(a.W + 31) / 32, 512, 0, s>>>(part, a.B * a.nC, a.W, a.Lambda, a.dLambda);
+  note_launches(1);
   return cudaGetLastError();
 }
 

@@ -46,7 +46,7 @@ _lib = None
 EXPORTS = ("rglru_status_string", "rglru_saved_bytes", "rglru_workspace_bytes",
            "rglru_gate_proj", "rglru_forward", "rglru_backward", "rglru_gate_proj_backward",
            "rglru_fused_forward", "rglru_fused_backward", "rglru_sync_status",
-           "rglru_debug_lookback")
+           "rglru_debug_lookback", "rglru_kernel_launches")
 
 
 def library_path() -> str:
@@ -79,6 +79,8 @@ def lib():
             L.rglru_sync_status.argtypes = [P, P]
             L.rglru_debug_lookback.argtypes = [ctypes.c_int32, ctypes.c_int32]
             L.rglru_debug_lookback.restype = None
+            L.rglru_kernel_launches.argtypes = []
+            L.rglru_kernel_launches.restype = ctypes.c_uint64
             for n in ("rglru_gate_proj", "rglru_forward", "rglru_backward",
                       "rglru_gate_proj_backward", "rglru_fused_forward", "rglru_fused_backward",
                       "rglru_sync_status"):
@@ -188,3 +190,7 @@ def rglru_sync_status(buf: torch.Tensor, stream=None) -> int:
 
 def rglru_debug_lookback(spin_limit: int, drop_tile: int) -> None:
     lib().rglru_debug_lookback(int(spin_limit), int(drop_tile))
+
+
+def rglru_kernel_launches() -> int:
+    return int(lib().rglru_kernel_launches())
