@@ -125,6 +125,23 @@ rglru_status rglru_gate_proj_backward(const rglru_shape *shape, const void *dlr,
                                       float *dWx, float *dbx, void *workspace,
                                       rglru_stream stream);
 
+/* Recurrence forward that allocates nothing and takes no `saved` buffer.  The pages have no
+ * counterpart; it exists for callers that may not allocate device memory at all (code
+ * running inside someone else's stream capture, under a fixed memory pool, in a real-time
+ * loop that must not touch the allocator, or in a plugin handed only its inputs and
+ * outputs).  Same arguments and outputs as rglru_forward minus `saved` (nothing is kept for
+ * a backward).  The look-back scratch is a static device array of
+ * RGLRU_NOALLOC_SCRATCH_BYTES per GPU, held from library load until process exit; a shape
+ * needing more (about 0.75 * B*T*W bytes, e.g. B4 T2048 W2048 fits) returns
+ * RGLRU_ERR_UNSUPPORTED.  The first call on each device finds the array's device address
+ * (cudaGetSymbolAddress) and should come before any stream capture.  All calls share the
+ * array; calls whose work overlaps on the GPU race on it. */
+#define RGLRU_NOALLOC_SCRATCH_BYTES ((size_t)16 << 20)
+rglru_status rglru_forward_noalloc(const rglru_shape *shape, const void *x, const void *lr,
+                                   const void *li, const float *Lambda,
+                                   const uint8_t *reset_mask, const int32_t *segment_pos,
+                                   const float *h0, void *y, float *hT, rglru_stream stream);
+
 /* Fused forward: the projections folded into the recurrence [P1 closing paragraph credits
  * the fusion strategy; the logits are never rounded to the I/O dtype].  Same outputs as
  * rglru_gate_proj followed by rglru_forward, without writing the logits. */

@@ -20,6 +20,10 @@ size_t dsize(int dt) { return dt == RGLRU_BF16 ? 2 : 4; }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+}  // namespace
+
+namespace rglru {
+
 // Validates the shape and fills `d`.
 rglru_status make_dims(const rglru_shape* s, Dims* d) {
   if (!s) return RGLRU_ERR_INVALID_ARG;
@@ -148,7 +152,7 @@ ScanBwdArgs bwd_args(const Dims& d, const void* dy, const float* dhT, const void
   return a;
 }
 
-}  // namespace
+}  // namespace rglru
 
 namespace rglru {
 void note_launches(unsigned n) { g_launches.fetch_add(n, std::memory_order_relaxed); }

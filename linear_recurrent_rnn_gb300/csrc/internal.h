@@ -121,6 +121,16 @@ struct ScanBwdArgs {
 // Adds n to the process-wide count of kernels enqueued (rglru_kernel_launches).
 void note_launches(unsigned n);
 
+// Host-side validation shared by the entry points (defined in api.cu).
+rglru_status make_dims(const rglru_shape* s, Dims* d);
+bool req(const void* p);  // non-null and 16-byte aligned
+bool opt(const void* p);  // null or 16-byte aligned
+rglru_status check_resets(const Dims& d, const uint8_t* rm, const int32_t* sp, const float* h0);
+rglru_status cuda_status(cudaError_t e);
+ScanFwdArgs fwd_args(const Dims& d, const void* x, const void* lr, const void* li,
+                     const float* Lambda, const uint8_t* rm, const int32_t* sp, const float* h0,
+                     void* y, float* hT, void* saved);
+
 // dtype codes used by the launchers (io of x/y/dy, of the logits, of dx, of dlr/dli)
 enum { DT_F32 = RGLRU_F32, DT_BF16 = RGLRU_BF16 };
 

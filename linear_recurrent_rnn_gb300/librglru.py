@@ -46,7 +46,10 @@ _lib = None
 EXPORTS = ("rglru_status_string", "rglru_saved_bytes", "rglru_workspace_bytes",
            "rglru_gate_proj", "rglru_forward", "rglru_backward", "rglru_gate_proj_backward",
            "rglru_fused_forward", "rglru_fused_backward", "rglru_sync_status",
-           "rglru_debug_lookback", "rglru_kernel_launches")
+           "rglru_debug_lookback", "rglru_kernel_launches", "rglru_forward_noalloc")
+
+# Static look-back scratch of rglru_forward_noalloc, per GPU (RGLRU_NOALLOC_SCRATCH_BYTES).
+NOALLOC_SCRATCH_BYTES = 16 << 20
 
 
 def library_path() -> str:
@@ -79,6 +82,8 @@ def lib():
             L.rglru_sync_status.argtypes = [P, P]
             L.rglru_debug_lookback.argtypes = [ctypes.c_int32, ctypes.c_int32]
             L.rglru_debug_lookback.restype = None
+            L.rglru_forward_noalloc.argtypes = [S] + [P] * 10
+            L.rglru_forward_noalloc.restype = ctypes.c_int
             L.rglru_kernel_launches.argtypes = []
             L.rglru_kernel_launches.restype = ctypes.c_uint64
             for n in ("rglru_gate_proj", "rglru_forward", "rglru_backward",
@@ -159,6 +164,15 @@ def rglru_backward(shape, dy, dhT, x, lr, li, Lambda, reset_mask, segment_pos, h
         ctypes.byref(shape), _p(dy), _p(dhT), _p(x), _p(lr), _p(li), _p(Lambda),
         _p(reset_mask), _p(segment_pos), _p(h0), _p(saved), _p(dx), _p(dlr), _p(dli),
         _p(dLambda), _p(dh0), _p(workspace), _stream(stream)))
+
+
+def rglru_forward_noalloc(shape, x, lr, li, Lambda, reset_mask, segment_pos, h0, y, hT,
+                          stream=None):
+    """rglru_forward for callers that may not allocate: no `saved` buffer, the look-back
+    scratch is the library's static per-GPU array (first call per device outside capture)."""
+    _check("rglru_forward_noalloc", lib().rglru_forward_noalloc(
+        ctypes.byref(shape), _p(x), _p(lr), _p(li), _p(Lambda), _p(reset_mask), _p(segment_pos),
+        _p(h0), _p(y), _p(hT), _stream(stream)))
 
 
 def rglru_gate_proj_backward(shape, dlr, dli, x, Wa, Wx, dx, dWa, dba, dWx, dbx, workspace,
