@@ -81,7 +81,10 @@ ComposedLayout composed_saved(const Dims& d) {
   return C;
 }
 struct ComposedWs {
-  size_t dxd, dlr, dli, gate, total;  // within `workspace`, after the backward scan layout
+  // within `workspace`, after the backward scan layout; the bridge regions (a CUDA-core
+  // forward recomputed for the backward) are used only while the tensor-core forward has no
+  // tensor-core backward partner
+  size_t dxd, dlr, dli, gate, bsaved, blr, bli, total;
 };
 ComposedWs composed_ws(const Dims& d) {
   ComposedWs C;
@@ -90,7 +93,10 @@ ComposedWs composed_ws(const Dims& d) {
   C.dlr = align_up(C.dxd + d.N * 4, 256);
   C.dli = align_up(C.dlr + d.N * 4, 256);
   C.gate = align_up(C.dli + d.N * 4, 256);
-  C.total = align_up(C.gate + gate_bwd_layout(d).total, 256);
+  C.bsaved = align_up(C.gate + gate_bwd_layout(d).total, 256);
+  C.blr = align_up(C.bsaved + scan_layout(d, false).total, 256);
+  C.bli = align_up(C.blr + d.N * 4, 256);
+  C.total = align_up(C.bli + d.N * 4, 256);
   return C;
 }
 
@@ -176,7 +182,9 @@ size_t rglru_saved_bytes(const rglru_shape* shape) {
   if (make_dims(shape, &d) != RGLRU_OK) return 0;
   const size_t a = scan_layout(d, false).total;
   const size_t b = composed_saved(d).total;
-  return a > b ? a : b;
+  const size_t f = fused_layout(d, false).total;
+  size_t m = a > b ? a : b;
+  return m > f ? m : f;
 }
 
 size_t rglru_workspace_bytes(const rglru_shape* shape) {
@@ -267,6 +275,9 @@ rglru_status rglru_fused_forward(const rglru_shape* shape, const void* x, const 
       !opt(hT) || !req(saved))
     return RGLRU_ERR_INVALID_ARG;
   if ((st = check_resets(d, reset_mask, segment_pos, h0)) != RGLRU_OK) return st;
+  if (fused_supported(d))
+    return cuda_status(launch_fused_fwd(d, x, Wa, ba, Wx, bx, Lambda, reset_mask, segment_pos,
+                                        h0, y, hT, saved, g_spin_limit, g_drop_tile, stream));
   uint8_t* sv = static_cast<uint8_t*>(saved);
   const ComposedLayout C = composed_saved(d);
   cudaError_t e = launch_gate_proj_simt(d, d.io, DT_F32, x, Wa, ba, Wx, bx, sv + C.lr, sv + C.li,
@@ -297,11 +308,28 @@ rglru_status rglru_fused_backward(const rglru_shape* shape, const void* dy, cons
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   const ComposedLayout C = composed_saved(d);
   const ComposedWs CW = composed_ws(d);
-  const ScanBwdArgs a = bwd_args(d, dy, dhT, x, sv + C.lr, sv + C.li, Lambda, reset_mask,
-                                 segment_pos, h0, saved, ws + CW.dxd, ws + CW.dlr, ws + CW.dli,
-                                 dLambda, dh0, workspace);
+  const void* lr = sv + C.lr;
+  const void* li = sv + C.li;
+  const void* fsaved = saved;
+  cudaError_t e = cudaSuccess;
+  if (fused_supported(d)) {
+    // Bridge: the forward ran on tensor cores and kept no logits; recompute them and the
+    // CUDA-core forward's chunk states in the workspace.
+    lr = ws + CW.blr;
+    li = ws + CW.bli;
+    fsaved = ws + CW.bsaved;
+    e = launch_gate_proj_simt(d, d.io, DT_F32, x, Wa, ba, Wx, bx, ws + CW.blr, ws + CW.bli,
+                              stream);
+    const ScanFwdArgs f = fwd_args(d, x, lr, li, Lambda, reset_mask, segment_pos, h0,
+                                   ws + CW.dxd, nullptr, ws + CW.bsaved);
+    if (e == cudaSuccess) e = cudaMemsetAsync(ws + CW.bsaved, 0, f.L.zero_bytes, stream);
+    if (e == cudaSuccess) e = launch_scan_fwd(f, d.io, DT_F32, d.mode == RGLRU_CANONICAL, stream);
+  }
+  const ScanBwdArgs a = bwd_args(d, dy, dhT, x, lr, li, Lambda, reset_mask, segment_pos, h0,
+                                 fsaved, ws + CW.dxd, ws + CW.dlr, ws + CW.dli, dLambda, dh0,
+                                 workspace);
   // The direct term of dx stays float32 until the projections are added: one rounding.
-  cudaError_t e = cudaMemsetAsync(workspace, 0, a.L.zero_bytes, stream);
+  if (e == cudaSuccess) e = cudaMemsetAsync(workspace, 0, a.L.zero_bytes, stream);
   if (e == cudaSuccess)
     e = launch_scan_bwd(a, d.io, DT_F32, DT_F32, DT_F32, d.mode == RGLRU_CANONICAL, stream);
   if (e == cudaSuccess)
@@ -319,7 +347,7 @@ rglru_status rglru_sync_status(const void* buf, rglru_stream stream) {
   cudaError_t e = cudaStreamSynchronize(stream);
   if (e == cudaSuccess) e = cudaMemcpy(&word, buf, sizeof(word), cudaMemcpyDeviceToHost);
   if (e != cudaSuccess) return cuda_status(e);
-  return (word & 1u) ? RGLRU_ERR_TIMEOUT : RGLRU_OK;
+  return word ? RGLRU_ERR_TIMEOUT : RGLRU_OK;
 }
 
 uint64_t rglru_kernel_launches(void) { return g_launches.load(std::memory_order_relaxed); }

@@ -1,0 +1,412 @@
+// Fused RG-LRU forward on one GB300: block-diagonal gate projections on the tcgen05 tensor
+// cores, gates / decay / multiplier / write and the exact chunked scan on the CUDA cores, in
+// one persistent kernel.  The gate logits live only in tensor memory (float32), never in HBM.
+//
+// Sources ("Fattori comparison" page): the operator takes the recurrent input and both raw
+// gate logits produced by two block-diagonal projections (first paragraph), fuses the sigmoid
+// gates, softplus(a_param) with the dynamic decay, the square-root multiplier, the input-gated
+// write and the recurrence (the fused-steps list), and the page closes by adopting that fusion
+// and adding an exact parallel chunked scan with partial chunks.  Math: r = sigmoid(lr),
+// i = sigmoid(li), log a = -8 r softplus(Lambda), m = sqrt(1 - a^2) (m = 1 and no carry at a
+// reset token), h_t = a h_{t-1} + m i x.
+//
+// Tile = (batch row b, gate block blk, 64 tokens).  For the tile the MMA computes the
+// transposed logits  lr^T[128 ch x 64 tok] = Wa[blk]^T (MN-major A, from W stored (in, out))
+// x x_tile^T (K-major B, the x tile as TMA lands it), and li^T likewise, so TMEM lane =
+// channel and column = token: each scan thread owns one channel and runs the recurrence over
+// its 64 tokens serially in registers.  Chunks are joined by the anchored decoupled look-back
+// of the scan kernels (flags and aggregates in `saved`), which makes the result bitwise
+// deterministic.
+//
+// Roles (192 threads, one CTA per SM, launched cooperatively so that all CTAs are resident):
+//   warp 0      TMA producer: Wa[blk], Wx[blk] once, then the x tile ring (3 stages)
+//   warp 1      MMA issuer: 2 x 8 tcgen05.mma (K = 16 each) per tile into a 2-deep TMEM ring
+//   warps 2..5  scan: TMEM -> registers, gate math, local scan, look-back, y -> smem -> TMA
+// CTA (blk, r) of the P CTAs serving gate block blk takes the block's tiles n = r, r + P, ...
+// in chunk-major order, so every tile it waits on is earlier in the same order.
+#include <cudaTypedefs.h>
+
+#include "host_util.h"
+#include "internal.h"
+#include "tc.cuh"
+
+namespace rglru {
+
+namespace {
+
+constexpr int NTHREADS = 192;
+constexpr int XSTAGES = 3;
+constexpr uint32_t W_BYTES = FUSED_K * FUSED_K * 2;  // one weight block, bf16
+constexpr uint32_t X_BYTES = FUSED_C * FUSED_K * 2;  // one x tile, bf16
+constexpr uint32_t Y_BYTES = FUSED_C * FUSED_K * 2;  // one y tile, bf16
+constexpr uint32_t SLAB_X = FUSED_C * 32;            // 16 channels x 64 tokens
+constexpr uint32_t SLAB_W = FUSED_K * 32;            // 16 out-channels x 128 in-rows
+constexpr uint32_t TMEM_COLS = 256;                  // 2 buffers x (lr 64 + li 64) columns
+constexpr int WAIT_LIMIT = 1 << 22;
+constexpr size_t SMEM_BYTES = 2 * W_BYTES + XSTAGES * X_BYTES + Y_BYTES + 256 + 1024;
+constexpr uint32_t STATUS_PIPE = 2u;
+
+struct FwdParams {
+  int B, T, W, nblk, nC, ng, P, canonical;
+  const float* Lambda;
+  const float* ba;
+  const float* bx;
+  const uint8_t* reset_mask;
+  const int32_t* segment_pos;
+  const float* h0;
+  float* hT;
+  uint8_t* scratch;
+  ScanLayout L;
+  int spin_limit, drop_tile;
+};
+
+struct Ctl {
+  volatile uint32_t* abort;
+  uint32_t* status;
+  // Bounded wait; after any failure in the CTA every later wait returns at once, so the
+  // kernel winds down in bounded time (with the failure recorded in the status word).
+  __device__ bool wait(uint64_t* bar, uint32_t parity) const {
+    if (*abort) return false;
+    if (tc::mbar_wait(bar, parity, WAIT_LIMIT)) return true;
+    *abort = 1u;
+    atomicOr(status, STATUS_PIPE);
+    return false;
+  }
+};
+
+__global__ void __launch_bounds__(NTHREADS, 1)
+    k_fused_fwd(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_wa,
+                const __grid_constant__ CUtensorMap tm_wx, const __grid_constant__ CUtensorMap tm_y,
+                FwdParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  uint8_t* s_wa = smem;
+  uint8_t* s_wx = smem + W_BYTES;
+  uint8_t* s_x = smem + 2 * W_BYTES;
+  uint8_t* s_y = s_x + XSTAGES * X_BYTES;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(s_y + Y_BYTES);
+  uint64_t* w_full = bars;
+  uint64_t* x_full = bars + 1;
+  uint64_t* x_empty = bars + 1 + XSTAGES;
+  uint64_t* acc_full = bars + 1 + 2 * XSTAGES;
+  uint64_t* acc_empty = acc_full + 2;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(acc_empty + 2);
+  volatile uint32_t* abort_flag = tmem_holder + 1;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int blk = blockIdx.x / p.P, rr = blockIdx.x % p.P;
+  const int ntiles = p.B * p.nC;
+  uint32_t* status = reinterpret_cast<uint32_t*>(p.scratch);
+  const Ctl ctl{abort_flag, status};
+
+  if (threadIdx.x == 0) {
+    tc::mbar_init(w_full, 1);
+    for (int s = 0; s < XSTAGES; ++s) {
+      tc::mbar_init(&x_full[s], 1);
+      tc::mbar_init(&x_empty[s], 4);
+    }
+    for (int a = 0; a < 2; ++a) {
+      tc::mbar_init(&acc_full[a], 1);
+      tc::mbar_init(&acc_empty[a], 4);
+    }
+    *abort_flag = 0u;
+    tc::fence_barrier_init();
+  }
+  if (warp == 0) {
+    tc::tmem_alloc(tmem_holder, TMEM_COLS);
+    tc::tmem_relinquish();
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      tc::prefetch_tmap(&tm_x);
+      tc::prefetch_tmap(&tm_wa);
+      tc::prefetch_tmap(&tm_wx);
+      tc::mbar_expect_tx(w_full, 2 * W_BYTES);
+      for (int g = 0; g < FUSED_K / 16; ++g) {
+        tc::tma_load_2d(s_wa + g * SLAB_W, &tm_wa, w_full, 16 * g, blk * FUSED_K);
+        tc::tma_load_2d(s_wx + g * SLAB_W, &tm_wx, w_full, 16 * g, blk * FUSED_K);
+      }
+      int it = 0;
+      for (int n = rr; n < ntiles; n += p.P, ++it) {
+        const int st = it % XSTAGES;
+        const uint32_t ph = (it / XSTAGES) & 1;
+        if (!ctl.wait(&x_empty[st], ph ^ 1u)) continue;
+        const int c = n / p.B, b = n % p.B;
+        tc::mbar_expect_tx(&x_full[st], X_BYTES);
+        for (int s = 0; s < FUSED_K / 16; ++s)
+          tc::tma_load_3d(s_x + st * X_BYTES + s * SLAB_X, &tm_x, &x_full[st],
+                          blk * FUSED_K + 16 * s, c * FUSED_C, b);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc = tc::idesc_bf16(128, FUSED_C, /*A MN-major*/ 1, /*B K-major*/ 0);
+      ctl.wait(w_full, 0);
+      const uint32_t wa = tc::smem_u32(s_wa), wx = tc::smem_u32(s_wx);
+      int it = 0;
+      for (int n = rr; n < ntiles; n += p.P, ++it) {
+        const int st = it % XSTAGES;
+        const uint32_t ph = (it / XSTAGES) & 1;
+        const int a = it & 1;
+        const uint32_t aph = (it >> 1) & 1;
+        if (!ctl.wait(&acc_empty[a], aph ^ 1u)) continue;
+        if (!ctl.wait(&x_full[st], ph)) continue;
+        tc::tc_fence_after();
+        const uint32_t xs = tc::smem_u32(s_x + st * X_BYTES);
+        const uint32_t d_r = tmem + a * 128, d_i = d_r + 64;
+#pragma unroll
+        for (int kk = 0; kk < FUSED_K / 16; ++kk) {
+          // A: W^T, MN-major, 16-channel groups 4 KB apart (LBO), 8-row K groups 256 B (SBO);
+          // B: x tile, K-major, one 16-channel slab per K step, 8-row groups 256 B apart.
+          const uint64_t bdesc = tc::smem_desc_sw32(xs + kk * SLAB_X, 16, 256);
+          tc::mma_bf16(d_r, tc::smem_desc_sw32(wa + kk * 512, SLAB_W, 256), bdesc, idesc, kk > 0);
+          tc::mma_bf16(d_i, tc::smem_desc_sw32(wx + kk * 512, SLAB_W, 256), bdesc, idesc, kk > 0);
+        }
+        tc::mma_commit(&acc_full[a]);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ scan warps
+    const int q = warp & 3;  // TMEM lane quadrant this warp may access
+    const int j = q * 32 + lane;
+    const int w = blk * FUSED_K + j;
+    const uint32_t lane_base = (uint32_t)(q * 32) << 16;
+    const float nk = -8.0f * softplus_f(p.Lambda[w]);
+    const float bra = p.ba ? p.ba[w] : 0.0f;
+    const float bri = p.bx ? p.bx[w] : 0.0f;
+    const int g = blk * (FUSED_K / 32) + q;
+    uint32_t* flags = reinterpret_cast<uint32_t*>(p.scratch + p.L.flags);
+    float* carry = reinterpret_cast<float*>(p.scratch + p.L.carry);
+    float2* agg = reinterpret_cast<float2*>(p.scratch + p.L.agg);
+    const bool store_thread = (warp == 2 && lane == 0);
+    if (store_thread) tc::prefetch_tmap(&tm_y);
+
+    int it = 0;
+    for (int n = rr; n < ntiles; n += p.P, ++it) {
+      const int c = n / p.B, b = n % p.B;
+      const int st = it % XSTAGES;
+      const uint32_t ph = (it / XSTAGES) & 1;
+      const int a = it & 1;
+      const uint32_t aph = (it >> 1) & 1;
+      ctl.wait(&acc_full[a], aph);
+      ctl.wait(&x_full[st], ph);
+      tc::tc_fence_after();
+
+      // Reset tokens of this tile as two 32-bit masks.
+      uint32_t rlo = 0, rhi = 0;
+      if (p.canonical) {
+        const int t_a = c * FUSED_C + lane, t_b = t_a + 32;
+        const size_t row = (size_t)b * p.T;
+        const bool fa = t_a < p.T && is_reset(p.reset_mask, p.segment_pos, row + t_a);
+        const bool fb = t_b < p.T && is_reset(p.reset_mask, p.segment_pos, row + t_b);
+        rlo = __ballot_sync(0xffffffffu, fa);
+        rhi = __ballot_sync(0xffffffffu, fb);
+      }
+      const int valid = min(FUSED_C, p.T - c * FUSED_C);
+      const uint8_t* xs = s_x + st * X_BYTES + (j >> 4) * SLAB_X + (j & 7) * 2;
+      const int xhalf = (j & 15) >> 3;
+
+      float hl[FUSED_C], Ac[FUSED_C];
+      float rh = 0.0f, rA = 1.0f;
+#pragma unroll
+      for (int sub = 0; sub < FUSED_C / 16; ++sub) {
+        float vr[16], vi[16];
+        tc::tmem_ld16(tmem + lane_base + a * 128 + sub * 16, vr);
+        tc::tmem_ld16(tmem + lane_base + a * 128 + 64 + sub * 16, vi);
+        tc::tmem_ld_wait();
+#pragma unroll
+        for (int u = 0; u < 16; ++u) {
+          const int tl = sub * 16 + u;
+          // x[tile token tl, channel j] in the 32-byte-swizzled slab (16-byte halves swap on
+          // rows 4..7 of every 8).
+          const float xv = __bfloat162float(*reinterpret_cast<const bf16*>(
+              xs + tl * 32 + ((xhalf ^ ((tl >> 2) & 1)) << 4)));
+          const float r = sigmoid_f(vr[u] + bra);
+          const float i = sigmoid_f(vi[u] + bri);
+          const float la = nk * r;
+          float abar = __expf(la);
+          float m = sqrtf(one_minus_a2(la));
+          const bool rst = ((tl < 32 ? (rlo >> tl) : (rhi >> (tl - 32))) & 1u) != 0u;
+          if (rst) {
+            abar = 0.0f;
+            m = 1.0f;
+          }
+          if (tl >= valid) {
+            abar = 1.0f;
+            m = 0.0f;
+          }
+          rh = fmaf(abar, rh, m * (i * xv));
+          rA *= abar;
+          hl[tl] = rh;
+          Ac[tl] = rA;
+        }
+      }
+      tc::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        tc::mbar_arrive(&acc_empty[a]);
+        tc::mbar_arrive(&x_empty[st]);
+      }
+
+      // Cross-chunk carry: anchored decoupled look-back over this warp's 32 channels.
+      const size_t cidx = (size_t)b * p.nC + c;
+      uint32_t* my_flag = flags + cidx * p.ng + g;
+      const bool publish = (blk * ntiles + n) != p.drop_tile;
+      float hin = 0.0f;
+      if (c == 0) {
+        if (p.canonical && p.h0) hin = p.h0[(size_t)b * p.W + w];
+      } else {
+        agg[cidx * p.W + w] = make_float2(rA, rh);
+        __threadfence();
+        __syncwarp();
+        if (lane == 0 && publish) st_release(my_flag, FLAG_AGG);
+        float accA = 1.0f, accB = 0.0f;
+        int cur = c - 1;
+        while (true) {
+          const size_t pidx = (size_t)b * p.nC + cur;
+          const bool anchor = (cur % ANCHOR) == 0;
+          const uint32_t f = spin_flag(flags + pidx * p.ng + g, anchor ? FLAG_INCL : FLAG_AGG,
+                                       p.spin_limit, status);
+          if (f == FLAG_TIMEOUT) {
+            hin = accB;
+            break;
+          }
+          if (anchor) {
+            const float hp = __ldcg(carry + ((size_t)b * (p.nC + 1) + cur + 1) * p.W + w);
+            hin = fmaf(accA, hp, accB);
+            break;
+          }
+          const float2 ag = __ldcg(agg + pidx * p.W + w);
+          accB = fmaf(accA, ag.y, accB);
+          accA *= ag.x;
+          --cur;
+        }
+      }
+      const float hend = fmaf(rA, hin, rh);
+      float* crow = carry + (size_t)b * (p.nC + 1) * p.W;
+      crow[(size_t)(c + 1) * p.W + w] = hend;
+      if (c == 0) crow[w] = hin;
+      if (c == p.nC - 1 && p.hT) p.hT[(size_t)b * p.W + w] = hend;
+      __threadfence();
+      __syncwarp();
+      if (lane == 0 && publish && c % ANCHOR == 0) st_release(my_flag, FLAG_INCL);
+
+      // y tile: registers -> smem [token][channel] -> TMA store (clipped at T).
+      if (store_thread) tc::tma_store_wait_read0();
+      tc::named_bar(1, 128);
+#pragma unroll
+      for (int tl = 0; tl < FUSED_C; ++tl)
+        *reinterpret_cast<bf16*>(s_y + tl * (FUSED_K * 2) + j * 2) =
+            __float2bfloat16_rn(fmaf(Ac[tl], hin, hl[tl]));
+      tc::fence_proxy_async_smem();
+      tc::named_bar(1, 128);
+      if (store_thread) {
+        tc::tma_store_3d(&tm_y, s_y, blk * FUSED_K, c * FUSED_C, b);
+        tc::tma_store_commit();
+      }
+    }
+    if (store_thread) tc::tma_store_wait0();
+  }
+
+  tc::tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc::tc_fence_after();
+    tc::tmem_dealloc(tmem, TMEM_COLS);
+  }
+}
+
+cudaError_t make_maps(const Dims& d, const void* x, const void* Wa, const void* Wx,
+                      const void* y, CUtensorMap* mx, CUtensorMap* mwa, CUtensorMap* mwx,
+                      CUtensorMap* my) {
+  const uint64_t W = d.W, T = d.T, B = d.B;
+  const uint64_t dims3[3] = {W, T, B};
+  const uint64_t str3[2] = {W * 2, T * W * 2};
+  const uint32_t box_x[3] = {16, FUSED_C, 1};
+  cudaError_t e = encode_tmap(mx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, x, dims3, str3, box_x,
+                              CU_TENSOR_MAP_SWIZZLE_32B);
+  if (e != cudaSuccess) return e;
+  const uint32_t box_y[3] = {FUSED_K, FUSED_C, 1};
+  e = encode_tmap(my, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, y, dims3, str3, box_y,
+                  CU_TENSOR_MAP_SWIZZLE_NONE);
+  if (e != cudaSuccess) return e;
+  // W[nblk][k][k] viewed as [nblk*k rows][k columns]
+  const uint64_t dimsw[2] = {(uint64_t)d.k, (uint64_t)d.nblk * d.k};
+  const uint64_t strw[1] = {(uint64_t)d.k * 2};
+  const uint32_t box_w[2] = {16, FUSED_K};
+  e = encode_tmap(mwa, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, Wa, dimsw, strw, box_w,
+                  CU_TENSOR_MAP_SWIZZLE_32B);
+  if (e != cudaSuccess) return e;
+  return encode_tmap(mwx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, Wx, dimsw, strw, box_w,
+                     CU_TENSOR_MAP_SWIZZLE_32B);
+}
+
+int ctas_per_block(const Dims& d) {
+  const int sms = sm_count();
+  return sms > 0 ? sms / d.nblk : 0;
+}
+
+}  // namespace
+
+bool fused_supported(const Dims& d) {
+  return d.io == RGLRU_BF16 && d.k == FUSED_K && ctas_per_block(d) >= 1;
+}
+
+cudaError_t launch_fused_fwd(const Dims& d, const void* x, const void* Wa, const float* ba,
+                             const void* Wx, const float* bx, const float* Lambda,
+                             const uint8_t* rm, const int32_t* sp, const float* h0, void* y,
+                             float* hT, void* saved, int spin_limit, int drop_tile,
+                             cudaStream_t s) {
+  if (!fused_supported(d)) return cudaErrorNotSupported;
+  CUtensorMap mx, mwa, mwx, my;
+  cudaError_t e = make_maps(d, x, Wa, Wx, y, &mx, &mwa, &mwx, &my);
+  if (e != cudaSuccess) return e;
+  FwdParams p;
+  p.B = d.B;
+  p.T = d.T;
+  p.W = d.W;
+  p.nblk = d.nblk;
+  p.nC = fused_chunks(d);
+  p.ng = d.ng;
+  p.P = ctas_per_block(d);
+  p.canonical = d.mode == RGLRU_CANONICAL;
+  p.Lambda = Lambda;
+  p.ba = ba;
+  p.bx = bx;
+  p.reset_mask = rm;
+  p.segment_pos = sp;
+  p.h0 = h0;
+  p.hT = hT;
+  p.scratch = static_cast<uint8_t*>(saved);
+  p.L = fused_layout(d, false);
+  p.spin_limit = spin_limit;
+  p.drop_tile = drop_tile;
+  e = cudaFuncSetAttribute(k_fused_fwd, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  e = cudaMemsetAsync(saved, 0, p.L.zero_bytes, s);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p.P * d.nblk);
+  cfg.blockDim = dim3(NTHREADS);
+  cfg.dynamicSmemBytes = SMEM_BYTES;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, k_fused_fwd, mx, mwa, mwx, my, p);
+  if (e == cudaSuccess) note_launches(1);
+  return e;
+}
+
+}  // namespace rglru

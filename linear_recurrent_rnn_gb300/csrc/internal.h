@@ -42,16 +42,31 @@ struct ScanLayout {
   size_t flags, zero_bytes, carry, agg, part, total;
 };
 
-inline ScanLayout scan_layout(const Dims& d, bool backward) {
+inline ScanLayout scan_layout_n(int B, int nC, int ng, int W, bool backward) {
   ScanLayout L;
-  const size_t nflags = (size_t)d.B * d.nC * d.ng;
+  const size_t nflags = (size_t)B * nC * ng;
   L.flags = 256;
   L.zero_bytes = align_up(L.flags + nflags * 4, 256);
   L.carry = L.zero_bytes;
-  L.agg = align_up(L.carry + (size_t)d.B * (d.nC + 1) * d.W * 4, 256);
-  L.part = align_up(L.agg + (size_t)d.B * d.nC * d.W * 8, 256);
-  L.total = backward ? align_up(L.part + (size_t)d.B * d.nC * d.W * 4, 256) : L.part;
+  L.agg = align_up(L.carry + (size_t)B * (nC + 1) * W * 4, 256);
+  L.part = align_up(L.agg + (size_t)B * nC * W * 8, 256);
+  L.total = backward ? align_up(L.part + (size_t)B * nC * W * 4, 256) : L.part;
   return L;
+}
+
+inline ScanLayout scan_layout(const Dims& d, bool backward) {
+  return scan_layout_n(d.B, d.nC, d.ng, d.W, backward);
+}
+
+// ---------------------------------------------------------------- fused tensor-core kernels
+// Gate-block width and tokens per tile of the fused kernels (the tile's MMA is M = 128
+// channels, N = 64 tokens, K = 128).
+constexpr int FUSED_K = 128;
+constexpr int FUSED_C = 64;
+
+inline int fused_chunks(const Dims& d) { return (d.T + FUSED_C - 1) / FUSED_C; }
+inline ScanLayout fused_layout(const Dims& d, bool backward) {
+  return scan_layout_n(d.B, fused_chunks(d), d.ng, d.W, backward);
 }
 
 // Split-K layout of the SIMT projection-weight gradient.
@@ -138,6 +153,15 @@ cudaError_t launch_scan_fwd(const ScanFwdArgs& a, int xt, int lt, bool canonical
                             cudaStream_t s);
 cudaError_t launch_scan_bwd(const ScanBwdArgs& a, int xt, int lt, int dxt, int dlt,
                             bool canonical, cudaStream_t s);
+
+// Fused forward on tensor cores (bf16 I/O, k == FUSED_K).  Returns cudaErrorNotSupported
+// when the shape is outside what the kernel covers (the caller then composes).
+cudaError_t launch_fused_fwd(const Dims& d, const void* x, const void* Wa, const float* ba,
+                             const void* Wx, const float* bx, const float* Lambda,
+                             const uint8_t* rm, const int32_t* sp, const float* h0, void* y,
+                             float* hT, void* saved, int spin_limit, int drop_tile,
+                             cudaStream_t s);
+bool fused_supported(const Dims& d);
 
 // SIMT projections (float32 accumulation).
 cudaError_t launch_gate_proj_simt(const Dims& d, int xt, int ot, const void* x, const void* Wa,

@@ -205,6 +205,22 @@ def test_fused_forward_backward(wl, seed, grad):
                 ba.double().numpy(), bx.double().numpy())
 
 
+def test_fused_forward_is_one_tensor_core_kernel():
+    """For bf16 I/O with 128-wide gate blocks the fused forward is a single kernel launch (the
+    tcgen05 kernel), not the composed projection + scan pair."""
+    wl = W_("one-kernel", 1, 64, 256, 128, "bf16", "restricted")
+    inp = generate(wl, 44)
+    sh = shape_for(wl)
+    d = {k: dev(v) for k, v in inp.items()}
+    y = torch.empty_like(d["x"])
+    saved = R.alloc_saved(sh)
+    n0 = R.rglru_kernel_launches()
+    R.rglru_fused_forward(sh, d["x"], d["Wa"], d["ba"], d["Wx"], d["bx"], d["Lambda"], None,
+                          None, None, y, None, saved)
+    assert R.rglru_kernel_launches() - n0 == 1
+    assert R.rglru_sync_status(saved) == R.OK
+
+
 def test_fused_deterministic():
     wl = W_("det", 2, 300, 256, 128, "bf16", "canonical", reset_p=0.01, h0_std=1.0)
     inp = generate(wl, 41)
