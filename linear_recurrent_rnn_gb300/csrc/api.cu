@@ -81,10 +81,7 @@ ComposedLayout composed_saved(const Dims& d) {
   return C;
 }
 struct ComposedWs {
-  // within `workspace`, after the backward scan layout; the bridge regions (a CUDA-core
-  // forward recomputed for the backward) are used only while the tensor-core forward has no
-  // tensor-core backward partner
-  size_t dxd, dlr, dli, gate, bsaved, blr, bli, total;
+  size_t dxd, dlr, dli, gate, total;  // within `workspace`, after the backward scan layout
 };
 ComposedWs composed_ws(const Dims& d) {
   ComposedWs C;
@@ -93,10 +90,7 @@ ComposedWs composed_ws(const Dims& d) {
   C.dlr = align_up(C.dxd + d.N * 4, 256);
   C.dli = align_up(C.dlr + d.N * 4, 256);
   C.gate = align_up(C.dli + d.N * 4, 256);
-  C.bsaved = align_up(C.gate + gate_bwd_layout(d).total, 256);
-  C.blr = align_up(C.bsaved + scan_layout(d, false).total, 256);
-  C.bli = align_up(C.blr + d.N * 4, 256);
-  C.total = align_up(C.bli + d.N * 4, 256);
+  C.total = align_up(C.gate + gate_bwd_layout(d).total, 256);
   return C;
 }
 
@@ -193,8 +187,10 @@ size_t rglru_workspace_bytes(const rglru_shape* shape) {
   size_t m = scan_layout(d, true).total;
   const size_t g = gate_bwd_layout(d).total;
   const size_t c = composed_ws(d).total;
+  const size_t f = fused_bwd_layout(d).total;
   if (g > m) m = g;
   if (c > m) m = c;
+  if (f > m) m = f;
   return m;
 }
 
@@ -308,23 +304,14 @@ rglru_status rglru_fused_backward(const rglru_shape* shape, const void* dy, cons
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   const ComposedLayout C = composed_saved(d);
   const ComposedWs CW = composed_ws(d);
+  if (fused_supported(d))
+    return cuda_status(launch_fused_bwd(d, dy, dhT, x, Wa, ba, Wx, bx, Lambda, reset_mask,
+                                        segment_pos, h0, saved, dx, dWa, dba, dWx, dbx, dLambda,
+                                        dh0, workspace, g_spin_limit, g_drop_tile, stream));
   const void* lr = sv + C.lr;
   const void* li = sv + C.li;
   const void* fsaved = saved;
   cudaError_t e = cudaSuccess;
-  if (fused_supported(d)) {
-    // Bridge: the forward ran on tensor cores and kept no logits; recompute them and the
-    // CUDA-core forward's chunk states in the workspace.
-    lr = ws + CW.blr;
-    li = ws + CW.bli;
-    fsaved = ws + CW.bsaved;
-    e = launch_gate_proj_simt(d, d.io, DT_F32, x, Wa, ba, Wx, bx, ws + CW.blr, ws + CW.bli,
-                              stream);
-    const ScanFwdArgs f = fwd_args(d, x, lr, li, Lambda, reset_mask, segment_pos, h0,
-                                   ws + CW.dxd, nullptr, ws + CW.bsaved);
-    if (e == cudaSuccess) e = cudaMemsetAsync(ws + CW.bsaved, 0, f.L.zero_bytes, stream);
-    if (e == cudaSuccess) e = launch_scan_fwd(f, d.io, DT_F32, d.mode == RGLRU_CANONICAL, stream);
-  }
   const ScanBwdArgs a = bwd_args(d, dy, dhT, x, lr, li, Lambda, reset_mask, segment_pos, h0,
                                  fsaved, ws + CW.dxd, ws + CW.dlr, ws + CW.dli, dLambda, dh0,
                                  workspace);

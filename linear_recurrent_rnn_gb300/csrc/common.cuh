@@ -66,6 +66,56 @@ __device__ __forceinline__ float softplus_f(float z) {
 // 1 - a^2 for a = e^la, la <= 0, without the cancellation of 1 - a*a as a -> 1.
 __device__ __forceinline__ float one_minus_a2(float la) { return -expm1f(2.0f * la); }
 
+// The same quantity from la and a = e^la (already computed), cheaper: for 2 la > -1/4 the
+// Taylor series of -expm1 at 0 truncated after x^7 (remainder below |x|^8 / 8! <= 4e-10,
+// well under float rounding), otherwise 1 - a*a, whose cancellation costs at most a factor
+// 1/(1 - e^-1/4) < 4.6 of one rounding.
+__device__ __forceinline__ float one_minus_a2_fast(float la, float a) {
+  const float x = 2.0f * la;
+  float p = fmaf(x, 1.0f / 5040.0f, 1.0f / 720.0f);
+  p = fmaf(x, p, 1.0f / 120.0f);
+  p = fmaf(x, p, 1.0f / 24.0f);
+  p = fmaf(x, p, 1.0f / 6.0f);
+  p = fmaf(x, p, 0.5f);
+  p = fmaf(x, p, 1.0f);
+  const float series = -x * p;
+  return x > -0.25f ? series : fmaf(-a, a, 1.0f);
+}
+
+// sqrt(v) for v >= 0 as v * rsqrt(v) (one special-function op), 0 at v = 0.
+__device__ __forceinline__ float sqrt_fast(float v) {
+  return v > 0.0f ? v * rsqrtf(v) : 0.0f;
+}
+
+// ---------------------------------------------------------------- value-as-flag slots
+// Look-back slots of the fused kernels carry their own readiness: a slot holds the all-ones
+// bit pattern (a NaN that float arithmetic never produces) until its value is stored with a
+// single-copy-atomic store.  A reader polls the slot itself, so one L2 round trip delivers
+// both the "ready" signal and the value.
+constexpr uint32_t SLOT_EMPTY32 = 0xffffffffu;
+constexpr uint64_t SLOT_EMPTY64 = 0xffffffffffffffffull;
+
+__device__ __forceinline__ uint64_t ld_relaxed_u64(const void* p) {
+  uint64_t v;
+  asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ uint32_t ld_relaxed_u32(const void* p) {
+  uint32_t v;
+  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_relaxed_u64(void* p, uint64_t v) {
+  asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+__device__ __forceinline__ void st_relaxed_u32(void* p, uint32_t v) {
+  asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ void slot_put2(float2* p, float a, float b) {
+  st_relaxed_u64(p, ((uint64_t)__float_as_uint(b) << 32) | __float_as_uint(a));
+}
+__device__ __forceinline__ void slot_put1(float* p, float a) { st_relaxed_u32(p, __float_as_uint(a)); }
+
 // Reset flag of token (b, t) in canonical mode.
 __device__ __forceinline__ bool is_reset(const uint8_t* reset_mask, const int32_t* segment_pos,
                                          size_t bt) {

@@ -1,0 +1,670 @@
+// Fused RG-LRU backward on one GB300: the gate logits are recomputed on the tcgen05 tensor
+// cores, the reverse scan and the pointwise derivatives run on the CUDA cores, and the
+// projection gradients dx += dlr Wa^T + dli Wx^T and dW = x^T dl go back to the tensor
+// cores, all in one persistent kernel; a small second kernel reduces the per-CTA partials.
+//
+// Sources ("Fattori comparison" page): the custom backward runs the reverse recurrence and the
+// pointwise derivatives, recomputing the sigmoids, the transition and the multiplier rather
+// than saving them; the a_param gradient is reduced over batch and time (done here on device,
+// in a fixed order).  The benchmark record checks gradients of x, both gate logits and
+// a_param, with the projections inside the measured layer.  Derivatives (loss
+// L = sum y dy + sum hT dhT, g_t = dL/dh_t):
+//   g_t = dy_t + abar_{t+1} g_{t+1}        (g_{T-1} = dy + dhT)
+//   dla = abar g (h_{t-1} - u abar / m)    (u = i x; zero at reset tokens)
+//   dlr = dla (-8 softplus) r (1 - r),  dli = g m u (1 - i),  dx_direct = g m i,
+//   dsoftplus = sum dla (-8 r),  dLambda = sigmoid(Lambda) dsoftplus,  dh0 = abar_0 g_0.
+//
+// Tile = (b, blk, 64 tokens), visited in reverse chunk order; two scan threads per channel,
+// one per 32-token half.  Per tile:
+//   1. MMA: lr^T, li^T = W^T x^T into TMEM (as in the forward).
+//   2. Pass 1 (tokens ascending): r, i, abar kept per token; the half's forward aggregate
+//      (state map h -> A h + B) and reverse aggregate (carry map c_in -> P c_in + S with
+//      P = prod abar, S = sum_t (prod_{s<=t} abar_s) dy_t).  The logits are then released.
+//   3. Halves exchange aggregates through shared memory; half 0 composes the tile's reverse
+//      aggregate and runs the anchored look-back toward larger t (lookback.cuh) for the carry
+//      from the right; the forward entry state comes from the chunk states the forward saved.
+//   4. Pass 2: h_{t-1} forward through the half, then g exactly in reverse with the pointwise
+//      gradients; dlr, dli go to shared memory as bf16 hi + lo pairs (v = hi + lo to ~2^-16),
+//      the direct dx term into the TMEM dx accumulator.
+//   5. MMA: dx^T += Wa (dlr_hi + dlr_lo)^T + Wx (dli_hi + dli_lo)^T on top of the direct term;
+//      dWa += x^T (dlr_hi + dlr_lo), dWx += x^T (dli_hi + dli_lo) accumulated in TMEM over the
+//      CTA's tiles.  The lo halves keep both products at float32-like accuracy: dl can be O(1)
+//      and a bf16-rounded dl alone would cost ~2^-9 |dl| in dx.
+//   6. dx TMEM -> bf16/f32 -> smem -> TMA store.
+// Roles: warp 0 TMA (W once; x + dy tiles, 2 stages), warp 1 MMA, warps 2..9 scan.  CTA
+// (blk, r) takes tiles r, r + P, ... of its block, so its partial sums cover a fixed set of
+// tiles: the result is bitwise reproducible.
+#include <cudaTypedefs.h>
+
+#include "host_util.h"
+#include "internal.h"
+#include "lookback.cuh"
+#include "tc.cuh"
+
+namespace rglru {
+
+namespace {
+
+constexpr int NSCAN = 8;
+constexpr int NTHREADS = 64 + NSCAN * 32;
+constexpr int HALF = FUSED_C / 2;
+constexpr int STAGES = 2;
+constexpr uint32_t W_BYTES = FUSED_K * FUSED_K * 2;
+constexpr uint32_t T_BYTES = FUSED_C * FUSED_K * 2;  // one 64 x 128 bf16 tile
+constexpr uint32_t SLAB_X = FUSED_C * 32;            // 16 channels x 64 tokens
+constexpr uint32_t SLAB_W = FUSED_K * 32;            // 16 out-channels x 128 in-rows
+constexpr uint32_t SLAB_D = FUSED_K * 32;            // 16 tokens x 128 channels (dl buffers)
+constexpr uint32_t TMEM_COLS = 512;
+constexpr uint32_t COL_LR = 0, COL_LI = 64, COL_DX = 128, COL_HP = 192, COL_DWA = 256,
+                   COL_DWX = 384;
+constexpr int WAIT_LIMIT = 1 << 22;
+constexpr uint32_t XCH_BYTES = 2 * FUSED_K * 16 + FUSED_K * 4;  // per-half aggregates + carry
+// W (2) + x/dy stages (2 x 2) + dl buffers (4) + bf16 dx staging (1) tiles, exchange, barriers
+constexpr size_t SMEM_BYTES =
+    2 * W_BYTES + STAGES * 2 * T_BYTES + 4 * T_BYTES + T_BYTES + XCH_BYTES + 256 + 1024;
+constexpr uint32_t STATUS_PIPE = 2u;
+
+struct BwdParams {
+  int B, T, W, nblk, nC, P, canonical;
+  const float* Lambda;
+  const float* ba;
+  const float* bx;
+  const uint8_t* reset_mask;
+  const int32_t* segment_pos;
+  const float* dhT;
+  const float* fwd_carry;  // [B][nC+1][W], state entering each chunk
+  float* dh0;
+  void* dx;                // written directly for float32 gradients
+  uint8_t* scratch;        // workspace
+  FusedBwdLayout F;
+  int spin_limit, drop_tile;
+};
+
+struct Ctl {
+  volatile uint32_t* abort;
+  uint32_t* status;
+  __device__ bool wait(uint64_t* bar, uint32_t parity) const {
+    if (*abort) return false;
+    if (tc::mbar_wait(bar, parity, WAIT_LIMIT)) return true;
+    *abort = 1u;
+    atomicOr(status, STATUS_PIPE);
+    return false;
+  }
+};
+
+// Element (token tl, channel j) of a 64 x 128 tile landed by TMA as 8 slabs of 16 channels
+// with 32-byte swizzle (16-byte halves swapped on rows 4..7 of every 8).
+__device__ __forceinline__ float tile_elem(const uint8_t* slab_base_j, int xhalf, int tl) {
+  return __bfloat162float(*reinterpret_cast<const bf16*>(
+      slab_base_j + tl * 32 + ((xhalf ^ ((tl >> 2) & 1)) << 4)));
+}
+
+// Packs 8 floats to 8 bf16 (round to nearest even).
+__device__ __forceinline__ uint4 pack8(const float* v) {
+  uint4 r;
+  __nv_bfloat162 p0 = __floats2bfloat162_rn(v[0], v[1]);
+  __nv_bfloat162 p1 = __floats2bfloat162_rn(v[2], v[3]);
+  __nv_bfloat162 p2 = __floats2bfloat162_rn(v[4], v[5]);
+  __nv_bfloat162 p3 = __floats2bfloat162_rn(v[6], v[7]);
+  r.x = *reinterpret_cast<uint32_t*>(&p0);
+  r.y = *reinterpret_cast<uint32_t*>(&p1);
+  r.z = *reinterpret_cast<uint32_t*>(&p2);
+  r.w = *reinterpret_cast<uint32_t*>(&p3);
+  return r;
+}
+
+// Writes 8 tokens of channel j (16-byte half `h8` of the 32-byte row of token group tg) as
+// hi and lo bf16 parts into the dl operand buffers [tg][channel row][16 tokens] (32-byte
+// swizzle: the two 16-byte halves swap on rows 4..7 of every 8).
+__device__ __forceinline__ void store_dl8(uint8_t* hi_buf, uint8_t* lo_buf, int tg, int h8, int j,
+                                          const float (&v)[8]) {
+  float hi[8], lo[8];
+#pragma unroll
+  for (int u = 0; u < 8; ++u) {
+    const bf16 h = __float2bfloat16_rn(v[u]);
+    hi[u] = __bfloat162float(h);
+    lo[u] = v[u] - hi[u];
+  }
+  const uint32_t at = tg * SLAB_D + j * 32 + ((h8 ^ ((j >> 2) & 1)) << 4);
+  *reinterpret_cast<uint4*>(hi_buf + at) = pack8(hi);
+  *reinterpret_cast<uint4*>(lo_buf + at) = pack8(lo);
+}
+
+// m = sqrt(1 - a^2) and 1/m (abar = a off resets), or (1, 1) at a reset token, (0, 0) past
+// T; one special-function op.  1/m is 0 where m is 0 (a = 1 exactly).
+__device__ __forceinline__ float2 multiplier(float la, float abar, bool rst, bool ok) {
+  const float om = one_minus_a2_fast(la, abar);
+  const float rs = om > 0.0f ? rsqrtf(om) : 0.0f;
+  const float m = om * rs;
+  return !ok ? make_float2(0.0f, 0.0f) : (rst ? make_float2(1.0f, 1.0f) : make_float2(m, rs));
+}
+
+// 10 warps: three share one SM sub-partition's 16 K registers, so at most 168 per thread.
+template <typename GT>
+__global__ void __launch_bounds__(NTHREADS, 1)
+    k_fused_bwd(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_dy,
+                const __grid_constant__ CUtensorMap tm_wa, const __grid_constant__ CUtensorMap tm_wx,
+                const __grid_constant__ CUtensorMap tm_dx, BwdParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  uint8_t* s_wa = smem;
+  uint8_t* s_wx = smem + W_BYTES;
+  uint8_t* s_in = smem + 2 * W_BYTES;               // stage s: x at s*2T, dy at s*2T + T
+  uint8_t* s_dl = s_in + STAGES * 2 * T_BYTES;      // r_hi, r_lo, i_hi, i_lo
+  uint8_t* s_dx = s_dl + 4 * T_BYTES;               // dx staging [token][channel]
+  float4* s_agg = reinterpret_cast<float4*>(s_dx + T_BYTES);  // [2][k]
+  float* s_cin = reinterpret_cast<float*>(s_agg + 2 * FUSED_K);                      // [k]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(s_cin + FUSED_K);
+  uint64_t* w_full = bars;
+  uint64_t* in_full = bars + 1;
+  uint64_t* in_empty = bars + 1 + STAGES;
+  uint64_t* lg_full = bars + 1 + 2 * STAGES;
+  uint64_t* lg_empty = lg_full + 1;
+  uint64_t* dl_full = lg_full + 2;
+  uint64_t* dl_empty = lg_full + 3;
+  uint64_t* dx_full = lg_full + 4;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(lg_full + 5);
+  volatile uint32_t* abort_flag = tmem_holder + 1;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int blk = blockIdx.x / p.P, rr = blockIdx.x % p.P;
+  const int ntiles = p.B * p.nC;
+  uint32_t* status = reinterpret_cast<uint32_t*>(p.scratch);
+  const Ctl ctl{abort_flag, status};
+
+  if (threadIdx.x == 0) {
+    tc::mbar_init(w_full, 1);
+    for (int s = 0; s < STAGES; ++s) {
+      tc::mbar_init(&in_full[s], 1);
+      tc::mbar_init(&in_empty[s], NSCAN + 1);  // scan warps + the dW MMAs
+    }
+    tc::mbar_init(lg_full, 1);
+    tc::mbar_init(lg_empty, NSCAN);
+    tc::mbar_init(dl_full, NSCAN);
+    tc::mbar_init(dl_empty, 1);
+    tc::mbar_init(dx_full, 1);
+    *abort_flag = 0u;
+    tc::fence_barrier_init();
+  }
+  if (warp == 0) {
+    tc::tmem_alloc(tmem_holder, TMEM_COLS);
+    tc::tmem_relinquish();
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+  int my_tiles = 0;
+  for (int n = rr; n < ntiles; n += p.P) ++my_tiles;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      tc::prefetch_tmap(&tm_x);
+      tc::prefetch_tmap(&tm_dy);
+      tc::mbar_expect_tx(w_full, 2 * W_BYTES);
+      for (int g = 0; g < FUSED_K / 16; ++g) {
+        tc::tma_load_2d(s_wa + g * SLAB_W, &tm_wa, w_full, 16 * g, blk * FUSED_K);
+        tc::tma_load_2d(s_wx + g * SLAB_W, &tm_wx, w_full, 16 * g, blk * FUSED_K);
+      }
+      for (int it = 0; it < my_tiles; ++it) {
+        const int n = rr + it * p.P;
+        const int st = it % STAGES;
+        const uint32_t ph = (it / STAGES) & 1;
+        if (!ctl.wait(&in_empty[st], ph ^ 1u)) continue;
+        const int c = p.nC - 1 - n / p.B, b = n % p.B;
+        uint8_t* xs = s_in + st * 2 * T_BYTES;
+        tc::mbar_expect_tx(&in_full[st], 2 * T_BYTES);
+        for (int s = 0; s < FUSED_K / 16; ++s) {
+          tc::tma_load_3d(xs + s * SLAB_X, &tm_x, &in_full[st], blk * FUSED_K + 16 * s,
+                          c * FUSED_C, b);
+          tc::tma_load_3d(xs + T_BYTES + s * SLAB_X, &tm_dy, &in_full[st],
+                          blk * FUSED_K + 16 * s, c * FUSED_C, b);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t id_lg = tc::idesc_bf16(128, FUSED_C, 1, 0);    // W^T x^T
+      constexpr uint32_t id_dx = tc::idesc_bf16(128, FUSED_C, 0, 1);    // W dl^T
+      constexpr uint32_t id_dw = tc::idesc_bf16(128, FUSED_K, 1, 0);    // x^T dl
+      ctl.wait(w_full, 0);
+      const uint32_t wa = tc::smem_u32(s_wa), wx = tc::smem_u32(s_wx);
+      const uint32_t dl0 = tc::smem_u32(s_dl);
+      auto logits = [&](int it) {
+        const int st = it % STAGES;
+        const uint32_t ph = (it / STAGES) & 1;
+        if (!ctl.wait(lg_empty, (it & 1) ^ 1u)) return;
+        if (!ctl.wait(&in_full[st], ph)) return;
+        tc::tc_fence_after();
+        const uint32_t xs = tc::smem_u32(s_in + st * 2 * T_BYTES);
+#pragma unroll
+        for (int kk = 0; kk < FUSED_K / 16; ++kk) {
+          const uint64_t bdesc = tc::smem_desc_sw32(xs + kk * SLAB_X, 16, 256);
+          tc::mma_bf16(tmem + COL_LR, tc::smem_desc_sw32(wa + kk * 512, SLAB_W, 256), bdesc,
+                       id_lg, kk > 0);
+          tc::mma_bf16(tmem + COL_LI, tc::smem_desc_sw32(wx + kk * 512, SLAB_W, 256), bdesc,
+                       id_lg, kk > 0);
+        }
+        tc::mma_commit(lg_full);
+      };
+      if (my_tiles > 0) logits(0);
+      for (int it = 0; it < my_tiles; ++it) {
+        if (it + 1 < my_tiles) logits(it + 1);
+        const int st = it % STAGES;
+        if (!ctl.wait(dl_full, it & 1)) continue;
+        tc::tc_fence_after();
+        // dx^T[in][tok] += W[in][out] dl^T[out][tok]: A = W K-major (one 16-column slab per K
+        // step), B = dl buffer MN-major (16-token groups 4 KB apart, 8-row groups 256 B).
+#pragma unroll
+        for (int kk = 0; kk < FUSED_K / 16; ++kk) {
+          const uint64_t a_a = tc::smem_desc_sw32(wa + kk * SLAB_W, 16, 256);
+          const uint64_t a_x = tc::smem_desc_sw32(wx + kk * SLAB_W, 16, 256);
+#pragma unroll
+          for (int part = 0; part < 2; ++part) {  // hi, then lo halves of dl
+            tc::mma_bf16(tmem + COL_DX, a_a,
+                         tc::smem_desc_sw32(dl0 + (0 + part) * T_BYTES + kk * 512, SLAB_D, 256),
+                         id_dx, 1);
+            tc::mma_bf16(tmem + COL_DX, a_x,
+                         tc::smem_desc_sw32(dl0 + (2 + part) * T_BYTES + kk * 512, SLAB_D, 256),
+                         id_dx, 1);
+          }
+        }
+        tc::mma_commit(dx_full);
+        // dW[in][out] += x^T[in][tok] dl[tok][out]: A = x tile MN-major (16-channel slabs 2 KB
+        // apart), B = dl buffer K-major (one 16-token group per K step).
+        const uint32_t xs = tc::smem_u32(s_in + st * 2 * T_BYTES);
+#pragma unroll
+        for (int kk = 0; kk < FUSED_C / 16; ++kk) {
+          const uint64_t adesc = tc::smem_desc_sw32(xs + kk * 512, SLAB_X, 256);
+          const uint32_t acc0 = (it > 0 || kk > 0) ? 1u : 0u;
+          tc::mma_bf16(tmem + COL_DWA, adesc,
+                       tc::smem_desc_sw32(dl0 + 0 * T_BYTES + kk * SLAB_D, 16, 256), id_dw, acc0);
+          tc::mma_bf16(tmem + COL_DWA, adesc,
+                       tc::smem_desc_sw32(dl0 + 1 * T_BYTES + kk * SLAB_D, 16, 256), id_dw, 1);
+          tc::mma_bf16(tmem + COL_DWX, adesc,
+                       tc::smem_desc_sw32(dl0 + 2 * T_BYTES + kk * SLAB_D, 16, 256), id_dw, acc0);
+          tc::mma_bf16(tmem + COL_DWX, adesc,
+                       tc::smem_desc_sw32(dl0 + 3 * T_BYTES + kk * SLAB_D, 16, 256), id_dw, 1);
+        }
+        tc::mma_commit(dl_empty);
+        tc::mma_commit(&in_empty[st]);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ scan warps
+    const int hf = (warp - 2) >> 2;
+    const int q = warp & 3;
+    const int j = q * 32 + lane;
+    const int w = blk * FUSED_K + j;
+    const int tb = hf * HALF;
+    const uint32_t tl_base = tmem + ((uint32_t)(q * 32) << 16);
+    const float nk = -8.0f * softplus_f(p.Lambda[w]);
+    const float bra = p.ba ? p.ba[w] : 0.0f;
+    const float bri = p.bx ? p.bx[w] : 0.0f;
+    float* rcar = reinterpret_cast<float*>(p.scratch + p.F.L.carry);
+    float2* agg = reinterpret_cast<float2*>(p.scratch + p.F.L.agg);
+    const bool store_thread = (warp == 2 && lane == 0);
+    if (store_thread) tc::prefetch_tmap(&tm_dx);
+    uint8_t* dl_rh = s_dl;
+    uint8_t* dl_rl = s_dl + T_BYTES;
+    uint8_t* dl_ih = s_dl + 2 * T_BYTES;
+    uint8_t* dl_il = s_dl + 3 * T_BYTES;
+    const int xhalf = (j & 15) >> 3;
+    float dsp_acc = 0.0f, dba_acc = 0.0f, dbx_acc = 0.0f;
+
+    for (int it = 0; it < my_tiles; ++it) {
+      const int n = rr + it * p.P;
+      const int c = p.nC - 1 - n / p.B, b = n % p.B;
+      const int st = it % STAGES;
+      const uint32_t ph = (it / STAGES) & 1;
+      const float hin_tile = p.fwd_carry[((size_t)b * (p.nC + 1) + c) * p.W + w];
+      ctl.wait(lg_full, it & 1);
+      ctl.wait(&in_full[st], ph);
+      tc::tc_fence_after();
+      const uint8_t* xj = s_in + st * 2 * T_BYTES + (j >> 4) * SLAB_X + (j & 7) * 2;
+      const uint8_t* dyj = xj + T_BYTES;
+
+      uint32_t rmask = 0;
+      if (p.canonical) {
+        const int t = c * FUSED_C + tb + lane;
+        rmask = __ballot_sync(0xffffffffu,
+                              t < p.T && is_reset(p.reset_mask, p.segment_pos, (size_t)b * p.T + t));
+      }
+      const int valid = min(FUSED_C, p.T - c * FUSED_C) - tb;
+
+      // Pass 1: gates of this half, its forward aggregate (fA, fB) and reverse aggregate
+      // (rP, rS).
+      float ab[HALF], rv[HALF], iv[HALF];
+      float fA = 1.0f, fB = 0.0f, rP = 1.0f, rS = 0.0f;
+#pragma unroll
+      for (int sub = 0; sub < HALF / 8; ++sub) {
+        float vr[8], vi[8];
+        tc::tmem_ld8(tl_base + COL_LR + tb + sub * 8, vr);
+        tc::tmem_ld8(tl_base + COL_LI + tb + sub * 8, vi);
+        tc::tmem_ld_wait();
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const int tt = sub * 8 + u;
+          const int tl = tb + tt;
+          const bool ok = tt < valid;
+          const bool rst = ((rmask >> tt) & 1u) != 0u;
+          const float xv = tile_elem(xj, xhalf, tl);
+          const float dyv = ok ? tile_elem(dyj, xhalf, tl) : 0.0f;
+          const float r = sigmoid_f(vr[u] + bra);
+          const float i = sigmoid_f(vi[u] + bri);
+          const float la = nk * r;
+          const float a = __expf(la);
+          const float m0 = sqrt_fast(one_minus_a2_fast(la, a));
+          const float abar = !ok ? 1.0f : (rst ? 0.0f : a);
+          const float m = !ok ? 0.0f : (rst ? 1.0f : m0);
+          fB = fmaf(abar, fB, m * (i * xv));
+          fA *= abar;
+          rP *= abar;
+          rS = fmaf(rP, dyv, rS);
+          ab[tt] = abar;
+          rv[tt] = r;
+          iv[tt] = i;
+        }
+      }
+      tc::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(lg_empty);  // logits consumed: next tile's may start
+
+      s_agg[hf * FUSED_K + j] = make_float4(fA, fB, rP, rS);
+      if (store_thread) tc::tma_store_wait_read0();  // the dx staging is free again
+      tc::named_bar(1, NSCAN * 32);
+      const float4 o = s_agg[(1 - hf) * FUSED_K + j];  // the other half's aggregates
+
+      // Half 0 owns the chunk's reverse carry: tile aggregate = half 0 o half 1.
+      if (hf == 0) {
+        const float tP = rP * o.z, tS = fmaf(rP, o.w, rS);
+        const size_t cidx = (size_t)b * p.nC + c;
+        const bool publish = (blk * ntiles + n) != p.drop_tile;
+        const bool anchor = ((p.nC - 1 - c) % ANCHOR) == 0;
+        float cin = 0.0f;
+        if (c == p.nC - 1) {
+          if (p.dhT) cin = p.dhT[(size_t)b * p.W + w];
+        } else {
+          if (!anchor && publish) slot_put2(agg + cidx * p.W + w, tP, tS);
+          // nearest anchor after this chunk (anchors counted from the last chunk)
+          const int an = p.nC - 1 - ((p.nC - 2 - c) / ANCHOR) * ANCHOR;
+          cin = lookback_carry(agg + (cidx + 1) * p.W + w, (long)p.W, an - c - 1,
+                               rcar + ((size_t)b * p.nC + an) * p.W + w, p.spin_limit, status);
+        }
+        const float cout = fmaf(tP, cin, tS);
+        if (publish) slot_put1(rcar + cidx * p.W + w, cout);
+        if (c == 0 && p.dh0) p.dh0[(size_t)b * p.W + w] = p.canonical ? cout : 0.0f;
+        s_cin[j] = cin;
+      }
+      tc::named_bar(1, NSCAN * 32);
+      const float cin_t = s_cin[j];
+      // carry into this half from the right, state entering it from the left
+      const float cin = hf == 1 ? cin_t : fmaf(o.z, cin_t, o.w);
+      const float hq = hf == 0 ? hin_tile : fmaf(o.x, hin_tile, o.y);
+
+      // The dl buffers and the dx accumulator are free once the previous tile's MMAs are done.
+      if (it > 0) ctl.wait(dl_empty, (it - 1) & 1);
+      tc::tc_fence_after();
+
+      // Pass 2a: h_{t-1} through the half.
+      // h_{t-1} of the half is parked in the spare TMEM columns (registers are the limit).
+      {
+        float h = hq;
+#pragma unroll
+        for (int sub = 0; sub < HALF / 16; ++sub) {
+          float hp16[16];
+#pragma unroll
+          for (int u = 0; u < 16; ++u) {
+            const int tt = sub * 16 + u;
+            const int tl = tb + tt;
+            const bool ok = tt < valid;
+            const bool rst = ((rmask >> tt) & 1u) != 0u;
+            const float la = nk * rv[tt];
+            const float m = multiplier(la, ab[tt], rst, ok).x;
+            hp16[u] = h;
+            h = fmaf(ab[tt], h, m * (iv[tt] * tile_elem(xj, xhalf, tl)));
+          }
+          tc::tmem_st16(tl_base + COL_HP + tb + sub * 16, hp16);
+        }
+        tc::tmem_st_wait();
+      }
+      // Pass 2b: g exactly, tokens descending, and the pointwise gradients.
+      float gnext = cin, abar_next = 1.0f;
+#pragma unroll
+      for (int sub = HALF / 8 - 1; sub >= 0; --sub) {  // 8 tokens at a time (registers)
+        float o_r[8], o_i[8], o_x[8], hp16[8];
+        tc::tmem_ld8(tl_base + COL_HP + tb + sub * 8, hp16);
+        tc::tmem_ld_wait();
+#pragma unroll
+        for (int u = 7; u >= 0; --u) {
+          const int tt = sub * 8 + u;
+          const int tl = tb + tt;
+          const bool ok = tt < valid;
+          const bool rst = ((rmask >> tt) & 1u) != 0u;
+          const float r = rv[tt], i = iv[tt], abar = ab[tt];
+          const float la = nk * r;
+          const float2 mm = multiplier(la, abar, rst, ok);
+          const float m = mm.x;
+          const float dyv = ok ? tile_elem(dyj, xhalf, tl) : 0.0f;
+          const float uu = i * tile_elem(xj, xhalf, tl);
+          const float gv = fmaf(abar_next, gnext, dyv);
+          // zero at reset tokens (abar = 0) and past T (m = 0)
+          const float alpha = (abar == 0.0f || m == 0.0f) ? 0.0f : abar * (hp16[u] - uu * abar * mm.y);
+          const float dla = gv * alpha;
+          o_r[u] = dla * nk * r * (1.0f - r);
+          o_i[u] = gv * m * uu * (1.0f - i);
+          o_x[u] = gv * m * i;
+          dsp_acc = fmaf(dla, -8.0f * r, dsp_acc);
+          dba_acc += o_r[u];
+          dbx_acc += o_i[u];
+          gnext = gv;
+          abar_next = abar;
+        }
+        const int tg = hf * (HALF / 16) + (sub >> 1);  // 16-token group of the dl buffers
+        store_dl8(dl_rh, dl_rl, tg, sub & 1, j, o_r);
+        store_dl8(dl_ih, dl_il, tg, sub & 1, j, o_i);
+        tc::tmem_st8(tl_base + COL_DX + tb + sub * 8, o_x);
+      }
+      tc::tmem_st_wait();
+      tc::fence_proxy_async_smem();
+      tc::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        tc::mbar_arrive(&in_empty[st]);
+        tc::mbar_arrive(dl_full);
+      }
+
+      // dx tile: TMEM -> smem [token][channel] -> TMA store (clipped at T).
+      ctl.wait(dx_full, it & 1);
+      tc::tc_fence_after();
+#pragma unroll
+      for (int sub = 0; sub < HALF / 16; ++sub) {
+        float v[16];
+        tc::tmem_ld16(tl_base + COL_DX + tb + sub * 16, v);
+        tc::tmem_ld_wait();
+#pragma unroll
+        for (int u = 0; u < 16; ++u) {
+          const int tl = tb + sub * 16 + u;
+          if (sizeof(GT) == 2) {
+            *reinterpret_cast<bf16*>(s_dx + tl * (FUSED_K * 2) + j * 2) = __float2bfloat16_rn(v[u]);
+          } else if (sub * 16 + u < valid) {
+            // float32 gradients go straight to HBM (128 contiguous bytes per warp and token)
+            static_cast<float*>(p.dx)[((size_t)b * p.T + c * FUSED_C + tl) * p.W + w] = v[u];
+          }
+        }
+      }
+      tc::tc_fence_before();
+      tc::fence_proxy_async_smem();
+      tc::named_bar(1, NSCAN * 32);
+      if (store_thread && sizeof(GT) == 2) {
+        tc::tma_store_3d(&tm_dx, s_dx, blk * FUSED_K, c * FUSED_C, b);
+        tc::tma_store_commit();
+      }
+    }
+    if (store_thread) tc::tma_store_wait0();
+
+    // Per-CTA, per-half partials of the per-channel sums.
+    float* vp = reinterpret_cast<float*>(p.scratch + p.F.vec_part) +
+                ((size_t)blockIdx.x * 2 + hf) * 3 * FUSED_K;
+    vp[j] = dsp_acc;
+    vp[FUSED_K + j] = dba_acc;
+    vp[2 * FUSED_K + j] = dbx_acc;
+
+    // Per-CTA dW partials: lane j of the accumulators is input channel j; each half copies
+    // 64 of the 128 output-channel columns.
+    if (my_tiles > 0) ctl.wait(dl_empty, (my_tiles - 1) & 1);
+    tc::tc_fence_after();
+    float* dwp = reinterpret_cast<float*>(p.scratch + p.F.dw_part) +
+                 (size_t)blockIdx.x * 2 * FUSED_K * FUSED_K;
+#pragma unroll
+    for (int mtx = 0; mtx < 2; ++mtx) {
+#pragma unroll
+      for (int sub = 0; sub < FUSED_K / 32; ++sub) {
+        const int col = hf * (FUSED_K / 2) + sub * 16;
+        float v[16];
+        if (my_tiles > 0) {
+          tc::tmem_ld16(tl_base + (mtx ? COL_DWX : COL_DWA) + col, v);
+          tc::tmem_ld_wait();
+        } else {
+#pragma unroll
+          for (int u = 0; u < 16; ++u) v[u] = 0.0f;
+        }
+        float4* dst = reinterpret_cast<float4*>(dwp + ((size_t)mtx * FUSED_K + j) * FUSED_K + col);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) dst[u] = make_float4(v[4 * u], v[4 * u + 1], v[4 * u + 2], v[4 * u + 3]);
+      }
+    }
+  }
+
+  tc::tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc::tc_fence_after();
+    tc::tmem_dealloc(tmem, TMEM_COLS);
+  }
+}
+
+// Sums the per-CTA (and per-half) partials of every gate block in a fixed order
+// (deterministic): dWa, dWx [nblk][k][k]; dba, dbx [W]; dLambda = sigmoid(Lambda) * sum.
+__global__ void k_fused_bwd_reduce(const float* dw_part, const float* vec_part, int P, int nblk,
+                                   const float* Lambda, float* dWa, float* dWx, float* dba,
+                                   float* dbx, float* dLambda) {
+  const int blk = blockIdx.y;
+  const int e = blockIdx.x * blockDim.x + threadIdx.x;  // element of the k x k block
+  if (e < FUSED_K * FUSED_K) {
+    float sa = 0.0f, sx = 0.0f;
+    for (int r = 0; r < P; ++r) {
+      const float* src = dw_part + (size_t)(blk * P + r) * 2 * FUSED_K * FUSED_K;
+      sa += src[e];
+      sx += src[FUSED_K * FUSED_K + e];
+    }
+    dWa[(size_t)blk * FUSED_K * FUSED_K + e] = sa;
+    dWx[(size_t)blk * FUSED_K * FUSED_K + e] = sx;
+  }
+  if (blockIdx.x == 0 && threadIdx.x < FUSED_K) {
+    const int j = threadIdx.x, w = blk * FUSED_K + j;
+    float s0 = 0.0f, s1 = 0.0f, s2 = 0.0f;
+    for (int r = 0; r < 2 * P; ++r) {
+      const float* src = vec_part + ((size_t)blk * P * 2 + r) * 3 * FUSED_K;
+      s0 += src[j];
+      s1 += src[FUSED_K + j];
+      s2 += src[2 * FUSED_K + j];
+    }
+    dLambda[w] = s0 * __fdividef(1.0f, 1.0f + expf(-Lambda[w]));
+    if (dba) dba[w] = s1;
+    if (dbx) dbx[w] = s2;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_fused_bwd(const Dims& d, const void* dy, const float* dhT, const void* x,
+                             const void* Wa, const float* ba, const void* Wx, const float* bx,
+                             const float* Lambda, const uint8_t* rm, const int32_t* sp,
+                             const float* h0, const void* saved, void* dx, float* dWa,
+                             float* dba, float* dWx, float* dbx, float* dLambda, float* dh0,
+                             void* ws, int spin_limit, int drop_tile, cudaStream_t s) {
+  (void)h0;  // the chunk entry states saved by the forward already include h0
+  if (!fused_supported(d)) return cudaErrorNotSupported;
+  const uint64_t W = d.W, T = d.T, B = d.B;
+  const uint64_t dims3[3] = {W, T, B};
+  const uint64_t str3[2] = {W * 2, T * W * 2};
+  const uint32_t box_in[3] = {16, FUSED_C, 1};
+  CUtensorMap mx, mdy, mwa, mwx, mdx;
+  cudaError_t e = encode_tmap(&mx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, x, dims3, str3, box_in,
+                              CU_TENSOR_MAP_SWIZZLE_32B);
+  if (e == cudaSuccess)
+    e = encode_tmap(&mdy, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, dy, dims3, str3, box_in,
+                    CU_TENSOR_MAP_SWIZZLE_32B);
+  const uint64_t dimsw[2] = {(uint64_t)d.k, (uint64_t)d.nblk * d.k};
+  const uint64_t strw[1] = {(uint64_t)d.k * 2};
+  const uint32_t box_w[2] = {16, FUSED_K};
+  if (e == cudaSuccess)
+    e = encode_tmap(&mwa, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, Wa, dimsw, strw, box_w,
+                    CU_TENSOR_MAP_SWIZZLE_32B);
+  if (e == cudaSuccess)
+    e = encode_tmap(&mwx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, Wx, dimsw, strw, box_w,
+                    CU_TENSOR_MAP_SWIZZLE_32B);
+  const bool gf32 = d.grad == RGLRU_F32;
+  const uint64_t gsz = gf32 ? 4 : 2;
+  const uint64_t strg[2] = {W * gsz, T * W * gsz};
+  const uint32_t box_dx[3] = {FUSED_K, FUSED_C, 1};
+  if (e == cudaSuccess)
+    e = encode_tmap(&mdx, gf32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                    3, dx, dims3, strg, box_dx, CU_TENSOR_MAP_SWIZZLE_NONE);
+  if (e != cudaSuccess) return e;
+
+  BwdParams p;
+  p.B = d.B;
+  p.T = d.T;
+  p.W = d.W;
+  p.nblk = d.nblk;
+  p.nC = fused_chunks(d);
+  p.P = fused_ctas_per_block(d);
+  p.canonical = d.mode == RGLRU_CANONICAL;
+  p.Lambda = Lambda;
+  p.ba = ba;
+  p.bx = bx;
+  p.reset_mask = rm;
+  p.segment_pos = sp;
+  p.dhT = dhT;
+  p.fwd_carry = reinterpret_cast<const float*>(static_cast<const uint8_t*>(saved) +
+                                               fused_layout(d, false).carry);
+  p.dh0 = dh0;
+  p.scratch = static_cast<uint8_t*>(ws);
+  p.F = fused_bwd_layout(d);
+  p.spin_limit = spin_limit;
+  p.drop_tile = drop_tile;
+  p.dx = dx;
+  const size_t smem = SMEM_BYTES;
+  auto kern = gf32 ? k_fused_bwd<float> : k_fused_bwd<bf16>;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  e = clear_slots(ws, p.F.L, s);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p.P * d.nblk);
+  cfg.blockDim = dim3(NTHREADS);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, kern, mx, mdy, mwa, mwx, mdx, p);
+  if (e != cudaSuccess) return e;
+  note_launches(1);
+  const uint8_t* wsb = static_cast<const uint8_t*>(ws);
+  k_fused_bwd_reduce<<<dim3((FUSED_K * FUSED_K + 255) / 256, d.nblk), 256, 0, s>>>(
+      reinterpret_cast<const float*>(wsb + p.F.dw_part),
+      reinterpret_cast<const float*>(wsb + p.F.vec_part), p.P, d.nblk, Lambda, dWa, dWx, dba,
+      dbx, dLambda);
+  note_launches(1);
+  return cudaGetLastError();
+}
+
+}  // namespace rglru

@@ -13,28 +13,31 @@
 // Tile = (batch row b, gate block blk, 64 tokens).  For the tile the MMA computes the
 // transposed logits  lr^T[128 ch x 64 tok] = Wa[blk]^T (MN-major A, from W stored (in, out))
 // x x_tile^T (K-major B, the x tile as TMA lands it), and li^T likewise, so TMEM lane =
-// channel and column = token: each scan thread owns one channel and runs the recurrence over
-// its 64 tokens serially in registers.  Chunks are joined by the anchored decoupled look-back
-// of the scan kernels (flags and aggregates in `saved`), which makes the result bitwise
-// deterministic.
+// channel and column = token.  Two scan threads own each channel, one per 32-token half: each
+// runs its half serially in registers from a zero state, the halves are joined through shared
+// memory, and chunks through the anchored look-back over value slots in `saved`
+// (lookback.cuh), which keeps the result bitwise deterministic.
 //
-// Roles (192 threads, one CTA per SM, launched cooperatively so that all CTAs are resident):
+// Roles (320 threads, one CTA per SM, launched cooperatively so that all CTAs are resident):
 //   warp 0      TMA producer: Wa[blk], Wx[blk] once, then the x tile ring (3 stages)
 //   warp 1      MMA issuer: 2 x 8 tcgen05.mma (K = 16 each) per tile into a 2-deep TMEM ring
-//   warps 2..5  scan: TMEM -> registers, gate math, local scan, look-back, y -> smem -> TMA
+//   warps 2..9  scan: warps 2-5 tokens 0-31, warps 6-9 tokens 32-63 (lane quadrant warp % 4)
 // CTA (blk, r) of the P CTAs serving gate block blk takes the block's tiles n = r, r + P, ...
 // in chunk-major order, so every tile it waits on is earlier in the same order.
 #include <cudaTypedefs.h>
 
 #include "host_util.h"
 #include "internal.h"
+#include "lookback.cuh"
 #include "tc.cuh"
 
 namespace rglru {
 
 namespace {
 
-constexpr int NTHREADS = 192;
+constexpr int NSCAN = 8;
+constexpr int NTHREADS = 64 + NSCAN * 32;
+constexpr int HALF = FUSED_C / 2;
 constexpr int XSTAGES = 3;
 constexpr uint32_t W_BYTES = FUSED_K * FUSED_K * 2;  // one weight block, bf16
 constexpr uint32_t X_BYTES = FUSED_C * FUSED_K * 2;  // one x tile, bf16
@@ -43,11 +46,13 @@ constexpr uint32_t SLAB_X = FUSED_C * 32;            // 16 channels x 64 tokens
 constexpr uint32_t SLAB_W = FUSED_K * 32;            // 16 out-channels x 128 in-rows
 constexpr uint32_t TMEM_COLS = 256;                  // 2 buffers x (lr 64 + li 64) columns
 constexpr int WAIT_LIMIT = 1 << 22;
-constexpr size_t SMEM_BYTES = 2 * W_BYTES + XSTAGES * X_BYTES + Y_BYTES + 256 + 1024;
+constexpr uint32_t XCH_BYTES = FUSED_K * 8 + FUSED_K * 4;  // half-0 aggregates + tile carry
+constexpr size_t SMEM_BYTES =
+    2 * W_BYTES + XSTAGES * X_BYTES + Y_BYTES + XCH_BYTES + 256 + 1024;
 constexpr uint32_t STATUS_PIPE = 2u;
 
 struct FwdParams {
-  int B, T, W, nblk, nC, ng, P, canonical;
+  int B, T, W, nblk, nC, P, canonical;
   const float* Lambda;
   const float* ba;
   const float* bx;
@@ -85,7 +90,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   uint8_t* s_wx = smem + W_BYTES;
   uint8_t* s_x = smem + 2 * W_BYTES;
   uint8_t* s_y = s_x + XSTAGES * X_BYTES;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(s_y + Y_BYTES);
+  float2* s_agg0 = reinterpret_cast<float2*>(s_y + Y_BYTES);  // half-0 aggregate per channel
+  float* s_hin = reinterpret_cast<float*>(s_agg0 + FUSED_K);  // carry into the tile
+  uint64_t* bars = reinterpret_cast<uint64_t*>(s_hin + FUSED_K);
   uint64_t* w_full = bars;
   uint64_t* x_full = bars + 1;
   uint64_t* x_empty = bars + 1 + XSTAGES;
@@ -104,11 +111,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     tc::mbar_init(w_full, 1);
     for (int s = 0; s < XSTAGES; ++s) {
       tc::mbar_init(&x_full[s], 1);
-      tc::mbar_init(&x_empty[s], 4);
+      tc::mbar_init(&x_empty[s], NSCAN);
     }
     for (int a = 0; a < 2; ++a) {
       tc::mbar_init(&acc_full[a], 1);
-      tc::mbar_init(&acc_empty[a], 4);
+      tc::mbar_init(&acc_empty[a], NSCAN);
     }
     *abort_flag = 0u;
     tc::fence_barrier_init();
@@ -175,19 +182,20 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     }
   } else {
     // ------------------------------------------------------------ scan warps
-    const int q = warp & 3;  // TMEM lane quadrant this warp may access
+    const int hf = (warp - 2) >> 2;  // token half of the tile
+    const int q = warp & 3;          // TMEM lane quadrant this warp may access
     const int j = q * 32 + lane;
     const int w = blk * FUSED_K + j;
+    const int tb = hf * HALF;
     const uint32_t lane_base = (uint32_t)(q * 32) << 16;
     const float nk = -8.0f * softplus_f(p.Lambda[w]);
     const float bra = p.ba ? p.ba[w] : 0.0f;
     const float bri = p.bx ? p.bx[w] : 0.0f;
-    const int g = blk * (FUSED_K / 32) + q;
-    uint32_t* flags = reinterpret_cast<uint32_t*>(p.scratch + p.L.flags);
     float* carry = reinterpret_cast<float*>(p.scratch + p.L.carry);
     float2* agg = reinterpret_cast<float2*>(p.scratch + p.L.agg);
     const bool store_thread = (warp == 2 && lane == 0);
     if (store_thread) tc::prefetch_tmap(&tm_y);
+    const int xhalf = (j & 15) >> 3;
 
     int it = 0;
     for (int n = rr; n < ntiles; n += p.P, ++it) {
@@ -200,53 +208,48 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       ctl.wait(&x_full[st], ph);
       tc::tc_fence_after();
 
-      // Reset tokens of this tile as two 32-bit masks.
-      uint32_t rlo = 0, rhi = 0;
+      uint32_t rmask = 0;
       if (p.canonical) {
-        const int t_a = c * FUSED_C + lane, t_b = t_a + 32;
-        const size_t row = (size_t)b * p.T;
-        const bool fa = t_a < p.T && is_reset(p.reset_mask, p.segment_pos, row + t_a);
-        const bool fb = t_b < p.T && is_reset(p.reset_mask, p.segment_pos, row + t_b);
-        rlo = __ballot_sync(0xffffffffu, fa);
-        rhi = __ballot_sync(0xffffffffu, fb);
+        const int t = c * FUSED_C + tb + lane;
+        rmask = __ballot_sync(0xffffffffu,
+                              t < p.T && is_reset(p.reset_mask, p.segment_pos, (size_t)b * p.T + t));
       }
-      const int valid = min(FUSED_C, p.T - c * FUSED_C);
+      const int valid = min(FUSED_C, p.T - c * FUSED_C) - tb;  // tokens of this half < T
       const uint8_t* xs = s_x + st * X_BYTES + (j >> 4) * SLAB_X + (j & 7) * 2;
-      const int xhalf = (j & 15) >> 3;
 
-      float hl[FUSED_C], Ac[FUSED_C];
+      // Local scan of this half from a zero state: hl = state after each token, Ac = product
+      // of abar up to it.
+      float hl[HALF], Ac[HALF];
       float rh = 0.0f, rA = 1.0f;
 #pragma unroll
-      for (int sub = 0; sub < FUSED_C / 16; ++sub) {
+      for (int sub = 0; sub < HALF / 16; ++sub) {
         float vr[16], vi[16];
-        tc::tmem_ld16(tmem + lane_base + a * 128 + sub * 16, vr);
-        tc::tmem_ld16(tmem + lane_base + a * 128 + 64 + sub * 16, vi);
+        tc::tmem_ld16(tmem + lane_base + a * 128 + tb + sub * 16, vr);
+        tc::tmem_ld16(tmem + lane_base + a * 128 + 64 + tb + sub * 16, vi);
         tc::tmem_ld_wait();
 #pragma unroll
         for (int u = 0; u < 16; ++u) {
-          const int tl = sub * 16 + u;
-          // x[tile token tl, channel j] in the 32-byte-swizzled slab (16-byte halves swap on
-          // rows 4..7 of every 8).
+          const int tt = sub * 16 + u;  // token within the half
+          const int tl = tb + tt;       // token within the tile
           const float xv = __bfloat162float(*reinterpret_cast<const bf16*>(
               xs + tl * 32 + ((xhalf ^ ((tl >> 2) & 1)) << 4)));
           const float r = sigmoid_f(vr[u] + bra);
           const float i = sigmoid_f(vi[u] + bri);
           const float la = nk * r;
           float abar = __expf(la);
-          float m = sqrtf(one_minus_a2(la));
-          const bool rst = ((tl < 32 ? (rlo >> tl) : (rhi >> (tl - 32))) & 1u) != 0u;
-          if (rst) {
+          float m = sqrt_fast(one_minus_a2_fast(la, abar));
+          if ((rmask >> tt) & 1u) {
             abar = 0.0f;
             m = 1.0f;
           }
-          if (tl >= valid) {
+          if (tt >= valid) {
             abar = 1.0f;
             m = 0.0f;
           }
           rh = fmaf(abar, rh, m * (i * xv));
           rA *= abar;
-          hl[tl] = rh;
-          Ac[tl] = rA;
+          hl[tt] = rh;
+          Ac[tt] = rA;
         }
       }
       tc::tc_fence_before();
@@ -256,58 +259,48 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         tc::mbar_arrive(&x_empty[st]);
       }
 
-      // Cross-chunk carry: anchored decoupled look-back over this warp's 32 channels.
-      const size_t cidx = (size_t)b * p.nC + c;
-      uint32_t* my_flag = flags + cidx * p.ng + g;
-      const bool publish = (blk * ntiles + n) != p.drop_tile;
-      float hin = 0.0f;
-      if (c == 0) {
-        if (p.canonical && p.h0) hin = p.h0[(size_t)b * p.W + w];
-      } else {
-        agg[cidx * p.W + w] = make_float2(rA, rh);
-        __threadfence();
-        __syncwarp();
-        if (lane == 0 && publish) st_release(my_flag, FLAG_AGG);
-        float accA = 1.0f, accB = 0.0f;
-        int cur = c - 1;
-        while (true) {
-          const size_t pidx = (size_t)b * p.nC + cur;
-          const bool anchor = (cur % ANCHOR) == 0;
-          const uint32_t f = spin_flag(flags + pidx * p.ng + g, anchor ? FLAG_INCL : FLAG_AGG,
-                                       p.spin_limit, status);
-          if (f == FLAG_TIMEOUT) {
-            hin = accB;
-            break;
-          }
-          if (anchor) {
-            const float hp = __ldcg(carry + ((size_t)b * (p.nC + 1) + cur + 1) * p.W + w);
-            hin = fmaf(accA, hp, accB);
-            break;
-          }
-          const float2 ag = __ldcg(agg + pidx * p.W + w);
-          accB = fmaf(accA, ag.y, accB);
-          accA *= ag.x;
-          --cur;
+      if (hf == 0) s_agg0[j] = make_float2(rA, rh);
+      if (store_thread) tc::tma_store_wait_read0();  // the y staging is free again
+      tc::named_bar(1, NSCAN * 32);
+
+      // Half 1 owns the chunk: its aggregate composed with half 0's is the tile's.
+      float A0 = 1.0f, B0 = 0.0f;
+      if (hf == 1) {
+        const float2 h0agg = s_agg0[j];
+        A0 = h0agg.x;
+        B0 = h0agg.y;
+        const float At = rA * A0, Bt = fmaf(rA, B0, rh);
+        const size_t cidx = (size_t)b * p.nC + c;
+        const bool publish = (blk * ntiles + n) != p.drop_tile;
+        const bool anchor = (c % ANCHOR) == 0;
+        float hin = 0.0f;
+        if (c == 0) {
+          if (p.canonical && p.h0) hin = p.h0[(size_t)b * p.W + w];
+        } else {
+          if (!anchor && publish) slot_put2(agg + cidx * p.W + w, At, Bt);
+          const int an = ((c - 1) / ANCHOR) * ANCHOR;  // nearest anchor before this chunk
+          hin = lookback_carry(agg + (cidx - 1) * p.W + w, -(long)p.W, c - 1 - an,
+                               carry + ((size_t)b * (p.nC + 1) + an + 1) * p.W + w,
+                               p.spin_limit, status);
         }
+        const float hend = fmaf(At, hin, Bt);
+        float* crow = carry + (size_t)b * (p.nC + 1) * p.W;
+        if (publish) slot_put1(crow + (size_t)(c + 1) * p.W + w, hend);
+        if (c == 0) slot_put1(crow + w, hin);
+        if (c == p.nC - 1 && p.hT) p.hT[(size_t)b * p.W + w] = hend;
+        s_hin[j] = hin;
       }
-      const float hend = fmaf(rA, hin, rh);
-      float* crow = carry + (size_t)b * (p.nC + 1) * p.W;
-      crow[(size_t)(c + 1) * p.W + w] = hend;
-      if (c == 0) crow[w] = hin;
-      if (c == p.nC - 1 && p.hT) p.hT[(size_t)b * p.W + w] = hend;
-      __threadfence();
-      __syncwarp();
-      if (lane == 0 && publish && c % ANCHOR == 0) st_release(my_flag, FLAG_INCL);
+      tc::named_bar(1, NSCAN * 32);
+      const float hin_t = s_hin[j];
+      const float hin = hf == 0 ? hin_t : fmaf(A0, hin_t, B0);
 
       // y tile: registers -> smem [token][channel] -> TMA store (clipped at T).
-      if (store_thread) tc::tma_store_wait_read0();
-      tc::named_bar(1, 128);
 #pragma unroll
-      for (int tl = 0; tl < FUSED_C; ++tl)
-        *reinterpret_cast<bf16*>(s_y + tl * (FUSED_K * 2) + j * 2) =
-            __float2bfloat16_rn(fmaf(Ac[tl], hin, hl[tl]));
+      for (int tt = 0; tt < HALF; ++tt)
+        *reinterpret_cast<bf16*>(s_y + (tb + tt) * (FUSED_K * 2) + j * 2) =
+            __float2bfloat16_rn(fmaf(Ac[tt], hin, hl[tt]));
       tc::fence_proxy_async_smem();
-      tc::named_bar(1, 128);
+      tc::named_bar(1, NSCAN * 32);
       if (store_thread) {
         tc::tma_store_3d(&tm_y, s_y, blk * FUSED_K, c * FUSED_C, b);
         tc::tma_store_commit();
@@ -356,8 +349,21 @@ int ctas_per_block(const Dims& d) {
 
 }  // namespace
 
+int fused_ctas_per_block(const Dims& d) {
+  const int p = ctas_per_block(d);
+  return p * d.nblk <= FUSED_MAX_CTAS ? p : FUSED_MAX_CTAS / d.nblk;
+}
+
 bool fused_supported(const Dims& d) {
-  return d.io == RGLRU_BF16 && d.k == FUSED_K && ctas_per_block(d) >= 1;
+  return d.io == RGLRU_BF16 && d.k == FUSED_K && fused_ctas_per_block(d) >= 1;
+}
+
+// Prepares a scan layout for slot-based look-back: status word cleared, every slot empty.
+cudaError_t clear_slots(void* buf, const ScanLayout& L, cudaStream_t s) {
+  cudaError_t e = cudaMemsetAsync(buf, 0, 256, s);
+  if (e == cudaSuccess)
+    e = cudaMemsetAsync(static_cast<uint8_t*>(buf) + L.carry, 0xff, L.part - L.carry, s);
+  return e;
 }
 
 cudaError_t launch_fused_fwd(const Dims& d, const void* x, const void* Wa, const float* ba,
@@ -375,8 +381,7 @@ cudaError_t launch_fused_fwd(const Dims& d, const void* x, const void* Wa, const
   p.W = d.W;
   p.nblk = d.nblk;
   p.nC = fused_chunks(d);
-  p.ng = d.ng;
-  p.P = ctas_per_block(d);
+  p.P = fused_ctas_per_block(d);
   p.canonical = d.mode == RGLRU_CANONICAL;
   p.Lambda = Lambda;
   p.ba = ba;
@@ -392,7 +397,7 @@ cudaError_t launch_fused_fwd(const Dims& d, const void* x, const void* Wa, const
   e = cudaFuncSetAttribute(k_fused_fwd, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)SMEM_BYTES);
   if (e != cudaSuccess) return e;
-  e = cudaMemsetAsync(saved, 0, p.L.zero_bytes, s);
+  e = clear_slots(saved, p.L, s);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.P * d.nblk);

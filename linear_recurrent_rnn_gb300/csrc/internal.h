@@ -69,6 +69,23 @@ inline ScanLayout fused_layout(const Dims& d, bool backward) {
   return scan_layout_n(d.B, fused_chunks(d), d.ng, d.W, backward);
 }
 
+// Fused backward workspace: the reverse look-back scratch, then per-CTA partial sums (the
+// kernel runs at most FUSED_MAX_CTAS CTAs, each owning one gate block): dWa / dWx partials
+// [cta][2][k][k] and per-channel partials [cta][3][k] (dLambda before the sigmoid, dba, dbx).
+constexpr int FUSED_MAX_CTAS = 256;
+struct FusedBwdLayout {
+  ScanLayout L;
+  size_t dw_part, vec_part, total;
+};
+inline FusedBwdLayout fused_bwd_layout(const Dims& d) {
+  FusedBwdLayout F;
+  F.L = scan_layout_n(d.B, fused_chunks(d), d.ng, d.W, false);
+  F.dw_part = align_up(F.L.total, 256);
+  F.vec_part = align_up(F.dw_part + (size_t)FUSED_MAX_CTAS * 2 * FUSED_K * FUSED_K * 4, 256);
+  F.total = align_up(F.vec_part + (size_t)FUSED_MAX_CTAS * 2 * 3 * FUSED_K * 4, 256);
+  return F;
+}
+
 // Split-K layout of the SIMT projection-weight gradient.
 inline int dw_splits(const Dims& d) {
   const int tiles = ((d.k + 63) / 64) * ((d.k + 63) / 64) * d.nblk * 2;
@@ -162,6 +179,19 @@ cudaError_t launch_fused_fwd(const Dims& d, const void* x, const void* Wa, const
                              float* hT, void* saved, int spin_limit, int drop_tile,
                              cudaStream_t s);
 bool fused_supported(const Dims& d);
+int fused_ctas_per_block(const Dims& d);
+// Clears the status word of a scan layout and marks every carry / aggregate slot empty.
+cudaError_t clear_slots(void* buf, const ScanLayout& L, cudaStream_t s);
+
+// Fused backward on tensor cores (same coverage as the fused forward; `saved` must come from
+// launch_fused_fwd).  dx is written in shape.grad; dWa / dWx / dba / dbx / dLambda reduced
+// deterministically on device; dh0 may be null.
+cudaError_t launch_fused_bwd(const Dims& d, const void* dy, const float* dhT, const void* x,
+                             const void* Wa, const float* ba, const void* Wx, const float* bx,
+                             const float* Lambda, const uint8_t* rm, const int32_t* sp,
+                             const float* h0, const void* saved, void* dx, float* dWa,
+                             float* dba, float* dWx, float* dbx, float* dLambda, float* dh0,
+                             void* ws, int spin_limit, int drop_tile, cudaStream_t s);
 
 // SIMT projections (float32 accumulation).
 cudaError_t launch_gate_proj_simt(const Dims& d, int xt, int ot, const void* x, const void* Wa,
