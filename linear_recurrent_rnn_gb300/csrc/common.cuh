@@ -66,20 +66,43 @@ __device__ __forceinline__ float softplus_f(float z) {
 // 1 - a^2 for a = e^la, la <= 0, without the cancellation of 1 - a*a as a -> 1.
 __device__ __forceinline__ float one_minus_a2(float la) { return -expm1f(2.0f * la); }
 
-// The same quantity from la and a = e^la (already computed), cheaper: for 2 la > -1/4 the
-// Taylor series of -expm1 at 0 truncated after x^7 (remainder below |x|^8 / 8! <= 4e-10,
-// well under float rounding), otherwise 1 - a*a, whose cancellation costs at most a factor
-// 1/(1 - e^-1/4) < 4.6 of one rounding.
-__device__ __forceinline__ float one_minus_a2_fast(float la, float a) {
-  const float x = 2.0f * la;
-  float p = fmaf(x, 1.0f / 5040.0f, 1.0f / 720.0f);
-  p = fmaf(x, p, 1.0f / 120.0f);
-  p = fmaf(x, p, 1.0f / 24.0f);
-  p = fmaf(x, p, 1.0f / 6.0f);
-  p = fmaf(x, p, 0.5f);
-  p = fmaf(x, p, 1.0f);
-  const float series = -x * p;
-  return x > -0.25f ? series : fmaf(-a, a, 1.0f);
+// The decay a = e^la and 1 - a^2 for la <= 0, from one short series.  The decay is multiplied
+// over as many tokens as the memory is long (~1 / (1 - a), 10^4 for a = 0.9999), so a
+// systematic relative error e in a grows to ~e / (1 - a) in the long-range products: a must
+// be accurate to the rounding of a float, not just to a few ulp of an approximate exponential.
+// For la > -1/8: e1 = expm1(la) from its Taylor series at 0 cut after la^7 (remainder below
+// |la|^8 / 8! < 2e-12), a = 1 + e1, and 1 - a^2 = -e1 (e1 + 2) without cancellation.
+// Otherwise (a < 0.89, memory of a few tokens) a = 2^(la log2 e) and 1 - a^2 = 1 - a a.
+__device__ __forceinline__ void decay_fast(float la, float& a, float& om) {
+  float p = fmaf(la, 1.0f / 5040.0f, 1.0f / 720.0f);
+  p = fmaf(la, p, 1.0f / 120.0f);
+  p = fmaf(la, p, 1.0f / 24.0f);
+  p = fmaf(la, p, 1.0f / 6.0f);
+  p = fmaf(la, p, 0.5f);
+  p = fmaf(la, p, 1.0f);
+  const float e1 = la * p;
+  float ax;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(ax) : "f"(la * 1.4426950408889634f));
+  const bool near = la > -0.125f;
+  a = near ? 1.0f + e1 : ax;
+  om = near ? -e1 * (e1 + 2.0f) : fmaf(-ax, ax, 1.0f);
+}
+
+// Single special-function-unit operations (PTX ex2.approx / rcp.approx, flush-to-zero).
+constexpr float LOG2E = 1.4426950408889634f;
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ float rcp_approx(float x) {
+  float y;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+// sigmoid(z + bias) with nb = -bias * log2(e) precomputed: 1 / (1 + 2^(-(z + bias) log2 e)).
+__device__ __forceinline__ float sigmoid_nb(float z, float nb) {
+  return rcp_approx(1.0f + ex2_approx(fmaf(z, -LOG2E, nb)));
 }
 
 // sqrt(v) for v >= 0 as v * rsqrt(v) (one special-function op), 0 at v = 0.

@@ -130,15 +130,6 @@ __device__ __forceinline__ void store_dl8(uint8_t* hi_buf, uint8_t* lo_buf, int 
   *reinterpret_cast<uint4*>(lo_buf + at) = pack8(lo);
 }
 
-// m = sqrt(1 - a^2) and 1/m (abar = a off resets), or (1, 1) at a reset token, (0, 0) past
-// T; one special-function op.  1/m is 0 where m is 0 (a = 1 exactly).
-__device__ __forceinline__ float2 multiplier(float la, float abar, bool rst, bool ok) {
-  const float om = one_minus_a2_fast(la, abar);
-  const float rs = om > 0.0f ? rsqrtf(om) : 0.0f;
-  const float m = om * rs;
-  return !ok ? make_float2(0.0f, 0.0f) : (rst ? make_float2(1.0f, 1.0f) : make_float2(m, rs));
-}
-
 // 10 warps: three share one SM sub-partition's 16 K registers, so at most 168 per thread.
 template <typename GT>
 __global__ void __launch_bounds__(NTHREADS, 1)
@@ -301,9 +292,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const int w = blk * FUSED_K + j;
     const int tb = hf * HALF;
     const uint32_t tl_base = tmem + ((uint32_t)(q * 32) << 16);
-    const float nk = -8.0f * softplus_f(p.Lambda[w]);
-    const float bra = p.ba ? p.ba[w] : 0.0f;
-    const float bri = p.bx ? p.bx[w] : 0.0f;
+    const float nk = -8.0f * softplus_f(p.Lambda[w]);  // log a = nk * r
+    const float nbr = p.ba ? -p.ba[w] * LOG2E : 0.0f;   // bias folded into the exponent
+    const float nbi = p.bx ? -p.bx[w] * LOG2E : 0.0f;
     float* rcar = reinterpret_cast<float*>(p.scratch + p.F.L.carry);
     float2* agg = reinterpret_cast<float2*>(p.scratch + p.F.L.agg);
     const bool store_thread = (warp == 2 && lane == 0);
@@ -335,13 +326,15 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       }
       const int valid = min(FUSED_C, p.T - c * FUSED_C) - tb;
 
-      // Pass 1: gates of this half, its forward aggregate (fA, fB) and reverse aggregate
-      // (rP, rS).
-      float ab[HALF], rv[HALF], iv[HALF];
+      // Pass 1 (tokens ascending): the gates once.  abar and i stay in registers; m, 1/m and
+      // r are parked in this thread's TMEM columns (over its logits, already read, and its dx
+      // columns, free until pass 2 writes the direct dx term).  Also the half's forward
+      // aggregate (fA, fB) and reverse aggregate (rP, rS).
+      float ab[HALF], iv[HALF];
       float fA = 1.0f, fB = 0.0f, rP = 1.0f, rS = 0.0f;
 #pragma unroll
       for (int sub = 0; sub < HALF / 8; ++sub) {
-        float vr[8], vi[8];
+        float vr[8], vi[8], m8[8], s8[8];
         tc::tmem_ld8(tl_base + COL_LR + tb + sub * 8, vr);
         tc::tmem_ld8(tl_base + COL_LI + tb + sub * 8, vi);
         tc::tmem_ld_wait();
@@ -353,25 +346,29 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           const bool rst = ((rmask >> tt) & 1u) != 0u;
           const float xv = tile_elem(xj, xhalf, tl);
           const float dyv = ok ? tile_elem(dyj, xhalf, tl) : 0.0f;
-          const float r = sigmoid_f(vr[u] + bra);
-          const float i = sigmoid_f(vi[u] + bri);
-          const float la = nk * r;
-          const float a = __expf(la);
-          const float m0 = sqrt_fast(one_minus_a2_fast(la, a));
+          const float r = sigmoid_nb(vr[u], nbr);
+          const float i = sigmoid_nb(vi[u], nbi);
+          float a, om;
+          decay_fast(nk * r, a, om);
+          const float rs0 = om > 0.0f ? rsqrtf(om) : 0.0f;
           const float abar = !ok ? 1.0f : (rst ? 0.0f : a);
-          const float m = !ok ? 0.0f : (rst ? 1.0f : m0);
+          const float m = !ok ? 0.0f : (rst ? 1.0f : om * rs0);
+          const float rs = !ok ? 0.0f : (rst ? 1.0f : rs0);
           fB = fmaf(abar, fB, m * (i * xv));
           fA *= abar;
           rP *= abar;
           rS = fmaf(rP, dyv, rS);
           ab[tt] = abar;
-          rv[tt] = r;
           iv[tt] = i;
+          m8[u] = m;
+          s8[u] = rs;
+          vr[u] = r;
         }
+        tc::tmem_st8(tl_base + COL_LR + tb + sub * 8, m8);
+        tc::tmem_st8(tl_base + COL_LI + tb + sub * 8, s8);
+        tc::tmem_st8(tl_base + COL_DX + tb + sub * 8, vr);
       }
-      tc::tc_fence_before();
-      __syncwarp();
-      if (lane == 0) tc::mbar_arrive(lg_empty);  // logits consumed: next tile's may start
+      tc::tmem_st_wait();
 
       s_agg[hf * FUSED_K + j] = make_float4(fA, fB, rP, rS);
       if (store_thread) tc::tma_store_wait_read0();  // the dx staging is free again
@@ -409,25 +406,21 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       if (it > 0) ctl.wait(dl_empty, (it - 1) & 1);
       tc::tc_fence_after();
 
-      // Pass 2a: h_{t-1} through the half.
-      // h_{t-1} of the half is parked in the spare TMEM columns (registers are the limit).
+      // Pass 2a: h_{t-1} through the half, parked in TMEM.
       {
         float h = hq;
 #pragma unroll
-        for (int sub = 0; sub < HALF / 16; ++sub) {
-          float hp16[16];
+        for (int sub = 0; sub < HALF / 8; ++sub) {
+          float m8[8], hp8[8];
+          tc::tmem_ld8(tl_base + COL_LR + tb + sub * 8, m8);
+          tc::tmem_ld_wait();
 #pragma unroll
-          for (int u = 0; u < 16; ++u) {
-            const int tt = sub * 16 + u;
-            const int tl = tb + tt;
-            const bool ok = tt < valid;
-            const bool rst = ((rmask >> tt) & 1u) != 0u;
-            const float la = nk * rv[tt];
-            const float m = multiplier(la, ab[tt], rst, ok).x;
-            hp16[u] = h;
-            h = fmaf(ab[tt], h, m * (iv[tt] * tile_elem(xj, xhalf, tl)));
+          for (int u = 0; u < 8; ++u) {
+            const int tt = sub * 8 + u;
+            hp8[u] = h;
+            h = fmaf(ab[tt], h, m8[u] * (iv[tt] * tile_elem(xj, xhalf, tb + tt)));
           }
-          tc::tmem_st16(tl_base + COL_HP + tb + sub * 16, hp16);
+          tc::tmem_st8(tl_base + COL_HP + tb + sub * 8, hp8);
         }
         tc::tmem_st_wait();
       }
@@ -435,28 +428,27 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       float gnext = cin, abar_next = 1.0f;
 #pragma unroll
       for (int sub = HALF / 8 - 1; sub >= 0; --sub) {  // 8 tokens at a time (registers)
-        float o_r[8], o_i[8], o_x[8], hp16[8];
-        tc::tmem_ld8(tl_base + COL_HP + tb + sub * 8, hp16);
+        float m8[8], s8[8], r8[8], hp8[8], o_r[8], o_i[8];
+        tc::tmem_ld8(tl_base + COL_LR + tb + sub * 8, m8);
+        tc::tmem_ld8(tl_base + COL_LI + tb + sub * 8, s8);
+        tc::tmem_ld8(tl_base + COL_DX + tb + sub * 8, r8);
+        tc::tmem_ld8(tl_base + COL_HP + tb + sub * 8, hp8);
         tc::tmem_ld_wait();
 #pragma unroll
         for (int u = 7; u >= 0; --u) {
           const int tt = sub * 8 + u;
           const int tl = tb + tt;
-          const bool ok = tt < valid;
-          const bool rst = ((rmask >> tt) & 1u) != 0u;
-          const float r = rv[tt], i = iv[tt], abar = ab[tt];
-          const float la = nk * r;
-          const float2 mm = multiplier(la, abar, rst, ok);
-          const float m = mm.x;
-          const float dyv = ok ? tile_elem(dyj, xhalf, tl) : 0.0f;
+          const float r = r8[u], i = iv[tt], abar = ab[tt], m = m8[u];
+          const float dyv = tt < valid ? tile_elem(dyj, xhalf, tl) : 0.0f;
           const float uu = i * tile_elem(xj, xhalf, tl);
           const float gv = fmaf(abar_next, gnext, dyv);
           // zero at reset tokens (abar = 0) and past T (m = 0)
-          const float alpha = (abar == 0.0f || m == 0.0f) ? 0.0f : abar * (hp16[u] - uu * abar * mm.y);
+          const float alpha =
+              (abar == 0.0f || m == 0.0f) ? 0.0f : abar * (hp8[u] - uu * abar * s8[u]);
           const float dla = gv * alpha;
           o_r[u] = dla * nk * r * (1.0f - r);
           o_i[u] = gv * m * uu * (1.0f - i);
-          o_x[u] = gv * m * i;
+          m8[u] = gv * m * i;  // direct dx term
           dsp_acc = fmaf(dla, -8.0f * r, dsp_acc);
           dba_acc += o_r[u];
           dbx_acc += o_i[u];
@@ -466,13 +458,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const int tg = hf * (HALF / 16) + (sub >> 1);  // 16-token group of the dl buffers
         store_dl8(dl_rh, dl_rl, tg, sub & 1, j, o_r);
         store_dl8(dl_ih, dl_il, tg, sub & 1, j, o_i);
-        tc::tmem_st8(tl_base + COL_DX + tb + sub * 8, o_x);
+        tc::tmem_st8(tl_base + COL_DX + tb + sub * 8, m8);
       }
       tc::tmem_st_wait();
       tc::fence_proxy_async_smem();
       tc::tc_fence_before();
       __syncwarp();
       if (lane == 0) {
+        tc::mbar_arrive(lg_empty);  // the logits columns are free for the next tile
         tc::mbar_arrive(&in_empty[st]);
         tc::mbar_arrive(dl_full);
       }

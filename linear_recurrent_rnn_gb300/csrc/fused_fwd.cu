@@ -188,9 +188,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const int w = blk * FUSED_K + j;
     const int tb = hf * HALF;
     const uint32_t lane_base = (uint32_t)(q * 32) << 16;
-    const float nk = -8.0f * softplus_f(p.Lambda[w]);
-    const float bra = p.ba ? p.ba[w] : 0.0f;
-    const float bri = p.bx ? p.bx[w] : 0.0f;
+    const float nk = -8.0f * softplus_f(p.Lambda[w]);  // log a = nk * r
+    const float nbr = p.ba ? -p.ba[w] * LOG2E : 0.0f;   // bias folded into the exponent
+    const float nbi = p.bx ? -p.bx[w] * LOG2E : 0.0f;
     float* carry = reinterpret_cast<float*>(p.scratch + p.L.carry);
     float2* agg = reinterpret_cast<float2*>(p.scratch + p.L.agg);
     const bool store_thread = (warp == 2 && lane == 0);
@@ -233,11 +233,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           const int tl = tb + tt;       // token within the tile
           const float xv = __bfloat162float(*reinterpret_cast<const bf16*>(
               xs + tl * 32 + ((xhalf ^ ((tl >> 2) & 1)) << 4)));
-          const float r = sigmoid_f(vr[u] + bra);
-          const float i = sigmoid_f(vi[u] + bri);
-          const float la = nk * r;
-          float abar = __expf(la);
-          float m = sqrt_fast(one_minus_a2_fast(la, abar));
+          const float r = sigmoid_nb(vr[u], nbr);
+          const float i = sigmoid_nb(vi[u], nbi);
+          float abar, om;
+          decay_fast(nk * r, abar, om);
+          float m = sqrt_fast(om);
           if ((rmask >> tt) & 1u) {
             abar = 0.0f;
             m = 1.0f;

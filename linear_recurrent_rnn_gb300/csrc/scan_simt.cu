@@ -94,7 +94,7 @@ __global__ void __launch_bounds__(128) k_scan_fwd(ScanFwdArgs a) {
       const float r = sigmoid_f(rs[j]);
       const float i = sigmoid_f(is[j]);
       const float la = nk[j] * r;
-      float abar = __expf(la);
+      float abar = expf(la);
       float m = sqrtf(one_minus_a2(la));
       if (rst) {
         abar = 0.0f;
@@ -261,7 +261,7 @@ __global__ void __launch_bounds__(128) k_scan_bwd(ScanBwdArgs a) {
       const float r = sigmoid_f(rs[j]);
       const float i = sigmoid_f(is[j]);
       const float la = nk[j] * r;
-      float abar = __expf(la);
+      float abar = expf(la);
       float m = sqrtf(one_minus_a2(la));
       if (rst) {
         abar = 0.0f;

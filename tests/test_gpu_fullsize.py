@@ -1,0 +1,83 @@
+"""GPU parity at the full sizes of the five RG-LRU workloads, in the configuration the
+benchmark times (fused forward + backward, bf16 gradients for bf16 I/O), checked on sampled
+gate blocks.  Gate blocks are independent in every output (the projections are
+block-diagonal and the recurrence is per channel), so the oracle run on the channels of one
+block, over the whole batch and sequence, is that block's exact reference: y, hT, dx, dWa,
+dWx, dba, dbx, dLambda and dh0 of the sampled blocks are compared element by element."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from helpers import assert_close, dev, host, mode_id, shape_for
+from linear_recurrent_rnn_gb300 import build as B_
+from linear_recurrent_rnn_gb300 import librglru as R
+from linear_recurrent_rnn_gb300.inputs import WORKLOADS, as_f64, generate
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    B_.build()
+    R.lib()
+
+
+def _run(wl, inp, sh):
+    d = {k: dev(v) for k, v in inp.items()}
+    y = torch.empty_like(d["x"])
+    hT = torch.empty(wl.B, wl.W, device="cuda")
+    saved, ws = R.alloc_saved(sh), R.alloc_workspace(sh)
+    R.rglru_fused_forward(sh, d["x"], d["Wa"], d["ba"], d["Wx"], d["bx"], d["Lambda"],
+                          d["reset_mask"], d["segment_pos"], d["h0"], y, hT, saved)
+    out = {"y": y, "hT": hT}
+    out["dx"] = torch.empty(d["x"].shape, dtype=R.TORCH_DT[sh.grad], device="cuda")
+    out["dWa"] = torch.empty(wl.nblk, wl.k, wl.k, device="cuda")
+    out["dWx"] = torch.empty_like(out["dWa"])
+    for k in ("dba", "dbx", "dLambda"):
+        out[k] = torch.empty(wl.W, device="cuda")
+    out["dh0"] = torch.empty(wl.B, wl.W, device="cuda")
+    R.rglru_fused_backward(sh, d["dy"], d["dhT"], d["x"], d["Wa"], d["ba"], d["Wx"], d["bx"],
+                           d["Lambda"], d["reset_mask"], d["segment_pos"], d["h0"], saved,
+                           out["dx"], out["dWa"], out["dba"], out["dWx"], out["dbx"],
+                           out["dLambda"], out["dh0"], ws)
+    assert R.rglru_sync_status(saved) == R.OK
+    assert R.rglru_sync_status(ws) == R.OK
+    return out
+
+
+def _sl(t, blk, k):
+    return None if t is None else t[..., blk * k:(blk + 1) * k]
+
+
+@pytest.mark.parametrize("cfg", [1, 2, 3, 4, 5])
+def test_full_size_sampled_blocks(cfg):
+    wl = WORKLOADS[cfg]
+    inp = generate(wl, cfg)
+    sh = shape_for(wl)
+    got = _run(wl, inp, sh)
+    mode = mode_id(wl)
+    gst = "f32" if sh.grad == R.F32 else "bf16"
+    for blk in sorted({0, wl.nblk // 2, wl.nblk - 1}):
+        k = wl.k
+        cs = slice(blk * k, (blk + 1) * k)
+        o = {name: as_f64(_sl(inp[name], blk, k)) for name in ("x", "dy", "ba", "bx", "Lambda")}
+        Wa = as_f64(inp["Wa"][blk:blk + 1])
+        Wx = as_f64(inp["Wx"][blk:blk + 1])
+        h0 = as_f64(_sl(inp["h0"], blk, k))
+        dhT = as_f64(_sl(inp["dhT"], blk, k))
+        rm, sp = as_f64(inp["reset_mask"]), as_f64(inp["segment_pos"])
+        y, hT = oracle.fused_forward(mode, o["x"], Wa, o["ba"], Wx, o["bx"], o["Lambda"], rm, sp, h0)
+        g = oracle.fused_backward(mode, o["x"], Wa, o["ba"], Wx, o["bx"], o["Lambda"], o["dy"], dhT,
+                                  rm, sp, h0)
+        tag = f"cfg{cfg} blk{blk} "
+        assert_close(tag + "y", host(got["y"][..., cs]), y, io=wl.io, kind="out")
+        assert_close(tag + "hT", host(got["hT"][:, cs]), hT, io=wl.io, kind="out")
+        assert_close(tag + "dx", host(got["dx"][..., cs]), g["dx"], io=wl.io, kind="grad", stored=gst)
+        assert_close(tag + "dWa", host(got["dWa"][blk:blk + 1]), g["dWa"], io=wl.io, kind="grad")
+        assert_close(tag + "dWx", host(got["dWx"][blk:blk + 1]), g["dWx"], io=wl.io, kind="grad")
+        for name in ("dba", "dbx", "dLambda"):
+            assert_close(tag + name, host(got[name][cs]), g[name], io=wl.io, kind="grad")
+        assert_close(tag + "dh0", host(got["dh0"][:, cs]), g["dh0"], io=wl.io, kind="grad")
