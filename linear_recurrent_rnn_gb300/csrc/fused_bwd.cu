@@ -45,9 +45,12 @@ namespace rglru {
 
 namespace {
 
-constexpr int NSCAN = 8;
+constexpr int NPART = 4;             // token parts of a tile, one scan thread each per channel
+constexpr int PT = FUSED_C / NPART;  // tokens per scan thread
+constexpr int NSCAN = 4 * NPART;     // scan warps (4 lane quadrants per part)
 constexpr int NTHREADS = 64 + NSCAN * 32;
-constexpr int HALF = FUSED_C / 2;
+// 18 warps share the SM's four 16 K-register sub-partitions (five per sub-partition): <= 96.
+constexpr int MAXREG = 96;
 constexpr int STAGES = 2;
 constexpr uint32_t W_BYTES = FUSED_K * FUSED_K * 2;
 constexpr uint32_t T_BYTES = FUSED_C * FUSED_K * 2;  // one 64 x 128 bf16 tile
@@ -58,7 +61,7 @@ constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t COL_LR = 0, COL_LI = 64, COL_DX = 128, COL_HP = 192, COL_DWA = 256,
                    COL_DWX = 384;
 constexpr int WAIT_LIMIT = 1 << 22;
-constexpr uint32_t XCH_BYTES = 2 * FUSED_K * 16 + FUSED_K * 4;  // per-half aggregates + carry
+constexpr uint32_t XCH_BYTES = NPART * FUSED_K * 16 + FUSED_K * 4;  // part aggregates + carry
 // W (2) + x/dy stages (2 x 2) + dl buffers (4) + bf16 dx staging (1) tiles, exchange, barriers
 constexpr size_t SMEM_BYTES =
     2 * W_BYTES + STAGES * 2 * T_BYTES + 4 * T_BYTES + T_BYTES + XCH_BYTES + 256 + 1024;
@@ -130,9 +133,8 @@ __device__ __forceinline__ void store_dl8(uint8_t* hi_buf, uint8_t* lo_buf, int 
   *reinterpret_cast<uint4*>(lo_buf + at) = pack8(lo);
 }
 
-// 10 warps: three share one SM sub-partition's 16 K registers, so at most 168 per thread.
 template <typename GT>
-__global__ void __launch_bounds__(NTHREADS, 1)
+__global__ void __maxnreg__(MAXREG)
     k_fused_bwd(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_dy,
                 const __grid_constant__ CUtensorMap tm_wa, const __grid_constant__ CUtensorMap tm_wx,
                 const __grid_constant__ CUtensorMap tm_dx, BwdParams p) {
@@ -144,8 +146,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   uint8_t* s_in = smem + 2 * W_BYTES;               // stage s: x at s*2T, dy at s*2T + T
   uint8_t* s_dl = s_in + STAGES * 2 * T_BYTES;      // r_hi, r_lo, i_hi, i_lo
   uint8_t* s_dx = s_dl + 4 * T_BYTES;               // dx staging [token][channel]
-  float4* s_agg = reinterpret_cast<float4*>(s_dx + T_BYTES);  // [2][k]
-  float* s_cin = reinterpret_cast<float*>(s_agg + 2 * FUSED_K);                      // [k]
+  float4* s_agg = reinterpret_cast<float4*>(s_dx + T_BYTES);       // [part][k]
+  float* s_cin = reinterpret_cast<float*>(s_agg + NPART * FUSED_K);  // [k]
   uint64_t* bars = reinterpret_cast<uint64_t*>(s_cin + FUSED_K);
   uint64_t* w_full = bars;
   uint64_t* in_full = bars + 1;
@@ -286,11 +288,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     }
   } else {
     // ------------------------------------------------------------ scan warps
-    const int hf = (warp - 2) >> 2;
+    const int part = (warp - 2) >> 2;
     const int q = warp & 3;
     const int j = q * 32 + lane;
     const int w = blk * FUSED_K + j;
-    const int tb = hf * HALF;
+    const int tb = part * PT;
     const uint32_t tl_base = tmem + ((uint32_t)(q * 32) << 16);
     const float nk = -8.0f * softplus_f(p.Lambda[w]);  // log a = nk * r
     const float nbr = p.ba ? -p.ba[w] * LOG2E : 0.0f;   // bias folded into the exponent
@@ -321,19 +323,20 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       uint32_t rmask = 0;
       if (p.canonical) {
         const int t = c * FUSED_C + tb + lane;
-        rmask = __ballot_sync(0xffffffffu,
-                              t < p.T && is_reset(p.reset_mask, p.segment_pos, (size_t)b * p.T + t));
+        rmask = __ballot_sync(0xffffffffu, lane < PT && t < p.T &&
+                                               is_reset(p.reset_mask, p.segment_pos,
+                                                        (size_t)b * p.T + t));
       }
       const int valid = min(FUSED_C, p.T - c * FUSED_C) - tb;
 
       // Pass 1 (tokens ascending): the gates once.  abar and i stay in registers; m, 1/m and
       // r are parked in this thread's TMEM columns (over its logits, already read, and its dx
-      // columns, free until pass 2 writes the direct dx term).  Also the half's forward
+      // columns, free until pass 2 writes the direct dx term).  Also the part's forward
       // aggregate (fA, fB) and reverse aggregate (rP, rS).
-      float ab[HALF], iv[HALF];
+      float ab[PT], iv[PT];
       float fA = 1.0f, fB = 0.0f, rP = 1.0f, rS = 0.0f;
 #pragma unroll
-      for (int sub = 0; sub < HALF / 8; ++sub) {
+      for (int sub = 0; sub < PT / 8; ++sub) {
         float vr[8], vi[8], m8[8], s8[8];
         tc::tmem_ld8(tl_base + COL_LR + tb + sub * 8, vr);
         tc::tmem_ld8(tl_base + COL_LI + tb + sub * 8, vi);
@@ -370,47 +373,46 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       }
       tc::tmem_st_wait();
 
-      s_agg[hf * FUSED_K + j] = make_float4(fA, fB, rP, rS);
+      s_agg[part * FUSED_K + j] = make_float4(fA, fB, rP, rS);
       if (store_thread) tc::tma_store_wait_read0();  // the dx staging is free again
       tc::named_bar(1, NSCAN * 32);
-      const float4 o = s_agg[(1 - hf) * FUSED_K + j];  // the other half's aggregates
-
-      // Half 0 owns the chunk's reverse carry: tile aggregate = half 0 o half 1.
-      if (hf == 0) {
-        const float tP = rP * o.z, tS = fmaf(rP, o.w, rS);
-        const size_t cidx = (size_t)b * p.nC + c;
-        const bool publish = (blk * ntiles + n) != p.drop_tile;
-        const bool anchor = ((p.nC - 1 - c) % ANCHOR) == 0;
-        float cin = 0.0f;
-        if (c == p.nC - 1) {
-          if (p.dhT) cin = p.dhT[(size_t)b * p.W + w];
-        } else {
-          if (!anchor && publish) slot_put2(agg + cidx * p.W + w, tP, tS);
-          // nearest anchor after this chunk (anchors counted from the last chunk)
-          const int an = p.nC - 1 - ((p.nC - 2 - c) / ANCHOR) * ANCHOR;
-          cin = lookback_carry(agg + (cidx + 1) * p.W + w, (long)p.W, an - c - 1,
-                               rcar + ((size_t)b * p.nC + an) * p.W + w, p.spin_limit, status);
+      // Entry-state map of this part (earlier parts composed) and carry map from the tile's
+      // right edge to this part (later parts composed).
+      float Fa = 1.0f, Fb = 0.0f, Rp = 1.0f, Rs = 0.0f;
+#pragma unroll
+      for (int pp = 0; pp < NPART; ++pp) {
+        if (pp < part) {
+          const float4 g = s_agg[pp * FUSED_K + j];
+          Fb = fmaf(g.x, Fb, g.y);
+          Fa *= g.x;
         }
-        const float cout = fmaf(tP, cin, tS);
-        if (publish) slot_put1(rcar + cidx * p.W + w, cout);
-        if (c == 0 && p.dh0) p.dh0[(size_t)b * p.W + w] = p.canonical ? cout : 0.0f;
-        s_cin[j] = cin;
       }
-      tc::named_bar(1, NSCAN * 32);
-      const float cin_t = s_cin[j];
-      // carry into this half from the right, state entering it from the left
-      const float cin = hf == 1 ? cin_t : fmaf(o.z, cin_t, o.w);
-      const float hq = hf == 0 ? hin_tile : fmaf(o.x, hin_tile, o.y);
+#pragma unroll
+      for (int pp = NPART - 1; pp > 0; --pp) {
+        if (pp > part) {
+          const float4 g = s_agg[pp * FUSED_K + j];
+          Rs = fmaf(g.z, Rs, g.w);
+          Rp *= g.z;
+        }
+      }
+
+      // Part 0 owns the chunk's reverse carry: its map after the later parts' is the tile's,
+      // published at once; the look-back itself waits until pass 2a is done.
+      const size_t cidx = (size_t)b * p.nC + c;
+      const bool publish = (blk * ntiles + n) != p.drop_tile;
+      const float tP = rP * Rp, tS = fmaf(rP, Rs, rS);
+      if (part == 0 && c < p.nC - 1 && ((p.nC - 1 - c) % ANCHOR) != 0 && publish)
+        slot_put2(agg + cidx * p.W + w, tP, tS);
 
       // The dl buffers and the dx accumulator are free once the previous tile's MMAs are done.
       if (it > 0) ctl.wait(dl_empty, (it - 1) & 1);
       tc::tc_fence_after();
 
-      // Pass 2a: h_{t-1} through the half, parked in TMEM.
+      // Pass 2a: h_{t-1} through the part, parked in TMEM.
       {
-        float h = hq;
+        float h = fmaf(Fa, hin_tile, Fb);  // state entering this part
 #pragma unroll
-        for (int sub = 0; sub < HALF / 8; ++sub) {
+        for (int sub = 0; sub < PT / 8; ++sub) {
           float m8[8], hp8[8];
           tc::tmem_ld8(tl_base + COL_LR + tb + sub * 8, m8);
           tc::tmem_ld_wait();
@@ -424,10 +426,29 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
         tc::tmem_st_wait();
       }
+
+      if (part == 0) {
+        float cin = 0.0f;
+        if (c == p.nC - 1) {
+          if (p.dhT) cin = p.dhT[(size_t)b * p.W + w];
+        } else {
+          // nearest anchor after this chunk (anchors counted from the last chunk)
+          const int an = p.nC - 1 - ((p.nC - 2 - c) / ANCHOR) * ANCHOR;
+          cin = lookback_carry(agg + (cidx + 1) * p.W + w, (long)p.W, an - c - 1,
+                               rcar + ((size_t)b * p.nC + an) * p.W + w, p.spin_limit, status);
+        }
+        const float cout = fmaf(tP, cin, tS);
+        if (publish) slot_put1(rcar + cidx * p.W + w, cout);
+        if (c == 0 && p.dh0) p.dh0[(size_t)b * p.W + w] = p.canonical ? cout : 0.0f;
+        s_cin[j] = cin;
+      }
+      tc::named_bar(1, NSCAN * 32);
+      const float cin = fmaf(Rp, s_cin[j], Rs);  // carry into this part from the right
+
       // Pass 2b: g exactly, tokens descending, and the pointwise gradients.
       float gnext = cin, abar_next = 1.0f;
 #pragma unroll
-      for (int sub = HALF / 8 - 1; sub >= 0; --sub) {  // 8 tokens at a time (registers)
+      for (int sub = PT / 8 - 1; sub >= 0; --sub) {  // 8 tokens at a time (registers)
         float m8[8], s8[8], r8[8], hp8[8], o_r[8], o_i[8];
         tc::tmem_ld8(tl_base + COL_LR + tb + sub * 8, m8);
         tc::tmem_ld8(tl_base + COL_LI + tb + sub * 8, s8);
@@ -455,9 +476,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           gnext = gv;
           abar_next = abar;
         }
-        const int tg = hf * (HALF / 16) + (sub >> 1);  // 16-token group of the dl buffers
-        store_dl8(dl_rh, dl_rl, tg, sub & 1, j, o_r);
-        store_dl8(dl_ih, dl_il, tg, sub & 1, j, o_i);
+        const int t8 = (tb >> 3) + sub;  // 8-token group: 16-token group t8/2, half t8%2
+        store_dl8(dl_rh, dl_rl, t8 >> 1, t8 & 1, j, o_r);
+        store_dl8(dl_ih, dl_il, t8 >> 1, t8 & 1, j, o_i);
         tc::tmem_st8(tl_base + COL_DX + tb + sub * 8, m8);
       }
       tc::tmem_st_wait();
@@ -474,7 +495,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       ctl.wait(dx_full, it & 1);
       tc::tc_fence_after();
 #pragma unroll
-      for (int sub = 0; sub < HALF / 16; ++sub) {
+      for (int sub = 0; sub < PT / 16; ++sub) {
         float v[16];
         tc::tmem_ld16(tl_base + COL_DX + tb + sub * 16, v);
         tc::tmem_ld_wait();
@@ -499,15 +520,15 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     }
     if (store_thread) tc::tma_store_wait0();
 
-    // Per-CTA, per-half partials of the per-channel sums.
+    // Per-CTA, per-part partials of the per-channel sums.
     float* vp = reinterpret_cast<float*>(p.scratch + p.F.vec_part) +
-                ((size_t)blockIdx.x * 2 + hf) * 3 * FUSED_K;
+                ((size_t)blockIdx.x * NPART + part) * 3 * FUSED_K;
     vp[j] = dsp_acc;
     vp[FUSED_K + j] = dba_acc;
     vp[2 * FUSED_K + j] = dbx_acc;
 
-    // Per-CTA dW partials: lane j of the accumulators is input channel j; each half copies
-    // 64 of the 128 output-channel columns.
+    // Per-CTA dW partials: lane j of the accumulators is input channel j; each part copies
+    // 128 / NPART of the output-channel columns.
     if (my_tiles > 0) ctl.wait(dl_empty, (my_tiles - 1) & 1);
     tc::tc_fence_after();
     float* dwp = reinterpret_cast<float*>(p.scratch + p.F.dw_part) +
@@ -515,8 +536,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 #pragma unroll
     for (int mtx = 0; mtx < 2; ++mtx) {
 #pragma unroll
-      for (int sub = 0; sub < FUSED_K / 32; ++sub) {
-        const int col = hf * (FUSED_K / 2) + sub * 16;
+      for (int sub = 0; sub < FUSED_K / NPART / 16; ++sub) {
+        const int col = part * (FUSED_K / NPART) + sub * 16;
         float v[16];
         if (my_tiles > 0) {
           tc::tmem_ld16(tl_base + (mtx ? COL_DWX : COL_DWA) + col, v);
@@ -560,8 +581,8 @@ __global__ void k_fused_bwd_reduce(const float* dw_part, const float* vec_part, 
   if (blockIdx.x == 0 && threadIdx.x < FUSED_K) {
     const int j = threadIdx.x, w = blk * FUSED_K + j;
     float s0 = 0.0f, s1 = 0.0f, s2 = 0.0f;
-    for (int r = 0; r < 2 * P; ++r) {
-      const float* src = vec_part + ((size_t)blk * P * 2 + r) * 3 * FUSED_K;
+    for (int r = 0; r < NPART * P; ++r) {
+      const float* src = vec_part + ((size_t)blk * P * NPART + r) * 3 * FUSED_K;
       s0 += src[j];
       s1 += src[FUSED_K + j];
       s2 += src[2 * FUSED_K + j];

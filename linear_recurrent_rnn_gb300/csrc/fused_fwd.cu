@@ -13,15 +13,15 @@
 // Tile = (batch row b, gate block blk, 64 tokens).  For the tile the MMA computes the
 // transposed logits  lr^T[128 ch x 64 tok] = Wa[blk]^T (MN-major A, from W stored (in, out))
 // x x_tile^T (K-major B, the x tile as TMA lands it), and li^T likewise, so TMEM lane =
-// channel and column = token.  Two scan threads own each channel, one per 32-token half: each
-// runs its half serially in registers from a zero state, the halves are joined through shared
-// memory, and chunks through the anchored look-back over value slots in `saved`
+// channel and column = token.  Four scan threads own each channel, one per 16-token part:
+// each runs its part serially in registers from a zero state, the parts are joined through
+// shared memory, and chunks through the anchored look-back over value slots in `saved`
 // (lookback.cuh), which keeps the result bitwise deterministic.
 //
-// Roles (320 threads, one CTA per SM, launched cooperatively so that all CTAs are resident):
-//   warp 0      TMA producer: Wa[blk], Wx[blk] once, then the x tile ring (3 stages)
-//   warp 1      MMA issuer: 2 x 8 tcgen05.mma (K = 16 each) per tile into a 2-deep TMEM ring
-//   warps 2..9  scan: warps 2-5 tokens 0-31, warps 6-9 tokens 32-63 (lane quadrant warp % 4)
+// Roles (576 threads, one CTA per SM, launched cooperatively so that all CTAs are resident):
+//   warp 0       TMA producer: Wa[blk], Wx[blk] once, then the x tile ring (3 stages)
+//   warp 1       MMA issuer: 2 x 8 tcgen05.mma (K = 16 each) per tile into a 2-deep TMEM ring
+//   warps 2..17  scan: warps 2+4p .. 5+4p take tokens 16p .. 16p+15 (lane quadrant warp % 4)
 // CTA (blk, r) of the P CTAs serving gate block blk takes the block's tiles n = r, r + P, ...
 // in chunk-major order, so every tile it waits on is earlier in the same order.
 #include <cudaTypedefs.h>
@@ -35,18 +35,24 @@ namespace rglru {
 
 namespace {
 
-constexpr int NSCAN = 8;
+constexpr int NPART = 4;              // token parts of a tile, one scan thread each per channel
+constexpr int PT = FUSED_C / NPART;   // tokens per scan thread
+constexpr int NSCAN = 4 * NPART;      // scan warps (4 lane quadrants per part)
 constexpr int NTHREADS = 64 + NSCAN * 32;
-constexpr int HALF = FUSED_C / 2;
+// 18 warps share the SM's four 16 K-register sub-partitions (five per sub-partition): <= 96.
+constexpr int MAXREG = 96;
 constexpr int XSTAGES = 3;
 constexpr uint32_t W_BYTES = FUSED_K * FUSED_K * 2;  // one weight block, bf16
 constexpr uint32_t X_BYTES = FUSED_C * FUSED_K * 2;  // one x tile, bf16
 constexpr uint32_t Y_BYTES = FUSED_C * FUSED_K * 2;  // one y tile, bf16
 constexpr uint32_t SLAB_X = FUSED_C * 32;            // 16 channels x 64 tokens
 constexpr uint32_t SLAB_W = FUSED_K * 32;            // 16 out-channels x 128 in-rows
-constexpr uint32_t TMEM_COLS = 256;                  // 2 buffers x (lr 64 + li 64) columns
+// 2 logits buffers x (lr 64 + li 64) columns, then 2 x 128 columns where each scan thread
+// parks its part's local states (16) and decay products (16) until the tile is finished.
+constexpr uint32_t TMEM_COLS = 512;
+constexpr uint32_t PARK_COL = 256;
 constexpr int WAIT_LIMIT = 1 << 22;
-constexpr uint32_t XCH_BYTES = FUSED_K * 8 + FUSED_K * 4;  // half-0 aggregates + tile carry
+constexpr uint32_t XCH_BYTES = 2 * NPART * FUSED_K * 8;  // part maps of two tiles
 constexpr size_t SMEM_BYTES =
     2 * W_BYTES + XSTAGES * X_BYTES + Y_BYTES + XCH_BYTES + 256 + 1024;
 constexpr uint32_t STATUS_PIPE = 2u;
@@ -79,7 +85,55 @@ struct Ctl {
   }
 };
 
-__global__ void __launch_bounds__(NTHREADS, 1)
+// Local scan of one scan thread's PT tokens from a zero state: hl = state after each token,
+// Ac = product of abar up to it, (rA, rh) = the part's map.  GENERAL handles resets, tokens
+// past T and decays with la <= -1/8; the fast variant (chosen warp-uniformly) has none.
+template <bool GENERAL>
+__device__ __forceinline__ void local_scan(uint32_t t_lr, uint32_t t_li, const uint8_t* xs,
+                                           int tb, int xoff0, int xoff1, float nk, float nbr,
+                                           float nbi, uint32_t rmask, int valid, float (&hl)[PT],
+                                           float (&Ac)[PT], float& rh, float& rA) {
+  rh = 0.0f;
+  rA = 1.0f;
+#pragma unroll
+  for (int sub = 0; sub < PT / 16; ++sub) {
+    float vr[16], vi[16];
+    tc::tmem_ld16(t_lr + sub * 16, vr);
+    tc::tmem_ld16(t_li + sub * 16, vi);
+    tc::tmem_ld_wait();
+#pragma unroll
+    for (int u = 0; u < 16; ++u) {
+      const int tt = sub * 16 + u;  // token within the part
+      const int tl = tb + tt;       // token within the tile
+      const float xv = __bfloat162float(*reinterpret_cast<const bf16*>(
+          xs + tl * 32 + (((tl >> 2) & 1) ? xoff1 : xoff0)));
+      const float r = sigmoid_nb(vr[u], nbr);
+      const float i = sigmoid_nb(vi[u], nbi);
+      float abar, om;
+      if (GENERAL)
+        decay_fast(nk * r, abar, om);
+      else
+        decay_near(nk * r, abar, om);
+      float m = sqrt_fast(om);
+      if (GENERAL) {
+        if ((rmask >> tt) & 1u) {
+          abar = 0.0f;
+          m = 1.0f;
+        }
+        if (tt >= valid) {
+          abar = 1.0f;
+          m = 0.0f;
+        }
+      }
+      rh = fmaf(abar, rh, m * (i * xv));
+      rA *= abar;
+      hl[tt] = rh;
+      Ac[tt] = rA;
+    }
+  }
+}
+
+__global__ void __maxnreg__(MAXREG)
     k_fused_fwd(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_wa,
                 const __grid_constant__ CUtensorMap tm_wx, const __grid_constant__ CUtensorMap tm_y,
                 FwdParams p) {
@@ -90,9 +144,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   uint8_t* s_wx = smem + W_BYTES;
   uint8_t* s_x = smem + 2 * W_BYTES;
   uint8_t* s_y = s_x + XSTAGES * X_BYTES;
-  float2* s_agg0 = reinterpret_cast<float2*>(s_y + Y_BYTES);  // half-0 aggregate per channel
-  float* s_hin = reinterpret_cast<float*>(s_agg0 + FUSED_K);  // carry into the tile
-  uint64_t* bars = reinterpret_cast<uint64_t*>(s_hin + FUSED_K);
+  float2* s_agg = reinterpret_cast<float2*>(s_y + Y_BYTES);  // [tile parity][part][channel]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(s_agg + 2 * NPART * FUSED_K);
   uint64_t* w_full = bars;
   uint64_t* x_full = bars + 1;
   uint64_t* x_empty = bars + 1 + XSTAGES;
@@ -182,11 +235,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     }
   } else {
     // ------------------------------------------------------------ scan warps
-    const int hf = (warp - 2) >> 2;  // token half of the tile
-    const int q = warp & 3;          // TMEM lane quadrant this warp may access
+    const int part = (warp - 2) >> 2;  // token part of the tile
+    const int q = warp & 3;            // TMEM lane quadrant this warp may access
     const int j = q * 32 + lane;
     const int w = blk * FUSED_K + j;
-    const int tb = hf * HALF;
+    const int tb = part * PT;
     const uint32_t lane_base = (uint32_t)(q * 32) << 16;
     const float nk = -8.0f * softplus_f(p.Lambda[w]);  // log a = nk * r
     const float nbr = p.ba ? -p.ba[w] * LOG2E : 0.0f;   // bias folded into the exponent
@@ -195,114 +248,144 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     float2* agg = reinterpret_cast<float2*>(p.scratch + p.L.agg);
     const bool store_thread = (warp == 2 && lane == 0);
     if (store_thread) tc::prefetch_tmap(&tm_y);
-    const int xhalf = (j & 15) >> 3;
+    // x[token tl, channel j] of a stage: 16-byte halves of the 32-byte row swap on rows 4..7
+    // of every 8 (32-byte swizzle), so two base pointers cover both row parities.
+    const int xoff0 = (j >> 4) * SLAB_X + (j & 7) * 2 + (((j & 15) >> 3) << 4);
+    const int xoff1 = (j >> 4) * SLAB_X + (j & 7) * 2 + ((((j & 15) >> 3) ^ 1) << 4);
+    int my_tiles = 0;
+    for (int n = rr; n < ntiles; n += p.P) ++my_tiles;
 
-    int it = 0;
-    for (int n = rr; n < ntiles; n += p.P, ++it) {
-      const int c = n / p.B, b = n % p.B;
-      const int st = it % XSTAGES;
-      const uint32_t ph = (it / XSTAGES) & 1;
-      const int a = it & 1;
-      const uint32_t aph = (it >> 1) & 1;
-      ctl.wait(&acc_full[a], aph);
-      ctl.wait(&x_full[st], ph);
-      tc::tc_fence_after();
+    // Software pipeline: iteration `it` runs the local scan of tile it (results parked in
+    // TMEM) and then finishes tile it-1, whose look-back slots have had a whole tile's time
+    // to fill.
+    // Warp-uniform: every channel of this warp has la > -1/8 on every token.
+    const bool near_all = __all_sync(0xffffffffu, nk > -0.125f);
 
-      uint32_t rmask = 0;
-      if (p.canonical) {
-        const int t = c * FUSED_C + tb + lane;
-        rmask = __ballot_sync(0xffffffffu,
-                              t < p.T && is_reset(p.reset_mask, p.segment_pos, (size_t)b * p.T + t));
-      }
-      const int valid = min(FUSED_C, p.T - c * FUSED_C) - tb;  // tokens of this half < T
-      const uint8_t* xs = s_x + st * X_BYTES + (j >> 4) * SLAB_X + (j & 7) * 2;
-
-      // Local scan of this half from a zero state: hl = state after each token, Ac = product
-      // of abar up to it.
-      float hl[HALF], Ac[HALF];
-      float rh = 0.0f, rA = 1.0f;
-#pragma unroll
-      for (int sub = 0; sub < HALF / 16; ++sub) {
-        float vr[16], vi[16];
-        tc::tmem_ld16(tmem + lane_base + a * 128 + tb + sub * 16, vr);
-        tc::tmem_ld16(tmem + lane_base + a * 128 + 64 + tb + sub * 16, vi);
-        tc::tmem_ld_wait();
-#pragma unroll
-        for (int u = 0; u < 16; ++u) {
-          const int tt = sub * 16 + u;  // token within the half
-          const int tl = tb + tt;       // token within the tile
-          const float xv = __bfloat162float(*reinterpret_cast<const bf16*>(
-              xs + tl * 32 + ((xhalf ^ ((tl >> 2) & 1)) << 4)));
-          const float r = sigmoid_nb(vr[u], nbr);
-          const float i = sigmoid_nb(vi[u], nbi);
-          float abar, om;
-          decay_fast(nk * r, abar, om);
-          float m = sqrt_fast(om);
-          if ((rmask >> tt) & 1u) {
-            abar = 0.0f;
-            m = 1.0f;
-          }
-          if (tt >= valid) {
-            abar = 1.0f;
-            m = 0.0f;
-          }
-          rh = fmaf(abar, rh, m * (i * xv));
-          rA *= abar;
-          hl[tt] = rh;
-          Ac[tt] = rA;
+    for (int it = 0; it <= my_tiles; ++it) {
+      // Request tile it-1's look-back slots now; they are consumed after this tile's scan.
+      LookbackReq lbq;
+      int lb_n = 0;
+      const float2* lb_agg = agg;
+      const float* lb_anchor = carry;
+      if (it > 0) {
+        const int n = rr + (it - 1) * p.P;
+        const int c = n / p.B, b = n % p.B;
+        if (c > 0) {
+          const size_t cidx = (size_t)b * p.nC + c;
+          const int an = ((c - 1) / ANCHOR) * ANCHOR;  // nearest anchor before this chunk
+          lb_n = c - 1 - an;
+          lb_agg = agg + (cidx - 1) * p.W + w;
+          lb_anchor = carry + ((size_t)b * (p.nC + 1) + an + 1) * p.W + w;
+          lookback_issue(lbq, lb_agg, -(long)p.W, lb_n, lb_anchor);
         }
       }
-      tc::tc_fence_before();
-      __syncwarp();
-      if (lane == 0) {
-        tc::mbar_arrive(&acc_empty[a]);
-        tc::mbar_arrive(&x_empty[st]);
-      }
+      if (it < my_tiles) {
+        const int n = rr + it * p.P;
+        const int c = n / p.B, b = n % p.B;
+        const int st = it % XSTAGES;
+        const uint32_t ph = (it / XSTAGES) & 1;
+        const int a = it & 1;
+        const uint32_t aph = (it >> 1) & 1;
+        ctl.wait(&acc_full[a], aph);
+        ctl.wait(&x_full[st], ph);
+        tc::tc_fence_after();
 
-      if (hf == 0) s_agg0[j] = make_float2(rA, rh);
+        uint32_t rmask = 0;
+        if (p.canonical) {
+          const int t = c * FUSED_C + tb + lane;
+          rmask = __ballot_sync(0xffffffffu, lane < PT && t < p.T &&
+                                                 is_reset(p.reset_mask, p.segment_pos,
+                                                          (size_t)b * p.T + t));
+        }
+        const int valid = min(FUSED_C, p.T - c * FUSED_C) - tb;  // tokens of this part < T
+        const uint8_t* xs = s_x + st * X_BYTES;
+        const uint32_t t_lr = tmem + lane_base + a * 128 + tb;
+        float hl[PT], Ac[PT], rh, rA;
+        if (near_all && rmask == 0u && valid >= PT)
+          local_scan<false>(t_lr, t_lr + 64, xs, tb, xoff0, xoff1, nk, nbr, nbi, rmask, valid,
+                            hl, Ac, rh, rA);
+        else
+          local_scan<true>(t_lr, t_lr + 64, xs, tb, xoff0, xoff1, nk, nbr, nbi, rmask, valid,
+                           hl, Ac, rh, rA);
+        const uint32_t park = tmem + lane_base + PARK_COL + a * 128 + part * 2 * PT;
+        tc::tmem_st16(park, hl);
+        tc::tmem_st16(park + PT, Ac);
+        tc::tmem_st_wait();
+        tc::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          tc::mbar_arrive(&acc_empty[a]);
+          tc::mbar_arrive(&x_empty[st]);
+        }
+        s_agg[(a * NPART + part) * FUSED_K + j] = make_float2(rA, rh);
+      }
       if (store_thread) tc::tma_store_wait_read0();  // the y staging is free again
       tc::named_bar(1, NSCAN * 32);
 
-      // Half 1 owns the chunk: its aggregate composed with half 0's is the tile's.
-      float A0 = 1.0f, B0 = 0.0f;
-      if (hf == 1) {
-        const float2 h0agg = s_agg0[j];
-        A0 = h0agg.x;
-        B0 = h0agg.y;
-        const float At = rA * A0, Bt = fmaf(rA, B0, rh);
-        const size_t cidx = (size_t)b * p.nC + c;
-        const bool publish = (blk * ntiles + n) != p.drop_tile;
-        const bool anchor = (c % ANCHOR) == 0;
-        float hin = 0.0f;
-        if (c == 0) {
-          if (p.canonical && p.h0) hin = p.h0[(size_t)b * p.W + w];
-        } else {
-          if (!anchor && publish) slot_put2(agg + cidx * p.W + w, At, Bt);
-          const int an = ((c - 1) / ANCHOR) * ANCHOR;  // nearest anchor before this chunk
-          hin = lookback_carry(agg + (cidx - 1) * p.W + w, -(long)p.W, c - 1 - an,
-                               carry + ((size_t)b * (p.nC + 1) + an + 1) * p.W + w,
-                               p.spin_limit, status);
+      // Publish tile it's map at once (the last part, from all parts' maps).
+      if (it < my_tiles && part == NPART - 1) {
+        const int n = rr + it * p.P;
+        const int c = n / p.B, b = n % p.B;
+        const int a = it & 1;
+        if (c > 0 && (c % ANCHOR) != 0 && (blk * ntiles + n) != p.drop_tile) {
+          float At = 1.0f, Bt = 0.0f;
+#pragma unroll
+          for (int pp = 0; pp < NPART; ++pp) {
+            const float2 g = s_agg[(a * NPART + pp) * FUSED_K + j];
+            Bt = fmaf(g.x, Bt, g.y);
+            At *= g.x;
+          }
+          slot_put2(agg + ((size_t)b * p.nC + c) * p.W + w, At, Bt);
         }
-        const float hend = fmaf(At, hin, Bt);
-        float* crow = carry + (size_t)b * (p.nC + 1) * p.W;
-        if (publish) slot_put1(crow + (size_t)(c + 1) * p.W + w, hend);
-        if (c == 0) slot_put1(crow + w, hin);
-        if (c == p.nC - 1 && p.hT) p.hT[(size_t)b * p.W + w] = hend;
-        s_hin[j] = hin;
+      }
+
+      // Finish tile it-1: every part derives the tile's carry itself (no barrier between the
+      // look-back and the output), the last part publishes the chunk-boundary state.
+      if (it > 0) {
+        const int n = rr + (it - 1) * p.P;
+        const int c = n / p.B, b = n % p.B;
+        const int a = (it - 1) & 1;
+        float Ae = 1.0f, Be = 0.0f, At = 1.0f, Bt = 0.0f;
+#pragma unroll
+        for (int pp = 0; pp < NPART; ++pp) {
+          const float2 g = s_agg[(a * NPART + pp) * FUSED_K + j];
+          if (pp < part) {
+            Be = fmaf(g.x, Be, g.y);
+            Ae *= g.x;
+          }
+          Bt = fmaf(g.x, Bt, g.y);
+          At *= g.x;
+        }
+        float hin_t = 0.0f;
+        if (c == 0) {
+          if (p.canonical && p.h0) hin_t = p.h0[(size_t)b * p.W + w];
+        } else {
+          hin_t = lookback_finish(lbq, lb_agg, -(long)p.W, lb_n, lb_anchor, p.spin_limit, status);
+        }
+        if (part == NPART - 1) {
+          const float hend = fmaf(At, hin_t, Bt);
+          float* crow = carry + (size_t)b * (p.nC + 1) * p.W;
+          if ((blk * ntiles + n) != p.drop_tile) slot_put1(crow + (size_t)(c + 1) * p.W + w, hend);
+          if (c == 0) slot_put1(crow + w, hin_t);
+          if (c == p.nC - 1 && p.hT) p.hT[(size_t)b * p.W + w] = hend;
+        }
+        const float hin = fmaf(Ae, hin_t, Be);
+        float hl[PT], Ac[PT];
+        const uint32_t park = tmem + lane_base + PARK_COL + a * 128 + part * 2 * PT;
+        tc::tmem_ld16(park, hl);
+        tc::tmem_ld16(park + PT, Ac);
+        tc::tmem_ld_wait();
+        // y tile: registers -> smem [token][channel] -> TMA store (clipped at T).
+#pragma unroll
+        for (int tt = 0; tt < PT; ++tt)
+          *reinterpret_cast<bf16*>(s_y + (tb + tt) * (FUSED_K * 2) + j * 2) =
+              __float2bfloat16_rn(fmaf(Ac[tt], hin, hl[tt]));
+        tc::fence_proxy_async_smem();
       }
       tc::named_bar(1, NSCAN * 32);
-      const float hin_t = s_hin[j];
-      const float hin = hf == 0 ? hin_t : fmaf(A0, hin_t, B0);
-
-      // y tile: registers -> smem [token][channel] -> TMA store (clipped at T).
-#pragma unroll
-      for (int tt = 0; tt < HALF; ++tt)
-        *reinterpret_cast<bf16*>(s_y + (tb + tt) * (FUSED_K * 2) + j * 2) =
-            __float2bfloat16_rn(fmaf(Ac[tt], hin, hl[tt]));
-      tc::fence_proxy_async_smem();
-      tc::named_bar(1, NSCAN * 32);
-      if (store_thread) {
-        tc::tma_store_3d(&tm_y, s_y, blk * FUSED_K, c * FUSED_C, b);
+      if (it > 0 && store_thread) {
+        const int n = rr + (it - 1) * p.P;
+        tc::tma_store_3d(&tm_y, s_y, blk * FUSED_K, (n / p.B) * FUSED_C, n % p.B);
         tc::tma_store_commit();
       }
     }

@@ -71,7 +71,8 @@ inline ScanLayout fused_layout(const Dims& d, bool backward) {
 
 // Fused backward workspace: the reverse look-back scratch, then per-CTA partial sums (the
 // kernel runs at most FUSED_MAX_CTAS CTAs, each owning one gate block): dWa / dWx partials
-// [cta][2][k][k] and per-channel partials [cta][3][k] (dLambda before the sigmoid, dba, dbx).
+// [cta][2][k][k] and per-channel partials [cta][part (4)][3][k] (dLambda before the sigmoid,
+// dba, dbx).
 constexpr int FUSED_MAX_CTAS = 256;
 struct FusedBwdLayout {
   ScanLayout L;
@@ -82,7 +83,7 @@ inline FusedBwdLayout fused_bwd_layout(const Dims& d) {
   F.L = scan_layout_n(d.B, fused_chunks(d), d.ng, d.W, false);
   F.dw_part = align_up(F.L.total, 256);
   F.vec_part = align_up(F.dw_part + (size_t)FUSED_MAX_CTAS * 2 * FUSED_K * FUSED_K * 4, 256);
-  F.total = align_up(F.vec_part + (size_t)FUSED_MAX_CTAS * 2 * 3 * FUSED_K * 4, 256);
+  F.total = align_up(F.vec_part + (size_t)FUSED_MAX_CTAS * 4 * 3 * FUSED_K * 4, 256);
   return F;
 }
 
