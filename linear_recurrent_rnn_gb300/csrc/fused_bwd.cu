@@ -14,24 +14,26 @@
 //   dlr = dla (-8 softplus) r (1 - r),  dli = g m u (1 - i),  dx_direct = g m i,
 //   dsoftplus = sum dla (-8 r),  dLambda = sigmoid(Lambda) dsoftplus,  dh0 = abar_0 g_0.
 //
-// Tile = (b, blk, 64 tokens), visited in reverse chunk order; two scan threads per channel,
-// one per 32-token half.  Per tile:
+// Tile = (b, blk, 64 tokens), visited in reverse chunk order; four scan threads per channel,
+// one per 16-token part.  Per tile:
 //   1. MMA: lr^T, li^T = W^T x^T into TMEM (as in the forward).
-//   2. Pass 1 (tokens ascending): r, i, abar kept per token; the half's forward aggregate
-//      (state map h -> A h + B) and reverse aggregate (carry map c_in -> P c_in + S with
-//      P = prod abar, S = sum_t (prod_{s<=t} abar_s) dy_t).  The logits are then released.
-//   3. Halves exchange aggregates through shared memory; half 0 composes the tile's reverse
-//      aggregate and runs the anchored look-back toward larger t (lookback.cuh) for the carry
-//      from the right; the forward entry state comes from the chunk states the forward saved.
-//   4. Pass 2: h_{t-1} forward through the half, then g exactly in reverse with the pointwise
+//   2. Pass 1 (tokens ascending): abar and i kept in registers, m and r parked in TMEM over
+//      the logits; the part's forward aggregate (state map h -> A h + B) and reverse aggregate
+//      (carry map c_in -> P c_in + S with P = prod abar, S = sum_t (prod_{s<=t} abar_s) dy_t).
+//   3. Parts exchange aggregates through shared memory; part 0 composes the tile's reverse
+//      aggregate, publishes it, and runs the anchored look-back toward larger t (lookback.cuh)
+//      for the carry from the right; the forward entry state comes from the chunk states the
+//      forward saved.
+//   4. Pass 2: h_{t-1} forward through the part, then g exactly in reverse with the pointwise
 //      gradients; dlr, dli go to shared memory as bf16 hi + lo pairs (v = hi + lo to ~2^-16),
 //      the direct dx term into the TMEM dx accumulator.
 //   5. MMA: dx^T += Wa (dlr_hi + dlr_lo)^T + Wx (dli_hi + dli_lo)^T on top of the direct term;
 //      dWa += x^T (dlr_hi + dlr_lo), dWx += x^T (dli_hi + dli_lo) accumulated in TMEM over the
 //      CTA's tiles.  The lo halves keep both products at float32-like accuracy: dl can be O(1)
 //      and a bf16-rounded dl alone would cost ~2^-9 |dl| in dx.
-//   6. dx TMEM -> bf16/f32 -> smem -> TMA store.
-// Roles: warp 0 TMA (W once; x + dy tiles, 2 stages), warp 1 MMA, warps 2..9 scan.  CTA
+//   6. dx TMEM -> bf16/f32 -> smem -> TMA store, done after pass 1 of the next tile, so the
+//      step-5 MMAs run while the scan warps work on that pass.
+// Roles: warp 0 TMA (W once; x + dy tiles, 2 stages), warp 1 MMA, warps 2..17 scan.  CTA
 // (blk, r) takes tiles r, r + P, ... of its block, so its partial sums cover a fixed set of
 // tiles: the result is bitwise reproducible.
 #include <cudaTypedefs.h>
@@ -95,13 +97,6 @@ struct Ctl {
   }
 };
 
-// Element (token tl, channel j) of a 64 x 128 tile landed by TMA as 8 slabs of 16 channels
-// with 32-byte swizzle (16-byte halves swapped on rows 4..7 of every 8).
-__device__ __forceinline__ float tile_elem(const uint8_t* slab_base_j, int xhalf, int tl) {
-  return __bfloat162float(*reinterpret_cast<const bf16*>(
-      slab_base_j + tl * 32 + ((xhalf ^ ((tl >> 2) & 1)) << 4)));
-}
-
 // Packs 8 floats to 8 bf16 (round to nearest even).
 __device__ __forceinline__ uint4 pack8(const float* v) {
   uint4 r;
@@ -131,6 +126,112 @@ __device__ __forceinline__ void store_dl8(uint8_t* hi_buf, uint8_t* lo_buf, int 
   const uint32_t at = tg * SLAB_D + j * 32 + ((h8 ^ ((j >> 2) & 1)) << 4);
   *reinterpret_cast<uint4*>(hi_buf + at) = pack8(hi);
   *reinterpret_cast<uint4*>(lo_buf + at) = pack8(lo);
+}
+
+// x (dy at + T_BYTES) of token tb + tt, channel j: xt = stage + tb * 32, and the two channel
+// offsets for the row parities of the 32-byte swizzle (tb is a multiple of 16, so the parity
+// is that of tt, known at compile time).
+__device__ __forceinline__ float tok_elem(const uint8_t* xt, int tt, int xoff0, int xoff1) {
+  return __bfloat162float(
+      *reinterpret_cast<const bf16*>(xt + tt * 32 + (((tt >> 2) & 1) ? xoff1 : xoff0)));
+}
+
+// Pass 1 over the PT tokens of a part (ascending): the gates once; abar and i stay in
+// registers, m and r are parked over the part's logits columns (already read); returns the
+// forward aggregate (h -> fA h + fB) and reverse aggregate (c -> rP c + rS) of the part.
+// GENERAL = false is the warp-uniform fast path: every token valid, no reset, and every decay
+// on the series branch (la > -1/8).
+template <bool GENERAL>
+__device__ __forceinline__ void bwd_pass1(uint32_t tcol, const uint8_t* xt, int xoff0, int xoff1,
+                                          float nk, float nbr, float nbi, uint32_t rmask,
+                                          int valid, float (&ab)[PT], float (&iv)[PT], float& fA,
+                                          float& fB, float& rP, float& rS) {
+#pragma unroll
+  for (int sub = 0; sub < PT / 8; ++sub) {
+    float vr[8], vi[8], m8[8];
+    tc::tmem_ld8(tcol + COL_LR + sub * 8, vr);
+    tc::tmem_ld8(tcol + COL_LI + sub * 8, vi);
+    tc::tmem_ld_wait();
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int tt = sub * 8 + u;
+      const float xv = tok_elem(xt, tt, xoff0, xoff1);
+      const float r = sigmoid_nb(vr[u], nbr);
+      const float i = sigmoid_nb(vi[u], nbi);
+      float a, om, abar, m, dyv;
+      if (GENERAL) {
+        decay_fast(nk * r, a, om);
+        const bool ok = tt < valid;
+        const bool rst = ((rmask >> tt) & 1u) != 0u;
+        dyv = ok ? tok_elem(xt + T_BYTES, tt, xoff0, xoff1) : 0.0f;
+        abar = !ok ? 1.0f : (rst ? 0.0f : a);
+        m = !ok ? 0.0f : (rst ? 1.0f : sqrt_fast(om));
+      } else {
+        decay_near(nk * r, a, om);
+        dyv = tok_elem(xt + T_BYTES, tt, xoff0, xoff1);
+        abar = a;
+        m = sqrt_fast(om);
+      }
+      fB = fmaf(abar, fB, m * (i * xv));
+      fA *= abar;
+      rP *= abar;
+      rS = fmaf(rP, dyv, rS);
+      ab[tt] = abar;
+      iv[tt] = i;
+      m8[u] = m;
+      vr[u] = r;
+    }
+    tc::tmem_st8(tcol + COL_LR + sub * 8, m8);
+    tc::tmem_st8(tcol + COL_LI + sub * 8, vr);
+  }
+  tc::tmem_st_wait();
+}
+
+// Pass 2b over the part (tokens descending): g exactly from the carry `cin` entering the
+// part's last token from the right, and the pointwise gradients.  dlr, dli go to the dl
+// operand buffers as bf16 hi + lo pairs, the direct dx term g m i to the TMEM dx columns.
+template <bool GENERAL>
+__device__ __forceinline__ void bwd_pass2b(uint32_t tcol, int tb, int j, const uint8_t* xt,
+                                           int xoff0, int xoff1, float nk, int valid,
+                                           const float (&ab)[PT], const float (&iv)[PT], float cin,
+                                           uint8_t* s_dl, float& dsp_acc, float& dba_acc,
+                                           float& dbx_acc) {
+  float gnext = cin, abar_next = 1.0f;
+#pragma unroll
+  for (int sub = PT / 8 - 1; sub >= 0; --sub) {  // 8 tokens at a time (registers)
+    float m8[8], r8[8], hp8[8], o_r[8], o_i[8];
+    tc::tmem_ld8(tcol + COL_LR + sub * 8, m8);
+    tc::tmem_ld8(tcol + COL_LI + sub * 8, r8);
+    tc::tmem_ld8(tcol + COL_HP + sub * 8, hp8);
+    tc::tmem_ld_wait();
+#pragma unroll
+    for (int u = 7; u >= 0; --u) {
+      const int tt = sub * 8 + u;
+      const float r = r8[u], i = iv[tt], abar = ab[tt], m = m8[u];
+      const float dyv = (!GENERAL || tt < valid) ? tok_elem(xt + T_BYTES, tt, xoff0, xoff1) : 0.0f;
+      const float uu = i * tok_elem(xt, tt, xoff0, xoff1);
+      const float gv = fmaf(abar_next, gnext, dyv);
+      // d h_t / d la = abar (h_{t-1} - u abar / m); zero at reset tokens (abar = 0), past T
+      // and where the decay is exactly 1 (m = 0)
+      const float alpha = ((GENERAL && abar == 0.0f) || m == 0.0f)
+                              ? 0.0f
+                              : abar * (hp8[u] - uu * abar * rcp_approx(m));
+      const float dla = gv * alpha;
+      o_r[u] = dla * nk * r * (1.0f - r);
+      o_i[u] = gv * m * uu * (1.0f - i);
+      m8[u] = gv * m * i;  // direct dx term
+      dsp_acc = fmaf(dla, -8.0f * r, dsp_acc);
+      dba_acc += o_r[u];
+      dbx_acc += o_i[u];
+      gnext = gv;
+      abar_next = abar;
+    }
+    const int t8 = (tb >> 3) + sub;  // 8-token group: 16-token group t8/2, half t8%2
+    store_dl8(s_dl, s_dl + T_BYTES, t8 >> 1, t8 & 1, j, o_r);
+    store_dl8(s_dl + 2 * T_BYTES, s_dl + 3 * T_BYTES, t8 >> 1, t8 & 1, j, o_i);
+    tc::tmem_st8(tcol + COL_DX + sub * 8, m8);
+  }
+  tc::tmem_st_wait();
 }
 
 template <typename GT>
@@ -293,7 +394,7 @@ __global__ void __maxnreg__(MAXREG)
     const int j = q * 32 + lane;
     const int w = blk * FUSED_K + j;
     const int tb = part * PT;
-    const uint32_t tl_base = tmem + ((uint32_t)(q * 32) << 16);
+    const uint32_t tcol = tmem + ((uint32_t)(q * 32) << 16) + tb;  // this thread's lane, part
     const float nk = -8.0f * softplus_f(p.Lambda[w]);  // log a = nk * r
     const float nbr = p.ba ? -p.ba[w] * LOG2E : 0.0f;   // bias folded into the exponent
     const float nbi = p.bx ? -p.bx[w] * LOG2E : 0.0f;
@@ -301,81 +402,84 @@ __global__ void __maxnreg__(MAXREG)
     float2* agg = reinterpret_cast<float2*>(p.scratch + p.F.L.agg);
     const bool store_thread = (warp == 2 && lane == 0);
     if (store_thread) tc::prefetch_tmap(&tm_dx);
-    uint8_t* dl_rh = s_dl;
-    uint8_t* dl_rl = s_dl + T_BYTES;
-    uint8_t* dl_ih = s_dl + 2 * T_BYTES;
-    uint8_t* dl_il = s_dl + 3 * T_BYTES;
-    const int xhalf = (j & 15) >> 3;
     float dsp_acc = 0.0f, dba_acc = 0.0f, dbx_acc = 0.0f;
+    const bool near_all = __all_sync(0xffffffffu, nk > -0.125f);
+    // Channel j of a token row in a stage: 16-channel slab, 2-byte column, and the 16-byte half
+    // of the 32-byte row (swapped on rows 4..7 of every 8 by the swizzle).
+    const int xoff0 = (j >> 4) * SLAB_X + (j & 7) * 2 + (((j & 15) >> 3) << 4);
+    const int xoff1 = (j >> 4) * SLAB_X + (j & 7) * 2 + ((((j & 15) >> 3) ^ 1) << 4);
 
-    for (int it = 0; it < my_tiles; ++it) {
+    // Software pipeline: iteration `it` runs pass 1 of tile it, then writes out the dx of tile
+    // it - 1 (whose MMAs ran on the tensor cores during that pass 1), then the rest of tile it.
+    // The last iteration only writes out the dx of the last tile.
+    for (int it = 0; it <= my_tiles; ++it) {
+      const bool have = it < my_tiles;
       const int n = rr + it * p.P;
       const int c = p.nC - 1 - n / p.B, b = n % p.B;
       const int st = it % STAGES;
       const uint32_t ph = (it / STAGES) & 1;
-      const float hin_tile = p.fwd_carry[((size_t)b * (p.nC + 1) + c) * p.W + w];
-      ctl.wait(lg_full, it & 1);
-      ctl.wait(&in_full[st], ph);
-      tc::tc_fence_after();
-      const uint8_t* xj = s_in + st * 2 * T_BYTES + (j >> 4) * SLAB_X + (j & 7) * 2;
-      const uint8_t* dyj = xj + T_BYTES;
-
-      uint32_t rmask = 0;
-      if (p.canonical) {
-        const int t = c * FUSED_C + tb + lane;
-        rmask = __ballot_sync(0xffffffffu, lane < PT && t < p.T &&
-                                               is_reset(p.reset_mask, p.segment_pos,
-                                                        (size_t)b * p.T + t));
-      }
-      const int valid = min(FUSED_C, p.T - c * FUSED_C) - tb;
-
-      // Pass 1 (tokens ascending): the gates once.  abar and i stay in registers; m, 1/m and
-      // r are parked in this thread's TMEM columns (over its logits, already read, and its dx
-      // columns, free until pass 2 writes the direct dx term).  Also the part's forward
-      // aggregate (fA, fB) and reverse aggregate (rP, rS).
+      const uint8_t* xt = s_in + st * 2 * T_BYTES + tb * 32;
       float ab[PT], iv[PT];
-      float fA = 1.0f, fB = 0.0f, rP = 1.0f, rS = 0.0f;
-#pragma unroll
-      for (int sub = 0; sub < PT / 8; ++sub) {
-        float vr[8], vi[8], m8[8], s8[8];
-        tc::tmem_ld8(tl_base + COL_LR + tb + sub * 8, vr);
-        tc::tmem_ld8(tl_base + COL_LI + tb + sub * 8, vi);
-        tc::tmem_ld_wait();
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          const int tt = sub * 8 + u;
-          const int tl = tb + tt;
-          const bool ok = tt < valid;
-          const bool rst = ((rmask >> tt) & 1u) != 0u;
-          const float xv = tile_elem(xj, xhalf, tl);
-          const float dyv = ok ? tile_elem(dyj, xhalf, tl) : 0.0f;
-          const float r = sigmoid_nb(vr[u], nbr);
-          const float i = sigmoid_nb(vi[u], nbi);
-          float a, om;
-          decay_fast(nk * r, a, om);
-          const float rs0 = om > 0.0f ? rsqrtf(om) : 0.0f;
-          const float abar = !ok ? 1.0f : (rst ? 0.0f : a);
-          const float m = !ok ? 0.0f : (rst ? 1.0f : om * rs0);
-          const float rs = !ok ? 0.0f : (rst ? 1.0f : rs0);
-          fB = fmaf(abar, fB, m * (i * xv));
-          fA *= abar;
-          rP *= abar;
-          rS = fmaf(rP, dyv, rS);
-          ab[tt] = abar;
-          iv[tt] = i;
-          m8[u] = m;
-          s8[u] = rs;
-          vr[u] = r;
+      float fA = 1.0f, fB = 0.0f, rP = 1.0f, rS = 0.0f, hin_tile = 0.0f;
+      int valid = 0;
+      bool fast = false;
+      if (have) {
+        hin_tile = p.fwd_carry[((size_t)b * (p.nC + 1) + c) * p.W + w];
+        uint32_t rmask = 0;
+        if (p.canonical) {
+          const int t = c * FUSED_C + tb + lane;
+          rmask = __ballot_sync(0xffffffffu, lane < PT && t < p.T &&
+                                                 is_reset(p.reset_mask, p.segment_pos,
+                                                          (size_t)b * p.T + t));
         }
-        tc::tmem_st8(tl_base + COL_LR + tb + sub * 8, m8);
-        tc::tmem_st8(tl_base + COL_LI + tb + sub * 8, s8);
-        tc::tmem_st8(tl_base + COL_DX + tb + sub * 8, vr);
+        valid = min(FUSED_C, p.T - c * FUSED_C) - tb;
+        fast = near_all && rmask == 0u && valid >= PT;
+        ctl.wait(lg_full, it & 1);
+        ctl.wait(&in_full[st], ph);
+        tc::tc_fence_after();
+        if (fast)
+          bwd_pass1<false>(tcol, xt, xoff0, xoff1, nk, nbr, nbi, 0u, PT, ab, iv, fA, fB, rP, rS);
+        else
+          bwd_pass1<true>(tcol, xt, xoff0, xoff1, nk, nbr, nbi, rmask, valid, ab, iv, fA, fB, rP,
+                          rS);
       }
-      tc::tmem_st_wait();
 
-      s_agg[part * FUSED_K + j] = make_float4(fA, fB, rP, rS);
-      if (store_thread) tc::tma_store_wait_read0();  // the dx staging is free again
-      tc::named_bar(1, NSCAN * 32);
+      // dx of tile it - 1: TMEM -> smem [token][channel] as bf16 (float32 goes straight to HBM).
+      if (it > 0) {
+        const int np = n - p.P;
+        const int cp = p.nC - 1 - np / p.B, bp = np % p.B;
+        const int validp = min(FUSED_C, p.T - cp * FUSED_C) - tb;
+        ctl.wait(dx_full, (it - 1) & 1);
+        tc::tc_fence_after();
+#pragma unroll
+        for (int sub = 0; sub < PT / 8; ++sub) {
+          float v[8];
+          tc::tmem_ld8(tcol + COL_DX + sub * 8, v);
+          tc::tmem_ld_wait();
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            const int tl = tb + sub * 8 + u;
+            if (sizeof(GT) == 2) {
+              *reinterpret_cast<bf16*>(s_dx + tl * (FUSED_K * 2) + j * 2) =
+                  __float2bfloat16_rn(v[u]);
+            } else if (sub * 8 + u < validp) {
+              // 128 contiguous bytes per warp and token
+              static_cast<float*>(p.dx)[((size_t)bp * p.T + cp * FUSED_C + tl) * p.W + w] = v[u];
+            }
+          }
+        }
+        tc::tc_fence_before();
+      }
+      if (have) s_agg[part * FUSED_K + j] = make_float4(fA, fB, rP, rS);
+      tc::fence_proxy_async_smem();
+      tc::named_bar(1, NSCAN * 32);  // barrier A: part aggregates and the dx staging
+      if (it > 0 && store_thread && sizeof(GT) == 2) {
+        const int np = n - p.P;
+        tc::tma_store_3d(&tm_dx, s_dx, blk * FUSED_K, (p.nC - 1 - np / p.B) * FUSED_C, np % p.B);
+        tc::tma_store_commit();
+      }
+      if (!have) break;
+
       // Entry-state map of this part (earlier parts composed) and carry map from the tile's
       // right edge to this part (later parts composed).
       float Fa = 1.0f, Fb = 0.0f, Rp = 1.0f, Rs = 0.0f;
@@ -397,16 +501,23 @@ __global__ void __maxnreg__(MAXREG)
       }
 
       // Part 0 owns the chunk's reverse carry: its map after the later parts' is the tile's,
-      // published at once; the look-back itself waits until pass 2a is done.
+      // published at once; the look-back slots are requested now and read after pass 2a.
       const size_t cidx = (size_t)b * p.nC + c;
       const bool publish = (blk * ntiles + n) != p.drop_tile;
       const float tP = rP * Rp, tS = fmaf(rP, Rs, rS);
-      if (part == 0 && c < p.nC - 1 && ((p.nC - 1 - c) % ANCHOR) != 0 && publish)
-        slot_put2(agg + cidx * p.W + w, tP, tS);
-
-      // The dl buffers and the dx accumulator are free once the previous tile's MMAs are done.
-      if (it > 0) ctl.wait(dl_empty, (it - 1) & 1);
-      tc::tc_fence_after();
+      LookbackReq lbq;
+      int lb_n = 0;
+      const float2* lb_agg = agg;
+      const float* lb_anchor = rcar;
+      if (part == 0 && c < p.nC - 1) {
+        if (((p.nC - 1 - c) % ANCHOR) != 0 && publish) slot_put2(agg + cidx * p.W + w, tP, tS);
+        // nearest anchor after this chunk (anchors counted from the last chunk)
+        const int an = p.nC - 1 - ((p.nC - 2 - c) / ANCHOR) * ANCHOR;
+        lb_n = an - c - 1;
+        lb_agg = agg + (cidx + 1) * p.W + w;
+        lb_anchor = rcar + ((size_t)b * p.nC + an) * p.W + w;
+        lookback_issue(lbq, lb_agg, (long)p.W, lb_n, lb_anchor);
+      }
 
       // Pass 2a: h_{t-1} through the part, parked in TMEM.
       {
@@ -414,15 +525,15 @@ __global__ void __maxnreg__(MAXREG)
 #pragma unroll
         for (int sub = 0; sub < PT / 8; ++sub) {
           float m8[8], hp8[8];
-          tc::tmem_ld8(tl_base + COL_LR + tb + sub * 8, m8);
+          tc::tmem_ld8(tcol + COL_LR + sub * 8, m8);
           tc::tmem_ld_wait();
 #pragma unroll
           for (int u = 0; u < 8; ++u) {
             const int tt = sub * 8 + u;
             hp8[u] = h;
-            h = fmaf(ab[tt], h, m8[u] * (iv[tt] * tile_elem(xj, xhalf, tb + tt)));
+            h = fmaf(ab[tt], h, m8[u] * (iv[tt] * tok_elem(xt, tt, xoff0, xoff1)));
           }
-          tc::tmem_st8(tl_base + COL_HP + tb + sub * 8, hp8);
+          tc::tmem_st8(tcol + COL_HP + sub * 8, hp8);
         }
         tc::tmem_st_wait();
       }
@@ -432,56 +543,26 @@ __global__ void __maxnreg__(MAXREG)
         if (c == p.nC - 1) {
           if (p.dhT) cin = p.dhT[(size_t)b * p.W + w];
         } else {
-          // nearest anchor after this chunk (anchors counted from the last chunk)
-          const int an = p.nC - 1 - ((p.nC - 2 - c) / ANCHOR) * ANCHOR;
-          cin = lookback_carry(agg + (cidx + 1) * p.W + w, (long)p.W, an - c - 1,
-                               rcar + ((size_t)b * p.nC + an) * p.W + w, p.spin_limit, status);
+          cin = lookback_finish(lbq, lb_agg, (long)p.W, lb_n, lb_anchor, p.spin_limit, status);
         }
         const float cout = fmaf(tP, cin, tS);
         if (publish) slot_put1(rcar + cidx * p.W + w, cout);
         if (c == 0 && p.dh0) p.dh0[(size_t)b * p.W + w] = p.canonical ? cout : 0.0f;
         s_cin[j] = cin;
       }
-      tc::named_bar(1, NSCAN * 32);
-      const float cin = fmaf(Rp, s_cin[j], Rs);  // carry into this part from the right
+      if (store_thread) tc::tma_store_wait_read0();  // dx staging free for the next iteration
+      tc::named_bar(1, NSCAN * 32);                   // barrier B: the tile's right carry
+      const float cin = fmaf(Rp, s_cin[j], Rs);      // carry into this part from the right
 
-      // Pass 2b: g exactly, tokens descending, and the pointwise gradients.
-      float gnext = cin, abar_next = 1.0f;
-#pragma unroll
-      for (int sub = PT / 8 - 1; sub >= 0; --sub) {  // 8 tokens at a time (registers)
-        float m8[8], s8[8], r8[8], hp8[8], o_r[8], o_i[8];
-        tc::tmem_ld8(tl_base + COL_LR + tb + sub * 8, m8);
-        tc::tmem_ld8(tl_base + COL_LI + tb + sub * 8, s8);
-        tc::tmem_ld8(tl_base + COL_DX + tb + sub * 8, r8);
-        tc::tmem_ld8(tl_base + COL_HP + tb + sub * 8, hp8);
-        tc::tmem_ld_wait();
-#pragma unroll
-        for (int u = 7; u >= 0; --u) {
-          const int tt = sub * 8 + u;
-          const int tl = tb + tt;
-          const float r = r8[u], i = iv[tt], abar = ab[tt], m = m8[u];
-          const float dyv = tt < valid ? tile_elem(dyj, xhalf, tl) : 0.0f;
-          const float uu = i * tile_elem(xj, xhalf, tl);
-          const float gv = fmaf(abar_next, gnext, dyv);
-          // zero at reset tokens (abar = 0) and past T (m = 0)
-          const float alpha =
-              (abar == 0.0f || m == 0.0f) ? 0.0f : abar * (hp8[u] - uu * abar * s8[u]);
-          const float dla = gv * alpha;
-          o_r[u] = dla * nk * r * (1.0f - r);
-          o_i[u] = gv * m * uu * (1.0f - i);
-          m8[u] = gv * m * i;  // direct dx term
-          dsp_acc = fmaf(dla, -8.0f * r, dsp_acc);
-          dba_acc += o_r[u];
-          dbx_acc += o_i[u];
-          gnext = gv;
-          abar_next = abar;
-        }
-        const int t8 = (tb >> 3) + sub;  // 8-token group: 16-token group t8/2, half t8%2
-        store_dl8(dl_rh, dl_rl, t8 >> 1, t8 & 1, j, o_r);
-        store_dl8(dl_ih, dl_il, t8 >> 1, t8 & 1, j, o_i);
-        tc::tmem_st8(tl_base + COL_DX + tb + sub * 8, m8);
-      }
-      tc::tmem_st_wait();
+      // The dl buffers are free once the previous tile's MMAs are done.
+      if (it > 0) ctl.wait(dl_empty, (it - 1) & 1);
+      tc::tc_fence_after();
+      if (fast)
+        bwd_pass2b<false>(tcol, tb, j, xt, xoff0, xoff1, nk, PT, ab, iv, cin, s_dl, dsp_acc,
+                          dba_acc, dbx_acc);
+      else
+        bwd_pass2b<true>(tcol, tb, j, xt, xoff0, xoff1, nk, valid, ab, iv, cin, s_dl, dsp_acc,
+                         dba_acc, dbx_acc);
       tc::fence_proxy_async_smem();
       tc::tc_fence_before();
       __syncwarp();
@@ -489,33 +570,6 @@ __global__ void __maxnreg__(MAXREG)
         tc::mbar_arrive(lg_empty);  // the logits columns are free for the next tile
         tc::mbar_arrive(&in_empty[st]);
         tc::mbar_arrive(dl_full);
-      }
-
-      // dx tile: TMEM -> smem [token][channel] -> TMA store (clipped at T).
-      ctl.wait(dx_full, it & 1);
-      tc::tc_fence_after();
-#pragma unroll
-      for (int sub = 0; sub < PT / 16; ++sub) {
-        float v[16];
-        tc::tmem_ld16(tl_base + COL_DX + tb + sub * 16, v);
-        tc::tmem_ld_wait();
-#pragma unroll
-        for (int u = 0; u < 16; ++u) {
-          const int tl = tb + sub * 16 + u;
-          if (sizeof(GT) == 2) {
-            *reinterpret_cast<bf16*>(s_dx + tl * (FUSED_K * 2) + j * 2) = __float2bfloat16_rn(v[u]);
-          } else if (sub * 16 + u < valid) {
-            // float32 gradients go straight to HBM (128 contiguous bytes per warp and token)
-            static_cast<float*>(p.dx)[((size_t)b * p.T + c * FUSED_C + tl) * p.W + w] = v[u];
-          }
-        }
-      }
-      tc::tc_fence_before();
-      tc::fence_proxy_async_smem();
-      tc::named_bar(1, NSCAN * 32);
-      if (store_thread && sizeof(GT) == 2) {
-        tc::tma_store_3d(&tm_dx, s_dx, blk * FUSED_K, c * FUSED_C, b);
-        tc::tma_store_commit();
       }
     }
     if (store_thread) tc::tma_store_wait0();
@@ -540,7 +594,7 @@ __global__ void __maxnreg__(MAXREG)
         const int col = part * (FUSED_K / NPART) + sub * 16;
         float v[16];
         if (my_tiles > 0) {
-          tc::tmem_ld16(tl_base + (mtx ? COL_DWX : COL_DWA) + col, v);
+          tc::tmem_ld16(tcol - tb + (mtx ? COL_DWX : COL_DWA) + col, v);
           tc::tmem_ld_wait();
         } else {
 #pragma unroll
