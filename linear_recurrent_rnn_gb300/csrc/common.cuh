@@ -124,6 +124,85 @@ __device__ __forceinline__ float sqrt_fast(float v) {
   return v > 0.0f ? v * rsqrtf(v) : 0.0f;
 }
 
+// ---------------------------------------------------------------- packed pairs
+// Two independent float32 lanes per instruction (the f32x2 arithmetic of sm_100 and later):
+// a scan thread runs two token chains side by side, one per lane.  Each lane rounds exactly as
+// the scalar instruction would.
+__device__ __forceinline__ float2 bc2(float a) { return make_float2(a, a); }
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) { return __ffma2_rn(a, b, c); }
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) { return __fmul2_rn(a, b); }
+__device__ __forceinline__ float2 add2(float2 a, float2 b) { return __fadd2_rn(a, b); }
+
+// sigmoid_nb on two logits.
+__device__ __forceinline__ float2 sigmoid2_nb(float2 z, float nb) {
+  const float2 s = fma2(z, bc2(-LOG2E), bc2(nb));
+  const float2 d = add2(make_float2(ex2_approx(s.x), ex2_approx(s.y)), bc2(1.0f));
+  return make_float2(rcp_approx(d.x), rcp_approx(d.y));
+}
+
+// decay_near / decay_fast on two lanes (same arithmetic, lane by lane).
+__device__ __forceinline__ float2 expm1_series2(float2 la) {
+  float2 p = fma2(la, bc2(1.0f / 5040.0f), bc2(1.0f / 720.0f));
+  p = fma2(la, p, bc2(1.0f / 120.0f));
+  p = fma2(la, p, bc2(1.0f / 24.0f));
+  p = fma2(la, p, bc2(1.0f / 6.0f));
+  p = fma2(la, p, bc2(0.5f));
+  p = fma2(la, p, bc2(1.0f));
+  return mul2(la, p);
+}
+__device__ __forceinline__ void decay_near2(float2 la, float2& a, float2& om) {
+  const float2 e1 = expm1_series2(la);
+  a = add2(e1, bc2(1.0f));
+  om = mul2(e1, fma2(e1, bc2(-1.0f), bc2(-2.0f)));  // -e1 (e1 + 2)
+}
+__device__ __forceinline__ void decay_fast2(float2 la, float2& a, float2& om) {
+  decay_near2(la, a, om);
+  if (!(la.x > -0.125f)) {
+    const float ax = ex2_approx(la.x * LOG2E);
+    a.x = ax;
+    om.x = fmaf(-ax, ax, 1.0f);
+  }
+  if (!(la.y > -0.125f)) {
+    const float ax = ex2_approx(la.y * LOG2E);
+    a.y = ax;
+    om.y = fmaf(-ax, ax, 1.0f);
+  }
+}
+__device__ __forceinline__ float2 sqrt_fast2(float2 v) {
+  return make_float2(sqrt_fast(v.x), sqrt_fast(v.y));
+}
+
+// ---------------------------------------------------------------- staged bf16 tiles
+// A [token][channel] bf16 tile staged by TMA as slabs of 16 channels x 32-byte token rows with
+// the 32-byte swizzle (the row's two 16-byte halves swap on rows 4..7 of every 8).  b0 / b1
+// are the shared-memory addresses of one channel in row tb (a multiple of 8) for rows of
+// swizzle parity 0 / 1; element (tb + tt, channel) is then at a compile-time offset from one
+// of them for a compile-time tt.
+__device__ __forceinline__ float lds_bf16(uint32_t addr) {
+  uint16_t v;
+  asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(addr));
+  return __uint_as_float((uint32_t)v << 16);
+}
+__device__ __forceinline__ float tok_elem(uint32_t b0, uint32_t b1, int tt) {
+  return lds_bf16((((tt >> 2) & 1) ? b1 : b0) + tt * 32);
+}
+
+// ---------------------------------------------------------------- tile walks
+// Chunk c and batch row b of the tiles n = r, r + P, r + 2P, ... of one gate block, with
+// n = c * B + b, stepped without a division per tile.
+struct TileWalk {
+  int c, b, dc, db, B;
+  __device__ TileWalk(int r, int P, int B_) : c(r / B_), b(r % B_), dc(P / B_), db(P % B_), B(B_) {}
+  __device__ void next() {
+    c += dc;
+    b += db;
+    if (b >= B) {
+      b -= B;
+      ++c;
+    }
+  }
+};
+
 // ---------------------------------------------------------------- value-as-flag slots
 // Look-back slots of the fused kernels carry their own readiness: a slot holds the all-ones
 // bit pattern (a NaN that float arithmetic never produces) until its value is stored with a

@@ -62,7 +62,7 @@ constexpr uint32_t SLAB_D = FUSED_K * 32;            // 16 tokens x 128 channels
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t COL_LR = 0, COL_LI = 64, COL_DX = 128, COL_HP = 192, COL_DWA = 256,
                    COL_DWX = 384;
-constexpr int WAIT_LIMIT = 1 << 22;
+constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;  // 2 s: a pipeline wait never lasts this
 constexpr uint32_t XCH_BYTES = NPART * FUSED_K * 16 + FUSED_K * 4;  // part aggregates + carry
 // W (2) + x/dy stages (2 x 2) + dl buffers (4) + bf16 dx staging (1) tiles, exchange, barriers
 constexpr size_t SMEM_BYTES =
@@ -83,6 +83,7 @@ struct BwdParams {
   uint8_t* scratch;        // workspace
   FusedBwdLayout F;
   int spin_limit, drop_tile;
+  int lb_dist, lb_shift;
 };
 
 struct Ctl {
@@ -90,146 +91,202 @@ struct Ctl {
   uint32_t* status;
   __device__ bool wait(uint64_t* bar, uint32_t parity) const {
     if (*abort) return false;
-    if (tc::mbar_wait(bar, parity, WAIT_LIMIT)) return true;
+    if (tc::mbar_wait(bar, parity, WAIT_LIMIT_NS)) return true;
     *abort = 1u;
     atomicOr(status, STATUS_PIPE);
     return false;
   }
 };
 
-// Packs 8 floats to 8 bf16 (round to nearest even).
-__device__ __forceinline__ uint4 pack8(const float* v) {
-  uint4 r;
-  __nv_bfloat162 p0 = __floats2bfloat162_rn(v[0], v[1]);
-  __nv_bfloat162 p1 = __floats2bfloat162_rn(v[2], v[3]);
-  __nv_bfloat162 p2 = __floats2bfloat162_rn(v[4], v[5]);
-  __nv_bfloat162 p3 = __floats2bfloat162_rn(v[6], v[7]);
-  r.x = *reinterpret_cast<uint32_t*>(&p0);
-  r.y = *reinterpret_cast<uint32_t*>(&p1);
-  r.z = *reinterpret_cast<uint32_t*>(&p2);
-  r.w = *reinterpret_cast<uint32_t*>(&p3);
-  return r;
+// v = hi + lo with hi = bf16(v) and lo = bf16(v - hi) (v - hi is exact in float32), for two
+// values at once; returns the bf16x2 bit patterns of (hi0, hi1) and (lo0, lo1).
+__device__ __forceinline__ void split_hi_lo(float2 v, uint32_t& hi, uint32_t& lo) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(v.x, v.y);
+  const float2 l = fma2(__bfloat1622float2(h), bc2(-1.0f), v);
+  const __nv_bfloat162 lb = __floats2bfloat162_rn(l.x, l.y);
+  hi = *reinterpret_cast<const uint32_t*>(&h);
+  lo = *reinterpret_cast<const uint32_t*>(&lb);
 }
 
-// Writes 8 tokens of channel j (16-byte half `h8` of the 32-byte row of token group tg) as
-// hi and lo bf16 parts into the dl operand buffers [tg][channel row][16 tokens] (32-byte
-// swizzle: the two 16-byte halves swap on rows 4..7 of every 8).
-__device__ __forceinline__ void store_dl8(uint8_t* hi_buf, uint8_t* lo_buf, int tg, int h8, int j,
-                                          const float (&v)[8]) {
-  float hi[8], lo[8];
-#pragma unroll
-  for (int u = 0; u < 8; ++u) {
-    const bf16 h = __float2bfloat16_rn(v[u]);
-    hi[u] = __bfloat162float(h);
-    lo[u] = v[u] - hi[u];
-  }
-  const uint32_t at = tg * SLAB_D + j * 32 + ((h8 ^ ((j >> 2) & 1)) << 4);
-  *reinterpret_cast<uint4*>(hi_buf + at) = pack8(hi);
-  *reinterpret_cast<uint4*>(lo_buf + at) = pack8(lo);
+// Writes 4 consecutive tokens of channel j (tokens u .. u + 3 of 16-token group tg, u a
+// multiple of 4) as hi and lo bf16 parts into the dl operand buffers [tg][channel row][16
+// tokens] (32-byte swizzle: the row's two 16-byte halves swap on rows 4..7 of every 8).
+__device__ __forceinline__ void store_dl4(uint8_t* hi_buf, uint8_t* lo_buf, int tg, int u, int j,
+                                          float2 v01, float2 v23) {
+  uint2 hi, lo;
+  split_hi_lo(v01, hi.x, lo.x);
+  split_hi_lo(v23, hi.y, lo.y);
+  const uint32_t at = tg * SLAB_D + j * 32 + (((u >> 3) ^ ((j >> 2) & 1)) << 4) + ((u >> 2) & 1) * 8;
+  *reinterpret_cast<uint2*>(hi_buf + at) = hi;
+  *reinterpret_cast<uint2*>(lo_buf + at) = lo;
 }
 
-// x (dy at + T_BYTES) of token tb + tt, channel j: xt = stage + tb * 32, and the two channel
-// offsets for the row parities of the 32-byte swizzle (tb is a multiple of 16, so the parity
-// is that of tt, known at compile time).
-__device__ __forceinline__ float tok_elem(const uint8_t* xt, int tt, int xoff0, int xoff1) {
-  return __bfloat162float(
-      *reinterpret_cast<const bf16*>(xt + tt * 32 + (((tt >> 2) & 1) ? xoff1 : xoff0)));
-}
+// The passes of a scan thread over its part's 16 tokens do the pointwise work on token pairs
+// (u, u + 1) in the two lanes of f32x2 operations (adjacent TMEM columns land in adjacent
+// registers) and run the recurrences as scalar chains.  Per-token values parked in TMEM sit at
+// column = token of the part; the thread's columns of each region start at tcol.
+constexpr int GRP = 4;  // tokens per TMEM load / store group
 
-// Pass 1 over the PT tokens of a part (ascending): the gates once; abar and i stay in
-// registers, m and r are parked over the part's logits columns (already read); returns the
-// forward aggregate (h -> fA h + fB) and reverse aggregate (c -> rP c + rS) of the part.
-// GENERAL = false is the warp-uniform fast path: every token valid, no reset, and every decay
-// on the series branch (la > -1/8).
+// Pass 1 (tokens ascending): the gates once; abar stays in registers, m -> COL_LR and r ->
+// COL_LI (over the logits, already read), i -> COL_HP; returns the part's maps: forward
+// h -> P h + fB and reverse c -> P c + S, with P = prod abar and S = sum_t (prod of abar up
+// to t) dy_t.  GENERAL = false is the warp-uniform fast path: every token valid, no reset,
+// every decay on the series branch.
 template <bool GENERAL>
-__device__ __forceinline__ void bwd_pass1(uint32_t tcol, const uint8_t* xt, int xoff0, int xoff1,
-                                          float nk, float nbr, float nbi, uint32_t rmask,
-                                          int valid, float (&ab)[PT], float (&iv)[PT], float& fA,
-                                          float& fB, float& rP, float& rS) {
+__device__ __forceinline__ void bwd_pass1(uint32_t tcol, uint32_t xb0, uint32_t xb1, float nk,
+                                          float nbr, float nbi, uint32_t rmask, int valid,
+                                          float2 (&ab)[PT / 2], float& P, float& fB, float& S) {
+  P = 1.0f;
+  fB = 0.0f;
+  S = 0.0f;
 #pragma unroll
-  for (int sub = 0; sub < PT / 8; ++sub) {
-    float vr[8], vi[8], m8[8];
-    tc::tmem_ld8(tcol + COL_LR + sub * 8, vr);
-    tc::tmem_ld8(tcol + COL_LI + sub * 8, vi);
+  for (int g = 0; g < PT / GRP; ++g) {
+    float vr[GRP], vi[GRP], m4[GRP], i4[GRP];
+    tc::tmem_ld4(tcol + COL_LR + g * GRP, vr);
+    tc::tmem_ld4(tcol + COL_LI + g * GRP, vi);
     tc::tmem_ld_wait();
 #pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      const int tt = sub * 8 + u;
-      const float xv = tok_elem(xt, tt, xoff0, xoff1);
-      const float r = sigmoid_nb(vr[u], nbr);
-      const float i = sigmoid_nb(vi[u], nbi);
-      float a, om, abar, m, dyv;
+    for (int q = 0; q < GRP / 2; ++q) {
+      const int u = g * GRP + 2 * q;
+      const float2 xv = make_float2(tok_elem(xb0, xb1, u), tok_elem(xb0, xb1, u + 1));
+      float2 dyv = make_float2(tok_elem(xb0 + T_BYTES, xb1 + T_BYTES, u),
+                               tok_elem(xb0 + T_BYTES, xb1 + T_BYTES, u + 1));
+      const float2 r = sigmoid2_nb(make_float2(vr[2 * q], vr[2 * q + 1]), nbr);
+      const float2 i = sigmoid2_nb(make_float2(vi[2 * q], vi[2 * q + 1]), nbi);
+      const float2 la = mul2(bc2(nk), r);
+      float2 abar, om;
+      if (GENERAL)
+        decay_fast2(la, abar, om);
+      else
+        decay_near2(la, abar, om);
+      float2 m = sqrt_fast2(om);
       if (GENERAL) {
-        decay_fast(nk * r, a, om);
-        const bool ok = tt < valid;
-        const bool rst = ((rmask >> tt) & 1u) != 0u;
-        dyv = ok ? tok_elem(xt + T_BYTES, tt, xoff0, xoff1) : 0.0f;
-        abar = !ok ? 1.0f : (rst ? 0.0f : a);
-        m = !ok ? 0.0f : (rst ? 1.0f : sqrt_fast(om));
-      } else {
-        decay_near(nk * r, a, om);
-        dyv = tok_elem(xt + T_BYTES, tt, xoff0, xoff1);
-        abar = a;
-        m = sqrt_fast(om);
+        if ((rmask >> u) & 1u) {
+          abar.x = 0.0f;
+          m.x = 1.0f;
+        }
+        if ((rmask >> (u + 1)) & 1u) {
+          abar.y = 0.0f;
+          m.y = 1.0f;
+        }
+        if (u >= valid) {
+          abar.x = 1.0f;
+          m.x = 0.0f;
+          dyv.x = 0.0f;
+        }
+        if (u + 1 >= valid) {
+          abar.y = 1.0f;
+          m.y = 0.0f;
+          dyv.y = 0.0f;
+        }
       }
-      fB = fmaf(abar, fB, m * (i * xv));
-      fA *= abar;
-      rP *= abar;
-      rS = fmaf(rP, dyv, rS);
-      ab[tt] = abar;
-      iv[tt] = i;
-      m8[u] = m;
-      vr[u] = r;
+      const float2 bv = mul2(m, mul2(i, xv));
+      fB = fmaf(abar.x, fB, bv.x);
+      P *= abar.x;
+      S = fmaf(P, dyv.x, S);
+      fB = fmaf(abar.y, fB, bv.y);
+      P *= abar.y;
+      S = fmaf(P, dyv.y, S);
+      ab[u / 2] = abar;
+      m4[2 * q] = m.x;
+      m4[2 * q + 1] = m.y;
+      vr[2 * q] = r.x;  // the logits are consumed: their registers take r and i
+      vr[2 * q + 1] = r.y;
+      i4[2 * q] = i.x;
+      i4[2 * q + 1] = i.y;
     }
-    tc::tmem_st8(tcol + COL_LR + sub * 8, m8);
-    tc::tmem_st8(tcol + COL_LI + sub * 8, vr);
+    tc::tmem_st4(tcol + COL_LR + g * GRP, m4);
+    tc::tmem_st4(tcol + COL_LI + g * GRP, vr);
+    tc::tmem_st4(tcol + COL_HP + g * GRP, i4);
   }
   tc::tmem_st_wait();
 }
 
-// Pass 2b over the part (tokens descending): g exactly from the carry `cin` entering the
-// part's last token from the right, and the pointwise gradients.  dlr, dli go to the dl
-// operand buffers as bf16 hi + lo pairs, the direct dx term g m i to the TMEM dx columns.
-template <bool GENERAL>
-__device__ __forceinline__ void bwd_pass2b(uint32_t tcol, int tb, int j, const uint8_t* xt,
-                                           int xoff0, int xoff1, float nk, int valid,
-                                           const float (&ab)[PT], const float (&iv)[PT], float cin,
-                                           uint8_t* s_dl, float& dsp_acc, float& dba_acc,
-                                           float& dbx_acc) {
-  float gnext = cin, abar_next = 1.0f;
+// Pass 2a (tokens ascending): h_{t-1} of every token from the state h entering the part,
+// parked in the dx columns (free once the previous tile's dx has been written out).
+__device__ __forceinline__ void bwd_pass2a(uint32_t tcol, uint32_t xb0, uint32_t xb1,
+                                           const float2 (&ab)[PT / 2], float h) {
 #pragma unroll
-  for (int sub = PT / 8 - 1; sub >= 0; --sub) {  // 8 tokens at a time (registers)
-    float m8[8], r8[8], hp8[8], o_r[8], o_i[8];
-    tc::tmem_ld8(tcol + COL_LR + sub * 8, m8);
-    tc::tmem_ld8(tcol + COL_LI + sub * 8, r8);
-    tc::tmem_ld8(tcol + COL_HP + sub * 8, hp8);
+  for (int g = 0; g < PT / GRP; ++g) {
+    float m4[GRP], i4[GRP], h4[GRP];
+    tc::tmem_ld4(tcol + COL_LR + g * GRP, m4);
+    tc::tmem_ld4(tcol + COL_HP + g * GRP, i4);
     tc::tmem_ld_wait();
 #pragma unroll
-    for (int u = 7; u >= 0; --u) {
-      const int tt = sub * 8 + u;
-      const float r = r8[u], i = iv[tt], abar = ab[tt], m = m8[u];
-      const float dyv = (!GENERAL || tt < valid) ? tok_elem(xt + T_BYTES, tt, xoff0, xoff1) : 0.0f;
-      const float uu = i * tok_elem(xt, tt, xoff0, xoff1);
-      const float gv = fmaf(abar_next, gnext, dyv);
+    for (int q = 0; q < GRP / 2; ++q) {
+      const int u = g * GRP + 2 * q;
+      const float2 xv = make_float2(tok_elem(xb0, xb1, u), tok_elem(xb0, xb1, u + 1));
+      const float2 bv = mul2(make_float2(m4[2 * q], m4[2 * q + 1]),
+                             mul2(make_float2(i4[2 * q], i4[2 * q + 1]), xv));
+      h4[2 * q] = h;
+      h = fmaf(ab[u / 2].x, h, bv.x);
+      h4[2 * q + 1] = h;
+      h = fmaf(ab[u / 2].y, h, bv.y);
+    }
+    tc::tmem_st4(tcol + COL_DX + g * GRP, h4);
+  }
+  tc::tmem_st_wait();
+}
+
+// Pass 2b (tokens descending): g exactly from the carry `cin` entering the part's last token
+// from the right, and the pointwise gradients; dlr, dli go to the dl operand buffers as bf16
+// hi + lo pairs, the direct dx term g m i over h_{t-1} in the dx columns (the accumulator of
+// the dx MMAs).
+template <bool GENERAL>
+__device__ __forceinline__ void bwd_pass2b(uint32_t tcol, int part, int j, uint32_t xb0,
+                                           uint32_t xb1, float nk, int valid,
+                                           const float2 (&ab)[PT / 2], float cin, uint8_t* s_dl,
+                                           float2& dsp, float2& dba, float2& dbx) {
+  float gnext = cin, anext = 1.0f;
+#pragma unroll
+  for (int g = PT / GRP - 1; g >= 0; --g) {
+    float m4[GRP], r4[GRP], i4[GRP], h4[GRP];
+    tc::tmem_ld4(tcol + COL_LR + g * GRP, m4);
+    tc::tmem_ld4(tcol + COL_LI + g * GRP, r4);
+    tc::tmem_ld4(tcol + COL_HP + g * GRP, i4);
+    tc::tmem_ld4(tcol + COL_DX + g * GRP, h4);
+    tc::tmem_ld_wait();
+    float2 o_r[GRP / 2], o_i[GRP / 2];
+#pragma unroll
+    for (int q = GRP / 2 - 1; q >= 0; --q) {
+      const int u = g * GRP + 2 * q;
+      const float2 xv = make_float2(tok_elem(xb0, xb1, u), tok_elem(xb0, xb1, u + 1));
+      float2 dyv = make_float2(tok_elem(xb0 + T_BYTES, xb1 + T_BYTES, u),
+                               tok_elem(xb0 + T_BYTES, xb1 + T_BYTES, u + 1));
+      if (GENERAL) {
+        if (u >= valid) dyv.x = 0.0f;
+        if (u + 1 >= valid) dyv.y = 0.0f;
+      }
+      const float2 abar = ab[u / 2];
+      const float2 m = make_float2(m4[2 * q], m4[2 * q + 1]);
+      const float2 r = make_float2(r4[2 * q], r4[2 * q + 1]);
+      const float2 i = make_float2(i4[2 * q], i4[2 * q + 1]);
+      float2 gv;
+      gv.y = fmaf(anext, gnext, dyv.y);
+      gv.x = fmaf(abar.y, gv.y, dyv.x);
+      gnext = gv.x;
+      anext = abar.x;
+      const float2 uu = mul2(i, xv);
       // d h_t / d la = abar (h_{t-1} - u abar / m); zero at reset tokens (abar = 0), past T
       // and where the decay is exactly 1 (m = 0)
-      const float alpha = ((GENERAL && abar == 0.0f) || m == 0.0f)
-                              ? 0.0f
-                              : abar * (hp8[u] - uu * abar * rcp_approx(m));
-      const float dla = gv * alpha;
-      o_r[u] = dla * nk * r * (1.0f - r);
-      o_i[u] = gv * m * uu * (1.0f - i);
-      m8[u] = gv * m * i;  // direct dx term
-      dsp_acc = fmaf(dla, -8.0f * r, dsp_acc);
-      dba_acc += o_r[u];
-      dbx_acc += o_i[u];
-      gnext = gv;
-      abar_next = abar;
+      const float2 nrs = make_float2(-rcp_approx(m.x), -rcp_approx(m.y));
+      float2 alpha = mul2(abar, fma2(mul2(uu, abar), nrs, make_float2(h4[2 * q], h4[2 * q + 1])));
+      if ((GENERAL && abar.x == 0.0f) || m.x == 0.0f) alpha.x = 0.0f;
+      if ((GENERAL && abar.y == 0.0f) || m.y == 0.0f) alpha.y = 0.0f;
+      const float2 dla = mul2(gv, alpha);
+      const float2 gm = mul2(gv, m);
+      o_r[q] = mul2(mul2(dla, bc2(nk)), mul2(r, fma2(r, bc2(-1.0f), bc2(1.0f))));
+      o_i[q] = mul2(mul2(gm, uu), fma2(i, bc2(-1.0f), bc2(1.0f)));
+      const float2 dd = mul2(gm, i);  // direct dx term
+      dsp = fma2(dla, mul2(bc2(-8.0f), r), dsp);
+      dba = add2(dba, o_r[q]);
+      dbx = add2(dbx, o_i[q]);
+      h4[2 * q] = dd.x;
+      h4[2 * q + 1] = dd.y;
     }
-    const int t8 = (tb >> 3) + sub;  // 8-token group: 16-token group t8/2, half t8%2
-    store_dl8(s_dl, s_dl + T_BYTES, t8 >> 1, t8 & 1, j, o_r);
-    store_dl8(s_dl + 2 * T_BYTES, s_dl + 3 * T_BYTES, t8 >> 1, t8 & 1, j, o_i);
-    tc::tmem_st8(tcol + COL_DX + sub * 8, m8);
+    store_dl4(s_dl, s_dl + T_BYTES, part, g * GRP, j, o_r[0], o_r[1]);
+    store_dl4(s_dl + 2 * T_BYTES, s_dl + 3 * T_BYTES, part, g * GRP, j, o_i[0], o_i[1]);
+    tc::tmem_st4(tcol + COL_DX + g * GRP, h4);
   }
   tc::tmem_st_wait();
 }
@@ -240,8 +297,8 @@ __global__ void __maxnreg__(MAXREG)
                 const __grid_constant__ CUtensorMap tm_wa, const __grid_constant__ CUtensorMap tm_wx,
                 const __grid_constant__ CUtensorMap tm_dx, BwdParams p) {
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                             ~uintptr_t(1023));
+  // 1024-byte aligned base, formed by pointer arithmetic so that it stays a shared pointer
+  uint8_t* smem = smem_raw + ((1024u - (tc::smem_u32(smem_raw) & 1023u)) & 1023u);
   uint8_t* s_wa = smem;
   uint8_t* s_wx = smem + W_BYTES;
   uint8_t* s_in = smem + 2 * W_BYTES;               // stage s: x at s*2T, dy at s*2T + T
@@ -302,12 +359,12 @@ __global__ void __maxnreg__(MAXREG)
         tc::tma_load_2d(s_wa + g * SLAB_W, &tm_wa, w_full, 16 * g, blk * FUSED_K);
         tc::tma_load_2d(s_wx + g * SLAB_W, &tm_wx, w_full, 16 * g, blk * FUSED_K);
       }
-      for (int it = 0; it < my_tiles; ++it) {
-        const int n = rr + it * p.P;
+      TileWalk tw(rr, p.P, p.B);  // tw.c counts chunks from the last one
+      for (int it = 0; it < my_tiles; ++it, tw.next()) {
         const int st = it % STAGES;
         const uint32_t ph = (it / STAGES) & 1;
         if (!ctl.wait(&in_empty[st], ph ^ 1u)) continue;
-        const int c = p.nC - 1 - n / p.B, b = n % p.B;
+        const int c = p.nC - 1 - tw.c, b = tw.b;
         uint8_t* xs = s_in + st * 2 * T_BYTES;
         tc::mbar_expect_tx(&in_full[st], 2 * T_BYTES);
         for (int s = 0; s < FUSED_K / 16; ++s) {
@@ -402,7 +459,7 @@ __global__ void __maxnreg__(MAXREG)
     float2* agg = reinterpret_cast<float2*>(p.scratch + p.F.L.agg);
     const bool store_thread = (warp == 2 && lane == 0);
     if (store_thread) tc::prefetch_tmap(&tm_dx);
-    float dsp_acc = 0.0f, dba_acc = 0.0f, dbx_acc = 0.0f;
+    float2 dsp = bc2(0.0f), dba = bc2(0.0f), dbx = bc2(0.0f);
     const bool near_all = __all_sync(0xffffffffu, nk > -0.125f);
     // Channel j of a token row in a stage: 16-channel slab, 2-byte column, and the 16-byte half
     // of the 32-byte row (swapped on rows 4..7 of every 8 by the swizzle).
@@ -412,15 +469,19 @@ __global__ void __maxnreg__(MAXREG)
     // Software pipeline: iteration `it` runs pass 1 of tile it, then writes out the dx of tile
     // it - 1 (whose MMAs ran on the tensor cores during that pass 1), then the rest of tile it.
     // The last iteration only writes out the dx of the last tile.
+    TileWalk cur(rr, p.P, p.B);  // tile it; cur.c counts chunks from the last one
+    int pc = 0, pb = 0;          // chunk and row of tile it - 1
     for (int it = 0; it <= my_tiles; ++it) {
       const bool have = it < my_tiles;
       const int n = rr + it * p.P;
-      const int c = p.nC - 1 - n / p.B, b = n % p.B;
+      const int c = p.nC - 1 - cur.c, b = cur.b;
       const int st = it % STAGES;
       const uint32_t ph = (it / STAGES) & 1;
-      const uint8_t* xt = s_in + st * 2 * T_BYTES + tb * 32;
-      float ab[PT], iv[PT];
-      float fA = 1.0f, fB = 0.0f, rP = 1.0f, rS = 0.0f, hin_tile = 0.0f;
+      const uint32_t xt = tc::smem_u32(s_in + st * 2 * T_BYTES + tb * 32);
+      const uint32_t xb0 = xt + xoff0, xb1 = xt + xoff1;
+      float2 ab[PT / 2];
+      float P = 1.0f, fB = 0.0f, S = 0.0f;
+      float hin_tile = 0.0f;
       int valid = 0;
       bool fast = false;
       if (have) {
@@ -438,16 +499,14 @@ __global__ void __maxnreg__(MAXREG)
         ctl.wait(&in_full[st], ph);
         tc::tc_fence_after();
         if (fast)
-          bwd_pass1<false>(tcol, xt, xoff0, xoff1, nk, nbr, nbi, 0u, PT, ab, iv, fA, fB, rP, rS);
+          bwd_pass1<false>(tcol, xb0, xb1, nk, nbr, nbi, 0u, PT, ab, P, fB, S);
         else
-          bwd_pass1<true>(tcol, xt, xoff0, xoff1, nk, nbr, nbi, rmask, valid, ab, iv, fA, fB, rP,
-                          rS);
+          bwd_pass1<true>(tcol, xb0, xb1, nk, nbr, nbi, rmask, valid, ab, P, fB, S);
       }
 
       // dx of tile it - 1: TMEM -> smem [token][channel] as bf16 (float32 goes straight to HBM).
       if (it > 0) {
-        const int np = n - p.P;
-        const int cp = p.nC - 1 - np / p.B, bp = np % p.B;
+        const int cp = pc, bp = pb;
         const int validp = min(FUSED_C, p.T - cp * FUSED_C) - tb;
         ctl.wait(dx_full, (it - 1) & 1);
         tc::tc_fence_after();
@@ -470,15 +529,17 @@ __global__ void __maxnreg__(MAXREG)
         }
         tc::tc_fence_before();
       }
-      if (have) s_agg[part * FUSED_K + j] = make_float4(fA, fB, rP, rS);
+      if (have) s_agg[part * FUSED_K + j] = make_float4(P, fB, P, S);  // the part's maps
       tc::fence_proxy_async_smem();
       tc::named_bar(1, NSCAN * 32);  // barrier A: part aggregates and the dx staging
       if (it > 0 && store_thread && sizeof(GT) == 2) {
-        const int np = n - p.P;
-        tc::tma_store_3d(&tm_dx, s_dx, blk * FUSED_K, (p.nC - 1 - np / p.B) * FUSED_C, np % p.B);
+        tc::tma_store_3d(&tm_dx, s_dx, blk * FUSED_K, pc * FUSED_C, pb);
         tc::tma_store_commit();
       }
       if (!have) break;
+      pc = c;
+      pb = b;
+      cur.next();
 
       // Entry-state map of this part (earlier parts composed) and carry map from the tile's
       // right edge to this part (later parts composed).
@@ -504,47 +565,30 @@ __global__ void __maxnreg__(MAXREG)
       // published at once; the look-back slots are requested now and read after pass 2a.
       const size_t cidx = (size_t)b * p.nC + c;
       const bool publish = (blk * ntiles + n) != p.drop_tile;
-      const float tP = rP * Rp, tS = fmaf(rP, Rs, rS);
+      const float4 g0 = s_agg[j];
+      const float tP = g0.z * Rp, tS = fmaf(g0.z, Rs, g0.w);
       LookbackReq lbq;
       int lb_n = 0;
       const float2* lb_agg = agg;
-      const float* lb_anchor = rcar;
-      if (part == 0 && c < p.nC - 1) {
-        if (((p.nC - 1 - c) % ANCHOR) != 0 && publish) slot_put2(agg + cidx * p.W + w, tP, tS);
-        // nearest anchor after this chunk (anchors counted from the last chunk)
-        const int an = p.nC - 1 - ((p.nC - 2 - c) / ANCHOR) * ANCHOR;
-        lb_n = an - c - 1;
-        lb_agg = agg + (cidx + 1) * p.W + w;
-        lb_anchor = rcar + ((size_t)b * p.nC + an) * p.W + w;
-        lookback_issue(lbq, lb_agg, (long)p.W, lb_n, lb_anchor);
+      const float* lb_anchor = nullptr;
+      if (part == 0) {
+        if (publish) slot_put2(agg + cidx * p.W + w, tP, tS);
+        // chunks counted from the last one; the anchor passes on its carry to the left
+        const LookbackSpan sp = lookback_span(p.nC - 1 - c, p.lb_dist, p.lb_shift);
+        lb_n = sp.n;
+        if (c < p.nC - 1) lb_agg = agg + (cidx + 1) * p.W + w;
+        if (sp.anchor >= 0) lb_anchor = rcar + ((size_t)b * p.nC + (p.nC - 1 - sp.anchor)) * p.W + w;
+        lookback_issue(lbq, lb_agg, (long)p.W, lb_n, lb_anchor,
+                       p.dhT ? p.dhT[(size_t)b * p.W + w] : 0.0f);
       }
 
-      // Pass 2a: h_{t-1} through the part, parked in TMEM.
-      {
-        float h = fmaf(Fa, hin_tile, Fb);  // state entering this part
-#pragma unroll
-        for (int sub = 0; sub < PT / 8; ++sub) {
-          float m8[8], hp8[8];
-          tc::tmem_ld8(tcol + COL_LR + sub * 8, m8);
-          tc::tmem_ld_wait();
-#pragma unroll
-          for (int u = 0; u < 8; ++u) {
-            const int tt = sub * 8 + u;
-            hp8[u] = h;
-            h = fmaf(ab[tt], h, m8[u] * (iv[tt] * tok_elem(xt, tt, xoff0, xoff1)));
-          }
-          tc::tmem_st8(tcol + COL_HP + sub * 8, hp8);
-        }
-        tc::tmem_st_wait();
-      }
+      // Pass 2a: h_{t-1} through the part, from the earlier parts' map applied to the tile's
+      // entry state.
+      bwd_pass2a(tcol, xb0, xb1, ab, fmaf(Fa, hin_tile, Fb));
 
       if (part == 0) {
-        float cin = 0.0f;
-        if (c == p.nC - 1) {
-          if (p.dhT) cin = p.dhT[(size_t)b * p.W + w];
-        } else {
-          cin = lookback_finish(lbq, lb_agg, (long)p.W, lb_n, lb_anchor, p.spin_limit, status);
-        }
+        const float cin =
+            lookback_finish(lbq, lb_agg, (long)p.W, lb_n, lb_anchor, p.spin_limit, status);
         const float cout = fmaf(tP, cin, tS);
         if (publish) slot_put1(rcar + cidx * p.W + w, cout);
         if (c == 0 && p.dh0) p.dh0[(size_t)b * p.W + w] = p.canonical ? cout : 0.0f;
@@ -558,11 +602,9 @@ __global__ void __maxnreg__(MAXREG)
       if (it > 0) ctl.wait(dl_empty, (it - 1) & 1);
       tc::tc_fence_after();
       if (fast)
-        bwd_pass2b<false>(tcol, tb, j, xt, xoff0, xoff1, nk, PT, ab, iv, cin, s_dl, dsp_acc,
-                          dba_acc, dbx_acc);
+        bwd_pass2b<false>(tcol, part, j, xb0, xb1, nk, PT, ab, cin, s_dl, dsp, dba, dbx);
       else
-        bwd_pass2b<true>(tcol, tb, j, xt, xoff0, xoff1, nk, valid, ab, iv, cin, s_dl, dsp_acc,
-                         dba_acc, dbx_acc);
+        bwd_pass2b<true>(tcol, part, j, xb0, xb1, nk, valid, ab, cin, s_dl, dsp, dba, dbx);
       tc::fence_proxy_async_smem();
       tc::tc_fence_before();
       __syncwarp();
@@ -577,9 +619,9 @@ __global__ void __maxnreg__(MAXREG)
     // Per-CTA, per-part partials of the per-channel sums.
     float* vp = reinterpret_cast<float*>(p.scratch + p.F.vec_part) +
                 ((size_t)blockIdx.x * NPART + part) * 3 * FUSED_K;
-    vp[j] = dsp_acc;
-    vp[FUSED_K + j] = dba_acc;
-    vp[2 * FUSED_K + j] = dbx_acc;
+    vp[j] = dsp.x + dsp.y;
+    vp[FUSED_K + j] = dba.x + dba.y;
+    vp[2 * FUSED_K + j] = dbx.x + dbx.y;
 
     // Per-CTA dW partials: lane j of the accumulators is input channel j; each part copies
     // 128 / NPART of the output-channel columns.
@@ -706,6 +748,9 @@ cudaError_t launch_fused_bwd(const Dims& d, const void* dy, const float* dhT, co
   p.F = fused_bwd_layout(d);
   p.spin_limit = spin_limit;
   p.drop_tile = drop_tile;
+  const LookbackPlan lp = lookback_plan(p.P, d.B);
+  p.lb_dist = lp.dist;
+  p.lb_shift = lp.shift;
   p.dx = dx;
   const size_t smem = SMEM_BYTES;
   auto kern = gf32 ? k_fused_bwd<float> : k_fused_bwd<bf16>;

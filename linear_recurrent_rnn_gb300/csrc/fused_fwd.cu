@@ -51,7 +51,7 @@ constexpr uint32_t SLAB_W = FUSED_K * 32;            // 16 out-channels x 128 in
 // parks its part's local states (16) and decay products (16) until the tile is finished.
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t PARK_COL = 256;
-constexpr int WAIT_LIMIT = 1 << 22;
+constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;  // 2 s: a pipeline wait never lasts this
 constexpr uint32_t XCH_BYTES = 2 * NPART * FUSED_K * 8;  // part maps of two tiles
 constexpr size_t SMEM_BYTES =
     2 * W_BYTES + XSTAGES * X_BYTES + Y_BYTES + XCH_BYTES + 256 + 1024;
@@ -69,6 +69,7 @@ struct FwdParams {
   uint8_t* scratch;
   ScanLayout L;
   int spin_limit, drop_tile;
+  int lb_dist, lb_shift;
 };
 
 struct Ctl {
@@ -78,59 +79,78 @@ struct Ctl {
   // kernel winds down in bounded time (with the failure recorded in the status word).
   __device__ bool wait(uint64_t* bar, uint32_t parity) const {
     if (*abort) return false;
-    if (tc::mbar_wait(bar, parity, WAIT_LIMIT)) return true;
+    if (tc::mbar_wait(bar, parity, WAIT_LIMIT_NS)) return true;
     *abort = 1u;
     atomicOr(status, STATUS_PIPE);
     return false;
   }
 };
 
-// Local scan of one scan thread's PT tokens from a zero state: hl = state after each token,
-// Ac = product of abar up to it, (rA, rh) = the part's map.  GENERAL handles resets, tokens
-// past T and decays with la <= -1/8; the fast variant (chosen warp-uniformly) has none.
+// Local scan of one scan thread's PT = 16 tokens from a zero state.  The pointwise work runs
+// on token pairs (u, u + 1) in the two lanes of f32x2 operations (adjacent TMEM columns land
+// in adjacent registers); the recurrence itself is a scalar chain.  The state after each token
+// (hl) and the product of abar up to it (Ac) are parked in TMEM as they are made, at columns
+// park + u and park + PT + u; (rA, rh) = the part's map.  GENERAL handles resets, tokens past
+// T and decays with la <= -1/8; the fast variant (chosen warp-uniformly) has none.
+constexpr int GRP = 8;  // tokens per TMEM load / store group
 template <bool GENERAL>
-__device__ __forceinline__ void local_scan(uint32_t t_lr, uint32_t t_li, const uint8_t* xs,
-                                           int tb, int xoff0, int xoff1, float nk, float nbr,
-                                           float nbi, uint32_t rmask, int valid, float (&hl)[PT],
-                                           float (&Ac)[PT], float& rh, float& rA) {
+__device__ __forceinline__ void local_scan(uint32_t t_lr, uint32_t t_li, uint32_t park,
+                                           uint32_t xb0, uint32_t xb1, float nk, float nbr,
+                                           float nbi, uint32_t rmask, int valid, float& rh,
+                                           float& rA) {
   rh = 0.0f;
   rA = 1.0f;
 #pragma unroll
-  for (int sub = 0; sub < PT / 16; ++sub) {
-    float vr[16], vi[16];
-    tc::tmem_ld16(t_lr + sub * 16, vr);
-    tc::tmem_ld16(t_li + sub * 16, vi);
+  for (int g = 0; g < PT / GRP; ++g) {
+    float vr[GRP], vi[GRP], oh[GRP], oa[GRP];
+    tc::tmem_ld8(t_lr + g * GRP, vr);
+    tc::tmem_ld8(t_li + g * GRP, vi);
     tc::tmem_ld_wait();
 #pragma unroll
-    for (int u = 0; u < 16; ++u) {
-      const int tt = sub * 16 + u;  // token within the part
-      const int tl = tb + tt;       // token within the tile
-      const float xv = __bfloat162float(*reinterpret_cast<const bf16*>(
-          xs + tl * 32 + (((tl >> 2) & 1) ? xoff1 : xoff0)));
-      const float r = sigmoid_nb(vr[u], nbr);
-      const float i = sigmoid_nb(vi[u], nbi);
-      float abar, om;
+    for (int q = 0; q < GRP / 2; ++q) {
+      const int u = g * GRP + 2 * q;  // tokens u, u + 1 of the part
+      const float2 xv = make_float2(tok_elem(xb0, xb1, u), tok_elem(xb0, xb1, u + 1));
+      const float2 r = sigmoid2_nb(make_float2(vr[2 * q], vr[2 * q + 1]), nbr);
+      const float2 i = sigmoid2_nb(make_float2(vi[2 * q], vi[2 * q + 1]), nbi);
+      const float2 la = mul2(bc2(nk), r);
+      float2 abar, om;
       if (GENERAL)
-        decay_fast(nk * r, abar, om);
+        decay_fast2(la, abar, om);
       else
-        decay_near(nk * r, abar, om);
-      float m = sqrt_fast(om);
+        decay_near2(la, abar, om);
+      float2 m = sqrt_fast2(om);
       if (GENERAL) {
-        if ((rmask >> tt) & 1u) {
-          abar = 0.0f;
-          m = 1.0f;
+        if ((rmask >> u) & 1u) {
+          abar.x = 0.0f;
+          m.x = 1.0f;
         }
-        if (tt >= valid) {
-          abar = 1.0f;
-          m = 0.0f;
+        if ((rmask >> (u + 1)) & 1u) {
+          abar.y = 0.0f;
+          m.y = 1.0f;
+        }
+        if (u >= valid) {
+          abar.x = 1.0f;
+          m.x = 0.0f;
+        }
+        if (u + 1 >= valid) {
+          abar.y = 1.0f;
+          m.y = 0.0f;
         }
       }
-      rh = fmaf(abar, rh, m * (i * xv));
-      rA *= abar;
-      hl[tt] = rh;
-      Ac[tt] = rA;
+      const float2 bv = mul2(m, mul2(i, xv));
+      rh = fmaf(abar.x, rh, bv.x);
+      rA *= abar.x;
+      oh[2 * q] = rh;
+      oa[2 * q] = rA;
+      rh = fmaf(abar.y, rh, bv.y);
+      rA *= abar.y;
+      oh[2 * q + 1] = rh;
+      oa[2 * q + 1] = rA;
     }
+    tc::tmem_st8(park + g * GRP, oh);
+    tc::tmem_st8(park + PT + g * GRP, oa);
   }
+  tc::tmem_st_wait();
 }
 
 __global__ void __maxnreg__(MAXREG)
@@ -138,8 +158,8 @@ __global__ void __maxnreg__(MAXREG)
                 const __grid_constant__ CUtensorMap tm_wx, const __grid_constant__ CUtensorMap tm_y,
                 FwdParams p) {
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                             ~uintptr_t(1023));
+  // 1024-byte aligned base, formed by pointer arithmetic so that it stays a shared pointer
+  uint8_t* smem = smem_raw + ((1024u - (tc::smem_u32(smem_raw) & 1023u)) & 1023u);
   uint8_t* s_wa = smem;
   uint8_t* s_wx = smem + W_BYTES;
   uint8_t* s_x = smem + 2 * W_BYTES;
@@ -194,15 +214,15 @@ __global__ void __maxnreg__(MAXREG)
         tc::tma_load_2d(s_wx + g * SLAB_W, &tm_wx, w_full, 16 * g, blk * FUSED_K);
       }
       int it = 0;
-      for (int n = rr; n < ntiles; n += p.P, ++it) {
+      TileWalk tw(rr, p.P, p.B);
+      for (int n = rr; n < ntiles; n += p.P, ++it, tw.next()) {
         const int st = it % XSTAGES;
         const uint32_t ph = (it / XSTAGES) & 1;
         if (!ctl.wait(&x_empty[st], ph ^ 1u)) continue;
-        const int c = n / p.B, b = n % p.B;
         tc::mbar_expect_tx(&x_full[st], X_BYTES);
         for (int s = 0; s < FUSED_K / 16; ++s)
           tc::tma_load_3d(s_x + st * X_BYTES + s * SLAB_X, &tm_x, &x_full[st],
-                          blk * FUSED_K + 16 * s, c * FUSED_C, b);
+                          blk * FUSED_K + 16 * s, tw.c * FUSED_C, tw.b);
       }
     }
   } else if (warp == 1) {
@@ -261,27 +281,26 @@ __global__ void __maxnreg__(MAXREG)
     // Warp-uniform: every channel of this warp has la > -1/8 on every token.
     const bool near_all = __all_sync(0xffffffffu, nk > -0.125f);
 
+    TileWalk cur(rr, p.P, p.B);  // tile it
+    int pc = 0, pb = 0;          // chunk and row of tile it - 1
     for (int it = 0; it <= my_tiles; ++it) {
       // Request tile it-1's look-back slots now; they are consumed after this tile's scan.
       LookbackReq lbq;
       int lb_n = 0;
       const float2* lb_agg = agg;
-      const float* lb_anchor = carry;
+      const float* lb_anchor = nullptr;
       if (it > 0) {
-        const int n = rr + (it - 1) * p.P;
-        const int c = n / p.B, b = n % p.B;
-        if (c > 0) {
-          const size_t cidx = (size_t)b * p.nC + c;
-          const int an = ((c - 1) / ANCHOR) * ANCHOR;  // nearest anchor before this chunk
-          lb_n = c - 1 - an;
-          lb_agg = agg + (cidx - 1) * p.W + w;
-          lb_anchor = carry + ((size_t)b * (p.nC + 1) + an + 1) * p.W + w;
-          lookback_issue(lbq, lb_agg, -(long)p.W, lb_n, lb_anchor);
-        }
+        const int c = pc, b = pb;
+        const LookbackSpan sp = lookback_span(c, p.lb_dist, p.lb_shift);
+        lb_n = sp.n;
+        if (c > 0) lb_agg = agg + ((size_t)b * p.nC + c - 1) * p.W + w;
+        // the anchor's boundary state (the state entering chunk anchor + 1), or h0
+        if (sp.anchor >= 0) lb_anchor = carry + ((size_t)b * (p.nC + 1) + sp.anchor + 1) * p.W + w;
+        const float init = (p.canonical && p.h0) ? p.h0[(size_t)b * p.W + w] : 0.0f;
+        lookback_issue(lbq, lb_agg, -(long)p.W, lb_n, lb_anchor, init);
       }
       if (it < my_tiles) {
-        const int n = rr + it * p.P;
-        const int c = n / p.B, b = n % p.B;
+        const int c = cur.c, b = cur.b;
         const int st = it % XSTAGES;
         const uint32_t ph = (it / XSTAGES) & 1;
         const int a = it & 1;
@@ -298,26 +317,22 @@ __global__ void __maxnreg__(MAXREG)
                                                           (size_t)b * p.T + t));
         }
         const int valid = min(FUSED_C, p.T - c * FUSED_C) - tb;  // tokens of this part < T
-        const uint8_t* xs = s_x + st * X_BYTES;
+        const uint32_t xt = tc::smem_u32(s_x + st * X_BYTES + tb * 32);
+        const uint32_t xb0 = xt + xoff0, xb1 = xt + xoff1;
         const uint32_t t_lr = tmem + lane_base + a * 128 + tb;
-        float hl[PT], Ac[PT], rh, rA;
-        if (near_all && rmask == 0u && valid >= PT)
-          local_scan<false>(t_lr, t_lr + 64, xs, tb, xoff0, xoff1, nk, nbr, nbi, rmask, valid,
-                            hl, Ac, rh, rA);
-        else
-          local_scan<true>(t_lr, t_lr + 64, xs, tb, xoff0, xoff1, nk, nbr, nbi, rmask, valid,
-                           hl, Ac, rh, rA);
         const uint32_t park = tmem + lane_base + PARK_COL + a * 128 + part * 2 * PT;
-        tc::tmem_st16(park, hl);
-        tc::tmem_st16(park + PT, Ac);
-        tc::tmem_st_wait();
+        float rh, rA;
+        if (near_all && rmask == 0u && valid >= PT)
+          local_scan<false>(t_lr, t_lr + 64, park, xb0, xb1, nk, nbr, nbi, 0u, PT, rh, rA);
+        else
+          local_scan<true>(t_lr, t_lr + 64, park, xb0, xb1, nk, nbr, nbi, rmask, valid, rh, rA);
         tc::tc_fence_before();
         __syncwarp();
         if (lane == 0) {
           tc::mbar_arrive(&acc_empty[a]);
           tc::mbar_arrive(&x_empty[st]);
         }
-        s_agg[(a * NPART + part) * FUSED_K + j] = make_float2(rA, rh);
+        s_agg[(a * NPART + part) * FUSED_K + j] = make_float2(rA, rh);  // the part's map
       }
       if (store_thread) tc::tma_store_wait_read0();  // the y staging is free again
       tc::named_bar(1, NSCAN * 32);
@@ -325,9 +340,9 @@ __global__ void __maxnreg__(MAXREG)
       // Publish tile it's map at once (the last part, from all parts' maps).
       if (it < my_tiles && part == NPART - 1) {
         const int n = rr + it * p.P;
-        const int c = n / p.B, b = n % p.B;
+        const int c = cur.c, b = cur.b;
         const int a = it & 1;
-        if (c > 0 && (c % ANCHOR) != 0 && (blk * ntiles + n) != p.drop_tile) {
+        if ((blk * ntiles + n) != p.drop_tile) {
           float At = 1.0f, Bt = 0.0f;
 #pragma unroll
           for (int pp = 0; pp < NPART; ++pp) {
@@ -343,7 +358,7 @@ __global__ void __maxnreg__(MAXREG)
       // look-back and the output), the last part publishes the chunk-boundary state.
       if (it > 0) {
         const int n = rr + (it - 1) * p.P;
-        const int c = n / p.B, b = n % p.B;
+        const int c = pc, b = pb;
         const int a = (it - 1) & 1;
         float Ae = 1.0f, Be = 0.0f, At = 1.0f, Bt = 0.0f;
 #pragma unroll
@@ -356,12 +371,8 @@ __global__ void __maxnreg__(MAXREG)
           Bt = fmaf(g.x, Bt, g.y);
           At *= g.x;
         }
-        float hin_t = 0.0f;
-        if (c == 0) {
-          if (p.canonical && p.h0) hin_t = p.h0[(size_t)b * p.W + w];
-        } else {
-          hin_t = lookback_finish(lbq, lb_agg, -(long)p.W, lb_n, lb_anchor, p.spin_limit, status);
-        }
+        const float hin_t =
+            lookback_finish(lbq, lb_agg, -(long)p.W, lb_n, lb_anchor, p.spin_limit, status);
         if (part == NPART - 1) {
           const float hend = fmaf(At, hin_t, Bt);
           float* crow = carry + (size_t)b * (p.nC + 1) * p.W;
@@ -375,19 +386,25 @@ __global__ void __maxnreg__(MAXREG)
         tc::tmem_ld16(park, hl);
         tc::tmem_ld16(park + PT, Ac);
         tc::tmem_ld_wait();
-        // y tile: registers -> smem [token][channel] -> TMA store (clipped at T).
+        // y tile: registers -> smem [token][channel] -> TMA store (clipped at T)
 #pragma unroll
-        for (int tt = 0; tt < PT; ++tt)
-          *reinterpret_cast<bf16*>(s_y + (tb + tt) * (FUSED_K * 2) + j * 2) =
-              __float2bfloat16_rn(fmaf(Ac[tt], hin, hl[tt]));
+        for (int u = 0; u < PT; u += 2) {
+          const float2 yv =
+              fma2(make_float2(Ac[u], Ac[u + 1]), bc2(hin), make_float2(hl[u], hl[u + 1]));
+          *reinterpret_cast<bf16*>(s_y + (tb + u) * (FUSED_K * 2) + j * 2) = __float2bfloat16_rn(yv.x);
+          *reinterpret_cast<bf16*>(s_y + (tb + u + 1) * (FUSED_K * 2) + j * 2) =
+              __float2bfloat16_rn(yv.y);
+        }
         tc::fence_proxy_async_smem();
       }
       tc::named_bar(1, NSCAN * 32);
       if (it > 0 && store_thread) {
-        const int n = rr + (it - 1) * p.P;
-        tc::tma_store_3d(&tm_y, s_y, blk * FUSED_K, (n / p.B) * FUSED_C, n % p.B);
+        tc::tma_store_3d(&tm_y, s_y, blk * FUSED_K, pc * FUSED_C, pb);
         tc::tma_store_commit();
       }
+      pc = cur.c;
+      pb = cur.b;
+      cur.next();
     }
     if (store_thread) tc::tma_store_wait0();
   }
@@ -477,6 +494,9 @@ cudaError_t launch_fused_fwd(const Dims& d, const void* x, const void* Wa, const
   p.L = fused_layout(d, false);
   p.spin_limit = spin_limit;
   p.drop_tile = drop_tile;
+  const LookbackPlan lp = lookback_plan(p.P, d.B);
+  p.lb_dist = lp.dist;
+  p.lb_shift = lp.shift;
   e = cudaFuncSetAttribute(k_fused_fwd, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)SMEM_BYTES);
   if (e != cudaSuccess) return e;

@@ -65,6 +65,24 @@ constexpr int FUSED_K = 128;
 constexpr int FUSED_C = 64;
 
 inline int fused_chunks(const Dims& d) { return (d.T + FUSED_C - 1) / FUSED_C; }
+
+// Look-back of the fused kernels (lookback.cuh): at most LB_SLOTS aggregates per look-back.
+// The anchor is at least `dist` chunks back, dist = ceil(P / B) with P CTAs sharing a gate
+// block's B * nC tiles in chunk order, so that the anchor's tile came at least one round of
+// the tile loop earlier; anchors are every 2^shift chunks, the largest power of two with
+// dist + 2^shift - 2 <= LB_SLOTS.
+constexpr int LB_SLOTS = 8;
+struct LookbackPlan {
+  int dist, shift;
+};
+inline LookbackPlan lookback_plan(int P, int B) {
+  int dist = (P + B - 1) / B;
+  if (dist < 1) dist = 1;
+  if (dist > LB_SLOTS + 1) dist = LB_SLOTS + 1;
+  int shift = 0;
+  while (dist + (2 << shift) - 2 <= LB_SLOTS) ++shift;
+  return {dist, shift};
+}
 inline ScanLayout fused_layout(const Dims& d, bool backward) {
   return scan_layout_n(d.B, fused_chunks(d), d.ng, d.W, backward);
 }

@@ -1,10 +1,13 @@
 // Anchored look-back over value slots (see common.cuh), shared by the fused kernels.
 //
-// The carry entering a chunk is  compose(agg[k_1], ..., agg[k_n]) applied to the boundary
-// state published by the nearest anchor chunk, where k_1 is the neighbouring chunk and k_n the
-// one next to the anchor.  All n aggregate slots and the anchor's slot are requested at once
-// (n <= ANCHOR - 1), so the wait costs about one L2 round trip when the slots are already
-// filled; an empty slot is re-polled with a bounded spin.
+// Chunks are counted in processing order (from the start in the forward, from the end in the
+// backward): chunk q publishes its affine aggregate and, once it knows its carry-in, the carry
+// it passes on.  Its own carry-in is compose(agg[q-1], ..., agg[a+1]) applied to the carry
+// passed on by the anchor chunk a, the nearest multiple of 2^shift at least `dist` chunks
+// back (or, for q < dist, to the initial value: h0 or dh_T).  Every carry is thus one fixed
+// expression of the inputs, whatever the timing, so the scan is bitwise deterministic; and
+// with dist = ceil(P / B) the anchor's tile sits at least one full round of the CTAs' tile
+// loop earlier, so its carry is normally published well before it is read.
 #pragma once
 
 #include "common.cuh"
@@ -12,115 +15,73 @@
 
 namespace rglru {
 
-// Split form: lookback_issue requests every slot at once (and returns immediately); the values
-// are consumed later by lookback_finish, which re-polls the slots that were still empty.  A
-// caller issues the requests, does other work, then finishes: the L2 round trip is hidden.
+// The slots of one look-back are all requested at once (lookback_issue, which returns at
+// once), consumed later (lookback_finish, which re-polls any slot that was still empty): the
+// L2 round trip hides behind the work in between.
 struct LookbackReq {
-  uint64_t v[ANCHOR - 1];
+  uint64_t v[LB_SLOTS];
   uint32_t hv;
 };
 
-__device__ __forceinline__ void lookback_issue(LookbackReq& q, const float2* first_agg,
-                                               long agg_step, int n, const float* anchor_state) {
-#pragma unroll
-  for (int s = 0; s < ANCHOR - 1; ++s)
-    q.v[s] = s < n ? ld_relaxed_u64(first_agg + s * agg_step) : 0ull;
-  q.hv = ld_relaxed_u32(anchor_state);
+// Where chunk q (processing order) looks back to: n = aggregates to compose, anchor = the
+// processing-order index of the anchor chunk (-1: the initial value).
+struct LookbackSpan {
+  int n, anchor;
+};
+__device__ __forceinline__ LookbackSpan lookback_span(int q, int dist, int shift) {
+  LookbackSpan s;
+  s.anchor = q >= dist ? ((q - dist) >> shift) << shift : -1;
+  s.n = q - 1 - s.anchor;
+  return s;
 }
 
+// first_agg: slot of chunk q-1 (processing order); agg_step: element offset to the next older
+// chunk's slot; anchor_state: the anchor's carry slot, or null to use init (the initial value).
+__device__ __forceinline__ void lookback_issue(LookbackReq& q, const float2* first_agg,
+                                               long agg_step, int n, const float* anchor_state,
+                                               float init) {
+#pragma unroll
+  for (int s = 0; s < LB_SLOTS; ++s)
+    q.v[s] = s < n ? ld_relaxed_u64(first_agg + s * agg_step) : 0ull;
+  q.hv = anchor_state ? ld_relaxed_u32(anchor_state) : __float_as_uint(init);
+}
+
+// A slot that stays empty past `limit` polls counts as the identity (or a zero carry), and the
+// timeout is recorded in *status.  Every slot still empty is re-requested in the same round,
+// so a round costs one L2 round trip however many slots were late.
 __device__ __forceinline__ float lookback_finish(LookbackReq& q, const float2* first_agg,
                                                  long agg_step, int n, const float* anchor_state,
                                                  int limit, uint32_t* status) {
+  for (int round = 0;; ++round) {
+    bool pending = anchor_state != nullptr && q.hv == SLOT_EMPTY32;
 #pragma unroll
-  for (int s = 0; s < ANCHOR - 1; ++s) {
-    if (s < n) {
-      int it = 0;
-      while (q.v[s] == SLOT_EMPTY64) {
-        if (++it > limit) {
-          atomicOr(status, STATUS_TIMEOUT);
-          q.v[s] = (uint64_t)__float_as_uint(1.0f);  // identity (A = 1, B = 0)
-          break;
-        }
-        __nanosleep(64);
-        q.v[s] = ld_relaxed_u64(first_agg + s * agg_step);
-      }
-    }
-  }
-  {
-    int it = 0;
-    while (q.hv == SLOT_EMPTY32) {
-      if (++it > limit) {
-        atomicOr(status, STATUS_TIMEOUT);
-        q.hv = 0u;
-        break;
-      }
-      __nanosleep(64);
-      q.hv = ld_relaxed_u32(anchor_state);
-    }
-  }
-  float accA = 1.0f, accB = 0.0f;
+    for (int s = 0; s < LB_SLOTS; ++s) pending |= s < n && q.v[s] == SLOT_EMPTY64;
+    if (!pending) break;
+    if (round >= limit) {
+      atomicOr(status, STATUS_TIMEOUT);
 #pragma unroll
-  for (int s = 0; s < ANCHOR - 1; ++s) {
+      for (int s = 0; s < LB_SLOTS; ++s)
+        if (q.v[s] == SLOT_EMPTY64) q.v[s] = (uint64_t)__float_as_uint(1.0f);  // A = 1, B = 0
+      if (q.hv == SLOT_EMPTY32) q.hv = 0u;
+      break;
+    }
+    __nanosleep(32);
+#pragma unroll
+    for (int s = 0; s < LB_SLOTS; ++s)
+      if (s < n && q.v[s] == SLOT_EMPTY64) q.v[s] = ld_relaxed_u64(first_agg + s * agg_step);
+    if (anchor_state != nullptr && q.hv == SLOT_EMPTY32) q.hv = ld_relaxed_u32(anchor_state);
+  }
+  // compose from the anchor's side: the oldest aggregate first
+  float c = __uint_as_float(q.hv);
+#pragma unroll
+  for (int s = LB_SLOTS - 1; s >= 0; --s) {
     if (s < n) {
       const float A = __uint_as_float((uint32_t)(q.v[s] & 0xffffffffu));
       const float B = __uint_as_float((uint32_t)(q.v[s] >> 32));
-      accB = fmaf(accA, B, accB);
-      accA *= A;
+      c = fmaf(A, c, B);
     }
   }
-  return fmaf(accA, __uint_as_float(q.hv), accB);
-}
-
-// first_agg: slot of k_1; agg_step: element offset from k_i to k_{i+1} (+-W); n: number of
-// aggregates to compose; anchor_state: slot of the anchor's boundary state.  A slot that
-// stays empty past `limit` polls counts as the identity (or a zero state), and the timeout is
-// recorded in *status.
-__device__ __forceinline__ float lookback_carry(const float2* first_agg, long agg_step, int n,
-                                                const float* anchor_state, int limit,
-                                                uint32_t* status) {
-  uint64_t v[ANCHOR - 1];
-#pragma unroll
-  for (int s = 0; s < ANCHOR - 1; ++s)
-    v[s] = s < n ? ld_relaxed_u64(first_agg + s * agg_step) : 0ull;
-  uint32_t hv = ld_relaxed_u32(anchor_state);
-#pragma unroll
-  for (int s = 0; s < ANCHOR - 1; ++s) {
-    if (s < n) {
-      int it = 0;
-      while (v[s] == SLOT_EMPTY64) {
-        if (++it > limit) {
-          atomicOr(status, STATUS_TIMEOUT);
-          v[s] = (uint64_t)__float_as_uint(1.0f);  // identity (A = 1, B = 0)
-          break;
-        }
-        __nanosleep(64);
-        v[s] = ld_relaxed_u64(first_agg + s * agg_step);
-      }
-    }
-  }
-  {
-    int it = 0;
-    while (hv == SLOT_EMPTY32) {
-      if (++it > limit) {
-        atomicOr(status, STATUS_TIMEOUT);
-        hv = 0u;
-        break;
-      }
-      __nanosleep(64);
-      hv = ld_relaxed_u32(anchor_state);
-    }
-  }
-  float accA = 1.0f, accB = 0.0f;
-#pragma unroll
-  for (int s = 0; s < ANCHOR - 1; ++s) {
-    if (s < n) {
-      const float A = __uint_as_float((uint32_t)(v[s] & 0xffffffffu));
-      const float B = __uint_as_float((uint32_t)(v[s] >> 32));
-      accB = fmaf(accA, B, accB);
-      accA *= A;
-    }
-  }
-  return fmaf(accA, __uint_as_float(hv), accB);
+  return c;
 }
 
 }  // namespace rglru

@@ -283,6 +283,49 @@ def test_lookback_timeout_is_reported():
     assert_close("y", host(y), yr, io="bf16", kind="out")
 
 
+@pytest.mark.parametrize("which", ["forward", "backward"])
+def test_fused_lookback_timeout_is_reported(which):
+    """The fused tensor-core kernels: a tile that never publishes its aggregate and carry makes
+    the later chunks' bounded look-back waits run out; the call finishes and the status word of
+    its scratch reports the timeout.  One gate block of 128 channels and 12 chunks, so every
+    tile has a CTA of its own and the dropped tile (chunk 5) lies inside its successors'
+    look-back windows."""
+    wl = W_("timeout-fused", 1, 12 * 64, 128, 128, "bf16", "restricted")
+    inp = generate(wl, 45)
+    sh = shape_for(wl)
+    d = {k: dev(v) for k, v in inp.items()}
+    y = torch.empty_like(d["x"])
+    saved = R.alloc_saved(sh)
+    ws = R.alloc_workspace(sh)
+    dx = torch.empty_like(d["x"])
+    dW = [torch.empty(1, 128, 128, device="cuda") for _ in range(2)]
+    dv = [torch.empty(128, device="cuda") for _ in range(3)]
+
+    def fwd():
+        R.rglru_fused_forward(sh, d["x"], d["Wa"], d["ba"], d["Wx"], d["bx"], d["Lambda"], None,
+                              None, None, y, None, saved)
+
+    def bwd():
+        R.rglru_fused_backward(sh, d["dy"], None, d["x"], d["Wa"], d["ba"], d["Wx"], d["bx"],
+                               d["Lambda"], None, None, None, saved, dx, dW[0], dv[0], dW[1],
+                               dv[1], dv[2], None, ws)
+
+    if which == "backward":
+        fwd()
+        assert R.rglru_sync_status(saved) == R.OK
+    R.rglru_debug_lookback(2000, 5)
+    try:
+        (fwd if which == "forward" else bwd)()
+        buf = saved if which == "forward" else ws
+        assert R.rglru_sync_status(buf) == R.ERR_TIMEOUT
+    finally:
+        R.rglru_debug_lookback(0, -1)
+    fwd()
+    bwd()
+    assert R.rglru_sync_status(saved) == R.OK
+    assert R.rglru_sync_status(ws) == R.OK
+
+
 def test_invalid_arguments_rejected_on_gpu():
     wl = W_("bad", 1, 8, 64, 64, "bf16", "restricted")
     sh = shape_for(wl)
