@@ -168,8 +168,14 @@ __device__ __forceinline__ void decay_fast2(float2 la, float2& a, float2& om) {
     om.y = fmaf(-ax, ax, 1.0f);
   }
 }
+// sqrt of two values >= 0, one special-function op each (PTX sqrt.approx, 0 at 0).
+__device__ __forceinline__ float sqrt_approx(float v) {
+  float y;
+  asm("sqrt.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(v));
+  return y;
+}
 __device__ __forceinline__ float2 sqrt_fast2(float2 v) {
-  return make_float2(sqrt_fast(v.x), sqrt_fast(v.y));
+  return make_float2(sqrt_approx(v.x), sqrt_approx(v.y));
 }
 
 // ---------------------------------------------------------------- staged bf16 tiles

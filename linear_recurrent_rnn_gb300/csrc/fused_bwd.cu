@@ -68,6 +68,7 @@ constexpr uint32_t XCH_BYTES = NPART * FUSED_K * 16 + FUSED_K * 4;  // part aggr
 constexpr size_t SMEM_BYTES =
     2 * W_BYTES + STAGES * 2 * T_BYTES + 4 * T_BYTES + T_BYTES + XCH_BYTES + 256 + 1024;
 constexpr uint32_t STATUS_PIPE = 2u;
+constexpr int BAR_SCAN = 1;  // named barrier of the scan warps
 
 struct BwdParams {
   int B, T, W, nblk, nC, P, canonical;
@@ -377,20 +378,22 @@ __global__ void __maxnreg__(MAXREG)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t id_lg = tc::idesc_bf16(128, FUSED_C, 1, 0);    // W^T x^T
-      constexpr uint32_t id_dx = tc::idesc_bf16(128, FUSED_C, 0, 1);    // W dl^T
-      constexpr uint32_t id_dw = tc::idesc_bf16(128, FUSED_K, 1, 0);    // x^T dl
-      ctl.wait(w_full, 0);
-      const uint32_t wa = tc::smem_u32(s_wa), wx = tc::smem_u32(s_wx);
-      const uint32_t dl0 = tc::smem_u32(s_dl);
-      auto logits = [&](int it) {
-        const int st = it % STAGES;
-        const uint32_t ph = (it / STAGES) & 1;
-        if (!ctl.wait(lg_empty, (it & 1) ^ 1u)) return;
-        if (!ctl.wait(&in_full[st], ph)) return;
-        tc::tc_fence_after();
-        const uint32_t xs = tc::smem_u32(s_in + st * 2 * T_BYTES);
+    // The whole warp runs the loop (the descriptor arithmetic stays warp-uniform); one elected
+    // lane issues the MMAs and commits.
+    const bool leader = tc::elect_one();
+    constexpr uint32_t id_lg = tc::idesc_bf16(128, FUSED_C, 1, 0);  // W^T x^T
+    constexpr uint32_t id_dx = tc::idesc_bf16(128, FUSED_C, 0, 1);  // W dl^T
+    constexpr uint32_t id_dw = tc::idesc_bf16(128, FUSED_K, 1, 0);  // x^T dl
+    ctl.wait(w_full, 0);
+    const uint32_t wa = tc::smem_u32(s_wa), wx = tc::smem_u32(s_wx);
+    const uint32_t dl0 = tc::smem_u32(s_dl);
+    auto logits = [&](int it) {
+      const int st = it % STAGES;
+      if (!ctl.wait(lg_empty, (it & 1) ^ 1u)) return;
+      if (!ctl.wait(&in_full[st], (it / STAGES) & 1)) return;
+      tc::tc_fence_after();
+      const uint32_t xs = tc::smem_u32(s_in + st * 2 * T_BYTES);
+      if (leader) {
 #pragma unroll
         for (int kk = 0; kk < FUSED_K / 16; ++kk) {
           const uint64_t bdesc = tc::smem_desc_sw32(xs + kk * SLAB_X, 16, 256);
@@ -400,13 +403,16 @@ __global__ void __maxnreg__(MAXREG)
                        id_lg, kk > 0);
         }
         tc::mma_commit(lg_full);
-      };
-      if (my_tiles > 0) logits(0);
-      for (int it = 0; it < my_tiles; ++it) {
-        if (it + 1 < my_tiles) logits(it + 1);
-        const int st = it % STAGES;
-        if (!ctl.wait(dl_full, it & 1)) continue;
-        tc::tc_fence_after();
+      }
+      __syncwarp();
+    };
+    if (my_tiles > 0) logits(0);
+    for (int it = 0; it < my_tiles; ++it) {
+      if (it + 1 < my_tiles) logits(it + 1);
+      const int st = it % STAGES;
+      if (!ctl.wait(dl_full, it & 1)) continue;
+      tc::tc_fence_after();
+      if (leader) {
         // dx^T[in][tok] += W[in][out] dl^T[out][tok]: A = W K-major (one 16-column slab per K
         // step), B = dl buffer MN-major (16-token groups 4 KB apart, 8-row groups 256 B).
 #pragma unroll
@@ -414,12 +420,12 @@ __global__ void __maxnreg__(MAXREG)
           const uint64_t a_a = tc::smem_desc_sw32(wa + kk * SLAB_W, 16, 256);
           const uint64_t a_x = tc::smem_desc_sw32(wx + kk * SLAB_W, 16, 256);
 #pragma unroll
-          for (int part = 0; part < 2; ++part) {  // hi, then lo halves of dl
+          for (int h = 0; h < 2; ++h) {  // hi, then lo halves of dl
             tc::mma_bf16(tmem + COL_DX, a_a,
-                         tc::smem_desc_sw32(dl0 + (0 + part) * T_BYTES + kk * 512, SLAB_D, 256),
+                         tc::smem_desc_sw32(dl0 + (0 + h) * T_BYTES + kk * 512, SLAB_D, 256),
                          id_dx, 1);
             tc::mma_bf16(tmem + COL_DX, a_x,
-                         tc::smem_desc_sw32(dl0 + (2 + part) * T_BYTES + kk * 512, SLAB_D, 256),
+                         tc::smem_desc_sw32(dl0 + (2 + h) * T_BYTES + kk * 512, SLAB_D, 256),
                          id_dx, 1);
           }
         }
@@ -443,6 +449,7 @@ __global__ void __maxnreg__(MAXREG)
         tc::mma_commit(dl_empty);
         tc::mma_commit(&in_empty[st]);
       }
+      __syncwarp();
     }
   } else {
     // ------------------------------------------------------------ scan warps
@@ -484,6 +491,22 @@ __global__ void __maxnreg__(MAXREG)
       float hin_tile = 0.0f;
       int valid = 0;
       bool fast = false;
+      // Part 0 requests the look-back slots of this tile's carry from the right now; they are
+      // read after pass 2a, so the L2 round trip hides behind passes 1 and 2a.
+      const size_t cidx = (size_t)b * p.nC + c;
+      LookbackReq lbq;
+      int lb_n = 0;
+      const float2* lb_agg = agg;
+      const float* lb_anchor = nullptr;
+      if (have && part == 0) {
+        // chunks counted from the last one; the anchor passes on its carry to the left
+        const LookbackSpan sp = lookback_span(p.nC - 1 - c, p.lb_dist, p.lb_shift);
+        lb_n = sp.n;
+        if (c < p.nC - 1) lb_agg = agg + (cidx + 1) * p.W + w;
+        if (sp.anchor >= 0) lb_anchor = rcar + ((size_t)b * p.nC + (p.nC - 1 - sp.anchor)) * p.W + w;
+        lookback_issue(lbq, lb_agg, (long)p.W, lb_n, lb_anchor,
+                       p.dhT ? p.dhT[(size_t)b * p.W + w] : 0.0f);
+      }
       if (have) {
         hin_tile = p.fwd_carry[((size_t)b * (p.nC + 1) + c) * p.W + w];
         uint32_t rmask = 0;
@@ -531,7 +554,7 @@ __global__ void __maxnreg__(MAXREG)
       }
       if (have) s_agg[part * FUSED_K + j] = make_float4(P, fB, P, S);  // the part's maps
       tc::fence_proxy_async_smem();
-      tc::named_bar(1, NSCAN * 32);  // barrier A: part aggregates and the dx staging
+      tc::named_bar(BAR_SCAN, NSCAN * 32);  // barrier A: part aggregates and the dx staging
       if (it > 0 && store_thread && sizeof(GT) == 2) {
         tc::tma_store_3d(&tm_dx, s_dx, blk * FUSED_K, pc * FUSED_C, pb);
         tc::tma_store_commit();
@@ -562,25 +585,11 @@ __global__ void __maxnreg__(MAXREG)
       }
 
       // Part 0 owns the chunk's reverse carry: its map after the later parts' is the tile's,
-      // published at once; the look-back slots are requested now and read after pass 2a.
-      const size_t cidx = (size_t)b * p.nC + c;
+      // published at once.
       const bool publish = (blk * ntiles + n) != p.drop_tile;
       const float4 g0 = s_agg[j];
       const float tP = g0.z * Rp, tS = fmaf(g0.z, Rs, g0.w);
-      LookbackReq lbq;
-      int lb_n = 0;
-      const float2* lb_agg = agg;
-      const float* lb_anchor = nullptr;
-      if (part == 0) {
-        if (publish) slot_put2(agg + cidx * p.W + w, tP, tS);
-        // chunks counted from the last one; the anchor passes on its carry to the left
-        const LookbackSpan sp = lookback_span(p.nC - 1 - c, p.lb_dist, p.lb_shift);
-        lb_n = sp.n;
-        if (c < p.nC - 1) lb_agg = agg + (cidx + 1) * p.W + w;
-        if (sp.anchor >= 0) lb_anchor = rcar + ((size_t)b * p.nC + (p.nC - 1 - sp.anchor)) * p.W + w;
-        lookback_issue(lbq, lb_agg, (long)p.W, lb_n, lb_anchor,
-                       p.dhT ? p.dhT[(size_t)b * p.W + w] : 0.0f);
-      }
+      if (part == 0 && publish) slot_put2(agg + cidx * p.W + w, tP, tS);
 
       // Pass 2a: h_{t-1} through the part, from the earlier parts' map applied to the tile's
       // entry state.
@@ -595,7 +604,7 @@ __global__ void __maxnreg__(MAXREG)
         s_cin[j] = cin;
       }
       if (store_thread) tc::tma_store_wait_read0();  // dx staging free for the next iteration
-      tc::named_bar(1, NSCAN * 32);                   // barrier B: the tile's right carry
+      tc::named_bar(BAR_SCAN, NSCAN * 32);                   // barrier B: the tile's right carry
       const float cin = fmaf(Rp, s_cin[j], Rs);      // carry into this part from the right
 
       // The dl buffers are free once the previous tile's MMAs are done.

@@ -227,7 +227,10 @@ __global__ void __maxnreg__(MAXREG)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    // The whole warp runs the loop (the descriptor arithmetic stays warp-uniform); one elected
+    // lane issues the MMAs and commits.
+    const bool leader = tc::elect_one();
+    {
       constexpr uint32_t idesc = tc::idesc_bf16(128, FUSED_C, /*A MN-major*/ 1, /*B K-major*/ 0);
       ctl.wait(w_full, 0);
       const uint32_t wa = tc::smem_u32(s_wa), wx = tc::smem_u32(s_wx);
@@ -247,10 +250,10 @@ __global__ void __maxnreg__(MAXREG)
           // A: W^T, MN-major, 16-channel groups 4 KB apart (LBO), 8-row K groups 256 B (SBO);
           // B: x tile, K-major, one 16-channel slab per K step, 8-row groups 256 B apart.
           const uint64_t bdesc = tc::smem_desc_sw32(xs + kk * SLAB_X, 16, 256);
-          tc::mma_bf16(d_r, tc::smem_desc_sw32(wa + kk * 512, SLAB_W, 256), bdesc, idesc, kk > 0);
-          tc::mma_bf16(d_i, tc::smem_desc_sw32(wx + kk * 512, SLAB_W, 256), bdesc, idesc, kk > 0);
+          if (leader) tc::mma_bf16(d_r, tc::smem_desc_sw32(wa + kk * 512, SLAB_W, 256), bdesc, idesc, kk > 0);
+          if (leader) tc::mma_bf16(d_i, tc::smem_desc_sw32(wx + kk * 512, SLAB_W, 256), bdesc, idesc, kk > 0);
         }
-        tc::mma_commit(&acc_full[a]);
+        if (leader) tc::mma_commit(&acc_full[a]);
       }
     }
   } else {

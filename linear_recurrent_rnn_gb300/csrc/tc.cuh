@@ -124,8 +124,15 @@ __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
 }
 
 // ---------------------------------------------------------------- named barriers
+// bar.sync / bar.arrive are the warp-aligned forms: the warp is reconverged first.
 __device__ __forceinline__ void named_bar(int id, int threads) {
+  __syncwarp();
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+// Arrives without waiting (the producer side of a producer / consumer handoff).
+__device__ __forceinline__ void named_arrive(int id, int threads) {
+  __syncwarp();
+  asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
 
 // ---------------------------------------------------------------- tcgen05
@@ -147,6 +154,17 @@ __device__ __forceinline__ void tc_fence_before() {
 }
 __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// True in exactly one lane of the converged warp.
+__device__ __forceinline__ bool elect_one() {
+  uint32_t pred;
+  asm volatile(
+      "{\n\t.reg .pred P;\n\t"
+      "elect.sync _|P, 0xffffffff;\n\t"
+      "selp.b32 %0, 1, 0, P;\n\t}"
+      : "=r"(pred));
+  return pred != 0;
 }
 
 // D[tmem] (+)= A[smem] * B[smem]; kind::f16 with bf16 inputs and f32 accumulation.
