@@ -173,6 +173,14 @@ rglru_status rglru_sync_status(const void *saved_or_workspace, rglru_stream stre
  * waits run out.  (0, -1) restores the defaults.  Process-wide; not thread-safe. */
 void rglru_debug_lookback(int32_t spin_limit, int32_t drop_tile);
 
+/* Profiling hook (no counterpart on the pages): when `start` and `stop` (cudaEvent_t handles
+ * owned by the caller) are both non-null, the next rglru_fused_forward or
+ * rglru_fused_backward call that runs its tensor-core kernel records `start` on the call's
+ * stream just before that kernel's launch and `stop` just after it, then forgets both; so a
+ * caller can time that kernel alone with cudaEventElapsedTime.  (NULL, NULL) cancels.
+ * Process-wide; not thread-safe. */
+void rglru_debug_kernel_events(void *start, void *stop);
+
 /* Launch accounting (no counterpart on the pages): the number of CUDA kernels this library
  * has enqueued since the process started (memsets excluded).  Lets a caller count the
  * kernels behind a timed region.  Process-wide, atomic. */

@@ -15,7 +15,6 @@ namespace {
 std::atomic<uint64_t> g_launches{0};
 int g_spin_limit = 1 << 22;
 int g_drop_tile = -1;
-
 size_t dsize(int dt) { return dt == RGLRU_BF16 ? 2 : 4; }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -23,6 +22,18 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 }  // namespace
 
 namespace rglru {
+
+cudaEvent_t g_kernel_events[2] = {nullptr, nullptr};
+
+void kernel_event_before(cudaStream_t s) {
+  if (g_kernel_events[0] && g_kernel_events[1]) cudaEventRecord(g_kernel_events[0], s);
+}
+void kernel_event_after(cudaStream_t s) {
+  if (g_kernel_events[0] && g_kernel_events[1]) {
+    cudaEventRecord(g_kernel_events[1], s);
+    g_kernel_events[0] = g_kernel_events[1] = nullptr;
+  }
+}
 
 // Validates the shape and fills `d`.
 rglru_status make_dims(const rglru_shape* s, Dims* d) {
@@ -338,6 +349,11 @@ rglru_status rglru_sync_status(const void* buf, rglru_stream stream) {
 }
 
 uint64_t rglru_kernel_launches(void) { return g_launches.load(std::memory_order_relaxed); }
+
+void rglru_debug_kernel_events(void* start, void* stop) {
+  rglru::g_kernel_events[0] = static_cast<cudaEvent_t>(start);
+  rglru::g_kernel_events[1] = static_cast<cudaEvent_t>(stop);
+}
 
 void rglru_debug_lookback(int32_t spin_limit, int32_t drop_tile) {
   g_spin_limit = spin_limit > 0 ? spin_limit : (1 << 22);

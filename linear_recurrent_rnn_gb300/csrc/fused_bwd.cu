@@ -1,7 +1,7 @@
 // Fused RG-LRU backward on one GB300: the gate logits are recomputed on the tcgen05 tensor
 // cores, the reverse scan and the pointwise derivatives run on the CUDA cores, and the
 // projection gradients dx += dlr Wa^T + dli Wx^T and dW = x^T dl go back to the tensor
-// cores, all in one persistent kernel; a small second kernel reduces the per-CTA partials.
+// cores, all in one persistent kernel, which also sums the per-CTA partials at its end.
 //
 // Sources ("Fattori comparison" page): the custom backward runs the reverse recurrence and the
 // pointwise derivatives, recomputing the sigmoids, the transition and the multiplier rather
@@ -69,6 +69,9 @@ constexpr size_t SMEM_BYTES =
     2 * W_BYTES + STAGES * 2 * T_BYTES + 4 * T_BYTES + T_BYTES + XCH_BYTES + 256 + 1024;
 constexpr uint32_t STATUS_PIPE = 2u;
 constexpr int BAR_SCAN = 1;  // named barrier of the scan warps
+// Workspace offset of the per-gate-block counters of CTAs done with their partial sums
+// (zeroed with the status word before every launch).
+constexpr size_t BWD_COUNTERS = 256;
 
 struct BwdParams {
   int B, T, W, nblk, nC, P, canonical;
@@ -81,6 +84,11 @@ struct BwdParams {
   const float* fwd_carry;  // [B][nC+1][W], state entering each chunk
   float* dh0;
   void* dx;                // written directly for float32 gradients
+  float* dWa;
+  float* dWx;
+  float* dba;
+  float* dbx;
+  float* dLambda;
   uint8_t* scratch;        // workspace
   FusedBwdLayout F;
   int spin_limit, drop_tile;
@@ -247,7 +255,7 @@ __device__ __forceinline__ void bwd_pass2b(uint32_t tcol, int part, int j, uint3
     tc::tmem_ld4(tcol + COL_HP + g * GRP, i4);
     tc::tmem_ld4(tcol + COL_DX + g * GRP, h4);
     tc::tmem_ld_wait();
-    float2 o_r[GRP / 2], o_i[GRP / 2];
+    float2 o_r[GRP / 2], o_i[GRP / 2];  // tokens (u, u + 1) of the two pairs
 #pragma unroll
     for (int q = GRP / 2 - 1; q >= 0; --q) {
       const int u = g * GRP + 2 * q;
@@ -664,37 +672,77 @@ __global__ void __maxnreg__(MAXREG)
     tc::tc_fence_after();
     tc::tmem_dealloc(tmem, TMEM_COLS);
   }
-}
 
-// Sums the per-CTA (and per-half) partials of every gate block in a fixed order
-// (deterministic): dWa, dWx [nblk][k][k]; dba, dbx [W]; dLambda = sigmoid(Lambda) * sum.
-__global__ void k_fused_bwd_reduce(const float* dw_part, const float* vec_part, int P, int nblk,
-                                   const float* Lambda, float* dWa, float* dWx, float* dba,
-                                   float* dbx, float* dLambda) {
-  const int blk = blockIdx.y;
-  const int e = blockIdx.x * blockDim.x + threadIdx.x;  // element of the k x k block
-  if (e < FUSED_K * FUSED_K) {
-    float sa = 0.0f, sx = 0.0f;
-    for (int r = 0; r < P; ++r) {
-      const float* src = dw_part + (size_t)(blk * P + r) * 2 * FUSED_K * FUSED_K;
-      sa += src[e];
-      sx += src[FUSED_K * FUSED_K + e];
+  // Sum of the partials of the block's P CTAs, once all of them have written theirs; each CTA
+  // sums a slice, every element in the same fixed order (deterministic): dWa, dWx [nblk][k][k];
+  // dba, dbx [W]; dLambda = sigmoid(Lambda) * sum.  The counters start at zero every call.
+  if (threadIdx.x == 0) {
+    uint32_t* done = reinterpret_cast<uint32_t*>(p.scratch + BWD_COUNTERS) + blk;
+    __threadfence();
+    atomicAdd(done, 1u);
+    const uint64_t t0 = tc::global_ns();
+    while (ld_acquire(done) < (uint32_t)p.P) {
+      if (tc::global_ns() - t0 > WAIT_LIMIT_NS) {
+        atomicOr(status, STATUS_PIPE);
+        break;
+      }
+      __nanosleep(256);
     }
-    dWa[(size_t)blk * FUSED_K * FUSED_K + e] = sa;
-    dWx[(size_t)blk * FUSED_K * FUSED_K + e] = sx;
   }
-  if (blockIdx.x == 0 && threadIdx.x < FUSED_K) {
-    const int j = threadIdx.x, w = blk * FUSED_K + j;
-    float s0 = 0.0f, s1 = 0.0f, s2 = 0.0f;
-    for (int r = 0; r < NPART * P; ++r) {
-      const float* src = vec_part + ((size_t)blk * P * NPART + r) * 3 * FUSED_K;
-      s0 += src[j];
-      s1 += src[FUSED_K + j];
-      s2 += src[2 * FUSED_K + j];
+  __syncthreads();
+  constexpr int KK = FUSED_K * FUSED_K;
+  constexpr int NV = 2 * KK / 4;  // float4 vectors of the block's dWa, dWx
+  const float4* dwp = reinterpret_cast<const float4*>(p.scratch + p.F.dw_part) +
+                      (size_t)blk * p.P * NV;
+  const int per = (NV + p.P - 1) / p.P;
+  const int v_end = min(NV, (rr + 1) * per);
+  // two vectors per thread and eight partials per round in flight: the sums are bound by the
+  // L2 round trip, not by the adds
+  for (int v0 = rr * per + threadIdx.x; v0 < v_end; v0 += 2 * NTHREADS) {
+    const int v1 = v0 + NTHREADS;
+    float4 acc0[8], acc1[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) acc0[u] = acc1[u] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    for (int r = 0; r < p.P; r += 8) {
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        if (r + u < p.P) {
+          const float4 a = dwp[(size_t)(r + u) * NV + v0];
+          acc0[u].x += a.x, acc0[u].y += a.y, acc0[u].z += a.z, acc0[u].w += a.w;
+          if (v1 < v_end) {
+            const float4 b = dwp[(size_t)(r + u) * NV + v1];
+            acc1[u].x += b.x, acc1[u].y += b.y, acc1[u].z += b.z, acc1[u].w += b.w;
+          }
+        }
+      }
     }
-    dLambda[w] = s0 * __fdividef(1.0f, 1.0f + expf(-Lambda[w]));
-    if (dba) dba[w] = s1;
-    if (dbx) dbx[w] = s2;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int v = h ? v1 : v0;
+      if (v >= v_end) break;
+      float4 t = h ? acc1[0] : acc0[0];
+#pragma unroll
+      for (int u = 1; u < 8; ++u) {
+        const float4 a = h ? acc1[u] : acc0[u];
+        t.x += a.x, t.y += a.y, t.z += a.z, t.w += a.w;
+      }
+      float* dst = v < NV / 2 ? p.dWa + (size_t)blk * KK + v * 4 : p.dWx + (size_t)blk * KK + (v - NV / 2) * 4;
+      *reinterpret_cast<float4*>(dst) = t;
+    }
+  }
+  if (rr == 0 && threadIdx.x < FUSED_K) {
+    const int j = threadIdx.x, w = blk * FUSED_K + j;
+    const float* vp = reinterpret_cast<const float*>(p.scratch + p.F.vec_part) +
+                      (size_t)blk * p.P * NPART * 3 * FUSED_K;
+    float s0 = 0.0f, s1 = 0.0f, s2 = 0.0f;
+    for (int r = 0; r < NPART * p.P; ++r) {
+      s0 += vp[(size_t)r * 3 * FUSED_K + j];
+      s1 += vp[(size_t)r * 3 * FUSED_K + FUSED_K + j];
+      s2 += vp[(size_t)r * 3 * FUSED_K + 2 * FUSED_K + j];
+    }
+    p.dLambda[w] = s0 * __fdividef(1.0f, 1.0f + expf(-p.Lambda[w]));
+    if (p.dba) p.dba[w] = s1;
+    if (p.dbx) p.dbx[w] = s2;
   }
 }
 
@@ -761,11 +809,16 @@ cudaError_t launch_fused_bwd(const Dims& d, const void* dy, const float* dhT, co
   p.lb_dist = lp.dist;
   p.lb_shift = lp.shift;
   p.dx = dx;
+  p.dWa = dWa;
+  p.dWx = dWx;
+  p.dba = dba;
+  p.dbx = dbx;
+  p.dLambda = dLambda;
   const size_t smem = SMEM_BYTES;
   auto kern = gf32 ? k_fused_bwd<float> : k_fused_bwd<bf16>;
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  e = clear_slots(ws, p.F.L, s);
+  e = clear_slots(ws, p.F.L, s, BWD_COUNTERS + (size_t)d.nblk * 4);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.P * d.nblk);
@@ -777,14 +830,10 @@ cudaError_t launch_fused_bwd(const Dims& d, const void* dy, const float* dhT, co
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  kernel_event_before(s);
   e = cudaLaunchKernelEx(&cfg, kern, mx, mdy, mwa, mwx, mdx, p);
+  kernel_event_after(s);
   if (e != cudaSuccess) return e;
-  note_launches(1);
-  const uint8_t* wsb = static_cast<const uint8_t*>(ws);
-  k_fused_bwd_reduce<<<dim3((FUSED_K * FUSED_K + 255) / 256, d.nblk), 256, 0, s>>>(
-      reinterpret_cast<const float*>(wsb + p.F.dw_part),
-      reinterpret_cast<const float*>(wsb + p.F.vec_part), p.P, d.nblk, Lambda, dWa, dWx, dba,
-      dbx, dLambda);
   note_launches(1);
   return cudaGetLastError();
 }

@@ -461,9 +461,10 @@ bool fused_supported(const Dims& d) {
   return d.io == RGLRU_BF16 && d.k == FUSED_K && fused_ctas_per_block(d) >= 1;
 }
 
-// Prepares a scan layout for slot-based look-back: status word cleared, every slot empty.
-cudaError_t clear_slots(void* buf, const ScanLayout& L, cudaStream_t s) {
-  cudaError_t e = cudaMemsetAsync(buf, 0, 256, s);
+// Prepares a scan layout for slot-based look-back: the first zero_bytes (status word and any
+// counters, at most the header and flag area) cleared, every slot empty.
+cudaError_t clear_slots(void* buf, const ScanLayout& L, cudaStream_t s, size_t zero_bytes) {
+  cudaError_t e = cudaMemsetAsync(buf, 0, zero_bytes, s);
   if (e == cudaSuccess)
     e = cudaMemsetAsync(static_cast<uint8_t*>(buf) + L.carry, 0xff, L.part - L.carry, s);
   return e;
@@ -503,7 +504,7 @@ cudaError_t launch_fused_fwd(const Dims& d, const void* x, const void* Wa, const
   e = cudaFuncSetAttribute(k_fused_fwd, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)SMEM_BYTES);
   if (e != cudaSuccess) return e;
-  e = clear_slots(saved, p.L, s);
+  e = clear_slots(saved, p.L, s, 256);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.P * d.nblk);
@@ -515,7 +516,9 @@ cudaError_t launch_fused_fwd(const Dims& d, const void* x, const void* Wa, const
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  kernel_event_before(s);
   e = cudaLaunchKernelEx(&cfg, k_fused_fwd, mx, mwa, mwx, my, p);
+  kernel_event_after(s);
   if (e == cudaSuccess) note_launches(1);
   return e;
 }

@@ -172,6 +172,11 @@ struct ScanBwdArgs {
 // Adds n to the process-wide count of kernels enqueued (rglru_kernel_launches).
 void note_launches(unsigned n);
 
+// rglru_debug_kernel_events: record the caller's events around the next tensor-core kernel.
+extern cudaEvent_t g_kernel_events[2];
+void kernel_event_before(cudaStream_t s);
+void kernel_event_after(cudaStream_t s);
+
 // Host-side validation shared by the entry points (defined in api.cu).
 rglru_status make_dims(const rglru_shape* s, Dims* d);
 bool req(const void* p);  // non-null and 16-byte aligned
@@ -200,7 +205,7 @@ cudaError_t launch_fused_fwd(const Dims& d, const void* x, const void* Wa, const
 bool fused_supported(const Dims& d);
 int fused_ctas_per_block(const Dims& d);
 // Clears the status word of a scan layout and marks every carry / aggregate slot empty.
-cudaError_t clear_slots(void* buf, const ScanLayout& L, cudaStream_t s);
+cudaError_t clear_slots(void* buf, const ScanLayout& L, cudaStream_t s, size_t zero_bytes);
 
 // Fused backward on tensor cores (same coverage as the fused forward; `saved` must come from
 // launch_fused_fwd).  dx is written in shape.grad; dWa / dWx / dba / dbx / dLambda reduced

@@ -46,7 +46,8 @@ _lib = None
 EXPORTS = ("rglru_status_string", "rglru_saved_bytes", "rglru_workspace_bytes",
            "rglru_gate_proj", "rglru_forward", "rglru_backward", "rglru_gate_proj_backward",
            "rglru_fused_forward", "rglru_fused_backward", "rglru_sync_status",
-           "rglru_debug_lookback", "rglru_kernel_launches", "rglru_forward_noalloc")
+           "rglru_debug_lookback", "rglru_kernel_launches", "rglru_forward_noalloc",
+           "rglru_debug_kernel_events")
 
 # Static look-back scratch of rglru_forward_noalloc, per GPU (RGLRU_NOALLOC_SCRATCH_BYTES).
 NOALLOC_SCRATCH_BYTES = 16 << 20
@@ -84,6 +85,8 @@ def lib():
             L.rglru_debug_lookback.restype = None
             L.rglru_forward_noalloc.argtypes = [S] + [P] * 10
             L.rglru_forward_noalloc.restype = ctypes.c_int
+            L.rglru_debug_kernel_events.argtypes = [ctypes.c_void_p, ctypes.c_void_p]
+            L.rglru_debug_kernel_events.restype = None
             L.rglru_kernel_launches.argtypes = []
             L.rglru_kernel_launches.restype = ctypes.c_uint64
             for n in ("rglru_gate_proj", "rglru_forward", "rglru_backward",
@@ -204,6 +207,13 @@ def rglru_sync_status(buf: torch.Tensor, stream=None) -> int:
 
 def rglru_debug_lookback(spin_limit: int, drop_tile: int) -> None:
     lib().rglru_debug_lookback(int(spin_limit), int(drop_tile))
+
+
+def rglru_debug_kernel_events(start, stop) -> None:
+    """Records the torch.cuda.Event pair `start`/`stop` around the next fused call's
+    tensor-core kernel (both already created, i.e. recorded once); None, None cancels."""
+    h = lambda e: None if e is None else ctypes.c_void_p(e.cuda_event)
+    lib().rglru_debug_kernel_events(h(start), h(stop))
 
 
 def rglru_kernel_launches() -> int:
