@@ -66,42 +66,6 @@ __device__ __forceinline__ float softplus_f(float z) {
 // 1 - a^2 for a = e^la, la <= 0, without the cancellation of 1 - a*a as a -> 1.
 __device__ __forceinline__ float one_minus_a2(float la) { return -expm1f(2.0f * la); }
 
-// The decay a = e^la and 1 - a^2 for la <= 0, from one short series.  The decay is multiplied
-// over as many tokens as the memory is long (~1 / (1 - a), 10^4 for a = 0.9999), so a
-// systematic relative error e in a grows to ~e / (1 - a) in the long-range products: a must
-// be accurate to the rounding of a float, not just to a few ulp of an approximate exponential.
-// For la > -1/8: e1 = expm1(la) from its Taylor series at 0 cut after la^7 (remainder below
-// |la|^8 / 8! < 2e-12), a = 1 + e1, and 1 - a^2 = -e1 (e1 + 2) without cancellation.
-// Otherwise (a < 0.89, memory of a few tokens) a = 2^(la log2 e) and 1 - a^2 = 1 - a a.
-// The series branch alone, for callers that know la > -1/8 for every token (a channel whose
-// softplus(Lambda) < 1/64, since r < 1).
-__device__ __forceinline__ void decay_near(float la, float& a, float& om) {
-  float p = fmaf(la, 1.0f / 5040.0f, 1.0f / 720.0f);
-  p = fmaf(la, p, 1.0f / 120.0f);
-  p = fmaf(la, p, 1.0f / 24.0f);
-  p = fmaf(la, p, 1.0f / 6.0f);
-  p = fmaf(la, p, 0.5f);
-  p = fmaf(la, p, 1.0f);
-  const float e1 = la * p;
-  a = 1.0f + e1;
-  om = -e1 * (e1 + 2.0f);
-}
-
-__device__ __forceinline__ void decay_fast(float la, float& a, float& om) {
-  float p = fmaf(la, 1.0f / 5040.0f, 1.0f / 720.0f);
-  p = fmaf(la, p, 1.0f / 120.0f);
-  p = fmaf(la, p, 1.0f / 24.0f);
-  p = fmaf(la, p, 1.0f / 6.0f);
-  p = fmaf(la, p, 0.5f);
-  p = fmaf(la, p, 1.0f);
-  const float e1 = la * p;
-  float ax;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(ax) : "f"(la * 1.4426950408889634f));
-  const bool near = la > -0.125f;
-  a = near ? 1.0f + e1 : ax;
-  om = near ? -e1 * (e1 + 2.0f) : fmaf(-ax, ax, 1.0f);
-}
-
 // Single special-function-unit operations (PTX ex2.approx / rcp.approx, flush-to-zero).
 constexpr float LOG2E = 1.4426950408889634f;
 __device__ __forceinline__ float ex2_approx(float x) {
@@ -114,14 +78,11 @@ __device__ __forceinline__ float rcp_approx(float x) {
   asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
-// sigmoid(z + bias) with nb = -bias * log2(e) precomputed: 1 / (1 + 2^(-(z + bias) log2 e)).
-__device__ __forceinline__ float sigmoid_nb(float z, float nb) {
-  return rcp_approx(1.0f + ex2_approx(fmaf(z, -LOG2E, nb)));
-}
-
-// sqrt(v) for v >= 0 as v * rsqrt(v) (one special-function op), 0 at v = 0.
-__device__ __forceinline__ float sqrt_fast(float v) {
-  return v > 0.0f ? v * rsqrtf(v) : 0.0f;
+// sqrt(v) for v >= 0 (PTX sqrt.approx, 0 at 0).
+__device__ __forceinline__ float sqrt_approx(float v) {
+  float y;
+  asm("sqrt.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(v));
+  return y;
 }
 
 // ---------------------------------------------------------------- packed pairs
@@ -133,49 +94,108 @@ __device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) { return __
 __device__ __forceinline__ float2 mul2(float2 a, float2 b) { return __fmul2_rn(a, b); }
 __device__ __forceinline__ float2 add2(float2 a, float2 b) { return __fadd2_rn(a, b); }
 
-// sigmoid_nb on two logits.
-__device__ __forceinline__ float2 sigmoid2_nb(float2 z, float nb) {
-  const float2 s = fma2(z, bc2(-LOG2E), bc2(nb));
-  const float2 d = add2(make_float2(ex2_approx(s.x), ex2_approx(s.y)), bc2(1.0f));
-  return make_float2(rcp_approx(d.x), rcp_approx(d.y));
-}
+// ---------------------------------------------------------------- gates from one rsqrt
+// The gates, the decay and the input multiplier of a token pair with two ex2 and one rsqrt per
+// token (the special-function unit runs ex2 at twice the rate of the other operations).  With
+// er = e^-(lr + ba), ei = e^-(li + bx), pr = 1 + er, pi = 1 + ei, so r = 1 / pr, i = 1 / pi:
+//   t = (pr pi^2)^(-1/2),  s = t pi = sqrt(r),  r = s^2,  i = t s pr,  la = nk r  (nk = -8 sp).
+// Near regime (la > -1/8): the decay and the multiplier come from two smooth factors,
+//   a = e^la = 1 + la P(la),            P(la) = expm1(la) / la,
+//   m = sqrt(1 - a^2) = sqrt(-2 la) Q(la),  Q(la) = sqrt((1 - e^(2 la)) / (-2 la)),
+// each a degree-3 polynomial fitted on [-1/8, 0] (relative error below 3e-8 in float64).  The
+// decay is multiplied over ~1 / (1 - a) tokens, so 1 - a = -la P(la) must carry no systematic
+// error beyond float rounding, which the fit gives.  As sqrt(-2 la) = C s with the per-channel
+// C = sqrt(-2 nk), the gated input weight is m i = C Q(la) s / pi = C Q(la) t: no sqrt and no
+// reciprocal.  The exponents are clamped (er <= 2^48, ei <= 2^39) so that pr pi^2 < 2^127 never
+// overflows: a gate that is clamped reads as 2^-48 (r) or 2^-39 (i) instead of something
+// smaller still, which changes no result in float32.
+constexpr float GATE_ZR_MAX = 48.0f, GATE_ZI_MAX = 39.0f;
+constexpr float DECAY_P1 = 4.999970987e-01f, DECAY_P2 = 1.665260549e-01f,
+                DECAY_P3 = 3.971588063e-02f;
+constexpr float MULT_Q1 = 4.999952308e-01f, MULT_Q2 = 2.081021452e-01f,
+                MULT_Q3 = 5.929165853e-02f;
+constexpr float NEAR_LA = -0.125f;  // the near regime: la > NEAR_LA
 
-// decay_near / decay_fast on two lanes (same arithmetic, lane by lane).
-__device__ __forceinline__ float2 expm1_series2(float2 la) {
-  float2 p = fma2(la, bc2(1.0f / 5040.0f), bc2(1.0f / 720.0f));
-  p = fma2(la, p, bc2(1.0f / 120.0f));
-  p = fma2(la, p, bc2(1.0f / 24.0f));
-  p = fma2(la, p, bc2(1.0f / 6.0f));
-  p = fma2(la, p, bc2(0.5f));
-  p = fma2(la, p, bc2(1.0f));
-  return mul2(la, p);
-}
-__device__ __forceinline__ void decay_near2(float2 la, float2& a, float2& om) {
-  const float2 e1 = expm1_series2(la);
-  a = add2(e1, bc2(1.0f));
-  om = mul2(e1, fma2(e1, bc2(-1.0f), bc2(-2.0f)));  // -e1 (e1 + 2)
-}
-__device__ __forceinline__ void decay_fast2(float2 la, float2& a, float2& om) {
-  decay_near2(la, a, om);
-  if (!(la.x > -0.125f)) {
-    const float ax = ex2_approx(la.x * LOG2E);
-    a.x = ax;
-    om.x = fmaf(-ax, ax, 1.0f);
-  }
-  if (!(la.y > -0.125f)) {
-    const float ax = ex2_approx(la.y * LOG2E);
-    a.y = ax;
-    om.y = fmaf(-ax, ax, 1.0f);
-  }
-}
-// sqrt of two values >= 0, one special-function op each (PTX sqrt.approx, 0 at 0).
-__device__ __forceinline__ float sqrt_approx(float v) {
+// Per-channel constants of the gate arithmetic.
+struct GateK {
+  float nk;   // -8 softplus(Lambda): log a = nk r
+  float cm;   // sqrt(-2 nk)
+  float nbr;  // -ba log2(e)
+  float nbi;  // -bx log2(e)
+};
+
+__device__ __forceinline__ float rsqrt_approx(float x) {
   float y;
-  asm("sqrt.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(v));
+  asm("rsqrt.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
-__device__ __forceinline__ float2 sqrt_fast2(float2 v) {
-  return make_float2(sqrt_approx(v.x), sqrt_approx(v.y));
+
+// The shared front of the gate arithmetic: t, s and the two sums pr, pi of a token pair.
+__device__ __forceinline__ void gate_front2(float2 lr, float2 li, const GateK& k, float2& t,
+                                            float2& s, float2& pr, float2& pi) {
+  float2 zr = fma2(lr, bc2(-LOG2E), bc2(k.nbr));
+  float2 zi = fma2(li, bc2(-LOG2E), bc2(k.nbi));
+  zr.x = fminf(zr.x, GATE_ZR_MAX);
+  zr.y = fminf(zr.y, GATE_ZR_MAX);
+  zi.x = fminf(zi.x, GATE_ZI_MAX);
+  zi.y = fminf(zi.y, GATE_ZI_MAX);
+  pr = add2(make_float2(ex2_approx(zr.x), ex2_approx(zr.y)), bc2(1.0f));
+  pi = add2(make_float2(ex2_approx(zi.x), ex2_approx(zi.y)), bc2(1.0f));
+  const float2 d = mul2(mul2(pr, pi), pi);
+  t = make_float2(rsqrt_approx(d.x), rsqrt_approx(d.y));
+  s = mul2(t, pi);
+}
+
+// Near-regime decay and gated input weight from la and t.
+__device__ __forceinline__ void gate_near2(float2 la, float2 t, float cm, float2& a, float2& mi) {
+  float2 p = fma2(la, bc2(DECAY_P3), bc2(DECAY_P2));
+  p = fma2(la, p, bc2(DECAY_P1));
+  p = fma2(la, p, bc2(1.0f));
+  a = fma2(la, p, bc2(1.0f));
+  float2 q = fma2(la, bc2(MULT_Q3), bc2(MULT_Q2));
+  q = fma2(la, q, bc2(MULT_Q1));
+  q = fma2(la, q, bc2(1.0f));
+  mi = mul2(mul2(bc2(cm), t), q);
+}
+
+// A token pair, every token in the near regime: decay a, gated input weight m i, and r.
+__device__ __forceinline__ void gates_near2(float2 lr, float2 li, const GateK& k, float2& a,
+                                            float2& mi, float2& r) {
+  float2 t, s, pr, pi;
+  gate_front2(lr, li, k, t, s, pr, pi);
+  r = mul2(s, s);
+  gate_near2(mul2(bc2(k.nk), r), t, k.cm, a, mi);
+}
+
+// The same, with i as well.
+__device__ __forceinline__ void gates_near2_i(float2 lr, float2 li, const GateK& k, float2& a,
+                                              float2& mi, float2& r, float2& i) {
+  float2 t, s, pr, pi;
+  gate_front2(lr, li, k, t, s, pr, pi);
+  r = mul2(s, s);
+  i = mul2(mul2(t, s), pr);
+  gate_near2(mul2(bc2(k.nk), r), t, k.cm, a, mi);
+}
+
+// Any token: the near-regime form where la > -1/8, else a = 2^(la log2 e) and m = sqrt(1 - a a)
+// (a < 0.89: a memory of a few tokens, where the relative accuracy of 1 - a is not at stake).
+// Also returns i.
+__device__ __forceinline__ void gates_any2(float2 lr, float2 li, const GateK& k, float2& a,
+                                           float2& mi, float2& r, float2& i) {
+  float2 t, s, pr, pi;
+  gate_front2(lr, li, k, t, s, pr, pi);
+  r = mul2(s, s);
+  i = mul2(mul2(t, s), pr);
+  const float2 la = mul2(bc2(k.nk), r);
+  gate_near2(la, t, k.cm, a, mi);
+  if (!(la.x > NEAR_LA)) {
+    a.x = ex2_approx(la.x * LOG2E);
+    mi.x = sqrt_approx(fmaf(-a.x, a.x, 1.0f)) * i.x;
+  }
+  if (!(la.y > NEAR_LA)) {
+    a.y = ex2_approx(la.y * LOG2E);
+    mi.y = sqrt_approx(fmaf(-a.y, a.y, 1.0f)) * i.y;
+  }
 }
 
 // ---------------------------------------------------------------- staged bf16 tiles

@@ -17,9 +17,10 @@
 // Tile = (b, blk, 64 tokens), visited in reverse chunk order; four scan threads per channel,
 // one per 16-token part.  Per tile:
 //   1. MMA: lr^T, li^T = W^T x^T into TMEM (as in the forward).
-//   2. Pass 1 (tokens ascending): abar and i kept in registers, m and r parked in TMEM over
-//      the logits; the part's forward aggregate (state map h -> A h + B) and reverse aggregate
-//      (carry map c_in -> P c_in + S with P = prod abar, S = sum_t (prod_{s<=t} abar_s) dy_t).
+//   2. Pass 1 (tokens ascending): abar kept in registers, m i and r parked in TMEM over the
+//      logits, i beside them; the part's forward aggregate (state map h -> A h + B) and reverse
+//      aggregate (carry map c_in -> P c_in + S with P = prod abar, S = sum_t (prod_{s<=t}
+//      abar_s) dy_t).
 //   3. Parts exchange aggregates through shared memory; part 0 composes the tile's reverse
 //      aggregate, publishes it, and runs the anchored look-back toward larger t (lookback.cuh)
 //      for the carry from the right; the forward entry state comes from the chunk states the
@@ -51,8 +52,9 @@ constexpr int NPART = 4;             // token parts of a tile, one scan thread e
 constexpr int PT = FUSED_C / NPART;  // tokens per scan thread
 constexpr int NSCAN = 4 * NPART;     // scan warps (4 lane quadrants per part)
 constexpr int NTHREADS = 64 + NSCAN * 32;
-// 18 warps share the SM's four 16 K-register sub-partitions (five per sub-partition): <= 96.
-constexpr int MAXREG = 96;
+// The warps share the SM's four 16 K-register sub-partitions: registers per thread <= 16384 /
+// (32 x warps per sub-partition), rounded down to a multiple of 8.
+constexpr int MAXREG = (16384 / (((NSCAN + 2 + 3) / 4) * 32)) / 8 * 8;
 constexpr int STAGES = 2;
 constexpr uint32_t W_BYTES = FUSED_K * FUSED_K * 2;
 constexpr uint32_t T_BYTES = FUSED_C * FUSED_K * 2;  // one 64 x 128 bf16 tile
@@ -136,23 +138,23 @@ __device__ __forceinline__ void store_dl4(uint8_t* hi_buf, uint8_t* lo_buf, int 
 // column = token of the part; the thread's columns of each region start at tcol.
 constexpr int GRP = 4;  // tokens per TMEM load / store group
 
-// Pass 1 (tokens ascending): the gates once; abar stays in registers, m -> COL_LR and r ->
+// Pass 1 (tokens ascending): the gates once; abar stays in registers, m i -> COL_LR and r ->
 // COL_LI (over the logits, already read), i -> COL_HP; returns the part's maps: forward
 // h -> P h + fB and reverse c -> P c + S, with P = prod abar and S = sum_t (prod of abar up
 // to t) dy_t.  GENERAL = false is the warp-uniform fast path: every token valid, no reset,
-// every decay on the series branch.
+// every decay in the near regime.
 template <bool GENERAL>
-__device__ __forceinline__ void bwd_pass1(uint32_t tcol, uint32_t xb0, uint32_t xb1, float nk,
-                                          float nbr, float nbi, uint32_t rmask, int valid,
+__device__ __forceinline__ void bwd_pass1(uint32_t tcol, uint32_t xb0, uint32_t xb1,
+                                          const GateK& gk, uint32_t rmask, int valid,
                                           float2 (&ab)[PT / 2], float& P, float& fB, float& S) {
   P = 1.0f;
   fB = 0.0f;
   S = 0.0f;
 #pragma unroll
   for (int g = 0; g < PT / GRP; ++g) {
-    float vr[GRP], vi[GRP], m4[GRP], i4[GRP];
-    tc::tmem_ld4(tcol + COL_LR + g * GRP, vr);
-    tc::tmem_ld4(tcol + COL_LI + g * GRP, vi);
+    float vr[GRP], vi[GRP], m4[GRP];
+    tc::tmem_ld(tcol + COL_LR + g * GRP, vr);
+    tc::tmem_ld(tcol + COL_LI + g * GRP, vi);
     tc::tmem_ld_wait();
 #pragma unroll
     for (int q = 0; q < GRP / 2; ++q) {
@@ -160,36 +162,33 @@ __device__ __forceinline__ void bwd_pass1(uint32_t tcol, uint32_t xb0, uint32_t 
       const float2 xv = make_float2(tok_elem(xb0, xb1, u), tok_elem(xb0, xb1, u + 1));
       float2 dyv = make_float2(tok_elem(xb0 + T_BYTES, xb1 + T_BYTES, u),
                                tok_elem(xb0 + T_BYTES, xb1 + T_BYTES, u + 1));
-      const float2 r = sigmoid2_nb(make_float2(vr[2 * q], vr[2 * q + 1]), nbr);
-      const float2 i = sigmoid2_nb(make_float2(vi[2 * q], vi[2 * q + 1]), nbi);
-      const float2 la = mul2(bc2(nk), r);
-      float2 abar, om;
-      if (GENERAL)
-        decay_fast2(la, abar, om);
-      else
-        decay_near2(la, abar, om);
-      float2 m = sqrt_fast2(om);
+      const float2 lr = make_float2(vr[2 * q], vr[2 * q + 1]);
+      const float2 li = make_float2(vi[2 * q], vi[2 * q + 1]);
+      float2 abar, mi, r, i;
       if (GENERAL) {
+        gates_any2(lr, li, gk, abar, mi, r, i);
         if ((rmask >> u) & 1u) {
           abar.x = 0.0f;
-          m.x = 1.0f;
+          mi.x = i.x;
         }
         if ((rmask >> (u + 1)) & 1u) {
           abar.y = 0.0f;
-          m.y = 1.0f;
+          mi.y = i.y;
         }
         if (u >= valid) {
           abar.x = 1.0f;
-          m.x = 0.0f;
+          mi.x = 0.0f;
           dyv.x = 0.0f;
         }
         if (u + 1 >= valid) {
           abar.y = 1.0f;
-          m.y = 0.0f;
+          mi.y = 0.0f;
           dyv.y = 0.0f;
         }
+      } else {
+        gates_near2_i(lr, li, gk, abar, mi, r, i);
       }
-      const float2 bv = mul2(m, mul2(i, xv));
+      const float2 bv = mul2(mi, xv);
       fB = fmaf(abar.x, fB, bv.x);
       P *= abar.x;
       S = fmaf(P, dyv.x, S);
@@ -197,16 +196,16 @@ __device__ __forceinline__ void bwd_pass1(uint32_t tcol, uint32_t xb0, uint32_t 
       P *= abar.y;
       S = fmaf(P, dyv.y, S);
       ab[u / 2] = abar;
-      m4[2 * q] = m.x;
-      m4[2 * q + 1] = m.y;
+      m4[2 * q] = mi.x;
+      m4[2 * q + 1] = mi.y;
       vr[2 * q] = r.x;  // the logits are consumed: their registers take r and i
       vr[2 * q + 1] = r.y;
-      i4[2 * q] = i.x;
-      i4[2 * q + 1] = i.y;
+      vi[2 * q] = i.x;
+      vi[2 * q + 1] = i.y;
     }
-    tc::tmem_st4(tcol + COL_LR + g * GRP, m4);
-    tc::tmem_st4(tcol + COL_LI + g * GRP, vr);
-    tc::tmem_st4(tcol + COL_HP + g * GRP, i4);
+    tc::tmem_st(tcol + COL_LR + g * GRP, m4);
+    tc::tmem_st(tcol + COL_LI + g * GRP, vr);
+    tc::tmem_st(tcol + COL_HP + g * GRP, vi);
   }
   tc::tmem_st_wait();
 }
@@ -217,22 +216,20 @@ __device__ __forceinline__ void bwd_pass2a(uint32_t tcol, uint32_t xb0, uint32_t
                                            const float2 (&ab)[PT / 2], float h) {
 #pragma unroll
   for (int g = 0; g < PT / GRP; ++g) {
-    float m4[GRP], i4[GRP], h4[GRP];
-    tc::tmem_ld4(tcol + COL_LR + g * GRP, m4);
-    tc::tmem_ld4(tcol + COL_HP + g * GRP, i4);
+    float m4[GRP], h4[GRP];
+    tc::tmem_ld(tcol + COL_LR + g * GRP, m4);
     tc::tmem_ld_wait();
 #pragma unroll
     for (int q = 0; q < GRP / 2; ++q) {
       const int u = g * GRP + 2 * q;
       const float2 xv = make_float2(tok_elem(xb0, xb1, u), tok_elem(xb0, xb1, u + 1));
-      const float2 bv = mul2(make_float2(m4[2 * q], m4[2 * q + 1]),
-                             mul2(make_float2(i4[2 * q], i4[2 * q + 1]), xv));
+      const float2 bv = mul2(make_float2(m4[2 * q], m4[2 * q + 1]), xv);
       h4[2 * q] = h;
       h = fmaf(ab[u / 2].x, h, bv.x);
       h4[2 * q + 1] = h;
       h = fmaf(ab[u / 2].y, h, bv.y);
     }
-    tc::tmem_st4(tcol + COL_DX + g * GRP, h4);
+    tc::tmem_st(tcol + COL_DX + g * GRP, h4);
   }
   tc::tmem_st_wait();
 }
@@ -240,9 +237,9 @@ __device__ __forceinline__ void bwd_pass2a(uint32_t tcol, uint32_t xb0, uint32_t
 // Pass 2b (tokens descending): g exactly from the carry `cin` entering the part's last token
 // from the right, and the pointwise gradients; dlr, dli go to the dl operand buffers as bf16
 // hi + lo pairs, the direct dx term g m i over h_{t-1} in the dx columns (the accumulator of
-// the dx MMAs).
+// the dx MMAs).  dsp sums dla r (the softplus gradient is -8 times the total).
 template <bool GENERAL>
-__device__ __forceinline__ void bwd_pass2b(uint32_t tcol, int part, int j, uint32_t xb0,
+__device__ __forceinline__ void bwd_pass2b(uint32_t tcol, int tb, int j, uint32_t xb0,
                                            uint32_t xb1, float nk, int valid,
                                            const float2 (&ab)[PT / 2], float cin, uint8_t* s_dl,
                                            float2& dsp, float2& dba, float2& dbx) {
@@ -250,10 +247,10 @@ __device__ __forceinline__ void bwd_pass2b(uint32_t tcol, int part, int j, uint3
 #pragma unroll
   for (int g = PT / GRP - 1; g >= 0; --g) {
     float m4[GRP], r4[GRP], i4[GRP], h4[GRP];
-    tc::tmem_ld4(tcol + COL_LR + g * GRP, m4);
-    tc::tmem_ld4(tcol + COL_LI + g * GRP, r4);
-    tc::tmem_ld4(tcol + COL_HP + g * GRP, i4);
-    tc::tmem_ld4(tcol + COL_DX + g * GRP, h4);
+    tc::tmem_ld(tcol + COL_LR + g * GRP, m4);
+    tc::tmem_ld(tcol + COL_LI + g * GRP, r4);
+    tc::tmem_ld(tcol + COL_HP + g * GRP, i4);
+    tc::tmem_ld(tcol + COL_DX + g * GRP, h4);
     tc::tmem_ld_wait();
     float2 o_r[GRP / 2], o_i[GRP / 2];  // tokens (u, u + 1) of the two pairs
 #pragma unroll
@@ -267,7 +264,7 @@ __device__ __forceinline__ void bwd_pass2b(uint32_t tcol, int part, int j, uint3
         if (u + 1 >= valid) dyv.y = 0.0f;
       }
       const float2 abar = ab[u / 2];
-      const float2 m = make_float2(m4[2 * q], m4[2 * q + 1]);
+      const float2 mi = make_float2(m4[2 * q], m4[2 * q + 1]);
       const float2 r = make_float2(r4[2 * q], r4[2 * q + 1]);
       const float2 i = make_float2(i4[2 * q], i4[2 * q + 1]);
       float2 gv;
@@ -275,27 +272,30 @@ __device__ __forceinline__ void bwd_pass2b(uint32_t tcol, int part, int j, uint3
       gv.x = fmaf(abar.y, gv.y, dyv.x);
       gnext = gv.x;
       anext = abar.x;
-      const float2 uu = mul2(i, xv);
-      // d h_t / d la = abar (h_{t-1} - u abar / m); zero at reset tokens (abar = 0), past T
-      // and where the decay is exactly 1 (m = 0)
-      const float2 nrs = make_float2(-rcp_approx(m.x), -rcp_approx(m.y));
-      float2 alpha = mul2(abar, fma2(mul2(uu, abar), nrs, make_float2(h4[2 * q], h4[2 * q + 1])));
-      if ((GENERAL && abar.x == 0.0f) || m.x == 0.0f) alpha.x = 0.0f;
-      if ((GENERAL && abar.y == 0.0f) || m.y == 0.0f) alpha.y = 0.0f;
+      // d h_t / d la = abar (h_{t-1} - abar x i / m) with i / m = i^2 / (m i); zero at reset
+      // tokens (abar = 0), past T and where the decay is exactly 1 (m = 0)
+      const float2 nw = mul2(mul2(i, i), make_float2(rcp_approx(-mi.x), rcp_approx(-mi.y)));
+      float2 alpha = mul2(abar, fma2(mul2(abar, xv), nw, make_float2(h4[2 * q], h4[2 * q + 1])));
+      if ((GENERAL && abar.x == 0.0f) || mi.x == 0.0f) alpha.x = 0.0f;
+      if ((GENERAL && abar.y == 0.0f) || mi.y == 0.0f) alpha.y = 0.0f;
       const float2 dla = mul2(gv, alpha);
-      const float2 gm = mul2(gv, m);
+      const float2 dd = mul2(gv, mi);  // direct dx term
       o_r[q] = mul2(mul2(dla, bc2(nk)), mul2(r, fma2(r, bc2(-1.0f), bc2(1.0f))));
-      o_i[q] = mul2(mul2(gm, uu), fma2(i, bc2(-1.0f), bc2(1.0f)));
-      const float2 dd = mul2(gm, i);  // direct dx term
-      dsp = fma2(dla, mul2(bc2(-8.0f), r), dsp);
+      o_i[q] = mul2(mul2(dd, xv), fma2(i, bc2(-1.0f), bc2(1.0f)));
+      dsp = fma2(dla, r, dsp);
       dba = add2(dba, o_r[q]);
       dbx = add2(dbx, o_i[q]);
       h4[2 * q] = dd.x;
       h4[2 * q + 1] = dd.y;
     }
-    store_dl4(s_dl, s_dl + T_BYTES, part, g * GRP, j, o_r[0], o_r[1]);
-    store_dl4(s_dl + 2 * T_BYTES, s_dl + 3 * T_BYTES, part, g * GRP, j, o_i[0], o_i[1]);
-    tc::tmem_st4(tcol + COL_DX + g * GRP, h4);
+#pragma unroll
+    for (int f = 0; f < GRP / 4; ++f) {
+      const int tu = tb + g * GRP + 4 * f;  // first token of the four within the tile
+      store_dl4(s_dl, s_dl + T_BYTES, tu >> 4, tu & 15, j, o_r[2 * f], o_r[2 * f + 1]);
+      store_dl4(s_dl + 2 * T_BYTES, s_dl + 3 * T_BYTES, tu >> 4, tu & 15, j, o_i[2 * f],
+                o_i[2 * f + 1]);
+    }
+    tc::tmem_st(tcol + COL_DX + g * GRP, h4);
   }
   tc::tmem_st_wait();
 }
@@ -467,15 +467,17 @@ __global__ void __maxnreg__(MAXREG)
     const int w = blk * FUSED_K + j;
     const int tb = part * PT;
     const uint32_t tcol = tmem + ((uint32_t)(q * 32) << 16) + tb;  // this thread's lane, part
-    const float nk = -8.0f * softplus_f(p.Lambda[w]);  // log a = nk * r
-    const float nbr = p.ba ? -p.ba[w] * LOG2E : 0.0f;   // bias folded into the exponent
-    const float nbi = p.bx ? -p.bx[w] * LOG2E : 0.0f;
+    GateK gk;
+    gk.nk = -8.0f * softplus_f(p.Lambda[w]);  // log a = nk * r
+    gk.cm = sqrtf(-2.0f * gk.nk);
+    gk.nbr = p.ba ? -p.ba[w] * LOG2E : 0.0f;  // biases folded into the exponents
+    gk.nbi = p.bx ? -p.bx[w] * LOG2E : 0.0f;
     float* rcar = reinterpret_cast<float*>(p.scratch + p.F.L.carry);
     float2* agg = reinterpret_cast<float2*>(p.scratch + p.F.L.agg);
     const bool store_thread = (warp == 2 && lane == 0);
     if (store_thread) tc::prefetch_tmap(&tm_dx);
     float2 dsp = bc2(0.0f), dba = bc2(0.0f), dbx = bc2(0.0f);
-    const bool near_all = __all_sync(0xffffffffu, nk > -0.125f);
+    const bool near_all = __all_sync(0xffffffffu, gk.nk > NEAR_LA);
     // Channel j of a token row in a stage: 16-channel slab, 2-byte column, and the 16-byte half
     // of the 32-byte row (swapped on rows 4..7 of every 8 by the swizzle).
     const int xoff0 = (j >> 4) * SLAB_X + (j & 7) * 2 + (((j & 15) >> 3) << 4);
@@ -530,9 +532,9 @@ __global__ void __maxnreg__(MAXREG)
         ctl.wait(&in_full[st], ph);
         tc::tc_fence_after();
         if (fast)
-          bwd_pass1<false>(tcol, xb0, xb1, nk, nbr, nbi, 0u, PT, ab, P, fB, S);
+          bwd_pass1<false>(tcol, xb0, xb1, gk, 0u, PT, ab, P, fB, S);
         else
-          bwd_pass1<true>(tcol, xb0, xb1, nk, nbr, nbi, rmask, valid, ab, P, fB, S);
+          bwd_pass1<true>(tcol, xb0, xb1, gk, rmask, valid, ab, P, fB, S);
       }
 
       // dx of tile it - 1: TMEM -> smem [token][channel] as bf16 (float32 goes straight to HBM).
@@ -619,9 +621,9 @@ __global__ void __maxnreg__(MAXREG)
       if (it > 0) ctl.wait(dl_empty, (it - 1) & 1);
       tc::tc_fence_after();
       if (fast)
-        bwd_pass2b<false>(tcol, part, j, xb0, xb1, nk, PT, ab, cin, s_dl, dsp, dba, dbx);
+        bwd_pass2b<false>(tcol, tb, j, xb0, xb1, gk.nk, PT, ab, cin, s_dl, dsp, dba, dbx);
       else
-        bwd_pass2b<true>(tcol, part, j, xb0, xb1, nk, valid, ab, cin, s_dl, dsp, dba, dbx);
+        bwd_pass2b<true>(tcol, tb, j, xb0, xb1, gk.nk, valid, ab, cin, s_dl, dsp, dba, dbx);
       tc::fence_proxy_async_smem();
       tc::tc_fence_before();
       __syncwarp();
@@ -636,7 +638,7 @@ __global__ void __maxnreg__(MAXREG)
     // Per-CTA, per-part partials of the per-channel sums.
     float* vp = reinterpret_cast<float*>(p.scratch + p.F.vec_part) +
                 ((size_t)blockIdx.x * NPART + part) * 3 * FUSED_K;
-    vp[j] = dsp.x + dsp.y;
+    vp[j] = -8.0f * (dsp.x + dsp.y);  // d sp = sum dla (-8 r)
     vp[FUSED_K + j] = dba.x + dba.y;
     vp[2 * FUSED_K + j] = dbx.x + dbx.y;
 

@@ -35,12 +35,13 @@ namespace rglru {
 
 namespace {
 
-constexpr int NPART = 4;              // token parts of a tile, one scan thread each per channel
+constexpr int NPART = 2;              // token parts of a tile, one scan thread each per channel
 constexpr int PT = FUSED_C / NPART;   // tokens per scan thread
 constexpr int NSCAN = 4 * NPART;      // scan warps (4 lane quadrants per part)
 constexpr int NTHREADS = 64 + NSCAN * 32;
-// 18 warps share the SM's four 16 K-register sub-partitions (five per sub-partition): <= 96.
-constexpr int MAXREG = 96;
+// The warps share the SM's four 16 K-register sub-partitions: registers per thread <= 16384 /
+// (32 x warps per sub-partition), rounded down to a multiple of 8.
+constexpr int MAXREG = (16384 / (((NSCAN + 2 + 3) / 4) * 32)) / 8 * 8;
 constexpr int XSTAGES = 3;
 constexpr uint32_t W_BYTES = FUSED_K * FUSED_K * 2;  // one weight block, bf16
 constexpr uint32_t X_BYTES = FUSED_C * FUSED_K * 2;  // one x tile, bf16
@@ -86,18 +87,17 @@ struct Ctl {
   }
 };
 
-// Local scan of one scan thread's PT = 16 tokens from a zero state.  The pointwise work runs
-// on token pairs (u, u + 1) in the two lanes of f32x2 operations (adjacent TMEM columns land
-// in adjacent registers); the recurrence itself is a scalar chain.  The state after each token
+// Local scan of one scan thread's PT tokens from a zero state.  The pointwise work runs on
+// token pairs (u, u + 1) in the two lanes of f32x2 operations (adjacent TMEM columns land in
+// adjacent registers); the recurrence itself is a scalar chain.  The state after each token
 // (hl) and the product of abar up to it (Ac) are parked in TMEM as they are made, at columns
 // park + u and park + PT + u; (rA, rh) = the part's map.  GENERAL handles resets, tokens past
 // T and decays with la <= -1/8; the fast variant (chosen warp-uniformly) has none.
 constexpr int GRP = 8;  // tokens per TMEM load / store group
 template <bool GENERAL>
 __device__ __forceinline__ void local_scan(uint32_t t_lr, uint32_t t_li, uint32_t park,
-                                           uint32_t xb0, uint32_t xb1, float nk, float nbr,
-                                           float nbi, uint32_t rmask, int valid, float& rh,
-                                           float& rA) {
+                                           uint32_t xb0, uint32_t xb1, const GateK& gk,
+                                           uint32_t rmask, int valid, float& rh, float& rA) {
   rh = 0.0f;
   rA = 1.0f;
 #pragma unroll
@@ -110,34 +110,32 @@ __device__ __forceinline__ void local_scan(uint32_t t_lr, uint32_t t_li, uint32_
     for (int q = 0; q < GRP / 2; ++q) {
       const int u = g * GRP + 2 * q;  // tokens u, u + 1 of the part
       const float2 xv = make_float2(tok_elem(xb0, xb1, u), tok_elem(xb0, xb1, u + 1));
-      const float2 r = sigmoid2_nb(make_float2(vr[2 * q], vr[2 * q + 1]), nbr);
-      const float2 i = sigmoid2_nb(make_float2(vi[2 * q], vi[2 * q + 1]), nbi);
-      const float2 la = mul2(bc2(nk), r);
-      float2 abar, om;
-      if (GENERAL)
-        decay_fast2(la, abar, om);
-      else
-        decay_near2(la, abar, om);
-      float2 m = sqrt_fast2(om);
+      const float2 lr = make_float2(vr[2 * q], vr[2 * q + 1]);
+      const float2 li = make_float2(vi[2 * q], vi[2 * q + 1]);
+      float2 abar, mi, r;
       if (GENERAL) {
+        float2 i;
+        gates_any2(lr, li, gk, abar, mi, r, i);
         if ((rmask >> u) & 1u) {
           abar.x = 0.0f;
-          m.x = 1.0f;
+          mi.x = i.x;
         }
         if ((rmask >> (u + 1)) & 1u) {
           abar.y = 0.0f;
-          m.y = 1.0f;
+          mi.y = i.y;
         }
         if (u >= valid) {
           abar.x = 1.0f;
-          m.x = 0.0f;
+          mi.x = 0.0f;
         }
         if (u + 1 >= valid) {
           abar.y = 1.0f;
-          m.y = 0.0f;
+          mi.y = 0.0f;
         }
+      } else {
+        gates_near2(lr, li, gk, abar, mi, r);
       }
-      const float2 bv = mul2(m, mul2(i, xv));
+      const float2 bv = mul2(mi, xv);
       rh = fmaf(abar.x, rh, bv.x);
       rA *= abar.x;
       oh[2 * q] = rh;
@@ -264,9 +262,11 @@ __global__ void __maxnreg__(MAXREG)
     const int w = blk * FUSED_K + j;
     const int tb = part * PT;
     const uint32_t lane_base = (uint32_t)(q * 32) << 16;
-    const float nk = -8.0f * softplus_f(p.Lambda[w]);  // log a = nk * r
-    const float nbr = p.ba ? -p.ba[w] * LOG2E : 0.0f;   // bias folded into the exponent
-    const float nbi = p.bx ? -p.bx[w] * LOG2E : 0.0f;
+    GateK gk;
+    gk.nk = -8.0f * softplus_f(p.Lambda[w]);  // log a = nk * r
+    gk.cm = sqrtf(-2.0f * gk.nk);
+    gk.nbr = p.ba ? -p.ba[w] * LOG2E : 0.0f;  // biases folded into the exponents
+    gk.nbi = p.bx ? -p.bx[w] * LOG2E : 0.0f;
     float* carry = reinterpret_cast<float*>(p.scratch + p.L.carry);
     float2* agg = reinterpret_cast<float2*>(p.scratch + p.L.agg);
     const bool store_thread = (warp == 2 && lane == 0);
@@ -282,7 +282,7 @@ __global__ void __maxnreg__(MAXREG)
     // TMEM) and then finishes tile it-1, whose look-back slots have had a whole tile's time
     // to fill.
     // Warp-uniform: every channel of this warp has la > -1/8 on every token.
-    const bool near_all = __all_sync(0xffffffffu, nk > -0.125f);
+    const bool near_all = __all_sync(0xffffffffu, gk.nk > NEAR_LA);
 
     TileWalk cur(rr, p.P, p.B);  // tile it
     int pc = 0, pb = 0;          // chunk and row of tile it - 1
@@ -326,9 +326,9 @@ __global__ void __maxnreg__(MAXREG)
         const uint32_t park = tmem + lane_base + PARK_COL + a * 128 + part * 2 * PT;
         float rh, rA;
         if (near_all && rmask == 0u && valid >= PT)
-          local_scan<false>(t_lr, t_lr + 64, park, xb0, xb1, nk, nbr, nbi, 0u, PT, rh, rA);
+          local_scan<false>(t_lr, t_lr + 64, park, xb0, xb1, gk, 0u, PT, rh, rA);
         else
-          local_scan<true>(t_lr, t_lr + 64, park, xb0, xb1, nk, nbr, nbi, rmask, valid, rh, rA);
+          local_scan<true>(t_lr, t_lr + 64, park, xb0, xb1, gk, rmask, valid, rh, rA);
         tc::tc_fence_before();
         __syncwarp();
         if (lane == 0) {
@@ -384,19 +384,23 @@ __global__ void __maxnreg__(MAXREG)
           if (c == p.nC - 1 && p.hT) p.hT[(size_t)b * p.W + w] = hend;
         }
         const float hin = fmaf(Ae, hin_t, Be);
-        float hl[PT], Ac[PT];
         const uint32_t park = tmem + lane_base + PARK_COL + a * 128 + part * 2 * PT;
-        tc::tmem_ld16(park, hl);
-        tc::tmem_ld16(park + PT, Ac);
-        tc::tmem_ld_wait();
         // y tile: registers -> smem [token][channel] -> TMA store (clipped at T)
 #pragma unroll
-        for (int u = 0; u < PT; u += 2) {
-          const float2 yv =
-              fma2(make_float2(Ac[u], Ac[u + 1]), bc2(hin), make_float2(hl[u], hl[u + 1]));
-          *reinterpret_cast<bf16*>(s_y + (tb + u) * (FUSED_K * 2) + j * 2) = __float2bfloat16_rn(yv.x);
-          *reinterpret_cast<bf16*>(s_y + (tb + u + 1) * (FUSED_K * 2) + j * 2) =
-              __float2bfloat16_rn(yv.y);
+        for (int c16 = 0; c16 < PT; c16 += 16) {
+          float hl[16], Ac[16];
+          tc::tmem_ld16(park + c16, hl);
+          tc::tmem_ld16(park + PT + c16, Ac);
+          tc::tmem_ld_wait();
+#pragma unroll
+          for (int u = 0; u < 16; u += 2) {
+            const float2 yv =
+                fma2(make_float2(Ac[u], Ac[u + 1]), bc2(hin), make_float2(hl[u], hl[u + 1]));
+            const int tl = tb + c16 + u;
+            *reinterpret_cast<bf16*>(s_y + tl * (FUSED_K * 2) + j * 2) = __float2bfloat16_rn(yv.x);
+            *reinterpret_cast<bf16*>(s_y + (tl + 1) * (FUSED_K * 2) + j * 2) =
+                __float2bfloat16_rn(yv.y);
+          }
         }
         tc::fence_proxy_async_smem();
       }

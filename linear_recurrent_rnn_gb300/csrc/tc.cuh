@@ -265,6 +265,14 @@ __device__ __forceinline__ void tmem_st_wait() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
+// The loads and stores above by array size.
+__device__ __forceinline__ void tmem_ld(uint32_t taddr, float (&v)[4]) { tmem_ld4(taddr, v); }
+__device__ __forceinline__ void tmem_ld(uint32_t taddr, float (&v)[8]) { tmem_ld8(taddr, v); }
+__device__ __forceinline__ void tmem_ld(uint32_t taddr, float (&v)[16]) { tmem_ld16(taddr, v); }
+__device__ __forceinline__ void tmem_st(uint32_t taddr, const float (&v)[4]) { tmem_st4(taddr, v); }
+__device__ __forceinline__ void tmem_st(uint32_t taddr, const float (&v)[8]) { tmem_st8(taddr, v); }
+__device__ __forceinline__ void tmem_st(uint32_t taddr, const float (&v)[16]) { tmem_st16(taddr, v); }
+
 // ---------------------------------------------------------------- descriptors
 // Shared-memory matrix descriptor (sm_100 format): start address, leading / stride byte
 // offsets (>> 4), version 1 at bits 46-47, layout type at bits 61-63 (6 = 32-byte swizzle).
