@@ -212,6 +212,15 @@ __device__ __forceinline__ float lds_bf16(uint32_t addr) {
 __device__ __forceinline__ float tok_elem(uint32_t b0, uint32_t b1, int tt) {
   return lds_bf16((((tt >> 2) & 1) ? b1 : b0) + tt * 32);
 }
+// The raw bf16 bits of the same element, and two of them packed (token u in the low half).
+__device__ __forceinline__ uint32_t tok_raw(uint32_t b0, uint32_t b1, int tt) {
+  uint16_t v;
+  asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"((((tt >> 2) & 1) ? b1 : b0) + tt * 32));
+  return v;
+}
+__device__ __forceinline__ float2 bf16x2_unpack(uint32_t v) {
+  return make_float2(__uint_as_float(v << 16), __uint_as_float(v & 0xffff0000u));
+}
 
 // ---------------------------------------------------------------- tile walks
 // Chunk c and batch row b of the tiles n = r, r + P, r + 2P, ... of one gate block, with
@@ -230,12 +239,13 @@ struct TileWalk {
 };
 
 // ---------------------------------------------------------------- value-as-flag slots
-// Look-back slots of the fused kernels carry their own readiness: a slot holds the all-ones
-// bit pattern (a NaN that float arithmetic never produces) until its value is stored with a
-// single-copy-atomic store.  A reader polls the slot itself, so one L2 round trip delivers
-// both the "ready" signal and the value.
-constexpr uint32_t SLOT_EMPTY32 = 0xffffffffu;
-constexpr uint64_t SLOT_EMPTY64 = 0xffffffffffffffffull;
+// Look-back slots of the fused kernels carry their own readiness: a value is stored bitwise
+// inverted with a single-copy-atomic store, so a slot reads zero until it is written (zero is
+// the inverse of the all-ones NaN, which float arithmetic never produces).  A reader polls the
+// slot itself, so one L2 round trip delivers both the "ready" signal and the value; and one
+// zero fill clears the slots together with the status word and counters before a call.
+constexpr uint32_t SLOT_EMPTY32 = 0u;
+constexpr uint64_t SLOT_EMPTY64 = 0ull;
 
 __device__ __forceinline__ uint64_t ld_relaxed_u64(const void* p) {
   uint64_t v;
@@ -253,10 +263,22 @@ __device__ __forceinline__ void st_relaxed_u64(void* p, uint64_t v) {
 __device__ __forceinline__ void st_relaxed_u32(void* p, uint32_t v) {
   asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
-__device__ __forceinline__ void slot_put2(float2* p, float a, float b) {
-  st_relaxed_u64(p, ((uint64_t)__float_as_uint(b) << 32) | __float_as_uint(a));
+__device__ __forceinline__ uint32_t slot_enc1(float a) { return ~__float_as_uint(a); }
+__device__ __forceinline__ uint64_t slot_enc2(float a, float b) {
+  return ~(((uint64_t)__float_as_uint(b) << 32) | __float_as_uint(a));
 }
-__device__ __forceinline__ void slot_put1(float* p, float a) { st_relaxed_u32(p, __float_as_uint(a)); }
+__device__ __forceinline__ float slot_dec1(uint32_t v) { return __uint_as_float(~v); }
+__device__ __forceinline__ float2 slot_dec2(uint64_t v) {
+  return make_float2(__uint_as_float(~(uint32_t)v), __uint_as_float(~(uint32_t)(v >> 32)));
+}
+__device__ __forceinline__ void slot_put2(float2* p, float a, float b) {
+  st_relaxed_u64(p, slot_enc2(a, b));
+}
+__device__ __forceinline__ void slot_put1(float* p, float a) { st_relaxed_u32(p, slot_enc1(a)); }
+// A slot written before this kernel started (plain load).
+__device__ __forceinline__ float slot_get1(const float* p) {
+  return slot_dec1(*reinterpret_cast<const uint32_t*>(p));
+}
 
 // Reset flag of token (b, t) in canonical mode.
 __device__ __forceinline__ bool is_reset(const uint8_t* reset_mask, const int32_t* segment_pos,

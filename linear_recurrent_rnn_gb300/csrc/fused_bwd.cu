@@ -48,7 +48,7 @@ namespace rglru {
 
 namespace {
 
-constexpr int NPART = 4;             // token parts of a tile, one scan thread each per channel
+constexpr int NPART = 2;             // token parts of a tile, one scan thread each per channel
 constexpr int PT = FUSED_C / NPART;  // tokens per scan thread
 constexpr int NSCAN = 4 * NPART;     // scan warps (4 lane quadrants per part)
 constexpr int NTHREADS = 64 + NSCAN * 32;
@@ -61,6 +61,7 @@ constexpr uint32_t T_BYTES = FUSED_C * FUSED_K * 2;  // one 64 x 128 bf16 tile
 constexpr uint32_t SLAB_X = FUSED_C * 32;            // 16 channels x 64 tokens
 constexpr uint32_t SLAB_W = FUSED_K * 32;            // 16 out-channels x 128 in-rows
 constexpr uint32_t SLAB_D = FUSED_K * 32;            // 16 tokens x 128 channels (dl buffers)
+constexpr uint32_t DY_ROW = FUSED_K * 2;             // dy tiles: [token][channel], unswizzled
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t COL_LR = 0, COL_LI = 64, COL_DX = 128, COL_HP = 192, COL_DWA = 256,
                    COL_DWX = 384;
@@ -71,6 +72,7 @@ constexpr size_t SMEM_BYTES =
     2 * W_BYTES + STAGES * 2 * T_BYTES + 4 * T_BYTES + T_BYTES + XCH_BYTES + 256 + 1024;
 constexpr uint32_t STATUS_PIPE = 2u;
 constexpr int BAR_SCAN = 1;  // named barrier of the scan warps
+constexpr uint32_t DW_BOX_BYTES = FUSED_K * 128;  // 128 rows x 32 float32 columns
 // Workspace offset of the per-gate-block counters of CTAs done with their partial sums
 // (zeroed with the status word before every launch).
 constexpr size_t BWD_COUNTERS = 256;
@@ -83,7 +85,7 @@ struct BwdParams {
   const uint8_t* reset_mask;
   const int32_t* segment_pos;
   const float* dhT;
-  const float* fwd_carry;  // [B][nC+1][W], state entering each chunk
+  const float* fwd_carry;  // [B][nC+1][W], state entering each chunk (slot-encoded)
   float* dh0;
   void* dx;                // written directly for float32 gradients
   float* dWa;
@@ -119,24 +121,26 @@ __device__ __forceinline__ void split_hi_lo(float2 v, uint32_t& hi, uint32_t& lo
   lo = *reinterpret_cast<const uint32_t*>(&lb);
 }
 
-// Writes 4 consecutive tokens of channel j (tokens u .. u + 3 of 16-token group tg, u a
-// multiple of 4) as hi and lo bf16 parts into the dl operand buffers [tg][channel row][16
-// tokens] (32-byte swizzle: the row's two 16-byte halves swap on rows 4..7 of every 8).
-__device__ __forceinline__ void store_dl4(uint8_t* hi_buf, uint8_t* lo_buf, int tg, int u, int j,
-                                          float2 v01, float2 v23) {
-  uint2 hi, lo;
-  split_hi_lo(v01, hi.x, lo.x);
-  split_hi_lo(v23, hi.y, lo.y);
-  const uint32_t at = tg * SLAB_D + j * 32 + (((u >> 3) ^ ((j >> 2) & 1)) << 4) + ((u >> 2) & 1) * 8;
-  *reinterpret_cast<uint2*>(hi_buf + at) = hi;
-  *reinterpret_cast<uint2*>(lo_buf + at) = lo;
+// Writes 8 consecutive tokens u .. u + 7 of channel j (tu = their first token in the tile, a
+// multiple of 8) as hi and lo bf16 parts, 16 bytes each: conflict-free, as the swizzle puts
+// rows 4..7 of every 8 in the other half of the bank space.
+__device__ __forceinline__ void store_dl8(uint8_t* hi_buf, uint8_t* lo_buf, int tu, int j,
+                                          const float2 (&v)[4]) {
+  uint4 hi, lo;
+  split_hi_lo(v[0], hi.x, lo.x);
+  split_hi_lo(v[1], hi.y, lo.y);
+  split_hi_lo(v[2], hi.z, lo.z);
+  split_hi_lo(v[3], hi.w, lo.w);
+  const uint32_t at = (tu >> 4) * SLAB_D + j * 32 + ((((tu >> 3) & 1) ^ ((j >> 2) & 1)) << 4);
+  *reinterpret_cast<uint4*>(hi_buf + at) = hi;
+  *reinterpret_cast<uint4*>(lo_buf + at) = lo;
 }
 
 // The passes of a scan thread over its part's 16 tokens do the pointwise work on token pairs
 // (u, u + 1) in the two lanes of f32x2 operations (adjacent TMEM columns land in adjacent
 // registers) and run the recurrences as scalar chains.  Per-token values parked in TMEM sit at
 // column = token of the part; the thread's columns of each region start at tcol.
-constexpr int GRP = 4;  // tokens per TMEM load / store group
+constexpr int GRP = 8;  // tokens per TMEM load / store group
 
 // Pass 1 (tokens ascending): the gates once; abar stays in registers, m i -> COL_LR and r ->
 // COL_LI (over the logits, already read), i -> COL_HP; returns the part's maps: forward
@@ -144,24 +148,33 @@ constexpr int GRP = 4;  // tokens per TMEM load / store group
 // to t) dy_t.  GENERAL = false is the warp-uniform fast path: every token valid, no reset,
 // every decay in the near regime.
 template <bool GENERAL>
-__device__ __forceinline__ void bwd_pass1(uint32_t tcol, uint32_t xb0, uint32_t xb1,
+__device__ __forceinline__ void bwd_pass1(uint32_t tcol, uint32_t xb0, uint32_t xb1, uint32_t dyb,
                                           const GateK& gk, uint32_t rmask, int valid,
-                                          float2 (&ab)[PT / 2], float& P, float& fB, float& S) {
+                                          float2 (&ab)[PT / 2], uint32_t (&xr)[PT / 2], float& P,
+                                          float& fB, float& S) {
   P = 1.0f;
   fB = 0.0f;
   S = 0.0f;
+  // the TMEM loads of group g + 1 are issued before group g is computed
+  float vr[GRP], vi[GRP];
+  tc::tmem_ld(tcol + COL_LR, vr);
+  tc::tmem_ld(tcol + COL_LI, vi);
+  tc::tmem_ld_wait();
+  tc::reg_fence(vr);
+  tc::reg_fence(vi);
 #pragma unroll
   for (int g = 0; g < PT / GRP; ++g) {
-    float vr[GRP], vi[GRP], m4[GRP];
-    tc::tmem_ld(tcol + COL_LR + g * GRP, vr);
-    tc::tmem_ld(tcol + COL_LI + g * GRP, vi);
-    tc::tmem_ld_wait();
+    float m4[GRP], nr[GRP], ni[GRP];
+    if (g + 1 < PT / GRP) {
+      tc::tmem_ld(tcol + COL_LR + (g + 1) * GRP, nr);
+      tc::tmem_ld(tcol + COL_LI + (g + 1) * GRP, ni);
+    }
 #pragma unroll
     for (int q = 0; q < GRP / 2; ++q) {
       const int u = g * GRP + 2 * q;
-      const float2 xv = make_float2(tok_elem(xb0, xb1, u), tok_elem(xb0, xb1, u + 1));
-      float2 dyv = make_float2(tok_elem(xb0 + T_BYTES, xb1 + T_BYTES, u),
-                               tok_elem(xb0 + T_BYTES, xb1 + T_BYTES, u + 1));
+      xr[u / 2] = tok_raw(xb0, xb1, u) | (tok_raw(xb0, xb1, u + 1) << 16);
+      const float2 xv = bf16x2_unpack(xr[u / 2]);
+      float2 dyv = make_float2(lds_bf16(dyb + u * DY_ROW), lds_bf16(dyb + (u + 1) * DY_ROW));
       const float2 lr = make_float2(vr[2 * q], vr[2 * q + 1]);
       const float2 li = make_float2(vi[2 * q], vi[2 * q + 1]);
       float2 abar, mi, r, i;
@@ -206,23 +219,36 @@ __device__ __forceinline__ void bwd_pass1(uint32_t tcol, uint32_t xb0, uint32_t 
     tc::tmem_st(tcol + COL_LR + g * GRP, m4);
     tc::tmem_st(tcol + COL_LI + g * GRP, vr);
     tc::tmem_st(tcol + COL_HP + g * GRP, vi);
+    if (g + 1 < PT / GRP) {
+      tc::tmem_ld_wait();
+      tc::reg_fence(nr);
+      tc::reg_fence(ni);
+#pragma unroll
+      for (int u = 0; u < GRP; ++u) {
+        vr[u] = nr[u];
+        vi[u] = ni[u];
+      }
+    }
   }
   tc::tmem_st_wait();
 }
 
 // Pass 2a (tokens ascending): h_{t-1} of every token from the state h entering the part,
 // parked in the dx columns (free once the previous tile's dx has been written out).
-__device__ __forceinline__ void bwd_pass2a(uint32_t tcol, uint32_t xb0, uint32_t xb1,
+__device__ __forceinline__ void bwd_pass2a(uint32_t tcol, const uint32_t (&xr)[PT / 2],
                                            const float2 (&ab)[PT / 2], float h) {
+  float m4[GRP];
+  tc::tmem_ld(tcol + COL_LR, m4);
+  tc::tmem_ld_wait();
+  tc::reg_fence(m4);
 #pragma unroll
   for (int g = 0; g < PT / GRP; ++g) {
-    float m4[GRP], h4[GRP];
-    tc::tmem_ld(tcol + COL_LR + g * GRP, m4);
-    tc::tmem_ld_wait();
+    float h4[GRP], nm[GRP];
+    if (g + 1 < PT / GRP) tc::tmem_ld(tcol + COL_LR + (g + 1) * GRP, nm);
 #pragma unroll
     for (int q = 0; q < GRP / 2; ++q) {
       const int u = g * GRP + 2 * q;
-      const float2 xv = make_float2(tok_elem(xb0, xb1, u), tok_elem(xb0, xb1, u + 1));
+      const float2 xv = bf16x2_unpack(xr[u / 2]);
       const float2 bv = mul2(make_float2(m4[2 * q], m4[2 * q + 1]), xv);
       h4[2 * q] = h;
       h = fmaf(ab[u / 2].x, h, bv.x);
@@ -230,6 +256,12 @@ __device__ __forceinline__ void bwd_pass2a(uint32_t tcol, uint32_t xb0, uint32_t
       h = fmaf(ab[u / 2].y, h, bv.y);
     }
     tc::tmem_st(tcol + COL_DX + g * GRP, h4);
+    if (g + 1 < PT / GRP) {
+      tc::tmem_ld_wait();
+      tc::reg_fence(nm);
+#pragma unroll
+      for (int u = 0; u < GRP; ++u) m4[u] = nm[u];
+    }
   }
   tc::tmem_st_wait();
 }
@@ -239,26 +271,37 @@ __device__ __forceinline__ void bwd_pass2a(uint32_t tcol, uint32_t xb0, uint32_t
 // hi + lo pairs, the direct dx term g m i over h_{t-1} in the dx columns (the accumulator of
 // the dx MMAs).  dsp sums dla r (the softplus gradient is -8 times the total).
 template <bool GENERAL>
-__device__ __forceinline__ void bwd_pass2b(uint32_t tcol, int tb, int j, uint32_t xb0,
-                                           uint32_t xb1, float nk, int valid,
-                                           const float2 (&ab)[PT / 2], float cin, uint8_t* s_dl,
-                                           float2& dsp, float2& dba, float2& dbx) {
+__device__ __forceinline__ void bwd_pass2b(uint32_t tcol, int tb, int j,
+                                           const uint32_t (&xr)[PT / 2], uint32_t dyb, float nk,
+                                           int valid, const float2 (&ab)[PT / 2], float cin,
+                                           uint8_t* s_dl, float2& dsp, float2& dba, float2& dbx) {
   float gnext = cin, anext = 1.0f;
+  constexpr int G0 = PT / GRP - 1;
+  float m4[GRP], r4[GRP], i4[GRP], h4[GRP];
+  tc::tmem_ld(tcol + COL_LR + G0 * GRP, m4);
+  tc::tmem_ld(tcol + COL_LI + G0 * GRP, r4);
+  tc::tmem_ld(tcol + COL_HP + G0 * GRP, i4);
+  tc::tmem_ld(tcol + COL_DX + G0 * GRP, h4);
+  tc::tmem_ld_wait();
+  tc::reg_fence(m4);
+  tc::reg_fence(r4);
+  tc::reg_fence(i4);
+  tc::reg_fence(h4);
 #pragma unroll
-  for (int g = PT / GRP - 1; g >= 0; --g) {
-    float m4[GRP], r4[GRP], i4[GRP], h4[GRP];
-    tc::tmem_ld(tcol + COL_LR + g * GRP, m4);
-    tc::tmem_ld(tcol + COL_LI + g * GRP, r4);
-    tc::tmem_ld(tcol + COL_HP + g * GRP, i4);
-    tc::tmem_ld(tcol + COL_DX + g * GRP, h4);
-    tc::tmem_ld_wait();
+  for (int g = G0; g >= 0; --g) {
+    float nm[GRP], nr[GRP], ni[GRP], nh[GRP];
+    if (g > 0) {
+      tc::tmem_ld(tcol + COL_LR + (g - 1) * GRP, nm);
+      tc::tmem_ld(tcol + COL_LI + (g - 1) * GRP, nr);
+      tc::tmem_ld(tcol + COL_HP + (g - 1) * GRP, ni);
+      tc::tmem_ld(tcol + COL_DX + (g - 1) * GRP, nh);
+    }
     float2 o_r[GRP / 2], o_i[GRP / 2];  // tokens (u, u + 1) of the two pairs
 #pragma unroll
     for (int q = GRP / 2 - 1; q >= 0; --q) {
       const int u = g * GRP + 2 * q;
-      const float2 xv = make_float2(tok_elem(xb0, xb1, u), tok_elem(xb0, xb1, u + 1));
-      float2 dyv = make_float2(tok_elem(xb0 + T_BYTES, xb1 + T_BYTES, u),
-                               tok_elem(xb0 + T_BYTES, xb1 + T_BYTES, u + 1));
+      const float2 xv = bf16x2_unpack(xr[u / 2]);
+      float2 dyv = make_float2(lds_bf16(dyb + u * DY_ROW), lds_bf16(dyb + (u + 1) * DY_ROW));
       if (GENERAL) {
         if (u >= valid) dyv.x = 0.0f;
         if (u + 1 >= valid) dyv.y = 0.0f;
@@ -288,14 +331,24 @@ __device__ __forceinline__ void bwd_pass2b(uint32_t tcol, int tb, int j, uint32_
       h4[2 * q] = dd.x;
       h4[2 * q + 1] = dd.y;
     }
-#pragma unroll
-    for (int f = 0; f < GRP / 4; ++f) {
-      const int tu = tb + g * GRP + 4 * f;  // first token of the four within the tile
-      store_dl4(s_dl, s_dl + T_BYTES, tu >> 4, tu & 15, j, o_r[2 * f], o_r[2 * f + 1]);
-      store_dl4(s_dl + 2 * T_BYTES, s_dl + 3 * T_BYTES, tu >> 4, tu & 15, j, o_i[2 * f],
-                o_i[2 * f + 1]);
-    }
+    static_assert(GRP == 8, "the dl stores take 8 tokens");
+    store_dl8(s_dl, s_dl + T_BYTES, tb + g * GRP, j, o_r);
+    store_dl8(s_dl + 2 * T_BYTES, s_dl + 3 * T_BYTES, tb + g * GRP, j, o_i);
     tc::tmem_st(tcol + COL_DX + g * GRP, h4);
+    if (g > 0) {
+      tc::tmem_ld_wait();
+      tc::reg_fence(nm);
+      tc::reg_fence(nr);
+      tc::reg_fence(ni);
+      tc::reg_fence(nh);
+#pragma unroll
+      for (int u = 0; u < GRP; ++u) {
+        m4[u] = nm[u];
+        r4[u] = nr[u];
+        i4[u] = ni[u];
+        h4[u] = nh[u];
+      }
+    }
   }
   tc::tmem_st_wait();
 }
@@ -304,7 +357,8 @@ template <typename GT>
 __global__ void __maxnreg__(MAXREG)
     k_fused_bwd(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_dy,
                 const __grid_constant__ CUtensorMap tm_wa, const __grid_constant__ CUtensorMap tm_wx,
-                const __grid_constant__ CUtensorMap tm_dx, BwdParams p) {
+                const __grid_constant__ CUtensorMap tm_dx,
+                const __grid_constant__ CUtensorMap tm_dwp, BwdParams p) {
   extern __shared__ uint8_t smem_raw[];
   // 1024-byte aligned base, formed by pointer arithmetic so that it stays a shared pointer
   uint8_t* smem = smem_raw + ((1024u - (tc::smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -376,12 +430,10 @@ __global__ void __maxnreg__(MAXREG)
         const int c = p.nC - 1 - tw.c, b = tw.b;
         uint8_t* xs = s_in + st * 2 * T_BYTES;
         tc::mbar_expect_tx(&in_full[st], 2 * T_BYTES);
-        for (int s = 0; s < FUSED_K / 16; ++s) {
+        for (int s = 0; s < FUSED_K / 16; ++s)
           tc::tma_load_3d(xs + s * SLAB_X, &tm_x, &in_full[st], blk * FUSED_K + 16 * s,
                           c * FUSED_C, b);
-          tc::tma_load_3d(xs + T_BYTES + s * SLAB_X, &tm_dy, &in_full[st],
-                          blk * FUSED_K + 16 * s, c * FUSED_C, b);
-        }
+        tc::tma_load_3d(xs + T_BYTES, &tm_dy, &in_full[st], blk * FUSED_K, c * FUSED_C, b);
       }
     }
   } else if (warp == 1) {
@@ -496,7 +548,9 @@ __global__ void __maxnreg__(MAXREG)
       const uint32_t ph = (it / STAGES) & 1;
       const uint32_t xt = tc::smem_u32(s_in + st * 2 * T_BYTES + tb * 32);
       const uint32_t xb0 = xt + xoff0, xb1 = xt + xoff1;
+      const uint32_t dyb = tc::smem_u32(s_in + st * 2 * T_BYTES + T_BYTES + tb * DY_ROW + j * 2);
       float2 ab[PT / 2];
+      uint32_t xr[PT / 2];  // x of the part's tokens, bf16 pairs
       float P = 1.0f, fB = 0.0f, S = 0.0f;
       float hin_tile = 0.0f;
       int valid = 0;
@@ -518,7 +572,7 @@ __global__ void __maxnreg__(MAXREG)
                        p.dhT ? p.dhT[(size_t)b * p.W + w] : 0.0f);
       }
       if (have) {
-        hin_tile = p.fwd_carry[((size_t)b * (p.nC + 1) + c) * p.W + w];
+        hin_tile = slot_get1(p.fwd_carry + ((size_t)b * (p.nC + 1) + c) * p.W + w);
         uint32_t rmask = 0;
         if (p.canonical) {
           const int t = c * FUSED_C + tb + lane;
@@ -532,9 +586,9 @@ __global__ void __maxnreg__(MAXREG)
         ctl.wait(&in_full[st], ph);
         tc::tc_fence_after();
         if (fast)
-          bwd_pass1<false>(tcol, xb0, xb1, gk, 0u, PT, ab, P, fB, S);
+          bwd_pass1<false>(tcol, xb0, xb1, dyb, gk, 0u, PT, ab, xr, P, fB, S);
         else
-          bwd_pass1<true>(tcol, xb0, xb1, gk, rmask, valid, ab, P, fB, S);
+          bwd_pass1<true>(tcol, xb0, xb1, dyb, gk, rmask, valid, ab, xr, P, fB, S);
       }
 
       // dx of tile it - 1: TMEM -> smem [token][channel] as bf16 (float32 goes straight to HBM).
@@ -603,7 +657,7 @@ __global__ void __maxnreg__(MAXREG)
 
       // Pass 2a: h_{t-1} through the part, from the earlier parts' map applied to the tile's
       // entry state.
-      bwd_pass2a(tcol, xb0, xb1, ab, fmaf(Fa, hin_tile, Fb));
+      bwd_pass2a(tcol, xr, ab, fmaf(Fa, hin_tile, Fb));
 
       if (part == 0) {
         const float cin =
@@ -621,9 +675,9 @@ __global__ void __maxnreg__(MAXREG)
       if (it > 0) ctl.wait(dl_empty, (it - 1) & 1);
       tc::tc_fence_after();
       if (fast)
-        bwd_pass2b<false>(tcol, tb, j, xb0, xb1, gk.nk, PT, ab, cin, s_dl, dsp, dba, dbx);
+        bwd_pass2b<false>(tcol, tb, j, xr, dyb, gk.nk, PT, ab, cin, s_dl, dsp, dba, dbx);
       else
-        bwd_pass2b<true>(tcol, tb, j, xb0, xb1, gk.nk, valid, ab, cin, s_dl, dsp, dba, dbx);
+        bwd_pass2b<true>(tcol, tb, j, xr, dyb, gk.nk, valid, ab, cin, s_dl, dsp, dba, dbx);
       tc::fence_proxy_async_smem();
       tc::tc_fence_before();
       __syncwarp();
@@ -642,14 +696,15 @@ __global__ void __maxnreg__(MAXREG)
     vp[FUSED_K + j] = dba.x + dba.y;
     vp[2 * FUSED_K + j] = dbx.x + dbx.y;
 
-    // Per-CTA dW partials: lane j of the accumulators is input channel j; each part copies
-    // 128 / NPART of the output-channel columns.
+    // Per-CTA dW partials: lane j of the accumulators is input channel j; each part takes
+    // 128 / NPART of the output-channel columns.  TMEM -> shared memory (the x / dy stages and
+    // the dl buffers are free now: row j of 128-byte-swizzled boxes of 32 columns, conflict-free
+    // 16-byte stores) -> TMA store of 4 boxes per matrix.
     if (my_tiles > 0) ctl.wait(dl_empty, (my_tiles - 1) & 1);
     tc::tc_fence_after();
-    float* dwp = reinterpret_cast<float*>(p.scratch + p.F.dw_part) +
-                 (size_t)blockIdx.x * 2 * FUSED_K * FUSED_K;
 #pragma unroll
     for (int mtx = 0; mtx < 2; ++mtx) {
+      uint8_t* stage = mtx ? s_dl : s_in;
 #pragma unroll
       for (int sub = 0; sub < FUSED_K / NPART / 16; ++sub) {
         const int col = part * (FUSED_K / NPART) + sub * 16;
@@ -661,10 +716,26 @@ __global__ void __maxnreg__(MAXREG)
 #pragma unroll
           for (int u = 0; u < 16; ++u) v[u] = 0.0f;
         }
-        float4* dst = reinterpret_cast<float4*>(dwp + ((size_t)mtx * FUSED_K + j) * FUSED_K + col);
+        uint8_t* row = stage + (col >> 5) * DW_BOX_BYTES + j * 128;
+        const int c0 = (col & 31) >> 2;  // the row's first 16-byte chunk
 #pragma unroll
-        for (int u = 0; u < 4; ++u) dst[u] = make_float4(v[4 * u], v[4 * u + 1], v[4 * u + 2], v[4 * u + 3]);
+        for (int u = 0; u < 4; ++u)
+          *reinterpret_cast<float4*>(row + (((c0 + u) ^ (j & 7)) << 4)) =
+              make_float4(v[4 * u], v[4 * u + 1], v[4 * u + 2], v[4 * u + 3]);
       }
+    }
+    tc::fence_proxy_async_smem();
+    tc::named_bar(BAR_SCAN, NSCAN * 32);
+    if (store_thread) {
+#pragma unroll
+      for (int mtx = 0; mtx < 2; ++mtx)
+#pragma unroll
+        for (int bx = 0; bx < FUSED_K / 32; ++bx)
+          tc::tma_store_2d(&tm_dwp, (mtx ? s_dl : s_in) + bx * DW_BOX_BYTES, bx * 32,
+                           ((int)blockIdx.x * 2 + mtx) * FUSED_K);
+      tc::tma_store_commit();
+      tc::tma_store_wait0();  // the partials are in global memory before the block's counter
+      tc::fence_proxy_async_global();
     }
   }
 
@@ -762,12 +833,13 @@ cudaError_t launch_fused_bwd(const Dims& d, const void* dy, const float* dhT, co
   const uint64_t dims3[3] = {W, T, B};
   const uint64_t str3[2] = {W * 2, T * W * 2};
   const uint32_t box_in[3] = {16, FUSED_C, 1};
-  CUtensorMap mx, mdy, mwa, mwx, mdx;
+  CUtensorMap mx, mdy, mwa, mwx, mdx, mdwp;
   cudaError_t e = encode_tmap(&mx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, x, dims3, str3, box_in,
                               CU_TENSOR_MAP_SWIZZLE_32B);
+  const uint32_t box_dy[3] = {FUSED_K, FUSED_C, 1};  // one unswizzled [token][channel] tile
   if (e == cudaSuccess)
-    e = encode_tmap(&mdy, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, dy, dims3, str3, box_in,
-                    CU_TENSOR_MAP_SWIZZLE_32B);
+    e = encode_tmap(&mdy, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, dy, dims3, str3, box_dy,
+                    CU_TENSOR_MAP_SWIZZLE_NONE);
   const uint64_t dimsw[2] = {(uint64_t)d.k, (uint64_t)d.nblk * d.k};
   const uint64_t strw[1] = {(uint64_t)d.k * 2};
   const uint32_t box_w[2] = {16, FUSED_K};
@@ -784,6 +856,15 @@ cudaError_t launch_fused_bwd(const Dims& d, const void* dy, const float* dhT, co
   if (e == cudaSuccess)
     e = encode_tmap(&mdx, gf32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
                     3, dx, dims3, strg, box_dx, CU_TENSOR_MAP_SWIZZLE_NONE);
+  const FusedBwdLayout F = fused_bwd_layout(d);
+  const int grid = fused_ctas_per_block(d) * d.nblk;
+  // per-CTA dW partials [cta][2][k][k] float32 viewed as [cta * 2 * k rows][k columns]
+  const uint64_t dims_p[2] = {(uint64_t)FUSED_K, (uint64_t)grid * 2 * FUSED_K};
+  const uint64_t str_p[1] = {(uint64_t)FUSED_K * 4};
+  const uint32_t box_p[2] = {32, FUSED_K};
+  if (e == cudaSuccess)
+    e = encode_tmap(&mdwp, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, static_cast<uint8_t*>(ws) + F.dw_part,
+                    dims_p, str_p, box_p, CU_TENSOR_MAP_SWIZZLE_128B);
   if (e != cudaSuccess) return e;
 
   BwdParams p;
@@ -804,7 +885,7 @@ cudaError_t launch_fused_bwd(const Dims& d, const void* dy, const float* dhT, co
                                                fused_layout(d, false).carry);
   p.dh0 = dh0;
   p.scratch = static_cast<uint8_t*>(ws);
-  p.F = fused_bwd_layout(d);
+  p.F = F;
   p.spin_limit = spin_limit;
   p.drop_tile = drop_tile;
   const LookbackPlan lp = lookback_plan(p.P, d.B);
@@ -820,10 +901,10 @@ cudaError_t launch_fused_bwd(const Dims& d, const void* dy, const float* dhT, co
   auto kern = gf32 ? k_fused_bwd<float> : k_fused_bwd<bf16>;
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  e = clear_slots(ws, p.F.L, s, BWD_COUNTERS + (size_t)d.nblk * 4);
+  e = clear_slots(ws, p.F.L, s);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(p.P * d.nblk);
+  cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(NTHREADS);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
@@ -833,7 +914,7 @@ cudaError_t launch_fused_bwd(const Dims& d, const void* dy, const float* dhT, co
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   kernel_event_before(s);
-  e = cudaLaunchKernelEx(&cfg, kern, mx, mdy, mwa, mwx, mdx, p);
+  e = cudaLaunchKernelEx(&cfg, kern, mx, mdy, mwa, mwx, mdx, mdwp, p);
   kernel_event_after(s);
   if (e != cudaSuccess) return e;
   note_launches(1);

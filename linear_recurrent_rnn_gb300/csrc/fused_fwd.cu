@@ -13,15 +13,18 @@
 // Tile = (batch row b, gate block blk, 64 tokens).  For the tile the MMA computes the
 // transposed logits  lr^T[128 ch x 64 tok] = Wa[blk]^T (MN-major A, from W stored (in, out))
 // x x_tile^T (K-major B, the x tile as TMA lands it), and li^T likewise, so TMEM lane =
-// channel and column = token.  Four scan threads own each channel, one per 16-token part:
-// each runs its part serially in registers from a zero state, the parts are joined through
-// shared memory, and chunks through the anchored look-back over value slots in `saved`
-// (lookback.cuh), which keeps the result bitwise deterministic.
+// channel and column = token.  Two scan threads own each channel, one per 32-token part: each
+// runs its part serially in registers from a zero state and parks the local states in TMEM;
+// an output thread per channel joins the parts, and chunks through the anchored look-back over
+// value slots in `saved` (lookback.cuh), which keeps the result bitwise deterministic.
 //
-// Roles (576 threads, one CTA per SM, launched cooperatively so that all CTAs are resident):
+// Roles (448 threads, one CTA per SM, launched cooperatively so that all CTAs are resident):
 //   warp 0       TMA producer: Wa[blk], Wx[blk] once, then the x tile ring (3 stages)
-//   warp 1       MMA issuer: 2 x 8 tcgen05.mma (K = 16 each) per tile into a 2-deep TMEM ring
-//   warps 2..17  scan: warps 2+4p .. 5+4p take tokens 16p .. 16p+15 (lane quadrant warp % 4)
+//   warp 1       MMA issuer: 2 x 8 tcgen05.mma (K = 16 each) per tile into a 4-deep TMEM ring
+//   warps 2..9   scan: warps 2+4p .. 5+4p take tokens 32p .. 32p+31 (lane quadrant warp % 4),
+//                tile after tile, parking each over its own logits, with no barrier
+//   warps 10..13 output: per parked tile, publish its aggregate, then finish the tile before
+//                it (look-back, chunk-boundary state, y through shared memory and a TMA store)
 // CTA (blk, r) of the P CTAs serving gate block blk takes the block's tiles n = r, r + P, ...
 // in chunk-major order, so every tile it waits on is earlier in the same order.
 #include <cudaTypedefs.h>
@@ -38,22 +41,25 @@ namespace {
 constexpr int NPART = 2;              // token parts of a tile, one scan thread each per channel
 constexpr int PT = FUSED_C / NPART;   // tokens per scan thread
 constexpr int NSCAN = 4 * NPART;      // scan warps (4 lane quadrants per part)
-constexpr int NTHREADS = 64 + NSCAN * 32;
+constexpr int NOUT = 4;               // output warps, one per TMEM lane quadrant
+constexpr int NTHREADS = 64 + (NSCAN + NOUT) * 32;
 // The warps share the SM's four 16 K-register sub-partitions: registers per thread <= 16384 /
 // (32 x warps per sub-partition), rounded down to a multiple of 8.
-constexpr int MAXREG = (16384 / (((NSCAN + 2 + 3) / 4) * 32)) / 8 * 8;
+constexpr int MAXREG = (16384 / (((NSCAN + NOUT + 2 + 3) / 4) * 32)) / 8 * 8;
+constexpr int BAR_OUT = 1;  // named barrier of the output warps
 constexpr int XSTAGES = 3;
 constexpr uint32_t W_BYTES = FUSED_K * FUSED_K * 2;  // one weight block, bf16
 constexpr uint32_t X_BYTES = FUSED_C * FUSED_K * 2;  // one x tile, bf16
 constexpr uint32_t Y_BYTES = FUSED_C * FUSED_K * 2;  // one y tile, bf16
 constexpr uint32_t SLAB_X = FUSED_C * 32;            // 16 channels x 64 tokens
 constexpr uint32_t SLAB_W = FUSED_K * 32;            // 16 out-channels x 128 in-rows
-// 2 logits buffers x (lr 64 + li 64) columns, then 2 x 128 columns where each scan thread
-// parks its part's local states (16) and decay products (16) until the tile is finished.
+// A ring of 4 tile buffers of 128 columns (lr 64 + li 64): the MMA writes a tile's logits,
+// the scan threads overwrite them in place with the local states (over lr) and the decay
+// products (over li), and the output threads read those out and release the buffer.
 constexpr uint32_t TMEM_COLS = 512;
-constexpr uint32_t PARK_COL = 256;
+constexpr int NBUF = 4;
 constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;  // 2 s: a pipeline wait never lasts this
-constexpr uint32_t XCH_BYTES = 2 * NPART * FUSED_K * 8;  // part maps of two tiles
+constexpr uint32_t XCH_BYTES = NBUF * NPART * FUSED_K * 8;  // part maps, one set per buffer
 constexpr size_t SMEM_BYTES =
     2 * W_BYTES + XSTAGES * X_BYTES + Y_BYTES + XCH_BYTES + 256 + 1024;
 constexpr uint32_t STATUS_PIPE = 2u;
@@ -90,13 +96,13 @@ struct Ctl {
 // Local scan of one scan thread's PT tokens from a zero state.  The pointwise work runs on
 // token pairs (u, u + 1) in the two lanes of f32x2 operations (adjacent TMEM columns land in
 // adjacent registers); the recurrence itself is a scalar chain.  The state after each token
-// (hl) and the product of abar up to it (Ac) are parked in TMEM as they are made, at columns
-// park + u and park + PT + u; (rA, rh) = the part's map.  GENERAL handles resets, tokens past
+// (hl) and the product of abar up to it (Ac) are parked in TMEM as they are made, over the
+// logits just read (hl over lr, Ac over li); (rA, rh) = the part's map.  GENERAL handles resets, tokens past
 // T and decays with la <= -1/8; the fast variant (chosen warp-uniformly) has none.
 constexpr int GRP = 8;  // tokens per TMEM load / store group
 template <bool GENERAL>
-__device__ __forceinline__ void local_scan(uint32_t t_lr, uint32_t t_li, uint32_t park,
-                                           uint32_t xb0, uint32_t xb1, const GateK& gk,
+__device__ __forceinline__ void local_scan(uint32_t t_lr, uint32_t t_li, uint32_t xb0,
+                                           uint32_t xb1, const GateK& gk,
                                            uint32_t rmask, int valid, float& rh, float& rA) {
   rh = 0.0f;
   rA = 1.0f;
@@ -145,8 +151,8 @@ __device__ __forceinline__ void local_scan(uint32_t t_lr, uint32_t t_li, uint32_
       oh[2 * q + 1] = rh;
       oa[2 * q + 1] = rA;
     }
-    tc::tmem_st8(park + g * GRP, oh);
-    tc::tmem_st8(park + PT + g * GRP, oa);
+    tc::tmem_st8(t_lr + g * GRP, oh);
+    tc::tmem_st8(t_li + g * GRP, oa);
   }
   tc::tmem_st_wait();
 }
@@ -162,14 +168,15 @@ __global__ void __maxnreg__(MAXREG)
   uint8_t* s_wx = smem + W_BYTES;
   uint8_t* s_x = smem + 2 * W_BYTES;
   uint8_t* s_y = s_x + XSTAGES * X_BYTES;
-  float2* s_agg = reinterpret_cast<float2*>(s_y + Y_BYTES);  // [tile parity][part][channel]
-  uint64_t* bars = reinterpret_cast<uint64_t*>(s_agg + 2 * NPART * FUSED_K);
+  float2* s_agg = reinterpret_cast<float2*>(s_y + Y_BYTES);  // [buffer][part][channel]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(s_agg + NBUF * NPART * FUSED_K);
   uint64_t* w_full = bars;
   uint64_t* x_full = bars + 1;
   uint64_t* x_empty = bars + 1 + XSTAGES;
   uint64_t* acc_full = bars + 1 + 2 * XSTAGES;
-  uint64_t* acc_empty = acc_full + 2;
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(acc_empty + 2);
+  uint64_t* acc_empty = acc_full + NBUF;  // buffer read out by the output warps
+  uint64_t* park_full = acc_empty + NBUF;  // a tile parked in its buffer (scan -> output)
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(park_full + NBUF);
   volatile uint32_t* abort_flag = tmem_holder + 1;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -184,9 +191,10 @@ __global__ void __maxnreg__(MAXREG)
       tc::mbar_init(&x_full[s], 1);
       tc::mbar_init(&x_empty[s], NSCAN);
     }
-    for (int a = 0; a < 2; ++a) {
+    for (int a = 0; a < NBUF; ++a) {
       tc::mbar_init(&acc_full[a], 1);
-      tc::mbar_init(&acc_empty[a], NSCAN);
+      tc::mbar_init(&acc_empty[a], NOUT);
+      tc::mbar_init(&park_full[a], NSCAN);
     }
     *abort_flag = 0u;
     tc::fence_barrier_init();
@@ -199,6 +207,8 @@ __global__ void __maxnreg__(MAXREG)
   __syncthreads();
   tc::tc_fence_after();
   const uint32_t tmem = *tmem_holder;
+  int my_tiles = 0;
+  for (int n = rr; n < ntiles; n += p.P) ++my_tiles;
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
@@ -236,8 +246,8 @@ __global__ void __maxnreg__(MAXREG)
       for (int n = rr; n < ntiles; n += p.P, ++it) {
         const int st = it % XSTAGES;
         const uint32_t ph = (it / XSTAGES) & 1;
-        const int a = it & 1;
-        const uint32_t aph = (it >> 1) & 1;
+        const int a = it % NBUF;
+        const uint32_t aph = (it / NBUF) & 1;
         if (!ctl.wait(&acc_empty[a], aph ^ 1u)) continue;
         if (!ctl.wait(&x_full[st], ph)) continue;
         tc::tc_fence_after();
@@ -254,8 +264,10 @@ __global__ void __maxnreg__(MAXREG)
         if (leader) tc::mma_commit(&acc_full[a]);
       }
     }
-  } else {
+  } else if (warp < 2 + NSCAN) {
     // ------------------------------------------------------------ scan warps
+    // Local scans back to back: each tile is parked in its TMEM buffer (with the parts' maps in
+    // shared memory) and handed to the output warps; no barrier among the scan warps.
     const int part = (warp - 2) >> 2;  // token part of the tile
     const int q = warp & 3;            // TMEM lane quadrant this warp may access
     const int j = q * 32 + lane;
@@ -267,151 +279,155 @@ __global__ void __maxnreg__(MAXREG)
     gk.cm = sqrtf(-2.0f * gk.nk);
     gk.nbr = p.ba ? -p.ba[w] * LOG2E : 0.0f;  // biases folded into the exponents
     gk.nbi = p.bx ? -p.bx[w] * LOG2E : 0.0f;
-    float* carry = reinterpret_cast<float*>(p.scratch + p.L.carry);
-    float2* agg = reinterpret_cast<float2*>(p.scratch + p.L.agg);
-    const bool store_thread = (warp == 2 && lane == 0);
-    if (store_thread) tc::prefetch_tmap(&tm_y);
     // x[token tl, channel j] of a stage: 16-byte halves of the 32-byte row swap on rows 4..7
     // of every 8 (32-byte swizzle), so two base pointers cover both row parities.
     const int xoff0 = (j >> 4) * SLAB_X + (j & 7) * 2 + (((j & 15) >> 3) << 4);
     const int xoff1 = (j >> 4) * SLAB_X + (j & 7) * 2 + ((((j & 15) >> 3) ^ 1) << 4);
-    int my_tiles = 0;
-    for (int n = rr; n < ntiles; n += p.P) ++my_tiles;
-
-    // Software pipeline: iteration `it` runs the local scan of tile it (results parked in
-    // TMEM) and then finishes tile it-1, whose look-back slots have had a whole tile's time
-    // to fill.
     // Warp-uniform: every channel of this warp has la > -1/8 on every token.
     const bool near_all = __all_sync(0xffffffffu, gk.nk > NEAR_LA);
 
-    TileWalk cur(rr, p.P, p.B);  // tile it
-    int pc = 0, pb = 0;          // chunk and row of tile it - 1
-    for (int it = 0; it <= my_tiles; ++it) {
-      // Request tile it-1's look-back slots now; they are consumed after this tile's scan.
-      LookbackReq lbq;
-      int lb_n = 0;
-      const float2* lb_agg = agg;
-      const float* lb_anchor = nullptr;
-      if (it > 0) {
-        const int c = pc, b = pb;
-        const LookbackSpan sp = lookback_span(c, p.lb_dist, p.lb_shift);
-        lb_n = sp.n;
-        if (c > 0) lb_agg = agg + ((size_t)b * p.nC + c - 1) * p.W + w;
-        // the anchor's boundary state (the state entering chunk anchor + 1), or h0
-        if (sp.anchor >= 0) lb_anchor = carry + ((size_t)b * (p.nC + 1) + sp.anchor + 1) * p.W + w;
-        const float init = (p.canonical && p.h0) ? p.h0[(size_t)b * p.W + w] : 0.0f;
-        lookback_issue(lbq, lb_agg, -(long)p.W, lb_n, lb_anchor, init);
+    TileWalk cur(rr, p.P, p.B);
+    for (int it = 0; it < my_tiles; ++it, cur.next()) {
+      const int c = cur.c, b = cur.b;
+      const int st = it % XSTAGES;
+      const uint32_t ph = (it / XSTAGES) & 1;
+      const int a = it % NBUF;
+      const uint32_t aph = (it / NBUF) & 1;
+      uint32_t rmask = 0;
+      if (p.canonical) {
+        const int t = c * FUSED_C + tb + lane;
+        rmask = __ballot_sync(0xffffffffu, lane < PT && t < p.T &&
+                                               is_reset(p.reset_mask, p.segment_pos,
+                                                        (size_t)b * p.T + t));
       }
-      if (it < my_tiles) {
-        const int c = cur.c, b = cur.b;
-        const int st = it % XSTAGES;
-        const uint32_t ph = (it / XSTAGES) & 1;
-        const int a = it & 1;
-        const uint32_t aph = (it >> 1) & 1;
-        ctl.wait(&acc_full[a], aph);
-        ctl.wait(&x_full[st], ph);
-        tc::tc_fence_after();
-
-        uint32_t rmask = 0;
-        if (p.canonical) {
-          const int t = c * FUSED_C + tb + lane;
-          rmask = __ballot_sync(0xffffffffu, lane < PT && t < p.T &&
-                                                 is_reset(p.reset_mask, p.segment_pos,
-                                                          (size_t)b * p.T + t));
-        }
-        const int valid = min(FUSED_C, p.T - c * FUSED_C) - tb;  // tokens of this part < T
-        const uint32_t xt = tc::smem_u32(s_x + st * X_BYTES + tb * 32);
-        const uint32_t xb0 = xt + xoff0, xb1 = xt + xoff1;
-        const uint32_t t_lr = tmem + lane_base + a * 128 + tb;
-        const uint32_t park = tmem + lane_base + PARK_COL + a * 128 + part * 2 * PT;
-        float rh, rA;
-        if (near_all && rmask == 0u && valid >= PT)
-          local_scan<false>(t_lr, t_lr + 64, park, xb0, xb1, gk, 0u, PT, rh, rA);
-        else
-          local_scan<true>(t_lr, t_lr + 64, park, xb0, xb1, gk, rmask, valid, rh, rA);
-        tc::tc_fence_before();
-        __syncwarp();
-        if (lane == 0) {
-          tc::mbar_arrive(&acc_empty[a]);
-          tc::mbar_arrive(&x_empty[st]);
-        }
-        s_agg[(a * NPART + part) * FUSED_K + j] = make_float2(rA, rh);  // the part's map
+      const int valid = min(FUSED_C, p.T - c * FUSED_C) - tb;  // tokens of this part < T
+      ctl.wait(&acc_full[a], aph);
+      ctl.wait(&x_full[st], ph);
+      tc::tc_fence_after();
+      const uint32_t xt = tc::smem_u32(s_x + st * X_BYTES + tb * 32);
+      const uint32_t xb0 = xt + xoff0, xb1 = xt + xoff1;
+      const uint32_t t_lr = tmem + lane_base + a * 128 + tb;
+      float rh, rA;
+      if (near_all && rmask == 0u && valid >= PT)
+        local_scan<false>(t_lr, t_lr + 64, xb0, xb1, gk, 0u, PT, rh, rA);
+      else
+        local_scan<true>(t_lr, t_lr + 64, xb0, xb1, gk, rmask, valid, rh, rA);
+      s_agg[(a * NPART + part) * FUSED_K + j] = make_float2(rA, rh);  // the part's map
+      tc::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        tc::mbar_arrive(&x_empty[st]);
+        tc::mbar_arrive(&park_full[a]);
       }
-      if (store_thread) tc::tma_store_wait_read0();  // the y staging is free again
-      tc::named_bar(1, NSCAN * 32);
+    }
+  } else {
+    // ------------------------------------------------------------ output warps
+    // One thread per channel.  Iteration it publishes tile it's aggregate as soon as it is
+    // parked, finishes tile it - 1 (look-back, carry, y), then requests tile it's look-back
+    // slots, which have the next tile's scan to arrive.
+    const int q = warp & 3;
+    const int j = q * 32 + lane;
+    const int w = blk * FUSED_K + j;
+    const uint32_t lane_base = (uint32_t)(q * 32) << 16;
+    float* carry = reinterpret_cast<float*>(p.scratch + p.L.carry);
+    float2* agg = reinterpret_cast<float2*>(p.scratch + p.L.agg);
+    const bool store_thread = (warp == 2 + NSCAN && lane == 0);
+    if (store_thread) tc::prefetch_tmap(&tm_y);
 
-      // Publish tile it's map at once (the last part, from all parts' maps).
-      if (it < my_tiles && part == NPART - 1) {
-        const int n = rr + it * p.P;
-        const int c = cur.c, b = cur.b;
-        const int a = it & 1;
-        if ((blk * ntiles + n) != p.drop_tile) {
-          float At = 1.0f, Bt = 0.0f;
+    TileWalk cur(rr, p.P, p.B);
+    int pc = 0, pb = 0;              // chunk and row of tile it - 1
+    float Pa[NPART], Pb[NPART];      // tile it - 1: the map of the parts before each part
+    float Ta = 1.0f, Tb = 0.0f;      // tile it - 1: the tile's map
+    LookbackReq lbq;                 // tile it - 1's look-back
+    int lb_n = 0;
+    const float2* lb_agg = agg;
+    const float* lb_anchor = nullptr;
 #pragma unroll
-          for (int pp = 0; pp < NPART; ++pp) {
-            const float2 g = s_agg[(a * NPART + pp) * FUSED_K + j];
-            Bt = fmaf(g.x, Bt, g.y);
-            At *= g.x;
-          }
-          slot_put2(agg + ((size_t)b * p.nC + c) * p.W + w, At, Bt);
-        }
-      }
-
-      // Finish tile it-1: every part derives the tile's carry itself (no barrier between the
-      // look-back and the output), the last part publishes the chunk-boundary state.
-      if (it > 0) {
-        const int n = rr + (it - 1) * p.P;
-        const int c = pc, b = pb;
-        const int a = (it - 1) & 1;
-        float Ae = 1.0f, Be = 0.0f, At = 1.0f, Bt = 0.0f;
+    for (int pp = 0; pp < NPART; ++pp) Pa[pp] = 1.0f, Pb[pp] = 0.0f;
+    for (int it = 0; it <= my_tiles; ++it) {
+      // 1. tile it, parked: its map (the parts composed) and its aggregate, published at once
+      float nPa[NPART], nPb[NPART], nTa = 1.0f, nTb = 0.0f;
+      const int n = rr + it * p.P;
+      if (it < my_tiles) {
+        const int a = it % NBUF;
+        ctl.wait(&park_full[a], (it / NBUF) & 1);
+        tc::tc_fence_after();
 #pragma unroll
         for (int pp = 0; pp < NPART; ++pp) {
           const float2 g = s_agg[(a * NPART + pp) * FUSED_K + j];
-          if (pp < part) {
-            Be = fmaf(g.x, Be, g.y);
-            Ae *= g.x;
-          }
-          Bt = fmaf(g.x, Bt, g.y);
-          At *= g.x;
+          nPa[pp] = nTa;
+          nPb[pp] = nTb;
+          nTb = fmaf(g.x, nTb, g.y);
+          nTa *= g.x;
         }
+        if ((blk * ntiles + n) != p.drop_tile)
+          slot_put2(agg + ((size_t)cur.b * p.nC + cur.c) * p.W + w, nTa, nTb);
+      }
+
+      // 2. finish tile it - 1: its carry-in, the chunk-boundary state, y
+      if (it > 0) {
+        const int a = (it - 1) % NBUF;
         const float hin_t =
             lookback_finish(lbq, lb_agg, -(long)p.W, lb_n, lb_anchor, p.spin_limit, status);
-        if (part == NPART - 1) {
-          const float hend = fmaf(At, hin_t, Bt);
-          float* crow = carry + (size_t)b * (p.nC + 1) * p.W;
-          if ((blk * ntiles + n) != p.drop_tile) slot_put1(crow + (size_t)(c + 1) * p.W + w, hend);
-          if (c == 0) slot_put1(crow + w, hin_t);
-          if (c == p.nC - 1 && p.hT) p.hT[(size_t)b * p.W + w] = hend;
-        }
-        const float hin = fmaf(Ae, hin_t, Be);
-        const uint32_t park = tmem + lane_base + PARK_COL + a * 128 + part * 2 * PT;
+        const float hend = fmaf(Ta, hin_t, Tb);
+        float* crow = carry + (size_t)pb * (p.nC + 1) * p.W;
+        if ((blk * ntiles + n - p.P) != p.drop_tile) slot_put1(crow + (size_t)(pc + 1) * p.W + w, hend);
+        if (pc == 0) slot_put1(crow + w, hin_t);
+        if (pc == p.nC - 1 && p.hT) p.hT[(size_t)pb * p.W + w] = hend;
+        if (store_thread) tc::tma_store_wait_read0();  // the y staging is free again
+        tc::named_bar(BAR_OUT, NOUT * 32);
         // y tile: registers -> smem [token][channel] -> TMA store (clipped at T)
 #pragma unroll
-        for (int c16 = 0; c16 < PT; c16 += 16) {
-          float hl[16], Ac[16];
-          tc::tmem_ld16(park + c16, hl);
-          tc::tmem_ld16(park + PT + c16, Ac);
-          tc::tmem_ld_wait();
+        for (int pp = 0; pp < NPART; ++pp) {
+          const float hin = fmaf(Pa[pp], hin_t, Pb[pp]);
+          const uint32_t park = tmem + lane_base + a * 128 + pp * PT;  // hl; Ac at + 64
 #pragma unroll
-          for (int u = 0; u < 16; u += 2) {
-            const float2 yv =
-                fma2(make_float2(Ac[u], Ac[u + 1]), bc2(hin), make_float2(hl[u], hl[u + 1]));
-            const int tl = tb + c16 + u;
-            *reinterpret_cast<bf16*>(s_y + tl * (FUSED_K * 2) + j * 2) = __float2bfloat16_rn(yv.x);
-            *reinterpret_cast<bf16*>(s_y + (tl + 1) * (FUSED_K * 2) + j * 2) =
-                __float2bfloat16_rn(yv.y);
+          for (int c16 = 0; c16 < PT; c16 += 16) {
+            float hl[16], Ac[16];
+            tc::tmem_ld16(park + c16, hl);
+            tc::tmem_ld16(park + 64 + c16, Ac);
+            tc::tmem_ld_wait();
+#pragma unroll
+            for (int u = 0; u < 16; u += 2) {
+              const float2 yv =
+                  fma2(make_float2(Ac[u], Ac[u + 1]), bc2(hin), make_float2(hl[u], hl[u + 1]));
+              const int tl = pp * PT + c16 + u;
+              *reinterpret_cast<bf16*>(s_y + tl * (FUSED_K * 2) + j * 2) = __float2bfloat16_rn(yv.x);
+              *reinterpret_cast<bf16*>(s_y + (tl + 1) * (FUSED_K * 2) + j * 2) =
+                  __float2bfloat16_rn(yv.y);
+            }
           }
         }
+        tc::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(&acc_empty[a]);  // the buffer and its maps are free
         tc::fence_proxy_async_smem();
+        tc::named_bar(BAR_OUT, NOUT * 32);
+        if (store_thread) {
+          tc::tma_store_3d(&tm_y, s_y, blk * FUSED_K, pc * FUSED_C, pb);
+          tc::tma_store_commit();
+        }
       }
-      tc::named_bar(1, NSCAN * 32);
-      if (it > 0 && store_thread) {
-        tc::tma_store_3d(&tm_y, s_y, blk * FUSED_K, pc * FUSED_C, pb);
-        tc::tma_store_commit();
+
+      // 3. request tile it's look-back slots; they are consumed in the next iteration
+      if (it < my_tiles) {
+        const int c = cur.c, b = cur.b;
+        const LookbackSpan sp = lookback_span(c, p.lb_dist, p.lb_shift);
+        lb_n = sp.n;
+        lb_agg = c > 0 ? agg + ((size_t)b * p.nC + c - 1) * p.W + w : agg;
+        // the anchor's boundary state (the state entering chunk anchor + 1), or h0
+        lb_anchor = sp.anchor >= 0 ? carry + ((size_t)b * (p.nC + 1) + sp.anchor + 1) * p.W + w
+                                   : nullptr;
+        const float h0v = (p.canonical && p.h0) ? p.h0[(size_t)b * p.W + w] : 0.0f;
+        lookback_issue(lbq, lb_agg, -(long)p.W, lb_n, lb_anchor, h0v);
+#pragma unroll
+        for (int pp = 0; pp < NPART; ++pp) Pa[pp] = nPa[pp], Pb[pp] = nPb[pp];
+        Ta = nTa;
+        Tb = nTb;
+        pc = c;
+        pb = b;
+        cur.next();
       }
-      pc = cur.c;
-      pb = cur.b;
-      cur.next();
     }
     if (store_thread) tc::tma_store_wait0();
   }
@@ -465,13 +481,10 @@ bool fused_supported(const Dims& d) {
   return d.io == RGLRU_BF16 && d.k == FUSED_K && fused_ctas_per_block(d) >= 1;
 }
 
-// Prepares a scan layout for slot-based look-back: the first zero_bytes (status word and any
-// counters, at most the header and flag area) cleared, every slot empty.
-cudaError_t clear_slots(void* buf, const ScanLayout& L, cudaStream_t s, size_t zero_bytes) {
-  cudaError_t e = cudaMemsetAsync(buf, 0, zero_bytes, s);
-  if (e == cudaSuccess)
-    e = cudaMemsetAsync(static_cast<uint8_t*>(buf) + L.carry, 0xff, L.part - L.carry, s);
-  return e;
+// Prepares a scan layout for slot-based look-back with one zero fill: the status word, any
+// counters in the header and every slot (empty reads as zero).
+cudaError_t clear_slots(void* buf, const ScanLayout& L, cudaStream_t s) {
+  return cudaMemsetAsync(buf, 0, L.part, s);
 }
 
 cudaError_t launch_fused_fwd(const Dims& d, const void* x, const void* Wa, const float* ba,
@@ -508,7 +521,7 @@ cudaError_t launch_fused_fwd(const Dims& d, const void* x, const void* Wa, const
   e = cudaFuncSetAttribute(k_fused_fwd, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)SMEM_BYTES);
   if (e != cudaSuccess) return e;
-  e = clear_slots(saved, p.L, s, 256);
+  e = clear_slots(saved, p.L, s);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.P * d.nblk);

@@ -205,7 +205,7 @@ cudaError_t launch_fused_fwd(const Dims& d, const void* x, const void* Wa, const
 bool fused_supported(const Dims& d);
 int fused_ctas_per_block(const Dims& d);
 // Clears the status word of a scan layout and marks every carry / aggregate slot empty.
-cudaError_t clear_slots(void* buf, const ScanLayout& L, cudaStream_t s, size_t zero_bytes);
+cudaError_t clear_slots(void* buf, const ScanLayout& L, cudaStream_t s);
 
 // Fused backward on tensor cores (same coverage as the fused forward; `saved` must come from
 // launch_fused_fwd).  dx is written in shape.grad; dWa / dWx / dba / dbx / dLambda reduced

@@ -43,7 +43,7 @@ __device__ __forceinline__ void lookback_issue(LookbackReq& q, const float2* fir
 #pragma unroll
   for (int s = 0; s < LB_SLOTS; ++s)
     q.v[s] = s < n ? ld_relaxed_u64(first_agg + s * agg_step) : 0ull;
-  q.hv = anchor_state ? ld_relaxed_u32(anchor_state) : __float_as_uint(init);
+  q.hv = anchor_state ? ld_relaxed_u32(anchor_state) : slot_enc1(init);
 }
 
 // A slot that stays empty past `limit` polls counts as the identity (or a zero carry), and the
@@ -61,8 +61,8 @@ __device__ __forceinline__ float lookback_finish(LookbackReq& q, const float2* f
       atomicOr(status, STATUS_TIMEOUT);
 #pragma unroll
       for (int s = 0; s < LB_SLOTS; ++s)
-        if (q.v[s] == SLOT_EMPTY64) q.v[s] = (uint64_t)__float_as_uint(1.0f);  // A = 1, B = 0
-      if (q.hv == SLOT_EMPTY32) q.hv = 0u;
+        if (q.v[s] == SLOT_EMPTY64) q.v[s] = slot_enc2(1.0f, 0.0f);  // the identity map
+      if (q.hv == SLOT_EMPTY32) q.hv = slot_enc1(0.0f);
       break;
     }
     __nanosleep(32);
@@ -72,13 +72,12 @@ __device__ __forceinline__ float lookback_finish(LookbackReq& q, const float2* f
     if (anchor_state != nullptr && q.hv == SLOT_EMPTY32) q.hv = ld_relaxed_u32(anchor_state);
   }
   // compose from the anchor's side: the oldest aggregate first
-  float c = __uint_as_float(q.hv);
+  float c = slot_dec1(q.hv);
 #pragma unroll
   for (int s = LB_SLOTS - 1; s >= 0; --s) {
     if (s < n) {
-      const float A = __uint_as_float((uint32_t)(q.v[s] & 0xffffffffu));
-      const float B = __uint_as_float((uint32_t)(q.v[s] >> 32));
-      c = fmaf(A, c, B);
+      const float2 ab = slot_dec2(q.v[s]);
+      c = fmaf(ab.x, c, ab.y);
     }
   }
   return c;

@@ -105,6 +105,15 @@ __device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, const void*
       : "memory");
 }
 
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, const void* src, int c0,
+                                             int c1) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+          reinterpret_cast<uint64_t>(map)),
+      "r"(smem_u32(src)), "r"(c0), "r"(c1)
+      : "memory");
+}
+
 __device__ __forceinline__ void tma_store_commit() {
   asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
@@ -113,6 +122,10 @@ __device__ __forceinline__ void tma_store_wait_read0() {
 }
 __device__ __forceinline__ void tma_store_wait0() {
   asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+// Orders this thread's async-proxy (TMA) global accesses with its later generic-proxy ones.
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
 }
 // Makes this thread's generic-proxy shared-memory writes visible to the async proxy (TMA).
 __device__ __forceinline__ void fence_proxy_async_smem() {
@@ -272,6 +285,14 @@ __device__ __forceinline__ void tmem_ld(uint32_t taddr, float (&v)[16]) { tmem_l
 __device__ __forceinline__ void tmem_st(uint32_t taddr, const float (&v)[4]) { tmem_st4(taddr, v); }
 __device__ __forceinline__ void tmem_st(uint32_t taddr, const float (&v)[8]) { tmem_st8(taddr, v); }
 __device__ __forceinline__ void tmem_st(uint32_t taddr, const float (&v)[16]) { tmem_st16(taddr, v); }
+
+// Ties registers filled by tcgen05.ld to the point after tcgen05.wait::ld: every later use reads
+// the output of an empty volatile asm placed after the wait, so none can be scheduled earlier.
+template <int N>
+__device__ __forceinline__ void reg_fence(float (&v)[N]) {
+#pragma unroll
+  for (int i = 0; i < N; ++i) asm volatile("" : "+f"(v[i]));
+}
 
 // ---------------------------------------------------------------- descriptors
 // Shared-memory matrix descriptor (sm_100 format): start address, leading / stride byte
