@@ -24,7 +24,8 @@
 //   warps 2..9   scan: warps 2+4p .. 5+4p take tokens 32p .. 32p+31 (lane quadrant warp % 4),
 //                tile after tile, parking each over its own logits, with no barrier
 //   warps 10..13 output: per parked tile, publish its aggregate, then finish the tile before
-//                it (look-back, chunk-boundary state, y through shared memory and a TMA store)
+//                it (look-back, chunk-boundary state, y): each warp its 32 channels, through
+//                its own double-buffered shared-memory strip and TMA store, with no barrier
 // CTA (blk, r) of the P CTAs serving gate block blk takes the block's tiles n = r, r + P, ...
 // in chunk-major order, so every tile it waits on is earlier in the same order.
 #include <cudaTypedefs.h>
@@ -46,11 +47,11 @@ constexpr int NTHREADS = 64 + (NSCAN + NOUT) * 32;
 // The warps share the SM's four 16 K-register sub-partitions: registers per thread <= 16384 /
 // (32 x warps per sub-partition), rounded down to a multiple of 8.
 constexpr int MAXREG = (16384 / (((NSCAN + NOUT + 2 + 3) / 4) * 32)) / 8 * 8;
-constexpr int BAR_OUT = 1;  // named barrier of the output warps
 constexpr int XSTAGES = 3;
 constexpr uint32_t W_BYTES = FUSED_K * FUSED_K * 2;  // one weight block, bf16
 constexpr uint32_t X_BYTES = FUSED_C * FUSED_K * 2;  // one x tile, bf16
-constexpr uint32_t Y_BYTES = FUSED_C * FUSED_K * 2;  // one y tile, bf16
+constexpr uint32_t YSTRIP_BYTES = FUSED_C * 32 * 2;  // y of 64 tokens x 32 channels, bf16
+constexpr uint32_t Y_BYTES = NOUT * 2 * YSTRIP_BYTES;  // two strips per output warp
 constexpr uint32_t SLAB_X = FUSED_C * 32;            // 16 channels x 64 tokens
 constexpr uint32_t SLAB_W = FUSED_K * 32;            // 16 out-channels x 128 in-rows
 // A ring of 4 tile buffers of 128 columns (lr 64 + li 64): the MMA writes a tile's logits,
@@ -331,8 +332,9 @@ __global__ void __maxnreg__(MAXREG)
     const uint32_t lane_base = (uint32_t)(q * 32) << 16;
     float* carry = reinterpret_cast<float*>(p.scratch + p.L.carry);
     float2* agg = reinterpret_cast<float2*>(p.scratch + p.L.agg);
-    const bool store_thread = (warp == 2 + NSCAN && lane == 0);
-    if (store_thread) tc::prefetch_tmap(&tm_y);
+    // y goes out per warp: 32 channels x 64 tokens through one of two shared-memory strips
+    uint8_t* ystrip = s_y + (warp - 2 - NSCAN) * 2 * YSTRIP_BYTES;
+    if (lane == 0) tc::prefetch_tmap(&tm_y);
 
     TileWalk cur(rr, p.P, p.B);
     int pc = 0, pb = 0;              // chunk and row of tile it - 1
@@ -374,9 +376,10 @@ __global__ void __maxnreg__(MAXREG)
         if ((blk * ntiles + n - p.P) != p.drop_tile) slot_put1(crow + (size_t)(pc + 1) * p.W + w, hend);
         if (pc == 0) slot_put1(crow + w, hin_t);
         if (pc == p.nC - 1 && p.hT) p.hT[(size_t)pb * p.W + w] = hend;
-        if (store_thread) tc::tma_store_wait_read0();  // the y staging is free again
-        tc::named_bar(BAR_OUT, NOUT * 32);
-        // y tile: registers -> smem [token][channel] -> TMA store (clipped at T)
+        uint8_t* yb = ystrip + ((it - 1) & 1) * YSTRIP_BYTES;
+        if (lane == 0) tc::tma_store_wait_read1();  // the strip stored two tiles ago is free
+        __syncwarp();
+        // y strip: registers -> smem [token][32 channels] -> TMA store (clipped at T)
 #pragma unroll
         for (int pp = 0; pp < NPART; ++pp) {
           const float hin = fmaf(Pa[pp], hin_t, Pb[pp]);
@@ -392,9 +395,8 @@ __global__ void __maxnreg__(MAXREG)
               const float2 yv =
                   fma2(make_float2(Ac[u], Ac[u + 1]), bc2(hin), make_float2(hl[u], hl[u + 1]));
               const int tl = pp * PT + c16 + u;
-              *reinterpret_cast<bf16*>(s_y + tl * (FUSED_K * 2) + j * 2) = __float2bfloat16_rn(yv.x);
-              *reinterpret_cast<bf16*>(s_y + (tl + 1) * (FUSED_K * 2) + j * 2) =
-                  __float2bfloat16_rn(yv.y);
+              *reinterpret_cast<bf16*>(yb + tl * 64 + lane * 2) = __float2bfloat16_rn(yv.x);
+              *reinterpret_cast<bf16*>(yb + (tl + 1) * 64 + lane * 2) = __float2bfloat16_rn(yv.y);
             }
           }
         }
@@ -402,9 +404,9 @@ __global__ void __maxnreg__(MAXREG)
         __syncwarp();
         if (lane == 0) tc::mbar_arrive(&acc_empty[a]);  // the buffer and its maps are free
         tc::fence_proxy_async_smem();
-        tc::named_bar(BAR_OUT, NOUT * 32);
-        if (store_thread) {
-          tc::tma_store_3d(&tm_y, s_y, blk * FUSED_K, pc * FUSED_C, pb);
+        __syncwarp();
+        if (lane == 0) {
+          tc::tma_store_3d(&tm_y, yb, blk * FUSED_K + q * 32, pc * FUSED_C, pb);
           tc::tma_store_commit();
         }
       }
@@ -429,7 +431,7 @@ __global__ void __maxnreg__(MAXREG)
         cur.next();
       }
     }
-    if (store_thread) tc::tma_store_wait0();
+    if (lane == 0) tc::tma_store_wait0();
   }
 
   tc::tc_fence_before();
@@ -450,7 +452,7 @@ cudaError_t make_maps(const Dims& d, const void* x, const void* Wa, const void* 
   cudaError_t e = encode_tmap(mx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, x, dims3, str3, box_x,
                               CU_TENSOR_MAP_SWIZZLE_32B);
   if (e != cudaSuccess) return e;
-  const uint32_t box_y[3] = {FUSED_K, FUSED_C, 1};
+  const uint32_t box_y[3] = {32, FUSED_C, 1};  // one output warp's strip
   e = encode_tmap(my, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, y, dims3, str3, box_y,
                   CU_TENSOR_MAP_SWIZZLE_NONE);
   if (e != cudaSuccess) return e;
