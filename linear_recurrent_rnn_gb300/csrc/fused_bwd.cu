@@ -768,38 +768,30 @@ __global__ void __maxnreg__(MAXREG)
   const float4* dwp = reinterpret_cast<const float4*>(p.scratch + p.F.dw_part) +
                       (size_t)blk * p.P * NV;
   const int per = (NV + p.P - 1) / p.P;
-  const int v_end = min(NV, (rr + 1) * per);
-  // two vectors per thread and eight partials per round in flight: the sums are bound by the
-  // L2 round trip, not by the adds
-  for (int v0 = rr * per + threadIdx.x; v0 < v_end; v0 += 2 * NTHREADS) {
-    const int v1 = v0 + NTHREADS;
-    float4 acc0[8], acc1[8];
-#pragma unroll
-    for (int u = 0; u < 8; ++u) acc0[u] = acc1[u] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-    for (int r = 0; r < p.P; r += 8) {
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        if (r + u < p.P) {
-          const float4 a = dwp[(size_t)(r + u) * NV + v0];
-          acc0[u].x += a.x, acc0[u].y += a.y, acc0[u].z += a.z, acc0[u].w += a.w;
-          if (v1 < v_end) {
-            const float4 b = dwp[(size_t)(r + u) * NV + v1];
-            acc1[u].x += b.x, acc1[u].y += b.y, acc1[u].z += b.z, acc1[u].w += b.w;
-          }
-        }
-      }
+  const int v0 = rr * per;
+  const int nv = max(0, min(NV, v0 + per) - v0);
+  // This CTA's slice of all P partials comes into shared memory (free now; at most
+  // (NV + P) x 16 bytes) by bulk copies in one round trip, completing on w_full's second phase;
+  // then each vector is summed over the partials in order.
+  float4* sbuf = reinterpret_cast<float4*>(smem);
+  if (nv > 0) {
+    if (threadIdx.x == 0) {
+      tc::fence_proxy_async_global();  // the partials were acquired through the counter
+      tc::mbar_expect_tx(w_full, (uint32_t)(p.P * nv * 16));
+      for (int r = 0; r < p.P; ++r)
+        tc::bulk_load(sbuf + (size_t)r * nv, dwp + (size_t)r * NV + v0, (uint32_t)nv * 16, w_full);
     }
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const int v = h ? v1 : v0;
-      if (v >= v_end) break;
-      float4 t = h ? acc1[0] : acc0[0];
-#pragma unroll
-      for (int u = 1; u < 8; ++u) {
-        const float4 a = h ? acc1[u] : acc0[u];
+    // always waited for, so that no copy is in flight when the CTA exits
+    if (!tc::mbar_wait(w_full, 1, WAIT_LIMIT_NS)) atomicOr(status, STATUS_PIPE);
+    for (int v = threadIdx.x; v < nv; v += NTHREADS) {
+      float4 t = sbuf[v];
+      for (int r = 1; r < p.P; ++r) {
+        const float4 a = sbuf[(size_t)r * nv + v];
         t.x += a.x, t.y += a.y, t.z += a.z, t.w += a.w;
       }
-      float* dst = v < NV / 2 ? p.dWa + (size_t)blk * KK + v * 4 : p.dWx + (size_t)blk * KK + (v - NV / 2) * 4;
+      const int vg = v0 + v;
+      float* dst = vg < NV / 2 ? p.dWa + (size_t)blk * KK + vg * 4
+                               : p.dWx + (size_t)blk * KK + (vg - NV / 2) * 4;
       *reinterpret_cast<float4*>(dst) = t;
     }
   }
