@@ -276,8 +276,51 @@ def run_ours(args, rank, world, local):
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(wl, T=args.cpu_sample_T)
+    if rank == 0 and world == 1:
+        line["decode"] = decode_step(flush, peak)
     if rank == 0:
         print(json.dumps(line), flush=True)
+
+
+def decode_step(flush, peak, W=2048, k=128, reps=20):
+    """The decode step (rglru_step) on the same layer width and gate blocks, bf16, canonical,
+    states carried in place: microseconds per step at batch 1 and 256 (L2 flushed before each
+    timed step), tokens/s at 256, and its bytes (weights once, x, h in and out, y) against the
+    measured copy bandwidth."""
+    import torch
+    from linear_recurrent_rnn_gb300 import librglru as R
+    from linear_recurrent_rnn_gb300.inputs import Workload, generate
+    out = {"workload": f"decode step, W{W} k{k} bf16 canonical, states carried in place"}
+    for B in (1, 256):
+        inp = generate(Workload("decode", B, 1, W, k, "bf16", "canonical", h0_std=1.0), 1)
+        d = {n: (v.cuda() if isinstance(v, torch.Tensor) else v) for n, v in inp.items()}
+        sh = R.make_shape(B, 1, W, W // k, R.BF16, R.BF16, R.CANONICAL)
+        x = d["x"].reshape(B, W).contiguous()
+        h = d["h0"].clone()
+        y = torch.empty_like(x)
+        step = lambda: R.rglru_step(sh, x, d["Wa"], d["ba"], d["Wx"], d["bx"], d["Lambda"],
+                                    None, h, y, h)
+        for _ in range(5):
+            step()
+        ts = []
+        for _ in range(reps):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            step()
+            b.record()
+            torch.cuda.synchronize()
+            ts.append(a.elapsed_time(b))
+        us = statistics.median(ts) * 1e3
+        nbytes = 2 * (W // k) * k * k * 2 + B * W * (2 + 4 + 4 + 2)
+        out[f"us_per_step_B{B}"] = us
+        if B == 256:
+            out["tokens_per_s_B256"] = B / (us / 1e6)
+            gbs = nbytes / (us / 1e6) / 1e9
+            out["roofline_B256"] = {"bound": "hbm", "unit": "GB/s", "achieved": gbs, "peak": peak,
+                                    "frac": (gbs / peak) if peak else None,
+                                    "algorithmic_bytes": nbytes}
+    return out
 
 
 def oracle_step(wl_sample, inp):

@@ -162,6 +162,22 @@ rglru_status rglru_fused_backward(const rglru_shape *shape, const void *dy, cons
                                   float *dba, float *dWx, float *dbx, float *dLambda,
                                   float *dh0, void *workspace, rglru_stream stream);
 
+/* One decode step with carried states [P1 semantic-limits list: an initial state and T = 1,
+ * both of which the prior art rejects]: for every row b the layer's forward of one token from
+ * the state h_in,
+ *   lr = x_blk @ Wa[blk] + ba,  li = x_blk @ Wx[blk] + bx,  r = sigmoid(lr), i = sigmoid(li),
+ *   a = exp(-8 r softplus(Lambda)),  h_out = abar h_in + m i x,  y = h_out,
+ * with abar = 0 and m = 1 on a canonical reset row, abar = a and m = sqrt(1 - a^2) otherwise;
+ * the same values as rglru_fused_forward with T = 1 and h0 = h_in.  shape.T must be 1.
+ * x, y [B, W] and Wa, Wx in shape.io; h_in, h_out [B, W] float32 (h_in NULL = zeros; h_out
+ * may be h_in, updated in place); reset uint8 [B] (nonzero = the token starts a segment; NULL
+ * = none; canonical mode only); ba, bx may be NULL.  k = W / nblk <= 512 (else
+ * RGLRU_ERR_UNSUPPORTED).  One kernel, no scratch. */
+rglru_status rglru_step(const rglru_shape *shape, const void *x, const void *Wa,
+                        const float *ba, const void *Wx, const float *bx, const float *Lambda,
+                        const uint8_t *reset, const float *h_in, void *y, float *h_out,
+                        rglru_stream stream);
+
 /* Synchronises `stream`, then reads the status word at the start of a `saved` or
  * `workspace` buffer (device pointer) last used on it: RGLRU_ERR_TIMEOUT if a bounded
  * look-back wait ran out, RGLRU_OK otherwise (RGLRU_ERR_CUDA if the read fails). */

@@ -339,6 +339,22 @@ rglru_status rglru_fused_backward(const rglru_shape* shape, const void* dy, cons
   return cuda_status(e);
 }
 
+rglru_status rglru_step(const rglru_shape* shape, const void* x, const void* Wa,
+                        const float* ba, const void* Wx, const float* bx, const float* Lambda,
+                        const uint8_t* reset, const float* h_in, void* y, float* h_out,
+                        rglru_stream stream) {
+  Dims d;
+  rglru_status st = make_dims(shape, &d);
+  if (st != RGLRU_OK) return st;
+  if (d.T != 1) return RGLRU_ERR_INVALID_ARG;
+  if (!req(x) || !req(Wa) || !req(Wx) || !opt(ba) || !opt(bx) || !req(Lambda) || !opt(reset) ||
+      !opt(h_in) || !req(y) || !req(h_out))
+    return RGLRU_ERR_INVALID_ARG;
+  if (d.mode == RGLRU_RESTRICTED && reset) return RGLRU_ERR_INVALID_ARG;
+  if (d.k > STEP_KMAX) return RGLRU_ERR_UNSUPPORTED;
+  return cuda_status(launch_step(d, x, Wa, ba, Wx, bx, Lambda, reset, h_in, y, h_out, stream));
+}
+
 rglru_status rglru_sync_status(const void* buf, rglru_stream stream) {
   if (!buf) return RGLRU_ERR_INVALID_ARG;
   uint32_t word = 0;

@@ -217,6 +217,14 @@ cudaError_t launch_fused_bwd(const Dims& d, const void* dy, const float* dhT, co
                              float* dba, float* dWx, float* dbx, float* dLambda, float* dh0,
                              void* ws, int spin_limit, int drop_tile, cudaStream_t s);
 
+// One decode step (T = 1) with carried states: projections, gates and the state update in one
+// kernel (decode.cu); k <= STEP_KMAX.
+constexpr int STEP_KMAX = 512;
+cudaError_t launch_step(const Dims& d, const void* x, const void* Wa, const float* ba,
+                        const void* Wx, const float* bx, const float* Lambda,
+                        const uint8_t* reset, const float* h_in, void* y, float* h_out,
+                        cudaStream_t s);
+
 // SIMT projections (float32 accumulation).
 cudaError_t launch_gate_proj_simt(const Dims& d, int xt, int ot, const void* x, const void* Wa,
                                   const float* ba, const void* Wx, const float* bx, void* lr,

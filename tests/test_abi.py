@@ -86,3 +86,20 @@ def test_host_validation_rejects_before_cuda(lib):
     bad = R.make_shape(1, 0, 16, 1, R.BF16, R.BF16, R.CANONICAL)
     assert _call_forward(lib, bad) == R.ERR_INVALID_ARG
     assert lib.rglru_sync_status(None, None) == R.ERR_INVALID_ARG
+
+
+def test_step_host_validation(lib):
+    """rglru_step checks its shape and pointers on the host (fake, never dereferenced
+    addresses): T must be 1, restricted mode takes no resets, k is bounded."""
+    A = 1 << 20
+    P = lambda v: None if v is None else ctypes.c_void_p(v)
+
+    def call(sh, reset=None, h_in=A, x=A):
+        return lib.rglru_step(ctypes.byref(sh), P(x), P(A), None, P(A), None, P(A), P(reset),
+                              P(h_in), P(A), P(A), None)
+    assert call(R.make_shape(2, 2, 256, 2, R.BF16, R.BF16, R.CANONICAL)) == R.ERR_INVALID_ARG
+    assert call(R.make_shape(2, 1, 256, 2, R.BF16, R.BF16, R.RESTRICTED),
+                reset=A) == R.ERR_INVALID_ARG
+    assert call(R.make_shape(2, 1, 256, 2, R.BF16, R.BF16, R.CANONICAL),
+                x=A + 4) == R.ERR_INVALID_ARG
+    assert call(R.make_shape(2, 1, 1024, 1, R.BF16, R.BF16, R.CANONICAL)) == R.ERR_UNSUPPORTED
