@@ -142,8 +142,8 @@ def measured_peaks():
 
 
 # DRAM traffic of one k_fused_bwd launch at B4 T2048 W2048 (dram__bytes_read.sum +
-# dram__bytes_write.sum, ncu --set full; 70.76 MB + 13.49 MB), taken on the current kernel.
-TRAFFIC_BYTES = 84258304
+# dram__bytes_write.sum, ncu --set full; 70.61 MB + 13.38 MB), taken on the current kernel.
+TRAFFIC_BYTES = 83984384
 
 
 def run_ours(args, rank, world, local):
@@ -276,7 +276,7 @@ def run_ours(args, rank, world, local):
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(wl, T=args.cpu_sample_T)
-    if rank == 0 and world == 1:
+    if rank == 0 and world == 1 and not args.no_decode:
         line["decode"] = decode_step(flush, peak)
     if rank == 0:
         print(json.dumps(line), flush=True)
@@ -399,6 +399,7 @@ def main(argv=None):
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", choices=("ours", "reference"), default="ours")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-decode", action="store_true", help="skip the decode-step measurement")
     p.add_argument("--cpu-sample-T", type=int, default=2048)
     p.add_argument("--ref-sample-T", type=int, default=256)
     args = p.parse_args(argv)
