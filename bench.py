@@ -273,6 +273,7 @@ def run_ours(args, rank, world, local):
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": launches,
         "clocks": clk,
+        "memory": memory_footprint(sh, wl),
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(wl, T=args.cpu_sample_T)
@@ -280,6 +281,18 @@ def run_ours(args, rank, world, local):
         line["decode"] = decode_step(flush, peak)
     if rank == 0:
         print(json.dumps(line), flush=True)
+
+
+def memory_footprint(sh, wl):
+    """What the layer keeps between its forward and backward, against the float32 states of
+    every token that a backward without recomputation would keep; and the scratch the backward
+    takes.  The library allocates nothing itself: these buffers are the caller's."""
+    from linear_recurrent_rnn_gb300 import librglru as R
+    saved = R.saved_bytes(sh)
+    all_states = wl.B * wl.T * wl.W * 4
+    return {"saved_bytes": saved, "saved_bytes_per_token": saved / (wl.B * wl.T),
+            "all_states_bytes": all_states, "saved_fraction_of_all_states": saved / all_states,
+            "workspace_bytes": R.workspace_bytes(sh), "library_allocations": 0}
 
 
 def decode_step(flush, peak, W=2048, k=128, reps=20):

@@ -79,13 +79,15 @@ typedef struct {
 const char *rglru_status_string(rglru_status s);
 
 /* Bytes of the `saved` buffer a forward call fills and the matching backward reads
- * (float32 chunk-boundary states plus the forward's look-back scratch).  A buffer filled by
- * rglru_forward is read by rglru_backward; one filled by rglru_fused_forward by
- * rglru_fused_backward.  0 on an invalid shape. */
+ * (float32 chunk-boundary states plus the forward's look-back scratch; for a fused call on a
+ * shape the tensor-core kernels do not take, also the float32 gate logits).  A buffer filled
+ * by rglru_forward is read by rglru_backward; one filled by rglru_fused_forward by
+ * rglru_fused_backward.  Sized for the current device.  0 on an invalid shape. */
 size_t rglru_saved_bytes(const rglru_shape *shape);
 
 /* Bytes of the `workspace` scratch taken by rglru_backward, rglru_gate_proj_backward and
- * rglru_fused_backward (the maximum over the three).  0 on an invalid shape. */
+ * rglru_fused_backward (the maximum over the three).  Sized for the current device.  0 on an
+ * invalid shape. */
 size_t rglru_workspace_bytes(const rglru_shape *shape);
 
 /* Block-diagonal gate projections [P1 first paragraph; P2 "protocol.scope"]:

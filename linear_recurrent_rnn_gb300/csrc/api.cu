@@ -185,11 +185,11 @@ const char* rglru_status_string(rglru_status s) {
 size_t rglru_saved_bytes(const rglru_shape* shape) {
   Dims d;
   if (make_dims(shape, &d) != RGLRU_OK) return 0;
+  // the unfused scan's layout, and the fused call's: the tensor-core kernels' own where they
+  // take the shape, else the composed path's (which keeps float32 logits)
   const size_t a = scan_layout(d, false).total;
-  const size_t b = composed_saved(d).total;
-  const size_t f = fused_layout(d, false).total;
-  size_t m = a > b ? a : b;
-  return m > f ? m : f;
+  const size_t f = fused_supported(d) ? fused_layout(d, false).total : composed_saved(d).total;
+  return a > f ? a : f;
 }
 
 size_t rglru_workspace_bytes(const rglru_shape* shape) {
@@ -197,10 +197,8 @@ size_t rglru_workspace_bytes(const rglru_shape* shape) {
   if (make_dims(shape, &d) != RGLRU_OK) return 0;
   size_t m = scan_layout(d, true).total;
   const size_t g = gate_bwd_layout(d).total;
-  const size_t c = composed_ws(d).total;
-  const size_t f = fused_bwd_layout(d).total;
+  const size_t f = fused_supported(d) ? fused_bwd_layout(d).total : composed_ws(d).total;
   if (g > m) m = g;
-  if (c > m) m = c;
   if (f > m) m = f;
   return m;
 }
