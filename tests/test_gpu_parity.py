@@ -148,6 +148,11 @@ FUSED_CASES = [
     (W_("bf16-T1-k128", 2, 1, 128, 128, "bf16", "canonical", h0_std=1.0), 34, None),
     (W_("bf16-reset-k64", 1, 70, 128, 64, "bf16", "canonical", reset_p=0.05, reset_t0=True,
         h0_std=1.0), 35, None),
+    # short memories: a^c down to 0.05, so many channels leave the near regime (la <= -1/8)
+    # and the tensor-core kernels take their general path with the exponential decay
+    (W_("bf16-far-k128", 2, 150, 256, 128, "bf16", "canonical", (0.05, 0.95), reset_p=0.05,
+        h0_std=1.0), 36, "f32"),
+    (W_("bf16-far-res-k128", 2, 130, 256, 128, "bf16", "restricted", (0.2, 0.9)), 37, None),
 ]
 
 
