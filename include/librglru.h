@@ -14,6 +14,9 @@
  *   [P2] "public_fattori_h800.json" — the benchmark record: shape B4 T2048 W2048, BF16 with
  *        an FP32 recurrent carry, the restricted contract (zero initial state, no resets),
  *        and the gradients it checks (x, both gate logits, a_param).
+ *   [P3] "linear_attention.reference" — small differentiable reference forms of other gated
+ *        linear recurrences; their signatures pack variable-length sequences into one row by
+ *        cu_seqlens offsets, with an initial state per sequence and the final states returned.
  *
  * Math (per batch row b, channel w, token t; c = 8 is fixed by the specification):
  *   r = sigmoid(lr), i = sigmoid(li), log a = -8 r softplus(Lambda_w), a = exp(log a)
@@ -163,6 +166,37 @@ rglru_status rglru_fused_backward(const rglru_shape *shape, const void *dy, cons
                                   const float *h0, const void *saved, void *dx, float *dWa,
                                   float *dba, float *dWx, float *dbx, float *dLambda,
                                   float *dh0, void *workspace, rglru_stream stream);
+
+/* Packed variable-length sequences [the packing boundary of P3 "linear_attention.reference"
+ * (cu_seqlens offsets, per-sequence initial and final states), applied to this layer]: one
+ * row of shape.T tokens (shape.B must be 1, canonical mode) holds num_seqs sequences, sequence
+ * s on tokens [cu_seqlens[s], cu_seqlens[s+1]) (device int32 [num_seqs + 1], non-decreasing
+ * from 0 to T; a malformed array gives wrong results, never an out-of-bounds access).  Each
+ * sequence is the layer on its own: its first token continues from h0[s] (float32
+ * [num_seqs][W], NULL = zeros) without a reset, and hT[s] (may be NULL) is the state after its
+ * last token; an empty sequence has hT[s] = h0[s].  Same computation as rglru_fused_forward on
+ * each sequence as a row of its own.  Tensor-core shapes only (bf16 I/O, k = 128), else
+ * RGLRU_ERR_UNSUPPORTED.  `saved` (rglru_saved_bytes of the shape) also keeps the token
+ * indices for the backward. */
+rglru_status rglru_fused_forward_varlen(const rglru_shape *shape, const void *x, const void *Wa,
+                                        const float *ba, const void *Wx, const float *bx,
+                                        const float *Lambda, const int32_t *cu_seqlens,
+                                        int32_t num_seqs, const float *h0, void *y, float *hT,
+                                        void *saved, rglru_stream stream);
+
+/* Gradients of rglru_fused_forward_varlen: dx, dWa, dba, dWx, dbx, dLambda as in
+ * rglru_fused_backward; dhT (float32 [num_seqs][W], NULL = zeros) is the gradient arriving at
+ * each sequence's final state; dh0 (may be NULL) receives each sequence's initial-state
+ * gradient (dhT[s] for an empty one).  `saved` must come from rglru_fused_forward_varlen with
+ * the same inputs and cu_seqlens. */
+rglru_status rglru_fused_backward_varlen(const rglru_shape *shape, const void *dy,
+                                         const float *dhT, const void *x, const void *Wa,
+                                         const float *ba, const void *Wx, const float *bx,
+                                         const float *Lambda, const int32_t *cu_seqlens,
+                                         int32_t num_seqs, const float *h0, const void *saved,
+                                         void *dx, float *dWa, float *dba, float *dWx,
+                                         float *dbx, float *dLambda, float *dh0,
+                                         void *workspace, rglru_stream stream);
 
 /* One decode step with carried states [P1 semantic-limits list: an initial state and T = 1,
  * both of which the prior art rejects]: for every row b the layer's forward of one token from

@@ -188,7 +188,7 @@ size_t rglru_saved_bytes(const rglru_shape* shape) {
   // the unfused scan's layout, and the fused call's: the tensor-core kernels' own where they
   // take the shape, else the composed path's (which keeps float32 logits)
   const size_t a = scan_layout(d, false).total;
-  const size_t f = fused_supported(d) ? fused_layout(d, false).total : composed_saved(d).total;
+  const size_t f = fused_supported(d) ? fused_fwd_layout(d).total : composed_saved(d).total;
   return a > f ? a : f;
 }
 
@@ -334,6 +334,79 @@ rglru_status rglru_fused_backward(const rglru_shape* shape, const void* dy, cons
   if (e == cudaSuccess)
     e = launch_gate_dw_simt(d, d.io, DT_F32, x, ws + CW.dlr, ws + CW.dli, dWa, dba, dWx, dbx,
                             ws + CW.gate, stream);
+  return cuda_status(e);
+}
+
+// Packed variable-length sequences: one row of T tokens, sequence s on [cu[s], cu[s+1]).
+static rglru_status varlen_setup(const rglru_shape* shape, const int32_t* cu, int32_t S,
+                                 const void* saved, Dims* d, Varlen* v) {
+  rglru_status st = make_dims(shape, d);
+  if (st != RGLRU_OK) return st;
+  if (d->B != 1 || d->mode != RGLRU_CANONICAL || S < 1 || !req(cu) || !req(saved))
+    return RGLRU_ERR_INVALID_ARG;
+  const FusedFwdLayout FL = fused_fwd_layout(*d);
+  v->cu_seqlens = cu;
+  v->S = S;
+  v->seq_start = reinterpret_cast<const int32_t*>(static_cast<const uint8_t*>(saved) + FL.seq_start);
+  v->seq_end = reinterpret_cast<const int32_t*>(static_cast<const uint8_t*>(saved) + FL.seq_end);
+  v->h0 = nullptr;
+  v->hT = nullptr;
+  v->dhT = nullptr;
+  v->dh0 = nullptr;
+  return RGLRU_OK;
+}
+
+rglru_status rglru_fused_forward_varlen(const rglru_shape* shape, const void* x, const void* Wa,
+                                        const float* ba, const void* Wx, const float* bx,
+                                        const float* Lambda, const int32_t* cu_seqlens,
+                                        int32_t num_seqs, const float* h0, void* y, float* hT,
+                                        void* saved, rglru_stream stream) {
+  Dims d;
+  Varlen v;
+  rglru_status st = varlen_setup(shape, cu_seqlens, num_seqs, saved, &d, &v);
+  if (st != RGLRU_OK) return st;
+  if (!req(x) || !req(Wa) || !req(Wx) || !opt(ba) || !opt(bx) || !req(Lambda) || !opt(h0) ||
+      !req(y) || !opt(hT))
+    return RGLRU_ERR_INVALID_ARG;
+  if (!fused_supported(d)) return RGLRU_ERR_UNSUPPORTED;
+  v.h0 = h0;
+  v.hT = hT;
+  cudaError_t e = launch_seq_index(v, d.T, d.W, const_cast<int32_t*>(v.seq_start),
+                                   const_cast<int32_t*>(v.seq_end), false, stream);
+  if (e == cudaSuccess)
+    e = launch_fused_fwd(d, x, Wa, ba, Wx, bx, Lambda, nullptr, nullptr, nullptr, y, nullptr,
+                         saved, g_spin_limit, g_drop_tile, stream, &v);
+  return cuda_status(e);
+}
+
+rglru_status rglru_fused_backward_varlen(const rglru_shape* shape, const void* dy,
+                                         const float* dhT, const void* x, const void* Wa,
+                                         const float* ba, const void* Wx, const float* bx,
+                                         const float* Lambda, const int32_t* cu_seqlens,
+                                         int32_t num_seqs, const float* h0, const void* saved,
+                                         void* dx, float* dWa, float* dba, float* dWx,
+                                         float* dbx, float* dLambda, float* dh0,
+                                         void* workspace, rglru_stream stream) {
+  Dims d;
+  Varlen v;
+  rglru_status st = varlen_setup(shape, cu_seqlens, num_seqs, saved, &d, &v);
+  if (st != RGLRU_OK) return st;
+  if (!req(dy) || !opt(dhT) || !req(x) || !req(Wa) || !req(Wx) || !opt(ba) || !opt(bx) ||
+      !req(Lambda) || !opt(h0) || !req(dx) || !req(dWa) || !req(dWx) || !opt(dba) ||
+      !opt(dbx) || !req(dLambda) || !opt(dh0) || !req(workspace))
+    return RGLRU_ERR_INVALID_ARG;
+  if (!fused_supported(d)) return RGLRU_ERR_UNSUPPORTED;
+  v.h0 = h0;
+  v.dhT = dhT;
+  v.dh0 = dh0;
+  // the token indices were written by the forward into `saved`; empty sequences' dh0 here
+  cudaError_t e = cudaSuccess;
+  if (dh0) e = launch_seq_index(v, d.T, d.W, const_cast<int32_t*>(v.seq_start),
+                                const_cast<int32_t*>(v.seq_end), true, stream);
+  if (e == cudaSuccess)
+    e = launch_fused_bwd(d, dy, nullptr, x, Wa, ba, Wx, bx, Lambda, nullptr, nullptr, nullptr,
+                         saved, dx, dWa, dba, dWx, dbx, dLambda, nullptr, workspace,
+                         g_spin_limit, g_drop_tile, stream, &v);
   return cuda_status(e);
 }
 

@@ -86,6 +86,12 @@ struct BwdParams {
   const int32_t* segment_pos;
   const float* dhT;
   const float* fwd_carry;  // [B][nC+1][W], state entering each chunk (slot-encoded)
+  // packed variable-length sequences (null seq_start: none); one row
+  const int32_t* seq_start;
+  const int32_t* seq_end;
+  const float* h0s;
+  const float* dhTs;
+  float* dh0s;
   float* dh0;
   void* dx;                // written directly for float32 gradients
   float* dWa;
@@ -147,11 +153,37 @@ constexpr int GRP = 8;  // tokens per TMEM load / store group
 // h -> P h + fB and reverse c -> P c + S, with P = prod abar and S = sum_t (prod of abar up
 // to t) dy_t.  GENERAL = false is the warp-uniform fast path: every token valid, no reset,
 // every decay in the near regime.
-template <bool GENERAL>
+// Packed sequences in a part: at a start token (smask) the token continues from its
+// sequence's initial state, h -> a h0[s] + m i x, so the recurrences take 0 for its decay while
+// ab keeps the true a (for the derivatives and dh0[s] = a g); at an end token (emask) dhT[s]
+// joins dy.
+struct SeqB {
+  uint32_t smask, emask;
+  const int32_t* start;  // sequence starting at each of the part's tokens (where smask)
+  const int32_t* end;    // sequence ending at each of the part's tokens (where emask)
+  const float* h0;       // h0[0][w], rows W apart, or null
+  const float* dhT;      // dhT[0][w] or null
+  float* dh0;            // dh0[0][w] or null
+  int W;
+};
+__device__ __forceinline__ float seqb_h0(const SeqB& sq, int u) {
+  return sq.h0 ? sq.h0[(size_t)sq.start[u] * sq.W] : 0.0f;
+}
+__device__ __forceinline__ float seqb_dhT(const SeqB& sq, int u) {
+  return sq.dhT ? sq.dhT[(size_t)sq.end[u] * sq.W] : 0.0f;
+}
+// The chains' decay of a token pair: 0 at sequence starts.
+__device__ __forceinline__ float2 chain_decay(const SeqB& sq, int u, float2 a) {
+  if ((sq.smask >> u) & 1u) a.x = 0.0f;
+  if ((sq.smask >> (u + 1)) & 1u) a.y = 0.0f;
+  return a;
+}
+
+template <bool GENERAL, bool VARLEN>
 __device__ __forceinline__ void bwd_pass1(uint32_t tcol, uint32_t xb0, uint32_t xb1, uint32_t dyb,
                                           const GateK& gk, uint32_t rmask, int valid,
-                                          float2 (&ab)[PT / 2], uint32_t (&xr)[PT / 2], float& P,
-                                          float& fB, float& S) {
+                                          float2 (&ab)[PT / 2], uint32_t (&xr)[PT / 2],
+                                          const SeqB& sq, float& P, float& fB, float& S) {
   P = 1.0f;
   fB = 0.0f;
   S = 0.0f;
@@ -201,12 +233,20 @@ __device__ __forceinline__ void bwd_pass1(uint32_t tcol, uint32_t xb0, uint32_t 
       } else {
         gates_near2_i(lr, li, gk, abar, mi, r, i);
       }
-      const float2 bv = mul2(mi, xv);
-      fB = fmaf(abar.x, fB, bv.x);
-      P *= abar.x;
+      float2 bv = mul2(mi, xv);
+      float2 ach = abar;  // the chains' decay
+      if (VARLEN && GENERAL && (sq.smask | sq.emask)) {
+        if ((sq.smask >> u) & 1u) bv.x = fmaf(abar.x, seqb_h0(sq, u), bv.x);
+        if ((sq.smask >> (u + 1)) & 1u) bv.y = fmaf(abar.y, seqb_h0(sq, u + 1), bv.y);
+        ach = chain_decay(sq, u, abar);
+        if ((sq.emask >> u) & 1u) dyv.x += seqb_dhT(sq, u);
+        if ((sq.emask >> (u + 1)) & 1u) dyv.y += seqb_dhT(sq, u + 1);
+      }
+      fB = fmaf(ach.x, fB, bv.x);
+      P *= ach.x;
       S = fmaf(P, dyv.x, S);
-      fB = fmaf(abar.y, fB, bv.y);
-      P *= abar.y;
+      fB = fmaf(ach.y, fB, bv.y);
+      P *= ach.y;
       S = fmaf(P, dyv.y, S);
       ab[u / 2] = abar;
       m4[2 * q] = mi.x;
@@ -235,8 +275,9 @@ __device__ __forceinline__ void bwd_pass1(uint32_t tcol, uint32_t xb0, uint32_t 
 
 // Pass 2a (tokens ascending): h_{t-1} of every token from the state h entering the part,
 // parked in the dx columns (free once the previous tile's dx has been written out).
+template <bool GENERAL, bool VARLEN>
 __device__ __forceinline__ void bwd_pass2a(uint32_t tcol, const uint32_t (&xr)[PT / 2],
-                                           const float2 (&ab)[PT / 2], float h) {
+                                           const float2 (&ab)[PT / 2], const SeqB& sq, float h) {
   float m4[GRP];
   tc::tmem_ld(tcol + COL_LR, m4);
   tc::tmem_ld_wait();
@@ -250,8 +291,11 @@ __device__ __forceinline__ void bwd_pass2a(uint32_t tcol, const uint32_t (&xr)[P
       const int u = g * GRP + 2 * q;
       const float2 xv = bf16x2_unpack(xr[u / 2]);
       const float2 bv = mul2(make_float2(m4[2 * q], m4[2 * q + 1]), xv);
+      // at a sequence start the state before the token is the sequence's initial state
+      if (VARLEN && GENERAL && ((sq.smask >> u) & 1u)) h = seqb_h0(sq, u);
       h4[2 * q] = h;
       h = fmaf(ab[u / 2].x, h, bv.x);
+      if (VARLEN && GENERAL && ((sq.smask >> (u + 1)) & 1u)) h = seqb_h0(sq, u + 1);
       h4[2 * q + 1] = h;
       h = fmaf(ab[u / 2].y, h, bv.y);
     }
@@ -270,10 +314,11 @@ __device__ __forceinline__ void bwd_pass2a(uint32_t tcol, const uint32_t (&xr)[P
 // from the right, and the pointwise gradients; dlr, dli go to the dl operand buffers as bf16
 // hi + lo pairs, the direct dx term g m i over h_{t-1} in the dx columns (the accumulator of
 // the dx MMAs).  dsp sums dla r (the softplus gradient is -8 times the total).
-template <bool GENERAL>
+template <bool GENERAL, bool VARLEN>
 __device__ __forceinline__ void bwd_pass2b(uint32_t tcol, int tb, int j,
                                            const uint32_t (&xr)[PT / 2], uint32_t dyb, float nk,
-                                           int valid, const float2 (&ab)[PT / 2], float cin,
+                                           int valid, const float2 (&ab)[PT / 2], const SeqB& sq,
+                                           float cin,
                                            uint8_t* s_dl, float2& dsp, float2& dba, float2& dbx) {
   float gnext = cin, anext = 1.0f;
   constexpr int G0 = PT / GRP - 1;
@@ -303,18 +348,27 @@ __device__ __forceinline__ void bwd_pass2b(uint32_t tcol, int tb, int j,
       const float2 xv = bf16x2_unpack(xr[u / 2]);
       float2 dyv = make_float2(lds_bf16(dyb + u * DY_ROW), lds_bf16(dyb + (u + 1) * DY_ROW));
       if (GENERAL) {
+        if (VARLEN) {
+          if ((sq.emask >> u) & 1u) dyv.x += seqb_dhT(sq, u);
+          if ((sq.emask >> (u + 1)) & 1u) dyv.y += seqb_dhT(sq, u + 1);
+        }
         if (u >= valid) dyv.x = 0.0f;
         if (u + 1 >= valid) dyv.y = 0.0f;
       }
       const float2 abar = ab[u / 2];
+      const float2 ach = (VARLEN && GENERAL) ? chain_decay(sq, u, abar) : abar;  // 0 at starts
       const float2 mi = make_float2(m4[2 * q], m4[2 * q + 1]);
       const float2 r = make_float2(r4[2 * q], r4[2 * q + 1]);
       const float2 i = make_float2(i4[2 * q], i4[2 * q + 1]);
       float2 gv;
       gv.y = fmaf(anext, gnext, dyv.y);
-      gv.x = fmaf(abar.y, gv.y, dyv.x);
+      gv.x = fmaf(ach.y, gv.y, dyv.x);
       gnext = gv.x;
-      anext = abar.x;
+      anext = ach.x;
+      if (VARLEN && GENERAL && sq.dh0) {  // d h0[s] = a g at the sequence's first token
+        if ((sq.smask >> u) & 1u) sq.dh0[(size_t)sq.start[u] * sq.W] = abar.x * gv.x;
+        if ((sq.smask >> (u + 1)) & 1u) sq.dh0[(size_t)sq.start[u + 1] * sq.W] = abar.y * gv.y;
+      }
       // d h_t / d la = abar (h_{t-1} - abar x i / m) with i / m = i^2 / (m i); zero at reset
       // tokens (abar = 0), past T and where the decay is exactly 1 (m = 0)
       const float2 nw = mul2(mul2(i, i), make_float2(rcp_approx(-mi.x), rcp_approx(-mi.y)));
@@ -353,7 +407,7 @@ __device__ __forceinline__ void bwd_pass2b(uint32_t tcol, int tb, int j,
   tc::tmem_st_wait();
 }
 
-template <typename GT>
+template <typename GT, bool VARLEN>
 __global__ void __maxnreg__(MAXREG)
     k_fused_bwd(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_dy,
                 const __grid_constant__ CUtensorMap tm_wa, const __grid_constant__ CUtensorMap tm_wx,
@@ -555,6 +609,8 @@ __global__ void __maxnreg__(MAXREG)
       float hin_tile = 0.0f;
       int valid = 0;
       bool fast = false;
+      uint32_t rmask = 0;
+      SeqB sq{0u, 0u, nullptr, nullptr, nullptr, nullptr, nullptr, p.W};
       // Part 0 requests the look-back slots of this tile's carry from the right now; they are
       // read after pass 2a, so the L2 round trip hides behind passes 1 and 2a.
       const size_t cidx = (size_t)b * p.nC + c;
@@ -573,7 +629,17 @@ __global__ void __maxnreg__(MAXREG)
       }
       if (have) {
         hin_tile = slot_get1(p.fwd_carry + ((size_t)b * (p.nC + 1) + c) * p.W + w);
-        uint32_t rmask = 0;
+        if (VARLEN) {
+          const size_t t0 = (size_t)b * p.T + (size_t)c * FUSED_C + tb;
+          const bool in = c * FUSED_C + tb + lane < p.T;
+          sq.start = p.seq_start + t0;
+          sq.end = p.seq_end + t0;
+          sq.smask = __ballot_sync(0xffffffffu, in && sq.start[lane] >= 0);
+          sq.emask = __ballot_sync(0xffffffffu, in && sq.end[lane] >= 0);
+          sq.h0 = p.h0s ? p.h0s + w : nullptr;
+          sq.dhT = p.dhTs ? p.dhTs + w : nullptr;
+          sq.dh0 = p.dh0s ? p.dh0s + w : nullptr;
+        }
         if (p.canonical) {
           const int t = c * FUSED_C + tb + lane;
           rmask = __ballot_sync(0xffffffffu, lane < PT && t < p.T &&
@@ -581,14 +647,14 @@ __global__ void __maxnreg__(MAXREG)
                                                           (size_t)b * p.T + t));
         }
         valid = min(FUSED_C, p.T - c * FUSED_C) - tb;
-        fast = near_all && rmask == 0u && valid >= PT;
+        fast = near_all && rmask == 0u && (sq.smask | sq.emask) == 0u && valid >= PT;
         ctl.wait(lg_full, it & 1);
         ctl.wait(&in_full[st], ph);
         tc::tc_fence_after();
         if (fast)
-          bwd_pass1<false>(tcol, xb0, xb1, dyb, gk, 0u, PT, ab, xr, P, fB, S);
+          bwd_pass1<false, VARLEN>(tcol, xb0, xb1, dyb, gk, 0u, PT, ab, xr, sq, P, fB, S);
         else
-          bwd_pass1<true>(tcol, xb0, xb1, dyb, gk, rmask, valid, ab, xr, P, fB, S);
+          bwd_pass1<true, VARLEN>(tcol, xb0, xb1, dyb, gk, rmask, valid, ab, xr, sq, P, fB, S);
       }
 
       // dx of tile it - 1: TMEM -> smem [token][channel] as bf16 (float32 goes straight to HBM).
@@ -657,7 +723,10 @@ __global__ void __maxnreg__(MAXREG)
 
       // Pass 2a: h_{t-1} through the part, from the earlier parts' map applied to the tile's
       // entry state.
-      bwd_pass2a(tcol, xr, ab, fmaf(Fa, hin_tile, Fb));
+      if (VARLEN && !fast)
+        bwd_pass2a<true, VARLEN>(tcol, xr, ab, sq, fmaf(Fa, hin_tile, Fb));
+      else
+        bwd_pass2a<false, VARLEN>(tcol, xr, ab, sq, fmaf(Fa, hin_tile, Fb));
 
       if (part == 0) {
         const float cin =
@@ -675,9 +744,9 @@ __global__ void __maxnreg__(MAXREG)
       if (it > 0) ctl.wait(dl_empty, (it - 1) & 1);
       tc::tc_fence_after();
       if (fast)
-        bwd_pass2b<false>(tcol, tb, j, xr, dyb, gk.nk, PT, ab, cin, s_dl, dsp, dba, dbx);
+        bwd_pass2b<false, VARLEN>(tcol, tb, j, xr, dyb, gk.nk, PT, ab, sq, cin, s_dl, dsp, dba, dbx);
       else
-        bwd_pass2b<true>(tcol, tb, j, xr, dyb, gk.nk, valid, ab, cin, s_dl, dsp, dba, dbx);
+        bwd_pass2b<true, VARLEN>(tcol, tb, j, xr, dyb, gk.nk, valid, ab, sq, cin, s_dl, dsp, dba, dbx);
       tc::fence_proxy_async_smem();
       tc::tc_fence_before();
       __syncwarp();
@@ -818,7 +887,8 @@ cudaError_t launch_fused_bwd(const Dims& d, const void* dy, const float* dhT, co
                              const float* Lambda, const uint8_t* rm, const int32_t* sp,
                              const float* h0, const void* saved, void* dx, float* dWa,
                              float* dba, float* dWx, float* dbx, float* dLambda, float* dh0,
-                             void* ws, int spin_limit, int drop_tile, cudaStream_t s) {
+                             void* ws, int spin_limit, int drop_tile, cudaStream_t s,
+                             const Varlen* vl) {
   (void)h0;  // the chunk entry states saved by the forward already include h0
   if (!fused_supported(d)) return cudaErrorNotSupported;
   const uint64_t W = d.W, T = d.T, B = d.B;
@@ -873,8 +943,15 @@ cudaError_t launch_fused_bwd(const Dims& d, const void* dy, const float* dhT, co
   p.reset_mask = rm;
   p.segment_pos = sp;
   p.dhT = dhT;
-  p.fwd_carry = reinterpret_cast<const float*>(static_cast<const uint8_t*>(saved) +
-                                               fused_layout(d, false).carry);
+  const FusedFwdLayout FL = fused_fwd_layout(d);
+  p.fwd_carry = reinterpret_cast<const float*>(static_cast<const uint8_t*>(saved) + FL.L.carry);
+  p.seq_start = vl ? reinterpret_cast<const int32_t*>(static_cast<const uint8_t*>(saved) + FL.seq_start)
+                   : nullptr;
+  p.seq_end = vl ? reinterpret_cast<const int32_t*>(static_cast<const uint8_t*>(saved) + FL.seq_end)
+                 : nullptr;
+  p.h0s = vl ? vl->h0 : nullptr;
+  p.dhTs = vl ? vl->dhT : nullptr;
+  p.dh0s = vl ? vl->dh0 : nullptr;
   p.dh0 = dh0;
   p.scratch = static_cast<uint8_t*>(ws);
   p.F = F;
@@ -890,7 +967,8 @@ cudaError_t launch_fused_bwd(const Dims& d, const void* dy, const float* dhT, co
   p.dbx = dbx;
   p.dLambda = dLambda;
   const size_t smem = SMEM_BYTES;
-  auto kern = gf32 ? k_fused_bwd<float> : k_fused_bwd<bf16>;
+  auto kern = vl ? (gf32 ? k_fused_bwd<float, true> : k_fused_bwd<bf16, true>)
+                 : (gf32 ? k_fused_bwd<float, false> : k_fused_bwd<bf16, false>);
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   e = clear_slots(ws, p.F.L, s);

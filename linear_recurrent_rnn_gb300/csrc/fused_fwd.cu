@@ -74,6 +74,11 @@ struct FwdParams {
   const int32_t* segment_pos;
   const float* h0;
   float* hT;
+  // packed variable-length sequences (null seq_start: none); one row
+  const int32_t* seq_start;
+  const int32_t* seq_end;
+  const float* h0s;
+  float* hTs;
   uint8_t* scratch;
   ScanLayout L;
   int spin_limit, drop_tile;
@@ -101,10 +106,22 @@ struct Ctl {
 // logits just read (hl over lr, Ac over li); (rA, rh) = the part's map.  GENERAL handles resets, tokens past
 // T and decays with la <= -1/8; the fast variant (chosen warp-uniformly) has none.
 constexpr int GRP = 8;  // tokens per TMEM load / store group
-template <bool GENERAL>
+// Sequence starts (smask): the token continues from its sequence's initial state instead of
+// the carried one, h -> a h0[s] + m i x.
+struct SeqStarts {
+  uint32_t smask;         // tokens of the part where a sequence starts
+  const int32_t* seq;     // sequence index of the part's tokens (valid where smask is set)
+  const float* h0;        // h0[0][w] of the channel, rows W apart, or null (zeros)
+  int W;
+};
+__device__ __forceinline__ float seq_h0(const SeqStarts& sq, int u) {
+  return sq.h0 ? sq.h0[(size_t)sq.seq[u] * sq.W] : 0.0f;
+}
+template <bool GENERAL, bool VARLEN>
 __device__ __forceinline__ void local_scan(uint32_t t_lr, uint32_t t_li, uint32_t xb0,
                                            uint32_t xb1, const GateK& gk,
-                                           uint32_t rmask, int valid, float& rh, float& rA) {
+                                           uint32_t rmask, int valid, const SeqStarts& sq,
+                                           float& rh, float& rA) {
   rh = 0.0f;
   rA = 1.0f;
 #pragma unroll
@@ -142,7 +159,17 @@ __device__ __forceinline__ void local_scan(uint32_t t_lr, uint32_t t_li, uint32_
       } else {
         gates_near2(lr, li, gk, abar, mi, r);
       }
-      const float2 bv = mul2(mi, xv);
+      float2 bv = mul2(mi, xv);
+      if (VARLEN && GENERAL && sq.smask) {
+        if ((sq.smask >> u) & 1u) {
+          bv.x = fmaf(abar.x, seq_h0(sq, u), bv.x);
+          abar.x = 0.0f;
+        }
+        if ((sq.smask >> (u + 1)) & 1u) {
+          bv.y = fmaf(abar.y, seq_h0(sq, u + 1), bv.y);
+          abar.y = 0.0f;
+        }
+      }
       rh = fmaf(abar.x, rh, bv.x);
       rA *= abar.x;
       oh[2 * q] = rh;
@@ -158,6 +185,7 @@ __device__ __forceinline__ void local_scan(uint32_t t_lr, uint32_t t_li, uint32_
   tc::tmem_st_wait();
 }
 
+template <bool VARLEN>
 __global__ void __maxnreg__(MAXREG)
     k_fused_fwd(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_wa,
                 const __grid_constant__ CUtensorMap tm_wx, const __grid_constant__ CUtensorMap tm_y,
@@ -302,6 +330,13 @@ __global__ void __maxnreg__(MAXREG)
                                                         (size_t)b * p.T + t));
       }
       const int valid = min(FUSED_C, p.T - c * FUSED_C) - tb;  // tokens of this part < T
+      SeqStarts sq{0u, nullptr, nullptr, p.W};
+      if (VARLEN) {
+        const int t = c * FUSED_C + tb + lane;
+        sq.seq = p.seq_start + (size_t)b * p.T + c * FUSED_C + tb;
+        sq.smask = __ballot_sync(0xffffffffu, lane < PT && t < p.T && sq.seq[lane] >= 0);
+        sq.h0 = p.h0s ? p.h0s + w : nullptr;
+      }
       ctl.wait(&acc_full[a], aph);
       ctl.wait(&x_full[st], ph);
       tc::tc_fence_after();
@@ -309,10 +344,10 @@ __global__ void __maxnreg__(MAXREG)
       const uint32_t xb0 = xt + xoff0, xb1 = xt + xoff1;
       const uint32_t t_lr = tmem + lane_base + a * 128 + tb;
       float rh, rA;
-      if (near_all && rmask == 0u && valid >= PT)
-        local_scan<false>(t_lr, t_lr + 64, xb0, xb1, gk, 0u, PT, rh, rA);
+      if (near_all && rmask == 0u && sq.smask == 0u && valid >= PT)
+        local_scan<false, VARLEN>(t_lr, t_lr + 64, xb0, xb1, gk, 0u, PT, sq, rh, rA);
       else
-        local_scan<true>(t_lr, t_lr + 64, xb0, xb1, gk, rmask, valid, rh, rA);
+        local_scan<true, VARLEN>(t_lr, t_lr + 64, xb0, xb1, gk, rmask, valid, sq, rh, rA);
       s_agg[(a * NPART + part) * FUSED_K + j] = make_float2(rA, rh);  // the part's map
       tc::tc_fence_before();
       __syncwarp();
@@ -376,6 +411,16 @@ __global__ void __maxnreg__(MAXREG)
         if ((blk * ntiles + n - p.P) != p.drop_tile) slot_put1(crow + (size_t)(pc + 1) * p.W + w, hend);
         if (pc == 0) slot_put1(crow + w, hin_t);
         if (pc == p.nC - 1 && p.hT) p.hT[(size_t)pb * p.W + w] = hend;
+        // packed sequences ending in the tile: their final state (warp-uniform masks)
+        uint32_t em0 = 0u, em1 = 0u;
+        int e0 = -1, e1 = -1;
+        if (VARLEN) {
+          const size_t tb0 = (size_t)pb * p.T + (size_t)pc * FUSED_C;
+          if (pc * FUSED_C + lane < p.T) e0 = p.seq_end[tb0 + lane];
+          if (pc * FUSED_C + 32 + lane < p.T) e1 = p.seq_end[tb0 + 32 + lane];
+          em0 = __ballot_sync(0xffffffffu, e0 >= 0);
+          em1 = __ballot_sync(0xffffffffu, e1 >= 0);
+        }
         uint8_t* yb = ystrip + ((it - 1) & 1) * YSTRIP_BYTES;
         if (lane == 0) tc::tma_store_wait_read1();  // the strip stored two tiles ago is free
         __syncwarp();
@@ -397,6 +442,17 @@ __global__ void __maxnreg__(MAXREG)
               const int tl = pp * PT + c16 + u;
               *reinterpret_cast<bf16*>(yb + tl * 64 + lane * 2) = __float2bfloat16_rn(yv.x);
               *reinterpret_cast<bf16*>(yb + (tl + 1) * 64 + lane * 2) = __float2bfloat16_rn(yv.y);
+              if (VARLEN && (em0 | em1) != 0u) {
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                  const int tt = tl + h;
+                  const uint32_t m = tt < 32 ? em0 : em1;
+                  if ((m >> (tt & 31)) & 1u) {
+                    const int sidx = __shfl_sync(0xffffffffu, tt < 32 ? e0 : e1, tt & 31);
+                    if (p.hTs) p.hTs[(size_t)sidx * p.W + w] = h ? yv.y : yv.x;
+                  }
+                }
+              }
             }
           }
         }
@@ -493,7 +549,7 @@ cudaError_t launch_fused_fwd(const Dims& d, const void* x, const void* Wa, const
                              const void* Wx, const float* bx, const float* Lambda,
                              const uint8_t* rm, const int32_t* sp, const float* h0, void* y,
                              float* hT, void* saved, int spin_limit, int drop_tile,
-                             cudaStream_t s) {
+                             cudaStream_t s, const Varlen* vl) {
   if (!fused_supported(d)) return cudaErrorNotSupported;
   CUtensorMap mx, mwa, mwx, my;
   cudaError_t e = make_maps(d, x, Wa, Wx, y, &mx, &mwa, &mwx, &my);
@@ -513,6 +569,17 @@ cudaError_t launch_fused_fwd(const Dims& d, const void* x, const void* Wa, const
   p.segment_pos = sp;
   p.h0 = h0;
   p.hT = hT;
+  p.seq_start = nullptr;
+  p.seq_end = nullptr;
+  p.h0s = nullptr;
+  p.hTs = nullptr;
+  if (vl) {
+    const FusedFwdLayout FL = fused_fwd_layout(d);
+    p.seq_start = reinterpret_cast<const int32_t*>(static_cast<uint8_t*>(saved) + FL.seq_start);
+    p.seq_end = reinterpret_cast<const int32_t*>(static_cast<uint8_t*>(saved) + FL.seq_end);
+    p.h0s = vl->h0;
+    p.hTs = vl->hT;
+  }
   p.scratch = static_cast<uint8_t*>(saved);
   p.L = fused_layout(d, false);
   p.spin_limit = spin_limit;
@@ -520,7 +587,8 @@ cudaError_t launch_fused_fwd(const Dims& d, const void* x, const void* Wa, const
   const LookbackPlan lp = lookback_plan(p.P, d.B);
   p.lb_dist = lp.dist;
   p.lb_shift = lp.shift;
-  e = cudaFuncSetAttribute(k_fused_fwd, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  auto kern = vl ? k_fused_fwd<true> : k_fused_fwd<false>;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)SMEM_BYTES);
   if (e != cudaSuccess) return e;
   e = clear_slots(saved, p.L, s);
@@ -536,7 +604,7 @@ cudaError_t launch_fused_fwd(const Dims& d, const void* x, const void* Wa, const
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   kernel_event_before(s);
-  e = cudaLaunchKernelEx(&cfg, k_fused_fwd, mx, mwa, mwx, my, p);
+  e = cudaLaunchKernelEx(&cfg, kern, mx, mwa, mwx, my, p);
   kernel_event_after(s);
   if (e == cudaSuccess) note_launches(1);
   return e;

@@ -86,6 +86,37 @@ inline LookbackPlan lookback_plan(int P, int B) {
 inline ScanLayout fused_layout(const Dims& d, bool backward) {
   return scan_layout_n(d.B, fused_chunks(d), d.ng, d.W, backward);
 }
+// Fused forward `saved`: the look-back scratch (its chunk-boundary states are where the
+// backward starts), then, for packed variable-length sequences, two int32 [T] token indices:
+// the sequence that starts at each token and the one that ends there (-1: none).
+struct FusedFwdLayout {
+  ScanLayout L;
+  size_t seq_start, seq_end, total;
+};
+inline FusedFwdLayout fused_fwd_layout(const Dims& d) {
+  FusedFwdLayout F;
+  F.L = fused_layout(d, false);
+  F.seq_start = align_up(F.L.total, 256);
+  F.seq_end = align_up(F.seq_start + (size_t)d.T * 4, 256);
+  F.total = align_up(F.seq_end + (size_t)d.T * 4, 256);
+  return F;
+}
+
+// Packed variable-length sequences (one row, sequence s on tokens [cu[s], cu[s+1])): the
+// per-sequence states and the token indices in `saved`.
+struct Varlen {
+  const int32_t* cu_seqlens;  // device [S + 1]
+  int S;
+  const int32_t* seq_start;   // [T]: s if sequence s (non-empty) starts at the token, else -1
+  const int32_t* seq_end;     // [T]: s if sequence s ends at the token, else -1
+  const float* h0;            // [S][W] or null (zeros)
+  float* hT;                  // [S][W] or null (forward)
+  const float* dhT;           // [S][W] or null (backward)
+  float* dh0;                 // [S][W] or null (backward)
+};
+// Fills the token indices (and, for empty sequences, hT = h0 or dh0 = dhT).
+cudaError_t launch_seq_index(const Varlen& v, int T, int W, int32_t* seq_start,
+                             int32_t* seq_end, bool backward, cudaStream_t s);
 
 // Fused backward workspace: the reverse look-back scratch, then per-CTA partial sums (the
 // kernel runs at most FUSED_MAX_CTAS CTAs, each owning one gate block): dWa / dWx partials
@@ -201,7 +232,7 @@ cudaError_t launch_fused_fwd(const Dims& d, const void* x, const void* Wa, const
                              const void* Wx, const float* bx, const float* Lambda,
                              const uint8_t* rm, const int32_t* sp, const float* h0, void* y,
                              float* hT, void* saved, int spin_limit, int drop_tile,
-                             cudaStream_t s);
+                             cudaStream_t s, const Varlen* vl = nullptr);
 bool fused_supported(const Dims& d);
 int fused_ctas_per_block(const Dims& d);
 // Clears the status word of a scan layout and marks every carry / aggregate slot empty.
@@ -215,7 +246,8 @@ cudaError_t launch_fused_bwd(const Dims& d, const void* dy, const float* dhT, co
                              const float* Lambda, const uint8_t* rm, const int32_t* sp,
                              const float* h0, const void* saved, void* dx, float* dWa,
                              float* dba, float* dWx, float* dbx, float* dLambda, float* dh0,
-                             void* ws, int spin_limit, int drop_tile, cudaStream_t s);
+                             void* ws, int spin_limit, int drop_tile, cudaStream_t s,
+                             const Varlen* vl = nullptr);
 
 // One decode step (T = 1) with carried states: projections, gates and the state update in one
 // kernel (decode.cu); k <= STEP_KMAX.

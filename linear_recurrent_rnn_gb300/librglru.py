@@ -47,7 +47,8 @@ EXPORTS = ("rglru_status_string", "rglru_saved_bytes", "rglru_workspace_bytes",
            "rglru_gate_proj", "rglru_forward", "rglru_backward", "rglru_gate_proj_backward",
            "rglru_fused_forward", "rglru_fused_backward", "rglru_sync_status",
            "rglru_debug_lookback", "rglru_kernel_launches", "rglru_forward_noalloc",
-           "rglru_debug_kernel_events", "rglru_step")
+           "rglru_debug_kernel_events", "rglru_step", "rglru_fused_forward_varlen",
+           "rglru_fused_backward_varlen")
 
 # Static look-back scratch of rglru_forward_noalloc, per GPU (RGLRU_NOALLOC_SCRATCH_BYTES).
 NOALLOC_SCRATCH_BYTES = 16 << 20
@@ -88,11 +89,15 @@ def lib():
             L.rglru_debug_kernel_events.argtypes = [ctypes.c_void_p, ctypes.c_void_p]
             L.rglru_debug_kernel_events.restype = None
             L.rglru_step.argtypes = [S] + [P] * 11
+            L.rglru_fused_forward_varlen.argtypes = [S] + [P] * 7 + [ctypes.c_int32] + [P] * 5
+            L.rglru_fused_backward_varlen.argtypes = ([S] + [P] * 9 + [ctypes.c_int32] +
+                                                      [P] * 11)
             L.rglru_kernel_launches.argtypes = []
             L.rglru_kernel_launches.restype = ctypes.c_uint64
             for n in ("rglru_gate_proj", "rglru_forward", "rglru_backward",
                       "rglru_gate_proj_backward", "rglru_fused_forward", "rglru_fused_backward",
-                      "rglru_sync_status", "rglru_step"):
+                      "rglru_sync_status", "rglru_step", "rglru_fused_forward_varlen",
+                      "rglru_fused_backward_varlen"):
                 getattr(L, n).restype = ctypes.c_int
             _lib = L
     return _lib
@@ -205,6 +210,22 @@ def rglru_step(shape, x, Wa, ba, Wx, bx, Lambda, reset, h_in, y, h_out, stream=N
     _check("rglru_step", lib().rglru_step(
         ctypes.byref(shape), _p(x), _p(Wa), _p(ba), _p(Wx), _p(bx), _p(Lambda), _p(reset),
         _p(h_in), _p(y), _p(h_out), _stream(stream)))
+
+
+def rglru_fused_forward_varlen(shape, x, Wa, ba, Wx, bx, Lambda, cu_seqlens, num_seqs, h0, y,
+                               hT, saved, stream=None):
+    _check("rglru_fused_forward_varlen", lib().rglru_fused_forward_varlen(
+        ctypes.byref(shape), _p(x), _p(Wa), _p(ba), _p(Wx), _p(bx), _p(Lambda), _p(cu_seqlens),
+        int(num_seqs), _p(h0), _p(y), _p(hT), _p(saved), _stream(stream)))
+
+
+def rglru_fused_backward_varlen(shape, dy, dhT, x, Wa, ba, Wx, bx, Lambda, cu_seqlens, num_seqs,
+                                h0, saved, dx, dWa, dba, dWx, dbx, dLambda, dh0, workspace,
+                                stream=None):
+    _check("rglru_fused_backward_varlen", lib().rglru_fused_backward_varlen(
+        ctypes.byref(shape), _p(dy), _p(dhT), _p(x), _p(Wa), _p(ba), _p(Wx), _p(bx), _p(Lambda),
+        _p(cu_seqlens), int(num_seqs), _p(h0), _p(saved), _p(dx), _p(dWa), _p(dba), _p(dWx),
+        _p(dbx), _p(dLambda), _p(dh0), _p(workspace), _stream(stream)))
 
 
 def rglru_sync_status(buf: torch.Tensor, stream=None) -> int:

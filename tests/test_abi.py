@@ -103,3 +103,29 @@ def test_step_host_validation(lib):
     assert call(R.make_shape(2, 1, 256, 2, R.BF16, R.BF16, R.CANONICAL),
                 x=A + 4) == R.ERR_INVALID_ARG
     assert call(R.make_shape(2, 1, 1024, 1, R.BF16, R.BF16, R.CANONICAL)) == R.ERR_UNSUPPORTED
+
+
+def test_varlen_host_validation(lib):
+    """The packed-sequence entry points check on the host (fake, never dereferenced
+    addresses): one row, canonical mode, at least one sequence, the offsets array present,
+    and tensor-core shapes only."""
+    A = 1 << 20
+    P = lambda v: None if v is None else ctypes.c_void_p(v)
+
+    def fwd(sh, cu=A, S=3, saved=A):
+        return lib.rglru_fused_forward_varlen(ctypes.byref(sh), P(A), P(A), None, P(A), None,
+                                              P(A), P(cu), S, None, P(A), None, P(saved), None)
+
+    def bwd(sh, cu=A, S=3, ws=A):
+        return lib.rglru_fused_backward_varlen(ctypes.byref(sh), P(A), None, P(A), P(A), None,
+                                               P(A), None, P(A), P(cu), S, None, P(A), P(A),
+                                               P(A), None, P(A), None, P(A), None, P(ws), None)
+    good = R.make_shape(1, 256, 256, 2, R.BF16, R.BF16, R.CANONICAL)
+    for call in (fwd, bwd):
+        assert call(R.make_shape(2, 256, 256, 2, R.BF16, R.BF16, R.CANONICAL)) == R.ERR_INVALID_ARG
+        assert call(R.make_shape(1, 256, 256, 2, R.BF16, R.BF16, R.RESTRICTED)) == R.ERR_INVALID_ARG
+        assert call(good, S=0) == R.ERR_INVALID_ARG
+        assert call(good, cu=None) == R.ERR_INVALID_ARG
+        assert call(R.make_shape(1, 256, 256, 4, R.BF16, R.BF16, R.CANONICAL)) == R.ERR_UNSUPPORTED
+    assert fwd(good, saved=None) == R.ERR_INVALID_ARG
+    assert bwd(good, ws=None) == R.ERR_INVALID_ARG

@@ -1,0 +1,89 @@
+"""Packed variable-length sequences (rglru_fused_forward_varlen / _backward_varlen) against the
+float64 oracle run on every sequence as a row of its own: sequence s continues from h0[s]
+without a reset, its final state is hT[s], dhT[s] joins the gradient at its last token and
+dh0[s] is its initial-state gradient; the parameter gradients are the sums over sequences.
+Lengths include empty sequences (hT = h0, dh0 = dhT), a leading empty one (the next sequence
+starts at token 0), a sequence of one token, and starts inside and across 64-token chunks."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from linear_recurrent_rnn_gb300 import librglru as R
+from linear_recurrent_rnn_gb300.inputs import Workload, as_f64, generate
+
+from helpers import assert_close, dev, host
+
+pytestmark = pytest.mark.gpu
+
+CASES = [
+    ([0, 1, 0, 70, 64, 33, 0, 130, 5, 1], (0.9, 0.999), 41, "bf16"),
+    ([200, 3, 97], (0.05, 0.95), 42, "bf16"),   # short memories: the general decay branch too
+    ([31, 1, 64, 129, 0, 2], (0.5, 0.999), 43, "f32"),   # float32 dx
+]
+
+
+@pytest.mark.parametrize("lengths,u_range,seed,grad", CASES, ids=["mixed", "far", "f32grad"])
+def test_varlen_matches_per_sequence_oracle(lengths, u_range, seed, grad):
+    T = int(sum(lengths))
+    S = len(lengths)
+    W, k = 256, 128
+    wl = Workload("varlen", 1, T, W, k, "bf16", "canonical", u_range, h0_std=1.0)
+    inp = generate(wl, seed)
+    rng = np.random.default_rng(seed)
+    h0s = torch.from_numpy(rng.standard_normal((S, W))).float()
+    dhTs = torch.from_numpy(rng.standard_normal((S, W))).float()
+    ba = torch.from_numpy(rng.normal(0.0, 0.1, W)).float()
+    bx = torch.from_numpy(rng.normal(0.0, 0.1, W)).float()
+    cu = np.concatenate([[0], np.cumsum(lengths)]).astype(np.int32)
+
+    d = {n: dev(v) for n, v in inp.items() if isinstance(v, torch.Tensor)}
+    gdt = R.BF16 if grad == "bf16" else R.F32
+    sh = R.make_shape(1, T, W, W // k, R.BF16, gdt, R.CANONICAL)
+    cu_d = torch.from_numpy(cu).cuda()
+    y = torch.empty_like(d["x"])
+    hT = torch.empty(S, W, device="cuda")
+    saved, ws = R.alloc_saved(sh), R.alloc_workspace(sh)
+    R.rglru_fused_forward_varlen(sh, d["x"], d["Wa"], dev(ba), d["Wx"], dev(bx), d["Lambda"],
+                                 cu_d, S, dev(h0s), y, hT, saved)
+    dx = torch.empty(1, T, W, device="cuda", dtype=R.TORCH_DT[gdt])
+    dWa = torch.empty(W // k, k, k, device="cuda")
+    dWx = torch.empty_like(dWa)
+    dba, dbx, dL = (torch.empty(W, device="cuda") for _ in range(3))
+    dh0 = torch.empty(S, W, device="cuda")
+    R.rglru_fused_backward_varlen(sh, d["dy"], dev(dhTs), d["x"], d["Wa"], dev(ba), d["Wx"],
+                                  dev(bx), d["Lambda"], cu_d, S, dev(h0s), saved, dx, dWa, dba,
+                                  dWx, dbx, dL, dh0, ws)
+    assert R.rglru_sync_status(saved) == R.OK
+    assert R.rglru_sync_status(ws) == R.OK
+
+    x, Wa, Wx, Lam, dy = (as_f64(inp[n]) for n in ("x", "Wa", "Wx", "Lambda", "dy"))
+    ba64, bx64 = ba.double().numpy(), bx.double().numpy()
+    h064, dhT64 = h0s.double().numpy(), dhTs.double().numpy()
+    y_ref = np.zeros((1, T, W))
+    hT_ref = np.zeros((S, W))
+    dh0_ref = np.zeros((S, W))
+    g_ref = {"dx": np.zeros((1, T, W)), "dWa": 0.0, "dWx": 0.0, "dba": 0.0, "dbx": 0.0,
+             "dLambda": 0.0}
+    for s in range(S):
+        a, b = int(cu[s]), int(cu[s + 1])
+        if a == b:
+            hT_ref[s] = h064[s]
+            dh0_ref[s] = dhT64[s]
+            continue
+        ys, hs = oracle.fused_forward(oracle.CANONICAL, x[:, a:b], Wa, ba64, Wx, bx64, Lam,
+                                      None, None, h064[s:s + 1])
+        g = oracle.fused_backward(oracle.CANONICAL, x[:, a:b], Wa, ba64, Wx, bx64, Lam,
+                                  dy[:, a:b], dhT64[s:s + 1], None, None, h064[s:s + 1])
+        y_ref[:, a:b] = ys
+        hT_ref[s] = hs[0]
+        dh0_ref[s] = g["dh0"][0]
+        g_ref["dx"][:, a:b] = g["dx"]
+        for n in ("dWa", "dWx", "dba", "dbx", "dLambda"):
+            g_ref[n] = g_ref[n] + g[n]
+    assert_close("y", host(y), y_ref, io="bf16", kind="out")
+    assert_close("hT", host(hT), hT_ref, io="bf16", kind="out")
+    assert_close("dx", host(dx), g_ref["dx"], io="bf16", kind="grad", stored=grad)
+    for n, got in (("dWa", dWa), ("dWx", dWx), ("dba", dba), ("dbx", dbx), ("dLambda", dL)):
+        assert_close(n, host(got), g_ref[n], io="bf16", kind="grad")
+    assert_close("dh0", host(dh0), dh0_ref, io="bf16", kind="grad")
