@@ -14,8 +14,8 @@
 //   dlr = dla (-8 softplus) r (1 - r),  dli = g m u (1 - i),  dx_direct = g m i,
 //   dsoftplus = sum dla (-8 r),  dLambda = sigmoid(Lambda) dsoftplus,  dh0 = abar_0 g_0.
 //
-// Tile = (b, blk, 64 tokens), visited in reverse chunk order; four scan threads per channel,
-// one per 16-token part.  Per tile:
+// Tile = (b, blk, 64 tokens), visited in reverse chunk order; two scan threads per channel,
+// one per 32-token part.  Per tile:
 //   1. MMA: lr^T, li^T = W^T x^T into TMEM (as in the forward).
 //   2. Pass 1 (tokens ascending): abar kept in registers, m i and r parked in TMEM over the
 //      logits, i beside them; the part's forward aggregate (state map h -> A h + B) and reverse
@@ -23,8 +23,9 @@
 //      abar_s) dy_t).
 //   3. Parts exchange aggregates through shared memory; part 0 composes the tile's reverse
 //      aggregate, publishes it, and runs the anchored look-back toward larger t (lookback.cuh)
-//      for the carry from the right; the forward entry state comes from the chunk states the
-//      forward saved.
+//      for the carry from the right (its slots requested at the tile's start and again once the
+//      tiles processed alongside have published); the forward entry state comes from the
+//      chunk states the forward saved.
 //   4. Pass 2: h_{t-1} forward through the part, then g exactly in reverse with the pointwise
 //      gradients; dlr, dli go to shared memory as bf16 hi + lo pairs (v = hi + lo to ~2^-16),
 //      the direct dx term into the TMEM dx accumulator.
@@ -34,7 +35,7 @@
 //      and a bf16-rounded dl alone would cost ~2^-9 |dl| in dx.
 //   6. dx TMEM -> bf16/f32 -> smem -> TMA store, done after pass 1 of the next tile, so the
 //      step-5 MMAs run while the scan warps work on that pass.
-// Roles: warp 0 TMA (W once; x + dy tiles, 2 stages), warp 1 MMA, warps 2..17 scan.  CTA
+// Roles: warp 0 TMA (W once; x + dy tiles, 2 stages), warp 1 MMA, warps 2..9 scan.  CTA
 // (blk, r) takes tiles r, r + P, ... of its block, so its partial sums cover a fixed set of
 // tiles: the result is bitwise reproducible.
 #include <cudaTypedefs.h>
@@ -142,7 +143,7 @@ __device__ __forceinline__ void store_dl8(uint8_t* hi_buf, uint8_t* lo_buf, int 
   *reinterpret_cast<uint4*>(lo_buf + at) = lo;
 }
 
-// The passes of a scan thread over its part's 16 tokens do the pointwise work on token pairs
+// The passes of a scan thread over its part's 32 tokens do the pointwise work on token pairs
 // (u, u + 1) in the two lanes of f32x2 operations (adjacent TMEM columns land in adjacent
 // registers) and run the recurrences as scalar chains.  Per-token values parked in TMEM sit at
 // column = token of the part; the thread's columns of each region start at tcol.
@@ -313,13 +314,17 @@ __device__ __forceinline__ void bwd_pass2a(uint32_t tcol, const uint32_t (&xr)[P
 // Pass 2b (tokens descending): g exactly from the carry `cin` entering the part's last token
 // from the right, and the pointwise gradients; dlr, dli go to the dl operand buffers as bf16
 // hi + lo pairs, the direct dx term g m i over h_{t-1} in the dx columns (the accumulator of
-// the dx MMAs).  dsp sums dla r (the softplus gradient is -8 times the total).
+// the dx MMAs).  dsp sums dla r (the softplus gradient is -8 times the total).  The logits
+// columns (COL_LR, COL_LI) are read for the last time by the loads of group 0; once those have
+// landed the warp arrives on lg_free, so the next tile's logits MMAs overlap the rest of the
+// pass.
 template <bool GENERAL, bool VARLEN>
 __device__ __forceinline__ void bwd_pass2b(uint32_t tcol, int tb, int j,
                                            const uint32_t (&xr)[PT / 2], uint32_t dyb, float nk,
                                            int valid, const float2 (&ab)[PT / 2], const SeqB& sq,
-                                           float cin,
+                                           float cin, uint64_t* lg_free,
                                            uint8_t* s_dl, float2& dsp, float2& dba, float2& dbx) {
+  static_assert(PT / GRP >= 2, "the logits columns are released after the second-to-last group");
   float gnext = cin, anext = 1.0f;
   constexpr int G0 = PT / GRP - 1;
   float m4[GRP], r4[GRP], i4[GRP], h4[GRP];
@@ -401,6 +406,11 @@ __device__ __forceinline__ void bwd_pass2b(uint32_t tcol, int tb, int j,
         r4[u] = nr[u];
         i4[u] = ni[u];
         h4[u] = nh[u];
+      }
+      if (g == 1) {  // every read of the logits columns has landed
+        tc::tc_fence_before();
+        __syncwarp();
+        if ((threadIdx.x & 31) == 0) tc::mbar_arrive(lg_free);
       }
     }
   }
@@ -693,6 +703,9 @@ __global__ void __maxnreg__(MAXREG)
       pc = c;
       pb = b;
       cur.next();
+      // The tiles processed alongside this one have published their aggregates by about now:
+      // ask again for the slots that were empty at the tile's start.
+      if (part == 0) lookback_refresh(lbq, lb_agg, (long)p.W, lb_n, lb_anchor);
 
       // Entry-state map of this part (earlier parts composed) and carry map from the tile's
       // right edge to this part (later parts composed).
@@ -744,14 +757,15 @@ __global__ void __maxnreg__(MAXREG)
       if (it > 0) ctl.wait(dl_empty, (it - 1) & 1);
       tc::tc_fence_after();
       if (fast)
-        bwd_pass2b<false, VARLEN>(tcol, tb, j, xr, dyb, gk.nk, PT, ab, sq, cin, s_dl, dsp, dba, dbx);
+        bwd_pass2b<false, VARLEN>(tcol, tb, j, xr, dyb, gk.nk, PT, ab, sq, cin, lg_empty, s_dl, dsp,
+                                  dba, dbx);
       else
-        bwd_pass2b<true, VARLEN>(tcol, tb, j, xr, dyb, gk.nk, valid, ab, sq, cin, s_dl, dsp, dba, dbx);
+        bwd_pass2b<true, VARLEN>(tcol, tb, j, xr, dyb, gk.nk, valid, ab, sq, cin, lg_empty, s_dl,
+                                 dsp, dba, dbx);
       tc::fence_proxy_async_smem();
       tc::tc_fence_before();
       __syncwarp();
       if (lane == 0) {
-        tc::mbar_arrive(lg_empty);  // the logits columns are free for the next tile
         tc::mbar_arrive(&in_empty[st]);
         tc::mbar_arrive(dl_full);
       }

@@ -46,6 +46,18 @@ __device__ __forceinline__ void lookback_issue(LookbackReq& q, const float2* fir
   q.hv = anchor_state ? ld_relaxed_u32(anchor_state) : slot_enc1(init);
 }
 
+// Re-requests every slot that was still empty when it was last read, and returns at once: a
+// caller that knows when the missing aggregates are likely to have been published (the tiles
+// processed alongside its own publish theirs at about the same point of their loop) requests
+// them again there, so that the round trip overlaps its work before lookback_finish.
+__device__ __forceinline__ void lookback_refresh(LookbackReq& q, const float2* first_agg,
+                                                 long agg_step, int n, const float* anchor_state) {
+#pragma unroll
+  for (int s = 0; s < LB_SLOTS; ++s)
+    if (s < n && q.v[s] == SLOT_EMPTY64) q.v[s] = ld_relaxed_u64(first_agg + s * agg_step);
+  if (anchor_state != nullptr && q.hv == SLOT_EMPTY32) q.hv = ld_relaxed_u32(anchor_state);
+}
+
 // A slot that stays empty past `limit` polls counts as the identity (or a zero carry), and the
 // timeout is recorded in *status.  Every slot still empty is re-requested in the same round,
 // so a round costs one L2 round trip however many slots were late.
