@@ -134,6 +134,14 @@ def algorithmic_bytes(wl):
     return fwd, bwd
 
 
+def tensor_flops(wl):
+    """Tensor-core FLOPs of one fused backward.  Algorithmic (the method's contractions): the
+    logits recompute (2 x 2Nk), dx += dl W^T (2 x 2Nk) and dW = x^T dl (2 x 2Nk), 12 N k.
+    Executed: the dx and dW products also take the bf16 low halves of dl, 20 N k."""
+    N = wl.B * wl.T * wl.W
+    return 12 * N * wl.k, 20 * N * wl.k
+
+
 def measured_peaks():
     try:
         return json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
@@ -247,6 +255,11 @@ def run_ours(args, rank, world, local):
     kern_ms = [e[0].elapsed_time(e[1]) for e in kev]
     kern_mean = statistics.fmean(kern_ms)
     achieved = bwd_b / (kern_mean / 1e3) / 1e9
+    flop_alg, flop_exec = tensor_flops(wl)
+    tpeak = peaks.get("bf16_tflops")
+    t_hbm_us = bwd_b / (peak * 1e9) * 1e6 if peak else None
+    t_tc_us = flop_alg / (tpeak * 1e12) * 1e6 if tpeak else None
+    combined_us = max(t_hbm_us, t_tc_us) if (t_hbm_us and t_tc_us) else None
     step_ms = total_ms / args.steps
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -268,7 +281,19 @@ def run_ours(args, rank, world, local):
                      "frac": (achieved / peak) if peak else None,
                      "peak_source": "measured (hbm_gbs)",
                      "algorithmic_bytes": bwd_b, "traffic": TRAFFIC_BYTES,
-                     "kernel_ms_mean": kern_mean},
+                     "kernel_ms_mean": kern_mean,
+                     # context bound: the same kernel against the tensor pipe, and the larger
+                     # of the two bounds (bytes / measured copy bandwidth, flops / measured
+                     # bf16 burst) against its duration
+                     "tensor": {"algorithmic_flop": flop_alg, "executed_flop": flop_exec,
+                                "achieved_tflops": flop_alg / (kern_mean / 1e3) / 1e12,
+                                "peak_tflops": tpeak,
+                                "frac": (flop_alg / (kern_mean / 1e3) / 1e12 / tpeak)
+                                if tpeak else None,
+                                "peak_source": "measured (bf16_tflops, burst)"},
+                     "combined_bound_us": combined_us,
+                     "frac_of_combined": (combined_us / (kern_mean * 1e3))
+                     if combined_us else None},
         "e2e": {"value": tokens * world * args.steps / (e2e_ms / 1e3), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": launches,

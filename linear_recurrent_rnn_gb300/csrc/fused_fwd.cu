@@ -124,12 +124,20 @@ __device__ __forceinline__ void local_scan(uint32_t t_lr, uint32_t t_li, uint32_
                                            float& rh, float& rA) {
   rh = 0.0f;
   rA = 1.0f;
+  // the logits of group g + 1 are requested before group g is computed
+  float vr[GRP], vi[GRP];
+  tc::tmem_ld8(t_lr, vr);
+  tc::tmem_ld8(t_li, vi);
+  tc::tmem_ld_wait();
+  tc::reg_fence(vr);
+  tc::reg_fence(vi);
 #pragma unroll
   for (int g = 0; g < PT / GRP; ++g) {
-    float vr[GRP], vi[GRP], oh[GRP], oa[GRP];
-    tc::tmem_ld8(t_lr + g * GRP, vr);
-    tc::tmem_ld8(t_li + g * GRP, vi);
-    tc::tmem_ld_wait();
+    float oh[GRP], oa[GRP], nr[GRP], ni[GRP];
+    if (g + 1 < PT / GRP) {
+      tc::tmem_ld8(t_lr + (g + 1) * GRP, nr);
+      tc::tmem_ld8(t_li + (g + 1) * GRP, ni);
+    }
 #pragma unroll
     for (int q = 0; q < GRP / 2; ++q) {
       const int u = g * GRP + 2 * q;  // tokens u, u + 1 of the part
@@ -181,6 +189,16 @@ __device__ __forceinline__ void local_scan(uint32_t t_lr, uint32_t t_li, uint32_
     }
     tc::tmem_st8(t_lr + g * GRP, oh);
     tc::tmem_st8(t_li + g * GRP, oa);
+    if (g + 1 < PT / GRP) {
+      tc::tmem_ld_wait();
+      tc::reg_fence(nr);
+      tc::reg_fence(ni);
+#pragma unroll
+      for (int u = 0; u < GRP; ++u) {
+        vr[u] = nr[u];
+        vi[u] = ni[u];
+      }
+    }
   }
   tc::tmem_st_wait();
 }
