@@ -1,0 +1,661 @@
+// Gated delta rule (GDN: one decay per value head and token; KDA: one per key channel) on the
+// CUDA cores of one GB300, forward and backward.
+//
+// Source ("linear_attention.reference" page, the recurrent reference's entry): the exact token
+// recurrence with scalar or per-key decay given as natural logarithms, grouped key heads,
+// initial and final states, packed sequences.  Per sequence and value head (key head
+// h / (Hv / Hk)), token t, S the [Dk, Dv] state:
+//   S' = D_t S (D_t = exp(g_t), or diag(exp(g_t)) per key),  u = beta_t (v_t - S'^T k_t),
+//   S = S' + k_t u^T,  o_t = scale S^T q_t.
+//
+// Geometry: the state lives in registers.  A thread owns 32 keys of one value column, so a
+// column is shared by KG = Dk / 32 adjacent lanes (lane = column-in-warp * KG + key group) and
+// S'^T k, S^T q are a 32-term dot product per thread plus log2(KG) shuffles.  Token data (k, q,
+// decays, beta, v) is staged in shared memory as float32 a block of tokens at a time and read
+// by every thread as broadcast 16-byte loads.
+//   forward:  CTA = (sequence, value head, slice of 4 x 32 / KG columns), 4 warps; the state
+//             entering every 16-token block is saved (float32, [slot][Hv][Dv][Dk]) for the
+//             backward.
+//   backward: CTA = (sequence, value head), all Dv columns; per 16-token block in reverse it
+//             restores the block's entry state, runs the block forward again keeping each
+//             token's state in thread-local memory, and then runs the reverse recurrence.  The
+//             sums over value columns (dq, dk, KDA's dg) fold the warp's columns with a
+//             halving butterfly of shuffles and the warps through shared memory.
+#include <algorithm>
+
+#include "common.cuh"
+#include "internal.h"
+#include "delta_rule.h"
+
+namespace rglru {
+
+namespace {
+
+constexpr int DR_TB = 16;                 // tokens per staged block = tokens per saved state
+constexpr unsigned FULL = 0xffffffffu;
+
+struct DrArgs {
+  int B, T, Hk, Hv, Dk, Dv, kda, vfirst, N, nslices;
+  float scale;
+  const void* q;
+  const void* k;
+  const void* v;
+  const float* g;
+  const float* beta;
+  const int32_t* cu;
+  const float* h0;
+  void* o;
+  float* hT;
+  float* saved;  // [slot][Hv][Dv][Dk]
+  // backward
+  const void* dout;
+  const float* dhT;
+  float* dq;      // [B*T][Hk][Dk], or per value head [B*T][Hv][Dk] when Hv > Hk
+  float* dk;
+  float* dv;
+  float* dg;
+  float* dbeta;
+  float* dh0;
+};
+
+// Sequence n: its batch row, first token within the row, length, and first saved-state slot.
+// Slots are laid out so that sequences never share one: floor(flat start / 16) + 2 n.
+struct Seq {
+  int b, s, len;
+  long slot0;
+};
+__device__ __forceinline__ Seq seq_of(const DrArgs& a, int n) {
+  Seq q;
+  if (a.cu) {
+    q.b = 0;
+    q.s = a.cu[n];
+    const int e = a.cu[n + 1];
+    q.len = max(0, min(e, a.T) - q.s);
+    q.s = min(max(q.s, 0), a.T);
+  } else {
+    q.b = n;
+    q.s = 0;
+    q.len = a.T;
+  }
+  q.slot0 = ((long)q.b * a.T + q.s) / DR_TB + 2L * n;
+  return q;
+}
+
+template <typename T>
+__device__ __forceinline__ float ldf(const void* p, size_t i) {
+  return to_f32<T>(static_cast<const T*>(p)[i]);
+}
+
+// The token-major staging of one block: k, q [TB][DK]; KDA decays and decays * k [TB][DK];
+// GDN decays, beta [TB]; the CTA's value columns of v (and of do) [TB][NC].
+template <typename T, int DK>
+__device__ void stage_block(const DrArgs& a, const Seq& sq, int hv, int t0, int nt, int c0,
+                            int NC, float* s_k, float* s_q, float* s_a, float* s_ak, float* s_v,
+                            float* s_do, float* s_b, float* s_ag) {
+  const int hk = hv / (a.Hv / a.Hk);
+  for (int e = threadIdx.x; e < DR_TB * DK; e += blockDim.x) {
+    const int tt = e / DK, i = e % DK;
+    float kv = 0.0f, qv = 0.0f, av = 1.0f;
+    if (tt < nt) {
+      const size_t row = (size_t)sq.b * a.T + sq.s + t0 + tt;
+      kv = ldf<T>(a.k, (row * a.Hk + hk) * DK + i);
+      qv = ldf<T>(a.q, (row * a.Hk + hk) * DK + i);
+      if (a.kda) av = expf(a.g[(row * a.Hv + hv) * DK + i]);
+    }
+    s_k[e] = kv;
+    s_q[e] = qv;
+    if (a.kda) {
+      s_a[e] = av;
+      s_ak[e] = av * kv;
+    }
+  }
+  for (int e = threadIdx.x; e < DR_TB * NC; e += blockDim.x) {
+    const int tt = e / NC, jc = e % NC, j = c0 + jc;
+    float vv = 0.0f, dv = 0.0f;
+    if (tt < nt && j < a.Dv) {
+      const size_t row = (size_t)sq.b * a.T + sq.s + t0 + tt;
+      vv = ldf<T>(a.v, (row * a.Hv + hv) * a.Dv + j);
+      if (s_do) dv = ldf<T>(a.dout, (row * a.Hv + hv) * a.Dv + j);
+    }
+    s_v[e] = vv;
+    if (s_do) s_do[e] = dv;
+  }
+  if (threadIdx.x < DR_TB) {
+    const int tt = threadIdx.x;
+    float bv = 0.0f, ag = 1.0f;
+    if (tt < nt) {
+      const size_t row = (size_t)sq.b * a.T + sq.s + t0 + tt;
+      bv = a.beta[row * a.Hv + hv];
+      if (!a.kda) ag = expf(a.g[row * a.Hv + hv]);
+    }
+    s_b[tt] = bv;
+    s_ag[tt] = ag;
+  }
+}
+
+// 32 consecutive floats of a staged row (16-byte aligned) into registers.
+__device__ __forceinline__ void ld32(const float* p, float (&r)[32]) {
+#pragma unroll
+  for (int x = 0; x < 8; ++x) {
+    const float4 v = reinterpret_cast<const float4*>(p)[x];
+    r[4 * x] = v.x, r[4 * x + 1] = v.y, r[4 * x + 2] = v.z, r[4 * x + 3] = v.w;
+  }
+}
+
+// Sum over the KG lanes that share a column.
+template <int KG>
+__device__ __forceinline__ float kg_sum(float x) {
+  if (KG >= 2) x += __shfl_xor_sync(FULL, x, 1);
+  if (KG >= 4) x += __shfl_xor_sync(FULL, x, 2);
+  return x;
+}
+
+// One token of the forward on a thread's 32 keys: S' = D S, w = S'^T k, u = beta (v - w),
+// S = S' + k u; returns w and u (the column's, identical on its KG lanes).
+template <int KG>
+__device__ __forceinline__ void fwd_token(float (&S)[32], const float* kr, const float* ar,
+                                          const float* akr, bool kda, float ag, float bt,
+                                          float vj, float& w, float& u) {
+  float kk[32];
+  ld32(kr, kk);
+  float part = 0.0f;
+  if (kda) {
+    float ak[32];
+    ld32(akr, ak);
+#pragma unroll
+    for (int x = 0; x < 32; ++x) part = fmaf(S[x], ak[x], part);
+    w = kg_sum<KG>(part);
+    u = bt * (vj - w);
+    float al[32];
+    ld32(ar, al);
+#pragma unroll
+    for (int x = 0; x < 32; ++x) S[x] = fmaf(al[x], S[x], kk[x] * u);
+  } else {
+#pragma unroll
+    for (int x = 0; x < 32; ++x) part = fmaf(S[x], kk[x], part);
+    w = ag * kg_sum<KG>(part);
+    u = bt * (vj - w);
+#pragma unroll
+    for (int x = 0; x < 32; ++x) S[x] = fmaf(ag, S[x], kk[x] * u);
+  }
+}
+
+template <typename T, int KG>
+__global__ void __launch_bounds__(128) k_dr_fwd(DrArgs a) {
+  constexpr int DK = 32 * KG, CPW = 32 / KG, NC = 4 * CPW;
+  extern __shared__ __align__(16) float sm[];
+  float* s_k = sm;
+  float* s_q = s_k + DR_TB * DK;
+  float* s_a = s_q + DR_TB * DK;
+  float* s_ak = s_a + DR_TB * DK;
+  float* s_v = s_ak + DR_TB * DK;
+  float* s_b = s_v + DR_TB * NC;
+  float* s_ag = s_b + DR_TB;
+  const int slice = blockIdx.x % a.nslices;
+  const int hv = (blockIdx.x / a.nslices) % a.Hv;
+  const int n = blockIdx.x / (a.nslices * a.Hv);
+  const Seq sq = seq_of(a, n);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int kg = lane % KG, jc = warp * CPW + lane / KG;
+  const int c0 = slice * NC, j = c0 + jc;
+  const bool live = j < a.Dv;
+  const int key0 = kg * 32;
+
+  float S[32];
+#pragma unroll
+  for (int x = 0; x < 32; ++x) S[x] = 0.0f;
+  if (a.h0 && live) {
+    const size_t base = (size_t)n * a.Hv + hv;
+#pragma unroll
+    for (int x = 0; x < 32; ++x)
+      S[x] = a.vfirst ? a.h0[(base * a.Dv + j) * DK + key0 + x]
+                      : a.h0[(base * DK + key0 + x) * a.Dv + j];
+  }
+  for (int t0 = 0; t0 < sq.len; t0 += DR_TB) {
+    const int nt = min(DR_TB, sq.len - t0);
+    __syncthreads();  // the previous block's staging is consumed
+    stage_block<T, DK>(a, sq, hv, t0, nt, c0, NC, s_k, s_q, s_a, s_ak, s_v, nullptr, s_b, s_ag);
+    __syncthreads();
+    if (a.saved && live) {  // the state entering the block
+      float* dst = a.saved + (((size_t)(sq.slot0 + t0 / DR_TB) * a.Hv + hv) * a.Dv + j) * DK + key0;
+#pragma unroll
+      for (int x = 0; x < 8; ++x)
+        reinterpret_cast<float4*>(dst)[x] = make_float4(S[4 * x], S[4 * x + 1], S[4 * x + 2], S[4 * x + 3]);
+    }
+    for (int tt = 0; tt < nt; ++tt) {
+      float w, u;
+      fwd_token<KG>(S, s_k + tt * DK + key0, s_a + tt * DK + key0, s_ak + tt * DK + key0,
+                    a.kda != 0, s_ag[tt], s_b[tt], s_v[tt * NC + jc], w, u);
+      float qq[32];
+      ld32(s_q + tt * DK + key0, qq);
+      float part = 0.0f;
+#pragma unroll
+      for (int x = 0; x < 32; ++x) part = fmaf(S[x], qq[x], part);
+      const float ov = a.scale * kg_sum<KG>(part);
+      if (kg == 0 && live) {
+        const size_t row = (size_t)sq.b * a.T + sq.s + t0 + tt;
+        static_cast<T*>(a.o)[(row * a.Hv + hv) * a.Dv + j] = from_f32<T>(ov);
+      }
+    }
+  }
+  if (a.hT && live) {
+    const size_t base = (size_t)n * a.Hv + hv;
+#pragma unroll
+    for (int x = 0; x < 32; ++x) {
+      if (a.vfirst)
+        a.hT[(base * a.Dv + j) * DK + key0 + x] = S[x];
+      else
+        a.hT[(base * DK + key0 + x) * a.Dv + j] = S[x];
+    }
+  }
+}
+
+size_t fwd_smem(int KG) {
+  const int DK = 32 * KG, NC = 4 * (32 / KG);
+  return (size_t)(4 * DR_TB * DK + DR_TB * NC + 2 * DR_TB) * sizeof(float);
+}
+
+// Sums 32 per-key values over the CPW columns of the warp with a halving butterfly: at level L
+// the lanes that differ in lane bit KG << L swap halves, so after log2(CPW) levels each lane
+// holds KG sums, of keys key0 + fold_key(lane) + x (x < KG).
+template <int KG, int L>
+__device__ __forceinline__ void fold(float (&v)[32], int lane) {
+  constexpr int M = KG << L, H = 16 >> L;
+  if constexpr (M < 32) {
+    const bool hi = (lane & M) != 0;
+#pragma unroll
+    for (int x = 0; x < H; ++x) {
+      const float send = hi ? v[x] : v[x + H];
+      const float keep = hi ? v[x + H] : v[x];
+      v[x] = keep + __shfl_xor_sync(FULL, send, M);
+    }
+    fold<KG, L + 1>(v, lane);
+  }
+}
+template <int KG>
+__device__ __forceinline__ int fold_key(int lane) {
+  int off = 0;
+#pragma unroll
+  for (int L = 0; (KG << L) < 32; ++L)
+    if (lane & (KG << L)) off += 16 >> L;
+  return off;
+}
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+  for (int m = 16; m > 0; m >>= 1) x += __shfl_xor_sync(FULL, x, m);
+  return x;
+}
+
+// Backward.  CTA = (sequence n, value head hv), blockDim = 32 x ceil(Dv / CPW).  Per 16-token
+// block, last block first: restore the block's entry state from `saved`, run the block forward
+// keeping every token's state before its decay (thread-local), w and u; then for each token in
+// reverse (dS the gradient of the state after the token):
+//   dS += scale q do^T;  dq = scale (S' + k u^T) do;  du = dS^T k;  dw = -beta du
+//   dk = dS u + S' dw;  dbeta = du . (v - w);  dv = beta du;  dS' = dS + k dw^T
+//   dg = <dS', S'> (GDN) or its row sums (KDA);  dS = D dS'
+// dq, dk (and KDA's dg) sum over the columns: warp butterfly, then the warps through shared
+// memory (double-buffered, one barrier per token).
+template <typename T, int KG>
+__global__ void __launch_bounds__(512, 1) k_dr_bwd(DrArgs a) {
+  constexpr int DK = 32 * KG, CPW = 32 / KG;
+  const int nwarps = blockDim.x >> 5, NC = nwarps * CPW;
+  const int NV = a.kda ? 3 : 2;      // per-key vectors reduced per token: dq, dk (, dg)
+  const int RS = NV * DK + 2;        // a warp's reduction row: vectors, dbeta, GDN dg
+  extern __shared__ __align__(16) float sm[];
+  float* s_k = sm;
+  float* s_q = s_k + DR_TB * DK;
+  float* s_a = s_q + DR_TB * DK;
+  float* s_ak = s_a + DR_TB * DK;
+  float* s_v = s_ak + DR_TB * DK;
+  float* s_do = s_v + DR_TB * NC;
+  float* s_b = s_do + DR_TB * NC;
+  float* s_ag = s_b + DR_TB;
+  float* s_red = s_ag + DR_TB;       // [2][nwarps][RS]
+  const int hv = blockIdx.x % a.Hv, n = blockIdx.x / a.Hv;
+  const int hk = hv / (a.Hv / a.Hk);
+  const Seq sq = seq_of(a, n);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int kg = lane % KG, jc = warp * CPW + lane / KG, j = jc;
+  const bool live = j < a.Dv;
+  const int key0 = kg * 32, kf = key0 + fold_key<KG>(lane);
+  const size_t hbase = (size_t)n * a.Hv + hv;
+  const bool per_vhead = a.Hv != a.Hk;  // dq, dk per value head, summed by a second kernel
+
+  float dS[32];
+#pragma unroll
+  for (int x = 0; x < 32; ++x) dS[x] = 0.0f;
+  if (a.dhT && live) {
+#pragma unroll
+    for (int x = 0; x < 32; ++x)
+      dS[x] = a.vfirst ? a.dhT[(hbase * a.Dv + j) * DK + key0 + x]
+                       : a.dhT[(hbase * DK + key0 + x) * a.Dv + j];
+  }
+  float hist[DR_TB][32];
+  float wh[DR_TB], uh[DR_TB];
+  const int nblk = (sq.len + DR_TB - 1) / DR_TB;
+  for (int blk = nblk - 1; blk >= 0; --blk) {
+    const int t0 = blk * DR_TB, nt = min(DR_TB, sq.len - t0);
+    __syncthreads();
+    stage_block<T, DK>(a, sq, hv, t0, nt, 0, NC, s_k, s_q, s_a, s_ak, s_v, s_do, s_b, s_ag);
+    __syncthreads();
+    float S[32];
+    if (live) {
+      const float* src = a.saved + (((size_t)(sq.slot0 + blk) * a.Hv + hv) * a.Dv + j) * DK + key0;
+#pragma unroll
+      for (int x = 0; x < 8; ++x) {
+        const float4 v = reinterpret_cast<const float4*>(src)[x];
+        S[4 * x] = v.x, S[4 * x + 1] = v.y, S[4 * x + 2] = v.z, S[4 * x + 3] = v.w;
+      }
+    } else {
+#pragma unroll
+      for (int x = 0; x < 32; ++x) S[x] = 0.0f;
+    }
+    for (int tt = 0; tt < nt; ++tt) {
+#pragma unroll
+      for (int x = 0; x < 32; ++x) hist[tt][x] = S[x];
+      fwd_token<KG>(S, s_k + tt * DK + key0, s_a + tt * DK + key0, s_ak + tt * DK + key0,
+                    a.kda != 0, s_ag[tt], s_b[tt], s_v[tt * NC + jc], wh[tt], uh[tt]);
+    }
+    for (int tt = nt - 1; tt >= 0; --tt) {
+      const float ag = s_ag[tt], bt = s_b[tt], u = uh[tt], w = wh[tt];
+      const float doj = s_do[tt * NC + jc], vj = s_v[tt * NC + jc];
+      const float* kr = s_k + tt * DK + key0;
+      const float* ar = s_a + tt * DK + key0;
+      float Sp[32], vec[32];
+#pragma unroll
+      for (int x = 0; x < 32; ++x) Sp[x] = hist[tt][x];
+      if (a.kda) {
+        float al[32];
+        ld32(ar, al);
+#pragma unroll
+        for (int x = 0; x < 32; ++x) Sp[x] *= al[x];
+      } else {
+#pragma unroll
+        for (int x = 0; x < 32; ++x) Sp[x] *= ag;
+      }
+      // dS += scale q do;  dq = scale (S' + k u) do
+      {
+        float qq[32], kk[32];
+        ld32(s_q + tt * DK + key0, qq);
+        ld32(kr, kk);
+        const float sd = a.scale * doj;
+#pragma unroll
+        for (int x = 0; x < 32; ++x) {
+          dS[x] = fmaf(qq[x], sd, dS[x]);
+          vec[x] = fmaf(kk[x], u, Sp[x]) * sd;
+        }
+      }
+      const int buf = tt & 1;
+      float* red = s_red + ((size_t)buf * nwarps + warp) * RS;
+      fold<KG, 0>(vec, lane);
+#pragma unroll
+      for (int x = 0; x < KG; ++x) red[kf + x] = vec[x];
+      // du = dS^T k;  dk = dS u + S' dw;  dS' = dS + k dw
+      float du, dw;
+      {
+        float kk[32];
+        ld32(kr, kk);
+        float part = 0.0f;
+#pragma unroll
+        for (int x = 0; x < 32; ++x) part = fmaf(dS[x], kk[x], part);
+        du = kg_sum<KG>(part);
+        dw = -bt * du;
+#pragma unroll
+        for (int x = 0; x < 32; ++x) {
+          vec[x] = fmaf(dS[x], u, Sp[x] * dw);
+          dS[x] = fmaf(kk[x], dw, dS[x]);
+        }
+      }
+      fold<KG, 0>(vec, lane);
+#pragma unroll
+      for (int x = 0; x < KG; ++x) red[DK + kf + x] = vec[x];
+      // dg from dS' and S', then dS = D dS'
+      float gpart = 0.0f;
+      if (a.kda) {
+        float al[32];
+        ld32(ar, al);
+#pragma unroll
+        for (int x = 0; x < 32; ++x) {
+          vec[x] = dS[x] * Sp[x];
+          dS[x] *= al[x];
+        }
+        fold<KG, 0>(vec, lane);
+#pragma unroll
+        for (int x = 0; x < KG; ++x) red[2 * DK + kf + x] = vec[x];
+      } else {
+#pragma unroll
+        for (int x = 0; x < 32; ++x) {
+          gpart = fmaf(dS[x], Sp[x], gpart);
+          dS[x] *= ag;
+        }
+      }
+      const float bpart = (kg == 0 && live) ? du * (vj - w) : 0.0f;
+      const float bsum = warp_sum(bpart), gsum = warp_sum(live ? gpart : 0.0f);
+      if (lane == 0) {
+        red[NV * DK] = bsum;
+        red[NV * DK + 1] = gsum;
+      }
+      const size_t row = (size_t)sq.b * a.T + sq.s + t0 + tt;
+      if (kg == 0 && live) a.dv[(row * a.Hv + hv) * a.Dv + j] = bt * du;
+      __syncthreads();
+      const float* rb = s_red + (size_t)buf * nwarps * RS;
+      for (int e = threadIdx.x; e < NV * DK + 1; e += blockDim.x) {
+        float s = 0.0f;
+        if (e < NV * DK) {
+          for (int ww = 0; ww < nwarps; ++ww) s += rb[ww * RS + e];
+          const int vsel = e / DK, i = e % DK;
+          if (vsel == 0 || vsel == 1) {
+            float* dst = vsel == 0 ? a.dq : a.dk;
+            const size_t o = per_vhead ? (row * a.Hv + hv) * DK + i : (row * a.Hk + hk) * DK + i;
+            dst[o] = s;
+          } else {
+            a.dg[(row * a.Hv + hv) * DK + i] = s;
+          }
+        } else {
+          float sb = 0.0f, sg = 0.0f;
+          for (int ww = 0; ww < nwarps; ++ww) {
+            sb += rb[ww * RS + NV * DK];
+            sg += rb[ww * RS + NV * DK + 1];
+          }
+          a.dbeta[row * a.Hv + hv] = sb;
+          if (!a.kda) a.dg[row * a.Hv + hv] = sg;
+        }
+      }
+    }
+  }
+  if (a.dh0 && live) {
+#pragma unroll
+    for (int x = 0; x < 32; ++x) {
+      if (a.vfirst)
+        a.dh0[(hbase * a.Dv + j) * DK + key0 + x] = dS[x];
+      else
+        a.dh0[(hbase * DK + key0 + x) * a.Dv + j] = dS[x];
+    }
+  }
+}
+
+// dq, dk of a key head: the sum over its Hv / Hk value heads (per-value-head values in ws).
+__global__ void k_dr_group_sum(const float* ws, float* out, size_t rows, int Hk, int grp, int Dk) {
+  const size_t total = rows * Hk * Dk;
+  for (size_t e = blockIdx.x * (size_t)blockDim.x + threadIdx.x; e < total;
+       e += (size_t)gridDim.x * blockDim.x) {
+    const int i = (int)(e % Dk);
+    const size_t rh = e / Dk;
+    const int h = (int)(rh % Hk);
+    const size_t row = rh / Hk;
+    float s = 0.0f;
+    for (int r = 0; r < grp; ++r) s += ws[((row * Hk + h) * grp + r) * Dk + i];
+    out[e] = s;
+  }
+}
+
+size_t bwd_smem(int KG, int nwarps, int kda) {
+  const int DK = 32 * KG, NC = nwarps * (32 / KG);
+  const int RS = (kda ? 3 : 2) * DK + 2;
+  return (size_t)(4 * DR_TB * DK + 2 * DR_TB * NC + 2 * DR_TB + 2 * nwarps * RS) * sizeof(float);
+}
+
+}  // namespace
+
+// ------------------------------------------------------------------ host side
+
+namespace {
+
+bool dr_dims_ok(const delta_shape* s) {
+  return s && s->B >= 1 && s->T >= 1 && s->Hk >= 1 && s->Hv >= 1 && s->Hv % s->Hk == 0 &&
+         (s->io == RGLRU_F32 || s->io == RGLRU_BF16);
+}
+bool dr_supported(const delta_shape* s) {
+  return (s->Dk == 32 || s->Dk == 64 || s->Dk == 128) && s->Dv >= 1 && s->Dv <= 128;
+}
+long dr_slots(const delta_shape* s, int N) { return (long)s->B * s->T / DR_TB + 2L * N + 1; }
+
+DrArgs dr_args(const delta_shape* s, int N, float scale, const void* q, const void* k,
+               const void* v, const float* g, const float* beta, const int32_t* cu,
+               const float* h0) {
+  DrArgs a{};
+  a.B = s->B;
+  a.T = s->T;
+  a.Hk = s->Hk;
+  a.Hv = s->Hv;
+  a.Dk = s->Dk;
+  a.Dv = s->Dv;
+  a.kda = s->kda ? 1 : 0;
+  a.vfirst = s->state_v_first ? 1 : 0;
+  a.N = N;
+  a.scale = scale;
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.g = g;
+  a.beta = beta;
+  a.cu = cu;
+  a.h0 = h0;
+  return a;
+}
+
+template <typename T, int KG>
+cudaError_t launch_fwd_t(DrArgs& a, cudaStream_t st) {
+  const int NC = 4 * (32 / KG);
+  a.nslices = (a.Dv + NC - 1) / NC;
+  const size_t smem = fwd_smem(KG);
+  cudaError_t e = cudaFuncSetAttribute(k_dr_fwd<T, KG>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  const long grid = (long)a.N * a.Hv * a.nslices;
+  if (grid < 1) return cudaSuccess;
+  k_dr_fwd<T, KG><<<(unsigned)grid, 128, smem, st>>>(a);
+  note_launches(1);
+  return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t launch_fwd_io(DrArgs& a, cudaStream_t st) {
+  switch (a.Dk) {
+    case 32: return launch_fwd_t<T, 1>(a, st);
+    case 64: return launch_fwd_t<T, 2>(a, st);
+    default: return launch_fwd_t<T, 4>(a, st);
+  }
+}
+
+template <typename T, int KG>
+cudaError_t launch_bwd_t(DrArgs& a, float* ws, cudaStream_t st) {
+  const int CPW = 32 / KG;
+  const int nwarps = (a.Dv + CPW - 1) / CPW;
+  const size_t smem = bwd_smem(KG, nwarps, a.kda);
+  cudaError_t e = cudaFuncSetAttribute(k_dr_bwd<T, KG>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  float* dq = a.dq;
+  float* dk = a.dk;
+  const size_t rows = (size_t)a.B * a.T;
+  const size_t per = rows * a.Hv * a.Dk;
+  if (a.Hv != a.Hk) {  // per value head first, then the group sums
+    a.dq = ws;
+    a.dk = ws + per;
+  }
+  k_dr_bwd<T, KG><<<(unsigned)((long)a.N * a.Hv), nwarps * 32, smem, st>>>(a);
+  note_launches(1);
+  e = cudaGetLastError();
+  if (e != cudaSuccess || a.Hv == a.Hk) return e;
+  const size_t total = rows * a.Hk * a.Dk;
+  const unsigned blocks = (unsigned)std::min<size_t>((total + 255) / 256, 4096);
+  k_dr_group_sum<<<blocks, 256, 0, st>>>(ws, dq, rows, a.Hk, a.Hv / a.Hk, a.Dk);
+  k_dr_group_sum<<<blocks, 256, 0, st>>>(ws + per, dk, rows, a.Hk, a.Hv / a.Hk, a.Dk);
+  note_launches(2);
+  return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t launch_bwd_io(DrArgs& a, float* ws, cudaStream_t st) {
+  switch (a.Dk) {
+    case 32: return launch_bwd_t<T, 1>(a, ws, st);
+    case 64: return launch_bwd_t<T, 2>(a, ws, st);
+    default: return launch_bwd_t<T, 4>(a, ws, st);
+  }
+}
+
+}  // namespace
+
+}  // namespace rglru
+
+using namespace rglru;
+
+extern "C" size_t delta_rule_saved_bytes(const delta_shape* s, int32_t num_seqs) {
+  if (!dr_dims_ok(s) || !dr_supported(s) || num_seqs < 1) return 0;
+  return (size_t)dr_slots(s, num_seqs) * s->Hv * s->Dk * s->Dv * sizeof(float);
+}
+
+extern "C" rglru_status delta_rule_forward(const delta_shape* s, const void* q, const void* k,
+                                           const void* v, const float* g, const float* beta,
+                                           float scale, const int32_t* cu, int32_t num_seqs,
+                                           const float* h0, void* o, float* hT, void* saved,
+                                           rglru_stream stream) {
+  if (!dr_dims_ok(s) || num_seqs < 1) return RGLRU_ERR_INVALID_ARG;
+  if (cu ? (s->B != 1 || !req(cu)) : num_seqs != s->B) return RGLRU_ERR_INVALID_ARG;
+  if (!req(q) || !req(k) || !req(v) || !req(g) || !req(beta) || !opt(h0) || !req(o) ||
+      !opt(hT) || !opt(saved))
+    return RGLRU_ERR_INVALID_ARG;
+  if (!dr_supported(s)) return RGLRU_ERR_UNSUPPORTED;
+  DrArgs a = dr_args(s, num_seqs, scale, q, k, v, g, beta, cu, h0);
+  a.o = o;
+  a.hT = hT;
+  a.saved = static_cast<float*>(saved);
+  const cudaError_t e = s->io == RGLRU_BF16 ? launch_fwd_io<bf16>(a, stream) : launch_fwd_io<float>(a, stream);
+  return cuda_status(e);
+}
+
+extern "C" size_t delta_rule_workspace_bytes(const delta_shape* s) {
+  if (!dr_dims_ok(s) || !dr_supported(s) || s->Hv == s->Hk) return 0;
+  return 2 * (size_t)s->B * s->T * s->Hv * s->Dk * sizeof(float);
+}
+
+extern "C" rglru_status delta_rule_backward(const delta_shape* s, const void* q, const void* k,
+                                            const void* v, const float* g, const float* beta,
+                                            float scale, const int32_t* cu, int32_t num_seqs,
+                                            const float* h0, const void* saved, const void* dout,
+                                            const float* dhT, float* dq, float* dk, float* dv,
+                                            float* dg, float* dbeta, float* dh0, void* workspace,
+                                            rglru_stream stream) {
+  (void)h0;  // the block states saved by the forward already include the initial states
+  if (!dr_dims_ok(s) || num_seqs < 1) return RGLRU_ERR_INVALID_ARG;
+  if (cu ? (s->B != 1 || !req(cu)) : num_seqs != s->B) return RGLRU_ERR_INVALID_ARG;
+  if (!req(q) || !req(k) || !req(v) || !req(g) || !req(beta) || !opt(h0) || !req(saved) ||
+      !req(dout) || !opt(dhT) || !req(dq) || !req(dk) || !req(dv) || !req(dg) || !req(dbeta) ||
+      !opt(dh0))
+    return RGLRU_ERR_INVALID_ARG;
+  if (!dr_supported(s)) return RGLRU_ERR_UNSUPPORTED;
+  if (s->Hv != s->Hk && !req(workspace)) return RGLRU_ERR_INVALID_ARG;
+  DrArgs a = dr_args(s, num_seqs, scale, q, k, v, g, beta, cu, nullptr);
+  a.saved = static_cast<float*>(const_cast<void*>(saved));
+  a.dout = dout;
+  a.dhT = dhT;
+  a.dq = dq;
+  a.dk = dk;
+  a.dv = dv;
+  a.dg = dg;
+  a.dbeta = dbeta;
+  a.dh0 = dh0;
+  float* ws = static_cast<float*>(workspace);
+  const cudaError_t e = s->io == RGLRU_BF16 ? launch_bwd_io<bf16>(a, ws, stream)
+                                            : launch_bwd_io<float>(a, ws, stream);
+  return cuda_status(e);
+}

@@ -1,4 +1,4 @@
-"""Thin ctypes binding of librglru (include/librglru.h).
+"""Thin ctypes binding of librglru (include/librglru.h and include/delta_rule.h).
 
 Argument marshalling only: every function here checks that its tensors are contiguous CUDA
 tensors, passes their device pointers and the current CUDA stream to the C ABI call of the
@@ -40,6 +40,13 @@ class Shape(ctypes.Structure):
                 f"grad={self.grad}, mode={self.mode})")
 
 
+class DeltaShape(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int32), ("T", ctypes.c_int32), ("Hk", ctypes.c_int32),
+                ("Hv", ctypes.c_int32), ("Dk", ctypes.c_int32), ("Dv", ctypes.c_int32),
+                ("io", ctypes.c_int32), ("kda", ctypes.c_int32),
+                ("state_v_first", ctypes.c_int32)]
+
+
 _lock = threading.Lock()
 _lib = None
 
@@ -48,7 +55,8 @@ EXPORTS = ("rglru_status_string", "rglru_saved_bytes", "rglru_workspace_bytes",
            "rglru_fused_forward", "rglru_fused_backward", "rglru_sync_status",
            "rglru_debug_lookback", "rglru_kernel_launches", "rglru_forward_noalloc",
            "rglru_debug_kernel_events", "rglru_step", "rglru_fused_forward_varlen",
-           "rglru_fused_backward_varlen")
+           "rglru_fused_backward_varlen", "delta_rule_saved_bytes", "delta_rule_workspace_bytes",
+           "delta_rule_forward", "delta_rule_backward")
 
 # Static look-back scratch of rglru_forward_noalloc, per GPU (RGLRU_NOALLOC_SCRATCH_BYTES).
 NOALLOC_SCRATCH_BYTES = 16 << 20
@@ -92,6 +100,17 @@ def lib():
             L.rglru_fused_forward_varlen.argtypes = [S] + [P] * 7 + [ctypes.c_int32] + [P] * 5
             L.rglru_fused_backward_varlen.argtypes = ([S] + [P] * 9 + [ctypes.c_int32] +
                                                       [P] * 11)
+            DS = ctypes.POINTER(DeltaShape)
+            L.delta_rule_saved_bytes.argtypes = [DS, ctypes.c_int32]
+            L.delta_rule_saved_bytes.restype = ctypes.c_size_t
+            L.delta_rule_workspace_bytes.argtypes = [DS]
+            L.delta_rule_workspace_bytes.restype = ctypes.c_size_t
+            L.delta_rule_forward.argtypes = ([DS] + [P] * 5 + [ctypes.c_float, P, ctypes.c_int32] +
+                                             [P] * 5)
+            L.delta_rule_backward.argtypes = ([DS] + [P] * 5 + [ctypes.c_float, P, ctypes.c_int32] +
+                                              [P] * 12)
+            L.delta_rule_forward.restype = ctypes.c_int
+            L.delta_rule_backward.restype = ctypes.c_int
             L.rglru_kernel_launches.argtypes = []
             L.rglru_kernel_launches.restype = ctypes.c_uint64
             for n in ("rglru_gate_proj", "rglru_forward", "rglru_backward",
@@ -246,3 +265,35 @@ def rglru_debug_kernel_events(start, stop) -> None:
 
 def rglru_kernel_launches() -> int:
     return int(lib().rglru_kernel_launches())
+
+
+# ---------------------------------------------------------------- gated delta rule
+
+def make_delta_shape(B, T, Hk, Hv, Dk, Dv, io=BF16, kda=False, state_v_first=False):
+    if isinstance(io, torch.dtype):
+        io = _DT[io]
+    return DeltaShape(int(B), int(T), int(Hk), int(Hv), int(Dk), int(Dv), int(io), int(bool(kda)),
+                      int(bool(state_v_first)))
+
+
+def delta_rule_saved_bytes(shape: DeltaShape, num_seqs: int) -> int:
+    return int(lib().delta_rule_saved_bytes(ctypes.byref(shape), int(num_seqs)))
+
+
+def delta_rule_workspace_bytes(shape: DeltaShape) -> int:
+    return int(lib().delta_rule_workspace_bytes(ctypes.byref(shape)))
+
+
+def delta_rule_forward(shape, q, k, v, g, beta, scale, cu_seqlens, num_seqs, h0, o, hT, saved,
+                       stream=None):
+    _check("delta_rule_forward", lib().delta_rule_forward(
+        ctypes.byref(shape), _p(q), _p(k), _p(v), _p(g), _p(beta), ctypes.c_float(scale),
+        _p(cu_seqlens), int(num_seqs), _p(h0), _p(o), _p(hT), _p(saved), _stream(stream)))
+
+
+def delta_rule_backward(shape, q, k, v, g, beta, scale, cu_seqlens, num_seqs, h0, saved, do,
+                        dhT, dq, dk, dv, dg, dbeta, dh0, workspace, stream=None):
+    _check("delta_rule_backward", lib().delta_rule_backward(
+        ctypes.byref(shape), _p(q), _p(k), _p(v), _p(g), _p(beta), ctypes.c_float(scale),
+        _p(cu_seqlens), int(num_seqs), _p(h0), _p(saved), _p(do), _p(dhT), _p(dq), _p(dk),
+        _p(dv), _p(dg), _p(dbeta), _p(dh0), _p(workspace), _stream(stream)))

@@ -13,6 +13,7 @@ from linear_recurrent_rnn_gb300 import librglru as R
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 HEADER = os.path.join(ROOT, "include", "librglru.h")
+HEADERS = (HEADER, os.path.join(ROOT, "include", "delta_rule.h"))
 
 
 @pytest.fixture(scope="module")
@@ -22,9 +23,11 @@ def lib():
 
 
 def declared_functions():
-    src = open(HEADER).read()
-    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
-    return sorted(set(re.findall(r"\b(rglru_[a-z_]+)\s*\(", src)))
+    names = set()
+    for h in HEADERS:
+        src = re.sub(r"/\*.*?\*/", "", open(h).read(), flags=re.S)
+        names |= set(re.findall(r"\b((?:rglru|delta_rule)_[a-z_]+)\s*\(", src))
+    return sorted(names)
 
 
 def test_header_declares_the_api():
@@ -38,7 +41,7 @@ def test_header_declares_the_api():
 def test_library_exports_every_declared_symbol(lib):
     out = subprocess.run(["nm", "-D", "--defined-only", B_.LIB], capture_output=True, text=True,
                          check=True).stdout
-    exported = set(re.findall(r"\bT (rglru_\w+)", out))
+    exported = set(re.findall(r"\bT ((?:rglru|delta_rule)_\w+)", out))
     missing = [n for n in declared_functions() if n not in exported]
     assert not missing, missing
     for n in declared_functions():
@@ -129,3 +132,27 @@ def test_varlen_host_validation(lib):
         assert call(R.make_shape(1, 256, 256, 4, R.BF16, R.BF16, R.CANONICAL)) == R.ERR_UNSUPPORTED
     assert fwd(good, saved=None) == R.ERR_INVALID_ARG
     assert bwd(good, ws=None) == R.ERR_INVALID_ARG
+
+
+def test_delta_rule_sizes_and_host_validation(lib):
+    """Scratch queries and host-side checks of the delta-rule entry points (fake, never
+    dereferenced addresses)."""
+    A = 1 << 20
+    P = lambda v: None if v is None else ctypes.c_void_p(v)
+    sh = R.make_delta_shape(2, 64, 2, 4, 64, 32, R.BF16)
+    assert R.delta_rule_saved_bytes(sh, 2) == (2 * 64 // 16 + 2 * 2 + 1) * 4 * 64 * 32 * 4
+    assert R.delta_rule_workspace_bytes(sh) == 2 * 2 * 64 * 4 * 64 * 4   # Hv > Hk
+    assert R.delta_rule_workspace_bytes(R.make_delta_shape(2, 64, 4, 4, 64, 32)) == 0
+    assert R.delta_rule_saved_bytes(R.make_delta_shape(2, 64, 2, 4, 48, 32), 2) == 0  # Dk 48
+    assert R.delta_rule_saved_bytes(R.make_delta_shape(2, 64, 2, 4, 64, 256), 2) == 0  # Dv 256
+
+    def fwd(shape, q=A, cu=None, N=2):
+        return lib.delta_rule_forward(ctypes.byref(shape), P(q), P(A), P(A), P(A), P(A),
+                                      ctypes.c_float(0.125), P(cu), N, None, P(A), None, P(A),
+                                      None)
+    assert fwd(sh, q=None) == R.ERR_INVALID_ARG
+    assert fwd(sh, q=A + 4) == R.ERR_INVALID_ARG                     # misaligned
+    assert fwd(sh, N=3) == R.ERR_INVALID_ARG                         # N must be B
+    assert fwd(sh, cu=A) == R.ERR_INVALID_ARG                        # packed needs B = 1
+    assert fwd(R.make_delta_shape(2, 64, 3, 4, 64, 32)) == R.ERR_INVALID_ARG   # Hv % Hk
+    assert fwd(R.make_delta_shape(2, 64, 2, 4, 96, 32)) == R.ERR_UNSUPPORTED   # Dk 96
