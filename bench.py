@@ -304,6 +304,8 @@ def run_ours(args, rank, world, local):
         line["cpu_baseline"] = cpu_baseline(wl, T=args.cpu_sample_T)
     if rank == 0 and world == 1 and not args.no_decode:
         line["decode"] = decode_step(flush, peak)
+    if rank == 0 and world == 1 and not args.no_delta:
+        line["delta_rule"] = delta_rule_measure(flush, peak)
     if rank == 0:
         print(json.dumps(line), flush=True)
 
@@ -358,6 +360,66 @@ def decode_step(flush, peak, W=2048, k=128, reps=20):
             out["roofline_B256"] = {"bound": "hbm", "unit": "GB/s", "achieved": gbs, "peak": peak,
                                     "frac": (gbs / peak) if peak else None,
                                     "algorithmic_bytes": nbytes}
+    return out
+
+
+# FP32 CUDA-core peak of the GB300 for the delta-rule kernels (no tensor cores): 152 SMs x 128
+# FP32 lanes x 2 FLOP per FMA x 2070 MHz (the maximum SM clock).
+ALU_FP32_TFLOPS = 152 * 128 * 2 * 2070e6 / 1e12
+
+
+def delta_rule_measure(flush, peak, reps=10):
+    """The gated delta rule (delta_rule_forward / _backward, GDN) at B4 T2048 with 16 heads of
+    128 x 128, bf16: milliseconds per call (L2 flushed before each), tokens/s of the pair, and
+    each kernel against the FP32 CUDA-core peak.  Algorithmic FLOPs per state element and
+    token: forward 7 (decay, S'^T k, the rank-1 write, S^T q); backward 22 (the forward again,
+    since the per-token states are not stored, and 15 for the reverse recurrence)."""
+    import torch
+    from linear_recurrent_rnn_gb300 import librglru as R
+    from linear_recurrent_rnn_gb300.delta_inputs import DELTA_WORKLOADS, generate
+    wl = DELTA_WORKLOADS["headline"]
+    inp = generate(wl, 7)
+    d = {n: (t.cuda() if isinstance(t, torch.Tensor) else t) for n, t in inp.items()}
+    sh = R.make_delta_shape(wl.B, wl.T, wl.Hk, wl.Hv, wl.Dk, wl.Dv, R.BF16)
+    scale = wl.Dk ** -0.5
+    N = wl.B
+    o = torch.empty_like(d["v"])
+    hT = torch.empty(N, wl.Hv, wl.Dk, wl.Dv, device="cuda")
+    saved = torch.empty(R.delta_rule_saved_bytes(sh, N), dtype=torch.uint8, device="cuda")
+    grads = {n: torch.empty(d[m].shape, device="cuda") for n, m in
+             (("dq", "q"), ("dk", "k"), ("dv", "v"), ("dg", "g"), ("dbeta", "beta"))}
+    dh0 = torch.empty_like(hT)
+    ws = torch.empty(max(1, R.delta_rule_workspace_bytes(sh)), dtype=torch.uint8, device="cuda")
+    fwd = lambda: R.delta_rule_forward(sh, d["q"], d["k"], d["v"], d["g"], d["beta"], scale, None,
+                                       N, None, o, hT, saved)
+    bwd = lambda: R.delta_rule_backward(sh, d["q"], d["k"], d["v"], d["g"], d["beta"], scale,
+                                        None, N, None, saved, d["do"], None, grads["dq"],
+                                        grads["dk"], grads["dv"], grads["dg"], grads["dbeta"],
+                                        dh0, ws)
+    for _ in range(3):
+        fwd()
+        bwd()
+    tf, tb = [], []
+    for _ in range(reps):
+        for fn, acc in ((fwd, tf), (bwd, tb)):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            fn()
+            b.record()
+            torch.cuda.synchronize()
+            acc.append(a.elapsed_time(b))
+    fms, bms = statistics.median(tf), statistics.median(tb)
+    elems = wl.B * wl.T * wl.Hv * wl.Dk * wl.Dv
+    out = {"workload": f"{wl.name} GDN bf16 (q, k unit length, exp(g) U[0.8, 1), beta U(0, 1))",
+           "fwd_ms": fms, "bwd_ms": bms, "tokens_per_s": wl.B * wl.T / ((fms + bms) / 1e3),
+           "saved_bytes": saved.numel()}
+    for name, flop, ms in (("fwd", 7 * elems, fms), ("bwd", 22 * elems, bms)):
+        tf_s = flop / (ms / 1e3) / 1e12
+        out[f"roofline_{name}"] = {"bound": "alu", "unit": "TFLOP/s", "achieved": tf_s,
+                                   "peak": ALU_FP32_TFLOPS, "frac": tf_s / ALU_FP32_TFLOPS,
+                                   "algorithmic_flop": flop,
+                                   "peak_source": "derived: 152 SMs x 128 FP32 lanes x 2 x 2070 MHz"}
     return out
 
 
@@ -438,6 +500,7 @@ def main(argv=None):
     p.add_argument("--impl", choices=("ours", "reference"), default="ours")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-decode", action="store_true", help="skip the decode-step measurement")
+    p.add_argument("--no-delta", action="store_true", help="skip the delta-rule measurement")
     p.add_argument("--cpu-sample-T", type=int, default=2048)
     p.add_argument("--ref-sample-T", type=int, default=256)
     args = p.parse_args(argv)

@@ -32,6 +32,11 @@ namespace rglru {
 namespace {
 
 constexpr int DR_TB = 16;                 // tokens per staged block = tokens per saved state
+// float32 rows of keys are stored as groups of 32 keys 36 floats apart: the KG groups a warp
+// reads at once then start 4 banks apart, so its broadcast 16-byte loads do not conflict
+constexpr int KGS = 36;
+// reduction rows: groups of 32 keys 33 floats apart (one bank apart)
+constexpr int RGS = 33;
 constexpr unsigned FULL = 0xffffffffu;
 
 struct DrArgs {
@@ -86,50 +91,109 @@ __device__ __forceinline__ float ldf(const void* p, size_t i) {
   return to_f32<T>(static_cast<const T*>(p)[i]);
 }
 
-// The token-major staging of one block: k, q [TB][DK]; KDA decays and decays * k [TB][DK];
-// GDN decays, beta [TB]; the CTA's value columns of v (and of do) [TB][NC].
+// ---- staging.  A block of DR_TB tokens comes in raw (storage dtype, as in global memory) by
+// 16-byte asynchronous copies into one of two raw buffers, one block ahead of the compute;
+// prepare_block then converts it in shared memory to float32 rows (and the decays, exp(g), and
+// for KDA decay * k).  Tokens past the sequence are zero-filled, never read from global memory.
+__device__ __forceinline__ void cp_async(void* dst, const void* src, uint32_t bytes, bool valid) {
+  const uint32_t d = (uint32_t)__cvta_generic_to_shared(dst);
+  if (bytes == 16)
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(d), "l"(src),
+                 "r"(valid ? 16u : 0u) : "memory");
+  else
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(d), "l"(src),
+                 "r"(valid ? 4u : 0u) : "memory");
+}
+__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_wait1() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
+
+// One raw stage: k, q [TB][DK], v (and do) [TB][NC] in the storage dtype; g [TB][DK] (KDA) or
+// [TB] (GDN) and beta [TB] as float32.
 template <typename T, int DK>
-__device__ void stage_block(const DrArgs& a, const Seq& sq, int hv, int t0, int nt, int c0,
-                            int NC, float* s_k, float* s_q, float* s_a, float* s_ak, float* s_v,
-                            float* s_do, float* s_b, float* s_ag) {
-  const int hk = hv / (a.Hv / a.Hk);
-  for (int e = threadIdx.x; e < DR_TB * DK; e += blockDim.x) {
-    const int tt = e / DK, i = e % DK;
-    float kv = 0.0f, qv = 0.0f, av = 1.0f;
-    if (tt < nt) {
-      const size_t row = (size_t)sq.b * a.T + sq.s + t0 + tt;
-      kv = ldf<T>(a.k, (row * a.Hk + hk) * DK + i);
-      qv = ldf<T>(a.q, (row * a.Hk + hk) * DK + i);
-      if (a.kda) av = expf(a.g[(row * a.Hv + hv) * DK + i]);
-    }
-    s_k[e] = kv;
-    s_q[e] = qv;
-    if (a.kda) {
-      s_a[e] = av;
-      s_ak[e] = av * kv;
-    }
+struct Raw {
+  static constexpr size_t kq_bytes = (size_t)DR_TB * DK * sizeof(T);
+  __host__ __device__ static size_t bytes(int NC, bool with_do) {
+    return 2 * kq_bytes + (with_do ? 2 : 1) * (size_t)DR_TB * NC * sizeof(T) +
+           (size_t)DR_TB * DK * 4 + DR_TB * 4;
   }
-  for (int e = threadIdx.x; e < DR_TB * NC; e += blockDim.x) {
-    const int tt = e / NC, jc = e % NC, j = c0 + jc;
-    float vv = 0.0f, dv = 0.0f;
-    if (tt < nt && j < a.Dv) {
-      const size_t row = (size_t)sq.b * a.T + sq.s + t0 + tt;
-      vv = ldf<T>(a.v, (row * a.Hv + hv) * a.Dv + j);
-      if (s_do) dv = ldf<T>(a.dout, (row * a.Hv + hv) * a.Dv + j);
+};
+
+template <typename T, int DK>
+__device__ void issue_block(const DrArgs& a, const Seq& sq, int hv, int t0, int nt, int c0,
+                            int NC, uint8_t* raw, bool with_do) {
+  constexpr int EV = 16 / sizeof(T);  // elements per 16-byte copy
+  const int hk = hv / (a.Hv / a.Hk);
+  T* rk = reinterpret_cast<T*>(raw);
+  T* rq = rk + DR_TB * DK;
+  T* rv = rq + DR_TB * DK;
+  T* rdo = rv + DR_TB * NC;
+  float* rg = reinterpret_cast<float*>(rv + (with_do ? 2 : 1) * DR_TB * NC);
+  float* rb = rg + DR_TB * DK;
+  const size_t row0 = (size_t)sq.b * a.T + sq.s + t0;  // first token of the block
+  constexpr int VK = DK / EV;
+  for (int e = threadIdx.x; e < DR_TB * VK; e += blockDim.x) {
+    const int tt = e / VK, x = e % VK;
+    const bool ok = tt < nt;
+    const size_t src = ((row0 + (ok ? tt : 0)) * a.Hk + hk) * DK + x * EV;
+    cp_async(rk + tt * DK + x * EV, static_cast<const T*>(a.k) + src, 16, ok);
+    cp_async(rq + tt * DK + x * EV, static_cast<const T*>(a.q) + src, 16, ok);
+  }
+  const int VN = NC / EV;
+  for (int e = threadIdx.x; e < DR_TB * VN; e += blockDim.x) {
+    const int tt = e / VN, x = e % VN, j = c0 + x * EV;
+    const bool ok = tt < nt && j < a.Dv;
+    const size_t src = ((row0 + (ok ? tt : 0)) * a.Hv + hv) * a.Dv + (ok ? j : 0);
+    cp_async(rv + tt * NC + x * EV, static_cast<const T*>(a.v) + src, 16, ok);
+    if (with_do) cp_async(rdo + tt * NC + x * EV, static_cast<const T*>(a.dout) + src, 16, ok);
+  }
+  if (a.kda) {
+    constexpr int VG = DK / 4;
+    for (int e = threadIdx.x; e < DR_TB * VG; e += blockDim.x) {
+      const int tt = e / VG, x = e % VG;
+      const bool ok = tt < nt;
+      const size_t src = ((row0 + (ok ? tt : 0)) * a.Hv + hv) * DK + x * 4;
+      cp_async(rg + tt * DK + x * 4, a.g + src, 16, ok);
     }
-    s_v[e] = vv;
-    if (s_do) s_do[e] = dv;
   }
   if (threadIdx.x < DR_TB) {
     const int tt = threadIdx.x;
-    float bv = 0.0f, ag = 1.0f;
-    if (tt < nt) {
-      const size_t row = (size_t)sq.b * a.T + sq.s + t0 + tt;
-      bv = a.beta[row * a.Hv + hv];
-      if (!a.kda) ag = expf(a.g[row * a.Hv + hv]);
+    const bool ok = tt < nt;
+    const size_t src = (row0 + (ok ? tt : 0)) * a.Hv + hv;
+    if (!a.kda) cp_async(rg + tt, a.g + src, 4, ok);
+    cp_async(rb + tt, a.beta + src, 4, ok);
+  }
+}
+
+template <typename T, int DK>
+__device__ void prepare_block(const DrArgs& a, const uint8_t* raw, int NC, bool with_do,
+                              float* s_k, float* s_q, float* s_a, float* s_ak, float* s_v,
+                              float* s_do, float* s_b, float* s_ag) {
+  const T* rk = reinterpret_cast<const T*>(raw);
+  const T* rq = rk + DR_TB * DK;
+  const T* rv = rq + DR_TB * DK;
+  const T* rdo = rv + DR_TB * NC;
+  const float* rg = reinterpret_cast<const float*>(rv + (with_do ? 2 : 1) * DR_TB * NC);
+  const float* rb = rg + DR_TB * DK;
+  constexpr int DKP = DK / 32 * KGS;
+  for (int e = threadIdx.x; e < DR_TB * DK; e += blockDim.x) {
+    const int tt = e / DK, i = e % DK;
+    const int d = tt * DKP + (i >> 5) * KGS + (i & 31);
+    const float kv = to_f32<T>(rk[e]);
+    s_k[d] = kv;
+    s_q[d] = to_f32<T>(rq[e]);
+    if (a.kda) {
+      const float av = expf(rg[e]);
+      s_a[d] = av;
+      s_ak[d] = av * kv;
     }
-    s_b[tt] = bv;
-    s_ag[tt] = ag;
+  }
+  for (int e = threadIdx.x; e < DR_TB * NC; e += blockDim.x) {
+    s_v[e] = to_f32<T>(rv[e]);
+    if (with_do) s_do[e] = to_f32<T>(rdo[e]);
+  }
+  if (threadIdx.x < DR_TB) {
+    s_b[threadIdx.x] = rb[threadIdx.x];
+    s_ag[threadIdx.x] = a.kda ? 1.0f : expf(rg[threadIdx.x]);
   }
 }
 
@@ -150,6 +214,19 @@ __device__ __forceinline__ float kg_sum(float x) {
   return x;
 }
 
+// sum_x a[x] b[x] over 32 terms in four interleaved partial sums (a shorter dependent chain).
+__device__ __forceinline__ float dot32(const float (&x)[32], const float (&y)[32]) {
+  float p0 = 0.0f, p1 = 0.0f, p2 = 0.0f, p3 = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 32; i += 4) {
+    p0 = fmaf(x[i], y[i], p0);
+    p1 = fmaf(x[i + 1], y[i + 1], p1);
+    p2 = fmaf(x[i + 2], y[i + 2], p2);
+    p3 = fmaf(x[i + 3], y[i + 3], p3);
+  }
+  return (p0 + p1) + (p2 + p3);
+}
+
 // One token of the forward on a thread's 32 keys: S' = D S, w = S'^T k, u = beta (v - w),
 // S = S' + k u; returns w and u (the column's, identical on its KG lanes).
 template <int KG>
@@ -162,8 +239,7 @@ __device__ __forceinline__ void fwd_token(float (&S)[32], const float* kr, const
   if (kda) {
     float ak[32];
     ld32(akr, ak);
-#pragma unroll
-    for (int x = 0; x < 32; ++x) part = fmaf(S[x], ak[x], part);
+    part = dot32(S, ak);
     w = kg_sum<KG>(part);
     u = bt * (vj - w);
     float al[32];
@@ -171,8 +247,7 @@ __device__ __forceinline__ void fwd_token(float (&S)[32], const float* kr, const
 #pragma unroll
     for (int x = 0; x < 32; ++x) S[x] = fmaf(al[x], S[x], kk[x] * u);
   } else {
-#pragma unroll
-    for (int x = 0; x < 32; ++x) part = fmaf(S[x], kk[x], part);
+    part = dot32(S, kk);
     w = ag * kg_sum<KG>(part);
     u = bt * (vj - w);
 #pragma unroll
@@ -182,15 +257,17 @@ __device__ __forceinline__ void fwd_token(float (&S)[32], const float* kr, const
 
 template <typename T, int KG>
 __global__ void __launch_bounds__(128) k_dr_fwd(DrArgs a) {
-  constexpr int DK = 32 * KG, CPW = 32 / KG, NC = 4 * CPW;
+  constexpr int DK = 32 * KG, CPW = 32 / KG, NC = 4 * CPW, DKP = KG * KGS;
   extern __shared__ __align__(16) float sm[];
   float* s_k = sm;
-  float* s_q = s_k + DR_TB * DK;
-  float* s_a = s_q + DR_TB * DK;
-  float* s_ak = s_a + DR_TB * DK;
-  float* s_v = s_ak + DR_TB * DK;
+  float* s_q = s_k + DR_TB * DKP;
+  float* s_a = s_q + DR_TB * DKP;
+  float* s_ak = s_a + DR_TB * DKP;
+  float* s_v = s_ak + DR_TB * DKP;
   float* s_b = s_v + DR_TB * NC;
   float* s_ag = s_b + DR_TB;
+  uint8_t* raw0 = reinterpret_cast<uint8_t*>(s_ag + DR_TB);
+  const size_t rawb = Raw<T, DK>::bytes(NC, false);
   const int slice = blockIdx.x % a.nslices;
   const int hv = (blockIdx.x / a.nslices) % a.Hv;
   const int n = blockIdx.x / (a.nslices * a.Hv);
@@ -199,7 +276,7 @@ __global__ void __launch_bounds__(128) k_dr_fwd(DrArgs a) {
   const int kg = lane % KG, jc = warp * CPW + lane / KG;
   const int c0 = slice * NC, j = c0 + jc;
   const bool live = j < a.Dv;
-  const int key0 = kg * 32;
+  const int key0 = kg * 32, kp0 = kg * KGS;  // first key, and its padded offset in a row
 
   float S[32];
 #pragma unroll
@@ -211,10 +288,19 @@ __global__ void __launch_bounds__(128) k_dr_fwd(DrArgs a) {
       S[x] = a.vfirst ? a.h0[(base * a.Dv + j) * DK + key0 + x]
                       : a.h0[(base * DK + key0 + x) * a.Dv + j];
   }
-  for (int t0 = 0; t0 < sq.len; t0 += DR_TB) {
-    const int nt = min(DR_TB, sq.len - t0);
-    __syncthreads();  // the previous block's staging is consumed
-    stage_block<T, DK>(a, sq, hv, t0, nt, c0, NC, s_k, s_q, s_a, s_ak, s_v, nullptr, s_b, s_ag);
+  const int nblk = (sq.len + DR_TB - 1) / DR_TB;
+  if (nblk > 0) issue_block<T, DK>(a, sq, hv, 0, min(DR_TB, sq.len), c0, NC, raw0, false);
+  cp_commit();
+  for (int blk = 0; blk < nblk; ++blk) {
+    const int t0 = blk * DR_TB, nt = min(DR_TB, sq.len - t0);
+    if (blk + 1 < nblk)  // the next block's copies overlap this block's tokens
+      issue_block<T, DK>(a, sq, hv, t0 + DR_TB, min(DR_TB, sq.len - t0 - DR_TB), c0, NC,
+                         raw0 + ((blk + 1) & 1) * rawb, false);
+    cp_commit();
+    cp_wait1();
+    __syncthreads();  // this block's copies have landed; the previous block is consumed
+    prepare_block<T, DK>(a, raw0 + (blk & 1) * rawb, NC, false, s_k, s_q, s_a, s_ak, s_v,
+                         nullptr, s_b, s_ag);
     __syncthreads();
     if (a.saved && live) {  // the state entering the block
       float* dst = a.saved + (((size_t)(sq.slot0 + t0 / DR_TB) * a.Hv + hv) * a.Dv + j) * DK + key0;
@@ -224,14 +310,11 @@ __global__ void __launch_bounds__(128) k_dr_fwd(DrArgs a) {
     }
     for (int tt = 0; tt < nt; ++tt) {
       float w, u;
-      fwd_token<KG>(S, s_k + tt * DK + key0, s_a + tt * DK + key0, s_ak + tt * DK + key0,
+      fwd_token<KG>(S, s_k + tt * DKP + kp0, s_a + tt * DKP + kp0, s_ak + tt * DKP + kp0,
                     a.kda != 0, s_ag[tt], s_b[tt], s_v[tt * NC + jc], w, u);
       float qq[32];
-      ld32(s_q + tt * DK + key0, qq);
-      float part = 0.0f;
-#pragma unroll
-      for (int x = 0; x < 32; ++x) part = fmaf(S[x], qq[x], part);
-      const float ov = a.scale * kg_sum<KG>(part);
+      ld32(s_q + tt * DKP + kp0, qq);
+      const float ov = a.scale * kg_sum<KG>(dot32(S, qq));
       if (kg == 0 && live) {
         const size_t row = (size_t)sq.b * a.T + sq.s + t0 + tt;
         static_cast<T*>(a.o)[(row * a.Hv + hv) * a.Dv + j] = from_f32<T>(ov);
@@ -250,9 +333,12 @@ __global__ void __launch_bounds__(128) k_dr_fwd(DrArgs a) {
   }
 }
 
+template <typename T>
 size_t fwd_smem(int KG) {
   const int DK = 32 * KG, NC = 4 * (32 / KG);
-  return (size_t)(4 * DR_TB * DK + DR_TB * NC + 2 * DR_TB) * sizeof(float);
+  const size_t raw = 2 * (size_t)DR_TB * DK * sizeof(T) + (size_t)DR_TB * NC * sizeof(T) +
+                     (size_t)DR_TB * DK * 4 + DR_TB * 4;
+  return (size_t)(4 * DR_TB * KG * KGS + DR_TB * NC + 2 * DR_TB) * sizeof(float) + 2 * raw;
 }
 
 // Sums 32 per-key values over the CPW columns of the warp with a halving butterfly: at level L
@@ -297,27 +383,32 @@ __device__ __forceinline__ float warp_sum(float x) {
 // memory (double-buffered, one barrier per token).
 template <typename T, int KG>
 __global__ void __launch_bounds__(512, 1) k_dr_bwd(DrArgs a) {
-  constexpr int DK = 32 * KG, CPW = 32 / KG;
+  constexpr int DK = 32 * KG, CPW = 32 / KG, DKP = KG * KGS, DKR = KG * RGS;
   const int nwarps = blockDim.x >> 5, NC = nwarps * CPW;
   const int NV = a.kda ? 3 : 2;      // per-key vectors reduced per token: dq, dk (, dg)
-  const int RS = NV * DK + 2;        // a warp's reduction row: vectors, dbeta, GDN dg
+  // a warp's reduction row: vectors, dbeta, GDN dg; a multiple of 4 floats, so that the raw
+  // staging after the rows stays 16-byte aligned
+  const int RS = (NV * DKR + 2 + 3) & ~3;
   extern __shared__ __align__(16) float sm[];
   float* s_k = sm;
-  float* s_q = s_k + DR_TB * DK;
-  float* s_a = s_q + DR_TB * DK;
-  float* s_ak = s_a + DR_TB * DK;
-  float* s_v = s_ak + DR_TB * DK;
+  float* s_q = s_k + DR_TB * DKP;
+  float* s_a = s_q + DR_TB * DKP;
+  float* s_ak = s_a + DR_TB * DKP;
+  float* s_v = s_ak + DR_TB * DKP;
   float* s_do = s_v + DR_TB * NC;
   float* s_b = s_do + DR_TB * NC;
   float* s_ag = s_b + DR_TB;
   float* s_red = s_ag + DR_TB;       // [2][nwarps][RS]
+  uint8_t* raw0 = reinterpret_cast<uint8_t*>(s_red + 2 * nwarps * RS);
+  const size_t rawb = Raw<T, DK>::bytes(NC, true);
   const int hv = blockIdx.x % a.Hv, n = blockIdx.x / a.Hv;
   const int hk = hv / (a.Hv / a.Hk);
   const Seq sq = seq_of(a, n);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int kg = lane % KG, jc = warp * CPW + lane / KG, j = jc;
   const bool live = j < a.Dv;
-  const int key0 = kg * 32, kf = key0 + fold_key<KG>(lane);
+  const int key0 = kg * 32, kp0 = kg * KGS;
+  const int kf = kg * RGS + fold_key<KG>(lane);  // this lane's folded sums in a reduction row
   const size_t hbase = (size_t)n * a.Hv + hv;
   const bool per_vhead = a.Hv != a.Hk;  // dq, dk per value head, summed by a second kernel
 
@@ -333,10 +424,20 @@ __global__ void __launch_bounds__(512, 1) k_dr_bwd(DrArgs a) {
   float hist[DR_TB][32];
   float wh[DR_TB], uh[DR_TB];
   const int nblk = (sq.len + DR_TB - 1) / DR_TB;
+  if (nblk > 0) {
+    const int tl = (nblk - 1) * DR_TB;
+    issue_block<T, DK>(a, sq, hv, tl, sq.len - tl, 0, NC, raw0 + ((nblk - 1) & 1) * rawb, true);
+  }
+  cp_commit();
   for (int blk = nblk - 1; blk >= 0; --blk) {
     const int t0 = blk * DR_TB, nt = min(DR_TB, sq.len - t0);
+    if (blk > 0)  // the previous block's copies overlap this block's work
+      issue_block<T, DK>(a, sq, hv, t0 - DR_TB, DR_TB, 0, NC, raw0 + ((blk - 1) & 1) * rawb, true);
+    cp_commit();
+    cp_wait1();
     __syncthreads();
-    stage_block<T, DK>(a, sq, hv, t0, nt, 0, NC, s_k, s_q, s_a, s_ak, s_v, s_do, s_b, s_ag);
+    prepare_block<T, DK>(a, raw0 + (blk & 1) * rawb, NC, true, s_k, s_q, s_a, s_ak, s_v, s_do,
+                         s_b, s_ag);
     __syncthreads();
     float S[32];
     if (live) {
@@ -353,14 +454,14 @@ __global__ void __launch_bounds__(512, 1) k_dr_bwd(DrArgs a) {
     for (int tt = 0; tt < nt; ++tt) {
 #pragma unroll
       for (int x = 0; x < 32; ++x) hist[tt][x] = S[x];
-      fwd_token<KG>(S, s_k + tt * DK + key0, s_a + tt * DK + key0, s_ak + tt * DK + key0,
+      fwd_token<KG>(S, s_k + tt * DKP + kp0, s_a + tt * DKP + kp0, s_ak + tt * DKP + kp0,
                     a.kda != 0, s_ag[tt], s_b[tt], s_v[tt * NC + jc], wh[tt], uh[tt]);
     }
     for (int tt = nt - 1; tt >= 0; --tt) {
       const float ag = s_ag[tt], bt = s_b[tt], u = uh[tt], w = wh[tt];
       const float doj = s_do[tt * NC + jc], vj = s_v[tt * NC + jc];
-      const float* kr = s_k + tt * DK + key0;
-      const float* ar = s_a + tt * DK + key0;
+      const float* kr = s_k + tt * DKP + kp0;
+      const float* ar = s_a + tt * DKP + kp0;
       float Sp[32], vec[32];
 #pragma unroll
       for (int x = 0; x < 32; ++x) Sp[x] = hist[tt][x];
@@ -376,7 +477,7 @@ __global__ void __launch_bounds__(512, 1) k_dr_bwd(DrArgs a) {
       // dS += scale q do;  dq = scale (S' + k u) do
       {
         float qq[32], kk[32];
-        ld32(s_q + tt * DK + key0, qq);
+        ld32(s_q + tt * DKP + kp0, qq);
         ld32(kr, kk);
         const float sd = a.scale * doj;
 #pragma unroll
@@ -395,10 +496,7 @@ __global__ void __launch_bounds__(512, 1) k_dr_bwd(DrArgs a) {
       {
         float kk[32];
         ld32(kr, kk);
-        float part = 0.0f;
-#pragma unroll
-        for (int x = 0; x < 32; ++x) part = fmaf(dS[x], kk[x], part);
-        du = kg_sum<KG>(part);
+        du = kg_sum<KG>(dot32(dS, kk));
         dw = -bt * du;
 #pragma unroll
         for (int x = 0; x < 32; ++x) {
@@ -408,7 +506,7 @@ __global__ void __launch_bounds__(512, 1) k_dr_bwd(DrArgs a) {
       }
       fold<KG, 0>(vec, lane);
 #pragma unroll
-      for (int x = 0; x < KG; ++x) red[DK + kf + x] = vec[x];
+      for (int x = 0; x < KG; ++x) red[DKR + kf + x] = vec[x];
       // dg from dS' and S', then dS = D dS'
       float gpart = 0.0f;
       if (a.kda) {
@@ -421,7 +519,7 @@ __global__ void __launch_bounds__(512, 1) k_dr_bwd(DrArgs a) {
         }
         fold<KG, 0>(vec, lane);
 #pragma unroll
-        for (int x = 0; x < KG; ++x) red[2 * DK + kf + x] = vec[x];
+        for (int x = 0; x < KG; ++x) red[2 * DKR + kf + x] = vec[x];
       } else {
 #pragma unroll
         for (int x = 0; x < 32; ++x) {
@@ -432,8 +530,8 @@ __global__ void __launch_bounds__(512, 1) k_dr_bwd(DrArgs a) {
       const float bpart = (kg == 0 && live) ? du * (vj - w) : 0.0f;
       const float bsum = warp_sum(bpart), gsum = warp_sum(live ? gpart : 0.0f);
       if (lane == 0) {
-        red[NV * DK] = bsum;
-        red[NV * DK + 1] = gsum;
+        red[NV * DKR] = bsum;
+        red[NV * DKR + 1] = gsum;
       }
       const size_t row = (size_t)sq.b * a.T + sq.s + t0 + tt;
       if (kg == 0 && live) a.dv[(row * a.Hv + hv) * a.Dv + j] = bt * du;
@@ -442,8 +540,9 @@ __global__ void __launch_bounds__(512, 1) k_dr_bwd(DrArgs a) {
       for (int e = threadIdx.x; e < NV * DK + 1; e += blockDim.x) {
         float s = 0.0f;
         if (e < NV * DK) {
-          for (int ww = 0; ww < nwarps; ++ww) s += rb[ww * RS + e];
           const int vsel = e / DK, i = e % DK;
+          const int re = vsel * DKR + (i >> 5) * RGS + (i & 31);
+          for (int ww = 0; ww < nwarps; ++ww) s += rb[ww * RS + re];
           if (vsel == 0 || vsel == 1) {
             float* dst = vsel == 0 ? a.dq : a.dk;
             const size_t o = per_vhead ? (row * a.Hv + hv) * DK + i : (row * a.Hk + hk) * DK + i;
@@ -454,8 +553,8 @@ __global__ void __launch_bounds__(512, 1) k_dr_bwd(DrArgs a) {
         } else {
           float sb = 0.0f, sg = 0.0f;
           for (int ww = 0; ww < nwarps; ++ww) {
-            sb += rb[ww * RS + NV * DK];
-            sg += rb[ww * RS + NV * DK + 1];
+            sb += rb[ww * RS + NV * DKR];
+            sg += rb[ww * RS + NV * DKR + 1];
           }
           a.dbeta[row * a.Hv + hv] = sb;
           if (!a.kda) a.dg[row * a.Hv + hv] = sg;
@@ -489,10 +588,14 @@ __global__ void k_dr_group_sum(const float* ws, float* out, size_t rows, int Hk,
   }
 }
 
+template <typename T>
 size_t bwd_smem(int KG, int nwarps, int kda) {
   const int DK = 32 * KG, NC = nwarps * (32 / KG);
-  const int RS = (kda ? 3 : 2) * DK + 2;
-  return (size_t)(4 * DR_TB * DK + 2 * DR_TB * NC + 2 * DR_TB + 2 * nwarps * RS) * sizeof(float);
+  const int RS = ((kda ? 3 : 2) * KG * RGS + 2 + 3) & ~3;
+  const size_t raw = 2 * (size_t)DR_TB * DK * sizeof(T) + 2 * (size_t)DR_TB * NC * sizeof(T) +
+                     (size_t)DR_TB * DK * 4 + DR_TB * 4;
+  return (size_t)(4 * DR_TB * KG * KGS + 2 * DR_TB * NC + 2 * DR_TB + 2 * nwarps * RS) *
+             sizeof(float) + 2 * raw;
 }
 
 }  // namespace
@@ -506,7 +609,9 @@ bool dr_dims_ok(const delta_shape* s) {
          (s->io == RGLRU_F32 || s->io == RGLRU_BF16);
 }
 bool dr_supported(const delta_shape* s) {
-  return (s->Dk == 32 || s->Dk == 64 || s->Dk == 128) && s->Dv >= 1 && s->Dv <= 128;
+  const int es = s->io == RGLRU_BF16 ? 2 : 4;
+  return (s->Dk == 32 || s->Dk == 64 || s->Dk == 128) && s->Dv >= 1 && s->Dv <= 128 &&
+         (s->Dv * es) % 16 == 0;
 }
 long dr_slots(const delta_shape* s, int N) { return (long)s->B * s->T / DR_TB + 2L * N + 1; }
 
@@ -538,7 +643,7 @@ template <typename T, int KG>
 cudaError_t launch_fwd_t(DrArgs& a, cudaStream_t st) {
   const int NC = 4 * (32 / KG);
   a.nslices = (a.Dv + NC - 1) / NC;
-  const size_t smem = fwd_smem(KG);
+  const size_t smem = fwd_smem<T>(KG);
   cudaError_t e = cudaFuncSetAttribute(k_dr_fwd<T, KG>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   const long grid = (long)a.N * a.Hv * a.nslices;
@@ -561,7 +666,7 @@ template <typename T, int KG>
 cudaError_t launch_bwd_t(DrArgs& a, float* ws, cudaStream_t st) {
   const int CPW = 32 / KG;
   const int nwarps = (a.Dv + CPW - 1) / CPW;
-  const size_t smem = bwd_smem(KG, nwarps, a.kda);
+  const size_t smem = bwd_smem<T>(KG, nwarps, a.kda);
   cudaError_t e = cudaFuncSetAttribute(k_dr_bwd<T, KG>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   float* dq = a.dq;
