@@ -21,8 +21,9 @@
  *     Without cu_seqlens N = B and sequence n is batch row n; with it B must be 1 and sequence
  *     n is tokens [cu_seqlens[n], cu_seqlens[n+1]) of row 0 (device int32 [N + 1], from 0 to T,
  *     non-decreasing; a malformed array gives wrong results, never an out-of-bounds access).
- *   - Supported: Dk in {32, 64, 128}, 1 <= Dv <= 128, Hv a multiple of Hk, every pointer
- *     16-byte aligned; else RGLRU_ERR_UNSUPPORTED (sizes) or RGLRU_ERR_INVALID_ARG.
+ *   - Supported: Dk in {32, 64, 128}, 1 <= Dv <= 128 with Dv x sizeof(io) a multiple of 16
+ *     bytes (rows of v come in by 16-byte copies), Hv a multiple of Hk, every pointer 16-byte
+ *     aligned; else RGLRU_ERR_UNSUPPORTED (sizes) or RGLRU_ERR_INVALID_ARG.
  *   - Ownership: the caller allocates every buffer, `saved` and `workspace` sized by the
  *     queries below; the library never allocates or synchronises.  All work is enqueued on
  *     `stream`.  Argument checks run on the host before any launch; launch failures return

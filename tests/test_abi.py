@@ -156,3 +156,4 @@ def test_delta_rule_sizes_and_host_validation(lib):
     assert fwd(sh, cu=A) == R.ERR_INVALID_ARG                        # packed needs B = 1
     assert fwd(R.make_delta_shape(2, 64, 3, 4, 64, 32)) == R.ERR_INVALID_ARG   # Hv % Hk
     assert fwd(R.make_delta_shape(2, 64, 2, 4, 96, 32)) == R.ERR_UNSUPPORTED   # Dk 96
+    assert fwd(R.make_delta_shape(2, 64, 2, 4, 64, 12)) == R.ERR_UNSUPPORTED   # 24-byte v rows
