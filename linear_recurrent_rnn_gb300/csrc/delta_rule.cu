@@ -366,23 +366,45 @@ __device__ __forceinline__ int fold_key(int lane) {
     if (lane & (KG << L)) off += 16 >> L;
   return off;
 }
+// The CTA's rank in its cluster, a float from the same offset of another CTA's shared memory,
+// and a barrier over the cluster (release / acquire).
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ float ld_peer(const float* p, uint32_t rank) {
+  const uint32_t a = (uint32_t)__cvta_generic_to_shared(p);
+  uint32_t ra;
+  float v;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(a), "r"(rank));
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(ra) : "memory");
+  return v;
+}
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
 __device__ __forceinline__ float warp_sum(float x) {
 #pragma unroll
   for (int m = 16; m > 0; m >>= 1) x += __shfl_xor_sync(FULL, x, m);
   return x;
 }
 
-// Backward.  CTA = (sequence n, value head hv), blockDim = 32 x ceil(Dv / CPW).  Per 16-token
+// Backward.  A cluster of two CTAs per (sequence n, value head hv), each with half of the value
+// columns (blockDim = 32 x ceil(Dv / 2 / CPW)).  Per 16-token
 // block, last block first: restore the block's entry state from `saved`, run the block forward
 // keeping every token's state before its decay (thread-local), w and u; then for each token in
 // reverse (dS the gradient of the state after the token):
 //   dS += scale q do^T;  dq = scale (S' + k u^T) do;  du = dS^T k;  dw = -beta du
 //   dk = dS u + S' dw;  dbeta = du . (v - w);  dv = beta du;  dS' = dS + k dw^T
 //   dg = <dS', S'> (GDN) or its row sums (KDA);  dS = D dS'
-// dq, dk (and KDA's dg) sum over the columns: warp butterfly, then the warps through shared
-// memory (double-buffered, one barrier per token).
+// dq, dk (and KDA's dg) sum over the columns: warp butterfly, the warps through shared memory,
+// and the two CTAs through distributed shared memory (each CTA writes the outputs of half of
+// the sums, own + peer in rank order); both exchanges are double-buffered, so a token costs one
+// CTA barrier and one cluster barrier.
 template <typename T, int KG>
-__global__ void __launch_bounds__(512, 1) k_dr_bwd(DrArgs a) {
+__global__ void __launch_bounds__(256, 1) k_dr_bwd(DrArgs a) {
   constexpr int DK = 32 * KG, CPW = 32 / KG, DKP = KG * KGS, DKR = KG * RGS;
   const int nwarps = blockDim.x >> 5, NC = nwarps * CPW;
   const int NV = a.kda ? 3 : 2;      // per-key vectors reduced per token: dq, dk (, dg)
@@ -399,13 +421,18 @@ __global__ void __launch_bounds__(512, 1) k_dr_bwd(DrArgs a) {
   float* s_b = s_do + DR_TB * NC;
   float* s_ag = s_b + DR_TB;
   float* s_red = s_ag + DR_TB;       // [2][nwarps][RS]
-  uint8_t* raw0 = reinterpret_cast<uint8_t*>(s_red + 2 * nwarps * RS);
+  const int NE = NV * DK + 2, XS = (NE + 3) & ~3;
+  float* s_xp = s_red + 2 * nwarps * RS;  // [2][XS]: this CTA's sums, read by its peer too
+  uint8_t* raw0 = reinterpret_cast<uint8_t*>(s_xp + 2 * XS);
   const size_t rawb = Raw<T, DK>::bytes(NC, true);
-  const int hv = blockIdx.x % a.Hv, n = blockIdx.x / a.Hv;
+  const uint32_t crank = cluster_rank();
+  const int pid = blockIdx.x >> 1;
+  const int hv = pid % a.Hv, n = pid / a.Hv;
   const int hk = hv / (a.Hv / a.Hk);
   const Seq sq = seq_of(a, n);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int kg = lane % KG, jc = warp * CPW + lane / KG, j = jc;
+  const int c0 = (int)crank * NC;  // this CTA's first value column
+  const int kg = lane % KG, jc = warp * CPW + lane / KG, j = c0 + jc;
   const bool live = j < a.Dv;
   const int key0 = kg * 32, kp0 = kg * KGS;
   const int kf = kg * RGS + fold_key<KG>(lane);  // this lane's folded sums in a reduction row
@@ -426,13 +453,13 @@ __global__ void __launch_bounds__(512, 1) k_dr_bwd(DrArgs a) {
   const int nblk = (sq.len + DR_TB - 1) / DR_TB;
   if (nblk > 0) {
     const int tl = (nblk - 1) * DR_TB;
-    issue_block<T, DK>(a, sq, hv, tl, sq.len - tl, 0, NC, raw0 + ((nblk - 1) & 1) * rawb, true);
+    issue_block<T, DK>(a, sq, hv, tl, sq.len - tl, c0, NC, raw0 + ((nblk - 1) & 1) * rawb, true);
   }
   cp_commit();
   for (int blk = nblk - 1; blk >= 0; --blk) {
     const int t0 = blk * DR_TB, nt = min(DR_TB, sq.len - t0);
     if (blk > 0)  // the previous block's copies overlap this block's work
-      issue_block<T, DK>(a, sq, hv, t0 - DR_TB, DR_TB, 0, NC, raw0 + ((blk - 1) & 1) * rawb, true);
+      issue_block<T, DK>(a, sq, hv, t0 - DR_TB, DR_TB, c0, NC, raw0 + ((blk - 1) & 1) * rawb, true);
     cp_commit();
     cp_wait1();
     __syncthreads();
@@ -536,13 +563,25 @@ __global__ void __launch_bounds__(512, 1) k_dr_bwd(DrArgs a) {
       const size_t row = (size_t)sq.b * a.T + sq.s + t0 + tt;
       if (kg == 0 && live) a.dv[(row * a.Hv + hv) * a.Dv + j] = bt * du;
       __syncthreads();
+      // this CTA's columns: the sum over its warps, for the peer as well
       const float* rb = s_red + (size_t)buf * nwarps * RS;
-      for (int e = threadIdx.x; e < NV * DK + 1; e += blockDim.x) {
+      float* xp = s_xp + buf * XS;
+      for (int e = threadIdx.x; e < NE; e += blockDim.x) {
+        const int re = e < NV * DK
+                           ? (e / DK) * DKR + ((e % DK) >> 5) * RGS + (e & 31)
+                           : NV * DKR + (e - NV * DK);
         float s = 0.0f;
+        for (int ww = 0; ww < nwarps; ++ww) s += rb[ww * RS + re];
+        xp[e] = s;
+      }
+      cluster_sync();
+      // the two halves' sums, added in rank order; the CTAs take alternate outputs
+      for (int e = 2 * threadIdx.x + (int)crank; e < NE; e += 2 * blockDim.x) {
+        const float s0 = crank == 0 ? xp[e] : ld_peer(xp + e, 0);
+        const float s1 = crank == 1 ? xp[e] : ld_peer(xp + e, 1);
+        const float s = s0 + s1;
         if (e < NV * DK) {
           const int vsel = e / DK, i = e % DK;
-          const int re = vsel * DKR + (i >> 5) * RGS + (i & 31);
-          for (int ww = 0; ww < nwarps; ++ww) s += rb[ww * RS + re];
           if (vsel == 0 || vsel == 1) {
             float* dst = vsel == 0 ? a.dq : a.dk;
             const size_t o = per_vhead ? (row * a.Hv + hv) * DK + i : (row * a.Hk + hk) * DK + i;
@@ -550,18 +589,15 @@ __global__ void __launch_bounds__(512, 1) k_dr_bwd(DrArgs a) {
           } else {
             a.dg[(row * a.Hv + hv) * DK + i] = s;
           }
-        } else {
-          float sb = 0.0f, sg = 0.0f;
-          for (int ww = 0; ww < nwarps; ++ww) {
-            sb += rb[ww * RS + NV * DKR];
-            sg += rb[ww * RS + NV * DKR + 1];
-          }
-          a.dbeta[row * a.Hv + hv] = sb;
-          if (!a.kda) a.dg[row * a.Hv + hv] = sg;
+        } else if (e == NV * DK) {
+          a.dbeta[row * a.Hv + hv] = s;
+        } else if (!a.kda) {
+          a.dg[row * a.Hv + hv] = s;
         }
       }
     }
   }
+  cluster_sync();  // the peer has read this CTA's last sums before either exits
   if (a.dh0 && live) {
 #pragma unroll
     for (int x = 0; x < 32; ++x) {
@@ -594,7 +630,8 @@ size_t bwd_smem(int KG, int nwarps, int kda) {
   const int RS = ((kda ? 3 : 2) * KG * RGS + 2 + 3) & ~3;
   const size_t raw = 2 * (size_t)DR_TB * DK * sizeof(T) + 2 * (size_t)DR_TB * NC * sizeof(T) +
                      (size_t)DR_TB * DK * 4 + DR_TB * 4;
-  return (size_t)(4 * DR_TB * KG * KGS + 2 * DR_TB * NC + 2 * DR_TB + 2 * nwarps * RS) *
+  const int XS = ((kda ? 3 : 2) * DK + 2 + 3) & ~3;
+  return (size_t)(4 * DR_TB * KG * KGS + 2 * DR_TB * NC + 2 * DR_TB + 2 * nwarps * RS + 2 * XS) *
              sizeof(float) + 2 * raw;
 }
 
@@ -665,7 +702,8 @@ cudaError_t launch_fwd_io(DrArgs& a, cudaStream_t st) {
 template <typename T, int KG>
 cudaError_t launch_bwd_t(DrArgs& a, float* ws, cudaStream_t st) {
   const int CPW = 32 / KG;
-  const int nwarps = (a.Dv + CPW - 1) / CPW;
+  const int half = (a.Dv + 1) / 2;  // columns per CTA of the pair
+  const int nwarps = (half + CPW - 1) / CPW;
   const size_t smem = bwd_smem<T>(KG, nwarps, a.kda);
   cudaError_t e = cudaFuncSetAttribute(k_dr_bwd<T, KG>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
@@ -677,7 +715,20 @@ cudaError_t launch_bwd_t(DrArgs& a, float* ws, cudaStream_t st) {
     a.dq = ws;
     a.dk = ws + per;
   }
-  k_dr_bwd<T, KG><<<(unsigned)((long)a.N * a.Hv), nwarps * 32, smem, st>>>(a);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(2L * a.N * a.Hv));
+  cfg.blockDim = dim3(nwarps * 32);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, k_dr_bwd<T, KG>, a);
+  if (e != cudaSuccess) return e;
   note_launches(1);
   e = cudaGetLastError();
   if (e != cudaSuccess || a.Hv == a.Hk) return e;
