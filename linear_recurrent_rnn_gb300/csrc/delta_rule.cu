@@ -403,7 +403,7 @@ __device__ __forceinline__ float warp_sum(float x) {
 // and the two CTAs through distributed shared memory (each CTA writes the outputs of half of
 // the sums, own + peer in rank order); both exchanges are double-buffered, so a token costs one
 // CTA barrier and one cluster barrier.
-template <typename T, int KG>
+template <typename T, int KG, int CL>
 __global__ void __launch_bounds__(256, 1) k_dr_bwd(DrArgs a) {
   constexpr int DK = 32 * KG, CPW = 32 / KG, DKP = KG * KGS, DKR = KG * RGS;
   const int nwarps = blockDim.x >> 5, NC = nwarps * CPW;
@@ -426,7 +426,7 @@ __global__ void __launch_bounds__(256, 1) k_dr_bwd(DrArgs a) {
   uint8_t* raw0 = reinterpret_cast<uint8_t*>(s_xp + 2 * XS);
   const size_t rawb = Raw<T, DK>::bytes(NC, true);
   const uint32_t crank = cluster_rank();
-  const int pid = blockIdx.x >> 1;
+  const int pid = blockIdx.x / CL;
   const int hv = pid % a.Hv, n = pid / a.Hv;
   const int hk = hv / (a.Hv / a.Hk);
   const Seq sq = seq_of(a, n);
@@ -575,11 +575,11 @@ __global__ void __launch_bounds__(256, 1) k_dr_bwd(DrArgs a) {
         xp[e] = s;
       }
       cluster_sync();
-      // the two halves' sums, added in rank order; the CTAs take alternate outputs
-      for (int e = 2 * threadIdx.x + (int)crank; e < NE; e += 2 * blockDim.x) {
-        const float s0 = crank == 0 ? xp[e] : ld_peer(xp + e, 0);
-        const float s1 = crank == 1 ? xp[e] : ld_peer(xp + e, 1);
-        const float s = s0 + s1;
+      // the CTAs' sums, added in rank order; the CTAs take outputs in turn
+      for (int e = CL * threadIdx.x + (int)crank; e < NE; e += CL * blockDim.x) {
+        float s = 0.0f;
+#pragma unroll
+        for (int r = 0; r < CL; ++r) s += (uint32_t)r == crank ? xp[e] : ld_peer(xp + e, (uint32_t)r);
         if (e < NV * DK) {
           const int vsel = e / DK, i = e % DK;
           if (vsel == 0 || vsel == 1) {
@@ -699,13 +699,15 @@ cudaError_t launch_fwd_io(DrArgs& a, cudaStream_t st) {
   }
 }
 
+constexpr int DR_CL = 2;  // CTAs per (sequence, head) in the backward (4 measured slower)
+
 template <typename T, int KG>
 cudaError_t launch_bwd_t(DrArgs& a, float* ws, cudaStream_t st) {
   const int CPW = 32 / KG;
-  const int half = (a.Dv + 1) / 2;  // columns per CTA of the pair
-  const int nwarps = (half + CPW - 1) / CPW;
+  const int part = (a.Dv + DR_CL - 1) / DR_CL;  // columns per CTA of the cluster
+  const int nwarps = (part + CPW - 1) / CPW;
   const size_t smem = bwd_smem<T>(KG, nwarps, a.kda);
-  cudaError_t e = cudaFuncSetAttribute(k_dr_bwd<T, KG>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  cudaError_t e = cudaFuncSetAttribute(k_dr_bwd<T, KG, DR_CL>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   float* dq = a.dq;
   float* dk = a.dk;
@@ -716,18 +718,18 @@ cudaError_t launch_bwd_t(DrArgs& a, float* ws, cudaStream_t st) {
     a.dk = ws + per;
   }
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)(2L * a.N * a.Hv));
+  cfg.gridDim = dim3((unsigned)((long)DR_CL * a.N * a.Hv));
   cfg.blockDim = dim3(nwarps * 32);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.x = DR_CL;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, k_dr_bwd<T, KG>, a);
+  e = cudaLaunchKernelEx(&cfg, k_dr_bwd<T, KG, DR_CL>, a);
   if (e != cudaSuccess) return e;
   note_launches(1);
   e = cudaGetLastError();
