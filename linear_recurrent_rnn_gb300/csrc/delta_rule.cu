@@ -167,7 +167,8 @@ __device__ void issue_block(const DrArgs& a, const Seq& sq, int hv, int t0, int 
 template <typename T, int DK>
 __device__ void prepare_block(const DrArgs& a, const uint8_t* raw, int NC, bool with_do,
                               float* s_k, float* s_q, float* s_a, float* s_ak, float* s_v,
-                              float* s_do, float* s_b, float* s_ag) {
+                              float* s_do, float* s_b, float* s_ag, float* s_aq = nullptr,
+                              float* s_kq = nullptr) {
   const T* rk = reinterpret_cast<const T*>(raw);
   const T* rq = rk + DR_TB * DK;
   const T* rv = rq + DR_TB * DK;
@@ -178,13 +179,25 @@ __device__ void prepare_block(const DrArgs& a, const uint8_t* raw, int NC, bool 
   for (int e = threadIdx.x; e < DR_TB * DK; e += blockDim.x) {
     const int tt = e / DK, i = e % DK;
     const int d = tt * DKP + (i >> 5) * KGS + (i & 31);
-    const float kv = to_f32<T>(rk[e]);
+    const float kv = to_f32<T>(rk[e]), qv = to_f32<T>(rq[e]);
     s_k[d] = kv;
-    s_q[d] = to_f32<T>(rq[e]);
+    s_q[d] = qv;
     if (a.kda) {
       const float av = expf(rg[e]);
       s_a[d] = av;
       s_ak[d] = av * kv;
+      if (s_aq) s_aq[d] = av * qv;
+    }
+  }
+  if (s_kq) {  // k . q of every token, one warp per token
+    const int nw = blockDim.x >> 5, lane = threadIdx.x & 31;
+    for (int tt = threadIdx.x >> 5; tt < DR_TB; tt += nw) {
+      float p = 0.0f;
+      for (int i = lane; i < DK; i += 32)
+        p = fmaf(to_f32<T>(rk[tt * DK + i]), to_f32<T>(rq[tt * DK + i]), p);
+#pragma unroll
+      for (int m = 16; m > 0; m >>= 1) p += __shfl_xor_sync(FULL, p, m);
+      if (lane == 0) s_kq[tt] = p;
     }
   }
   for (int e = threadIdx.x; e < DR_TB * NC; e += blockDim.x) {
@@ -255,18 +268,28 @@ __device__ __forceinline__ void fwd_token(float (&S)[32], const float* kr, const
   }
 }
 
+// Value columns per forward thread: two (sharing every shared-memory load of k and q, and
+// giving the thread two independent chains) except at Dk = 32, where a CTA would span more
+// columns than a head has.
+constexpr int fwd_cpt(int KG) { return KG == 1 ? 1 : 2; }
+// Columns of one forward CTA: 4 warps x (32 / KG) column slots x columns per thread.
+constexpr int fwd_cols(int KG) { return 4 * (32 / KG) * fwd_cpt(KG); }
+
 template <typename T, int KG>
 __global__ void __launch_bounds__(128) k_dr_fwd(DrArgs a) {
-  constexpr int DK = 32 * KG, CPW = 32 / KG, NC = 4 * CPW, DKP = KG * KGS;
+  constexpr int DK = 32 * KG, CPW = 32 / KG, CPT = fwd_cpt(KG), NH = 4 * CPW;
+  constexpr int NC = fwd_cols(KG), DKP = KG * KGS;
   extern __shared__ __align__(16) float sm[];
   float* s_k = sm;
   float* s_q = s_k + DR_TB * DKP;
   float* s_a = s_q + DR_TB * DKP;
   float* s_ak = s_a + DR_TB * DKP;
-  float* s_v = s_ak + DR_TB * DKP;
+  float* s_aq = s_ak + DR_TB * DKP;
+  float* s_v = s_aq + DR_TB * DKP;
   float* s_b = s_v + DR_TB * NC;
   float* s_ag = s_b + DR_TB;
-  uint8_t* raw0 = reinterpret_cast<uint8_t*>(s_ag + DR_TB);
+  float* s_kq = s_ag + DR_TB;
+  uint8_t* raw0 = reinterpret_cast<uint8_t*>(s_kq + DR_TB);
   const size_t rawb = Raw<T, DK>::bytes(NC, false);
   const int slice = blockIdx.x % a.nslices;
   const int hv = (blockIdx.x / a.nslices) % a.Hv;
@@ -274,19 +297,28 @@ __global__ void __launch_bounds__(128) k_dr_fwd(DrArgs a) {
   const Seq sq = seq_of(a, n);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int kg = lane % KG, jc = warp * CPW + lane / KG;
-  const int c0 = slice * NC, j = c0 + jc;
-  const bool live = j < a.Dv;
+  const int c0 = slice * NC;
+  int j[CPT];
+  bool live[CPT];
+#pragma unroll
+  for (int c = 0; c < CPT; ++c) {
+    j[c] = c0 + c * NH + jc;  // column c of this thread (c-th half of the CTA's columns)
+    live[c] = j[c] < a.Dv;
+  }
   const int key0 = kg * 32, kp0 = kg * KGS;  // first key, and its padded offset in a row
+  const size_t base = (size_t)n * a.Hv + hv;
 
-  float S[32];
+  float S[CPT][32];
 #pragma unroll
-  for (int x = 0; x < 32; ++x) S[x] = 0.0f;
-  if (a.h0 && live) {
-    const size_t base = (size_t)n * a.Hv + hv;
+  for (int c = 0; c < CPT; ++c) {
 #pragma unroll
-    for (int x = 0; x < 32; ++x)
-      S[x] = a.vfirst ? a.h0[(base * a.Dv + j) * DK + key0 + x]
-                      : a.h0[(base * DK + key0 + x) * a.Dv + j];
+    for (int x = 0; x < 32; ++x) S[c][x] = 0.0f;
+    if (a.h0 && live[c]) {
+#pragma unroll
+      for (int x = 0; x < 32; ++x)
+        S[c][x] = a.vfirst ? a.h0[(base * a.Dv + j[c]) * DK + key0 + x]
+                           : a.h0[(base * DK + key0 + x) * a.Dv + j[c]];
+    }
   }
   const int nblk = (sq.len + DR_TB - 1) / DR_TB;
   if (nblk > 0) issue_block<T, DK>(a, sq, hv, 0, min(DR_TB, sq.len), c0, NC, raw0, false);
@@ -300,45 +332,100 @@ __global__ void __launch_bounds__(128) k_dr_fwd(DrArgs a) {
     cp_wait1();
     __syncthreads();  // this block's copies have landed; the previous block is consumed
     prepare_block<T, DK>(a, raw0 + (blk & 1) * rawb, NC, false, s_k, s_q, s_a, s_ak, s_v,
-                         nullptr, s_b, s_ag);
+                         nullptr, s_b, s_ag, s_aq, s_kq);
     __syncthreads();
-    if (a.saved && live) {  // the state entering the block
-      float* dst = a.saved + (((size_t)(sq.slot0 + t0 / DR_TB) * a.Hv + hv) * a.Dv + j) * DK + key0;
+    if (a.saved) {  // the state entering the block
 #pragma unroll
-      for (int x = 0; x < 8; ++x)
-        reinterpret_cast<float4*>(dst)[x] = make_float4(S[4 * x], S[4 * x + 1], S[4 * x + 2], S[4 * x + 3]);
+      for (int c = 0; c < CPT; ++c) {
+        if (!live[c]) continue;
+        float* dst =
+            a.saved + (((size_t)(sq.slot0 + t0 / DR_TB) * a.Hv + hv) * a.Dv + j[c]) * DK + key0;
+#pragma unroll
+        for (int x = 0; x < 8; ++x)
+          reinterpret_cast<float4*>(dst)[x] =
+              make_float4(S[c][4 * x], S[c][4 * x + 1], S[c][4 * x + 2], S[c][4 * x + 3]);
+      }
     }
     for (int tt = 0; tt < nt; ++tt) {
-      float w, u;
-      fwd_token<KG>(S, s_k + tt * DKP + kp0, s_a + tt * DKP + kp0, s_ak + tt * DKP + kp0,
-                    a.kda != 0, s_ag[tt], s_b[tt], s_v[tt * NC + jc], w, u);
-      float qq[32];
-      ld32(s_q + tt * DKP + kp0, qq);
-      const float ov = a.scale * kg_sum<KG>(dot32(S, qq));
-      if (kg == 0 && live) {
+      // Both products read the state before the token: with S' = D S,
+      //   w = S'^T k,  u = beta (v - w),  S_t = S' + k u^T,
+      //   o = scale S_t^T q = scale (S'^T q + (k . q) u),
+      // so S'^T k and S'^T q of the thread's columns form one step of independent dot
+      // products over the same k and q registers.
+      const int r = tt * DKP + kp0;
+      const float bt = s_b[tt], kq = s_kq[tt];
+      float kk[32], pk[CPT], pq[CPT], ag = 1.0f;
+      ld32(s_k + r, kk);
+      if (a.kda) {
+        float ak[32], aq[32];
+        ld32(s_ak + r, ak);
+        ld32(s_aq + r, aq);
+#pragma unroll
+        for (int c = 0; c < CPT; ++c) {
+          pk[c] = dot32(S[c], ak);
+          pq[c] = dot32(S[c], aq);
+        }
+      } else {
+        float qq[32];
+        ld32(s_q + r, qq);
+        ag = s_ag[tt];
+#pragma unroll
+        for (int c = 0; c < CPT; ++c) {
+          pk[c] = ag * dot32(S[c], kk);
+          pq[c] = ag * dot32(S[c], qq);
+        }
+      }
+      float u[CPT];
+#pragma unroll
+      for (int c = 0; c < CPT; ++c) {
+        pk[c] = kg_sum<KG>(pk[c]);
+        pq[c] = kg_sum<KG>(pq[c]);
+        u[c] = bt * (s_v[tt * NC + c * NH + jc] - pk[c]);
+      }
+      if (a.kda) {
+        float al[32];
+        ld32(s_a + r, al);
+#pragma unroll
+        for (int c = 0; c < CPT; ++c)
+#pragma unroll
+          for (int x = 0; x < 32; ++x) S[c][x] = fmaf(al[x], S[c][x], kk[x] * u[c]);
+      } else {
+#pragma unroll
+        for (int c = 0; c < CPT; ++c)
+#pragma unroll
+          for (int x = 0; x < 32; ++x) S[c][x] = fmaf(ag, S[c][x], kk[x] * u[c]);
+      }
+      if (kg == 0) {
         const size_t row = (size_t)sq.b * a.T + sq.s + t0 + tt;
-        static_cast<T*>(a.o)[(row * a.Hv + hv) * a.Dv + j] = from_f32<T>(ov);
+#pragma unroll
+        for (int c = 0; c < CPT; ++c)
+          if (live[c])
+            static_cast<T*>(a.o)[(row * a.Hv + hv) * a.Dv + j[c]] =
+                from_f32<T>(a.scale * fmaf(kq, u[c], pq[c]));
       }
     }
   }
-  if (a.hT && live) {
-    const size_t base = (size_t)n * a.Hv + hv;
+  if (a.hT) {
 #pragma unroll
-    for (int x = 0; x < 32; ++x) {
-      if (a.vfirst)
-        a.hT[(base * a.Dv + j) * DK + key0 + x] = S[x];
-      else
-        a.hT[(base * DK + key0 + x) * a.Dv + j] = S[x];
+    for (int c = 0; c < CPT; ++c) {
+      if (!live[c]) continue;
+#pragma unroll
+      for (int x = 0; x < 32; ++x) {
+        if (a.vfirst)
+          a.hT[(base * a.Dv + j[c]) * DK + key0 + x] = S[c][x];
+        else
+          a.hT[(base * DK + key0 + x) * a.Dv + j[c]] = S[c][x];
+      }
     }
   }
 }
 
 template <typename T>
 size_t fwd_smem(int KG) {
-  const int DK = 32 * KG, NC = 4 * (32 / KG);
+  const int DK = 32 * KG, NC = fwd_cols(KG);
   const size_t raw = 2 * (size_t)DR_TB * DK * sizeof(T) + (size_t)DR_TB * NC * sizeof(T) +
                      (size_t)DR_TB * DK * 4 + DR_TB * 4;
-  return (size_t)(4 * DR_TB * KG * KGS + DR_TB * NC + 2 * DR_TB) * sizeof(float) + 2 * raw;
+  return (size_t)(5 * DR_TB * KG * KGS + DR_TB * NC + 3 * DR_TB) * sizeof(float) + 2 * raw;
 }
 
 // Sums 32 per-key values over the CPW columns of the warp with a halving butterfly: at level L
@@ -678,7 +765,7 @@ DrArgs dr_args(const delta_shape* s, int N, float scale, const void* q, const vo
 
 template <typename T, int KG>
 cudaError_t launch_fwd_t(DrArgs& a, cudaStream_t st) {
-  const int NC = 4 * (32 / KG);
+  const int NC = fwd_cols(KG);
   a.nslices = (a.Dv + NC - 1) / NC;
   const size_t smem = fwd_smem<T>(KG);
   cudaError_t e = cudaFuncSetAttribute(k_dr_fwd<T, KG>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
