@@ -667,9 +667,49 @@ __global__ void __maxnreg__(MAXREG)
           bwd_pass1<true, VARLEN>(tcol, xb0, xb1, dyb, gk, rmask, valid, ab, xr, sq, P, fB, S);
       }
 
-      // dx of tile it - 1: TMEM -> smem [token][channel] as bf16 (float32 goes straight to HBM).
+      if (have) s_agg[part * FUSED_K + j] = make_float4(P, fB, P, S);  // the part's maps
+      if (store_thread) tc::tma_store_wait_read0();  // the dx staging is free again
+      tc::named_bar(BAR_SCAN, NSCAN * 32);  // barrier A: the parts' maps, the dx staging
+      const int cp = pc, bp = pb;           // tile it - 1
+      float Fa = 1.0f, Fb = 0.0f, Rp = 1.0f, Rs = 0.0f, tP = 1.0f, tS = 0.0f;
+      const bool publish = (blk * ntiles + n) != p.drop_tile;
+      if (have) {
+        pc = c;
+        pb = b;
+        cur.next();
+        // The tiles processed alongside this one have published their aggregates by about now:
+        // ask again for the slots that were empty at the tile's start.
+        if (part == 0) lookback_refresh(lbq, lb_agg, (long)p.W, lb_n, lb_anchor);
+        // Entry-state map of this part (earlier parts composed) and carry map from the tile's
+        // right edge to this part (later parts composed).
+#pragma unroll
+        for (int pp = 0; pp < NPART; ++pp) {
+          if (pp < part) {
+            const float4 g = s_agg[pp * FUSED_K + j];
+            Fb = fmaf(g.x, Fb, g.y);
+            Fa *= g.x;
+          }
+        }
+#pragma unroll
+        for (int pp = NPART - 1; pp > 0; --pp) {
+          if (pp > part) {
+            const float4 g = s_agg[pp * FUSED_K + j];
+            Rs = fmaf(g.z, Rs, g.w);
+            Rp *= g.z;
+          }
+        }
+        // Part 0 owns the chunk's reverse carry: its map after the later parts' is the tile's,
+        // published at once.
+        const float4 g0 = s_agg[j];
+        tP = g0.z * Rp;
+        tS = fmaf(g0.z, Rs, g0.w);
+        if (part == 0 && publish) slot_put2(agg + cidx * p.W + w, tP, tS);
+      }
+
+      // dx of tile it - 1: TMEM -> smem [token][channel] as bf16 (float32 goes straight to HBM),
+      // here so that its MMAs have had pass 1 and the exchange to finish and the look-back round
+      // trip has this to overlap; before pass 2a, which reuses the dx columns.
       if (it > 0) {
-        const int cp = pc, bp = pb;
         const int validp = min(FUSED_C, p.T - cp * FUSED_C) - tb;
         ctl.wait(dx_full, (it - 1) & 1);
         tc::tc_fence_after();
@@ -691,48 +731,16 @@ __global__ void __maxnreg__(MAXREG)
           }
         }
         tc::tc_fence_before();
+        tc::fence_proxy_async_smem();  // the staging, for the TMA store after the next barrier
       }
-      if (have) s_agg[part * FUSED_K + j] = make_float4(P, fB, P, S);  // the part's maps
-      tc::fence_proxy_async_smem();
-      tc::named_bar(BAR_SCAN, NSCAN * 32);  // barrier A: part aggregates and the dx staging
-      if (it > 0 && store_thread && sizeof(GT) == 2) {
-        tc::tma_store_3d(&tm_dx, s_dx, blk * FUSED_K, pc * FUSED_C, pb);
-        tc::tma_store_commit();
-      }
-      if (!have) break;
-      pc = c;
-      pb = b;
-      cur.next();
-      // The tiles processed alongside this one have published their aggregates by about now:
-      // ask again for the slots that were empty at the tile's start.
-      if (part == 0) lookback_refresh(lbq, lb_agg, (long)p.W, lb_n, lb_anchor);
-
-      // Entry-state map of this part (earlier parts composed) and carry map from the tile's
-      // right edge to this part (later parts composed).
-      float Fa = 1.0f, Fb = 0.0f, Rp = 1.0f, Rs = 0.0f;
-#pragma unroll
-      for (int pp = 0; pp < NPART; ++pp) {
-        if (pp < part) {
-          const float4 g = s_agg[pp * FUSED_K + j];
-          Fb = fmaf(g.x, Fb, g.y);
-          Fa *= g.x;
+      if (!have) {
+        tc::named_bar(BAR_SCAN, NSCAN * 32);  // the last tile's dx staging is complete
+        if (it > 0 && store_thread && sizeof(GT) == 2) {
+          tc::tma_store_3d(&tm_dx, s_dx, blk * FUSED_K, cp * FUSED_C, bp);
+          tc::tma_store_commit();
         }
+        break;
       }
-#pragma unroll
-      for (int pp = NPART - 1; pp > 0; --pp) {
-        if (pp > part) {
-          const float4 g = s_agg[pp * FUSED_K + j];
-          Rs = fmaf(g.z, Rs, g.w);
-          Rp *= g.z;
-        }
-      }
-
-      // Part 0 owns the chunk's reverse carry: its map after the later parts' is the tile's,
-      // published at once.
-      const bool publish = (blk * ntiles + n) != p.drop_tile;
-      const float4 g0 = s_agg[j];
-      const float tP = g0.z * Rp, tS = fmaf(g0.z, Rs, g0.w);
-      if (part == 0 && publish) slot_put2(agg + cidx * p.W + w, tP, tS);
 
       // Pass 2a: h_{t-1} through the part, from the earlier parts' map applied to the tile's
       // entry state.
@@ -749,9 +757,12 @@ __global__ void __maxnreg__(MAXREG)
         if (c == 0 && p.dh0) p.dh0[(size_t)b * p.W + w] = p.canonical ? cout : 0.0f;
         s_cin[j] = cin;
       }
-      if (store_thread) tc::tma_store_wait_read0();  // dx staging free for the next iteration
-      tc::named_bar(BAR_SCAN, NSCAN * 32);                   // barrier B: the tile's right carry
-      const float cin = fmaf(Rp, s_cin[j], Rs);      // carry into this part from the right
+      tc::named_bar(BAR_SCAN, NSCAN * 32);  // barrier B: the tile's right carry, the dx staging
+      if (it > 0 && store_thread && sizeof(GT) == 2) {
+        tc::tma_store_3d(&tm_dx, s_dx, blk * FUSED_K, cp * FUSED_C, bp);
+        tc::tma_store_commit();
+      }
+      const float cin = fmaf(Rp, s_cin[j], Rs);  // carry into this part from the right
 
       // The dl buffers are free once the previous tile's MMAs are done.
       if (it > 0) ctl.wait(dl_empty, (it - 1) & 1);
