@@ -486,10 +486,11 @@ __device__ __forceinline__ float warp_sum(float x) {
 //   dS += scale q do^T;  dq = scale (S' + k u^T) do;  du = dS^T k;  dw = -beta du
 //   dk = dS u + S' dw;  dbeta = du . (v - w);  dv = beta du;  dS' = dS + k dw^T
 //   dg = <dS', S'> (GDN) or its row sums (KDA);  dS = D dS'
-// dq, dk (and KDA's dg) sum over the columns: warp butterfly, the warps through shared memory,
-// and the two CTAs through distributed shared memory (each CTA writes the outputs of half of
-// the sums, own + peer in rank order); both exchanges are double-buffered, so a token costs one
-// CTA barrier and one cluster barrier.
+// dq, dk (and KDA's dg) sum over the columns: warp butterfly, the warps through shared memory
+// (one CTA barrier per token), and the CTAs of the cluster through distributed shared memory
+// once per block: the sums feed only outputs, never the recurrence, so a block's per-token CTA
+// sums are kept and each CTA writes its share of the outputs, the CTAs' sums added in rank
+// order, after one cluster barrier.
 template <typename T, int KG, int CL>
 __global__ void __launch_bounds__(256, 1) k_dr_bwd(DrArgs a) {
   constexpr int DK = 32 * KG, CPW = 32 / KG, DKP = KG * KGS, DKR = KG * RGS;
@@ -509,8 +510,9 @@ __global__ void __launch_bounds__(256, 1) k_dr_bwd(DrArgs a) {
   float* s_ag = s_b + DR_TB;
   float* s_red = s_ag + DR_TB;       // [2][nwarps][RS]
   const int NE = NV * DK + 2, XS = (NE + 3) & ~3;
-  float* s_xp = s_red + 2 * nwarps * RS;  // [2][XS]: this CTA's sums, read by its peer too
-  uint8_t* raw0 = reinterpret_cast<uint8_t*>(s_xp + 2 * XS);
+  // [2 blocks][DR_TB tokens][XS]: this CTA's sums of a block, read by its peers too
+  float* s_xp = s_red + 2 * nwarps * RS;
+  uint8_t* raw0 = reinterpret_cast<uint8_t*>(s_xp + 2 * DR_TB * XS);
   const size_t rawb = Raw<T, DK>::bytes(NC, true);
   const uint32_t crank = cluster_rank();
   const int pid = blockIdx.x / CL;
@@ -650,9 +652,9 @@ __global__ void __launch_bounds__(256, 1) k_dr_bwd(DrArgs a) {
       const size_t row = (size_t)sq.b * a.T + sq.s + t0 + tt;
       if (kg == 0 && live) a.dv[(row * a.Hv + hv) * a.Dv + j] = bt * du;
       __syncthreads();
-      // this CTA's columns: the sum over its warps, for the peer as well
+      // this CTA's columns: the sum over its warps, kept for the block's exchange
       const float* rb = s_red + (size_t)buf * nwarps * RS;
-      float* xp = s_xp + buf * XS;
+      float* xp = s_xp + ((size_t)(blk & 1) * DR_TB + tt) * XS;
       for (int e = threadIdx.x; e < NE; e += blockDim.x) {
         const int re = e < NV * DK
                            ? (e / DK) * DKR + ((e % DK) >> 5) * RGS + (e & 31)
@@ -661,26 +663,30 @@ __global__ void __launch_bounds__(256, 1) k_dr_bwd(DrArgs a) {
         for (int ww = 0; ww < nwarps; ++ww) s += rb[ww * RS + re];
         xp[e] = s;
       }
-      cluster_sync();
-      // the CTAs' sums, added in rank order; the CTAs take outputs in turn
-      for (int e = CL * threadIdx.x + (int)crank; e < NE; e += CL * blockDim.x) {
-        float s = 0.0f;
+    }
+    // The block's outputs: the CTAs' sums, added in rank order; the CTAs take outputs in turn.
+    cluster_sync();
+    const float* xb = s_xp + (size_t)(blk & 1) * DR_TB * XS;
+    for (int f = CL * threadIdx.x + (int)crank; f < nt * NE; f += CL * blockDim.x) {
+      const int tt = f / NE, e = f % NE;
+      float s = 0.0f;
 #pragma unroll
-        for (int r = 0; r < CL; ++r) s += (uint32_t)r == crank ? xp[e] : ld_peer(xp + e, (uint32_t)r);
-        if (e < NV * DK) {
-          const int vsel = e / DK, i = e % DK;
-          if (vsel == 0 || vsel == 1) {
-            float* dst = vsel == 0 ? a.dq : a.dk;
-            const size_t o = per_vhead ? (row * a.Hv + hv) * DK + i : (row * a.Hk + hk) * DK + i;
-            dst[o] = s;
-          } else {
-            a.dg[(row * a.Hv + hv) * DK + i] = s;
-          }
-        } else if (e == NV * DK) {
-          a.dbeta[row * a.Hv + hv] = s;
-        } else if (!a.kda) {
-          a.dg[row * a.Hv + hv] = s;
+      for (int r = 0; r < CL; ++r)
+        s += (uint32_t)r == crank ? xb[tt * XS + e] : ld_peer(xb + tt * XS + e, (uint32_t)r);
+      const size_t row = (size_t)sq.b * a.T + sq.s + t0 + tt;
+      if (e < NV * DK) {
+        const int vsel = e / DK, i = e % DK;
+        if (vsel == 0 || vsel == 1) {
+          float* dst = vsel == 0 ? a.dq : a.dk;
+          const size_t o = per_vhead ? (row * a.Hv + hv) * DK + i : (row * a.Hk + hk) * DK + i;
+          dst[o] = s;
+        } else {
+          a.dg[(row * a.Hv + hv) * DK + i] = s;
         }
+      } else if (e == NV * DK) {
+        a.dbeta[row * a.Hv + hv] = s;
+      } else if (!a.kda) {
+        a.dg[row * a.Hv + hv] = s;
       }
     }
   }
@@ -718,8 +724,8 @@ size_t bwd_smem(int KG, int nwarps, int kda) {
   const size_t raw = 2 * (size_t)DR_TB * DK * sizeof(T) + 2 * (size_t)DR_TB * NC * sizeof(T) +
                      (size_t)DR_TB * DK * 4 + DR_TB * 4;
   const int XS = ((kda ? 3 : 2) * DK + 2 + 3) & ~3;
-  return (size_t)(4 * DR_TB * KG * KGS + 2 * DR_TB * NC + 2 * DR_TB + 2 * nwarps * RS + 2 * XS) *
-             sizeof(float) + 2 * raw;
+  return (size_t)(4 * DR_TB * KG * KGS + 2 * DR_TB * NC + 2 * DR_TB + 2 * nwarps * RS +
+                  2 * DR_TB * XS) * sizeof(float) + 2 * raw;
 }
 
 }  // namespace
