@@ -410,10 +410,28 @@ def delta_rule_measure(flush, peak, reps=10):
             torch.cuda.synchronize()
             acc.append(a.elapsed_time(b))
     fms, bms = statistics.median(tf), statistics.median(tb)
+    # the E4M3 state quantize-dequantize (64-column tiles), in place on the saved block states
+    # seen as float32 [n, 128, 128] states: read and written once, against HBM
+    st = saved.view(torch.float32).view(-1, wl.Dk, wl.Dv)
+    tq = []
+    for _ in range(reps):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        R.delta_rule_state_fp8_qdq(st, st, 64)
+        b.record()
+        torch.cuda.synchronize()
+        tq.append(a.elapsed_time(b))
+    qms = statistics.median(tq)
+    qbytes = 2 * st.numel() * 4
     elems = wl.B * wl.T * wl.Hv * wl.Dk * wl.Dv
     out = {"workload": f"{wl.name} GDN bf16 (q, k unit length, exp(g) U[0.8, 1), beta U(0, 1))",
            "fwd_ms": fms, "bwd_ms": bms, "tokens_per_s": wl.B * wl.T / ((fms + bms) / 1e3),
-           "saved_bytes": saved.numel()}
+           "saved_bytes": saved.numel(),
+           "state_fp8_qdq": {"states": st.shape[0], "ms": qms, "bound": "hbm", "unit": "GB/s",
+                             "achieved": qbytes / (qms / 1e3) / 1e9, "peak": peak,
+                             "frac": (qbytes / (qms / 1e3) / 1e9 / peak) if peak else None,
+                             "algorithmic_bytes": qbytes}}
     for name, flop, ms in (("fwd", 7 * elems, fms), ("bwd", 22 * elems, bms)):
         tf_s = flop / (ms / 1e3) / 1e12
         out[f"roofline_{name}"] = {"bound": "alu", "unit": "TFLOP/s", "achieved": tf_s,

@@ -76,6 +76,15 @@ rglru_status delta_rule_backward(const delta_shape *shape, const void *q, const 
                                  float *dq, float *dk, float *dv, float *dg, float *dbeta,
                                  float *dh0, void *workspace, rglru_stream stream);
 
+/* FP8 (E4M3) quantize-dequantize of float32 key-first states [n_states][Dk][Dv] [P3 "FP8
+ * state" entry: dynamic E4M3 QDQ, one scale per [Dk, block_v] tile, an all-zero tile with
+ * scale one, partial value tiles valid; its gradient is the identity]: per tile amax, scale =
+ * amax / 448 (1 if amax is 0), each value replaced by code * scale with code the E4M3 value
+ * nearest value / scale (ties to even, saturating at +-448), all in float32.  out may equal
+ * state (in place).  Any n_states, Dk, Dv, block_v >= 1. */
+rglru_status delta_rule_state_fp8_qdq(const float *state, float *out, int64_t n_states,
+                                      int Dk, int Dv, int block_v, rglru_stream stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -23,6 +23,9 @@
 //             halving butterfly of shuffles and the warps through shared memory.
 #include <algorithm>
 
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
+
 #include "common.cuh"
 #include "internal.h"
 #include "delta_rule.h"
@@ -717,6 +720,43 @@ __global__ void k_dr_group_sum(const float* ws, float* out, size_t rows, int Hk,
   }
 }
 
+// FP8 (E4M3) quantize-dequantize of key-first states [n][Dk][Dv], one scale per [Dk, block_v]
+// tile: amax over the tile, scale = amax / 448 (1 for an all-zero tile), each value replaced
+// by its E4M3 code (nearest, ties to even, saturating at 448) of value / scale, times scale.
+// The scale, the division and the product are IEEE float32 operations, so the codes are the
+// ones a float32 reference picks.  CTA = (state, tile), 8 warps over the tile's rows, lanes
+// over its columns (coalesced row segments); the second pass re-reads the tile from L2.
+__device__ __forceinline__ float qdq_e4m3(float x, float scale) {
+  const __nv_fp8_storage_t q = __nv_cvt_float_to_fp8(__fdiv_rn(x, scale), __NV_SATFINITE, __NV_E4M3);
+  const __half_raw h = __nv_cvt_fp8_to_halfraw(q, __NV_E4M3);
+  return __fmul_rn(__half2float(__half(h)), scale);
+}
+__global__ void __launch_bounds__(256) k_state_qdq(const float* st, float* out, int Dk, int Dv,
+                                                 int block_v, int ntiles) {
+  __shared__ float s_amax[8];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const size_t state = blockIdx.x / ntiles;
+  const int v0 = (int)(blockIdx.x % ntiles) * block_v;
+  const int bw = min(block_v, Dv - v0);
+  const size_t base = state * (size_t)Dk * Dv + v0;
+  float m = 0.0f;
+  for (int i = warp; i < Dk; i += 8)
+    for (int c = lane; c < bw; c += 32) m = fmaxf(m, fabsf(st[base + (size_t)i * Dv + c]));
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(FULL, m, o));
+  if (lane == 0) s_amax[warp] = m;
+  __syncthreads();
+  float amax = 0.0f;
+#pragma unroll
+  for (int w = 0; w < 8; ++w) amax = fmaxf(amax, s_amax[w]);
+  const float scale = amax > 0.0f ? __fdiv_rn(amax, 448.0f) : 1.0f;
+  for (int i = warp; i < Dk; i += 8)
+    for (int c = lane; c < bw; c += 32) {
+      const size_t e = base + (size_t)i * Dv + c;
+      out[e] = qdq_e4m3(st[e], scale);
+    }
+}
+
 template <typename T>
 size_t bwd_smem(int KG, int nwarps, int kda) {
   const int DK = 32 * KG, NC = nwarps * (32 / KG);
@@ -909,4 +949,17 @@ extern "C" rglru_status delta_rule_backward(const delta_shape* s, const void* q,
   const cudaError_t e = s->io == RGLRU_BF16 ? launch_bwd_io<bf16>(a, ws, stream)
                                             : launch_bwd_io<float>(a, ws, stream);
   return cuda_status(e);
+}
+
+extern "C" rglru_status delta_rule_state_fp8_qdq(const float* state, float* out,
+                                                 int64_t n_states, int Dk, int Dv, int block_v,
+                                                 rglru_stream stream) {
+  if (n_states < 1 || Dk < 1 || Dv < 1 || block_v < 1 || !req(state) || !req(out))
+    return RGLRU_ERR_INVALID_ARG;
+  const long ntiles = (Dv + block_v - 1) / block_v;
+  const long grid = n_states * ntiles;
+  if (grid > 0x7fffffffL) return RGLRU_ERR_UNSUPPORTED;
+  k_state_qdq<<<(unsigned)grid, 256, 0, stream>>>(state, out, Dk, Dv, block_v, (int)ntiles);
+  note_launches(1);
+  return cuda_status(cudaGetLastError());
 }

@@ -56,7 +56,7 @@ EXPORTS = ("rglru_status_string", "rglru_saved_bytes", "rglru_workspace_bytes",
            "rglru_debug_lookback", "rglru_kernel_launches", "rglru_forward_noalloc",
            "rglru_debug_kernel_events", "rglru_step", "rglru_fused_forward_varlen",
            "rglru_fused_backward_varlen", "delta_rule_saved_bytes", "delta_rule_workspace_bytes",
-           "delta_rule_forward", "delta_rule_backward")
+           "delta_rule_forward", "delta_rule_backward", "delta_rule_state_fp8_qdq")
 
 # Static look-back scratch of rglru_forward_noalloc, per GPU (RGLRU_NOALLOC_SCRATCH_BYTES).
 NOALLOC_SCRATCH_BYTES = 16 << 20
@@ -109,6 +109,9 @@ def lib():
                                              [P] * 5)
             L.delta_rule_backward.argtypes = ([DS] + [P] * 5 + [ctypes.c_float, P, ctypes.c_int32] +
                                               [P] * 12)
+            L.delta_rule_state_fp8_qdq.argtypes = [P, P, ctypes.c_int64, ctypes.c_int, ctypes.c_int,
+                                              ctypes.c_int, P]
+            L.delta_rule_state_fp8_qdq.restype = ctypes.c_int
             L.delta_rule_forward.restype = ctypes.c_int
             L.delta_rule_backward.restype = ctypes.c_int
             L.rglru_kernel_launches.argtypes = []
@@ -297,3 +300,11 @@ def delta_rule_backward(shape, q, k, v, g, beta, scale, cu_seqlens, num_seqs, h0
         ctypes.byref(shape), _p(q), _p(k), _p(v), _p(g), _p(beta), ctypes.c_float(scale),
         _p(cu_seqlens), int(num_seqs), _p(h0), _p(saved), _p(do), _p(dhT), _p(dq), _p(dk),
         _p(dv), _p(dg), _p(dbeta), _p(dh0), _p(workspace), _stream(stream)))
+
+
+def delta_rule_state_fp8_qdq(state, out, block_v=64, stream=None):
+    """E4M3 quantize-dequantize of float32 key-first states [..., Dk, Dv] (out may be state)."""
+    Dk, Dv = state.shape[-2], state.shape[-1]
+    n = state.numel() // (Dk * Dv)
+    _check("delta_rule_state_fp8_qdq", lib().delta_rule_state_fp8_qdq(
+        _p(state), _p(out), int(n), int(Dk), int(Dv), int(block_v), _stream(stream)))

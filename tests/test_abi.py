@@ -26,7 +26,7 @@ def declared_functions():
     names = set()
     for h in HEADERS:
         src = re.sub(r"/\*.*?\*/", "", open(h).read(), flags=re.S)
-        names |= set(re.findall(r"\b((?:rglru|delta_rule)_[a-z_]+)\s*\(", src))
+        names |= set(re.findall(r"\b((?:rglru|delta_rule)_[a-z0-9_]+)\s*\(", src))
     return sorted(names)
 
 
@@ -157,3 +157,13 @@ def test_delta_rule_sizes_and_host_validation(lib):
     assert fwd(R.make_delta_shape(2, 64, 3, 4, 64, 32)) == R.ERR_INVALID_ARG   # Hv % Hk
     assert fwd(R.make_delta_shape(2, 64, 2, 4, 96, 32)) == R.ERR_UNSUPPORTED   # Dk 96
     assert fwd(R.make_delta_shape(2, 64, 2, 4, 64, 12)) == R.ERR_UNSUPPORTED   # 24-byte v rows
+
+
+def test_state_qdq_host_validation(lib):
+    A = 1 << 20
+    P = lambda v: None if v is None else ctypes.c_void_p(v)
+    q = lambda st=A, out=A, n=2, dk=8, dv=8, bv=4: lib.delta_rule_state_fp8_qdq(P(st), P(out), n, dk, dv, bv, None)
+    assert q(st=None) == R.ERR_INVALID_ARG
+    assert q(out=A + 4) == R.ERR_INVALID_ARG
+    assert q(n=0) == R.ERR_INVALID_ARG
+    assert q(bv=0) == R.ERR_INVALID_ARG
