@@ -424,10 +424,32 @@ def delta_rule_measure(flush, peak, reps=10):
         tq.append(a.elapsed_time(b))
     qms = statistics.median(tq)
     qbytes = 2 * st.numel() * 4
+    # decode: one token per sequence from states carried in place (T = 1), batch 1 and 64
+    dec = {}
+    for Bd in (1, 64):
+        dsh = R.make_delta_shape(Bd, 1, wl.Hk, wl.Hv, wl.Dk, wl.Dv, R.BF16)
+        tok = {n: d[n][:1, :1].expand(Bd, 1, *d[n].shape[2:]).contiguous()
+               for n in ("q", "k", "v", "g", "beta")}
+        hs = torch.zeros(Bd, wl.Hv, wl.Dk, wl.Dv, device="cuda")
+        od = torch.empty_like(tok["v"])
+        step = lambda: R.delta_rule_forward(dsh, tok["q"], tok["k"], tok["v"], tok["g"],
+                                            tok["beta"], scale, None, Bd, hs, od, hs, None)
+        for _ in range(3):
+            step()
+        td = []
+        for _ in range(reps):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            step()
+            b.record()
+            torch.cuda.synchronize()
+            td.append(a.elapsed_time(b))
+        dec[f"us_per_step_B{Bd}"] = statistics.median(td) * 1e3
     elems = wl.B * wl.T * wl.Hv * wl.Dk * wl.Dv
     out = {"workload": f"{wl.name} GDN bf16 (q, k unit length, exp(g) U[0.8, 1), beta U(0, 1))",
            "fwd_ms": fms, "bwd_ms": bms, "tokens_per_s": wl.B * wl.T / ((fms + bms) / 1e3),
-           "saved_bytes": saved.numel(),
+           "saved_bytes": saved.numel(), "decode": dec,
            "state_fp8_qdq": {"states": st.shape[0], "ms": qms, "bound": "hbm", "unit": "GB/s",
                              "achieved": qbytes / (qms / 1e3) / 1e9, "peak": peak,
                              "frac": (qbytes / (qms / 1e3) / 1e9 / peak) if peak else None,

@@ -58,7 +58,8 @@ size_t delta_rule_workspace_bytes(const delta_shape *shape);
 
 /* Forward: o (shape.io) and, if hT is not NULL, the final states (float32) from the initial
  * states h0 (NULL = zeros).  `saved` (delta_rule_saved_bytes, may be NULL when no backward
- * follows) receives the block states for the backward.  cu_seqlens NULL: num_seqs must be B. */
+ * follows) receives the block states for the backward.  cu_seqlens NULL: num_seqs must be B.
+ * hT may equal h0 (states carried in place), which with T = 1 is a decode step. */
 rglru_status delta_rule_forward(const delta_shape *shape, const void *q, const void *k,
                                 const void *v, const float *g, const float *beta, float scale,
                                 const int32_t *cu_seqlens, int32_t num_seqs, const float *h0,

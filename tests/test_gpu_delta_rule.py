@@ -119,3 +119,29 @@ def test_delta_rule_full_size_sampled_heads():
         for n in ("dq", "dk", "dv", "dg", "dbeta"):
             check(n, got[n][b:b + 1, :, h:h + 1], ref[n], 1e-3)
         check("dh0", got["dh0"][b:b + 1, h:h + 1], ref["dh0"], 1e-3)
+
+
+def test_decode_loop_reproduces_forward():
+    """T = 1 calls with the states carried in place (hT = h0) reproduce the forward over the
+    whole sequence, token by token (same float32 arithmetic per token: equal to rounding)."""
+    wl = DeltaWorkload("dec", 2, 24, 2, 4, 64, 64, "f32", kda=True, h0_std=0.5)
+    inp = generate(wl, 21)
+    d = {n: (t.cuda() if isinstance(t, torch.Tensor) else t) for n, t in inp.items()}
+    scale = wl.Dk ** -0.5
+    full = R.make_delta_shape(wl.B, wl.T, wl.Hk, wl.Hv, wl.Dk, wl.Dv, R.F32, True)
+    o = torch.empty_like(d["v"])
+    hT = torch.empty_like(d["h0"])
+    R.delta_rule_forward(full, d["q"], d["k"], d["v"], d["g"], d["beta"], scale, None, wl.B,
+                         d["h0"], o, hT, None)
+    one = R.make_delta_shape(wl.B, 1, wl.Hk, wl.Hv, wl.Dk, wl.Dv, R.F32, True)
+    h = d["h0"].clone()
+    outs = []
+    for t in range(wl.T):
+        sl = lambda x: x[:, t:t + 1].contiguous()
+        ot = torch.empty_like(sl(d["v"]))
+        R.delta_rule_forward(one, sl(d["q"]), sl(d["k"]), sl(d["v"]), sl(d["g"]), sl(d["beta"]),
+                             scale, None, wl.B, h, ot, h, None)
+        outs.append(ot)
+    torch.cuda.synchronize()
+    check("o", torch.cat(outs, 1).cpu().double().numpy(), o.cpu().double().numpy(), 1e-5)
+    check("hT", h.cpu().double().numpy(), hT.cpu().double().numpy(), 1e-5)
