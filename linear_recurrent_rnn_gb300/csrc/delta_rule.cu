@@ -10,17 +10,20 @@
 //
 // Geometry: the state lives in registers.  A thread owns 32 keys of one value column, so a
 // column is shared by KG = Dk / 32 adjacent lanes (lane = column-in-warp * KG + key group) and
-// S'^T k, S^T q are a 32-term dot product per thread plus log2(KG) shuffles.  Token data (k, q,
-// decays, beta, v) is staged in shared memory as float32 a block of tokens at a time and read
-// by every thread as broadcast 16-byte loads.
-//   forward:  CTA = (sequence, value head, slice of 4 x 32 / KG columns), 4 warps; the state
-//             entering every 16-token block is saved (float32, [slot][Hv][Dv][Dk]) for the
-//             backward.
-//   backward: CTA = (sequence, value head), all Dv columns; per 16-token block in reverse it
-//             restores the block's entry state, runs the block forward again keeping each
-//             token's state in thread-local memory, and then runs the reverse recurrence.  The
-//             sums over value columns (dq, dk, KDA's dg) fold the warp's columns with a
-//             halving butterfly of shuffles and the warps through shared memory.
+// S'^T k, S'^T q are 32-term dot products per thread plus log2(KG) shuffles.  Token data (k, q,
+// decays, beta, v) comes in by asynchronous copies a block of 16 tokens ahead, is converted in
+// shared memory to float32 rows with padded 32-key groups, and is read by every thread as
+// broadcast 16-byte loads.
+//   forward:  CTA = (sequence, value head, 2 x 4 x 32 / KG columns), 4 warps, two value
+//             columns per thread (one at Dk = 32) sharing the k / q loads; the state entering
+//             every 16-token block is saved (float32, [slot][Hv][Dv][Dk]) for the backward.
+//   backward: a cluster of two CTAs per (sequence, value head), half of the Dv columns each;
+//             per 16-token block in reverse it restores the block's entry state, runs the
+//             block forward again keeping each token's state in thread-local memory, and then
+//             runs the reverse recurrence.  The sums over value columns (dq, dk, KDA's dg) fold
+//             the warp's columns with a halving butterfly of shuffles, the warps through shared
+//             memory, and the two CTAs through distributed shared memory once per block.
+//   k_state_qdq: the E4M3 quantize-dequantize of states, one scale per [Dk, block_v] tile.
 #include <algorithm>
 
 #include <cuda_fp16.h>
