@@ -145,3 +145,45 @@ def test_decode_loop_reproduces_forward():
     torch.cuda.synchronize()
     check("o", torch.cat(outs, 1).cpu().double().numpy(), o.cpu().double().numpy(), 1e-5)
     check("hT", h.cpu().double().numpy(), hT.cpu().double().numpy(), 1e-5)
+
+
+def _padded(shape, dtype, pad=256, fill=12345.0):
+    """A tensor view of `shape` inside a buffer with `pad` canary elements on both sides."""
+    n = int(np.prod(shape))
+    buf = torch.full((n + 2 * pad,), fill, dtype=dtype, device="cuda")
+    return buf, buf[pad:pad + n].view(shape)
+
+
+def test_outputs_stay_in_bounds_and_runs_are_bitwise_equal():
+    """Every output of the forward and the backward lives inside a buffer padded with canary
+    values on both sides (packed sequences with an empty one, grouped heads, KDA, ragged Dv);
+    no canary may change, and a second run must give bitwise the same outputs (fixed-order
+    sums, including the cluster's rank-ordered exchange)."""
+    wl = DeltaWorkload("cn", 1, 70, 2, 4, 64, 40, "f32", kda=True, h0_std=0.5,
+                       lengths=(30, 0, 17, 23))
+    inp = generate(wl, 31)
+    d = {n: (t.cuda() if isinstance(t, torch.Tensor) else t) for n, t in inp.items()}
+    N = 4
+    sh = R.make_delta_shape(wl.B, wl.T, wl.Hk, wl.Hv, wl.Dk, wl.Dv, R.F32, True)
+    scale = wl.Dk ** -0.5
+    runs = []
+    for _ in range(2):
+        bufs, outs = {}, {}
+        for n, shape in (("o", d["v"].shape), ("hT", (N, wl.Hv, wl.Dk, wl.Dv)),
+                         ("dq", d["q"].shape), ("dk", d["k"].shape), ("dv", d["v"].shape),
+                         ("dg", d["g"].shape), ("dbeta", d["beta"].shape),
+                         ("dh0", (N, wl.Hv, wl.Dk, wl.Dv))):
+            bufs[n], outs[n] = _padded(shape, torch.float32)
+        saved = torch.empty(R.delta_rule_saved_bytes(sh, N), dtype=torch.uint8, device="cuda")
+        ws = torch.empty(max(1, R.delta_rule_workspace_bytes(sh)), dtype=torch.uint8, device="cuda")
+        R.delta_rule_forward(sh, d["q"], d["k"], d["v"], d["g"], d["beta"], scale,
+                             d["cu_seqlens"], N, d["h0"], outs["o"], outs["hT"], saved)
+        R.delta_rule_backward(sh, d["q"], d["k"], d["v"], d["g"], d["beta"], scale,
+                              d["cu_seqlens"], N, d["h0"], saved, d["do"], d["dhT"], outs["dq"],
+                              outs["dk"], outs["dv"], outs["dg"], outs["dbeta"], outs["dh0"], ws)
+        torch.cuda.synchronize()
+        for n, b in bufs.items():
+            assert torch.all(b[:256] == 12345.0) and torch.all(b[-256:] == 12345.0), n
+        runs.append({n: t.clone() for n, t in outs.items()})
+    for n in runs[0]:
+        assert torch.equal(runs[0][n], runs[1][n]), n
