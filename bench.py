@@ -492,10 +492,48 @@ def cpu_baseline(wl, T=2048, min_seconds=10.0):
         dt = time.perf_counter() - t0
         if dt >= min_seconds:
             break
-    return {"value": reps * ws.B * ws.T / dt, "unit": UNIT, "cores": cpu_cores(),
-            "kind": "oracle",
+    out = {"value": reps * ws.B * ws.T / dt, "unit": UNIT, "cores": cpu_cores(),
+           "kind": "oracle",
+           "sample": f"B1 T{T} W{wl.W} (all {wl.nblk} blocks) fused fwd+bwd, float64, "
+                     f"{reps} repetitions in {dt:.1f} s",
+           "cpu_model": cpu_model()}
+    out["single_thread"] = cpu_baseline_single_thread(wl)
+    return out
+
+
+def cpu_model():
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.lower().startswith(("model name", "cpu model", "hardware")):
+                return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    import platform
+    return platform.processor() or platform.machine()
+
+
+def cpu_baseline_single_thread(wl, T=512):
+    """The same oracle on one thread (a subprocess with OMP_NUM_THREADS=1), on a smaller
+    sample (T tokens of batch row 0, all channels), timed once after a warm-up call."""
+    code = (
+        "import sys, time, json; sys.path.insert(0, %r)\n"
+        "import bench\n"
+        "from linear_recurrent_rnn_gb300.inputs import generate\n"
+        "wl = bench.workload().scaled(B=1, T=%d)\n"
+        "inp = generate(wl, 2)\n"
+        "bench.oracle_step(wl, inp)\n"
+        "t0 = time.perf_counter(); bench.oracle_step(wl, inp); dt = time.perf_counter() - t0\n"
+        "print(json.dumps({'value': wl.T / dt, 'seconds': dt}))\n" % (ROOT, T))
+    env = dict(os.environ, OMP_NUM_THREADS="1")
+    try:
+        r = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True,
+                           timeout=300)
+        res = json.loads(r.stdout.strip().splitlines()[-1])
+    except Exception as e:  # reported, not fatal: the multi-core figure is the baseline
+        return {"error": str(e)[:200]}
+    return {"value": res["value"], "unit": UNIT, "cores": 1,
             "sample": f"B1 T{T} W{wl.W} (all {wl.nblk} blocks) fused fwd+bwd, float64, "
-                      f"{reps} repetitions in {dt:.1f} s"}
+                      f"one call in {res['seconds']:.1f} s"}
 
 
 def run_reference(args, rank, world):
