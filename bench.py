@@ -304,6 +304,8 @@ def run_ours(args, rank, world, local):
         line["cpu_baseline"] = cpu_baseline(wl, T=args.cpu_sample_T)
     if rank == 0 and world == 1 and not args.no_decode:
         line["decode"] = decode_step(flush, peak)
+    if rank == 0 and world == 1 and not args.no_varlen:
+        line["varlen"] = varlen_measure(flush, peak)
     if rank == 0 and world == 1 and not args.no_delta:
         line["delta_rule"] = delta_rule_measure(flush, peak)
     if rank == 0:
@@ -361,6 +363,77 @@ def decode_step(flush, peak, W=2048, k=128, reps=20):
                                     "frac": (gbs / peak) if peak else None,
                                     "algorithmic_bytes": nbytes}
     return out
+
+
+def varlen_measure(flush, peak, reps=10, W=2048, k=128, T=8192, seed=5):
+    """Packed variable-length sequences (rglru_fused_forward_varlen / _backward_varlen): the
+    headline's 8192 tokens in one row, sequence lengths drawn U[1, 2048] until the row is full
+    (the last one truncated), each sequence with its own float32 initial state N(0, 0.5^2) and
+    final-state gradient; bf16, canonical.  Milliseconds per call (L2 flushed before each),
+    tokens/s of the pair, and the backward kernel's algorithmic bytes (the headline's, plus
+    h0, dhT read and dh0 written per sequence) against the measured copy bandwidth."""
+    import numpy as np
+    import torch
+    from linear_recurrent_rnn_gb300 import librglru as R
+    from linear_recurrent_rnn_gb300.inputs import Workload, generate, packed_lengths
+    lengths = packed_lengths(seed, T, 1, 2048)
+    S = len(lengths)
+    rng = np.random.default_rng(seed + 1)
+    wl = Workload("varlen", 1, T, W, k, "bf16", "canonical", (0.9, 0.999))
+    inp = generate(wl, seed)
+    d = {n: v.cuda() for n, v in inp.items() if isinstance(v, torch.Tensor)}
+    cu = torch.tensor(np.concatenate([[0], np.cumsum(lengths)]), dtype=torch.int32).cuda()
+    h0 = (torch.from_numpy(rng.standard_normal((S, W))).float() * 0.5).cuda()
+    dhT = torch.from_numpy(rng.standard_normal((S, W))).float().cuda()
+    sh = R.make_shape(1, T, W, W // k, R.BF16, R.BF16, R.CANONICAL)
+    y = torch.empty_like(d["x"])
+    hT = torch.empty(S, W, device="cuda")
+    saved, ws = R.alloc_saved(sh), R.alloc_workspace(sh)
+    dx = torch.empty_like(d["x"])
+    dWa = torch.empty(W // k, k, k, device="cuda")
+    dWx = torch.empty_like(dWa)
+    dba, dbx, dL = (torch.empty(W, device="cuda") for _ in range(3))
+    dh0 = torch.empty(S, W, device="cuda")
+    ba, bx = d["ba"], d["bx"]
+    fwd = lambda: R.rglru_fused_forward_varlen(sh, d["x"], d["Wa"], ba, d["Wx"], bx, d["Lambda"],
+                                               cu, S, h0, y, hT, saved)
+    bwd = lambda: R.rglru_fused_backward_varlen(sh, d["dy"], dhT, d["x"], d["Wa"], ba, d["Wx"],
+                                                bx, d["Lambda"], cu, S, h0, saved, dx, dWa, dba,
+                                                dWx, dbx, dL, dh0, ws)
+    for _ in range(3):
+        fwd()
+        bwd()
+    tf, tb, tk = [], [], []
+    for _ in range(reps):
+        for fn, acc in ((fwd, tf), (bwd, tb)):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            ka, kb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            if fn is bwd:
+                ka.record()  # creates the events
+                kb.record()
+                R.rglru_debug_kernel_events(ka, kb)
+            a.record()
+            fn()
+            b.record()
+            torch.cuda.synchronize()
+            acc.append(a.elapsed_time(b))
+            if fn is bwd:
+                tk.append(ka.elapsed_time(kb))
+    if R.rglru_sync_status(saved) != R.OK or R.rglru_sync_status(ws) != R.OK:
+        raise RuntimeError("look-back timeout in the packed-sequence measurement")
+    fms, bms, kms = statistics.median(tf), statistics.median(tb), statistics.median(tk)
+    _, bwd_b = algorithmic_bytes(wl)
+    bwd_b += 3 * S * W * 4
+    gbs = bwd_b / (kms / 1e3) / 1e9
+    return {"workload": f"packed B1 T{T} W{W} k{k} bf16 canonical, {S} sequences of U[1, 2048] "
+                        "tokens, per-sequence h0 and dhT",
+            "sequences": S, "fwd_ms": fms, "bwd_ms": bms,
+            "tokens_per_s": T / ((fms + bms) / 1e3),
+            "roofline_bwd": {"bound": "hbm", "unit": "GB/s", "kernel": "k_fused_bwd (varlen)",
+                             "achieved": gbs, "peak": peak,
+                             "frac": (gbs / peak) if peak else None,
+                             "algorithmic_bytes": bwd_b, "kernel_ms": kms}}
 
 
 # FP32 CUDA-core peak of the GB300 for the delta-rule kernels (no tensor cores): 152 SMs x 128
@@ -579,6 +652,8 @@ def main(argv=None):
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-decode", action="store_true", help="skip the decode-step measurement")
     p.add_argument("--no-delta", action="store_true", help="skip the delta-rule measurement")
+    p.add_argument("--no-varlen", action="store_true",
+                   help="skip the packed-sequence (varlen) measurement")
     p.add_argument("--cpu-sample-T", type=int, default=2048)
     p.add_argument("--ref-sample-T", type=int, default=256)
     args = p.parse_args(argv)

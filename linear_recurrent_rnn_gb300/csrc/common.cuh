@@ -288,6 +288,32 @@ __device__ __forceinline__ bool is_reset(const uint8_t* reset_mask, const int32_
   return false;
 }
 
+// The markers of one token that decide a fused tile's path, as stored: the reset-mask byte or
+// the segment position (canonical mode), and the packed sequence that starts / ends at the
+// token (-1: none).  The fused kernels request a tile's markers one tile ahead of their use,
+// so that the load's round trip hides behind a tile of work.
+struct TokMarks {
+  int rs, st, en;
+};
+__device__ __forceinline__ TokMarks tok_marks_load(const uint8_t* reset_mask,
+                                                   const int32_t* segment_pos,
+                                                   const int32_t* seq_start,
+                                                   const int32_t* seq_end, size_t bt, bool in) {
+  TokMarks m{-1, -1, -1};
+  if (in) {
+    if (reset_mask) m.rs = reset_mask[bt];
+    else if (segment_pos) m.rs = segment_pos[bt];
+    if (seq_start) m.st = seq_start[bt];
+    if (seq_end) m.en = seq_end[bt];
+  }
+  return m;
+}
+// Reset flag from the stored marker (-1: a token past T, never a reset).
+__device__ __forceinline__ bool tok_marks_reset(const TokMarks& m, const uint8_t* reset_mask,
+                                                const int32_t* segment_pos) {
+  return reset_mask ? m.rs > 0 : (segment_pos ? m.rs == 0 : false);
+}
+
 // ---------------------------------------------------------------- look-back flags
 // A scan tile publishes FLAG_AGG once its own affine aggregate (A, B) is stored, and
 // FLAG_INCL once its chunk-boundary state (the "inclusive prefix") is stored.  Flags are

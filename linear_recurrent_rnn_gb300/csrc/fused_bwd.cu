@@ -159,19 +159,16 @@ constexpr int GRP = 8;  // tokens per TMEM load / store group
 // ab keeps the true a (for the derivatives and dh0[s] = a g); at an end token (emask) dhT[s]
 // joins dy.
 struct SeqB {
+  const BwdParams& p;  // the sequence arrays (seq_start, seq_end, h0s, dhTs, dh0s)
   uint32_t smask, emask;
-  const int32_t* start;  // sequence starting at each of the part's tokens (where smask)
-  const int32_t* end;    // sequence ending at each of the part's tokens (where emask)
-  const float* h0;       // h0[0][w], rows W apart, or null
-  const float* dhT;      // dhT[0][w] or null
-  float* dh0;            // dh0[0][w] or null
-  int W;
+  int t0;  // row index of the part's first token (packed sequences: one row)
+  int w;   // channel
 };
 __device__ __forceinline__ float seqb_h0(const SeqB& sq, int u) {
-  return sq.h0 ? sq.h0[(size_t)sq.start[u] * sq.W] : 0.0f;
+  return sq.p.h0s ? sq.p.h0s[(size_t)sq.p.seq_start[sq.t0 + u] * sq.p.W + sq.w] : 0.0f;
 }
 __device__ __forceinline__ float seqb_dhT(const SeqB& sq, int u) {
-  return sq.dhT ? sq.dhT[(size_t)sq.end[u] * sq.W] : 0.0f;
+  return sq.p.dhTs ? sq.p.dhTs[(size_t)sq.p.seq_end[sq.t0 + u] * sq.p.W + sq.w] : 0.0f;
 }
 // The chains' decay of a token pair: 0 at sequence starts.
 __device__ __forceinline__ float2 chain_decay(const SeqB& sq, int u, float2 a) {
@@ -337,10 +334,14 @@ __device__ __forceinline__ void bwd_pass2b(uint32_t tcol, int tb, int j,
   tc::reg_fence(r4);
   tc::reg_fence(i4);
   tc::reg_fence(h4);
+  // The general packed-sequence variant loads each group when it needs it (no prefetch of
+  // the next): its extra loads and addresses would otherwise raise the register peak of the
+  // whole kernel.
+  constexpr bool PREF = !(VARLEN && GENERAL);
 #pragma unroll
   for (int g = G0; g >= 0; --g) {
     float nm[GRP], nr[GRP], ni[GRP], nh[GRP];
-    if (g > 0) {
+    if (PREF && g > 0) {
       tc::tmem_ld(tcol + COL_LR + (g - 1) * GRP, nm);
       tc::tmem_ld(tcol + COL_LI + (g - 1) * GRP, nr);
       tc::tmem_ld(tcol + COL_HP + (g - 1) * GRP, ni);
@@ -370,9 +371,11 @@ __device__ __forceinline__ void bwd_pass2b(uint32_t tcol, int tb, int j,
       gv.x = fmaf(ach.y, gv.y, dyv.x);
       gnext = gv.x;
       anext = ach.x;
-      if (VARLEN && GENERAL && sq.dh0) {  // d h0[s] = a g at the sequence's first token
-        if ((sq.smask >> u) & 1u) sq.dh0[(size_t)sq.start[u] * sq.W] = abar.x * gv.x;
-        if ((sq.smask >> (u + 1)) & 1u) sq.dh0[(size_t)sq.start[u + 1] * sq.W] = abar.y * gv.y;
+      if (VARLEN && GENERAL && sq.p.dh0s) {  // d h0[s] = a g at the sequence's first token
+        float* dh0 = sq.p.dh0s + sq.w;
+        const int32_t* st = sq.p.seq_start + sq.t0;
+        if ((sq.smask >> u) & 1u) dh0[(size_t)st[u] * sq.p.W] = abar.x * gv.x;
+        if ((sq.smask >> (u + 1)) & 1u) dh0[(size_t)st[u + 1] * sq.p.W] = abar.y * gv.y;
       }
       // d h_t / d la = abar (h_{t-1} - abar x i / m) with i / m = i^2 / (m i); zero at reset
       // tokens (abar = 0), past T and where the decay is exactly 1 (m = 0)
@@ -394,6 +397,12 @@ __device__ __forceinline__ void bwd_pass2b(uint32_t tcol, int tb, int j,
     store_dl8(s_dl, s_dl + T_BYTES, tb + g * GRP, j, o_r);
     store_dl8(s_dl + 2 * T_BYTES, s_dl + 3 * T_BYTES, tb + g * GRP, j, o_i);
     tc::tmem_st(tcol + COL_DX + g * GRP, h4);
+    if (!PREF && g > 0) {
+      tc::tmem_ld(tcol + COL_LR + (g - 1) * GRP, nm);
+      tc::tmem_ld(tcol + COL_LI + (g - 1) * GRP, nr);
+      tc::tmem_ld(tcol + COL_HP + (g - 1) * GRP, ni);
+      tc::tmem_ld(tcol + COL_DX + (g - 1) * GRP, nh);
+    }
     if (g > 0) {
       tc::tmem_ld_wait();
       tc::reg_fence(nm);
@@ -422,7 +431,7 @@ __global__ void __maxnreg__(MAXREG)
     k_fused_bwd(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_dy,
                 const __grid_constant__ CUtensorMap tm_wa, const __grid_constant__ CUtensorMap tm_wx,
                 const __grid_constant__ CUtensorMap tm_dx,
-                const __grid_constant__ CUtensorMap tm_dwp, BwdParams p) {
+                const __grid_constant__ CUtensorMap tm_dwp, const __grid_constant__ BwdParams p) {
   extern __shared__ uint8_t smem_raw[];
   // 1024-byte aligned base, formed by pointer arithmetic so that it stays a shared pointer
   uint8_t* smem = smem_raw + ((1024u - (tc::smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -604,10 +613,30 @@ __global__ void __maxnreg__(MAXREG)
     // The last iteration only writes out the dx of the last tile.
     TileWalk cur(rr, p.P, p.B);  // tile it; cur.c counts chunks from the last one
     int pc = 0, pb = 0;          // chunk and row of tile it - 1
+    // this lane's token markers of a tile (one token of the part each)
+    const int32_t* seq_start = VARLEN ? p.seq_start : nullptr;
+    const int32_t* seq_end = VARLEN ? p.seq_end : nullptr;
+    auto marks = [&](const TileWalk& tw) {
+      const int t = (p.nC - 1 - tw.c) * FUSED_C + tb + lane;
+      return tok_marks_load(p.reset_mask, p.segment_pos, seq_start, seq_end,
+                            (size_t)tw.b * p.T + t, t < p.T);
+    };
+    // The packed-sequence view of tile (b, c) for the general passes, built where it is used
+    // so that its pointers are not live across the tile.
+    auto seqb = [&](uint32_t sm, uint32_t em, int b_, int c_) {
+      return SeqB{p, sm, em, b_ * p.T + c_ * FUSED_C + tb, w};
+    };
+    TokMarks mk = marks(cur);  // tile it's, requested during tile it - 1
     for (int it = 0; it <= my_tiles; ++it) {
       const bool have = it < my_tiles;
       const int n = rr + it * p.P;
       const int c = p.nC - 1 - cur.c, b = cur.b;
+      const TokMarks now = mk;
+      if (it + 1 < my_tiles) {
+        TileWalk nx = cur;
+        nx.next();
+        mk = marks(nx);
+      }
       const int st = it % STAGES;
       const uint32_t ph = (it / STAGES) & 1;
       const uint32_t xt = tc::smem_u32(s_in + st * 2 * T_BYTES + tb * 32);
@@ -619,8 +648,7 @@ __global__ void __maxnreg__(MAXREG)
       float hin_tile = 0.0f;
       int valid = 0;
       bool fast = false;
-      uint32_t rmask = 0;
-      SeqB sq{0u, 0u, nullptr, nullptr, nullptr, nullptr, nullptr, p.W};
+      uint32_t rmask = 0, smask = 0, emask = 0;
       // Part 0 requests the look-back slots of this tile's carry from the right now; they are
       // read after pass 2a, so the L2 round trip hides behind passes 1 and 2a.
       const size_t cidx = (size_t)b * p.nC + c;
@@ -640,31 +668,20 @@ __global__ void __maxnreg__(MAXREG)
       if (have) {
         hin_tile = slot_get1(p.fwd_carry + ((size_t)b * (p.nC + 1) + c) * p.W + w);
         if (VARLEN) {
-          const size_t t0 = (size_t)b * p.T + (size_t)c * FUSED_C + tb;
-          const bool in = c * FUSED_C + tb + lane < p.T;
-          sq.start = p.seq_start + t0;
-          sq.end = p.seq_end + t0;
-          sq.smask = __ballot_sync(0xffffffffu, in && sq.start[lane] >= 0);
-          sq.emask = __ballot_sync(0xffffffffu, in && sq.end[lane] >= 0);
-          sq.h0 = p.h0s ? p.h0s + w : nullptr;
-          sq.dhT = p.dhTs ? p.dhTs + w : nullptr;
-          sq.dh0 = p.dh0s ? p.dh0s + w : nullptr;
+          smask = __ballot_sync(0xffffffffu, now.st >= 0);
+          emask = __ballot_sync(0xffffffffu, now.en >= 0);
         }
-        if (p.canonical) {
-          const int t = c * FUSED_C + tb + lane;
-          rmask = __ballot_sync(0xffffffffu, lane < PT && t < p.T &&
-                                                 is_reset(p.reset_mask, p.segment_pos,
-                                                          (size_t)b * p.T + t));
-        }
+        rmask = __ballot_sync(0xffffffffu, tok_marks_reset(now, p.reset_mask, p.segment_pos));
         valid = min(FUSED_C, p.T - c * FUSED_C) - tb;
-        fast = near_all && rmask == 0u && (sq.smask | sq.emask) == 0u && valid >= PT;
+        fast = near_all && rmask == 0u && (smask | emask) == 0u && valid >= PT;
         ctl.wait(lg_full, it & 1);
         ctl.wait(&in_full[st], ph);
         tc::tc_fence_after();
         if (fast)
-          bwd_pass1<false, VARLEN>(tcol, xb0, xb1, dyb, gk, 0u, PT, ab, xr, sq, P, fB, S);
+          bwd_pass1<false, VARLEN>(tcol, xb0, xb1, dyb, gk, 0u, PT, ab, xr, SeqB{p, 0u, 0u, 0, 0}, P, fB, S);
         else
-          bwd_pass1<true, VARLEN>(tcol, xb0, xb1, dyb, gk, rmask, valid, ab, xr, sq, P, fB, S);
+          bwd_pass1<true, VARLEN>(tcol, xb0, xb1, dyb, gk, rmask, valid, ab, xr,
+                                  seqb(smask, emask, b, c), P, fB, S);
       }
 
       if (have) s_agg[part * FUSED_K + j] = make_float4(P, fB, P, S);  // the part's maps
@@ -745,9 +762,9 @@ __global__ void __maxnreg__(MAXREG)
       // Pass 2a: h_{t-1} through the part, from the earlier parts' map applied to the tile's
       // entry state.
       if (VARLEN && !fast)
-        bwd_pass2a<true, VARLEN>(tcol, xr, ab, sq, fmaf(Fa, hin_tile, Fb));
+        bwd_pass2a<true, VARLEN>(tcol, xr, ab, seqb(smask, emask, b, c), fmaf(Fa, hin_tile, Fb));
       else
-        bwd_pass2a<false, VARLEN>(tcol, xr, ab, sq, fmaf(Fa, hin_tile, Fb));
+        bwd_pass2a<false, VARLEN>(tcol, xr, ab, SeqB{p, 0u, 0u, 0, 0}, fmaf(Fa, hin_tile, Fb));
 
       if (part == 0) {
         const float cin =
@@ -768,10 +785,11 @@ __global__ void __maxnreg__(MAXREG)
       if (it > 0) ctl.wait(dl_empty, (it - 1) & 1);
       tc::tc_fence_after();
       if (fast)
-        bwd_pass2b<false, VARLEN>(tcol, tb, j, xr, dyb, gk.nk, PT, ab, sq, cin, lg_empty, s_dl, dsp,
+        bwd_pass2b<false, VARLEN>(tcol, tb, j, xr, dyb, gk.nk, PT, ab, SeqB{p, 0u, 0u, 0, 0}, cin, lg_empty, s_dl, dsp,
                                   dba, dbx);
       else
-        bwd_pass2b<true, VARLEN>(tcol, tb, j, xr, dyb, gk.nk, valid, ab, sq, cin, lg_empty, s_dl,
+        bwd_pass2b<true, VARLEN>(tcol, tb, j, xr, dyb, gk.nk, valid, ab,
+                                 seqb(smask, emask, b, c), cin, lg_empty, s_dl,
                                  dsp, dba, dbx);
       tc::fence_proxy_async_smem();
       tc::tc_fence_before();
@@ -965,8 +983,8 @@ cudaError_t launch_fused_bwd(const Dims& d, const void* dy, const float* dhT, co
   p.Lambda = Lambda;
   p.ba = ba;
   p.bx = bx;
-  p.reset_mask = rm;
-  p.segment_pos = sp;
+  p.reset_mask = p.canonical ? rm : nullptr;  // restricted mode has no resets
+  p.segment_pos = p.canonical ? sp : nullptr;
   p.dhT = dhT;
   const FusedFwdLayout FL = fused_fwd_layout(d);
   p.fwd_carry = reinterpret_cast<const float*>(static_cast<const uint8_t*>(saved) + FL.L.carry);

@@ -333,26 +333,34 @@ __global__ void __maxnreg__(MAXREG)
     // Warp-uniform: every channel of this warp has la > -1/8 on every token.
     const bool near_all = __all_sync(0xffffffffu, gk.nk > NEAR_LA);
 
+    // this lane's token markers of a tile (lane < PT: one token of the part each)
+    const int32_t* seq_start = VARLEN ? p.seq_start : nullptr;
+    auto marks = [&](const TileWalk& tw) {
+      const int t = tw.c * FUSED_C + tb + lane;
+      return tok_marks_load(p.reset_mask, p.segment_pos, seq_start, nullptr,
+                            (size_t)tw.b * p.T + t, lane < PT && t < p.T);
+    };
     TileWalk cur(rr, p.P, p.B);
+    TokMarks mk = marks(cur);  // tile it's, requested during tile it - 1
     for (int it = 0; it < my_tiles; ++it, cur.next()) {
       const int c = cur.c, b = cur.b;
       const int st = it % XSTAGES;
       const uint32_t ph = (it / XSTAGES) & 1;
       const int a = it % NBUF;
       const uint32_t aph = (it / NBUF) & 1;
-      uint32_t rmask = 0;
-      if (p.canonical) {
-        const int t = c * FUSED_C + tb + lane;
-        rmask = __ballot_sync(0xffffffffu, lane < PT && t < p.T &&
-                                               is_reset(p.reset_mask, p.segment_pos,
-                                                        (size_t)b * p.T + t));
+      const TokMarks now = mk;
+      if (it + 1 < my_tiles) {
+        TileWalk nx = cur;
+        nx.next();
+        mk = marks(nx);
       }
+      const uint32_t rmask =
+          __ballot_sync(0xffffffffu, tok_marks_reset(now, p.reset_mask, p.segment_pos));
       const int valid = min(FUSED_C, p.T - c * FUSED_C) - tb;  // tokens of this part < T
       SeqStarts sq{0u, nullptr, nullptr, p.W};
       if (VARLEN) {
-        const int t = c * FUSED_C + tb + lane;
         sq.seq = p.seq_start + (size_t)b * p.T + c * FUSED_C + tb;
-        sq.smask = __ballot_sync(0xffffffffu, lane < PT && t < p.T && sq.seq[lane] >= 0);
+        sq.smask = __ballot_sync(0xffffffffu, now.st >= 0);
         sq.h0 = p.h0s ? p.h0s + w : nullptr;
       }
       ctl.wait(&acc_full[a], aph);
@@ -397,12 +405,21 @@ __global__ void __maxnreg__(MAXREG)
     int lb_n = 0;
     const float2* lb_agg = agg;
     const float* lb_anchor = nullptr;
+    // packed sequences ending at the tile's tokens lane and 32 + lane: tile it - 1's, and tile
+    // it's, requested an iteration ahead of their use
+    int pe0 = -1, pe1 = -1;
 #pragma unroll
     for (int pp = 0; pp < NPART; ++pp) Pa[pp] = 1.0f, Pb[pp] = 0.0f;
     for (int it = 0; it <= my_tiles; ++it) {
       // 1. tile it, parked: its map (the parts composed) and its aggregate, published at once
       float nPa[NPART], nPb[NPART], nTa = 1.0f, nTb = 0.0f;
       const int n = rr + it * p.P;
+      int ce0 = -1, ce1 = -1;
+      if (VARLEN && it < my_tiles) {
+        const size_t tb0 = (size_t)cur.b * p.T + (size_t)cur.c * FUSED_C;
+        if (cur.c * FUSED_C + lane < p.T) ce0 = p.seq_end[tb0 + lane];
+        if (cur.c * FUSED_C + 32 + lane < p.T) ce1 = p.seq_end[tb0 + 32 + lane];
+      }
       if (it < my_tiles) {
         const int a = it % NBUF;
         ctl.wait(&park_full[a], (it / NBUF) & 1);
@@ -431,11 +448,8 @@ __global__ void __maxnreg__(MAXREG)
         if (pc == p.nC - 1 && p.hT) p.hT[(size_t)pb * p.W + w] = hend;
         // packed sequences ending in the tile: their final state (warp-uniform masks)
         uint32_t em0 = 0u, em1 = 0u;
-        int e0 = -1, e1 = -1;
+        const int e0 = pe0, e1 = pe1;
         if (VARLEN) {
-          const size_t tb0 = (size_t)pb * p.T + (size_t)pc * FUSED_C;
-          if (pc * FUSED_C + lane < p.T) e0 = p.seq_end[tb0 + lane];
-          if (pc * FUSED_C + 32 + lane < p.T) e1 = p.seq_end[tb0 + 32 + lane];
           em0 = __ballot_sync(0xffffffffu, e0 >= 0);
           em1 = __ballot_sync(0xffffffffu, e1 >= 0);
         }
@@ -460,17 +474,26 @@ __global__ void __maxnreg__(MAXREG)
               const int tl = pp * PT + c16 + u;
               *reinterpret_cast<bf16*>(yb + tl * 64 + lane * 2) = __float2bfloat16_rn(yv.x);
               *reinterpret_cast<bf16*>(yb + (tl + 1) * 64 + lane * 2) = __float2bfloat16_rn(yv.y);
-              if (VARLEN && (em0 | em1) != 0u) {
+            }
+          }
+        }
+        if (VARLEN && (em0 | em1) != 0u) {
+          // the final state of each packed sequence ending in the tile: the float32 y of its
+          // last token, taken again from the parked columns (off the loop above: rare)
+          static_assert(NPART == 2 && PT == 32, "em0 / em1 are the two parts' tokens");
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                  const int tt = tl + h;
-                  const uint32_t m = tt < 32 ? em0 : em1;
-                  if ((m >> (tt & 31)) & 1u) {
-                    const int sidx = __shfl_sync(0xffffffffu, tt < 32 ? e0 : e1, tt & 31);
-                    if (p.hTs) p.hTs[(size_t)sidx * p.W + w] = h ? yv.y : yv.x;
-                  }
-                }
-              }
+          for (int pp = 0; pp < NPART; ++pp) {
+            uint32_t m = pp == 0 ? em0 : em1;
+            const float hin = fmaf(Pa[pp], hin_t, Pb[pp]);
+            const uint32_t park = tmem + lane_base + a * 128 + pp * PT;
+            while (m != 0u) {
+              const int u = __ffs(m) - 1;
+              m &= m - 1u;
+              const float hl = tc::tmem_ld1(park + u);
+              const float Ac = tc::tmem_ld1(park + 64 + u);
+              tc::tmem_ld_wait();
+              const int sidx = __shfl_sync(0xffffffffu, pp == 0 ? e0 : e1, u);
+              if (p.hTs) p.hTs[(size_t)sidx * p.W + w] = fmaf(Ac, hin, hl);
             }
           }
         }
@@ -500,6 +523,8 @@ __global__ void __maxnreg__(MAXREG)
         for (int pp = 0; pp < NPART; ++pp) Pa[pp] = nPa[pp], Pb[pp] = nPb[pp];
         Ta = nTa;
         Tb = nTb;
+        pe0 = ce0;
+        pe1 = ce1;
         pc = c;
         pb = b;
         cur.next();
@@ -583,8 +608,8 @@ cudaError_t launch_fused_fwd(const Dims& d, const void* x, const void* Wa, const
   p.Lambda = Lambda;
   p.ba = ba;
   p.bx = bx;
-  p.reset_mask = rm;
-  p.segment_pos = sp;
+  p.reset_mask = p.canonical ? rm : nullptr;  // restricted mode has no resets
+  p.segment_pos = p.canonical ? sp : nullptr;
   p.h0 = h0;
   p.hT = hT;
   p.seq_start = nullptr;

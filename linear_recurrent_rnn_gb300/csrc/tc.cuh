@@ -262,6 +262,11 @@ __device__ __forceinline__ void tmem_st8(uint32_t taddr, const float (&v)[8]) {
       "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7]))
       : "memory");
 }
+__device__ __forceinline__ float tmem_ld1(uint32_t taddr) {
+  uint32_t r;
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];" : "=r"(r) : "r"(taddr));
+  return __uint_as_float(r);
+}
 __device__ __forceinline__ void tmem_ld2(uint32_t taddr, float (&v)[2]) {
   uint32_t r[2];
   asm volatile("tcgen05.ld.sync.aligned.32x32b.x2.b32 {%0, %1}, [%2];"

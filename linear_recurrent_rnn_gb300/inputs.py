@@ -98,6 +98,17 @@ def segment_positions(rng: np.random.Generator, T: int, lo: int, hi: int,
     return pos
 
 
+def packed_lengths(seed: int, T: int, lo: int, hi: int) -> list:
+    """Sequence lengths drawn U[lo, hi] until they fill T tokens (the last one truncated), for
+    packed variable-length sequences given by cu_seqlens."""
+    rng = np.random.default_rng(seed)
+    lengths, t = [], 0
+    while t < T:
+        n = min(int(rng.integers(lo, hi + 1)), T - t)
+        lengths.append(n)
+        t += n
+    return lengths
+
 def _normal(rng, shape, std=1.0):
     return (rng.standard_normal(size=shape, dtype=np.float32) * np.float32(std))
 

@@ -87,3 +87,69 @@ def test_varlen_matches_per_sequence_oracle(lengths, u_range, seed, grad):
     for n, got in (("dWa", dWa), ("dWx", dWx), ("dba", dba), ("dbx", dbx), ("dLambda", dL)):
         assert_close(n, host(got), g_ref[n], io="bf16", kind="grad")
     assert_close("dh0", host(dh0), dh0_ref, io="bf16", kind="grad")
+
+
+def test_varlen_full_size_sampled_blocks():
+    """The packed configuration the benchmark times: 8192 tokens in one row, W2048 in 16 gate
+    blocks of 128, bf16, sequence lengths U[1, 2048] (the last one truncated), per-sequence h0
+    and dhT.  Gate blocks are independent in every output, so the oracle run per sequence on
+    the channels of one block is that block's exact reference; three blocks are compared."""
+    from linear_recurrent_rnn_gb300.inputs import packed_lengths
+    T, W, k = 8192, 2048, 128
+    lengths = packed_lengths(5, T, 1, 2048)
+    S = len(lengths)
+    wl = Workload("varlen", 1, T, W, k, "bf16", "canonical", (0.9, 0.999))
+    inp = generate(wl, 5)
+    rng = np.random.default_rng(6)
+    h0s = torch.from_numpy(rng.standard_normal((S, W)) * 0.5).float()
+    dhTs = torch.from_numpy(rng.standard_normal((S, W))).float()
+    cu = np.concatenate([[0], np.cumsum(lengths)]).astype(np.int32)
+    d = {n: dev(v) for n, v in inp.items() if isinstance(v, torch.Tensor)}
+    sh = R.make_shape(1, T, W, W // k, R.BF16, R.BF16, R.CANONICAL)
+    cu_d = torch.from_numpy(cu).cuda()
+    y = torch.empty_like(d["x"])
+    hT = torch.empty(S, W, device="cuda")
+    saved, ws = R.alloc_saved(sh), R.alloc_workspace(sh)
+    R.rglru_fused_forward_varlen(sh, d["x"], d["Wa"], d["ba"], d["Wx"], d["bx"], d["Lambda"],
+                                 cu_d, S, dev(h0s), y, hT, saved)
+    dx = torch.empty_like(d["x"])
+    dWa = torch.empty(W // k, k, k, device="cuda")
+    dWx = torch.empty_like(dWa)
+    dba, dbx, dL = (torch.empty(W, device="cuda") for _ in range(3))
+    dh0 = torch.empty(S, W, device="cuda")
+    R.rglru_fused_backward_varlen(sh, d["dy"], dev(dhTs), d["x"], d["Wa"], d["ba"], d["Wx"],
+                                  d["bx"], d["Lambda"], cu_d, S, dev(h0s), saved, dx, dWa, dba,
+                                  dWx, dbx, dL, dh0, ws)
+    assert R.rglru_sync_status(saved) == R.OK
+    assert R.rglru_sync_status(ws) == R.OK
+    got = {n: host(t) for n, t in (("y", y), ("hT", hT), ("dx", dx), ("dWa", dWa), ("dWx", dWx),
+                                   ("dba", dba), ("dbx", dbx), ("dLambda", dL), ("dh0", dh0))}
+    for blk in (0, 7, 15):
+        cs = slice(blk * k, (blk + 1) * k)
+        x, dy = as_f64(inp["x"][..., cs]), as_f64(inp["dy"][..., cs])
+        ba, bx, Lam = (as_f64(inp[n][cs]) for n in ("ba", "bx", "Lambda"))
+        Wa, Wx = as_f64(inp["Wa"][blk:blk + 1]), as_f64(inp["Wx"][blk:blk + 1])
+        h0, dhT = h0s[:, cs].double().numpy(), dhTs[:, cs].double().numpy()
+        y_ref, dx_ref = np.zeros((1, T, k)), np.zeros((1, T, k))
+        hT_ref, dh0_ref = np.zeros((S, k)), np.zeros((S, k))
+        acc = {n: 0.0 for n in ("dWa", "dWx", "dba", "dbx", "dLambda")}
+        for s in range(S):
+            a, b = int(cu[s]), int(cu[s + 1])
+            ys, hs = oracle.fused_forward(oracle.CANONICAL, x[:, a:b], Wa, ba, Wx, bx, Lam,
+                                          None, None, h0[s:s + 1])
+            g = oracle.fused_backward(oracle.CANONICAL, x[:, a:b], Wa, ba, Wx, bx, Lam,
+                                      dy[:, a:b], dhT[s:s + 1], None, None, h0[s:s + 1])
+            y_ref[:, a:b], dx_ref[:, a:b] = ys, g["dx"]
+            hT_ref[s], dh0_ref[s] = hs[0], g["dh0"][0]
+            for n in acc:
+                acc[n] = acc[n] + g[n]
+        tag = f"blk{blk} "
+        assert_close(tag + "y", got["y"][..., cs], y_ref, io="bf16", kind="out")
+        assert_close(tag + "hT", got["hT"][:, cs], hT_ref, io="bf16", kind="out")
+        assert_close(tag + "dx", got["dx"][..., cs], dx_ref, io="bf16", kind="grad",
+                     stored="bf16")
+        assert_close(tag + "dWa", got["dWa"][blk:blk + 1], acc["dWa"], io="bf16", kind="grad")
+        assert_close(tag + "dWx", got["dWx"][blk:blk + 1], acc["dWx"], io="bf16", kind="grad")
+        for n in ("dba", "dbx", "dLambda"):
+            assert_close(tag + n, got[n][cs], acc[n], io="bf16", kind="grad")
+        assert_close(tag + "dh0", got["dh0"][:, cs], dh0_ref, io="bf16", kind="grad")
