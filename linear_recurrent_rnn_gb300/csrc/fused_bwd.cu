@@ -626,17 +626,10 @@ __global__ void __maxnreg__(MAXREG)
     auto seqb = [&](uint32_t sm, uint32_t em, int b_, int c_) {
       return SeqB{p, sm, em, b_ * p.T + c_ * FUSED_C + tb, w};
     };
-    TokMarks mk = marks(cur);  // tile it's, requested during tile it - 1
     for (int it = 0; it <= my_tiles; ++it) {
       const bool have = it < my_tiles;
       const int n = rr + it * p.P;
       const int c = p.nC - 1 - cur.c, b = cur.b;
-      const TokMarks now = mk;
-      if (it + 1 < my_tiles) {
-        TileWalk nx = cur;
-        nx.next();
-        mk = marks(nx);
-      }
       const int st = it % STAGES;
       const uint32_t ph = (it / STAGES) & 1;
       const uint32_t xt = tc::smem_u32(s_in + st * 2 * T_BYTES + tb * 32);
@@ -666,7 +659,12 @@ __global__ void __maxnreg__(MAXREG)
                        p.dhT ? p.dhT[(size_t)b * p.W + w] : 0.0f);
       }
       if (have) {
+        // the markers are requested before the waits for the tile's operands and read after
+        const TokMarks now = marks(cur);
         hin_tile = slot_get1(p.fwd_carry + ((size_t)b * (p.nC + 1) + c) * p.W + w);
+        ctl.wait(lg_full, it & 1);
+        ctl.wait(&in_full[st], ph);
+        tc::tc_fence_after();
         if (VARLEN) {
           smask = __ballot_sync(0xffffffffu, now.st >= 0);
           emask = __ballot_sync(0xffffffffu, now.en >= 0);
@@ -674,9 +672,6 @@ __global__ void __maxnreg__(MAXREG)
         rmask = __ballot_sync(0xffffffffu, tok_marks_reset(now, p.reset_mask, p.segment_pos));
         valid = min(FUSED_C, p.T - c * FUSED_C) - tb;
         fast = near_all && rmask == 0u && (smask | emask) == 0u && valid >= PT;
-        ctl.wait(lg_full, it & 1);
-        ctl.wait(&in_full[st], ph);
-        tc::tc_fence_after();
         if (fast)
           bwd_pass1<false, VARLEN>(tcol, xb0, xb1, dyb, gk, 0u, PT, ab, xr, SeqB{p, 0u, 0u, 0, 0}, P, fB, S);
         else
