@@ -372,7 +372,7 @@ rglru_status rglru_fused_forward_varlen(const rglru_shape* shape, const void* x,
   v.h0 = h0;
   v.hT = hT;
   cudaError_t e = launch_seq_index(v, d.T, d.W, const_cast<int32_t*>(v.seq_start),
-                                   const_cast<int32_t*>(v.seq_end), false, stream);
+                                   const_cast<int32_t*>(v.seq_end), stream);
   if (e == cudaSuccess)
     e = launch_fused_fwd(d, x, Wa, ba, Wx, bx, Lambda, nullptr, nullptr, nullptr, y, nullptr,
                          saved, g_spin_limit, g_drop_tile, stream, &v);
@@ -401,8 +401,7 @@ rglru_status rglru_fused_backward_varlen(const rglru_shape* shape, const void* d
   v.dh0 = dh0;
   // the token indices were written by the forward into `saved`; empty sequences' dh0 here
   cudaError_t e = cudaSuccess;
-  if (dh0) e = launch_seq_index(v, d.T, d.W, const_cast<int32_t*>(v.seq_start),
-                                const_cast<int32_t*>(v.seq_end), true, stream);
+  if (dh0) e = launch_seq_empty_dh0(v, d.W, stream);
   if (e == cudaSuccess)
     e = launch_fused_bwd(d, dy, nullptr, x, Wa, ba, Wx, bx, Lambda, nullptr, nullptr, nullptr,
                          saved, dx, dWa, dba, dWx, dbx, dLambda, nullptr, workspace,

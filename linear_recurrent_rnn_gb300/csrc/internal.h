@@ -114,9 +114,11 @@ struct Varlen {
   const float* dhT;           // [S][W] or null (backward)
   float* dh0;                 // [S][W] or null (backward)
 };
-// Fills the token indices (and, for empty sequences, hT = h0 or dh0 = dhT).
+// Forward: fills the token indices and, for empty sequences, hT = h0 (one launch).
 cudaError_t launch_seq_index(const Varlen& v, int T, int W, int32_t* seq_start,
-                             int32_t* seq_end, bool backward, cudaStream_t s);
+                             int32_t* seq_end, cudaStream_t s);
+// Backward: dh0 = dhT for empty sequences (the token indices are the forward's).
+cudaError_t launch_seq_empty_dh0(const Varlen& v, int W, cudaStream_t s);
 
 // Fused backward workspace: the reverse look-back scratch, then per-CTA partial sums (the
 // kernel runs at most FUSED_MAX_CTAS CTAs, each owning one gate block): dWa / dWx partials
