@@ -6,7 +6,10 @@ One step = rglru_fused_forward + rglru_fused_backward over one batch of seeded s
 input already resident in HBM: the gate projections, gates, decay, multiplier, write and
 scan, then the reverse scan, pointwise gradients, the on-device Lambda reduction and the
 projection gradients (dx, dWa, dWx, dba, dbx).  L2 is flushed (a 256 MiB write) before every
-timed step; CUDA events bracket each step on the launching stream.
+timed step; two CUDA events bracket each step on the launching stream, with nothing else
+recorded between them.  A second pass records the forward / backward split and the backward
+kernel's own duration (for the roofline); a third replays the step captured in a CUDA graph
+(`graph`).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -193,13 +196,9 @@ def run_ours(args, rank, world, local):
     if R.rglru_sync_status(saved) != R.OK or R.rglru_sync_status(ws) != R.OK:
         raise RuntimeError("look-back timeout during warm-up")
 
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
-    # the backward tensor-core kernel alone, between events the library records around its
-    # launch (the call also runs the look-back slot clear and the partial-sum reduction)
-    kev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
-    for e in kev:
-        for x_ in e:
-            x_.record(stream)  # creates the event
+    # The step: each timed between two events on the launching stream (nothing else recorded
+    # inside it), the L2 flushed before each.
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
     clocks = ClockSampler(local)
     dist_barrier(world)
     torch.cuda.synchronize()
@@ -209,22 +208,69 @@ def run_ours(args, rank, world, local):
         flush.zero_()
         ev[k][0].record(stream)
         fwd()
-        ev[k][1].record(stream)
-        R.rglru_debug_kernel_events(kev[k][0], kev[k][1])
         bwd()
-        ev[k][2].record(stream)
+        ev[k][1].record(stream)
     torch.cuda.synchronize()
     launches = R.rglru_kernel_launches() - n0
     clk = clocks.stop()
     dist_barrier(world)
     if R.rglru_sync_status(saved) != R.OK or R.rglru_sync_status(ws) != R.OK:
         raise RuntimeError("look-back timeout during the timed region")
-    fwd_ms = [e[0].elapsed_time(e[1]) for e in ev]
-    bwd_ms = [e[1].elapsed_time(e[2]) for e in ev]
-    total_ms = sum(fwd_ms) + sum(bwd_ms)
-    total_ms = dist_max(total_ms, world, device="cuda")
+    step_list = [e[0].elapsed_time(e[1]) for e in ev]
+    total_ms = dist_max(sum(step_list), world, device="cuda")
     tokens = wl.B * wl.T
     value = tokens * world * args.steps / (total_ms / 1e3)
+
+    # A second pass for the split: the forward call, and the backward's tensor-core kernel
+    # alone between events the library records around its launch (the call also runs the
+    # look-back slot clear).
+    sev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    kev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
+    for e in kev:
+        for x_ in e:
+            x_.record(stream)  # creates the event
+    for k in range(args.steps):
+        flush.zero_()
+        sev[k][0].record(stream)
+        fwd()
+        sev[k][1].record(stream)
+        R.rglru_debug_kernel_events(kev[k][0], kev[k][1])
+        bwd()
+        sev[k][2].record(stream)
+    torch.cuda.synchronize()
+    fwd_ms = [e[0].elapsed_time(e[1]) for e in sev]
+    bwd_ms = [e[1].elapsed_time(e[2]) for e in sev]
+
+    # The same step captured once in a CUDA graph (the library's calls enqueue only stream-
+    # ordered work, so they capture as they are) and replayed.
+    graph = None
+    if world == 1:
+        gs = torch.cuda.Stream()
+        gs.wait_stream(stream)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=gs):
+            R.rglru_fused_forward(sh, x, Wa, ba, Wx, bx, L, None, None, None, y, hT, saved, gs)
+            R.rglru_fused_backward(sh, dy, None, x, Wa, ba, Wx, bx, L, None, None, None, saved,
+                                   dx, dWa, dba, dWx, dbx, dL, None, ws, gs)
+        stream.wait_stream(gs)
+        for _ in range(args.warmup):
+            g.replay()
+        torch.cuda.synchronize()
+        gev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
+        for k in range(args.steps):
+            flush.zero_()
+            gev[k][0].record(stream)
+            g.replay()
+            gev[k][1].record(stream)
+        torch.cuda.synchronize()
+        if R.rglru_sync_status(saved) != R.OK or R.rglru_sync_status(ws) != R.OK:
+            raise RuntimeError("look-back timeout in the graph replays")
+        g_ms = sum(e[0].elapsed_time(e[1]) for e in gev)
+        graph = {"ms_per_step": g_ms / args.steps,
+                 "value": tokens * args.steps / (g_ms / 1e3), "unit": UNIT,
+                 "how": "forward + backward calls captured once in a CUDA graph, replayed; "
+                        "L2 flushed before every replay"}
+        del g
 
     # end to end through the C ABI with host buffers: H2D of x and dy from pinned memory, the
     # step, D2H of the parameter gradients, all inside the events
@@ -272,9 +318,9 @@ def run_ours(args, rank, world, local):
                    "parallelism": f"dp{world} (independent batches, no collective)"},
         "fwd_ms": {"median": statistics.median(fwd_ms), "min": min(fwd_ms), "max": max(fwd_ms),
                    "mean": statistics.fmean(fwd_ms)},
-        "fwd_bwd_ms": {"median": statistics.median([a + b for a, b in zip(fwd_ms, bwd_ms)]),
-                       "min": min(a + b for a, b in zip(fwd_ms, bwd_ms)),
-                       "max": max(a + b for a, b in zip(fwd_ms, bwd_ms))},
+        "bwd_ms": {"median": statistics.median(bwd_ms), "min": min(bwd_ms), "max": max(bwd_ms)},
+        "fwd_bwd_ms": {"median": statistics.median(step_list), "min": min(step_list),
+                       "max": max(step_list)},
         "hbm_fraction_of_8TBps": (fwd_b + bwd_b) / (step_ms / 1e3) / 8e12,
         "roofline": {"bound": "hbm", "unit": "GB/s", "kernel": "k_fused_bwd",
                      "achieved": achieved, "peak": peak,
@@ -298,6 +344,7 @@ def run_ours(args, rank, world, local):
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": launches,
         "clocks": clk,
+        "graph": graph,
         "memory": memory_footprint(sh, wl),
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
