@@ -353,6 +353,8 @@ def run_ours(args, rank, world, local):
         line["decode"] = decode_step(flush, peak)
     if rank == 0 and world == 1 and not args.no_varlen:
         line["varlen"] = varlen_measure(flush, peak)
+    if rank == 0 and world == 1 and not args.no_unfused:
+        line["unfused"] = unfused_measure(flush, peak)
     if rank == 0 and world == 1 and not args.no_delta:
         line["delta_rule"] = delta_rule_measure(flush, peak)
     if rank == 0:
@@ -481,6 +483,68 @@ def varlen_measure(flush, peak, reps=10, W=2048, k=128, T=8192, seed=5):
                              "achieved": gbs, "peak": peak,
                              "frac": (gbs / peak) if peak else None,
                              "algorithmic_bytes": bwd_b, "kernel_ms": kms}}
+
+
+def unfused_measure(flush, peak, reps=10):
+    """The unfused API at the headline shape (B4 T2048 W2048, 16 blocks of 128, bf16, restricted):
+    rglru_gate_proj (logits to HBM), rglru_forward and rglru_backward (the scan kernels over
+    stored logits), rglru_gate_proj_backward.  Milliseconds per call (L2 flushed before each),
+    tokens/s of the four, and the two scan calls against the measured copy bandwidth with
+    their compulsory bytes: forward x, lr, li read and y written (8 bytes per element, plus
+    Lambda and hT); backward x, lr, li, dy read and dx, dlr, dli written (14 bytes per element,
+    plus Lambda and dLambda).  Each scan call also clears its look-back slots; the backward
+    call also reduces the Lambda partials (a second, small kernel)."""
+    import torch
+    from linear_recurrent_rnn_gb300 import librglru as R
+    from linear_recurrent_rnn_gb300.inputs import WORKLOADS, generate
+    wl = WORKLOADS[2]
+    inp = generate(wl, 2)
+    d = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+    sh = R.make_shape(wl.B, wl.T, wl.W, wl.nblk, R.BF16, R.BF16, R.RESTRICTED)
+    x = d["x"]
+    lr, li, y, dx, dlr, dli = (torch.empty_like(x) for _ in range(6))
+    hT = torch.empty(wl.B, wl.W, device="cuda")
+    dL, dba, dbx = (torch.empty(wl.W, device="cuda") for _ in range(3))
+    dWa = torch.empty(wl.nblk, wl.k, wl.k, device="cuda")
+    dWx = torch.empty_like(dWa)
+    saved, ws = R.alloc_saved(sh), R.alloc_workspace(sh)
+    calls = {
+        "gate_proj": lambda: R.rglru_gate_proj(sh, x, d["Wa"], d["ba"], d["Wx"], d["bx"], lr, li),
+        "forward": lambda: R.rglru_forward(sh, x, lr, li, d["Lambda"], None, None, None, y, hT,
+                                           saved),
+        "backward": lambda: R.rglru_backward(sh, d["dy"], None, x, lr, li, d["Lambda"], None,
+                                             None, None, saved, dx, dlr, dli, dL, None, ws),
+        "gate_proj_backward": lambda: R.rglru_gate_proj_backward(sh, dlr, dli, x, d["Wa"],
+                                                                 d["Wx"], dx, dWa, dba, dWx,
+                                                                 dbx, ws),
+    }
+    for _ in range(3):
+        for fn in calls.values():
+            fn()
+    torch.cuda.synchronize()
+    times = {n: [] for n in calls}
+    for _ in range(reps):
+        for n, fn in calls.items():
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            fn()
+            b.record()
+            torch.cuda.synchronize()
+            times[n].append(a.elapsed_time(b))
+    if R.rglru_sync_status(saved) != R.OK or R.rglru_sync_status(ws) != R.OK:
+        raise RuntimeError("look-back timeout in the unfused measurement")
+    ms = {n: statistics.median(t) for n, t in times.items()}
+    N = wl.B * wl.T * wl.W
+    out = {"workload": f"{wl.name} unfused API (logits through HBM)",
+           "ms": ms, "tokens_per_s": wl.B * wl.T / (sum(ms.values()) / 1e3)}
+    for n, nbytes in (("forward", 8 * N + 4 * wl.W + 4 * wl.B * wl.W),
+                      ("backward", 14 * N + 8 * wl.W)):
+        gbs = nbytes / (ms[n] / 1e3) / 1e9
+        out[f"roofline_{n}"] = {"bound": "hbm", "unit": "GB/s", "achieved": gbs, "peak": peak,
+                                "frac": (gbs / peak) if peak else None,
+                                "algorithmic_bytes": nbytes, "timed": "the whole call"}
+    return out
 
 
 # FP32 CUDA-core peak of the GB300 for the delta-rule kernels (no tensor cores): 152 SMs x 128
@@ -701,6 +765,8 @@ def main(argv=None):
     p.add_argument("--no-delta", action="store_true", help="skip the delta-rule measurement")
     p.add_argument("--no-varlen", action="store_true",
                    help="skip the packed-sequence (varlen) measurement")
+    p.add_argument("--no-unfused", action="store_true",
+                   help="skip the unfused-API (scan kernels over stored logits) measurement")
     p.add_argument("--cpu-sample-T", type=int, default=2048)
     p.add_argument("--ref-sample-T", type=int, default=256)
     args = p.parse_args(argv)

@@ -14,12 +14,22 @@ namespace rglru {
 // each lane two channels x SUB tokens.
 constexpr int SC = 16;
 constexpr int SUB = 8;
-// Every ANCHOR-th chunk (counted from the start in the forward, from the end in the
-// backward) publishes its chunk-boundary state; a tile's look-back composes the aggregates of
-// the chunks after the nearest anchor and applies them to that anchor's state.  The carry
-// each tile sees is therefore a fixed expression of the inputs, independent of timing: the
-// scan is bitwise deterministic.
-constexpr int ANCHOR = 8;
+// Look-back of the SIMT scan kernels.  Chunks are counted in processing order (from the start
+// in the forward, from the end in the backward); every STEP-th chunk publishes its
+// chunk-boundary state, and a chunk q applies the aggregates of the chunks after its anchor
+// to the anchor's state, the anchor being the nearest publishing chunk at least DIST
+// chunks back (or, for q < DIST, the initial state).  Tiles are handed out in chunk order
+// and about a dozen chunks' tiles are resident at once, so the anchor's state has normally
+// been published before it is asked for.  The carry each tile sees is a fixed expression of
+// the inputs, independent of timing: the scan is bitwise deterministic.
+// The backward keeps fewer tiles resident (more registers per thread) than the forward, so
+// each direction has its own distance and step.
+template <bool BWD>
+struct LbPlan {
+  static constexpr int DIST = BWD ? 12 : 8;
+  static constexpr int STEP = BWD ? 4 : 2;
+  static constexpr int MAX = DIST + STEP - 2;  // aggregates composed at most
+};
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
@@ -154,10 +164,13 @@ struct GateBwdLayout {
   size_t dw_part, db_part, total;
 };
 
+// The partials start past a 256-byte header: the first word of a workspace is the status word
+// that the scan backward sets and rglru_sync_status reads, so a projection backward run after
+// it on the same workspace must leave that word alone.
 inline GateBwdLayout gate_bwd_layout(const Dims& d) {
   GateBwdLayout L;
   const int S = dw_splits(d);
-  L.dw_part = 0;
+  L.dw_part = 256;
   L.db_part = align_up((size_t)S * 2 * d.nblk * d.k * d.k * 4, 256);
   L.total = align_up(L.db_part + (size_t)S * 2 * d.W * 4, 256);
   return L;

@@ -12,12 +12,13 @@
 // serially in float32 registers; the two halves are joined with one shuffle of their affine
 // aggregates (A, B) (h -> A h + B, composed as (A2, B2) o (A1, B1) = (A2 A1, A2 B1 + B2)).
 // Across tiles the carry travels by decoupled look-back: each tile publishes its aggregate and
-// composes its predecessors' aggregates back to the nearest anchor chunk (every ANCHOR-th),
-// whose boundary state it applies them to; anchors then publish their own boundary state.
-// Stopping at fixed anchors rather than at whichever state happens to be published first
-// keeps the rounding, and so the result, independent of timing.  Tiles are handed out by an
-// atomic ticket in dependency order, so
-// every tile a warp waits on is held by a warp that is already running; waits are bounded.
+// composes its predecessors' aggregates back to its anchor chunk (every STEP-th, at least
+// DIST back, or the initial state; LbPlan), whose boundary state it applies them to; anchors then
+// publish their own boundary state.  All of a look-back's flags are polled together and its
+// aggregates loaded together.  Stopping at fixed anchors rather than at whichever state
+// happens to be published first keeps the rounding, and so the result, independent of
+// timing.  Tiles are handed out by an atomic ticket in dependency order, so every tile a warp
+// waits on is held by a warp that is already running; waits are bounded.
 #include "common.cuh"
 #include "internal.h"
 
@@ -49,8 +50,93 @@ __device__ __forceinline__ Tile grab_tile(uint32_t* ticket, int B, int nC, int n
   return r;
 }
 
+// The look-back span of processing-order chunk q: `anchor` (-1: the initial state) and the
+// n aggregates of chunks q-1 .. q-n composed onto it.
+template <bool BWD>
+__device__ __forceinline__ void lb_span(int q, int& anchor, int& n) {
+  using LP = LbPlan<BWD>;
+  if (q < LP::DIST) {
+    anchor = -1;
+    n = q;
+  } else {
+    anchor = ((q - LP::DIST) / LP::STEP) * LP::STEP;
+    n = q - 1 - anchor;
+  }
+}
+
+// Polls a tile's look-back flags together: bit k < n is the aggregate of processing-order
+// chunk q-1-k (FLAG_AGG), bit n the anchor's boundary state (FLAG_INCL; none when anchor < 0).
+// Each round issues one load per flag still short before testing any, so a round costs one
+// L2 round trip however many flags are late.  Returns the mask of the flags seen set; after
+// `limit` rounds the timeout is recorded in *status and the caller goes on without the
+// missing ones.  fbase: the flag of (row, chunk 0, group); ng: the flag stride per chunk.
+template <bool reverse>
+__device__ __forceinline__ uint32_t poll_flags(const uint32_t* fbase, int ng, int q, int n,
+                                               int anchor, int nC, int limit, uint32_t* status) {
+  constexpr int LB_MAX = LbPlan<reverse>::MAX;
+  const uint32_t all = anchor >= 0 ? (2u << n) - 1u : (1u << n) - 1u;
+  uint32_t got = 0u;
+  for (int round = 0;; ++round) {
+    if (got == all) return got;
+    if (round > limit) {
+      atomicOr(status, STATUS_TIMEOUT);
+      return got;
+    }
+    if (round > 0) __nanosleep(64);
+    const uint32_t want = all & ~got;
+    uint32_t f[LB_MAX + 1];
+#pragma unroll
+    for (int k = 0; k <= LB_MAX; ++k) {
+      f[k] = 0u;
+      if ((want >> k) & 1u) {
+        const int pq = k < n ? q - 1 - k : anchor;
+        f[k] = ld_acquire(fbase + (size_t)(reverse ? nC - 1 - pq : pq) * ng);
+      }
+    }
+#pragma unroll
+    for (int k = 0; k <= LB_MAX; ++k)
+      if (((want >> k) & 1u) && f[k] >= (k < n ? FLAG_AGG : FLAG_INCL)) got |= 1u << k;
+  }
+}
+
+// Composes the aggregates the poll found (chunk q-1-k for bit k, float4 = two channels'
+// (A, B) at agg + (row_chunk0 + chunk) * W) newest first onto the state `hp`, in batches
+// of seven loads.
+template <bool reverse>
+__device__ __forceinline__ void lb_compose(const float2* agg, size_t row_c0, int W, int w,
+                                           int q, int n, uint32_t got, int nC, float2 hp,
+                                           float (&out)[2]) {
+  constexpr int LB_MAX = LbPlan<reverse>::MAX;
+  float accA[2] = {1.0f, 1.0f}, accB[2] = {0.0f, 0.0f};
+#pragma unroll
+  for (int k0 = 0; k0 < LB_MAX; k0 += 7) {
+    float4 ag[7];
+#pragma unroll
+    for (int u = 0; u < 7; ++u) {
+      const int k = k0 + u;
+      if (k < n && ((got >> k) & 1u)) {
+        const int pq = q - 1 - k;
+        ag[u] = __ldcg(reinterpret_cast<const float4*>(
+            agg + (row_c0 + (size_t)(reverse ? nC - 1 - pq : pq)) * W + w));
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < 7; ++u) {
+      const int k = k0 + u;
+      if (k < n && ((got >> k) & 1u)) {
+        accB[0] = fmaf(accA[0], ag[u].y, accB[0]);
+        accA[0] *= ag[u].x;
+        accB[1] = fmaf(accA[1], ag[u].w, accB[1]);
+        accA[1] *= ag[u].z;
+      }
+    }
+  }
+  out[0] = fmaf(accA[0], hp.x, accB[0]);
+  out[1] = fmaf(accA[1], hp.y, accB[1]);
+}
+
 template <typename XT, typename LT, bool CANON>
-__global__ void __launch_bounds__(128) k_scan_fwd(ScanFwdArgs a) {
+__global__ void __launch_bounds__(128, 5) k_scan_fwd(ScanFwdArgs a) {
   uint32_t* status = reinterpret_cast<uint32_t*>(a.scratch);
   uint32_t* ticket = status + 1;
   uint32_t* flags = reinterpret_cast<uint32_t*>(a.scratch + a.L.flags);
@@ -126,47 +212,30 @@ __global__ void __launch_bounds__(128) k_scan_fwd(ScanFwdArgs a) {
   const size_t cidx = ((size_t)tl.b * a.nC + tl.c);
   uint32_t* my_flag = flags + cidx * a.ng + tl.g;
   const bool publish = (int)tl.ticket != a.drop_tile;
+  // Every chunk publishes its aggregate (the chunks before DIST compose back to chunk 0).
+  if (half == 1 && wok)
+    *reinterpret_cast<float4*>(agg + cidx * a.W + w) = make_float4(At[0], Bt[0], At[1], Bt[1]);
+  __threadfence();
+  __syncwarp();
+  if (lane == 16 && publish) st_release(my_flag, FLAG_AGG);
+  // Look-back: the aggregates of the chunks after the anchor, applied to the state after the
+  // anchor (or to h0).
   float hin[2] = {0.0f, 0.0f};
-  if (tl.c == 0) {
-    if (CANON && a.h0 && wok) {
-      hin[0] = a.h0[(size_t)tl.b * a.W + w];
-      hin[1] = a.h0[(size_t)tl.b * a.W + w + 1];
-    }
-  } else {
-    if (half == 1 && wok)
-      *reinterpret_cast<float4*>(agg + cidx * a.W + w) = make_float4(At[0], Bt[0], At[1], Bt[1]);
-    __threadfence();
-    __syncwarp();
-    if (lane == 16 && publish) st_release(my_flag, FLAG_AGG);
-    float accA[2] = {1.0f, 1.0f}, accB[2] = {0.0f, 0.0f};
-    int cur = tl.c - 1;
-    while (true) {
-      const size_t pidx = (size_t)tl.b * a.nC + cur;
-      const bool anchor = (cur % ANCHOR) == 0;
-      const uint32_t f = spin_flag(flags + pidx * a.ng + tl.g, anchor ? FLAG_INCL : FLAG_AGG,
-                                   a.spin_limit, status);
-      if (f == FLAG_TIMEOUT) {
-        hin[0] = accB[0];
-        hin[1] = accB[1];
-        break;
+  {
+    int an, n;
+    lb_span<false>(tl.c, an, n);
+    const uint32_t got = poll_flags<false>(flags + (size_t)tl.b * a.nC * a.ng + tl.g, a.ng, tl.c,
+                                           n, an, a.nC, a.spin_limit, status);
+    if (wok) {
+      float2 hp = make_float2(0.0f, 0.0f);
+      if (an >= 0) {
+        if ((got >> n) & 1u)
+          hp = __ldcg(reinterpret_cast<const float2*>(
+              carry + ((size_t)tl.b * (a.nC + 1) + an + 1) * a.W + w));
+      } else if (CANON && a.h0) {
+        hp = make_float2(a.h0[(size_t)tl.b * a.W + w], a.h0[(size_t)tl.b * a.W + w + 1]);
       }
-      if (anchor) {
-        if (wok) {
-          const float2 hp =
-              __ldcg(reinterpret_cast<const float2*>(carry + ((size_t)tl.b * (a.nC + 1) + cur + 1) * a.W + w));
-          hin[0] = fmaf(accA[0], hp.x, accB[0]);
-          hin[1] = fmaf(accA[1], hp.y, accB[1]);
-        }
-        break;
-      }
-      if (wok) {
-        const float4 ag = __ldcg(reinterpret_cast<const float4*>(agg + pidx * a.W + w));
-        accB[0] = fmaf(accA[0], ag.y, accB[0]);
-        accA[0] *= ag.x;
-        accB[1] = fmaf(accA[1], ag.w, accB[1]);
-        accA[1] *= ag.z;
-      }
-      --cur;
+      lb_compose<false>(agg, (size_t)tl.b * a.nC, a.W, w, tl.c, n, got, a.nC, hp, hin);
     }
   }
 
@@ -183,7 +252,7 @@ __global__ void __launch_bounds__(128) k_scan_fwd(ScanFwdArgs a) {
   }
   __threadfence();
   __syncwarp();
-  if (lane == 16 && publish && tl.c % ANCHOR == 0) st_release(my_flag, FLAG_INCL);
+  if (lane == 16 && publish && tl.c % LbPlan<false>::STEP == 0) st_release(my_flag, FLAG_INCL);
 
   // Outputs: y = local state + (product of abar) * state entering this half.
   float hs[2];
@@ -340,46 +409,30 @@ __global__ void __launch_bounds__(128) k_scan_bwd(ScanBwdArgs a) {
   const size_t cidx = ((size_t)tl.b * a.nC + tl.c);
   uint32_t* my_flag = flags + cidx * a.ng + tl.g;
   const bool publish = (int)tl.ticket != a.drop_tile;
+  const int q = a.nC - 1 - tl.c;  // processing order: from the last chunk
+  if (half == 0 && wok)
+    *reinterpret_cast<float4*>(agg + cidx * a.W + w) = make_float4(At[0], Bt[0], At[1], Bt[1]);
+  __threadfence();
+  __syncwarp();
+  if (lane == 0 && publish) st_release(my_flag, FLAG_AGG);
+  // Look-back toward the end: the aggregates of the chunks between this one and the anchor,
+  // applied to the carry the anchor passes left (or to dhT).
   float cin[2] = {0.0f, 0.0f};
-  if (tl.c == a.nC - 1) {
-    if (a.dhT && wok) {
-      cin[0] = a.dhT[(size_t)tl.b * a.W + w];
-      cin[1] = a.dhT[(size_t)tl.b * a.W + w + 1];
-    }
-  } else {
-    if (half == 0 && wok)
-      *reinterpret_cast<float4*>(agg + cidx * a.W + w) = make_float4(At[0], Bt[0], At[1], Bt[1]);
-    __threadfence();
-    __syncwarp();
-    if (lane == 0 && publish) st_release(my_flag, FLAG_AGG);
-    float accA[2] = {1.0f, 1.0f}, accB[2] = {0.0f, 0.0f};
-    int cur = tl.c + 1;
-    while (true) {
-      const size_t pidx = (size_t)tl.b * a.nC + cur;
-      const bool anchor = ((a.nC - 1 - cur) % ANCHOR) == 0;
-      const uint32_t f = spin_flag(flags + pidx * a.ng + tl.g, anchor ? FLAG_INCL : FLAG_AGG,
-                                   a.spin_limit, status);
-      if (f == FLAG_TIMEOUT) {
-        cin[0] = accB[0];
-        cin[1] = accB[1];
-        break;
+  {
+    int an, n;
+    lb_span<true>(q, an, n);
+    const uint32_t got = poll_flags<true>(flags + (size_t)tl.b * a.nC * a.ng + tl.g, a.ng, q, n,
+                                          an, a.nC, a.spin_limit, status);
+    if (wok) {
+      float2 cv = make_float2(0.0f, 0.0f);
+      if (an >= 0) {
+        if ((got >> n) & 1u)
+          cv = __ldcg(reinterpret_cast<const float2*>(
+              rcar + ((size_t)tl.b * a.nC + (a.nC - 1 - an)) * a.W + w));
+      } else if (a.dhT) {
+        cv = make_float2(a.dhT[(size_t)tl.b * a.W + w], a.dhT[(size_t)tl.b * a.W + w + 1]);
       }
-      if (anchor) {
-        if (wok) {
-          const float2 cv = __ldcg(reinterpret_cast<const float2*>(rcar + pidx * a.W + w));
-          cin[0] = fmaf(accA[0], cv.x, accB[0]);
-          cin[1] = fmaf(accA[1], cv.y, accB[1]);
-        }
-        break;
-      }
-      if (wok) {
-        const float4 ag = __ldcg(reinterpret_cast<const float4*>(agg + pidx * a.W + w));
-        accB[0] = fmaf(accA[0], ag.y, accB[0]);
-        accA[0] *= ag.x;
-        accB[1] = fmaf(accA[1], ag.w, accB[1]);
-        accA[1] *= ag.z;
-      }
-      ++cur;
+      lb_compose<true>(agg, (size_t)tl.b * a.nC, a.W, w, q, n, got, a.nC, cv, cin);
     }
   }
   const float co0 = fmaf(At[0], cin[0], Bt[0]);
@@ -394,7 +447,8 @@ __global__ void __launch_bounds__(128) k_scan_bwd(ScanBwdArgs a) {
   }
   __threadfence();
   __syncwarp();
-  if (lane == 0 && publish && (a.nC - 1 - tl.c) % ANCHOR == 0) st_release(my_flag, FLAG_INCL);
+  if (lane == 0 && publish && (a.nC - 1 - tl.c) % LbPlan<true>::STEP == 0)
+    st_release(my_flag, FLAG_INCL);
 
   // Outputs.
   float ch[2];

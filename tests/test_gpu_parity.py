@@ -198,6 +198,39 @@ def check_fused(wl, inp, got, gst, ba=None, bx=None, sl=slice(None)):
         assert_close(k, got[k], g[k], io=wl.io, kind="grad")
 
 
+def test_unfused_step_on_one_workspace():
+    """The unfused training step on one workspace (scan backward, then the projection
+    backward): the status word the scan leaves in the workspace survives the projection
+    backward's partial sums, and those give bitwise the gradients of a run on a workspace of
+    their own."""
+    wl = W_("bf16-unfused", 2, 130, 256, 128, "bf16", "canonical", reset_p=0.05, h0_std=1.0)
+    inp = generate(wl, 31, want_logits=True)
+    sh = shape_for(wl)
+    d = {k: dev(v) for k, v in inp.items()}
+    y = torch.empty_like(d["x"])
+    hT = torch.empty(wl.B, wl.W, device="cuda")
+    dx, dlr, dli = (torch.empty_like(d["x"]) for _ in range(3))
+    dL = torch.empty(wl.W, device="cuda")
+    dh0 = torch.empty(wl.B, wl.W, device="cuda")
+    saved, ws = R.alloc_saved(sh), R.alloc_workspace(sh)
+    R.rglru_forward(sh, d["x"], d["lr"], d["li"], d["Lambda"], d["reset_mask"],
+                    d["segment_pos"], d["h0"], y, hT, saved)
+    R.rglru_backward(sh, d["dy"], d["dhT"], d["x"], d["lr"], d["li"], d["Lambda"],
+                     d["reset_mask"], d["segment_pos"], d["h0"], saved, dx, dlr, dli, dL, dh0, ws)
+    grads = []
+    for w in (ws, R.alloc_workspace(sh)):
+        dxw = dx.clone()
+        g = [torch.empty(wl.nblk, wl.k, wl.k, device="cuda") for _ in range(2)]
+        b = [torch.empty(wl.W, device="cuda") for _ in range(2)]
+        R.rglru_gate_proj_backward(sh, dlr, dli, d["x"], d["Wa"], d["Wx"], dxw, g[0], b[0], g[1],
+                                   b[1], w)
+        grads.append([dxw] + g + b)
+    assert R.rglru_sync_status(saved) == R.OK
+    assert R.rglru_sync_status(ws) == R.OK
+    for a, b in zip(*grads):
+        assert torch.equal(a, b)
+
+
 @pytest.mark.parametrize("wl,seed,grad", FUSED_CASES,
                          ids=[c[0].name + ("-g" + c[2] if c[2] else "") for c in FUSED_CASES])
 def test_fused_forward_backward(wl, seed, grad):
