@@ -193,19 +193,38 @@ __global__ void __launch_bounds__(256) k_dw_part(int BT, int W, int k, int nblk,
   }
 }
 
-// Split partials of the bias gradients: dbp[split][gate][w] = sum_{n in split} G[n, w].
+// Split partials of the bias gradients: dbp[split][gate][w] = sum_{n in split} G[n, w].  A
+// thread takes two channels (one 4- or 8-byte load per token) and four interleaved running
+// sums, combined in a fixed order, so the result does not depend on timing.
 template <typename GT>
 __global__ void __launch_bounds__(256) k_db_part(int BT, int W, int splits, const GT* gr,
                                                  const GT* gi, float* dbp) {
-  const int w = blockIdx.x * 256 + threadIdx.x;
+  const int w = (blockIdx.x * 256 + threadIdx.x) * 2;
   const int gate = blockIdx.y, split = blockIdx.z;
   if (w >= W) return;
   const GT* g = gate ? gi : gr;
   const long per = (BT + splits - 1) / splits;
   const long nb = split * per, ne = min((long)BT, nb + per);
-  float s = 0.0f;
-  for (long n = nb; n < ne; ++n) s += to_f32(g[(size_t)n * W + w]);
-  dbp[((size_t)split * 2 + gate) * W + w] = s;
+  float s0[4] = {0.0f, 0.0f, 0.0f, 0.0f}, s1[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+  long n = nb;
+  for (; n + 4 <= ne; n += 4) {
+    float2 v[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) v[u] = Pair<GT>::load(g + (size_t)(n + u) * W + w);
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      s0[u] += v[u].x;
+      s1[u] += v[u].y;
+    }
+  }
+  for (; n < ne; ++n) {
+    const float2 v = Pair<GT>::load(g + (size_t)n * W + w);
+    s0[0] += v.x;
+    s1[0] += v.y;
+  }
+  float* out = dbp + ((size_t)split * 2 + gate) * W + w;
+  out[0] = (s0[0] + s0[1]) + (s0[2] + s0[3]);
+  out[1] = (s1[0] + s1[1]) + (s1[2] + s1[3]);
 }
 
 // out[e] = sum over splits (in split order) of part[split][e], for `count` elements.
@@ -262,15 +281,16 @@ cudaError_t dwk(const Dims& d, const void* x, const void* gr, const void* gi, fl
                                                                    2 * per_gate, dWx);
   note_launches(1);
   if (dba || dbx) {
-    k_db_part<GT><<<dim3((d.W + 255) / 256, 2, S), 256, 0, s>>>(BT, d.W, S, (const GT*)gr,
-                                                                (const GT*)gi, dbp);
+    const int SD = db_splits(d);
+    k_db_part<GT><<<dim3((d.W + 511) / 512, 2, SD), 256, 0, s>>>(BT, d.W, SD, (const GT*)gr,
+                                                                 (const GT*)gi, dbp);
     note_launches(1);
     if (dba) {
-      k_sum_splits<<<(d.W + 255) / 256, 256, 0, s>>>(dbp, S, (size_t)d.W, 2 * (size_t)d.W, dba);
+      k_sum_splits<<<(d.W + 255) / 256, 256, 0, s>>>(dbp, SD, (size_t)d.W, 2 * (size_t)d.W, dba);
       note_launches(1);
     }
     if (dbx) {
-      k_sum_splits<<<(d.W + 255) / 256, 256, 0, s>>>(dbp + d.W, S, (size_t)d.W, 2 * (size_t)d.W,
+      k_sum_splits<<<(d.W + 255) / 256, 256, 0, s>>>(dbp + d.W, SD, (size_t)d.W, 2 * (size_t)d.W,
                                                      dbx);
       note_launches(1);
     }

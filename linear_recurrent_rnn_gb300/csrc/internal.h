@@ -160,6 +160,19 @@ inline int dw_splits(const Dims& d) {
   return (int)s;
 }
 
+// Token splits of the bias-gradient partial sums: about 600 CTAs of 512 channels (two per
+// thread) x one gate, each split at least 64 tokens.
+inline int db_splits(const Dims& d) {
+  const long cols = (long)((d.W + 511) / 512) * 2;
+  const long BT = (long)d.B * d.T;
+  long s = (600 + cols - 1) / cols;
+  const long smax = (BT + 63) / 64;
+  if (s > smax) s = smax;
+  if (s < 1) s = 1;
+  if (s > 256) s = 256;
+  return (int)s;
+}
+
 struct GateBwdLayout {
   size_t dw_part, db_part, total;
 };
@@ -171,8 +184,8 @@ inline GateBwdLayout gate_bwd_layout(const Dims& d) {
   GateBwdLayout L;
   const int S = dw_splits(d);
   L.dw_part = 256;
-  L.db_part = align_up((size_t)S * 2 * d.nblk * d.k * d.k * 4, 256);
-  L.total = align_up(L.db_part + (size_t)S * 2 * d.W * 4, 256);
+  L.db_part = align_up(L.dw_part + (size_t)S * 2 * d.nblk * d.k * d.k * 4, 256);
+  L.total = align_up(L.db_part + (size_t)db_splits(d) * 2 * d.W * 4, 256);
   return L;
 }
 
