@@ -250,9 +250,11 @@ __global__ void __launch_bounds__(128, 5) k_scan_fwd(ScanFwdArgs a) {
     if (half == 1 && tl.c == a.nC - 1 && a.hT)
       *reinterpret_cast<float2*>(a.hT + (size_t)tl.b * a.W + w) = make_float2(he0, he1);
   }
-  __threadfence();
-  __syncwarp();
-  if (lane == 16 && publish && tl.c % LbPlan<false>::STEP == 0) st_release(my_flag, FLAG_INCL);
+  if (tl.c % LbPlan<false>::STEP == 0) {  // only anchors publish their state (warp-uniform)
+    __threadfence();
+    __syncwarp();
+    if (lane == 16 && publish) st_release(my_flag, FLAG_INCL);
+  }
 
   // Outputs: y = local state + (product of abar) * state entering this half.
   float hs[2];
@@ -445,10 +447,11 @@ __global__ void __launch_bounds__(128) k_scan_bwd(ScanBwdArgs a) {
           CANON ? make_float2(co0, co1) : make_float2(0.0f, 0.0f);
     }
   }
-  __threadfence();
-  __syncwarp();
-  if (lane == 0 && publish && (a.nC - 1 - tl.c) % LbPlan<true>::STEP == 0)
-    st_release(my_flag, FLAG_INCL);
+  if ((a.nC - 1 - tl.c) % LbPlan<true>::STEP == 0) {  // only anchors publish (warp-uniform)
+    __threadfence();
+    __syncwarp();
+    if (lane == 0 && publish) st_release(my_flag, FLAG_INCL);
+  }
 
   // Outputs.
   float ch[2];
