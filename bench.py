@@ -124,16 +124,30 @@ def workload():
     return WORKLOADS[2]
 
 
-def algorithmic_bytes(wl):
-    """Compulsory HBM bytes per step: every input read once, every output written once.
-    fwd: x (2N) read, y (2N) written, Wa/Wx, biases, Lambda read, hT written.
-    bwd: x, dy (4N) read, dx (2N) written, Wa/Wx, biases, Lambda read, dWa/dWx (f32), dba,
-    dbx, dLambda written.  Saved chunk states and look-back flags are overhead, not counted."""
+def algorithmic_bytes(wl, grad=None):
+    """Compulsory HBM bytes of one fused forward and one fused backward: every input read
+    once, every output written once.  s = bytes of an activation element (the I/O dtype),
+    g = bytes of a dx element (the gradient dtype; the I/O dtype unless given).
+    fwd: x read and y written (2sN), Wa/Wx, biases, Lambda read, hT written; canonical inputs
+         also read h0 and the reset markers (uint8 mask or int32 segment positions).
+    bwd: x, dy read (2sN), dx written (gN), Wa/Wx, biases, Lambda read, dWa/dWx (float32),
+         dba, dbx, dLambda written; canonical inputs also read dhT and the markers and write
+         dh0.  Saved chunk states and look-back slots are overhead, not counted."""
     N = wl.B * wl.T * wl.W
-    wbytes = 2 * wl.nblk * wl.k * wl.k * 2
+    s = 2 if wl.io == "bf16" else 4
+    g = s if grad is None else (2 if grad == "bf16" else 4)
+    wbytes = 2 * wl.nblk * wl.k * wl.k * s
     vec = wl.W * 4
-    fwd = 4 * N + wbytes + 3 * vec + wl.B * wl.W * 4
-    bwd = 6 * N + wbytes + 3 * vec + 2 * wl.nblk * wl.k * wl.k * 4 + 3 * vec
+    state = wl.B * wl.W * 4
+    marks = 0
+    if wl.mode == "canonical":
+        marks = wl.B * wl.T * (4 if wl.seg_len is not None else 1) if (
+            wl.seg_len is not None or wl.reset_p > 0 or wl.reset_t0) else 0
+    h0 = state if (wl.mode == "canonical" and wl.h0_std > 0) else 0
+    fwd = 2 * s * N + wbytes + 3 * vec + state + h0 + marks
+    bwd = (2 * s + g) * N + wbytes + 3 * vec + 2 * wl.nblk * wl.k * wl.k * 4 + 3 * vec + marks
+    if wl.mode == "canonical":
+        bwd += 2 * state   # dhT read, dh0 written
     return fwd, bwd
 
 
@@ -153,8 +167,30 @@ def measured_peaks():
 
 
 # DRAM traffic of one k_fused_bwd launch at B4 T2048 W2048 (dram__bytes_read.sum +
-# dram__bytes_write.sum, ncu --set full; 70.51 MB + 13.51 MB), taken on the current kernel.
-TRAFFIC_BYTES = 84017664
+# dram__bytes_write.sum from one ncu capture; writes still resident in L2 when the kernel
+# ends are not counted).  It holds for the kernel sources whose hash is recorded beside it;
+# when they have changed since, the line reports null until the counters are taken again.
+TRAFFIC = {"bytes": None, "sources_sha16": None}
+KERNEL_SOURCES = ("fused_bwd.cu", "tc.cuh", "common.cuh", "lookback.cuh", "internal.h")
+
+
+def kernel_sources_sha16():
+    import hashlib
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "linear_recurrent_rnn_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def traffic_field():
+    sha = kernel_sources_sha16()
+    ok = TRAFFIC["bytes"] is not None and TRAFFIC["sources_sha16"] == sha
+    return (TRAFFIC["bytes"] if ok else None,
+            {"source": "ncu dram__bytes_read.sum + dram__bytes_write.sum, one launch",
+             "kernel_sources_sha16": sha, "captured_on_sha16": TRAFFIC["sources_sha16"],
+             "note": "null when the kernel changed after the capture; L2-resident writes at "
+                     "the kernel's end are not counted"})
 
 
 def run_ours(args, rank, world, local):
@@ -273,10 +309,11 @@ def run_ours(args, rank, world, local):
         del g
 
     # end to end through the C ABI with host buffers: H2D of x and dy from pinned memory, the
-    # step, D2H of the parameter gradients, all inside the events
+    # step, D2H of every result (y, dx and the parameter gradients), all inside the events
     hx = inp["x"].pin_memory()
     hdy = inp["dy"].pin_memory()
-    hout = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in (dWa, dWx, dba, dbx, dL)]
+    results = (y, dx, dWa, dWx, dba, dbx, dL)
+    hout = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in results]
     e2e_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
     for k in range(args.warmup + args.steps):
         if k >= args.warmup:
@@ -286,7 +323,7 @@ def run_ours(args, rank, world, local):
         dy.copy_(hdy, non_blocking=True)
         fwd()
         bwd()
-        for h, d in zip(hout, (dWa, dWx, dba, dbx, dL)):
+        for h, d in zip(hout, results):
             h.copy_(d, non_blocking=True)
         if k >= args.warmup:
             e2e_ev[k - args.warmup][1].record(stream)
@@ -296,6 +333,7 @@ def run_ours(args, rank, world, local):
     d2h = sum(h.numel() * h.element_size() for h in hout)
 
     fwd_b, bwd_b = algorithmic_bytes(wl)
+    traffic_bytes, traffic_src = traffic_field()
     peaks = measured_peaks()
     peak = peaks.get("hbm_gbs")
     kern_ms = [e[0].elapsed_time(e[1]) for e in kev]
@@ -326,7 +364,8 @@ def run_ours(args, rank, world, local):
                      "achieved": achieved, "peak": peak,
                      "frac": (achieved / peak) if peak else None,
                      "peak_source": "measured (hbm_gbs)",
-                     "algorithmic_bytes": bwd_b, "traffic": TRAFFIC_BYTES,
+                     "algorithmic_bytes": bwd_b, "traffic": traffic_bytes,
+                     "traffic_source": traffic_src,
                      "kernel_ms_mean": kern_mean,
                      # context bound: the same kernel against the tensor pipe, and the larger
                      # of the two bounds (bytes / measured copy bandwidth, flops / measured
@@ -355,6 +394,9 @@ def run_ours(args, rank, world, local):
         line["varlen"] = varlen_measure(flush, peak)
     if rank == 0 and world == 1 and not args.no_unfused:
         line["unfused"] = unfused_measure(flush, peak)
+        line["protocol"] = protocol_measure(flush)
+    if rank == 0 and world == 1 and not args.no_configs:
+        line["configs"] = configs_measure(flush, peak)
     if rank == 0 and world == 1 and not args.no_delta:
         line["delta_rule"] = delta_rule_measure(flush, peak)
     if rank == 0:
@@ -472,8 +514,8 @@ def varlen_measure(flush, peak, reps=10, W=2048, k=128, T=8192, seed=5):
     if R.rglru_sync_status(saved) != R.OK or R.rglru_sync_status(ws) != R.OK:
         raise RuntimeError("look-back timeout in the packed-sequence measurement")
     fms, bms, kms = statistics.median(tf), statistics.median(tb), statistics.median(tk)
-    _, bwd_b = algorithmic_bytes(wl)
-    bwd_b += 3 * S * W * 4
+    _, bwd_b = algorithmic_bytes(wl.scaled(mode="restricted"))
+    bwd_b += 3 * S * W * 4   # per-sequence h0, dhT read, dh0 written
     gbs = bwd_b / (kms / 1e3) / 1e9
     return {"workload": f"packed B1 T{T} W{W} k{k} bf16 canonical, {S} sequences of U[1, 2048] "
                         "tokens, per-sequence h0 and dhT",
@@ -483,6 +525,154 @@ def varlen_measure(flush, peak, reps=10, W=2048, k=128, T=8192, seed=5):
                              "achieved": gbs, "peak": peak,
                              "frac": (gbs / peak) if peak else None,
                              "algorithmic_bytes": bwd_b, "kernel_ms": kms}}
+
+
+def stats(v):
+    return {"median": statistics.median(v), "min": min(v), "max": max(v),
+            "mean": statistics.fmean(v)}
+
+
+def configs_measure(flush, peak, reps=10, cfgs=(1, 3, 4, 5)):
+    """The other synthetic workloads of the layer's specification through the fused calls
+    (rglru_fused_forward + rglru_fused_backward), each with its own seeded inputs: forward and
+    forward + backward milliseconds (L2 flushed before each sample; the two calls back to back
+    inside the pair), tokens/s of the pair, and the pair's compulsory bytes against the
+    measured copy bandwidth and against 8 TB/s.  Gradients are stored in the I/O dtype, as in
+    the headline.  `path` names the kernels the shape takes."""
+    import torch
+    from linear_recurrent_rnn_gb300 import librglru as R
+    from linear_recurrent_rnn_gb300.inputs import WORKLOADS, generate
+    out = {}
+    for cfg in cfgs:
+        wl = WORKLOADS[cfg]
+        inp = generate(wl, cfg)
+        d = {n: (v.cuda() if isinstance(v, torch.Tensor) else v) for n, v in inp.items()}
+        del inp
+        io = R.BF16 if wl.io == "bf16" else R.F32
+        mode = R.CANONICAL if wl.mode == "canonical" else R.RESTRICTED
+        sh = R.make_shape(wl.B, wl.T, wl.W, wl.nblk, io, io, mode)
+        x = d["x"]
+        y = torch.empty_like(x)
+        hT = torch.empty(wl.B, wl.W, device="cuda")
+        saved, ws = R.alloc_saved(sh), R.alloc_workspace(sh)
+        dx = torch.empty_like(x)
+        dWa = torch.empty(wl.nblk, wl.k, wl.k, device="cuda")
+        dWx = torch.empty_like(dWa)
+        dba, dbx, dL = (torch.empty(wl.W, device="cuda") for _ in range(3))
+        dh0 = torch.empty(wl.B, wl.W, device="cuda") if wl.mode == "canonical" else None
+        args_f = (sh, x, d["Wa"], d["ba"], d["Wx"], d["bx"], d["Lambda"], d["reset_mask"],
+                  d["segment_pos"], d["h0"], y, hT, saved)
+        fwd = lambda: R.rglru_fused_forward(*args_f)
+        bwd = lambda: R.rglru_fused_backward(sh, d["dy"], d["dhT"], x, d["Wa"], d["ba"], d["Wx"],
+                                             d["bx"], d["Lambda"], d["reset_mask"],
+                                             d["segment_pos"], d["h0"], saved, dx, dWa, dba,
+                                             dWx, dbx, dL, dh0, ws)
+        for _ in range(3):
+            fwd()
+            bwd()
+        torch.cuda.synchronize()
+        n0 = R.rglru_kernel_launches()
+        fwd()
+        n1 = R.rglru_kernel_launches()
+        bwd()
+        n2 = R.rglru_kernel_launches()
+        tf, tp = [], []
+        for _ in range(reps):
+            flush.zero_()
+            e = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+            e[0].record()
+            fwd()
+            e[1].record()
+            bwd()
+            e[2].record()
+            torch.cuda.synchronize()
+            tf.append(e[0].elapsed_time(e[1]))
+            tp.append(e[0].elapsed_time(e[2]))
+        if R.rglru_sync_status(saved) != R.OK or R.rglru_sync_status(ws) != R.OK:
+            raise RuntimeError(f"look-back timeout in configuration {cfg}")
+        fb, bb = algorithmic_bytes(wl)
+        pm = statistics.median(tp)
+        gbs = (fb + bb) / (pm / 1e3) / 1e9
+        out[str(cfg)] = {
+            "workload": wl.name, "B": wl.B, "T": wl.T, "W": wl.W, "k": wl.k, "io": wl.io,
+            "mode": wl.mode, "path": R.fused_path(sh),
+            "kernels": {"fwd": n1 - n0, "bwd": n2 - n1},
+            "fwd_ms": stats(tf), "fwd_bwd_ms": stats(tp),
+            "tokens_per_s": wl.B * wl.T / (pm / 1e3),
+            "algorithmic_bytes": fb + bb, "achieved_gbs": gbs,
+            "hbm_frac_measured": (gbs / peak) if peak else None,
+            "hbm_frac_of_8TBps": gbs / 8e3}
+        del d, x, y, dx, saved, ws
+        torch.cuda.empty_cache()
+    return out
+
+
+def protocol_measure(flush, reps=5):
+    """The pages' timing protocol at the headline shape: two rounds, the fused and the unfused
+    variant in A-B order in the first and B-A in the second, `reps` samples of each per round
+    (10 per variant), every sample the forward and then the backward with events around each
+    and the L2 flushed before it; median / min / max / mean of forward and forward + backward.
+    Unfused = rglru_gate_proj + rglru_forward, then rglru_backward + rglru_gate_proj_backward."""
+    import torch
+    from linear_recurrent_rnn_gb300 import librglru as R
+    from linear_recurrent_rnn_gb300.inputs import WORKLOADS, generate
+    wl = WORKLOADS[2]
+    inp = generate(wl, 2)
+    d = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+    sh = R.make_shape(wl.B, wl.T, wl.W, wl.nblk, R.BF16, R.BF16, R.RESTRICTED)
+    x = d["x"]
+    lr, li, y, dx, dlr, dli = (torch.empty_like(x) for _ in range(6))
+    hT = torch.empty(wl.B, wl.W, device="cuda")
+    dL, dba, dbx = (torch.empty(wl.W, device="cuda") for _ in range(3))
+    dWa = torch.empty(wl.nblk, wl.k, wl.k, device="cuda")
+    dWx = torch.empty_like(dWa)
+    saved, ws = R.alloc_saved(sh), R.alloc_workspace(sh)
+    Wa, Wx, ba, bx, L, dy = d["Wa"], d["Wx"], d["ba"], d["bx"], d["Lambda"], d["dy"]
+
+    def fused_f():
+        R.rglru_fused_forward(sh, x, Wa, ba, Wx, bx, L, None, None, None, y, hT, saved)
+
+    def fused_b():
+        R.rglru_fused_backward(sh, dy, None, x, Wa, ba, Wx, bx, L, None, None, None, saved, dx,
+                               dWa, dba, dWx, dbx, dL, None, ws)
+
+    def unf_f():
+        R.rglru_gate_proj(sh, x, Wa, ba, Wx, bx, lr, li)
+        R.rglru_forward(sh, x, lr, li, L, None, None, None, y, hT, saved)
+
+    def unf_b():
+        R.rglru_backward(sh, dy, None, x, lr, li, L, None, None, None, saved, dx, dlr, dli, dL,
+                         None, ws)
+        R.rglru_gate_proj_backward(sh, dlr, dli, x, Wa, Wx, dx, dWa, dba, dWx, dbx, ws)
+
+    variants = {"fused": (fused_f, fused_b), "unfused": (unf_f, unf_b)}
+    for f, b in variants.values():
+        for _ in range(3):
+            f()
+            b()
+    torch.cuda.synchronize()
+    res = {n: {"fwd": [], "fwd_bwd": []} for n in variants}
+    for order in (("fused", "unfused"), ("unfused", "fused")):
+        for n in order:
+            f, b = variants[n]
+            for _ in range(reps):
+                flush.zero_()
+                e = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+                e[0].record()
+                f()
+                e[1].record()
+                b()
+                e[2].record()
+                torch.cuda.synchronize()
+                res[n]["fwd"].append(e[0].elapsed_time(e[1]))
+                res[n]["fwd_bwd"].append(e[0].elapsed_time(e[2]))
+    if R.rglru_sync_status(saved) != R.OK or R.rglru_sync_status(ws) != R.OK:
+        raise RuntimeError("look-back timeout in the protocol measurement")
+    out = {"workload": wl.name, "rounds": "2 x 5 samples per variant, AB then BA",
+           "unit": "ms"}
+    for n, r in res.items():
+        out[n] = {"fwd_ms": stats(r["fwd"]), "fwd_bwd_ms": stats(r["fwd_bwd"])}
+    return out
 
 
 def unfused_measure(flush, peak, reps=10):
@@ -767,6 +957,8 @@ def main(argv=None):
                    help="skip the packed-sequence (varlen) measurement")
     p.add_argument("--no-unfused", action="store_true",
                    help="skip the unfused-API (scan kernels over stored logits) measurement")
+    p.add_argument("--no-configs", action="store_true",
+                   help="skip the other synthetic workloads (configurations 1, 3, 4, 5)")
     p.add_argument("--cpu-sample-T", type=int, default=2048)
     p.add_argument("--ref-sample-T", type=int, default=256)
     args = p.parse_args(argv)

@@ -3,8 +3,9 @@
  * per key channel), forward and backward, on one NVIDIA GB300 (sm_103a).  Compiled into
  * librglru; the same status codes, dtypes and stream conventions as librglru.h.
  *
- * Source of the operation: [P3] "linear_attention.reference" — the recurrent reference's
- * entry: GDN (scalar decay) or KDA (per-key decay) exact token recurrence; q, k [B, T, Hk, Dk],
+ * Source of the operation: [P3] "linear_attention.reference", entry
+ * recurrent_delta_rule_reference: a token-by-token form of the rule whose decay is one number
+ * per value head (GDN) or one per key channel (KDA); q, k [B, T, Hk, Dk],
  * v [B, T, Hv, Dv], beta [B, T, Hv], g [B, T, Hv] (GDN) or [B, T, Hv, Dk] (KDA); the state
  * [N, Hv, Dk, Dv] or, value first, [N, Hv, Dv, Dk]; output and final state returned, gradients
  * through the initial state; gates are natural logarithms; q, k, v, beta already normalised or

@@ -140,12 +140,21 @@ rglru_status rglru_gate_proj_backward(const rglru_shape *shape, const void *dlr,
  * needing more (about 0.75 * B*T*W bytes, e.g. B4 T2048 W2048 fits) returns
  * RGLRU_ERR_UNSUPPORTED.  The first call on each device finds the array's device address
  * (cudaGetSymbolAddress) and should come before any stream capture.  All calls share the
- * array; calls whose work overlaps on the GPU race on it. */
+ * array; calls whose work overlaps on the GPU race on it.  A look-back wait that runs out
+ * marks the status word inside the array (the results of that call are then wrong, and the
+ * call itself still returns RGLRU_OK): read it with rglru_forward_noalloc_status before the
+ * next call, which clears it. */
 #define RGLRU_NOALLOC_SCRATCH_BYTES ((size_t)16 << 20)
 rglru_status rglru_forward_noalloc(const rglru_shape *shape, const void *x, const void *lr,
                                    const void *li, const float *Lambda,
                                    const uint8_t *reset_mask, const int32_t *segment_pos,
                                    const float *h0, void *y, float *hT, rglru_stream stream);
+
+/* Status of the last rglru_forward_noalloc call on the current device (no counterpart on the
+ * pages): synchronises `stream`, then reads the status word of the static scratch;
+ * RGLRU_ERR_TIMEOUT if a bounded look-back wait of that call ran out, RGLRU_OK otherwise
+ * (RGLRU_ERR_CUDA if the read fails).  Allocates nothing. */
+rglru_status rglru_forward_noalloc_status(rglru_stream stream);
 
 /* Fused forward: the projections folded into the recurrence [P1 closing paragraph credits
  * the fusion strategy; the logits are never rounded to the I/O dtype].  Same outputs as
@@ -232,6 +241,10 @@ void rglru_debug_lookback(int32_t spin_limit, int32_t drop_tile);
  * caller can time that kernel alone with cudaEventElapsedTime.  (NULL, NULL) cancels.
  * Process-wide; not thread-safe. */
 void rglru_debug_kernel_events(void *start, void *stop);
+
+/* Which kernels rglru_fused_forward / rglru_fused_backward run for `shape` (no counterpart on
+ * the pages): a short static description, "invalid shape" if the shape is rejected. */
+const char *rglru_fused_path(const rglru_shape *shape);
 
 /* Launch accounting (no counterpart on the pages): the number of CUDA kernels this library
  * has enqueued since the process started (memsets excluded).  Lets a caller count the

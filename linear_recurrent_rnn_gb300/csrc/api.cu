@@ -434,6 +434,15 @@ rglru_status rglru_sync_status(const void* buf, rglru_stream stream) {
   return word ? RGLRU_ERR_TIMEOUT : RGLRU_OK;
 }
 
+const char* rglru_fused_path(const rglru_shape* shape) {
+  Dims d;
+  if (make_dims(shape, &d) != RGLRU_OK) return "invalid shape";
+  if (fused_supported(d))
+    return "fused: k_fused_fwd / k_fused_bwd (tcgen05 projections and CUDA-core scan in one "
+           "kernel each)";
+  return "composed: float32 SIMT projections, CUDA-core scan kernels (float32 logits kept)";
+}
+
 uint64_t rglru_kernel_launches(void) { return g_launches.load(std::memory_order_relaxed); }
 
 void rglru_debug_kernel_events(void* start, void* stop) {

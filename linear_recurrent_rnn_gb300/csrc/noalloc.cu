@@ -86,4 +86,15 @@ rglru_status rglru_forward_noalloc(const rglru_shape* shape, const void* x, cons
   return cuda_status(e);
 }
 
+rglru_status rglru_forward_noalloc_status(rglru_stream stream) {
+  void* scratch = nullptr;
+  cudaError_t e = scratch_address(&scratch);
+  if (e != cudaSuccess) return cuda_status(e);
+  uint32_t word = 0;
+  e = cudaStreamSynchronize(stream);
+  if (e == cudaSuccess) e = cudaMemcpy(&word, scratch, sizeof(word), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_status(e);
+  return word ? RGLRU_ERR_TIMEOUT : RGLRU_OK;
+}
+
 }  // extern "C"

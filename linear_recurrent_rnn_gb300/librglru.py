@@ -54,6 +54,7 @@ EXPORTS = ("rglru_status_string", "rglru_saved_bytes", "rglru_workspace_bytes",
            "rglru_gate_proj", "rglru_forward", "rglru_backward", "rglru_gate_proj_backward",
            "rglru_fused_forward", "rglru_fused_backward", "rglru_sync_status",
            "rglru_debug_lookback", "rglru_kernel_launches", "rglru_forward_noalloc",
+           "rglru_forward_noalloc_status", "rglru_fused_path",
            "rglru_debug_kernel_events", "rglru_step", "rglru_fused_forward_varlen",
            "rglru_fused_backward_varlen", "delta_rule_saved_bytes", "delta_rule_workspace_bytes",
            "delta_rule_forward", "delta_rule_backward", "delta_rule_state_fp8_qdq")
@@ -94,6 +95,10 @@ def lib():
             L.rglru_debug_lookback.restype = None
             L.rglru_forward_noalloc.argtypes = [S] + [P] * 10
             L.rglru_forward_noalloc.restype = ctypes.c_int
+            L.rglru_forward_noalloc_status.argtypes = [P]
+            L.rglru_forward_noalloc_status.restype = ctypes.c_int
+            L.rglru_fused_path.argtypes = [S]
+            L.rglru_fused_path.restype = ctypes.c_char_p
             L.rglru_debug_kernel_events.argtypes = [ctypes.c_void_p, ctypes.c_void_p]
             L.rglru_debug_kernel_events.restype = None
             L.rglru_step.argtypes = [S] + [P] * 11
@@ -137,6 +142,11 @@ def make_shape(B, T, W, nblk, io=BF16, grad=None, mode=CANONICAL) -> Shape:
     elif isinstance(grad, torch.dtype):
         grad = _DT[grad]
     return Shape(int(B), int(T), int(W), int(nblk), int(io), int(grad), int(mode))
+
+
+def fused_path(shape: Shape) -> str:
+    """Which kernels the fused calls run for this shape (a description from the library)."""
+    return lib().rglru_fused_path(ctypes.byref(shape)).decode()
 
 
 def saved_bytes(shape: Shape) -> int:
@@ -204,6 +214,12 @@ def rglru_forward_noalloc(shape, x, lr, li, Lambda, reset_mask, segment_pos, h0,
     _check("rglru_forward_noalloc", lib().rglru_forward_noalloc(
         ctypes.byref(shape), _p(x), _p(lr), _p(li), _p(Lambda), _p(reset_mask), _p(segment_pos),
         _p(h0), _p(y), _p(hT), _stream(stream)))
+
+
+def rglru_forward_noalloc_status(stream=None) -> int:
+    """Synchronises the stream and returns the status word of the last rglru_forward_noalloc
+    call on the current device (the next call clears it)."""
+    return int(lib().rglru_forward_noalloc_status(_stream(stream)))
 
 
 def rglru_gate_proj_backward(shape, dlr, dli, x, Wa, Wx, dx, dWa, dba, dWx, dbx, workspace,

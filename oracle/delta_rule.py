@@ -5,8 +5,9 @@ head and token; KDA: one decay per key channel), forward and hand-derived backwa
 check the CUDA library element by element.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
 CPU-baseline leg of ``bench.py`` may import it; it shares no code with the CUDA library.
 
-Passages followed ("linear_attention.reference" page, the recurrent reference's entry): the
-exact token recurrence of GDN (scalar decay) or KDA (per-key decay); inputs q, k [B, T, Hk, Dk],
+Passages followed ("linear_attention.reference" page, entry recurrent_delta_rule_reference):
+the rule stepped one token at a time, with its decay one number per value head (GDN) or one
+per key channel (KDA); inputs q, k [B, T, Hk, Dk],
 v [B, T, Hv, Dv], beta [B, T, Hv], g [B, T, Hv] (GDN) or [B, T, Hv, Dk] (KDA); the state
 [N, Hv, Dk, Dv] (key first) or [N, Hv, Dv, Dk] with state_v_first; the output and the final
 state returned, with gradients through the initial state; gates given as natural logarithms;

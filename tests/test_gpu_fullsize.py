@@ -81,3 +81,33 @@ def test_full_size_sampled_blocks(cfg):
         for name in ("dba", "dbx", "dLambda"):
             assert_close(tag + name, host(got[name][cs]), g[name], io=wl.io, kind="grad")
         assert_close(tag + "dh0", host(got["dh0"][:, cs]), g["dh0"], io=wl.io, kind="grad")
+
+
+def test_full_size_headline_float32_gradients():
+    """The headline workload (B4 T2048 W2048, restricted) with float32-stored gradients, so the
+    gradient bound is the literal E <= 2e-3 with no allowance for a bf16 rounding of the
+    stored value; sampled gate blocks as above."""
+    cfg = 2
+    wl = WORKLOADS[cfg]
+    inp = generate(wl, cfg)
+    sh = shape_for(wl, "f32")
+    got = _run(wl, inp, sh)
+    assert got["dx"].dtype == torch.float32
+    for blk in (1, wl.nblk - 2):
+        k = wl.k
+        cs = slice(blk * k, (blk + 1) * k)
+        o = {name: as_f64(_sl(inp[name], blk, k)) for name in ("x", "dy", "ba", "bx", "Lambda")}
+        Wa = as_f64(inp["Wa"][blk:blk + 1])
+        Wx = as_f64(inp["Wx"][blk:blk + 1])
+        y, hT = oracle.fused_forward(oracle.RESTRICTED, o["x"], Wa, o["ba"], Wx, o["bx"],
+                                     o["Lambda"])
+        g = oracle.fused_backward(oracle.RESTRICTED, o["x"], Wa, o["ba"], Wx, o["bx"],
+                                  o["Lambda"], o["dy"])
+        tag = f"cfg2-g32 blk{blk} "
+        assert_close(tag + "y", host(got["y"][..., cs]), y, io=wl.io, kind="out")
+        assert_close(tag + "dx", host(got["dx"][..., cs]), g["dx"], io=wl.io, kind="grad",
+                     stored="f32")
+        assert_close(tag + "dWa", host(got["dWa"][blk:blk + 1]), g["dWa"], io=wl.io, kind="grad")
+        assert_close(tag + "dWx", host(got["dWx"][blk:blk + 1]), g["dWx"], io=wl.io, kind="grad")
+        for name in ("dba", "dbx", "dLambda"):
+            assert_close(tag + name, host(got[name][cs]), g[name], io=wl.io, kind="grad")

@@ -3,14 +3,17 @@ inside another owner's stream capture, under a fixed memory pool, in an allocati
 real-time loop, or in a plugin handed only its inputs and outputs).  It keeps its look-back
 scratch in the library's static per-GPU array instead of a caller `saved` buffer.
 
-Checked through the C ABI against rglru_forward, the entry point that takes a caller buffer,
-on two calls in a row with different shapes and modes (so the second call sees the first
-call's leftovers in the shared array), within the tolerance the other parity tests use.
-This file is collected last so that a failure here leaves every other test already run."""
+Checked through the C ABI on two calls in a row with different shapes and modes (so the
+second call sees the first call's leftovers in the shared array): against rglru_forward, the
+entry point that takes a caller buffer and runs the same kernel on the same inputs, bit for
+bit; and against the float64 oracle within the tolerance of the other parity tests.  A
+dropped look-back publish must show up in rglru_forward_noalloc_status.  This file is
+collected last so that a failure here leaves every other test already run."""
 import pytest
 import torch
 
-from helpers import assert_close, dev, host, shape_for
+import oracle
+from helpers import assert_close, dev, host, mode_id, oracle_inputs, shape_for
 from linear_recurrent_rnn_gb300 import build as B_
 from linear_recurrent_rnn_gb300 import librglru as R
 from linear_recurrent_rnn_gb300.inputs import Workload, generate
@@ -35,11 +38,12 @@ def _both(wl, seed):
     h_ref = torch.empty(wl.B, wl.W, device="cuda")
     saved = R.alloc_saved(sh)
     R.rglru_forward(sh, *args, y_ref, h_ref, saved)
+    assert R.rglru_sync_status(saved) == R.OK
     y = torch.full_like(d["x"], float("nan"))
     h = torch.full((wl.B, wl.W), float("nan"), device="cuda")
     R.rglru_forward_noalloc(sh, *args, y, h)
-    torch.cuda.synchronize()
-    return y, h, y_ref, h_ref
+    assert R.rglru_forward_noalloc_status() == R.OK
+    return inp, y, h, y_ref, h_ref
 
 
 def test_noalloc_forward_matches_forward_twice():
@@ -47,9 +51,38 @@ def test_noalloc_forward_matches_forward_twice():
                      h0_std=1.0)
     second = Workload("noalloc-2", 3, 1000, 128, 128, "bf16", "restricted")
     for wl, seed in ((first, 51), (second, 52)):
-        y, h, y_ref, h_ref = _both(wl, seed)
-        assert_close("y", host(y), host(y_ref), io=wl.io, kind="out")
-        assert_close("hT", host(h), host(h_ref), io=wl.io, kind="out")
+        inp, y, h, y_ref, h_ref = _both(wl, seed)
+        # the same kernel on the same inputs: equal bit for bit
+        assert torch.equal(y, y_ref)
+        assert torch.equal(h, h_ref)
+        o = oracle_inputs(inp)
+        yo, ho = oracle.forward(mode_id(wl), o["x"], o["lr"], o["li"], o["Lambda"],
+                                o["reset_mask"], o["segment_pos"], o["h0"])
+        assert_close("y", host(y), yo, io=wl.io, kind="out")
+        assert_close("hT", host(h), ho, io=wl.io, kind="out")
+
+
+def test_noalloc_timeout_is_reported():
+    """A scan tile that never publishes makes its successor's bounded wait run out; the call
+    finishes, and the status query of the static scratch reports the timeout.  The next call
+    clears the word."""
+    wl = Workload("noalloc-timeout", 1, 128, 64, 64, "bf16", "restricted")
+    inp = generate(wl, 43, want_logits=True)
+    sh = shape_for(wl)
+    d = {k: dev(v) for k, v in inp.items()}
+    y = torch.empty_like(d["x"])
+    R.rglru_debug_lookback(2000, 5)
+    try:
+        R.rglru_forward_noalloc(sh, d["x"], d["lr"], d["li"], d["Lambda"], None, None, None, y,
+                                None)
+        assert R.rglru_forward_noalloc_status() == R.ERR_TIMEOUT
+    finally:
+        R.rglru_debug_lookback(0, -1)
+    R.rglru_forward_noalloc(sh, d["x"], d["lr"], d["li"], d["Lambda"], None, None, None, y, None)
+    assert R.rglru_forward_noalloc_status() == R.OK
+    o = oracle_inputs(inp)
+    yo, _ = oracle.forward(oracle.RESTRICTED, o["x"], o["lr"], o["li"], o["Lambda"])
+    assert_close("y", host(y), yo, io="bf16", kind="out")
 
 
 def test_noalloc_rejects_shapes_beyond_the_static_scratch():
