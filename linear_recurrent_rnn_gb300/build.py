@@ -17,7 +17,7 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "librglru.so")
 SOURCES = ["api.cu", "scan_simt.cu", "gemm_simt.cu", "noalloc.cu", "host_util.cu", "fused_fwd.cu", "fused_bwd.cu",
-           "decode.cu", "varlen.cu", "delta_rule.cu"]
+           "decode.cu", "varlen.cu", "delta_rule.cu", "proj_tc.cu"]
 HEADERS = ["common.cuh", "internal.h", "tc.cuh", "host_util.h", "lookback.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",

@@ -91,6 +91,19 @@ ComposedLayout composed_saved(const Dims& d) {
   C.total = align_up(C.li + d.N * 4, 256);
   return C;
 }
+// Scratch of the projection backward inside a workspace: the SIMT kernels' partial sums, or
+// the tensor-core kernels' per-CTA dW / db partials, both after a 256-byte header (a scan
+// backward run on the same workspace keeps its status word there).
+constexpr size_t PROJ_PART_OFFSET = 256;
+size_t gate_bwd_ws_bytes(const Dims& d) {
+  size_t a = gate_bwd_layout(d).total;
+  if (proj_tc_supported(d)) {
+    const size_t b = PROJ_PART_OFFSET + proj_dw_part_bytes(d);
+    if (b > a) a = b;
+  }
+  return a;
+}
+
 struct ComposedWs {
   size_t dxd, dlr, dli, gate, total;  // within `workspace`, after the backward scan layout
 };
@@ -101,7 +114,7 @@ ComposedWs composed_ws(const Dims& d) {
   C.dlr = align_up(C.dxd + d.N * 4, 256);
   C.dli = align_up(C.dlr + d.N * 4, 256);
   C.gate = align_up(C.dli + d.N * 4, 256);
-  C.total = align_up(C.gate + gate_bwd_layout(d).total, 256);
+  C.total = align_up(C.gate + gate_bwd_ws_bytes(d), 256);
   return C;
 }
 
@@ -154,6 +167,7 @@ ScanBwdArgs bwd_args(const Dims& d, const void* dy, const float* dhT, const void
   a.dx = dx;
   a.dlr = dlr;
   a.dli = dli;
+  a.dl_plane = d.N;
   a.dLambda = dLambda;
   a.dh0 = dh0;
   a.scratch = static_cast<uint8_t*>(ws);
@@ -196,7 +210,7 @@ size_t rglru_workspace_bytes(const rglru_shape* shape) {
   Dims d;
   if (make_dims(shape, &d) != RGLRU_OK) return 0;
   size_t m = scan_layout(d, true).total;
-  const size_t g = gate_bwd_layout(d).total;
+  const size_t g = gate_bwd_ws_bytes(d);
   const size_t f = fused_supported(d) ? fused_bwd_layout(d).total : composed_ws(d).total;
   if (g > m) m = g;
   if (f > m) m = f;
@@ -211,6 +225,8 @@ rglru_status rglru_gate_proj(const rglru_shape* shape, const void* x, const void
   if (st != RGLRU_OK) return st;
   if (!req(x) || !req(Wa) || !req(Wx) || !req(lr) || !req(li) || !opt(ba) || !opt(bx))
     return RGLRU_ERR_INVALID_ARG;
+  if (proj_tc_supported(d))
+    return cuda_status(launch_proj_fwd(d, d.io, x, Wa, ba, Wx, bx, lr, li, stream));
   return cuda_status(launch_gate_proj_simt(d, d.io, d.io, x, Wa, ba, Wx, bx, lr, li, stream));
 }
 
@@ -260,11 +276,20 @@ rglru_status rglru_gate_proj_backward(const rglru_shape* shape, const void* dlr,
   if (!req(dlr) || !req(dli) || !req(x) || !req(Wa) || !req(Wx) || !req(dx) || !req(dWa) ||
       !req(dWx) || !opt(dba) || !opt(dbx) || !req(workspace))
     return RGLRU_ERR_INVALID_ARG;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  if (proj_tc_supported(d) && d.grad == RGLRU_BF16) {
+    // one bf16 plane per gradient; dx accumulates in place
+    cudaError_t e = launch_proj_dx(d, DT_BF16, dlr, dli, d.N, 1, Wa, Wx, dx, 0, dx, stream);
+    if (e == cudaSuccess)
+      e = launch_proj_dw(d, x, dlr, dli, d.N, 1,
+                         reinterpret_cast<float*>(ws + PROJ_PART_OFFSET), dWa, dba, dWx, dbx,
+                         stream);
+    return cuda_status(e);
+  }
   cudaError_t e =
       launch_gate_dx_simt(d, d.io, d.grad, d.grad, dlr, dli, Wa, Wx, nullptr, dx, stream);
   if (e == cudaSuccess)
-    e = launch_gate_dw_simt(d, d.io, d.grad, x, dlr, dli, dWa, dba, dWx, dbx,
-                            static_cast<uint8_t*>(workspace), stream);
+    e = launch_gate_dw_simt(d, d.io, d.grad, x, dlr, dli, dWa, dba, dWx, dbx, ws, stream);
   return cuda_status(e);
 }
 
@@ -285,8 +310,11 @@ rglru_status rglru_fused_forward(const rglru_shape* shape, const void* x, const 
                                         h0, y, hT, saved, g_spin_limit, g_drop_tile, stream));
   uint8_t* sv = static_cast<uint8_t*>(saved);
   const ComposedLayout C = composed_saved(d);
-  cudaError_t e = launch_gate_proj_simt(d, d.io, DT_F32, x, Wa, ba, Wx, bx, sv + C.lr, sv + C.li,
-                                        stream);
+  cudaError_t e =
+      proj_tc_supported(d)
+          ? launch_proj_fwd(d, DT_F32, x, Wa, ba, Wx, bx, sv + C.lr, sv + C.li, stream)
+          : launch_gate_proj_simt(d, d.io, DT_F32, x, Wa, ba, Wx, bx, sv + C.lr, sv + C.li,
+                                  stream);
   const ScanFwdArgs a = fwd_args(d, x, sv + C.lr, sv + C.li, Lambda, reset_mask, segment_pos, h0,
                                  y, hT, saved);
   if (e == cudaSuccess) e = cudaMemsetAsync(saved, 0, a.L.zero_bytes, stream);
@@ -326,6 +354,20 @@ rglru_status rglru_fused_backward(const rglru_shape* shape, const void* dy, cons
                                  workspace);
   // The direct term of dx stays float32 until the projections are added: one rounding.
   if (e == cudaSuccess) e = cudaMemsetAsync(workspace, 0, a.L.zero_bytes, stream);
+  if (proj_tc_supported(d)) {
+    // dlr, dli as bf16 hi + lo planes (the same bytes as float32), the operands of the
+    // tensor-core products
+    if (e == cudaSuccess)
+      e = launch_scan_bwd(a, d.io, DT_F32, DT_F32, DT_SPLIT, d.mode == RGLRU_CANONICAL, stream);
+    if (e == cudaSuccess)
+      e = launch_proj_dx(d, d.grad, ws + CW.dlr, ws + CW.dli, d.N, 2, Wa, Wx, ws + CW.dxd, 1,
+                         dx, stream);
+    if (e == cudaSuccess)
+      e = launch_proj_dw(d, x, ws + CW.dlr, ws + CW.dli, d.N, 2,
+                         reinterpret_cast<float*>(ws + CW.gate + PROJ_PART_OFFSET), dWa, dba,
+                         dWx, dbx, stream);
+    return cuda_status(e);
+  }
   if (e == cudaSuccess)
     e = launch_scan_bwd(a, d.io, DT_F32, DT_F32, DT_F32, d.mode == RGLRU_CANONICAL, stream);
   if (e == cudaSuccess)
@@ -440,6 +482,9 @@ const char* rglru_fused_path(const rglru_shape* shape) {
   if (fused_supported(d))
     return "fused: k_fused_fwd / k_fused_bwd (tcgen05 projections and CUDA-core scan in one "
            "kernel each)";
+  if (proj_tc_supported(d))
+    return "composed: tcgen05 projections (k_proj_fwd, k_proj_dx, k_proj_dw), CUDA-core scan "
+           "kernels (float32 logits kept)";
   return "composed: float32 SIMT projections, CUDA-core scan kernels (float32 logits kept)";
 }
 

@@ -38,6 +38,28 @@ struct Pair<bf16> {
   static __device__ __forceinline__ float load1(const bf16* p) { return __bfloat162float(*p); }
 };
 
+// A float32 value stored as two bf16 planes `plane` elements apart: hi = bf16(v) and
+// lo = bf16(v - hi) (v - hi is exact in float32), so hi + lo carries v to ~2^-16 relative and
+// each plane can be an operand of a bf16 tensor-core product.
+struct SplitBf16 {};
+template <typename T>
+struct OutPair {
+  using E = T;
+  static __device__ __forceinline__ void store(E* p, size_t, float a, float b) {
+    Pair<T>::store(p, a, b);
+  }
+};
+template <>
+struct OutPair<SplitBf16> {
+  using E = bf16;
+  static __device__ __forceinline__ void store(bf16* p, size_t plane, float a, float b) {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    const float2 hf = __bfloat1622float2(h);
+    *reinterpret_cast<__nv_bfloat162*>(p) = h;
+    *reinterpret_cast<__nv_bfloat162*>(p + plane) = __floats2bfloat162_rn(a - hf.x, b - hf.y);
+  }
+};
+
 template <typename T>
 __device__ __forceinline__ T from_f32(float v);
 template <>

@@ -221,6 +221,7 @@ struct ScanBwdArgs {
   void* dx;
   void* dlr;
   void* dli;
+  size_t dl_plane;   // DT_SPLIT gradients: elements between the hi and lo planes
   float* dLambda;
   float* dh0;
   uint8_t* scratch;  // `workspace`
@@ -246,8 +247,9 @@ ScanFwdArgs fwd_args(const Dims& d, const void* x, const void* lr, const void* l
                      const float* Lambda, const uint8_t* rm, const int32_t* sp, const float* h0,
                      void* y, float* hT, void* saved);
 
-// dtype codes used by the launchers (io of x/y/dy, of the logits, of dx, of dlr/dli)
-enum { DT_F32 = RGLRU_F32, DT_BF16 = RGLRU_BF16 };
+// dtype codes used by the launchers (io of x/y/dy, of the logits, of dx, of dlr/dli);
+// DT_SPLIT: float32 values written as bf16 hi and lo planes (SplitBf16)
+enum { DT_F32 = RGLRU_F32, DT_BF16 = RGLRU_BF16, DT_SPLIT = 2 };
 
 cudaError_t launch_scan_fwd(const ScanFwdArgs& a, int xt, int lt, bool canonical,
                             cudaStream_t s);
@@ -284,6 +286,24 @@ cudaError_t launch_step(const Dims& d, const void* x, const void* Wa, const floa
                         const void* Wx, const float* bx, const float* Lambda,
                         const uint8_t* reset, const float* h_in, void* y, float* h_out,
                         cudaStream_t s);
+
+// Tensor-core projections (proj_tc.cu): bf16 operands, float32 accumulation, k a multiple of
+// 16 up to PROJ_TC_KMAX.  The gradient operands dlr, dli are `nplanes` bf16 planes each
+// ([plane][R][W], plane stride plane_elems elements): one plane, or hi + lo of a float32
+// value.  dx = add + dl W^T (add float32 or bf16, may alias dx); dW / db through
+// per-CTA partial sums (proj_dw_part_bytes) reduced in a fixed order.
+constexpr int PROJ_TC_KMAX = 160;
+bool proj_tc_supported(const Dims& d);
+size_t proj_dw_part_bytes(const Dims& d);
+cudaError_t launch_proj_fwd(const Dims& d, int ot, const void* x, const void* Wa,
+                            const float* ba, const void* Wx, const float* bx, void* lr, void* li,
+                            cudaStream_t s);
+cudaError_t launch_proj_dx(const Dims& d, int ot, const void* dlr, const void* dli,
+                           size_t plane_elems, int nplanes, const void* Wa, const void* Wx,
+                           const void* add, int add_f32, void* dx, cudaStream_t s);
+cudaError_t launch_proj_dw(const Dims& d, const void* x, const void* dlr, const void* dli,
+                           size_t plane_elems, int nplanes, float* part, float* dWa, float* dba,
+                           float* dWx, float* dbx, cudaStream_t s);
 
 // SIMT projections (float32 accumulation).
 cudaError_t launch_gate_proj_simt(const Dims& d, int xt, int ot, const void* x, const void* Wa,

@@ -1,0 +1,838 @@
+// Block-diagonal gate projections and their gradients on the tcgen05 tensor cores: bf16
+// operands staged by TMA, float32 accumulation in tensor memory, for gate blocks of
+// k = 16 .. 160 channels (k a multiple of 16).
+//
+// Sources ("Fattori comparison" page, first paragraph: the two block-diagonal gate projections
+// feed the recurrence; the benchmark record's protocol scope puts them inside the measured
+// layer).  Rows r run over the B T tokens; per gate block blk:
+//   forward   lr[r, blk k + j]  = sum_i x[r, blk k + i] Wa[blk][i][j] + ba[blk k + j]
+//             li                = the same with Wx, bx
+//   backward  dx[r, blk k + i]  = add[r, blk k + i] + sum_j dlr[r, blk k + j] Wa[blk][i][j]
+//                                                   + sum_j dli[r, blk k + j] Wx[blk][i][j]
+//             dWa[blk][i][j]    = sum_r x[r, blk k + i] dlr[r, blk k + j],  dba = sum_r dlr
+//             dWx, dbx          = the same with dli
+// The gradient operands dlr / dli come as one bf16 plane, or as two (hi + lo, v = hi + lo to
+// ~2^-16) when they were float32: each plane is one more product into the same accumulator.
+//
+// Every operand tile is 128 rows of one gate block, loaded by TMA as 16-channel slabs with
+// the 32-byte swizzle (128 rows x 32 bytes = 4 KB a slab): a slab is one K = 16 step of a
+// K-major operand, and 16 consecutive M or N indices of an MN-major one.  One CTA per SM:
+// warp 0 issues the TMA loads, warp 1 the MMAs (one elected lane), warps 2..5 read the
+// accumulators back (warp w reaches TMEM lanes 32 (w % 4) .. 32 (w % 4) + 31, so it owns those
+// rows of a tile).  Pipeline waits are bounded (2 s); a wait that runs out winds the CTA down.
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+
+#include "host_util.h"
+#include "internal.h"
+#include "tc.cuh"
+
+namespace rglru {
+
+namespace {
+
+constexpr int TR = 128;                   // rows of a tile
+constexpr uint32_t SLAB = TR * 32;        // one 16-channel slab of a tile
+constexpr int NTHREADS = 192;             // TMA, MMA, 4 epilogue warps
+constexpr uint64_t WAIT_NS = 2000000000ull;
+constexpr size_t SMEM_MAX = 232448;       // 227 KB of dynamic shared memory per CTA
+constexpr int NBOX = 4;                   // output staging boxes per epilogue warp
+
+// Bytes of one operand tile (128 rows x k bf16).
+__host__ __device__ constexpr uint32_t tile_bytes(int k) { return (uint32_t)(k / 16) * SLAB; }
+// TMEM columns of a k-wide accumulator, rounded up to a multiple of 32.
+__host__ __device__ constexpr uint32_t kcols(int k) { return (uint32_t)((k + 31) / 32 * 32); }
+// Bytes past the dW kernel's operand ring that an x operand may read (see k_proj_dw).
+__host__ __device__ constexpr uint32_t dw_pad(int k) {
+  return (uint32_t)((k + 127) / 128) * 8 * SLAB - tile_bytes(k);
+}
+
+struct Abort {
+  uint32_t* flag;  // shared: set once a wait has run out; every later wait returns at once
+  __device__ bool wait(uint64_t* bar, uint32_t parity) const {
+    if (*reinterpret_cast<volatile uint32_t*>(flag)) return false;
+    if (tc::mbar_wait(bar, parity, WAIT_NS)) return true;
+    *reinterpret_cast<volatile uint32_t*>(flag) = 1u;
+    return false;
+  }
+};
+
+// A row of 16 float32 values written into a staging box of 32 rows x 16 columns of T, laid
+// out as the TMA store with the matching swizzle expects (bf16: 32-byte rows, 32-byte swizzle;
+// float32: 64-byte rows, 64-byte swizzle).  Conflict-free: the eight lanes of a quarter warp
+// land in eight different 16-byte bank groups.
+template <typename T>
+__device__ __forceinline__ void stage_row(uint8_t* box, int row, const float (&v)[16]);
+template <>
+__device__ __forceinline__ void stage_row<bf16>(uint8_t* box, int row, const float (&v)[16]) {
+#pragma unroll
+  for (int c = 0; c < 2; ++c) {
+    uint4 q;
+    uint32_t* w = &q.x;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const __nv_bfloat162 h = __floats2bfloat162_rn(v[8 * c + 2 * u], v[8 * c + 2 * u + 1]);
+      w[u] = *reinterpret_cast<const uint32_t*>(&h);
+    }
+    *reinterpret_cast<uint4*>(box + row * 32 + ((c ^ ((row >> 2) & 1)) << 4)) = q;
+  }
+}
+template <>
+__device__ __forceinline__ void stage_row<float>(uint8_t* box, int row, const float (&v)[16]) {
+#pragma unroll
+  for (int c = 0; c < 4; ++c)
+    *reinterpret_cast<float4*>(box + row * 64 + ((c ^ ((row >> 1) & 3)) << 4)) =
+        make_float4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
+}
+
+// Output staging of one epilogue warp: NBOX boxes used in turn, each freed once the TMA store
+// that last read it is done reading.
+template <typename T>
+struct Stager {
+  uint8_t* base;
+  uint32_t n;  // boxes used so far
+  static constexpr uint32_t BOX = 32 * 16 * sizeof(T);
+  __device__ uint8_t* next() {
+    uint8_t* b = base + (n % NBOX) * BOX;
+    if ((threadIdx.x & 31) == 0 && n >= NBOX) tc::tma_store_wait_read_n<NBOX - 1>();
+    __syncwarp();
+    ++n;
+    return b;
+  }
+  // Hands the box just written to the TMA store of rows [row0, row0 + 32), columns [col0, +16).
+  __device__ void store(const CUtensorMap* map, uint8_t* box, int col0, int row0) {
+    tc::fence_proxy_async_smem();
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) {
+      tc::tma_store_2d(map, box, col0, row0);
+      tc::tma_store_commit();
+    }
+  }
+  __device__ void drain() {
+    if ((threadIdx.x & 31) == 0) tc::tma_store_wait0();
+    __syncwarp();
+  }
+};
+
+struct ProjParams {
+  int R, k, nblk, P;     // rows, gate block, blocks, CTAs per (block, matrix group)
+  const float* bias[2];  // forward: ba, bx (null = zero)
+  const void* add;       // dx: the addend (float32 or bf16 [R][W]); may alias the output
+  int add_f32;
+  int W;
+  int nplanes;           // gradient operand planes (1, or 2 for hi + lo)
+  int nmat;              // dW: matrices per CTA (2: both; 1: CTA group m handles matrix m)
+  float* part;           // dW: partial sums [blk][r][m][k * k + k]
+};
+
+// ================================================================ forward projection
+// CTA (blk, r) keeps Wa[blk], Wx[blk] in shared memory and takes the row tiles r, r + P, ...
+// Per tile the x tile feeds two accumulations, lr then li, each into the next slot of a ring
+// of k-column TMEM buffers; the epilogue warps add the bias, convert and store.
+template <typename OT>
+__global__ void __launch_bounds__(NTHREADS, 1)
+    k_proj_fwd(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_wa,
+               const __grid_constant__ CUtensorMap tm_wx,
+               const __grid_constant__ CUtensorMap tm_lr,
+               const __grid_constant__ CUtensorMap tm_li, const __grid_constant__ ProjParams p,
+               int stages) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024u - (tc::smem_u32(smem_raw) & 1023u)) & 1023u);
+  const int k = p.k;
+  const uint32_t TB = tile_bytes(k);
+  const uint32_t WB = (uint32_t)k * k * 2;
+  const uint32_t KC = kcols(k);
+  const int NS = 512 / (int)KC;  // TMEM ring slots
+  uint8_t* s_w[2] = {smem, smem + WB};
+  uint8_t* s_x = smem + 2 * WB;
+  uint8_t* s_stage = s_x + stages * TB;
+  float* s_bias = reinterpret_cast<float*>(s_stage + 4 * NBOX * Stager<OT>::BOX);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(s_bias + 2 * k);
+  uint64_t* w_full = bars;
+  uint64_t* x_full = bars + 1;
+  uint64_t* x_empty = x_full + stages;
+  uint64_t* acc_full = x_empty + stages;  // [NS]
+  uint64_t* acc_empty = acc_full + NS;    // [NS]
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(acc_empty + NS);
+  uint32_t* abort_flag = tmem_holder + 1;
+  const Abort ctl{abort_flag};
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int blk = blockIdx.x / p.P, rr = blockIdx.x % p.P;
+  const int ntiles = (p.R + TR - 1) / TR;
+  int my_tiles = 0;
+  for (int n = rr; n < ntiles; n += p.P) ++my_tiles;
+
+  if (threadIdx.x == 0) {
+    tc::mbar_init(w_full, 1);
+    for (int s = 0; s < stages; ++s) {
+      tc::mbar_init(&x_full[s], 1);
+      tc::mbar_init(&x_empty[s], 1);
+    }
+    for (int s = 0; s < NS; ++s) {
+      tc::mbar_init(&acc_full[s], 1);
+      tc::mbar_init(&acc_empty[s], 4);
+    }
+    *abort_flag = 0u;
+    tc::fence_barrier_init();
+  }
+  for (int j = threadIdx.x; j < 2 * k; j += NTHREADS) {
+    const float* b = p.bias[j >= k];
+    s_bias[j] = b ? b[blk * k + (j % k)] : 0.0f;
+  }
+  if (warp == 0) {
+    tc::tmem_alloc(tmem_holder, 512);
+    tc::tmem_relinquish();
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      tc::prefetch_tmap(&tm_x);
+      tc::mbar_expect_tx(w_full, 2 * WB);
+      for (int s = 0; s < k / 16; ++s) {
+        tc::tma_load_2d(s_w[0] + s * (k * 32), &tm_wa, w_full, 16 * s, blk * k);
+        tc::tma_load_2d(s_w[1] + s * (k * 32), &tm_wx, w_full, 16 * s, blk * k);
+      }
+      for (int it = 0; it < my_tiles; ++it) {
+        const int st = it % stages;
+        if (!ctl.wait(&x_empty[st], ((it / stages) & 1) ^ 1u)) break;
+        const int row0 = (rr + it * p.P) * TR;
+        uint8_t* xs = s_x + st * TB;
+        tc::mbar_expect_tx(&x_full[st], TB);
+        for (int s = 0; s < k / 16; ++s)
+          tc::tma_load_2d(xs + s * SLAB, &tm_x, &x_full[st], blk * k + 16 * s, row0);
+      }
+    }
+  } else if (warp == 1) {
+    const bool leader = tc::elect_one();
+    const uint32_t idesc = tc::idesc_bf16(TR, k, 0, 1);  // A = x K-major, B = W MN-major
+    ctl.wait(w_full, 0);
+    for (int it = 0; it < my_tiles; ++it) {
+      const int st = it % stages;
+      if (!ctl.wait(&x_full[st], (it / stages) & 1)) break;
+      const uint32_t xs = tc::smem_u32(s_x + st * TB);
+#pragma unroll 1
+      for (int m = 0; m < 2; ++m) {
+        const int u = 2 * it + m, slot = u % NS;
+        if (!ctl.wait(&acc_empty[slot], ((u / NS) & 1) ^ 1u)) break;
+        tc::tc_fence_after();
+        const uint32_t ws = tc::smem_u32(s_w[m]);
+        if (leader) {
+          for (int kk = 0; kk < k / 16; ++kk)
+            tc::mma_bf16(tmem + slot * KC, tc::smem_desc_sw32(xs + kk * SLAB, 16, 256),
+                         tc::smem_desc_sw32(ws + kk * 512, (uint32_t)k * 32, 256), idesc, kk > 0);
+          tc::mma_commit(&acc_full[slot]);
+        }
+        __syncwarp();
+      }
+      if (leader) tc::mma_commit(&x_empty[st]);
+      __syncwarp();
+    }
+  } else {
+    const int q = warp & 3;  // TMEM lane quadrant = rows 32 q .. 32 q + 31 of a tile
+    Stager<OT> sg{s_stage + (warp - 2) * NBOX * Stager<OT>::BOX, 0u};
+    const CUtensorMap* out[2] = {&tm_lr, &tm_li};
+    for (int it = 0; it < my_tiles; ++it) {
+      const int row0 = (rr + it * p.P) * TR + 32 * q;
+#pragma unroll 1
+      for (int m = 0; m < 2; ++m) {
+        const int u = 2 * it + m, slot = u % NS;
+        if (!ctl.wait(&acc_full[slot], (u / NS) & 1)) break;
+        tc::tc_fence_after();
+        const uint32_t ta = tmem + ((uint32_t)(32 * q) << 16) + slot * KC;
+        for (int c = 0; c < k / 16; ++c) {
+          float v[16];
+          tc::tmem_ld16(ta + 16 * c, v);
+          tc::tmem_ld_wait();
+          tc::reg_fence(v);
+#pragma unroll
+          for (int e = 0; e < 16; ++e) v[e] += s_bias[m * k + 16 * c + e];
+          uint8_t* box = sg.next();
+          stage_row<OT>(box, lane, v);
+          sg.store(out[m], box, blk * k + 16 * c, row0);
+        }
+        tc::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(&acc_empty[slot]);
+      }
+    }
+    sg.drain();
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc::tc_fence_after();
+    tc::tmem_dealloc(tmem, 512);
+  }
+}
+
+// ================================================================ dx of the projections
+// CTA (blk, r) keeps Wa[blk], Wx[blk] in shared memory (the K-major B operand of dx = dl W^T)
+// and takes the row tiles r, r + P, ...  Per tile the 2 x nplanes gradient operand tiles pass
+// through a ring of `stages` buffers, each one K-loop into the tile's accumulator (one of two
+// TMEM buffers); the epilogue adds the addend tile and stores dx.
+template <typename OT>
+__global__ void __launch_bounds__(NTHREADS, 1)
+    k_proj_dx(const __grid_constant__ CUtensorMap tm_dla, const __grid_constant__ CUtensorMap tm_dlx,
+              const __grid_constant__ CUtensorMap tm_wa,
+              const __grid_constant__ CUtensorMap tm_wx, const __grid_constant__ CUtensorMap tm_dx,
+              const __grid_constant__ ProjParams p, int stages) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024u - (tc::smem_u32(smem_raw) & 1023u)) & 1023u);
+  const int k = p.k;
+  const uint32_t TB = tile_bytes(k);
+  const uint32_t WB = (uint32_t)k * k * 2;
+  const uint32_t KC = kcols(k);
+  const int NOP = 2 * p.nplanes;  // operand tiles per row tile
+  uint8_t* s_w[2] = {smem, smem + WB};
+  uint8_t* s_in = smem + 2 * WB;
+  uint8_t* s_stage = s_in + stages * TB;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(s_stage + 4 * NBOX * Stager<OT>::BOX);
+  uint64_t* w_full = bars;
+  uint64_t* in_full = bars + 1;
+  uint64_t* in_empty = in_full + stages;
+  uint64_t* acc_full = in_empty + stages;  // [2]
+  uint64_t* acc_empty = acc_full + 2;      // [2]
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(acc_empty + 2);
+  uint32_t* abort_flag = tmem_holder + 1;
+  const Abort ctl{abort_flag};
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int blk = blockIdx.x / p.P, rr = blockIdx.x % p.P;
+  const int ntiles = (p.R + TR - 1) / TR;
+  int my_tiles = 0;
+  for (int n = rr; n < ntiles; n += p.P) ++my_tiles;
+
+  if (threadIdx.x == 0) {
+    tc::mbar_init(w_full, 1);
+    for (int s = 0; s < stages; ++s) {
+      tc::mbar_init(&in_full[s], 1);
+      tc::mbar_init(&in_empty[s], 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      tc::mbar_init(&acc_full[s], 1);
+      tc::mbar_init(&acc_empty[s], 4);
+    }
+    *abort_flag = 0u;
+    tc::fence_barrier_init();
+  }
+  if (warp == 0) {
+    tc::tmem_alloc(tmem_holder, 512);
+    tc::tmem_relinquish();
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      tc::prefetch_tmap(&tm_dla);
+      tc::prefetch_tmap(&tm_dlx);
+      tc::mbar_expect_tx(w_full, 2 * WB);
+      for (int s = 0; s < k / 16; ++s) {
+        tc::tma_load_2d(s_w[0] + s * (k * 32), &tm_wa, w_full, 16 * s, blk * k);
+        tc::tma_load_2d(s_w[1] + s * (k * 32), &tm_wx, w_full, 16 * s, blk * k);
+      }
+      // operand o of a row tile: matrix o / nplanes, plane o % nplanes; each matrix's gradient
+      // tensor map is [nplanes][R][W], the plane its outermost coordinate
+      int u = 0;
+      bool ok = true;
+      for (int it = 0; it < my_tiles && ok; ++it) {
+        const int row0 = (rr + it * p.P) * TR;
+        for (int o = 0; o < NOP; ++o, ++u) {
+          const int st = u % stages;
+          if (!(ok = ctl.wait(&in_empty[st], ((u / stages) & 1) ^ 1u))) break;
+          uint8_t* buf = s_in + st * TB;
+          const int m = o / p.nplanes, pl = o % p.nplanes;
+          tc::mbar_expect_tx(&in_full[st], TB);
+          for (int s = 0; s < k / 16; ++s)
+            tc::tma_load_3d(buf + s * SLAB, m ? &tm_dlx : &tm_dla, &in_full[st],
+                            blk * k + 16 * s, row0, pl);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    const bool leader = tc::elect_one();
+    const uint32_t idesc = tc::idesc_bf16(TR, k, 0, 0);  // A = dl K-major, B = W K-major
+    ctl.wait(w_full, 0);
+    int u = 0;
+    for (int it = 0; it < my_tiles; ++it) {
+      const int slot = it & 1;
+      if (!ctl.wait(&acc_empty[slot], ((it >> 1) & 1) ^ 1u)) break;
+      tc::tc_fence_after();
+      bool ok = true;
+      for (int o = 0; o < NOP; ++o, ++u) {
+        const int st = u % stages;
+        if (!ctl.wait(&in_full[st], (u / stages) & 1)) {
+          ok = false;
+          break;
+        }
+        tc::tc_fence_after();
+        const uint32_t a0 = tc::smem_u32(s_in + st * TB);
+        const uint32_t w0 = tc::smem_u32(s_w[o / p.nplanes]);
+        if (leader) {
+          for (int kk = 0; kk < k / 16; ++kk)
+            tc::mma_bf16(tmem + slot * KC, tc::smem_desc_sw32(a0 + kk * SLAB, 16, 256),
+                         tc::smem_desc_sw32(w0 + kk * (k * 32), 16, 256), idesc,
+                         (o > 0 || kk > 0) ? 1u : 0u);
+          tc::mma_commit(&in_empty[st]);
+        }
+        __syncwarp();
+      }
+      if (!ok) break;
+      if (leader) tc::mma_commit(&acc_full[slot]);
+      __syncwarp();
+    }
+  } else {
+    const int q = warp & 3;
+    Stager<OT> sg{s_stage + (warp - 2) * NBOX * Stager<OT>::BOX, 0u};
+    for (int it = 0; it < my_tiles; ++it) {
+      const int slot = it & 1;
+      const int rw = (rr + it * p.P) * TR + 32 * q;  // the warp's first row
+      const int row = rw + lane;
+      if (!ctl.wait(&acc_full[slot], (it >> 1) & 1)) break;
+      tc::tc_fence_after();
+      const uint32_t ta = tmem + ((uint32_t)(32 * q) << 16) + slot * KC;
+      const bool in = row < p.R;
+      const size_t at = (size_t)row * p.W + (size_t)blk * k;
+      for (int c = 0; c < k / 16; ++c) {
+        float v[16];
+        tc::tmem_ld16(ta + 16 * c, v);
+        // the addend's 16 values of this row while the accumulator load is in flight
+        float a[16];
+        if (p.add_f32) {
+          const float4* src = reinterpret_cast<const float4*>(
+              static_cast<const float*>(p.add) + at + 16 * c);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float4 t = in ? src[e] : make_float4(0.f, 0.f, 0.f, 0.f);
+            a[4 * e] = t.x, a[4 * e + 1] = t.y, a[4 * e + 2] = t.z, a[4 * e + 3] = t.w;
+          }
+        } else {
+          const uint4* src = reinterpret_cast<const uint4*>(
+              static_cast<const bf16*>(p.add) + at + 16 * c);
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const uint4 t = in ? src[e] : make_uint4(0u, 0u, 0u, 0u);
+            const uint32_t w4[4] = {t.x, t.y, t.z, t.w};
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+              a[8 * e + 2 * h] = __uint_as_float(w4[h] << 16);
+              a[8 * e + 2 * h + 1] = __uint_as_float(w4[h] & 0xffff0000u);
+            }
+          }
+        }
+        tc::tmem_ld_wait();
+        tc::reg_fence(v);
+#pragma unroll
+        for (int e = 0; e < 16; ++e) v[e] += a[e];
+        uint8_t* box = sg.next();
+        stage_row<OT>(box, lane, v);
+        sg.store(&tm_dx, box, blk * k + 16 * c, rw);
+      }
+      tc::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(&acc_empty[slot]);
+    }
+    sg.drain();
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc::tc_fence_after();
+    tc::tmem_dealloc(tmem, 512);
+  }
+}
+
+// ================================================================ dW, db of the projections
+// CTA (blk, g, r): matrix group g (both matrices when nmat = 2, else matrix g) over the row
+// tiles r, r + P, ...  Per tile the x tile and the group's gradient operand tiles pass through
+// a ring of buffers; dW += x^T dl (M = input channel i in steps of 128, N = j) and db += 1^T dl
+// (an all-ones A operand: every lane of that accumulator holds the column sums) accumulate in
+// TMEM over the CTA's tiles; at the end the epilogue warps write the CTA's partial sums, which
+// k_proj_dw_reduce adds over the CTAs in a fixed order.
+__global__ void __launch_bounds__(NTHREADS, 1)
+    k_proj_dw(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_dla,
+              const __grid_constant__ CUtensorMap tm_dlx,
+              const __grid_constant__ ProjParams p, int stages) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024u - (tc::smem_u32(smem_raw) & 1023u)) & 1023u);
+  const int k = p.k;
+  const uint32_t TB = tile_bytes(k);
+  const int MB = (k + 127) / 128;          // 128-channel row blocks of dW
+  const uint32_t KC = kcols(k);
+  const int NDL = p.nmat * p.nplanes;      // gradient operand tiles per row tile
+  uint8_t* s_ones = smem;                  // 128 x 16 bf16 ones, one K-major slab
+  // `stages` operand buffers of TB bytes, then a pad: the x operand of the last 128-channel
+  // row block reads MB * 8 slabs from its buffer's start, past the k / 16 loaded ones (those
+  // lanes of the accumulator are never read), so every such read stays in shared memory
+  uint8_t* s_in = smem + SLAB;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(s_in + stages * TB + dw_pad(k));
+  uint64_t* in_full = bars;
+  uint64_t* in_empty = in_full + stages;
+  uint64_t* done = in_empty + stages;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(done + 1);
+  uint32_t* abort_flag = tmem_holder + 1;
+  const Abort ctl{abort_flag};
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int groups = 2 / p.nmat;
+  const int blk = blockIdx.x / (groups * p.P);
+  const int g = (blockIdx.x / p.P) % groups;
+  const int rr = blockIdx.x % p.P;
+  const int ntiles = (p.R + TR - 1) / TR;
+  int my_tiles = 0;
+  for (int n = rr; n < ntiles; n += p.P) ++my_tiles;
+  // TMEM per matrix of the group: MB dW accumulators (lanes = i - 128 mb) and one db
+  const uint32_t MCOLS = (uint32_t)(MB + 1) * KC;
+
+  for (int e = threadIdx.x; e < (int)(SLAB / 4); e += NTHREADS)
+    reinterpret_cast<uint32_t*>(s_ones)[e] = 0x3F803F80u;  // bf16 1.0 pairs
+  tc::fence_proxy_async_smem();
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < stages; ++s) {
+      tc::mbar_init(&in_full[s], 1);
+      tc::mbar_init(&in_empty[s], 1);
+    }
+    tc::mbar_init(done, 1);
+    *abort_flag = 0u;
+    tc::fence_barrier_init();
+  }
+  if (warp == 0) {
+    tc::tmem_alloc(tmem_holder, 512);
+    tc::tmem_relinquish();
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      tc::prefetch_tmap(&tm_x);
+      tc::prefetch_tmap(&tm_dla);
+      tc::prefetch_tmap(&tm_dlx);
+      int u = 0;
+      bool ok = true;
+      for (int it = 0; it < my_tiles && ok; ++it) {
+        const int row0 = (rr + it * p.P) * TR;
+        for (int o = 0; o <= NDL; ++o, ++u) {  // operand 0: x; then the gradient planes
+          const int st = u % stages;
+          if (!(ok = ctl.wait(&in_empty[st], ((u / stages) & 1) ^ 1u))) break;
+          uint8_t* buf = s_in + st * TB;
+          tc::mbar_expect_tx(&in_full[st], TB);
+          if (o == 0) {
+            for (int s = 0; s < k / 16; ++s)
+              tc::tma_load_2d(buf + s * SLAB, &tm_x, &in_full[st], blk * k + 16 * s, row0);
+          } else {
+            const int m = p.nmat == 2 ? (o - 1) / p.nplanes : g;
+            const int pl = (o - 1) % p.nplanes;
+            for (int s = 0; s < k / 16; ++s)
+              tc::tma_load_3d(buf + s * SLAB, m ? &tm_dlx : &tm_dla, &in_full[st],
+                              blk * k + 16 * s, row0, pl);
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    const bool leader = tc::elect_one();
+    const uint32_t id_dw = tc::idesc_bf16(TR, k, 1, 1);  // A = x MN-major, B = dl MN-major
+    const uint32_t id_db = tc::idesc_bf16(TR, k, 0, 1);  // A = ones K-major
+    const uint32_t ones = tc::smem_u32(s_ones);
+    int u = 0;
+    bool ok = true;
+    for (int it = 0; it < my_tiles && ok; ++it) {
+      const int sx = u % stages;
+      if (!ctl.wait(&in_full[sx], (u / stages) & 1)) break;
+      ++u;
+      const uint32_t xs = tc::smem_u32(s_in + sx * TB);
+      for (int o = 0; o < NDL; ++o, ++u) {
+        const int st = u % stages;
+        if (!ctl.wait(&in_full[st], (u / stages) & 1)) {
+          ok = false;
+          break;
+        }
+        tc::tc_fence_after();
+        const int mi = p.nmat == 2 ? o / p.nplanes : 0;  // matrix within the group
+        const uint32_t dl = tc::smem_u32(s_in + st * TB);
+        const uint32_t acc = tmem + mi * MCOLS;
+        if (leader) {
+          for (int kk = 0; kk < TR / 16; ++kk) {
+            const uint32_t first = (it == 0 && o % p.nplanes == 0 && kk == 0) ? 0u : 1u;
+            const uint64_t bdesc = tc::smem_desc_sw32(dl + kk * 512, SLAB, 256);
+            for (int mb = 0; mb < MB; ++mb)
+              tc::mma_bf16(acc + mb * KC,
+                           tc::smem_desc_sw32(xs + mb * 8 * SLAB + kk * 512, SLAB, 256), bdesc,
+                           id_dw, first);
+            tc::mma_bf16(acc + MB * KC, tc::smem_desc_sw32(ones, 16, 256), bdesc, id_db, first);
+          }
+          tc::mma_commit(&in_empty[st]);
+        }
+        __syncwarp();
+      }
+      if (leader) tc::mma_commit(&in_empty[sx]);
+      __syncwarp();
+    }
+    if (leader) tc::mma_commit(done);
+    __syncwarp();
+  } else {
+    // partial sums of this CTA: dW rows i = 32 q + lane (+ 128 mb), then db from lane 0
+    const int q = warp & 3;
+    const bool ok = my_tiles == 0 || ctl.wait(done, 0);
+    tc::tc_fence_after();
+    for (int mi = 0; mi < p.nmat; ++mi) {
+      const int m = p.nmat == 2 ? mi : g;
+      float* dst = p.part + (((size_t)blk * p.P + rr) * 2 + m) * ((size_t)k * k + k);
+      for (int mb = 0; mb < MB; ++mb) {
+        const int i = 128 * mb + 32 * q + lane;
+        const uint32_t ta = tmem + ((uint32_t)(32 * q) << 16) + mi * MCOLS + mb * KC;
+        for (int c = 0; c < k / 16; ++c) {
+          float v[16];
+          if (my_tiles > 0 && ok) {
+            tc::tmem_ld16(ta + 16 * c, v);
+            tc::tmem_ld_wait();
+            tc::reg_fence(v);
+          } else {
+#pragma unroll
+            for (int e = 0; e < 16; ++e) v[e] = 0.0f;
+          }
+          if (i < k) {
+            float4* o4 = reinterpret_cast<float4*>(dst + (size_t)i * k + 16 * c);
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              o4[e] = make_float4(v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
+          }
+        }
+      }
+      if (q == 0) {  // the db accumulator: every lane holds the sums; lane l writes j = l mod 32
+        const uint32_t ta = tmem + mi * MCOLS + MB * KC;
+        for (int c = 0; c < k / 16; ++c) {
+          float v[16];
+          if (my_tiles > 0 && ok) {
+            tc::tmem_ld16(ta + 16 * c, v);
+            tc::tmem_ld_wait();
+            tc::reg_fence(v);
+          } else {
+#pragma unroll
+            for (int e = 0; e < 16; ++e) v[e] = 0.0f;
+          }
+#pragma unroll
+          for (int e = 0; e < 16; ++e)
+            if (((16 * c + e) & 31) == lane) dst[(size_t)k * k + 16 * c + e] = v[e];
+        }
+      }
+    }
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc::tc_fence_after();
+    tc::tmem_dealloc(tmem, 512);
+  }
+}
+
+// dW and db: the P partial sums of every (block, matrix) added in CTA order (deterministic).
+__global__ void k_proj_dw_reduce(const float* __restrict__ part, int nblk, int P, int k,
+                                 float* dWa, float* dWx, float* dba, float* dbx) {
+  const size_t per = (size_t)k * k + k;
+  const size_t total = (size_t)nblk * 2 * per;
+  for (size_t e = (size_t)blockIdx.x * blockDim.x + threadIdx.x; e < total;
+       e += (size_t)gridDim.x * blockDim.x) {
+    const size_t blk = e / (2 * per), rem = e % (2 * per);
+    const int m = (int)(rem / per);
+    const size_t off = rem % per;
+    const float* src = part + (blk * P * 2 + m) * per + off;
+    float s = 0.0f;
+    for (int r = 0; r < P; ++r) s += src[(size_t)r * 2 * per];
+    if (off < (size_t)k * k) {
+      (m ? dWx : dWa)[blk * k * k + off] = s;
+    } else {
+      float* db = m ? dbx : dba;
+      if (db) db[blk * k + (off - (size_t)k * k)] = s;
+    }
+  }
+}
+
+// ---------------------------------------------------------------- host side
+int ctas_per_group(int groups) {
+  const int sms = sm_count();
+  const int p = groups > 0 ? sms / groups : 0;
+  return p < 1 ? 1 : p;
+}
+
+cudaError_t weight_maps(const Dims& d, const void* Wa, const void* Wx, CUtensorMap* ma,
+                        CUtensorMap* mx) {
+  // W [nblk][k][k] viewed as [nblk * k rows (i)][k columns (j)]; box 16 columns x k rows
+  const uint64_t dims[2] = {(uint64_t)d.k, (uint64_t)d.nblk * d.k};
+  const uint64_t str[1] = {(uint64_t)d.k * 2};
+  const uint32_t box[2] = {16, (uint32_t)d.k};
+  cudaError_t e = encode_tmap(ma, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, Wa, dims, str, box,
+                              CU_TENSOR_MAP_SWIZZLE_32B);
+  if (e != cudaSuccess) return e;
+  return encode_tmap(mx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, Wx, dims, str, box,
+                     CU_TENSOR_MAP_SWIZZLE_32B);
+}
+
+// An activation [R][W] bf16 as operand tiles: boxes of 16 channels x 128 rows.
+cudaError_t act_map(const Dims& d, const void* base, CUtensorMap* m) {
+  const uint64_t R = (uint64_t)d.B * d.T;
+  const uint64_t dims[2] = {(uint64_t)d.W, R};
+  const uint64_t str[1] = {(uint64_t)d.W * 2};
+  const uint32_t box[2] = {16, TR};
+  return encode_tmap(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, str, box,
+                     CU_TENSOR_MAP_SWIZZLE_32B);
+}
+
+// The gradient operand of one matrix: nplanes planes [R][W] bf16, `plane_elems` apart.
+cudaError_t planes_map(const Dims& d, const void* base, size_t plane_elems, int nplanes,
+                       CUtensorMap* m) {
+  const uint64_t R = (uint64_t)d.B * d.T;
+  const uint64_t dims[3] = {(uint64_t)d.W, R, (uint64_t)nplanes};
+  const uint64_t str[2] = {(uint64_t)d.W * 2, (uint64_t)plane_elems * 2};
+  const uint32_t box[3] = {16, TR, 1};
+  return encode_tmap(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, str, box,
+                     CU_TENSOR_MAP_SWIZZLE_32B);
+}
+
+// An output [R][W] of 16-column x 32-row boxes (bf16: 32-byte rows; float32: 64-byte rows).
+cudaError_t out_map(const Dims& d, void* base, int dt, CUtensorMap* m) {
+  const uint64_t R = (uint64_t)d.B * d.T;
+  const uint64_t es = dt == DT_F32 ? 4 : 2;
+  const uint64_t dims[2] = {(uint64_t)d.W, R};
+  const uint64_t str[1] = {(uint64_t)d.W * es};
+  const uint32_t box[2] = {16, 32};
+  return encode_tmap(m, dt == DT_F32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                     2, base, dims, str, box,
+                     dt == DT_F32 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B);
+}
+
+size_t bars_bytes(int n) { return 256 + (size_t)n * 8; }
+
+}  // namespace
+
+bool proj_tc_supported(const Dims& d) {
+  return d.io == RGLRU_BF16 && d.k % 16 == 0 && d.k >= 16 && d.k <= PROJ_TC_KMAX &&
+         sm_count() > 0;
+}
+
+size_t proj_dw_part_bytes(const Dims& d) {
+  const int nmat = 2 * ((d.k + 127) / 128 + 1) * (int)kcols(d.k) <= 512 ? 2 : 1;
+  const int P = ctas_per_group(d.nblk * (2 / nmat));
+  return (size_t)d.nblk * P * 2 * ((size_t)d.k * d.k + d.k) * 4;
+}
+
+cudaError_t launch_proj_fwd(const Dims& d, int ot, const void* x, const void* Wa,
+                            const float* ba, const void* Wx, const float* bx, void* lr, void* li,
+                            cudaStream_t s) {
+  if (!proj_tc_supported(d)) return cudaErrorNotSupported;
+  CUtensorMap mx, mwa, mwx, mlr, mli;
+  cudaError_t e = act_map(d, x, &mx);
+  if (e == cudaSuccess) e = weight_maps(d, Wa, Wx, &mwa, &mwx);
+  if (e == cudaSuccess) e = out_map(d, lr, ot, &mlr);
+  if (e == cudaSuccess) e = out_map(d, li, ot, &mli);
+  if (e != cudaSuccess) return e;
+  ProjParams p = {};
+  p.R = d.B * d.T;
+  p.k = d.k;
+  p.nblk = d.nblk;
+  p.W = d.W;
+  p.P = ctas_per_group(d.nblk);
+  p.bias[0] = ba;
+  p.bias[1] = bx;
+  const size_t box = 32 * 16 * (ot == DT_F32 ? 4 : 2);
+  const int NS = 512 / (int)kcols(d.k);
+  const size_t fixed = 1024 + 2 * (size_t)d.k * d.k * 2 + 4 * NBOX * box + 2 * d.k * 4 +
+                       bars_bytes(1 + 2 * NS);
+  int stages = 4;
+  while (stages > 1 && fixed + stages * (size_t)tile_bytes(d.k) + 16 * stages > SMEM_MAX) --stages;
+  const size_t smem = fixed + stages * (size_t)tile_bytes(d.k) + 16 * stages;
+  if (smem > SMEM_MAX) return cudaErrorNotSupported;
+  auto kern = ot == DT_F32 ? k_proj_fwd<float> : k_proj_fwd<bf16>;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  kern<<<p.P * d.nblk, NTHREADS, smem, s>>>(mx, mwa, mwx, mlr, mli, p, stages);
+  note_launches(1);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_proj_dx(const Dims& d, int ot, const void* dlr, const void* dli,
+                           size_t plane_elems, int nplanes, const void* Wa, const void* Wx,
+                           const void* add, int add_f32, void* dx, cudaStream_t s) {
+  if (!proj_tc_supported(d)) return cudaErrorNotSupported;
+  CUtensorMap mdla, mdlx, mwa, mwx, mdx;
+  cudaError_t e = planes_map(d, dlr, plane_elems, nplanes, &mdla);
+  if (e == cudaSuccess) e = planes_map(d, dli, plane_elems, nplanes, &mdlx);
+  if (e == cudaSuccess) e = weight_maps(d, Wa, Wx, &mwa, &mwx);
+  if (e == cudaSuccess) e = out_map(d, dx, ot, &mdx);
+  if (e != cudaSuccess) return e;
+  ProjParams p = {};
+  p.R = d.B * d.T;
+  p.k = d.k;
+  p.nblk = d.nblk;
+  p.W = d.W;
+  p.P = ctas_per_group(d.nblk);
+  p.add = add;
+  p.add_f32 = add_f32;
+  p.nplanes = nplanes;
+  const size_t box = 32 * 16 * (ot == DT_F32 ? 4 : 2);
+  const size_t fixed = 1024 + 2 * (size_t)d.k * d.k * 2 + 4 * NBOX * box + bars_bytes(5);
+  int stages = 4;
+  while (stages > 2 && fixed + stages * (size_t)tile_bytes(d.k) + 16 * stages > SMEM_MAX) --stages;
+  const size_t smem = fixed + stages * (size_t)tile_bytes(d.k) + 16 * stages;
+  if (smem > SMEM_MAX) return cudaErrorNotSupported;
+  auto kern = ot == DT_F32 ? k_proj_dx<float> : k_proj_dx<bf16>;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  kern<<<p.P * d.nblk, NTHREADS, smem, s>>>(mdla, mdlx, mwa, mwx, mdx, p, stages);
+  note_launches(1);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_proj_dw(const Dims& d, const void* x, const void* dlr, const void* dli,
+                           size_t plane_elems, int nplanes, float* part, float* dWa, float* dba,
+                           float* dWx, float* dbx, cudaStream_t s) {
+  if (!proj_tc_supported(d)) return cudaErrorNotSupported;
+  CUtensorMap mx, mdla, mdlx;
+  cudaError_t e = act_map(d, x, &mx);
+  if (e == cudaSuccess) e = planes_map(d, dlr, plane_elems, nplanes, &mdla);
+  if (e == cudaSuccess) e = planes_map(d, dli, plane_elems, nplanes, &mdlx);
+  if (e != cudaSuccess) return e;
+  ProjParams p = {};
+  p.R = d.B * d.T;
+  p.k = d.k;
+  p.nblk = d.nblk;
+  p.W = d.W;
+  p.nplanes = nplanes;
+  const int MB = (d.k + 127) / 128;
+  p.nmat = 2 * (MB + 1) * (int)kcols(d.k) <= 512 ? 2 : 1;
+  const int groups = 2 / p.nmat;
+  p.P = ctas_per_group(d.nblk * groups);
+  p.part = part;
+  const size_t TB = tile_bytes(d.k);
+  const size_t fixed = 1024 + SLAB + dw_pad(d.k) + bars_bytes(1);
+  // all operands of one row tile (x and the group's gradient planes) are held at once
+  const int need = p.nmat * nplanes + 1;
+  int stages = 8;
+  while (stages > need && fixed + stages * TB + 16 * stages > SMEM_MAX) --stages;
+  const size_t smem = fixed + stages * TB + 16 * stages;
+  if (smem > SMEM_MAX) return cudaErrorNotSupported;
+  e = cudaFuncSetAttribute(k_proj_dw, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  k_proj_dw<<<p.P * d.nblk * groups, NTHREADS, smem, s>>>(mx, mdla, mdlx, p, stages);
+  note_launches(1);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const size_t total = (size_t)d.nblk * 2 * ((size_t)d.k * d.k + d.k);
+  const int rgrid = (int)std::min<size_t>((total + 255) / 256, 4096);
+  k_proj_dw_reduce<<<rgrid, 256, 0, s>>>(part, d.nblk, p.P, d.k, dWa, dWx, dba, dbx);
+  note_launches(1);
+  return cudaGetLastError();
+}
+
+}  // namespace rglru

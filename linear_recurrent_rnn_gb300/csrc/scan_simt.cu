@@ -461,8 +461,9 @@ __global__ void __launch_bounds__(128, 4) k_scan_bwd(ScanBwdArgs a) {
 #pragma unroll
   for (int j = 0; j < 2; ++j) ch[j] = half == 1 ? cin[j] : fmaf(A1[j], cin[j], B1[j]);
   DXT* dx = static_cast<DXT*>(a.dx);
-  DLT* dlr = static_cast<DLT*>(a.dlr);
-  DLT* dli = static_cast<DLT*>(a.dli);
+  using DLE = typename OutPair<DLT>::E;
+  DLE* dlr = static_cast<DLE*>(a.dlr);
+  DLE* dli = static_cast<DLE*>(a.dli);
   float dsp[2] = {0.0f, 0.0f};
 #pragma unroll
   for (int s = 0; s < SUB; ++s) {
@@ -476,8 +477,8 @@ __global__ void __launch_bounds__(128, 4) k_scan_bwd(ScanBwdArgs a) {
     if (wok && t < a.T) {
       const size_t idx = ((size_t)tl.b * a.T + t) * a.W + w;
       Pair<DXT>::store(dx + idx, g[0] * cx[0][s], g[1] * cx[1][s]);
-      Pair<DLT>::store(dlr + idx, g[0] * cr[0][s], g[1] * cr[1][s]);
-      Pair<DLT>::store(dli + idx, g[0] * ci[0][s], g[1] * ci[1][s]);
+      OutPair<DLT>::store(dlr + idx, a.dl_plane, g[0] * cr[0][s], g[1] * cr[1][s]);
+      OutPair<DLT>::store(dli + idx, a.dl_plane, g[0] * ci[0][s], g[1] * ci[1][s]);
     }
   }
 #pragma unroll
@@ -558,6 +559,8 @@ cudaError_t launch_scan_bwd(const ScanBwdArgs& a, int xt, int lt, int dxt, int d
     return bwd_dispatch_mode<bf16, float, bf16, float>(a, canonical, s);
   if (xt == DT_BF16 && lt == DT_F32 && dxt == DT_F32 && dlt == DT_F32)
     return bwd_dispatch_mode<bf16, float, float, float>(a, canonical, s);
+  if (xt == DT_BF16 && lt == DT_F32 && dxt == DT_F32 && dlt == DT_SPLIT)
+    return bwd_dispatch_mode<bf16, float, float, SplitBf16>(a, canonical, s);
   return cudaErrorInvalidValue;
 }
 

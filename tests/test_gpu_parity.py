@@ -100,6 +100,13 @@ GEMM_CASES = [
     (W_("bf16-k160", 1, 150, 320, 160, "bf16", "restricted"), 23, "f32"),
     (W_("bf16-k64", 1, 33, 192, 64, "bf16", "restricted"), 24, None),
     (W_("bf16-k16-T1", 1, 1, 32, 16, "bf16", "restricted"), 25, None),
+    # tensor-core projections: k = 160 (dW of one matrix per CTA, two 128-channel row blocks),
+    # k = 48 (accumulators padded to 64 columns), and more row tiles than CTAs per gate block
+    # so that the operand rings and TMEM buffers turn over
+    (W_("bf16-k160-g16", 1, 150, 320, 160, "bf16", "restricted"), 26, None),
+    (W_("bf16-k48", 1, 300, 192, 48, "bf16", "restricted"), 27, None),
+    (W_("bf16-k128-multi", 1, 1500, 2048, 128, "bf16", "restricted"), 28, None),
+    (W_("bf16-k160-multi", 2, 4000, 480, 160, "bf16", "restricted"), 29, None),
 ]
 
 
@@ -153,6 +160,11 @@ FUSED_CASES = [
     (W_("bf16-far-k128", 2, 150, 256, 128, "bf16", "canonical", (0.05, 0.95), reset_p=0.05,
         h0_std=1.0), 36, "f32"),
     (W_("bf16-far-res-k128", 2, 130, 256, 128, "bf16", "restricted", (0.2, 0.9)), 37, None),
+    # gate blocks the fused kernels do not take: tensor-core projections around the CUDA-core
+    # scan, bf16-stored gradients
+    (W_("bf16-res-k160", 2, 300, 480, 160, "bf16", "restricted"), 38, None),
+    (W_("bf16-can-k96", 2, 200, 192, 96, "bf16", "canonical", reset_p=0.02, h0_std=1.0), 39,
+     None),
 ]
 
 
@@ -241,6 +253,17 @@ def test_fused_forward_backward(wl, seed, grad):
     got = {k: host(v) for k, v in run_fused_gpu(wl, inp, sh, ba, bx).items()}
     check_fused(wl, inp, got, "f32" if sh.grad == R.F32 else "bf16",
                 ba.double().numpy(), bx.double().numpy())
+
+
+def test_fused_path_names_the_kernels():
+    """The fused calls run the one-kernel tensor-core pair for bf16 gate blocks of 128, the
+    tensor-core projections around the CUDA-core scan for other bf16 gate blocks (multiples of
+    16 up to 160), and the float32 SIMT projections for float32 I/O."""
+    assert R.fused_path(R.make_shape(4, 2048, 2048, 16, R.BF16)).startswith("fused")
+    p5 = R.fused_path(R.make_shape(8, 4096, 4000, 25, R.BF16))
+    assert p5.startswith("composed") and "tcgen05" in p5
+    assert "SIMT" in R.fused_path(R.make_shape(1, 64, 128, 2, R.F32))
+    assert "SIMT" in R.fused_path(R.make_shape(1, 64, 8 * 24, 8, R.BF16))  # k = 24
 
 
 def test_fused_forward_is_one_tensor_core_kernel():
