@@ -666,6 +666,28 @@ int ctas_per_group(int groups) {
   return p < 1 ? 1 : p;
 }
 
+// Row tiles one dW accumulator takes at most.  The tensor core adds each K = 16 step into the
+// float32 accumulator with a rounding that does not average out the way round-to-nearest sums
+// do, so its error grows with the number of steps: measured at B8 T4096 with gate blocks of
+// 160, 85 tiles (683 steps) per accumulator put two diagonal dW elements at E = 3.5e-3.  The
+// row tiles are therefore split over enough CTAs that none accumulates more than this many;
+// the per-CTA partials are then added on the CUDA cores in float32.
+constexpr int DW_TILES_MAX = 16;
+
+int dw_ctas_per_group(const Dims& d, int groups) {
+  const int ntiles = (d.B * d.T + TR - 1) / TR;
+  int P = ctas_per_group(groups);
+  const int pmin = (ntiles + DW_TILES_MAX - 1) / DW_TILES_MAX;
+  if (P < pmin) {  // whole waves of CTAs over the SMs
+    const int sms = sm_count() > 0 ? sm_count() : 1;
+    const long waves = ((long)groups * pmin + sms - 1) / sms;
+    P = (int)std::max<long>(pmin, waves * sms / groups);
+  }
+  return std::max(1, std::min(P, ntiles));
+}
+
+int dw_nmat(const Dims& d) { return 2 * ((d.k + 127) / 128 + 1) * (int)kcols(d.k) <= 512 ? 2 : 1; }
+
 cudaError_t weight_maps(const Dims& d, const void* Wa, const void* Wx, CUtensorMap* ma,
                         CUtensorMap* mx) {
   // W [nblk][k][k] viewed as [nblk * k rows (i)][k columns (j)]; box 16 columns x k rows
@@ -722,8 +744,7 @@ bool proj_tc_supported(const Dims& d) {
 }
 
 size_t proj_dw_part_bytes(const Dims& d) {
-  const int nmat = 2 * ((d.k + 127) / 128 + 1) * (int)kcols(d.k) <= 512 ? 2 : 1;
-  const int P = ctas_per_group(d.nblk * (2 / nmat));
+  const int P = dw_ctas_per_group(d, d.nblk * (2 / dw_nmat(d)));
   return (size_t)d.nblk * P * 2 * ((size_t)d.k * d.k + d.k) * 4;
 }
 
@@ -809,10 +830,9 @@ cudaError_t launch_proj_dw(const Dims& d, const void* x, const void* dlr, const 
   p.nblk = d.nblk;
   p.W = d.W;
   p.nplanes = nplanes;
-  const int MB = (d.k + 127) / 128;
-  p.nmat = 2 * (MB + 1) * (int)kcols(d.k) <= 512 ? 2 : 1;
+  p.nmat = dw_nmat(d);
   const int groups = 2 / p.nmat;
-  p.P = ctas_per_group(d.nblk * groups);
+  p.P = dw_ctas_per_group(d, d.nblk * groups);
   p.part = part;
   const size_t TB = tile_bytes(d.k);
   const size_t fixed = 1024 + SLAB + dw_pad(d.k) + bars_bytes(1);
