@@ -381,8 +381,8 @@ __device__ __forceinline__ void bwd_pass2b(uint32_t tcol, int tb, int j,
       // tokens (abar = 0), past T and where the decay is exactly 1 (m = 0)
       const float2 nw = mul2(mul2(i, i), make_float2(rcp_approx(-mi.x), rcp_approx(-mi.y)));
       float2 alpha = mul2(abar, fma2(mul2(abar, xv), nw, make_float2(h4[2 * q], h4[2 * q + 1])));
-      if ((GENERAL && abar.x == 0.0f) || mi.x == 0.0f) alpha.x = 0.0f;
-      if ((GENERAL && abar.y == 0.0f) || mi.y == 0.0f) alpha.y = 0.0f;
+      if (GENERAL && (abar.x == 0.0f || mi.x == 0.0f)) alpha.x = 0.0f;
+      if (GENERAL && (abar.y == 0.0f || mi.y == 0.0f)) alpha.y = 0.0f;
       const float2 dla = mul2(gv, alpha);
       const float2 dd = mul2(gv, mi);  // direct dx term
       o_r[q] = mul2(mul2(dla, bc2(nk)), mul2(r, fma2(r, bc2(-1.0f), bc2(1.0f))));
@@ -602,7 +602,10 @@ __global__ void __maxnreg__(MAXREG)
     const bool store_thread = (warp == 2 && lane == 0);
     if (store_thread) tc::prefetch_tmap(&tm_dx);
     float2 dsp = bc2(0.0f), dba = bc2(0.0f), dbx = bc2(0.0f);
-    const bool near_all = __all_sync(0xffffffffu, gk.nk > NEAR_LA);
+    // The fast path needs every channel of the warp in the near regime and with a nonzero
+    // multiplier constant: then m i > 0 on every token (the exponent clamps keep t > 0), so its
+    // pass 2b needs no test for m = 0.
+    const bool near_all = __all_sync(0xffffffffu, gk.nk > NEAR_LA && gk.cm > 0.0f);
     // Channel j of a token row in a stage: 16-channel slab, 2-byte column, and the 16-byte half
     // of the 32-byte row (swapped on rows 4..7 of every 8 by the swizzle).
     const int xoff0 = (j >> 4) * SLAB_X + (j & 7) * 2 + (((j & 15) >> 3) << 4);
