@@ -79,14 +79,18 @@ rglru_status cuda_status(cudaError_t e) {
   return RGLRU_ERR_CUDA;
 }
 
-// Fused layer through the separate kernels (float32 logits kept in `saved`).
+// The fused layer through separate kernels: the logits are kept in `saved` (float32, or as bf16
+// hi + lo planes on the tensor-core route: the same 4 bytes per element).
+bool composed_tc(const Dims& d) { return proj_tc_supported(d) && logits_scan_supported(d); }
+
 struct ComposedLayout {
-  size_t lr, li, total;  // within `saved`, after the scan layout
+  size_t lr, li, total;  // within `saved`, after the scan's own layout
 };
 ComposedLayout composed_saved(const Dims& d) {
   ComposedLayout C;
-  const ScanLayout L = scan_layout(d, false);
-  C.lr = align_up(L.total, 256);
+  size_t base = scan_layout(d, false).total;
+  if (composed_tc(d) && fused_fwd_layout(d).total > base) base = fused_fwd_layout(d).total;
+  C.lr = align_up(base, 256);
   C.li = align_up(C.lr + d.N * 4, 256);
   C.total = align_up(C.li + d.N * 4, 256);
   return C;
@@ -109,8 +113,9 @@ struct ComposedWs {
 };
 ComposedWs composed_ws(const Dims& d) {
   ComposedWs C;
-  const ScanLayout L = scan_layout(d, true);
-  C.dxd = align_up(L.total, 256);
+  size_t base = scan_layout(d, true).total;
+  if (composed_tc(d) && fused_bwd_layout(d).total > base) base = fused_bwd_layout(d).total;
+  C.dxd = align_up(base, 256);
   C.dlr = align_up(C.dxd + d.N * 4, 256);
   C.dli = align_up(C.dlr + d.N * 4, 256);
   C.gate = align_up(C.dli + d.N * 4, 256);
@@ -181,6 +186,8 @@ ScanBwdArgs bwd_args(const Dims& d, const void* dy, const float* dhT, const void
 
 namespace rglru {
 void note_launches(unsigned n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
+int debug_spin_limit() { return g_spin_limit; }
+int debug_drop_tile() { return g_drop_tile; }
 }  // namespace rglru
 
 extern "C" {
@@ -201,7 +208,8 @@ size_t rglru_saved_bytes(const rglru_shape* shape) {
   if (make_dims(shape, &d) != RGLRU_OK) return 0;
   // the unfused scan's layout, and the fused call's: the tensor-core kernels' own where they
   // take the shape, else the composed path's (which keeps float32 logits)
-  const size_t a = scan_layout(d, false).total;
+  size_t a = scan_layout(d, false).total;
+  if (logits_scan_supported(d) && fused_fwd_layout(d).total > a) a = fused_fwd_layout(d).total;
   const size_t f = fused_supported(d) ? fused_fwd_layout(d).total : composed_saved(d).total;
   return a > f ? a : f;
 }
@@ -210,6 +218,7 @@ size_t rglru_workspace_bytes(const rglru_shape* shape) {
   Dims d;
   if (make_dims(shape, &d) != RGLRU_OK) return 0;
   size_t m = scan_layout(d, true).total;
+  if (logits_scan_supported(d) && fused_bwd_layout(d).total > m) m = fused_bwd_layout(d).total;
   const size_t g = gate_bwd_ws_bytes(d);
   const size_t f = fused_supported(d) ? fused_bwd_layout(d).total : composed_ws(d).total;
   if (g > m) m = g;
@@ -240,6 +249,9 @@ rglru_status rglru_forward(const rglru_shape* shape, const void* x, const void* 
   if (!req(x) || !req(lr) || !req(li) || !req(Lambda) || !req(y) || !opt(hT) || !req(saved))
     return RGLRU_ERR_INVALID_ARG;
   if ((st = check_resets(d, reset_mask, segment_pos, h0)) != RGLRU_OK) return st;
+  if (logits_scan_supported(d))  // bf16: the fused scan kernel with the logits given
+    return cuda_status(launch_logits_fwd(d, x, lr, li, d.N, 1, Lambda, reset_mask, segment_pos,
+                                         h0, y, hT, saved, g_spin_limit, g_drop_tile, stream));
   const ScanFwdArgs a = fwd_args(d, x, lr, li, Lambda, reset_mask, segment_pos, h0, y, hT, saved);
   cudaError_t e = cudaMemsetAsync(saved, 0, a.L.zero_bytes, stream);
   if (e == cudaSuccess) e = launch_scan_fwd(a, d.io, d.io, d.mode == RGLRU_CANONICAL, stream);
@@ -258,6 +270,11 @@ rglru_status rglru_backward(const rglru_shape* shape, const void* dy, const floa
       !req(dx) || !req(dlr) || !req(dli) || !req(dLambda) || !opt(dh0) || !req(workspace))
     return RGLRU_ERR_INVALID_ARG;
   if ((st = check_resets(d, reset_mask, segment_pos, h0)) != RGLRU_OK) return st;
+  if (logits_scan_supported(d))
+    return cuda_status(launch_logits_bwd(d, dy, dhT, x, lr, li, d.N, 1, Lambda, reset_mask,
+                                         segment_pos, saved, d.grad, dx, d.grad, dlr, dli, 0,
+                                         dLambda, dh0, workspace, g_spin_limit, g_drop_tile,
+                                         stream));
   const ScanBwdArgs a = bwd_args(d, dy, dhT, x, lr, li, Lambda, reset_mask, segment_pos, h0, saved,
                                  dx, dlr, dli, dLambda, dh0, workspace);
   cudaError_t e = cudaMemsetAsync(workspace, 0, a.L.zero_bytes, stream);
@@ -310,11 +327,16 @@ rglru_status rglru_fused_forward(const rglru_shape* shape, const void* x, const 
                                         h0, y, hT, saved, g_spin_limit, g_drop_tile, stream));
   uint8_t* sv = static_cast<uint8_t*>(saved);
   const ComposedLayout C = composed_saved(d);
-  cudaError_t e =
-      proj_tc_supported(d)
-          ? launch_proj_fwd(d, DT_F32, x, Wa, ba, Wx, bx, sv + C.lr, sv + C.li, stream)
-          : launch_gate_proj_simt(d, d.io, DT_F32, x, Wa, ba, Wx, bx, sv + C.lr, sv + C.li,
-                                  stream);
+  if (composed_tc(d)) {
+    // tensor-core projections to bf16 hi + lo logit planes, then the fused scan kernel on them
+    cudaError_t e = launch_proj_fwd(d, DT_SPLIT, x, Wa, ba, Wx, bx, sv + C.lr, sv + C.li, stream);
+    if (e == cudaSuccess)
+      e = launch_logits_fwd(d, x, sv + C.lr, sv + C.li, d.N, 2, Lambda, reset_mask, segment_pos,
+                            h0, y, hT, saved, g_spin_limit, g_drop_tile, stream);
+    return cuda_status(e);
+  }
+  cudaError_t e = launch_gate_proj_simt(d, d.io, DT_F32, x, Wa, ba, Wx, bx, sv + C.lr, sv + C.li,
+                                        stream);
   const ScanFwdArgs a = fwd_args(d, x, sv + C.lr, sv + C.li, Lambda, reset_mask, segment_pos, h0,
                                  y, hT, saved);
   if (e == cudaSuccess) e = cudaMemsetAsync(saved, 0, a.L.zero_bytes, stream);
@@ -353,12 +375,12 @@ rglru_status rglru_fused_backward(const rglru_shape* shape, const void* dy, cons
                                  fsaved, ws + CW.dxd, ws + CW.dlr, ws + CW.dli, dLambda, dh0,
                                  workspace);
   // The direct term of dx stays float32 until the projections are added: one rounding.
-  if (e == cudaSuccess) e = cudaMemsetAsync(workspace, 0, a.L.zero_bytes, stream);
-  if (proj_tc_supported(d)) {
-    // dlr, dli as bf16 hi + lo planes (the same bytes as float32), the operands of the
-    // tensor-core products
-    if (e == cudaSuccess)
-      e = launch_scan_bwd(a, d.io, DT_F32, DT_F32, DT_SPLIT, d.mode == RGLRU_CANONICAL, stream);
+  if (composed_tc(d)) {
+    // the fused scan kernel on the saved hi + lo logit planes; dlr, dli out as bf16 hi + lo
+    // planes (the same bytes as float32), the operands of the tensor-core products
+    e = launch_logits_bwd(d, dy, dhT, x, lr, li, d.N, 2, Lambda, reset_mask, segment_pos, saved,
+                          DT_F32, ws + CW.dxd, DT_SPLIT, ws + CW.dlr, ws + CW.dli, d.N, dLambda,
+                          dh0, workspace, g_spin_limit, g_drop_tile, stream);
     if (e == cudaSuccess)
       e = launch_proj_dx(d, d.grad, ws + CW.dlr, ws + CW.dli, d.N, 2, Wa, Wx, ws + CW.dxd, 1,
                          dx, stream);
@@ -368,6 +390,7 @@ rglru_status rglru_fused_backward(const rglru_shape* shape, const void* dy, cons
                          dWx, dbx, stream);
     return cuda_status(e);
   }
+  if (e == cudaSuccess) e = cudaMemsetAsync(workspace, 0, a.L.zero_bytes, stream);
   if (e == cudaSuccess)
     e = launch_scan_bwd(a, d.io, DT_F32, DT_F32, DT_F32, d.mode == RGLRU_CANONICAL, stream);
   if (e == cudaSuccess)
@@ -482,9 +505,9 @@ const char* rglru_fused_path(const rglru_shape* shape) {
   if (fused_supported(d))
     return "fused: k_fused_fwd / k_fused_bwd (tcgen05 projections and CUDA-core scan in one "
            "kernel each)";
-  if (proj_tc_supported(d))
-    return "composed: tcgen05 projections (k_proj_fwd, k_proj_dx, k_proj_dw), CUDA-core scan "
-           "kernels (float32 logits kept)";
+  if (composed_tc(d))
+    return "composed: tcgen05 projections (k_proj_fwd, k_proj_dx, k_proj_dw) around the fused "
+           "scan kernels with the logits given (kept as bf16 hi + lo planes)";
   return "composed: float32 SIMT projections, CUDA-core scan kernels (float32 logits kept)";
 }
 

@@ -71,6 +71,16 @@ constexpr uint32_t XCH_BYTES = NPART * FUSED_K * 16 + FUSED_K * 4;  // part aggr
 // W (2) + x/dy stages (2 x 2) + dl buffers (4) + bf16 dx staging (1) tiles, exchange, barriers
 constexpr size_t SMEM_BYTES =
     2 * W_BYTES + STAGES * 2 * T_BYTES + 4 * T_BYTES + T_BYTES + XCH_BYTES + 256 + 1024;
+// Given-logits mode (the backward of rglru_backward and of the composed layer): no weights and
+// no projection products; each stage holds x, dy and up to two bf16 planes of each logit tile,
+// a 64 x 64 identity lays the logits out in TMEM, and dlr / dli go to global memory.
+constexpr int LG_PLANES = 2;
+constexpr uint32_t LG_STAGE_BYTES = (2 + 2 * LG_PLANES) * T_BYTES;
+constexpr uint32_t ID_BYTES = FUSED_C * FUSED_C * 2;
+constexpr size_t LG_SMEM_BYTES = ID_BYTES + STAGES * LG_STAGE_BYTES + T_BYTES + XCH_BYTES + 256 + 1024;
+// Given-logits output of dlr, dli: LGM_SAME in the dx dtype, LGM_SPLIT as float32 values in
+// bf16 hi + lo planes (the operands of the tensor-core projection backward).
+constexpr int LGM_NONE = 0, LGM_SAME = 1, LGM_SPLIT = 2;
 constexpr uint32_t STATUS_PIPE = 2u;
 constexpr int BAR_SCAN = 1;  // named barrier of the scan warps
 constexpr uint32_t DW_BOX_BYTES = FUSED_K * 128;  // 128 rows x 32 float32 columns
@@ -80,6 +90,10 @@ constexpr size_t BWD_COUNTERS = 256;
 
 struct BwdParams {
   int B, T, W, nblk, nC, P, canonical;
+  int nplanes;     // given logits: bf16 planes per logit
+  void* dlr;       // given logits: outputs dlr, dli ([B][T][W]; split: lo plane dl_plane later)
+  void* dli;
+  size_t dl_plane;
   const float* Lambda;
   const float* ba;
   const float* bx;
@@ -315,12 +329,43 @@ __device__ __forceinline__ void bwd_pass2a(uint32_t tcol, const uint32_t (&xr)[P
 // columns (COL_LR, COL_LI) are read for the last time by the loads of group 0; once those have
 // landed the warp arrives on lg_free, so the next tile's logits MMAs overlap the rest of the
 // pass.
-template <bool GENERAL, bool VARLEN>
+// Given-logits output of one token pair of dlr / dli: token index t0 (row b) of channel w.
+template <typename GT, int LGM>
+__device__ __forceinline__ void store_dl_pair(void* base, size_t plane, size_t idx, int W,
+                                              float2 v, bool ok0, bool ok1) {
+  if (LGM == LGM_SPLIT) {
+    bf16* p = static_cast<bf16*>(base) + idx;
+    const bf16 h0 = __float2bfloat16_rn(v.x), h1 = __float2bfloat16_rn(v.y);
+    if (ok0) {
+      p[0] = h0;
+      p[plane] = __float2bfloat16_rn(v.x - __bfloat162float(h0));
+    }
+    if (ok1) {
+      p[W] = h1;
+      p[plane + W] = __float2bfloat16_rn(v.y - __bfloat162float(h1));
+    }
+  } else {
+    GT* p = static_cast<GT*>(base) + idx;
+    if (ok0) p[0] = from_f32<GT>(v.x);
+    if (ok1) p[W] = from_f32<GT>(v.y);
+  }
+}
+struct DlOut {
+  void* dlr;
+  void* dli;
+  size_t plane;
+  size_t idx0;  // element index of (b, the part's first token, w)
+  int W;
+  int valid;    // tokens of the part before T (and a real channel: else 0)
+};
+
+template <bool GENERAL, bool VARLEN, typename GT = float, int LGM = LGM_NONE>
 __device__ __forceinline__ void bwd_pass2b(uint32_t tcol, int tb, int j,
                                            const uint32_t (&xr)[PT / 2], uint32_t dyb, float nk,
                                            int valid, const float2 (&ab)[PT / 2], const SeqB& sq,
                                            float cin, uint64_t* lg_free,
-                                           uint8_t* s_dl, float2& dsp, float2& dba, float2& dbx) {
+                                           uint8_t* s_dl, float2& dsp, float2& dba, float2& dbx,
+                                           const DlOut& dlo = DlOut{}) {
   static_assert(PT / GRP >= 2, "the logits columns are released after the second-to-last group");
   float gnext = cin, anext = 1.0f;
   constexpr int G0 = PT / GRP - 1;
@@ -394,8 +439,20 @@ __device__ __forceinline__ void bwd_pass2b(uint32_t tcol, int tb, int j,
       h4[2 * q + 1] = dd.y;
     }
     static_assert(GRP == 8, "the dl stores take 8 tokens");
-    store_dl8(s_dl, s_dl + T_BYTES, tb + g * GRP, j, o_r);
-    store_dl8(s_dl + 2 * T_BYTES, s_dl + 3 * T_BYTES, tb + g * GRP, j, o_i);
+    if (LGM == LGM_NONE) {
+      store_dl8(s_dl, s_dl + T_BYTES, tb + g * GRP, j, o_r);
+      store_dl8(s_dl + 2 * T_BYTES, s_dl + 3 * T_BYTES, tb + g * GRP, j, o_i);
+    } else {
+#pragma unroll
+      for (int q = 0; q < GRP / 2; ++q) {
+        const int u = g * GRP + 2 * q;
+        const size_t idx = dlo.idx0 + (size_t)u * dlo.W;
+        store_dl_pair<GT, LGM>(dlo.dlr, dlo.plane, idx, dlo.W, o_r[q], u < dlo.valid,
+                               u + 1 < dlo.valid);
+        store_dl_pair<GT, LGM>(dlo.dli, dlo.plane, idx, dlo.W, o_i[q], u < dlo.valid,
+                               u + 1 < dlo.valid);
+      }
+    }
     tc::tmem_st(tcol + COL_DX + g * GRP, h4);
     if (!PREF && g > 0) {
       tc::tmem_ld(tcol + COL_LR + (g - 1) * GRP, nm);
@@ -426,7 +483,7 @@ __device__ __forceinline__ void bwd_pass2b(uint32_t tcol, int tb, int j,
   tc::tmem_st_wait();
 }
 
-template <typename GT, bool VARLEN>
+template <typename GT, bool VARLEN, int LGM>
 __global__ void __maxnreg__(MAXREG)
     k_fused_bwd(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_dy,
                 const __grid_constant__ CUtensorMap tm_wa, const __grid_constant__ CUtensorMap tm_wx,
@@ -435,11 +492,13 @@ __global__ void __maxnreg__(MAXREG)
   extern __shared__ uint8_t smem_raw[];
   // 1024-byte aligned base, formed by pointer arithmetic so that it stays a shared pointer
   uint8_t* smem = smem_raw + ((1024u - (tc::smem_u32(smem_raw) & 1023u)) & 1023u);
-  uint8_t* s_wa = smem;
+  constexpr bool LG = LGM != LGM_NONE;
+  constexpr uint32_t STB = LG ? LG_STAGE_BYTES : 2 * T_BYTES;
+  uint8_t* s_wa = smem;                             // LG: the identity
   uint8_t* s_wx = smem + W_BYTES;
-  uint8_t* s_in = smem + 2 * W_BYTES;               // stage s: x at s*2T, dy at s*2T + T
-  uint8_t* s_dl = s_in + STAGES * 2 * T_BYTES;      // r_hi, r_lo, i_hi, i_lo
-  uint8_t* s_dx = s_dl + 4 * T_BYTES;               // dx staging [token][channel]
+  uint8_t* s_in = smem + (LG ? ID_BYTES : 2 * W_BYTES);  // stage s: x, dy (+ LG: logit planes)
+  uint8_t* s_dl = s_in + STAGES * STB;              // r_hi, r_lo, i_hi, i_lo (none in LG)
+  uint8_t* s_dx = s_dl + (LG ? 0 : 4 * T_BYTES);    // dx staging [token][channel]
   float4* s_agg = reinterpret_cast<float4*>(s_dx + T_BYTES);       // [part][k]
   float* s_cin = reinterpret_cast<float*>(s_agg + NPART * FUSED_K);  // [k]
   uint64_t* bars = reinterpret_cast<uint64_t*>(s_cin + FUSED_K);
@@ -474,6 +533,7 @@ __global__ void __maxnreg__(MAXREG)
     *abort_flag = 0u;
     tc::fence_barrier_init();
   }
+  if (LG) tc::write_identity_sw32(s_wa, FUSED_C);
   if (warp == 0) {
     tc::tmem_alloc(tmem_holder, TMEM_COLS);
     tc::tmem_relinquish();
@@ -490,10 +550,14 @@ __global__ void __maxnreg__(MAXREG)
     if (lane == 0) {
       tc::prefetch_tmap(&tm_x);
       tc::prefetch_tmap(&tm_dy);
-      tc::mbar_expect_tx(w_full, 2 * W_BYTES);
-      for (int g = 0; g < FUSED_K / 16; ++g) {
-        tc::tma_load_2d(s_wa + g * SLAB_W, &tm_wa, w_full, 16 * g, blk * FUSED_K);
-        tc::tma_load_2d(s_wx + g * SLAB_W, &tm_wx, w_full, 16 * g, blk * FUSED_K);
+      if (!LG) {
+        tc::mbar_expect_tx(w_full, 2 * W_BYTES);
+        for (int g = 0; g < FUSED_K / 16; ++g) {
+          tc::tma_load_2d(s_wa + g * SLAB_W, &tm_wa, w_full, 16 * g, blk * FUSED_K);
+          tc::tma_load_2d(s_wx + g * SLAB_W, &tm_wx, w_full, 16 * g, blk * FUSED_K);
+        }
+      } else {
+        tc::mbar_arrive(w_full);  // the identity is in place (written before the CTA barrier)
       }
       TileWalk tw(rr, p.P, p.B);  // tw.c counts chunks from the last one
       for (int it = 0; it < my_tiles; ++it, tw.next()) {
@@ -501,12 +565,20 @@ __global__ void __maxnreg__(MAXREG)
         const uint32_t ph = (it / STAGES) & 1;
         if (!ctl.wait(&in_empty[st], ph ^ 1u)) continue;
         const int c = p.nC - 1 - tw.c, b = tw.b;
-        uint8_t* xs = s_in + st * 2 * T_BYTES;
-        tc::mbar_expect_tx(&in_full[st], 2 * T_BYTES);
+        uint8_t* xs = s_in + st * STB;
+        tc::mbar_expect_tx(&in_full[st], LG ? (2 + 2 * p.nplanes) * T_BYTES : 2 * T_BYTES);
         for (int s = 0; s < FUSED_K / 16; ++s)
           tc::tma_load_3d(xs + s * SLAB_X, &tm_x, &in_full[st], blk * FUSED_K + 16 * s,
                           c * FUSED_C, b);
         tc::tma_load_3d(xs + T_BYTES, &tm_dy, &in_full[st], blk * FUSED_K, c * FUSED_C, b);
+        if (LG) {  // tm_wa / tm_wx map the logit planes [plane][B][T][W]
+          for (int g = 0; g < 2; ++g)
+            for (int pl = 0; pl < p.nplanes; ++pl)
+              for (int s = 0; s < FUSED_K / 16; ++s)
+                tc::tma_load_4d(xs + (2 + g * LG_PLANES + pl) * T_BYTES + s * SLAB_X,
+                                g ? &tm_wx : &tm_wa, &in_full[st], blk * FUSED_K + 16 * s,
+                                c * FUSED_C, b, pl);
+        }
       }
     }
   } else if (warp == 1) {
@@ -525,22 +597,39 @@ __global__ void __maxnreg__(MAXREG)
       if (!ctl.wait(lg_empty, (it & 1) ^ 1u)) return;
       if (!ctl.wait(&in_full[st], (it / STAGES) & 1)) return;
       tc::tc_fence_after();
-      const uint32_t xs = tc::smem_u32(s_in + st * 2 * T_BYTES);
+      const uint32_t xs = tc::smem_u32(s_in + st * STB);
       if (leader) {
+        if (!LG) {
 #pragma unroll
-        for (int kk = 0; kk < FUSED_K / 16; ++kk) {
-          const uint64_t bdesc = tc::smem_desc_sw32(xs + kk * SLAB_X, 16, 256);
-          tc::mma_bf16(tmem + COL_LR, tc::smem_desc_sw32(wa + kk * 512, SLAB_W, 256), bdesc,
-                       id_lg, kk > 0);
-          tc::mma_bf16(tmem + COL_LI, tc::smem_desc_sw32(wx + kk * 512, SLAB_W, 256), bdesc,
-                       id_lg, kk > 0);
+          for (int kk = 0; kk < FUSED_K / 16; ++kk) {
+            const uint64_t bdesc = tc::smem_desc_sw32(xs + kk * SLAB_X, 16, 256);
+            tc::mma_bf16(tmem + COL_LR, tc::smem_desc_sw32(wa + kk * 512, SLAB_W, 256), bdesc,
+                         id_lg, kk > 0);
+            tc::mma_bf16(tmem + COL_LI, tc::smem_desc_sw32(wx + kk * 512, SLAB_W, 256), bdesc,
+                         id_lg, kk > 0);
+          }
+        } else {
+          // l^T = L^T I: A = the logit plane tile MN-major, B = the identity K-major
+          for (int g = 0; g < 2; ++g)
+            for (int pl = 0; pl < p.nplanes; ++pl)
+#pragma unroll
+              for (int kk = 0; kk < FUSED_C / 16; ++kk)
+                tc::mma_bf16(tmem + (g ? COL_LI : COL_LR),
+                             tc::smem_desc_sw32(xs + (2 + g * LG_PLANES + pl) * T_BYTES + kk * 512,
+                                                SLAB_X, 256),
+                             tc::smem_desc_sw32(wa + kk * SLAB_X, 16, 256), id_lg,
+                             (pl > 0 || kk > 0) ? 1u : 0u);
         }
         tc::mma_commit(lg_full);
+        if (LG) tc::mma_commit(&in_empty[st]);  // the logit planes are read
       }
       __syncwarp();
     };
-    if (my_tiles > 0) logits(0);
-    for (int it = 0; it < my_tiles; ++it) {
+    if (LG) {
+      for (int it = 0; it < my_tiles; ++it) logits(it);
+    }
+    if (!LG && my_tiles > 0) logits(0);
+    for (int it = 0; it < my_tiles && !LG; ++it) {
       if (it + 1 < my_tiles) logits(it + 1);
       const int st = it % STAGES;
       if (!ctl.wait(dl_full, it & 1)) continue;
@@ -589,7 +678,9 @@ __global__ void __maxnreg__(MAXREG)
     const int part = (warp - 2) >> 2;
     const int q = warp & 3;
     const int j = q * 32 + lane;
-    const int w = blk * FUSED_K + j;
+    // channels past W (LG only): nothing stored, their reads take a real channel's
+    const bool wok = !LG || blk * FUSED_K + j < p.W;
+    const int w = LG ? min(blk * FUSED_K + j, p.W - 1) : blk * FUSED_K + j;
     const int tb = part * PT;
     const uint32_t tcol = tmem + ((uint32_t)(q * 32) << 16) + tb;  // this thread's lane, part
     GateK gk;
@@ -635,9 +726,9 @@ __global__ void __maxnreg__(MAXREG)
       const int c = p.nC - 1 - cur.c, b = cur.b;
       const int st = it % STAGES;
       const uint32_t ph = (it / STAGES) & 1;
-      const uint32_t xt = tc::smem_u32(s_in + st * 2 * T_BYTES + tb * 32);
+      const uint32_t xt = tc::smem_u32(s_in + st * STB + tb * 32);
       const uint32_t xb0 = xt + xoff0, xb1 = xt + xoff1;
-      const uint32_t dyb = tc::smem_u32(s_in + st * 2 * T_BYTES + T_BYTES + tb * DY_ROW + j * 2);
+      const uint32_t dyb = tc::smem_u32(s_in + st * STB + T_BYTES + tb * DY_ROW + j * 2);
       float2 ab[PT / 2];
       uint32_t xr[PT / 2];  // x of the part's tokens, bf16 pairs
       float P = 1.0f, fB = 0.0f, S = 0.0f;
@@ -718,7 +809,7 @@ __global__ void __maxnreg__(MAXREG)
         const float4 g0 = s_agg[j];
         tP = g0.z * Rp;
         tS = fmaf(g0.z, Rs, g0.w);
-        if (part == 0 && publish) slot_put2(agg + cidx * p.W + w, tP, tS);
+        if (part == 0 && publish && wok) slot_put2(agg + cidx * p.W + w, tP, tS);
       }
 
       // dx of tile it - 1: TMEM -> smem [token][channel] as bf16 (float32 goes straight to HBM),
@@ -726,7 +817,7 @@ __global__ void __maxnreg__(MAXREG)
       // trip has this to overlap; before pass 2a, which reuses the dx columns.
       if (it > 0) {
         const int validp = min(FUSED_C, p.T - cp * FUSED_C) - tb;
-        ctl.wait(dx_full, (it - 1) & 1);
+        if (!LG) ctl.wait(dx_full, (it - 1) & 1);  // LG: no products; the lane wrote it itself
         tc::tc_fence_after();
 #pragma unroll
         for (int sub = 0; sub < PT / 8; ++sub) {
@@ -739,7 +830,7 @@ __global__ void __maxnreg__(MAXREG)
             if (sizeof(GT) == 2) {
               *reinterpret_cast<bf16*>(s_dx + tl * (FUSED_K * 2) + j * 2) =
                   __float2bfloat16_rn(v[u]);
-            } else if (sub * 8 + u < validp) {
+            } else if (sub * 8 + u < validp && wok) {
               // 128 contiguous bytes per warp and token
               static_cast<float*>(p.dx)[((size_t)bp * p.T + cp * FUSED_C + tl) * p.W + w] = v[u];
             }
@@ -768,8 +859,8 @@ __global__ void __maxnreg__(MAXREG)
         const float cin =
             lookback_finish(lbq, lb_agg, (long)p.W, lb_n, lb_anchor, p.spin_limit, status);
         const float cout = fmaf(tP, cin, tS);
-        if (publish) slot_put1(rcar + cidx * p.W + w, cout);
-        if (c == 0 && p.dh0) p.dh0[(size_t)b * p.W + w] = p.canonical ? cout : 0.0f;
+        if (publish && wok) slot_put1(rcar + cidx * p.W + w, cout);
+        if (c == 0 && p.dh0 && wok) p.dh0[(size_t)b * p.W + w] = p.canonical ? cout : 0.0f;
         s_cin[j] = cin;
       }
       tc::named_bar(BAR_SCAN, NSCAN * 32);  // barrier B: the tile's right carry, the dx staging
@@ -780,15 +871,19 @@ __global__ void __maxnreg__(MAXREG)
       const float cin = fmaf(Rp, s_cin[j], Rs);  // carry into this part from the right
 
       // The dl buffers are free once the previous tile's MMAs are done.
-      if (it > 0) ctl.wait(dl_empty, (it - 1) & 1);
+      if (it > 0 && !LG) ctl.wait(dl_empty, (it - 1) & 1);
       tc::tc_fence_after();
+      const DlOut dlo{p.dlr, p.dli, p.dl_plane,
+                      ((size_t)b * p.T + (size_t)c * FUSED_C + tb) * p.W + w, p.W,
+                      wok ? valid : 0};
       if (fast)
-        bwd_pass2b<false, VARLEN>(tcol, tb, j, xr, dyb, gk.nk, PT, ab, SeqB{p, 0u, 0u, 0, 0}, cin, lg_empty, s_dl, dsp,
-                                  dba, dbx);
+        bwd_pass2b<false, VARLEN, GT, LGM>(tcol, tb, j, xr, dyb, gk.nk, PT, ab,
+                                           SeqB{p, 0u, 0u, 0, 0}, cin, lg_empty, s_dl, dsp, dba,
+                                           dbx, dlo);
       else
-        bwd_pass2b<true, VARLEN>(tcol, tb, j, xr, dyb, gk.nk, valid, ab,
-                                 seqb(smask, emask, b, c), cin, lg_empty, s_dl,
-                                 dsp, dba, dbx);
+        bwd_pass2b<true, VARLEN, GT, LGM>(tcol, tb, j, xr, dyb, gk.nk, valid, ab,
+                                          seqb(smask, emask, b, c), cin, lg_empty, s_dl, dsp,
+                                          dba, dbx, dlo);
       tc::fence_proxy_async_smem();
       tc::tc_fence_before();
       __syncwarp();
@@ -809,11 +904,11 @@ __global__ void __maxnreg__(MAXREG)
     // Per-CTA dW partials: lane j of the accumulators is input channel j; each part takes
     // 128 / NPART of the output-channel columns.  TMEM -> shared memory (the x / dy stages and
     // the dl buffers are free now: row j of 128-byte-swizzled boxes of 32 columns, conflict-free
-    // 16-byte stores) -> TMA store of 4 boxes per matrix.
-    if (my_tiles > 0) ctl.wait(dl_empty, (my_tiles - 1) & 1);
+    // 16-byte stores) -> TMA store of 4 boxes per matrix.  (Given logits: no projections.)
+    if (my_tiles > 0 && !LG) ctl.wait(dl_empty, (my_tiles - 1) & 1);
     tc::tc_fence_after();
 #pragma unroll
-    for (int mtx = 0; mtx < 2; ++mtx) {
+    for (int mtx = 0; mtx < (LG ? 0 : 2); ++mtx) {
       uint8_t* stage = mtx ? s_dl : s_in;
 #pragma unroll
       for (int sub = 0; sub < FUSED_K / NPART / 16; ++sub) {
@@ -836,7 +931,7 @@ __global__ void __maxnreg__(MAXREG)
     }
     tc::fence_proxy_async_smem();
     tc::named_bar(BAR_SCAN, NSCAN * 32);
-    if (store_thread) {
+    if (store_thread && !LG) {
 #pragma unroll
       for (int mtx = 0; mtx < 2; ++mtx)
 #pragma unroll
@@ -879,7 +974,7 @@ __global__ void __maxnreg__(MAXREG)
                       (size_t)blk * p.P * NV;
   const int per = (NV + p.P - 1) / p.P;
   const int v0 = rr * per;
-  const int nv = max(0, min(NV, v0 + per) - v0);
+  const int nv = LG ? 0 : max(0, min(NV, v0 + per) - v0);
   // This CTA's slice of all P partials comes into shared memory (free now; at most
   // (NV + P) x 16 bytes) by bulk copies in one round trip, completing on w_full's second phase;
   // then each vector is summed over the partials in order.
@@ -905,7 +1000,7 @@ __global__ void __maxnreg__(MAXREG)
       *reinterpret_cast<float4*>(dst) = t;
     }
   }
-  if (rr == 0 && threadIdx.x < FUSED_K) {
+  if (rr == 0 && threadIdx.x < FUSED_K && blk * FUSED_K + (int)threadIdx.x < p.W) {
     const int j = threadIdx.x, w = blk * FUSED_K + j;
     const float* vp = reinterpret_cast<const float*>(p.scratch + p.F.vec_part) +
                       (size_t)blk * p.P * NPART * 3 * FUSED_K;
@@ -970,7 +1065,7 @@ cudaError_t launch_fused_bwd(const Dims& d, const void* dy, const float* dhT, co
                     dims_p, str_p, box_p, CU_TENSOR_MAP_SWIZZLE_128B);
   if (e != cudaSuccess) return e;
 
-  BwdParams p;
+  BwdParams p = {};
   p.B = d.B;
   p.T = d.T;
   p.W = d.W;
@@ -1008,8 +1103,8 @@ cudaError_t launch_fused_bwd(const Dims& d, const void* dy, const float* dhT, co
   p.dbx = dbx;
   p.dLambda = dLambda;
   const size_t smem = SMEM_BYTES;
-  auto kern = vl ? (gf32 ? k_fused_bwd<float, true> : k_fused_bwd<bf16, true>)
-                 : (gf32 ? k_fused_bwd<float, false> : k_fused_bwd<bf16, false>);
+  auto kern = vl ? (gf32 ? k_fused_bwd<float, true, LGM_NONE> : k_fused_bwd<bf16, true, LGM_NONE>)
+                 : (gf32 ? k_fused_bwd<float, false, LGM_NONE> : k_fused_bwd<bf16, false, LGM_NONE>);
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   e = clear_slots(ws, p.F.L, s);
@@ -1027,6 +1122,92 @@ cudaError_t launch_fused_bwd(const Dims& d, const void* dy, const float* dhT, co
   kernel_event_before(s);
   e = cudaLaunchKernelEx(&cfg, kern, mx, mdy, mwa, mwx, mdx, mdwp, p);
   kernel_event_after(s);
+  if (e != cudaSuccess) return e;
+  note_launches(1);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_logits_bwd(const Dims& d, const void* dy, const float* dhT, const void* x,
+                              const void* lr, const void* li, size_t plane_elems, int nplanes,
+                              const float* Lambda, const uint8_t* rm, const int32_t* sp,
+                              const void* saved, int dx_dt, void* dx, int dl_dt, void* dlr,
+                              void* dli, size_t dl_plane, float* dLambda, float* dh0, void* ws,
+                              int spin_limit, int drop_tile, cudaStream_t s) {
+  if (!logits_scan_supported(d) || nplanes < 1 || nplanes > LG_PLANES)
+    return cudaErrorNotSupported;
+  const uint64_t W = d.W, T = d.T, B = d.B;
+  const uint64_t dims3[3] = {W, T, B};
+  const uint64_t str3[2] = {W * 2, T * W * 2};
+  const uint32_t box_in[3] = {16, FUSED_C, 1};
+  CUtensorMap mx, mdy, mlr, mli, mdx, mdwp;
+  cudaError_t e = encode_tmap(&mx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, x, dims3, str3, box_in,
+                              CU_TENSOR_MAP_SWIZZLE_32B);
+  const uint32_t box_dy[3] = {FUSED_K, FUSED_C, 1};
+  if (e == cudaSuccess)
+    e = encode_tmap(&mdy, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, dy, dims3, str3, box_dy,
+                    CU_TENSOR_MAP_SWIZZLE_NONE);
+  if (e == cudaSuccess) e = encode_logit_planes(d, lr, plane_elems, nplanes, &mlr);
+  if (e == cudaSuccess) e = encode_logit_planes(d, li, plane_elems, nplanes, &mli);
+  const bool gf32 = dx_dt == DT_F32;
+  const uint64_t gsz = gf32 ? 4 : 2;
+  const uint64_t strg[2] = {W * gsz, T * W * gsz};
+  const uint32_t box_dx[3] = {FUSED_K, FUSED_C, 1};
+  if (e == cudaSuccess)
+    e = encode_tmap(&mdx, gf32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                    3, dx, dims3, strg, box_dx, CU_TENSOR_MAP_SWIZZLE_NONE);
+  if (e != cudaSuccess) return e;
+  mdwp = mdx;  // unused without projections
+  BwdParams p = {};
+  p.B = d.B;
+  p.T = d.T;
+  p.W = d.W;
+  p.nblk = logits_slices(d);
+  p.nC = fused_chunks(d);
+  p.P = logits_ctas_per_slice(d);
+  p.canonical = d.mode == RGLRU_CANONICAL;
+  p.nplanes = nplanes;
+  p.dlr = dlr;
+  p.dli = dli;
+  p.dl_plane = dl_plane;
+  p.Lambda = Lambda;
+  p.reset_mask = p.canonical ? rm : nullptr;
+  p.segment_pos = p.canonical ? sp : nullptr;
+  p.dhT = dhT;
+  const FusedFwdLayout FL = fused_fwd_layout(d);
+  p.fwd_carry = reinterpret_cast<const float*>(static_cast<const uint8_t*>(saved) + FL.L.carry);
+  p.dh0 = dh0;
+  p.scratch = static_cast<uint8_t*>(ws);
+  p.F = fused_bwd_layout(d);
+  p.spin_limit = spin_limit;
+  p.drop_tile = drop_tile;
+  const LookbackPlan lp = lookback_plan(p.P, d.B);
+  p.lb_dist = lp.dist;
+  p.lb_shift = lp.shift;
+  p.dx = dx;
+  p.dLambda = dLambda;
+  decltype(&k_fused_bwd<float, false, LGM_SAME>) kern;
+  if (dl_dt == DT_SPLIT) {
+    if (!gf32) return cudaErrorNotSupported;
+    kern = k_fused_bwd<float, false, LGM_SPLIT>;
+  } else {
+    if ((dl_dt == DT_F32) != gf32) return cudaErrorNotSupported;
+    kern = gf32 ? k_fused_bwd<float, false, LGM_SAME> : k_fused_bwd<bf16, false, LGM_SAME>;
+  }
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)LG_SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  e = clear_slots(ws, p.F.L, s);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p.P * p.nblk);
+  cfg.blockDim = dim3(NTHREADS);
+  cfg.dynamicSmemBytes = LG_SMEM_BYTES;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, kern, mx, mdy, mlr, mli, mdx, mdwp, p);
   if (e != cudaSuccess) return e;
   note_launches(1);
   return cudaGetLastError();

@@ -63,10 +63,20 @@ constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;  // 2 s: a pipeline wait never
 constexpr uint32_t XCH_BYTES = NBUF * NPART * FUSED_K * 8;  // part maps, one set per buffer
 constexpr size_t SMEM_BYTES =
     2 * W_BYTES + XSTAGES * X_BYTES + Y_BYTES + XCH_BYTES + 256 + 1024;
+// Given-logits mode (the scan of rglru_forward and of the composed layer): no weights; each
+// stage holds the x tile and up to two bf16 planes of each logit tile, and a 64 x 64 identity
+// takes the place of W in the MMA that lays the logits out in TMEM.
+constexpr int LG_PLANES = 2;
+constexpr int LG_STAGES = 2;
+constexpr uint32_t LG_STAGE_BYTES = (1 + 2 * LG_PLANES) * X_BYTES;
+constexpr uint32_t ID_BYTES = FUSED_C * FUSED_C * 2;
+constexpr size_t LG_SMEM_BYTES =
+    ID_BYTES + LG_STAGES * LG_STAGE_BYTES + Y_BYTES + XCH_BYTES + 256 + 1024;
 constexpr uint32_t STATUS_PIPE = 2u;
 
 struct FwdParams {
   int B, T, W, nblk, nC, P, canonical;
+  int nplanes;  // given-logits mode: bf16 planes per logit (1, or 2 = hi + lo)
   const float* Lambda;
   const float* ba;
   const float* bx;
@@ -203,24 +213,29 @@ __device__ __forceinline__ void local_scan(uint32_t t_lr, uint32_t t_li, uint32_
   tc::tmem_st_wait();
 }
 
-template <bool VARLEN>
+// LG: given-logits mode.  tm_wa / tm_wx then map the bf16 logit planes lr, li
+// [plane][B][T][W]; blk is a 128-channel slice of W (the last one may be partial: its channels
+// past W read zeros and write nothing).
+template <bool VARLEN, bool LG>
 __global__ void __maxnreg__(MAXREG)
     k_fused_fwd(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_wa,
                 const __grid_constant__ CUtensorMap tm_wx, const __grid_constant__ CUtensorMap tm_y,
                 FwdParams p) {
+  constexpr int XS = LG ? LG_STAGES : XSTAGES;
+  constexpr uint32_t STB = LG ? LG_STAGE_BYTES : X_BYTES;
   extern __shared__ uint8_t smem_raw[];
   // 1024-byte aligned base, formed by pointer arithmetic so that it stays a shared pointer
   uint8_t* smem = smem_raw + ((1024u - (tc::smem_u32(smem_raw) & 1023u)) & 1023u);
-  uint8_t* s_wa = smem;
-  uint8_t* s_wx = smem + W_BYTES;
-  uint8_t* s_x = smem + 2 * W_BYTES;
-  uint8_t* s_y = s_x + XSTAGES * X_BYTES;
+  uint8_t* s_wa = smem;            // LG: the identity
+  uint8_t* s_wx = smem + W_BYTES;  // (unused in LG)
+  uint8_t* s_x = smem + (LG ? ID_BYTES : 2 * W_BYTES);
+  uint8_t* s_y = s_x + XS * STB;
   float2* s_agg = reinterpret_cast<float2*>(s_y + Y_BYTES);  // [buffer][part][channel]
   uint64_t* bars = reinterpret_cast<uint64_t*>(s_agg + NBUF * NPART * FUSED_K);
   uint64_t* w_full = bars;
   uint64_t* x_full = bars + 1;
-  uint64_t* x_empty = bars + 1 + XSTAGES;
-  uint64_t* acc_full = bars + 1 + 2 * XSTAGES;
+  uint64_t* x_empty = bars + 1 + XS;
+  uint64_t* acc_full = bars + 1 + 2 * XS;
   uint64_t* acc_empty = acc_full + NBUF;  // buffer read out by the output warps
   uint64_t* park_full = acc_empty + NBUF;  // a tile parked in its buffer (scan -> output)
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(park_full + NBUF);
@@ -234,9 +249,10 @@ __global__ void __maxnreg__(MAXREG)
 
   if (threadIdx.x == 0) {
     tc::mbar_init(w_full, 1);
-    for (int s = 0; s < XSTAGES; ++s) {
+    for (int s = 0; s < XS; ++s) {
       tc::mbar_init(&x_full[s], 1);
-      tc::mbar_init(&x_empty[s], NSCAN);
+      // LG: the stage also holds the logit planes, read by the MMA
+      tc::mbar_init(&x_empty[s], NSCAN + (LG ? 1 : 0));
     }
     for (int a = 0; a < NBUF; ++a) {
       tc::mbar_init(&acc_full[a], 1);
@@ -246,6 +262,7 @@ __global__ void __maxnreg__(MAXREG)
     *abort_flag = 0u;
     tc::fence_barrier_init();
   }
+  if (LG) tc::write_identity_sw32(s_wa, FUSED_C);
   if (warp == 0) {
     tc::tmem_alloc(tmem_holder, TMEM_COLS);
     tc::tmem_relinquish();
@@ -263,21 +280,34 @@ __global__ void __maxnreg__(MAXREG)
       tc::prefetch_tmap(&tm_x);
       tc::prefetch_tmap(&tm_wa);
       tc::prefetch_tmap(&tm_wx);
-      tc::mbar_expect_tx(w_full, 2 * W_BYTES);
-      for (int g = 0; g < FUSED_K / 16; ++g) {
-        tc::tma_load_2d(s_wa + g * SLAB_W, &tm_wa, w_full, 16 * g, blk * FUSED_K);
-        tc::tma_load_2d(s_wx + g * SLAB_W, &tm_wx, w_full, 16 * g, blk * FUSED_K);
+      if (!LG) {
+        tc::mbar_expect_tx(w_full, 2 * W_BYTES);
+        for (int g = 0; g < FUSED_K / 16; ++g) {
+          tc::tma_load_2d(s_wa + g * SLAB_W, &tm_wa, w_full, 16 * g, blk * FUSED_K);
+          tc::tma_load_2d(s_wx + g * SLAB_W, &tm_wx, w_full, 16 * g, blk * FUSED_K);
+        }
+      } else {
+        tc::mbar_arrive(w_full);  // the identity is in place (written before the CTA barrier)
       }
       int it = 0;
       TileWalk tw(rr, p.P, p.B);
       for (int n = rr; n < ntiles; n += p.P, ++it, tw.next()) {
-        const int st = it % XSTAGES;
-        const uint32_t ph = (it / XSTAGES) & 1;
+        const int st = it % XS;
+        const uint32_t ph = (it / XS) & 1;
         if (!ctl.wait(&x_empty[st], ph ^ 1u)) continue;
-        tc::mbar_expect_tx(&x_full[st], X_BYTES);
+        uint8_t* sb = s_x + st * STB;
+        tc::mbar_expect_tx(&x_full[st], LG ? (1 + 2 * p.nplanes) * X_BYTES : X_BYTES);
         for (int s = 0; s < FUSED_K / 16; ++s)
-          tc::tma_load_3d(s_x + st * X_BYTES + s * SLAB_X, &tm_x, &x_full[st],
-                          blk * FUSED_K + 16 * s, tw.c * FUSED_C, tw.b);
+          tc::tma_load_3d(sb + s * SLAB_X, &tm_x, &x_full[st], blk * FUSED_K + 16 * s,
+                          tw.c * FUSED_C, tw.b);
+        if (LG) {
+          for (int g = 0; g < 2; ++g)
+            for (int pl = 0; pl < p.nplanes; ++pl)
+              for (int s = 0; s < FUSED_K / 16; ++s)
+                tc::tma_load_4d(sb + (1 + g * LG_PLANES + pl) * X_BYTES + s * SLAB_X,
+                                g ? &tm_wx : &tm_wa, &x_full[st], blk * FUSED_K + 16 * s,
+                                tw.c * FUSED_C, tw.b, pl);
+        }
       }
     }
   } else if (warp == 1) {
@@ -291,24 +321,42 @@ __global__ void __maxnreg__(MAXREG)
       const uint32_t wa = tc::smem_u32(s_wa), wx = tc::smem_u32(s_wx);
       int it = 0;
       for (int n = rr; n < ntiles; n += p.P, ++it) {
-        const int st = it % XSTAGES;
-        const uint32_t ph = (it / XSTAGES) & 1;
+        const int st = it % XS;
+        const uint32_t ph = (it / XS) & 1;
         const int a = it % NBUF;
         const uint32_t aph = (it / NBUF) & 1;
         if (!ctl.wait(&acc_empty[a], aph ^ 1u)) continue;
         if (!ctl.wait(&x_full[st], ph)) continue;
         tc::tc_fence_after();
-        const uint32_t xs = tc::smem_u32(s_x + st * X_BYTES);
+        const uint32_t xs = tc::smem_u32(s_x + st * STB);
         const uint32_t d_r = tmem + a * 128, d_i = d_r + 64;
+        if (!LG) {
 #pragma unroll
-        for (int kk = 0; kk < FUSED_K / 16; ++kk) {
-          // A: W^T, MN-major, 16-channel groups 4 KB apart (LBO), 8-row K groups 256 B (SBO);
-          // B: x tile, K-major, one 16-channel slab per K step, 8-row groups 256 B apart.
-          const uint64_t bdesc = tc::smem_desc_sw32(xs + kk * SLAB_X, 16, 256);
-          if (leader) tc::mma_bf16(d_r, tc::smem_desc_sw32(wa + kk * 512, SLAB_W, 256), bdesc, idesc, kk > 0);
-          if (leader) tc::mma_bf16(d_i, tc::smem_desc_sw32(wx + kk * 512, SLAB_W, 256), bdesc, idesc, kk > 0);
+          for (int kk = 0; kk < FUSED_K / 16; ++kk) {
+            // A: W^T, MN-major, 16-channel groups 4 KB apart (LBO), 8-row K groups 256 B (SBO);
+            // B: x tile, K-major, one 16-channel slab per K step, 8-row groups 256 B apart.
+            const uint64_t bdesc = tc::smem_desc_sw32(xs + kk * SLAB_X, 16, 256);
+            if (leader) tc::mma_bf16(d_r, tc::smem_desc_sw32(wa + kk * 512, SLAB_W, 256), bdesc, idesc, kk > 0);
+            if (leader) tc::mma_bf16(d_i, tc::smem_desc_sw32(wx + kk * 512, SLAB_W, 256), bdesc, idesc, kk > 0);
+          }
+        } else if (leader) {
+          // lr^T = L_r^T I: A = the logit plane tile, MN-major (16-channel slabs 2 KB apart,
+          // 16 tokens per K step); B = the identity, K-major; the planes accumulate (hi + lo)
+          for (int g = 0; g < 2; ++g)
+            for (int pl = 0; pl < p.nplanes; ++pl)
+#pragma unroll
+              for (int kk = 0; kk < FUSED_C / 16; ++kk)
+                tc::mma_bf16(g ? d_i : d_r,
+                             tc::smem_desc_sw32(xs + (1 + g * LG_PLANES + pl) * X_BYTES + kk * 512,
+                                                SLAB_X, 256),
+                             tc::smem_desc_sw32(wa + kk * SLAB_X, 16, 256), idesc,
+                             (pl > 0 || kk > 0) ? 1u : 0u);
         }
-        if (leader) tc::mma_commit(&acc_full[a]);
+        if (leader) {
+          tc::mma_commit(&acc_full[a]);
+          if (LG) tc::mma_commit(&x_empty[st]);  // the logit planes are read
+        }
+        __syncwarp();
       }
     }
   } else if (warp < 2 + NSCAN) {
@@ -318,7 +366,8 @@ __global__ void __maxnreg__(MAXREG)
     const int part = (warp - 2) >> 2;  // token part of the tile
     const int q = warp & 3;            // TMEM lane quadrant this warp may access
     const int j = q * 32 + lane;
-    const int w = blk * FUSED_K + j;
+    // channels past W (LG only) compute, unstored
+    const int w = LG ? min(blk * FUSED_K + j, p.W - 1) : blk * FUSED_K + j;
     const int tb = part * PT;
     const uint32_t lane_base = (uint32_t)(q * 32) << 16;
     GateK gk;
@@ -344,8 +393,8 @@ __global__ void __maxnreg__(MAXREG)
     TokMarks mk = marks(cur);  // tile it's, requested during tile it - 1
     for (int it = 0; it < my_tiles; ++it, cur.next()) {
       const int c = cur.c, b = cur.b;
-      const int st = it % XSTAGES;
-      const uint32_t ph = (it / XSTAGES) & 1;
+      const int st = it % XS;
+      const uint32_t ph = (it / XS) & 1;
       const int a = it % NBUF;
       const uint32_t aph = (it / NBUF) & 1;
       const TokMarks now = mk;
@@ -366,7 +415,7 @@ __global__ void __maxnreg__(MAXREG)
       ctl.wait(&acc_full[a], aph);
       ctl.wait(&x_full[st], ph);
       tc::tc_fence_after();
-      const uint32_t xt = tc::smem_u32(s_x + st * X_BYTES + tb * 32);
+      const uint32_t xt = tc::smem_u32(s_x + st * STB + tb * 32);
       const uint32_t xb0 = xt + xoff0, xb1 = xt + xoff1;
       const uint32_t t_lr = tmem + lane_base + a * 128 + tb;
       float rh, rA;
@@ -389,7 +438,9 @@ __global__ void __maxnreg__(MAXREG)
     // slots, which have the next tile's scan to arrive.
     const int q = warp & 3;
     const int j = q * 32 + lane;
-    const int w = blk * FUSED_K + j;
+    // channels past W (LG only): nothing stored, their look-back reads a real channel's
+    const bool wok = !LG || blk * FUSED_K + j < p.W;
+    const int w = LG ? min(blk * FUSED_K + j, p.W - 1) : blk * FUSED_K + j;
     const uint32_t lane_base = (uint32_t)(q * 32) << 16;
     float* carry = reinterpret_cast<float*>(p.scratch + p.L.carry);
     float2* agg = reinterpret_cast<float2*>(p.scratch + p.L.agg);
@@ -432,7 +483,7 @@ __global__ void __maxnreg__(MAXREG)
           nTb = fmaf(g.x, nTb, g.y);
           nTa *= g.x;
         }
-        if ((blk * ntiles + n) != p.drop_tile)
+        if ((blk * ntiles + n) != p.drop_tile && wok)
           slot_put2(agg + ((size_t)cur.b * p.nC + cur.c) * p.W + w, nTa, nTb);
       }
 
@@ -443,9 +494,10 @@ __global__ void __maxnreg__(MAXREG)
             lookback_finish(lbq, lb_agg, -(long)p.W, lb_n, lb_anchor, p.spin_limit, status);
         const float hend = fmaf(Ta, hin_t, Tb);
         float* crow = carry + (size_t)pb * (p.nC + 1) * p.W;
-        if ((blk * ntiles + n - p.P) != p.drop_tile) slot_put1(crow + (size_t)(pc + 1) * p.W + w, hend);
-        if (pc == 0) slot_put1(crow + w, hin_t);
-        if (pc == p.nC - 1 && p.hT) p.hT[(size_t)pb * p.W + w] = hend;
+        if ((blk * ntiles + n - p.P) != p.drop_tile && wok)
+          slot_put1(crow + (size_t)(pc + 1) * p.W + w, hend);
+        if (pc == 0 && wok) slot_put1(crow + w, hin_t);
+        if (pc == p.nC - 1 && p.hT && wok) p.hT[(size_t)pb * p.W + w] = hend;
         // packed sequences ending in the tile: their final state (warp-uniform masks)
         uint32_t em0 = 0u, em1 = 0u;
         const int e0 = pe0, e1 = pe1;
@@ -630,7 +682,7 @@ cudaError_t launch_fused_fwd(const Dims& d, const void* x, const void* Wa, const
   const LookbackPlan lp = lookback_plan(p.P, d.B);
   p.lb_dist = lp.dist;
   p.lb_shift = lp.shift;
-  auto kern = vl ? k_fused_fwd<true> : k_fused_fwd<false>;
+  auto kern = vl ? k_fused_fwd<true, false> : k_fused_fwd<false, false>;
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)SMEM_BYTES);
   if (e != cudaSuccess) return e;
@@ -649,6 +701,95 @@ cudaError_t launch_fused_fwd(const Dims& d, const void* x, const void* Wa, const
   kernel_event_before(s);
   e = cudaLaunchKernelEx(&cfg, kern, mx, mwa, mwx, my, p);
   kernel_event_after(s);
+  if (e == cudaSuccess) note_launches(1);
+  return e;
+}
+
+int logits_slices(const Dims& d) { return (d.W + FUSED_K - 1) / FUSED_K; }
+
+int logits_ctas_per_slice(const Dims& d) {
+  const int sms = sm_count();
+  const int n = logits_slices(d);
+  if (sms <= 0 || n > sms || n > FUSED_MAX_CTAS) return 0;
+  const int p = sms / n;
+  return p * n <= FUSED_MAX_CTAS ? p : FUSED_MAX_CTAS / n;
+}
+
+bool logits_scan_supported(const Dims& d) {
+  return d.io == RGLRU_BF16 && logits_ctas_per_slice(d) >= 1;
+}
+
+cudaError_t encode_logit_planes(const Dims& d, const void* base, size_t plane_elems, int nplanes,
+                                CUtensorMap* m) {
+  const uint64_t W = d.W, T = d.T, B = d.B;
+  const uint64_t dims[4] = {W, T, B, (uint64_t)nplanes};
+  const uint64_t str[3] = {W * 2, T * W * 2, (uint64_t)plane_elems * 2};
+  const uint32_t box[4] = {16, FUSED_C, 1, 1};
+  return encode_tmap(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, base, dims, str, box,
+                     CU_TENSOR_MAP_SWIZZLE_32B);
+}
+
+cudaError_t launch_logits_fwd(const Dims& d, const void* x, const void* lr, const void* li,
+                              size_t plane_elems, int nplanes, const float* Lambda,
+                              const uint8_t* rm, const int32_t* sp, const float* h0, void* y,
+                              float* hT, void* saved, int spin_limit, int drop_tile,
+                              cudaStream_t s) {
+  if (!logits_scan_supported(d) || nplanes < 1 || nplanes > LG_PLANES)
+    return cudaErrorNotSupported;
+  const uint64_t W = d.W, T = d.T, B = d.B;
+  const uint64_t dims3[3] = {W, T, B};
+  const uint64_t str3[2] = {W * 2, T * W * 2};
+  const uint32_t box_x[3] = {16, FUSED_C, 1};
+  CUtensorMap mx, mlr, mli, my;
+  cudaError_t e = encode_tmap(&mx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, x, dims3, str3, box_x,
+                              CU_TENSOR_MAP_SWIZZLE_32B);
+  const uint32_t box_y[3] = {32, FUSED_C, 1};
+  if (e == cudaSuccess)
+    e = encode_tmap(&my, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, y, dims3, str3, box_y,
+                    CU_TENSOR_MAP_SWIZZLE_NONE);
+  if (e == cudaSuccess) e = encode_logit_planes(d, lr, plane_elems, nplanes, &mlr);
+  if (e == cudaSuccess) e = encode_logit_planes(d, li, plane_elems, nplanes, &mli);
+  if (e != cudaSuccess) return e;
+  FwdParams p = {};
+  p.B = d.B;
+  p.T = d.T;
+  p.W = d.W;
+  p.nblk = logits_slices(d);
+  p.nC = fused_chunks(d);
+  p.P = logits_ctas_per_slice(d);
+  p.canonical = d.mode == RGLRU_CANONICAL;
+  p.nplanes = nplanes;
+  p.Lambda = Lambda;
+  p.ba = nullptr;
+  p.bx = nullptr;
+  p.reset_mask = p.canonical ? rm : nullptr;
+  p.segment_pos = p.canonical ? sp : nullptr;
+  p.h0 = h0;
+  p.hT = hT;
+  p.scratch = static_cast<uint8_t*>(saved);
+  p.L = fused_layout(d, false);
+  p.spin_limit = spin_limit;
+  p.drop_tile = drop_tile;
+  const LookbackPlan lp = lookback_plan(p.P, d.B);
+  p.lb_dist = lp.dist;
+  p.lb_shift = lp.shift;
+  auto kern = k_fused_fwd<false, true>;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)LG_SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  e = clear_slots(saved, p.L, s);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p.P * p.nblk);
+  cfg.blockDim = dim3(NTHREADS);
+  cfg.dynamicSmemBytes = LG_SMEM_BYTES;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, kern, mx, mlr, mli, my, p);
   if (e == cudaSuccess) note_launches(1);
   return e;
 }

@@ -2,6 +2,7 @@
 // buffer layouts of `saved` / `workspace`, kernel argument blocks and launchers.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -231,6 +232,9 @@ struct ScanBwdArgs {
 
 // Adds n to the process-wide count of kernels enqueued (rglru_kernel_launches).
 void note_launches(unsigned n);
+// The failure-injection settings of rglru_debug_lookback (look-back poll limit, dropped tile).
+int debug_spin_limit();
+int debug_drop_tile();
 
 // rglru_debug_kernel_events: record the caller's events around the next tensor-core kernel.
 extern cudaEvent_t g_kernel_events[2];
@@ -265,6 +269,28 @@ cudaError_t launch_fused_fwd(const Dims& d, const void* x, const void* Wa, const
                              cudaStream_t s, const Varlen* vl = nullptr);
 bool fused_supported(const Dims& d);
 int fused_ctas_per_block(const Dims& d);
+// The same kernels with the logits given instead of projected (rglru_forward / rglru_backward
+// and the composed layer, bf16 x): `nplanes` bf16 planes per logit (1, or 2 = hi + lo of a
+// float32 value), `plane_elems` apart; 128-channel slices of W, the last one partial.
+int logits_slices(const Dims& d);
+int logits_ctas_per_slice(const Dims& d);
+bool logits_scan_supported(const Dims& d);
+// dx: the direct term only (dx_dt: DT_BF16 or DT_F32); dlr / dli in dl_dt (the dx dtype, or
+// DT_SPLIT with a float32 dx: hi + lo planes dl_plane elements apart); dLambda, dh0 as in the
+// fused backward.  `saved` comes from launch_logits_fwd with the same inputs.
+cudaError_t launch_logits_bwd(const Dims& d, const void* dy, const float* dhT, const void* x,
+                              const void* lr, const void* li, size_t plane_elems, int nplanes,
+                              const float* Lambda, const uint8_t* rm, const int32_t* sp,
+                              const void* saved, int dx_dt, void* dx, int dl_dt, void* dlr,
+                              void* dli, size_t dl_plane, float* dLambda, float* dh0, void* ws,
+                              int spin_limit, int drop_tile, cudaStream_t s);
+cudaError_t encode_logit_planes(const Dims& d, const void* base, size_t plane_elems, int nplanes,
+                                CUtensorMap* m);
+cudaError_t launch_logits_fwd(const Dims& d, const void* x, const void* lr, const void* li,
+                              size_t plane_elems, int nplanes, const float* Lambda,
+                              const uint8_t* rm, const int32_t* sp, const float* h0, void* y,
+                              float* hT, void* saved, int spin_limit, int drop_tile,
+                              cudaStream_t s);
 // Clears the status word of a scan layout and marks every carry / aggregate slot empty.
 cudaError_t clear_slots(void* buf, const ScanLayout& L, cudaStream_t s);
 

@@ -67,7 +67,10 @@ rglru_status rglru_forward_noalloc(const rglru_shape* shape, const void* x, cons
   if (!req(x) || !req(lr) || !req(li) || !req(Lambda) || !req(y) || !opt(hT))
     return RGLRU_ERR_INVALID_ARG;
   if ((st = check_resets(d, reset_mask, segment_pos, h0)) != RGLRU_OK) return st;
-  const size_t need = scan_layout(d, false).total;
+  // bf16 goes through the fused scan kernel with the logits given (as rglru_forward does),
+  // float32 through the CUDA-core scan
+  const bool lg = logits_scan_supported(d);
+  const size_t need = lg ? fused_fwd_layout(d).total : scan_layout(d, false).total;
   if (need > kScratchBytes) {
     fprintf(stderr,
             "librglru: rglru_forward_noalloc needs %zu bytes of look-back scratch for this "
@@ -79,6 +82,10 @@ rglru_status rglru_forward_noalloc(const rglru_shape* shape, const void* x, cons
   void* scratch = nullptr;
   cudaError_t e = scratch_address(&scratch);
   if (e != cudaSuccess) return cuda_status(e);
+  if (lg)
+    return cuda_status(launch_logits_fwd(d, x, lr, li, d.N, 1, Lambda, reset_mask, segment_pos,
+                                         h0, y, hT, scratch, debug_spin_limit(),
+                                         debug_drop_tile(), stream));
   const ScanFwdArgs a =
       fwd_args(d, x, lr, li, Lambda, reset_mask, segment_pos, h0, y, hT, scratch);
   e = cudaMemsetAsync(scratch, 0, a.L.zero_bytes, stream);

@@ -129,13 +129,16 @@ struct ProjParams {
 // ================================================================ forward projection
 // CTA (blk, r) keeps Wa[blk], Wx[blk] in shared memory and takes the row tiles r, r + P, ...
 // Per tile the x tile feeds two accumulations, lr then li, each into the next slot of a ring
-// of k-column TMEM buffers; the epilogue warps add the bias, convert and store.
-template <typename OT>
+// of k-column TMEM buffers; the epilogue warps add the bias, convert and store.  SPLIT: the
+// float32 logits go out as bf16 hi and lo planes (tm_lr2 / tm_li2 map the lo planes).
+template <typename OT, bool SPLIT>
 __global__ void __launch_bounds__(NTHREADS, 1)
     k_proj_fwd(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_wa,
                const __grid_constant__ CUtensorMap tm_wx,
                const __grid_constant__ CUtensorMap tm_lr,
-               const __grid_constant__ CUtensorMap tm_li, const __grid_constant__ ProjParams p,
+               const __grid_constant__ CUtensorMap tm_li,
+               const __grid_constant__ CUtensorMap tm_lr2,
+               const __grid_constant__ CUtensorMap tm_li2, const __grid_constant__ ProjParams p,
                int stages) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (tc::smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -237,6 +240,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const int q = warp & 3;  // TMEM lane quadrant = rows 32 q .. 32 q + 31 of a tile
     Stager<OT> sg{s_stage + (warp - 2) * NBOX * Stager<OT>::BOX, 0u};
     const CUtensorMap* out[2] = {&tm_lr, &tm_li};
+    const CUtensorMap* out2[2] = {&tm_lr2, &tm_li2};
     for (int it = 0; it < my_tiles; ++it) {
       const int row0 = (rr + it * p.P) * TR + 32 * q;
 #pragma unroll 1
@@ -255,6 +259,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           uint8_t* box = sg.next();
           stage_row<OT>(box, lane, v);
           sg.store(out[m], box, blk * k + 16 * c, row0);
+          if (SPLIT) {  // lo = v - bf16(v), exact in float32, then rounded to bf16
+#pragma unroll
+            for (int e = 0; e < 16; ++e) v[e] -= __bfloat162float(__float2bfloat16_rn(v[e]));
+            uint8_t* box2 = sg.next();
+            stage_row<OT>(box2, lane, v);
+            sg.store(out2[m], box2, blk * k + 16 * c, row0);
+          }
         }
         tc::tc_fence_before();
         __syncwarp();
@@ -752,12 +763,21 @@ cudaError_t launch_proj_fwd(const Dims& d, int ot, const void* x, const void* Wa
                             const float* ba, const void* Wx, const float* bx, void* lr, void* li,
                             cudaStream_t s) {
   if (!proj_tc_supported(d)) return cudaErrorNotSupported;
-  CUtensorMap mx, mwa, mwx, mlr, mli;
+  const bool split = ot == DT_SPLIT;
+  const int et = split ? DT_BF16 : ot;  // element type of each output plane
+  CUtensorMap mx, mwa, mwx, mlr, mli, mlr2, mli2;
   cudaError_t e = act_map(d, x, &mx);
   if (e == cudaSuccess) e = weight_maps(d, Wa, Wx, &mwa, &mwx);
-  if (e == cudaSuccess) e = out_map(d, lr, ot, &mlr);
-  if (e == cudaSuccess) e = out_map(d, li, ot, &mli);
+  if (e == cudaSuccess) e = out_map(d, lr, et, &mlr);
+  if (e == cudaSuccess) e = out_map(d, li, et, &mli);
   if (e != cudaSuccess) return e;
+  mlr2 = mlr;
+  mli2 = mli;
+  if (split) {  // the lo planes follow the hi planes, N elements later
+    e = out_map(d, static_cast<bf16*>(lr) + d.N, DT_BF16, &mlr2);
+    if (e == cudaSuccess) e = out_map(d, static_cast<bf16*>(li) + d.N, DT_BF16, &mli2);
+    if (e != cudaSuccess) return e;
+  }
   ProjParams p = {};
   p.R = d.B * d.T;
   p.k = d.k;
@@ -766,7 +786,7 @@ cudaError_t launch_proj_fwd(const Dims& d, int ot, const void* x, const void* Wa
   p.P = ctas_per_group(d.nblk);
   p.bias[0] = ba;
   p.bias[1] = bx;
-  const size_t box = 32 * 16 * (ot == DT_F32 ? 4 : 2);
+  const size_t box = 32 * 16 * (et == DT_F32 ? 4 : 2);
   const int NS = 512 / (int)kcols(d.k);
   const size_t fixed = 1024 + 2 * (size_t)d.k * d.k * 2 + 4 * NBOX * box + 2 * d.k * 4 +
                        bars_bytes(1 + 2 * NS);
@@ -774,10 +794,11 @@ cudaError_t launch_proj_fwd(const Dims& d, int ot, const void* x, const void* Wa
   while (stages > 1 && fixed + stages * (size_t)tile_bytes(d.k) + 16 * stages > SMEM_MAX) --stages;
   const size_t smem = fixed + stages * (size_t)tile_bytes(d.k) + 16 * stages;
   if (smem > SMEM_MAX) return cudaErrorNotSupported;
-  auto kern = ot == DT_F32 ? k_proj_fwd<float> : k_proj_fwd<bf16>;
+  auto kern = split ? k_proj_fwd<bf16, true>
+                    : (ot == DT_F32 ? k_proj_fwd<float, false> : k_proj_fwd<bf16, false>);
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  kern<<<p.P * d.nblk, NTHREADS, smem, s>>>(mx, mwa, mwx, mlr, mli, p, stages);
+  kern<<<p.P * d.nblk, NTHREADS, smem, s>>>(mx, mwa, mwx, mlr, mli, mlr2, mli2, p, stages);
   note_launches(1);
   return cudaGetLastError();
 }

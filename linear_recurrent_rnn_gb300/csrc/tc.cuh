@@ -96,6 +96,16 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, u
       : "memory");
 }
 
+__device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, uint64_t* bar,
+                                            int c0, int c1, int c2, int c3) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2),
+      "r"(c3)
+      : "memory");
+}
+
 // Bulk copy of `bytes` (a multiple of 16, both addresses 16-byte aligned) from global memory to
 // this CTA's shared memory, completing as transaction bytes on `bar`.
 __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes,
@@ -330,6 +340,26 @@ __device__ __forceinline__ uint64_t smem_desc_sw32(uint32_t saddr, uint32_t lbo,
   d |= (uint64_t)1u << 46;
   d |= (uint64_t)6u << 61;
   return d;
+}
+
+// The n x n identity (bf16, n a multiple of 16) as a K-major MMA operand in the slab layout
+// that TMA gives a [row][column] tile with the 32-byte swizzle: slab s holds columns
+// 16 s .. 16 s + 15 of all n rows, 32 bytes a row, the row's 16-byte halves swapped on rows
+// 4..7 of every 8.  As the B operand of D = L^T I it copies the MN-major tile L into the
+// accumulator exactly (one product with 1.0 per output).  Called by every thread of the CTA
+// before a CTA barrier; the fence hands the generic-proxy writes to the tensor core.
+__device__ __forceinline__ void write_identity_sw32(uint8_t* dst, int n) {
+  const int chunks = n * n * 2 / 16;
+  for (int q = threadIdx.x; q < chunks; q += blockDim.x) {
+    const int slab = q / (2 * n), row = (q % (2 * n)) / 2, half = q % 2;
+    const int k0 = slab * 16 + ((half ^ ((row >> 2) & 1)) << 3);
+    uint32_t w[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+      w[e] = (k0 + 2 * e == row ? 0x3F80u : 0u) | (k0 + 2 * e + 1 == row ? 0x3F800000u : 0u);
+    *reinterpret_cast<uint4*>(dst + q * 16) = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+  fence_proxy_async_smem();
 }
 
 // Instruction descriptor of kind::f16: f32 accumulator, bf16 A and B, the majorness of each

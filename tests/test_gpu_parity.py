@@ -323,9 +323,10 @@ def test_outputs_stay_in_bounds():
 
 
 def test_lookback_timeout_is_reported():
-    """A tile that never publishes makes its successor's bounded wait run out; the call still
-    finishes and the status word reports the timeout.  Afterwards the defaults are back."""
-    wl = W_("timeout", 1, 128, 64, 64, "bf16", "restricted")
+    """The CUDA-core scan (float32 I/O): a tile that never publishes makes its successor's
+    bounded wait run out; the call still finishes and the status word reports the timeout.
+    Afterwards the defaults are back."""
+    wl = W_("timeout", 1, 128, 64, 64, "f32", "restricted")
     inp = generate(wl, 43, want_logits=True)
     sh = shape_for(wl)
     d = {k: dev(v) for k, v in inp.items()}
@@ -339,6 +340,48 @@ def test_lookback_timeout_is_reported():
         R.rglru_debug_lookback(0, -1)
     R.rglru_forward(sh, d["x"], d["lr"], d["li"], d["Lambda"], None, None, None, y, None, saved)
     assert R.rglru_sync_status(saved) == R.OK
+    o = oracle_inputs(inp)
+    yr, _ = oracle.forward(oracle.RESTRICTED, o["x"], o["lr"], o["li"], o["Lambda"])
+    assert_close("y", host(y), yr, io="f32", kind="out")
+
+
+@pytest.mark.parametrize("which", ["forward", "backward"])
+def test_given_logits_lookback_timeout_is_reported(which):
+    """rglru_forward / rglru_backward with bf16 I/O run the tensor-core scan kernels with the
+    logits given: a tile that never publishes makes the later chunks' bounded look-back waits
+    run out; the call finishes and the status word of its scratch reports the timeout.  One
+    128-channel slice and 12 chunks, so every tile has a CTA of its own and the dropped tile
+    (chunk 5) lies inside its successors' look-back windows."""
+    wl = W_("timeout-lg", 1, 12 * 64, 128, 128, "bf16", "restricted")
+    inp = generate(wl, 46, want_logits=True)
+    sh = shape_for(wl)
+    d = {k: dev(v) for k, v in inp.items()}
+    y = torch.empty_like(d["x"])
+    saved, ws = R.alloc_saved(sh), R.alloc_workspace(sh)
+    dx, dlr, dli = (torch.empty_like(d["x"]) for _ in range(3))
+    dL = torch.empty(wl.W, device="cuda")
+
+    def fwd():
+        R.rglru_forward(sh, d["x"], d["lr"], d["li"], d["Lambda"], None, None, None, y, None,
+                        saved)
+
+    def bwd():
+        R.rglru_backward(sh, d["dy"], None, d["x"], d["lr"], d["li"], d["Lambda"], None, None,
+                         None, saved, dx, dlr, dli, dL, None, ws)
+
+    if which == "backward":
+        fwd()
+        assert R.rglru_sync_status(saved) == R.OK
+    R.rglru_debug_lookback(2000, 5)
+    try:
+        (fwd if which == "forward" else bwd)()
+        assert R.rglru_sync_status(saved if which == "forward" else ws) == R.ERR_TIMEOUT
+    finally:
+        R.rglru_debug_lookback(0, -1)
+    fwd()
+    bwd()
+    assert R.rglru_sync_status(saved) == R.OK
+    assert R.rglru_sync_status(ws) == R.OK
     o = oracle_inputs(inp)
     yr, _ = oracle.forward(oracle.RESTRICTED, o["x"], o["lr"], o["li"], o["Lambda"])
     assert_close("y", host(y), yr, io="bf16", kind="out")

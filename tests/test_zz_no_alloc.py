@@ -63,10 +63,12 @@ def test_noalloc_forward_matches_forward_twice():
 
 
 def test_noalloc_timeout_is_reported():
-    """A scan tile that never publishes makes its successor's bounded wait run out; the call
+    """A tile that never publishes makes its successors' bounded waits run out; the call
     finishes, and the status query of the static scratch reports the timeout.  The next call
     clears the word."""
-    wl = Workload("noalloc-timeout", 1, 128, 64, 64, "bf16", "restricted")
+    # 12 chunks of one 128-channel slice: every tile has a CTA of its own, and the dropped
+    # tile (chunk 5) lies inside its successors' look-back windows
+    wl = Workload("noalloc-timeout", 1, 12 * 64, 128, 128, "bf16", "restricted")
     inp = generate(wl, 43, want_logits=True)
     sh = shape_for(wl)
     d = {k: dev(v) for k, v in inp.items()}
