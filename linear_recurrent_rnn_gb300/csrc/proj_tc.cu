@@ -37,7 +37,7 @@ constexpr uint32_t SLAB = TR * 32;        // one 16-channel slab of a tile
 constexpr int NTHREADS = 192;             // TMA, MMA, 4 epilogue warps
 constexpr uint64_t WAIT_NS = 2000000000ull;
 constexpr size_t SMEM_MAX = 232448;       // 227 KB of dynamic shared memory per CTA
-constexpr int NBOX = 4;                   // output staging boxes per epilogue warp
+constexpr int NCMAX = PROJ_TC_KMAX / 16;   // 16-column chunks of a row, at most
 
 // Bytes of one operand tile (128 rows x k bf16).
 __host__ __device__ constexpr uint32_t tile_bytes(int k) { return (uint32_t)(k / 16) * SLAB; }
@@ -86,16 +86,17 @@ __device__ __forceinline__ void stage_row<float>(uint8_t* box, int row, const fl
         make_float4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
 }
 
-// Output staging of one epilogue warp: NBOX boxes used in turn, each freed once the TMA store
-// that last read it is done reading.
-template <typename T>
+// Output staging of one epilogue warp: NB boxes used in turn, each freed once the TMA store
+// that last read it is done reading.  The stores are small (32 rows x 16 columns), so how many
+// are in flight sets the output bandwidth: the launchers take the deepest NB that fits.
+template <typename T, int NB>
 struct Stager {
   uint8_t* base;
   uint32_t n;  // boxes used so far
   static constexpr uint32_t BOX = 32 * 16 * sizeof(T);
   __device__ uint8_t* next() {
-    uint8_t* b = base + (n % NBOX) * BOX;
-    if ((threadIdx.x & 31) == 0 && n >= NBOX) tc::tma_store_wait_read_n<NBOX - 1>();
+    uint8_t* b = base + (n % NB) * BOX;
+    if ((threadIdx.x & 31) == 0 && n >= NB) tc::tma_store_wait_read_n<NB - 1>();
     __syncwarp();
     ++n;
     return b;
@@ -131,7 +132,7 @@ struct ProjParams {
 // Per tile the x tile feeds two accumulations, lr then li, each into the next slot of a ring
 // of k-column TMEM buffers; the epilogue warps add the bias, convert and store.  SPLIT: the
 // float32 logits go out as bf16 hi and lo planes (tm_lr2 / tm_li2 map the lo planes).
-template <typename OT, bool SPLIT>
+template <typename OT, bool SPLIT, int NB>
 __global__ void __launch_bounds__(NTHREADS, 1)
     k_proj_fwd(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_wa,
                const __grid_constant__ CUtensorMap tm_wx,
@@ -150,7 +151,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   uint8_t* s_w[2] = {smem, smem + WB};
   uint8_t* s_x = smem + 2 * WB;
   uint8_t* s_stage = s_x + stages * TB;
-  float* s_bias = reinterpret_cast<float*>(s_stage + 4 * NBOX * Stager<OT>::BOX);
+  float* s_bias = reinterpret_cast<float*>(s_stage + 4 * NB * Stager<OT, NB>::BOX);
   uint64_t* bars = reinterpret_cast<uint64_t*>(s_bias + 2 * k);
   uint64_t* w_full = bars;
   uint64_t* x_full = bars + 1;
@@ -238,7 +239,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     }
   } else {
     const int q = warp & 3;  // TMEM lane quadrant = rows 32 q .. 32 q + 31 of a tile
-    Stager<OT> sg{s_stage + (warp - 2) * NBOX * Stager<OT>::BOX, 0u};
+    Stager<OT, NB> sg{s_stage + (warp - 2) * NB * Stager<OT, NB>::BOX, 0u};
     const CUtensorMap* out[2] = {&tm_lr, &tm_li};
     const CUtensorMap* out2[2] = {&tm_lr2, &tm_li2};
     for (int it = 0; it < my_tiles; ++it) {
@@ -287,7 +288,49 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 // and takes the row tiles r, r + P, ...  Per tile the 2 x nplanes gradient operand tiles pass
 // through a ring of `stages` buffers, each one K-loop into the tile's accumulator (one of two
 // TMEM buffers); the epilogue adds the addend tile and stores dx.
-template <typename OT>
+// Loads the 16 addend values of chunk c of this thread's row (zero past the rows).
+template <typename AT>
+struct AddChunk;
+template <>
+struct AddChunk<float> {
+  float4 v[4];
+  __device__ void load(const float* row, int c, bool in) {
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+      v[e] = in ? reinterpret_cast<const float4*>(row + 16 * c)[e] : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  __device__ void add_to(float (&a)[16]) const {
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      a[4 * e] += v[e].x;
+      a[4 * e + 1] += v[e].y;
+      a[4 * e + 2] += v[e].z;
+      a[4 * e + 3] += v[e].w;
+    }
+  }
+};
+template <>
+struct AddChunk<bf16> {
+  uint4 v[2];
+  __device__ void load(const bf16* row, int c, bool in) {
+#pragma unroll
+    for (int e = 0; e < 2; ++e)
+      v[e] = in ? reinterpret_cast<const uint4*>(row + 16 * c)[e] : make_uint4(0u, 0u, 0u, 0u);
+  }
+  __device__ void add_to(float (&a)[16]) const {
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const uint32_t w4[4] = {v[e].x, v[e].y, v[e].z, v[e].w};
+#pragma unroll
+      for (int h = 0; h < 4; ++h) {
+        a[8 * e + 2 * h] += __uint_as_float(w4[h] << 16);
+        a[8 * e + 2 * h + 1] += __uint_as_float(w4[h] & 0xffff0000u);
+      }
+    }
+  }
+};
+
+template <typename OT, typename AT, int NB>
 __global__ void __launch_bounds__(NTHREADS, 1)
     k_proj_dx(const __grid_constant__ CUtensorMap tm_dla, const __grid_constant__ CUtensorMap tm_dlx,
               const __grid_constant__ CUtensorMap tm_wa,
@@ -303,7 +346,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   uint8_t* s_w[2] = {smem, smem + WB};
   uint8_t* s_in = smem + 2 * WB;
   uint8_t* s_stage = s_in + stages * TB;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(s_stage + 4 * NBOX * Stager<OT>::BOX);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(s_stage + 4 * NB * Stager<OT, NB>::BOX);
   uint64_t* w_full = bars;
   uint64_t* in_full = bars + 1;
   uint64_t* in_empty = in_full + stages;
@@ -402,47 +445,31 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     }
   } else {
     const int q = warp & 3;
-    Stager<OT> sg{s_stage + (warp - 2) * NBOX * Stager<OT>::BOX, 0u};
+    Stager<OT, NB> sg{s_stage + (warp - 2) * NB * Stager<OT, NB>::BOX, 0u};
+    const int NC = k / 16;
     for (int it = 0; it < my_tiles; ++it) {
       const int slot = it & 1;
       const int rw = (rr + it * p.P) * TR + 32 * q;  // the warp's first row
       const int row = rw + lane;
+      const bool in = row < p.R;
+      const AT* arow = static_cast<const AT*>(p.add) + (size_t)row * p.W + (size_t)blk * k;
+      // the addend's whole row is requested before the accumulator is waited for (one memory
+      // round trip per tile instead of one per chunk)
+      AddChunk<AT> add[NCMAX];
+#pragma unroll
+      for (int c = 0; c < NCMAX; ++c)
+        if (c < NC) add[c].load(arow, c, in);
       if (!ctl.wait(&acc_full[slot], (it >> 1) & 1)) break;
       tc::tc_fence_after();
       const uint32_t ta = tmem + ((uint32_t)(32 * q) << 16) + slot * KC;
-      const bool in = row < p.R;
-      const size_t at = (size_t)row * p.W + (size_t)blk * k;
-      for (int c = 0; c < k / 16; ++c) {
+#pragma unroll
+      for (int c = 0; c < NCMAX; ++c) {
+        if (c >= NC) break;
         float v[16];
         tc::tmem_ld16(ta + 16 * c, v);
-        // the addend's 16 values of this row while the accumulator load is in flight
-        float a[16];
-        if (p.add_f32) {
-          const float4* src = reinterpret_cast<const float4*>(
-              static_cast<const float*>(p.add) + at + 16 * c);
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float4 t = in ? src[e] : make_float4(0.f, 0.f, 0.f, 0.f);
-            a[4 * e] = t.x, a[4 * e + 1] = t.y, a[4 * e + 2] = t.z, a[4 * e + 3] = t.w;
-          }
-        } else {
-          const uint4* src = reinterpret_cast<const uint4*>(
-              static_cast<const bf16*>(p.add) + at + 16 * c);
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const uint4 t = in ? src[e] : make_uint4(0u, 0u, 0u, 0u);
-            const uint32_t w4[4] = {t.x, t.y, t.z, t.w};
-#pragma unroll
-            for (int h = 0; h < 4; ++h) {
-              a[8 * e + 2 * h] = __uint_as_float(w4[h] << 16);
-              a[8 * e + 2 * h + 1] = __uint_as_float(w4[h] & 0xffff0000u);
-            }
-          }
-        }
         tc::tmem_ld_wait();
         tc::reg_fence(v);
-#pragma unroll
-        for (int e = 0; e < 16; ++e) v[e] += a[e];
+        add[c].add_to(v);
         uint8_t* box = sg.next();
         stage_row<OT>(box, lane, v);
         sg.store(&tm_dx, box, blk * k + 16 * c, rw);
@@ -788,14 +815,26 @@ cudaError_t launch_proj_fwd(const Dims& d, int ot, const void* x, const void* Wa
   p.bias[1] = bx;
   const size_t box = 32 * 16 * (et == DT_F32 ? 4 : 2);
   const int NS = 512 / (int)kcols(d.k);
-  const size_t fixed = 1024 + 2 * (size_t)d.k * d.k * 2 + 4 * NBOX * box + 2 * d.k * 4 +
-                       bars_bytes(1 + 2 * NS);
-  int stages = 4;
+  // the deepest output staging (16, 8 or 4 boxes a warp) with at least two x stages, then as
+  // many x stages (up to 4) as fit
+  int nb = 16, stages = 0;
+  size_t fixed = 0;
+  for (; nb >= 4; nb /= 2) {
+    fixed = 1024 + 2 * (size_t)d.k * d.k * 2 + 4 * nb * box + 2 * d.k * 4 + bars_bytes(1 + 2 * NS);
+    if (fixed + 2 * ((size_t)tile_bytes(d.k) + 16) <= SMEM_MAX || nb == 4) break;
+  }
+  stages = 4;
   while (stages > 1 && fixed + stages * (size_t)tile_bytes(d.k) + 16 * stages > SMEM_MAX) --stages;
   const size_t smem = fixed + stages * (size_t)tile_bytes(d.k) + 16 * stages;
   if (smem > SMEM_MAX) return cudaErrorNotSupported;
-  auto kern = split ? k_proj_fwd<bf16, true>
-                    : (ot == DT_F32 ? k_proj_fwd<float, false> : k_proj_fwd<bf16, false>);
+  using KF = decltype(&k_proj_fwd<bf16, false, 4>);
+  KF kern;
+  if (split)
+    kern = nb == 16 ? k_proj_fwd<bf16, true, 16> : nb == 8 ? k_proj_fwd<bf16, true, 8> : k_proj_fwd<bf16, true, 4>;
+  else if (ot == DT_F32)
+    kern = nb == 16 ? k_proj_fwd<float, false, 16> : nb == 8 ? k_proj_fwd<float, false, 8> : k_proj_fwd<float, false, 4>;
+  else
+    kern = nb == 16 ? k_proj_fwd<bf16, false, 16> : nb == 8 ? k_proj_fwd<bf16, false, 8> : k_proj_fwd<bf16, false, 4>;
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   kern<<<p.P * d.nblk, NTHREADS, smem, s>>>(mx, mwa, mwx, mlr, mli, mlr2, mli2, p, stages);
@@ -823,12 +862,25 @@ cudaError_t launch_proj_dx(const Dims& d, int ot, const void* dlr, const void* d
   p.add_f32 = add_f32;
   p.nplanes = nplanes;
   const size_t box = 32 * 16 * (ot == DT_F32 ? 4 : 2);
-  const size_t fixed = 1024 + 2 * (size_t)d.k * d.k * 2 + 4 * NBOX * box + bars_bytes(5);
+  int nb = 16;
+  size_t fixed = 0;
+  for (; nb >= 4; nb /= 2) {
+    fixed = 1024 + 2 * (size_t)d.k * d.k * 2 + 4 * nb * box + bars_bytes(5);
+    if (fixed + 2 * ((size_t)tile_bytes(d.k) + 16) <= SMEM_MAX || nb == 4) break;
+  }
   int stages = 4;
   while (stages > 2 && fixed + stages * (size_t)tile_bytes(d.k) + 16 * stages > SMEM_MAX) --stages;
   const size_t smem = fixed + stages * (size_t)tile_bytes(d.k) + 16 * stages;
   if (smem > SMEM_MAX) return cudaErrorNotSupported;
-  auto kern = ot == DT_F32 ? k_proj_dx<float> : k_proj_dx<bf16>;
+  using KD = decltype(&k_proj_dx<bf16, bf16, 4>);
+  KD kern;
+#define RGLRU_DX_KERN(O, A) \
+  (nb == 16 ? k_proj_dx<O, A, 16> : nb == 8 ? k_proj_dx<O, A, 8> : k_proj_dx<O, A, 4>)
+  if (ot == DT_F32)
+    kern = add_f32 ? RGLRU_DX_KERN(float, float) : RGLRU_DX_KERN(float, bf16);
+  else
+    kern = add_f32 ? RGLRU_DX_KERN(bf16, float) : RGLRU_DX_KERN(bf16, bf16);
+#undef RGLRU_DX_KERN
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   kern<<<p.P * d.nblk, NTHREADS, smem, s>>>(mdla, mdlx, mwa, mwx, mdx, p, stages);
