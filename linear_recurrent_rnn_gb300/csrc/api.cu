@@ -433,14 +433,25 @@ rglru_status rglru_fused_forward_varlen(const rglru_shape* shape, const void* x,
   if (!req(x) || !req(Wa) || !req(Wx) || !opt(ba) || !opt(bx) || !req(Lambda) || !opt(h0) ||
       !req(y) || !opt(hT))
     return RGLRU_ERR_INVALID_ARG;
-  if (!fused_supported(d)) return RGLRU_ERR_UNSUPPORTED;
+  if (!fused_supported(d) && !composed_tc(d)) return RGLRU_ERR_UNSUPPORTED;
   v.h0 = h0;
   v.hT = hT;
   cudaError_t e = launch_seq_index(v, d.T, d.W, const_cast<int32_t*>(v.seq_start),
                                    const_cast<int32_t*>(v.seq_end), stream);
+  if (fused_supported(d)) {
+    if (e == cudaSuccess)
+      e = launch_fused_fwd(d, x, Wa, ba, Wx, bx, Lambda, nullptr, nullptr, nullptr, y, nullptr,
+                           saved, g_spin_limit, g_drop_tile, stream, &v);
+    return cuda_status(e);
+  }
+  // other gate blocks: tensor-core projections to hi + lo logit planes, then the packed scan
+  uint8_t* sv = static_cast<uint8_t*>(saved);
+  const ComposedLayout C = composed_saved(d);
   if (e == cudaSuccess)
-    e = launch_fused_fwd(d, x, Wa, ba, Wx, bx, Lambda, nullptr, nullptr, nullptr, y, nullptr,
-                         saved, g_spin_limit, g_drop_tile, stream, &v);
+    e = launch_proj_fwd(d, DT_SPLIT, x, Wa, ba, Wx, bx, sv + C.lr, sv + C.li, stream);
+  if (e == cudaSuccess)
+    e = launch_logits_fwd(d, x, sv + C.lr, sv + C.li, d.N, 2, Lambda, nullptr, nullptr, nullptr,
+                          y, nullptr, saved, g_spin_limit, g_drop_tile, stream, &v);
   return cuda_status(e);
 }
 
@@ -460,17 +471,38 @@ rglru_status rglru_fused_backward_varlen(const rglru_shape* shape, const void* d
       !req(Lambda) || !opt(h0) || !req(dx) || !req(dWa) || !req(dWx) || !opt(dba) ||
       !opt(dbx) || !req(dLambda) || !opt(dh0) || !req(workspace))
     return RGLRU_ERR_INVALID_ARG;
-  if (!fused_supported(d)) return RGLRU_ERR_UNSUPPORTED;
+  if (!fused_supported(d) && !composed_tc(d)) return RGLRU_ERR_UNSUPPORTED;
   v.h0 = h0;
   v.dhT = dhT;
   v.dh0 = dh0;
   // the token indices were written by the forward into `saved`; empty sequences' dh0 here
   cudaError_t e = cudaSuccess;
   if (dh0) e = launch_seq_empty_dh0(v, d.W, stream);
+  if (fused_supported(d)) {
+    if (e == cudaSuccess)
+      e = launch_fused_bwd(d, dy, nullptr, x, Wa, ba, Wx, bx, Lambda, nullptr, nullptr, nullptr,
+                           saved, dx, dWa, dba, dWx, dbx, dLambda, nullptr, workspace,
+                           g_spin_limit, g_drop_tile, stream, &v);
+    return cuda_status(e);
+  }
+  // other gate blocks: the packed scan backward on the saved logit planes (float32 direct dx
+  // term, dl as hi + lo planes), then the tensor-core projection backward
+  const uint8_t* sv = static_cast<const uint8_t*>(saved);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  const ComposedLayout C = composed_saved(d);
+  const ComposedWs CW = composed_ws(d);
   if (e == cudaSuccess)
-    e = launch_fused_bwd(d, dy, nullptr, x, Wa, ba, Wx, bx, Lambda, nullptr, nullptr, nullptr,
-                         saved, dx, dWa, dba, dWx, dbx, dLambda, nullptr, workspace,
-                         g_spin_limit, g_drop_tile, stream, &v);
+    e = launch_logits_bwd(d, dy, nullptr, x, sv + C.lr, sv + C.li, d.N, 2, Lambda, nullptr,
+                          nullptr, saved, DT_F32, ws + CW.dxd, DT_SPLIT, ws + CW.dlr,
+                          ws + CW.dli, d.N, dLambda, nullptr, workspace, g_spin_limit,
+                          g_drop_tile, stream, &v);
+  if (e == cudaSuccess)
+    e = launch_proj_dx(d, d.grad, ws + CW.dlr, ws + CW.dli, d.N, 2, Wa, Wx, ws + CW.dxd, 1, dx,
+                       stream);
+  if (e == cudaSuccess)
+    e = launch_proj_dw(d, x, ws + CW.dlr, ws + CW.dli, d.N, 2,
+                       reinterpret_cast<float*>(ws + CW.gate + PROJ_PART_OFFSET), dWa, dba, dWx,
+                       dbx, stream);
   return cuda_status(e);
 }
 

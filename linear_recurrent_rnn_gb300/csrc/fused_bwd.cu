@@ -177,6 +177,7 @@ struct SeqB {
   uint32_t smask, emask;
   int t0;  // row index of the part's first token (packed sequences: one row)
   int w;   // channel
+  bool ok = true;  // the channel is stored (false: a lane past W of a partial slice)
 };
 __device__ __forceinline__ float seqb_h0(const SeqB& sq, int u) {
   return sq.p.h0s ? sq.p.h0s[(size_t)sq.p.seq_start[sq.t0 + u] * sq.p.W + sq.w] : 0.0f;
@@ -419,8 +420,8 @@ __device__ __forceinline__ void bwd_pass2b(uint32_t tcol, int tb, int j,
       if (VARLEN && GENERAL && sq.p.dh0s) {  // d h0[s] = a g at the sequence's first token
         float* dh0 = sq.p.dh0s + sq.w;
         const int32_t* st = sq.p.seq_start + sq.t0;
-        if ((sq.smask >> u) & 1u) dh0[(size_t)st[u] * sq.p.W] = abar.x * gv.x;
-        if ((sq.smask >> (u + 1)) & 1u) dh0[(size_t)st[u + 1] * sq.p.W] = abar.y * gv.y;
+        if (((sq.smask >> u) & 1u) && sq.ok) dh0[(size_t)st[u] * sq.p.W] = abar.x * gv.x;
+        if (((sq.smask >> (u + 1)) & 1u) && sq.ok) dh0[(size_t)st[u + 1] * sq.p.W] = abar.y * gv.y;
       }
       // d h_t / d la = abar (h_{t-1} - abar x i / m) with i / m = i^2 / (m i); zero at reset
       // tokens (abar = 0), past T and where the decay is exactly 1 (m = 0)
@@ -718,7 +719,7 @@ __global__ void __maxnreg__(MAXREG)
     // The packed-sequence view of tile (b, c) for the general passes, built where it is used
     // so that its pointers are not live across the tile.
     auto seqb = [&](uint32_t sm, uint32_t em, int b_, int c_) {
-      return SeqB{p, sm, em, b_ * p.T + c_ * FUSED_C + tb, w};
+      return SeqB{p, sm, em, b_ * p.T + c_ * FUSED_C + tb, w, wok};
     };
     for (int it = 0; it <= my_tiles; ++it) {
       const bool have = it < my_tiles;
@@ -1132,7 +1133,7 @@ cudaError_t launch_logits_bwd(const Dims& d, const void* dy, const float* dhT, c
                               const float* Lambda, const uint8_t* rm, const int32_t* sp,
                               const void* saved, int dx_dt, void* dx, int dl_dt, void* dlr,
                               void* dli, size_t dl_plane, float* dLambda, float* dh0, void* ws,
-                              int spin_limit, int drop_tile, cudaStream_t s) {
+                              int spin_limit, int drop_tile, cudaStream_t s, const Varlen* vl) {
   if (!logits_scan_supported(d) || nplanes < 1 || nplanes > LG_PLANES)
     return cudaErrorNotSupported;
   const uint64_t W = d.W, T = d.T, B = d.B;
@@ -1175,6 +1176,13 @@ cudaError_t launch_logits_bwd(const Dims& d, const void* dy, const float* dhT, c
   p.dhT = dhT;
   const FusedFwdLayout FL = fused_fwd_layout(d);
   p.fwd_carry = reinterpret_cast<const float*>(static_cast<const uint8_t*>(saved) + FL.L.carry);
+  if (vl) {
+    p.seq_start = reinterpret_cast<const int32_t*>(static_cast<const uint8_t*>(saved) + FL.seq_start);
+    p.seq_end = reinterpret_cast<const int32_t*>(static_cast<const uint8_t*>(saved) + FL.seq_end);
+    p.h0s = vl->h0;
+    p.dhTs = vl->dhT;
+    p.dh0s = vl->dh0;
+  }
   p.dh0 = dh0;
   p.scratch = static_cast<uint8_t*>(ws);
   p.F = fused_bwd_layout(d);
@@ -1188,8 +1196,9 @@ cudaError_t launch_logits_bwd(const Dims& d, const void* dy, const float* dhT, c
   decltype(&k_fused_bwd<float, false, LGM_SAME>) kern;
   if (dl_dt == DT_SPLIT) {
     if (!gf32) return cudaErrorNotSupported;
-    kern = k_fused_bwd<float, false, LGM_SPLIT>;
+    kern = vl ? k_fused_bwd<float, true, LGM_SPLIT> : k_fused_bwd<float, false, LGM_SPLIT>;
   } else {
+    if (vl) return cudaErrorNotSupported;
     if ((dl_dt == DT_F32) != gf32) return cudaErrorNotSupported;
     kern = gf32 ? k_fused_bwd<float, false, LGM_SAME> : k_fused_bwd<bf16, false, LGM_SAME>;
   }

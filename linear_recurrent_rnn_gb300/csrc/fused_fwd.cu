@@ -545,7 +545,7 @@ __global__ void __maxnreg__(MAXREG)
               const float Ac = tc::tmem_ld1(park + 64 + u);
               tc::tmem_ld_wait();
               const int sidx = __shfl_sync(0xffffffffu, pp == 0 ? e0 : e1, u);
-              if (p.hTs) p.hTs[(size_t)sidx * p.W + w] = fmaf(Ac, hin, hl);
+              if (p.hTs && wok) p.hTs[(size_t)sidx * p.W + w] = fmaf(Ac, hin, hl);
             }
           }
         }
@@ -733,7 +733,7 @@ cudaError_t launch_logits_fwd(const Dims& d, const void* x, const void* lr, cons
                               size_t plane_elems, int nplanes, const float* Lambda,
                               const uint8_t* rm, const int32_t* sp, const float* h0, void* y,
                               float* hT, void* saved, int spin_limit, int drop_tile,
-                              cudaStream_t s) {
+                              cudaStream_t s, const Varlen* vl) {
   if (!logits_scan_supported(d) || nplanes < 1 || nplanes > LG_PLANES)
     return cudaErrorNotSupported;
   const uint64_t W = d.W, T = d.T, B = d.B;
@@ -766,6 +766,13 @@ cudaError_t launch_logits_fwd(const Dims& d, const void* x, const void* lr, cons
   p.segment_pos = p.canonical ? sp : nullptr;
   p.h0 = h0;
   p.hT = hT;
+  if (vl) {
+    const FusedFwdLayout FL = fused_fwd_layout(d);
+    p.seq_start = reinterpret_cast<const int32_t*>(static_cast<uint8_t*>(saved) + FL.seq_start);
+    p.seq_end = reinterpret_cast<const int32_t*>(static_cast<uint8_t*>(saved) + FL.seq_end);
+    p.h0s = vl->h0;
+    p.hTs = vl->hT;
+  }
   p.scratch = static_cast<uint8_t*>(saved);
   p.L = fused_layout(d, false);
   p.spin_limit = spin_limit;
@@ -773,7 +780,7 @@ cudaError_t launch_logits_fwd(const Dims& d, const void* x, const void* lr, cons
   const LookbackPlan lp = lookback_plan(p.P, d.B);
   p.lb_dist = lp.dist;
   p.lb_shift = lp.shift;
-  auto kern = k_fused_fwd<false, true>;
+  auto kern = vl ? k_fused_fwd<true, true> : k_fused_fwd<false, true>;
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)LG_SMEM_BYTES);
   if (e != cudaSuccess) return e;

@@ -283,14 +283,15 @@ cudaError_t launch_logits_bwd(const Dims& d, const void* dy, const float* dhT, c
                               const float* Lambda, const uint8_t* rm, const int32_t* sp,
                               const void* saved, int dx_dt, void* dx, int dl_dt, void* dlr,
                               void* dli, size_t dl_plane, float* dLambda, float* dh0, void* ws,
-                              int spin_limit, int drop_tile, cudaStream_t s);
+                              int spin_limit, int drop_tile, cudaStream_t s,
+                              const Varlen* vl = nullptr);
 cudaError_t encode_logit_planes(const Dims& d, const void* base, size_t plane_elems, int nplanes,
                                 CUtensorMap* m);
 cudaError_t launch_logits_fwd(const Dims& d, const void* x, const void* lr, const void* li,
                               size_t plane_elems, int nplanes, const float* Lambda,
                               const uint8_t* rm, const int32_t* sp, const float* h0, void* y,
                               float* hT, void* saved, int spin_limit, int drop_tile,
-                              cudaStream_t s);
+                              cudaStream_t s, const Varlen* vl = nullptr);
 // Clears the status word of a scan layout and marks every carry / aggregate slot empty.
 cudaError_t clear_slots(void* buf, const ScanLayout& L, cudaStream_t s);
 

@@ -17,17 +17,21 @@ from helpers import assert_close, dev, host
 pytestmark = pytest.mark.gpu
 
 CASES = [
-    ([0, 1, 0, 70, 64, 33, 0, 130, 5, 1], (0.9, 0.999), 41, "bf16"),
-    ([200, 3, 97], (0.05, 0.95), 42, "bf16"),   # short memories: the general decay branch too
-    ([31, 1, 64, 129, 0, 2], (0.5, 0.999), 43, "f32"),   # float32 dx
+    ([0, 1, 0, 70, 64, 33, 0, 130, 5, 1], (0.9, 0.999), 41, "bf16", 256, 128),
+    ([200, 3, 97], (0.05, 0.95), 42, "bf16", 256, 128),   # short memories: general decay too
+    ([31, 1, 64, 129, 0, 2], (0.5, 0.999), 43, "f32", 256, 128),   # float32 dx
+    # gate blocks of 160 (tensor-core projections around the packed scan; the last 128-channel
+    # slice of W = 320 is partial) and of 48
+    ([0, 1, 0, 70, 64, 33, 0, 130, 5, 1], (0.9, 0.999), 44, "bf16", 320, 160),
+    ([95, 0, 3, 200], (0.5, 0.999), 45, "f32", 192, 48),
 ]
 
 
-@pytest.mark.parametrize("lengths,u_range,seed,grad", CASES, ids=["mixed", "far", "f32grad"])
-def test_varlen_matches_per_sequence_oracle(lengths, u_range, seed, grad):
+@pytest.mark.parametrize("lengths,u_range,seed,grad,W,k", CASES,
+                         ids=["mixed", "far", "f32grad", "k160", "k48-f32grad"])
+def test_varlen_matches_per_sequence_oracle(lengths, u_range, seed, grad, W, k):
     T = int(sum(lengths))
     S = len(lengths)
-    W, k = 256, 128
     wl = Workload("varlen", 1, T, W, k, "bf16", "canonical", u_range, h0_std=1.0)
     inp = generate(wl, seed)
     rng = np.random.default_rng(seed)
