@@ -14,8 +14,20 @@
 // a time, lane = channel: the four rows' x segments go to shared memory and every lane runs
 // its two dot products over the block's k inputs with the weights shared by the four rows.
 // The gate arithmetic is the CUDA-core forward's (accurate exp / expm1 / log1p forms).
+//
+// Large batches (bf16, B >= STEP_TC_MIN_B, k a multiple of 32) take k_step_tc instead: the step
+// is then a [B x k] x [k x k] product per gate block and matrix, which goes to the tcgen05
+// tensor cores.  CTA = (128-row tile, gate block, 32-channel slice): TMA brings the x tile
+// (16-channel slabs, 32-byte swizzle) and the two 32-column weight slices, one thread issues
+// the k / 16 MMAs of M = 128 rows x N = 32 channels per matrix into TMEM, and each of the four
+// warps then takes its 32 rows (its TMEM lane quadrant): lr, li from TMEM, x from the staged
+// tile, the state row requested before the MMA wait, and the same gate arithmetic as k_step.
+#include <cudaTypedefs.h>
+
 #include "common.cuh"
+#include "host_util.h"
 #include "internal.h"
+#include "tc.cuh"
 
 namespace rglru {
 
@@ -205,7 +217,168 @@ __global__ void __launch_bounds__(DEC_WARPS * 32) k_step(DecArgs a) {
   }
 }
 
+// ---------------------------------------------------------------- tensor-core step
+constexpr int STC_ROWS = 128;
+constexpr int STC_N = 32;  // channels per CTA
+constexpr uint32_t STC_SLAB = STC_ROWS * 32;  // 16 channels x 128 rows of x
+
+__global__ void __launch_bounds__(128, 1)
+    k_step_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_wa,
+              const __grid_constant__ CUtensorMap tm_wx, const __grid_constant__ DecArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024u - (tc::smem_u32(smem_raw) & 1023u)) & 1023u);
+  const int k = a.k;
+  const int nsl = k / STC_N;
+  const int blk = blockIdx.x / nsl, j0 = (blockIdx.x % nsl) * STC_N;
+  const int row0 = blockIdx.y * STC_ROWS;
+  const uint32_t XB = (uint32_t)(k / 16) * STC_SLAB;   // x tile
+  const uint32_t WS = (uint32_t)k * 32;                // one 16-column weight slab
+  uint8_t* s_x = smem;
+  uint8_t* s_w[2] = {smem + XB, smem + XB + 2 * WS};
+  float* s_c = reinterpret_cast<float*>(smem + XB + 4 * WS);  // per channel: nk, ba, bx
+  uint64_t* bars = reinterpret_cast<uint64_t*>(s_c + 3 * STC_N);
+  uint64_t* full = bars;
+  uint64_t* done = bars + 1;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 2);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    tc::mbar_init(full, 1);
+    tc::mbar_init(done, 1);
+    tc::fence_barrier_init();
+  }
+  if (warp == 0) {
+    tc::tmem_alloc(tmem_holder, 2 * STC_N);
+    tc::tmem_relinquish();
+  }
+  if (threadIdx.x < STC_N) {
+    const int w = blk * k + j0 + threadIdx.x;
+    s_c[threadIdx.x] = -8.0f * softplus_f(a.Lambda[w]);
+    s_c[STC_N + threadIdx.x] = a.ba ? a.ba[w] : 0.0f;
+    s_c[2 * STC_N + threadIdx.x] = a.bx ? a.bx[w] : 0.0f;
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+  if (threadIdx.x == 0) {
+    tc::mbar_expect_tx(full, XB + 4 * WS);
+    for (int s = 0; s < k / 16; ++s)
+      tc::tma_load_2d(s_x + s * STC_SLAB, &tm_x, full, blk * k + 16 * s, row0);
+    for (int m = 0; m < 2; ++m)
+      for (int s = 0; s < 2; ++s)
+        tc::tma_load_2d(s_w[m] + s * WS, m ? &tm_wx : &tm_wa, full, j0 + 16 * s, blk * k);
+  }
+  // this thread's row: its state segment and reset flag, requested before any wait
+  const int q = warp & 3;
+  const int row = row0 + 32 * q + lane;
+  const bool live = row < a.B;
+  const size_t o = (size_t)row * a.W + (size_t)blk * k + j0;
+  float4 hp[STC_N / 4];
+#pragma unroll
+  for (int e = 0; e < STC_N / 4; ++e)
+    hp[e] = (live && a.h_in) ? reinterpret_cast<const float4*>(a.h_in + o)[e]
+                             : make_float4(0.f, 0.f, 0.f, 0.f);
+  const bool rst = live && a.canonical && a.reset && a.reset[row] != 0;
+  if (warp == 0) {
+    const bool leader = tc::elect_one();
+    const bool ok = tc::mbar_wait(full, 0, 2000000000ull);
+    tc::tc_fence_after();
+    if (leader && ok) {
+      const uint32_t idesc = tc::idesc_bf16(STC_ROWS, STC_N, 0, 1);  // x K-major, W MN-major
+      const uint32_t xs = tc::smem_u32(s_x);
+      for (int m = 0; m < 2; ++m) {
+        const uint32_t ws = tc::smem_u32(s_w[m]);
+        for (int kk = 0; kk < k / 16; ++kk)
+          tc::mma_bf16(tmem + m * STC_N, tc::smem_desc_sw32(xs + kk * STC_SLAB, 16, 256),
+                       tc::smem_desc_sw32(ws + kk * 512, WS, 256), idesc, kk > 0);
+      }
+    }
+    if (leader) tc::mma_commit(done);  // arrives once the MMAs (if any) are done
+    __syncwarp();
+  }
+  const bool ok = tc::mbar_wait(done, 0, 2000000000ull);
+  tc::tc_fence_after();
+  float lr[STC_N], li[STC_N];
+  {
+    float t[16];
+    const uint32_t ta = tmem + ((uint32_t)(32 * q) << 16);
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      tc::tmem_ld16(ta + 16 * h, t);
+      tc::tmem_ld_wait();
+#pragma unroll
+      for (int e = 0; e < 16; ++e) lr[16 * h + e] = t[e];
+      tc::tmem_ld16(ta + STC_N + 16 * h, t);
+      tc::tmem_ld_wait();
+#pragma unroll
+      for (int e = 0; e < 16; ++e) li[16 * h + e] = t[e];
+    }
+  }
+  if (live && ok) {
+    // x of the row's 32 channels from the staged tile: two slabs, 32-byte rows whose 16-byte
+    // halves are swapped on rows 4..7 of every 8
+    const int r = 32 * q + lane;
+    float xv[STC_N];
+#pragma unroll
+    for (int s = 0; s < 2; ++s) {
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        const uint4 u = *reinterpret_cast<const uint4*>(
+            s_x + (j0 / 16 + s) * STC_SLAB + r * 32 + ((hh ^ ((r >> 2) & 1)) << 4));
+        const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          xv[16 * s + 8 * hh + 2 * e] = __uint_as_float(w4[e] << 16);
+          xv[16 * s + 8 * hh + 2 * e + 1] = __uint_as_float(w4[e] & 0xffff0000u);
+        }
+      }
+    }
+    const float* hpf = reinterpret_cast<const float*>(hp);
+    float hn[STC_N];
+#pragma unroll
+    for (int c = 0; c < STC_N; ++c) {
+      const float rg = sigmoid_f(lr[c] + s_c[STC_N + c]);
+      const float ig = sigmoid_f(li[c] + s_c[2 * STC_N + c]);
+      const float la = s_c[c] * rg;
+      float abar = expf(la);
+      float m = sqrtf(one_minus_a2(la));
+      if (rst) {
+        abar = 0.0f;
+        m = 1.0f;
+      }
+      hn[c] = fmaf(abar, hpf[c], m * (ig * xv[c]));
+    }
+#pragma unroll
+    for (int e = 0; e < STC_N / 4; ++e)
+      reinterpret_cast<float4*>(a.h_out + o)[e] =
+          make_float4(hn[4 * e], hn[4 * e + 1], hn[4 * e + 2], hn[4 * e + 3]);
+#pragma unroll
+    for (int e = 0; e < STC_N / 8; ++e) {
+      uint4 u;
+      uint32_t* pu = &u.x;
+#pragma unroll
+      for (int h = 0; h < 4; ++h) {
+        const __nv_bfloat162 v = __floats2bfloat162_rn(hn[8 * e + 2 * h], hn[8 * e + 2 * h + 1]);
+        pu[h] = *reinterpret_cast<const uint32_t*>(&v);
+      }
+      reinterpret_cast<uint4*>(static_cast<bf16*>(a.y) + o)[e] = u;
+    }
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc::tc_fence_after();
+    tc::tmem_dealloc(tmem, 2 * STC_N);
+  }
+}
+
 }  // namespace
+
+bool step_tc_supported(const Dims& d) {
+  return d.io == RGLRU_BF16 && d.B >= STEP_TC_MIN_B && d.k % STC_N == 0 && d.k <= 256 &&
+         sm_count() > 0;
+}
 
 size_t step_smem_bytes(int k) { return (size_t)(2 * 32 + DEC_WARPS * DEC_RW) * k * 4; }
 
@@ -228,6 +401,34 @@ cudaError_t launch_step(const Dims& d, const void* x, const void* Wa, const floa
   a.h_in = h_in;
   a.y = y;
   a.h_out = h_out;
+  if (step_tc_supported(d)) {
+    // x [B][W] in 16-channel x 128-row boxes; W[nblk][k][k] as [nblk k rows][k columns] in
+    // 16-column x k-row boxes (the 32-channel slice: two of them)
+    CUtensorMap mx, mwa, mwx;
+    const uint64_t dx[2] = {(uint64_t)d.W, (uint64_t)d.B};
+    const uint64_t sx[1] = {(uint64_t)d.W * 2};
+    const uint32_t bx_[2] = {16, STC_ROWS};
+    cudaError_t e = encode_tmap(&mx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, x, dx, sx, bx_,
+                                CU_TENSOR_MAP_SWIZZLE_32B);
+    const uint64_t dw[2] = {(uint64_t)d.k, (uint64_t)d.nblk * d.k};
+    const uint64_t sw[1] = {(uint64_t)d.k * 2};
+    const uint32_t bw[2] = {16, (uint32_t)d.k};
+    if (e == cudaSuccess)
+      e = encode_tmap(&mwa, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, Wa, dw, sw, bw,
+                      CU_TENSOR_MAP_SWIZZLE_32B);
+    if (e == cudaSuccess)
+      e = encode_tmap(&mwx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, Wx, dw, sw, bw,
+                      CU_TENSOR_MAP_SWIZZLE_32B);
+    if (e != cudaSuccess) return e;
+    const size_t smem = 1024 + (size_t)(d.k / 16) * STC_SLAB + 4 * (size_t)d.k * 32 +
+                        3 * STC_N * 4 + 64;
+    e = cudaFuncSetAttribute(k_step_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    const dim3 grid((unsigned)(d.nblk * (d.k / STC_N)), (unsigned)((d.B + STC_ROWS - 1) / STC_ROWS));
+    k_step_tc<<<grid, 128, smem, s>>>(mx, mwa, mwx, a);
+    note_launches(1);
+    return cudaGetLastError();
+  }
   const size_t smem = step_smem_bytes(d.k);
   const dim3 grid((unsigned)(d.nblk * ((d.k + 31) / 32)), (unsigned)((d.B + DEC_ROWS - 1) / DEC_ROWS));
   cudaError_t e;

@@ -309,6 +309,9 @@ cudaError_t launch_fused_bwd(const Dims& d, const void* dy, const float* dhT, co
 // One decode step (T = 1) with carried states: projections, gates and the state update in one
 // kernel (decode.cu); k <= STEP_KMAX.
 constexpr int STEP_KMAX = 512;
+// Batches from this size (bf16, k a multiple of 32 up to 256) take the tensor-core step.
+constexpr int STEP_TC_MIN_B = 64;
+bool step_tc_supported(const Dims& d);
 cudaError_t launch_step(const Dims& d, const void* x, const void* Wa, const float* ba,
                         const void* Wx, const float* bx, const float* Lambda,
                         const uint8_t* reset, const float* h_in, void* y, float* h_out,

@@ -21,6 +21,11 @@ STEP_CASES = [
     (Workload("step-f32-canonical", 70, 1, 128, 64, "f32", "canonical", reset_p=0.2,
               h0_std=0.5), 5),
     (Workload("step-bf16-k160", 1, 1, 320, 160, "bf16", "canonical", h0_std=1.0), 6),
+    # batches of 64 and more take the tensor-core step (128-row tiles: one ragged, two)
+    (Workload("step-tc-bf16-canonical", 200, 1, 256, 128, "bf16", "canonical", reset_p=0.3,
+              h0_std=1.0), 7),
+    (Workload("step-tc-bf16-k160", 70, 1, 320, 160, "bf16", "restricted"), 8),
+    (Workload("step-tc-bf16-k64", 128, 1, 192, 64, "bf16", "canonical", h0_std=0.5), 9),
 ]
 
 
@@ -48,9 +53,11 @@ def test_step_matches_forward_of_one_token(wl, seed):
     assert_close("h_out", host(h_out), hr, io=wl.io, kind="out")
 
 
-def test_decode_loop_reproduces_forward():
-    """T steps with the state updated in place equal the forward over T tokens."""
-    wl = Workload("decode-loop", 3, 40, 256, 128, "bf16", "canonical", reset_p=0.05, h0_std=1.0)
+@pytest.mark.parametrize("B", [3, 96])
+def test_decode_loop_reproduces_forward(B):
+    """T steps with the state updated in place equal the forward over T tokens (B = 96: the
+    tensor-core step)."""
+    wl = Workload("decode-loop", B, 40, 256, 128, "bf16", "canonical", reset_p=0.05, h0_std=1.0)
     inp = generate(wl, 11)
     d = {k: dev(v) if isinstance(v, torch.Tensor) else v for k, v in inp.items()}
     sh = R.make_shape(wl.B, 1, wl.W, wl.nblk, R.BF16, R.BF16, R.CANONICAL)
