@@ -111,3 +111,61 @@ def test_full_size_headline_float32_gradients():
         assert_close(tag + "dWx", host(got["dWx"][blk:blk + 1]), g["dWx"], io=wl.io, kind="grad")
         for name in ("dba", "dbx", "dLambda"):
             assert_close(tag + name, host(got[name][cs]), g[name], io=wl.io, kind="grad")
+
+
+def test_full_size_unfused_calls_sampled_blocks():
+    """The unfused calls at the headline size (B4 T2048 W2048 bf16, restricted), as the bench
+    times them: rglru_gate_proj (tcgen05), rglru_forward and rglru_backward (the scan kernels
+    with the logits given), rglru_gate_proj_backward (tcgen05).  The oracle runs on the
+    channels of three sampled gate blocks over the whole batch and sequence: exact per block,
+    since every output of a block depends on that block's channels only."""
+    wl = WORKLOADS[2]
+    inp = generate(wl, 2, want_dlogits=True)
+    sh = shape_for(wl)
+    d = {k: dev(v) for k, v in inp.items()}
+    x = d["x"]
+    lr, li, y, dx, dlr, dli = (torch.empty_like(x) for _ in range(6))
+    hT = torch.empty(wl.B, wl.W, device="cuda")
+    dL = torch.empty(wl.W, device="cuda")
+    saved, ws = R.alloc_saved(sh), R.alloc_workspace(sh)
+    R.rglru_gate_proj(sh, x, d["Wa"], d["ba"], d["Wx"], d["bx"], lr, li)
+    R.rglru_forward(sh, x, lr, li, d["Lambda"], None, None, None, y, hT, saved)
+    R.rglru_backward(sh, d["dy"], None, x, lr, li, d["Lambda"], None, None, None, saved, dx, dlr,
+                     dli, dL, None, ws)
+    assert R.rglru_sync_status(saved) == R.OK
+    assert R.rglru_sync_status(ws) == R.OK
+    # the projection backward on the upstream logit gradients of the generator
+    dxp = dx.clone()
+    dWa = torch.empty(wl.nblk, wl.k, wl.k, device="cuda")
+    dWx = torch.empty_like(dWa)
+    dba, dbx = (torch.empty(wl.W, device="cuda") for _ in range(2))
+    R.rglru_gate_proj_backward(sh, d["dlr"], d["dli"], x, d["Wa"], d["Wx"], dxp, dWa, dba, dWx,
+                               dbx, ws)
+    torch.cuda.synchronize()
+    for blk in (0, 9, wl.nblk - 1):
+        k = wl.k
+        cs = slice(blk * k, (blk + 1) * k)
+        xo = as_f64(inp["x"][..., cs])
+        Wa = as_f64(inp["Wa"][blk:blk + 1])
+        Wx = as_f64(inp["Wx"][blk:blk + 1])
+        rl, ri = oracle.gate_proj(xo, Wa, as_f64(inp["ba"][cs]), Wx, as_f64(inp["bx"][cs]))
+        tag = f"blk{blk} "
+        assert_close(tag + "lr", host(lr[..., cs]), rl, io="bf16", kind="out")
+        assert_close(tag + "li", host(li[..., cs]), ri, io="bf16", kind="out")
+        # the scan on the logits as stored (bf16)
+        lro, lio = host(lr[..., cs]), host(li[..., cs])
+        yr, hr = oracle.forward(oracle.RESTRICTED, xo, lro, lio, as_f64(inp["Lambda"][cs]))
+        g = oracle.backward(oracle.RESTRICTED, xo, lro, lio, as_f64(inp["Lambda"][cs]),
+                            as_f64(inp["dy"][..., cs]))
+        assert_close(tag + "y", host(y[..., cs]), yr, io="bf16", kind="out")
+        assert_close(tag + "hT", host(hT[:, cs]), hr, io="bf16", kind="out")
+        for n, got in (("dx", dx), ("dlr", dlr), ("dli", dli)):
+            assert_close(tag + n, host(got[..., cs]), g[n], io="bf16", kind="grad", stored="bf16")
+        assert_close(tag + "dLambda", host(dL[cs]), g["dLambda"], io="bf16", kind="grad")
+        p = oracle.gate_proj_backward(xo, Wa, Wx, as_f64(inp["dlr"][..., cs]),
+                                      as_f64(inp["dli"][..., cs]), dx_in=host(dx[..., cs]))
+        assert_close(tag + "dx+proj", host(dxp[..., cs]), p["dx"], io="bf16", kind="grad",
+                     stored="bf16")
+        for n, got in (("dWa", dWa[blk:blk + 1]), ("dWx", dWx[blk:blk + 1]), ("dba", dba[cs]),
+                       ("dbx", dbx[cs])):
+            assert_close(tag + n, host(got), p[n], io="bf16", kind="grad")
