@@ -58,14 +58,12 @@ struct Abort {
   }
 };
 
-// A row of 16 float32 values written into a staging box of 32 rows x 16 columns of T, laid
-// out as the TMA store with the matching swizzle expects (bf16: 32-byte rows, 32-byte swizzle;
-// float32: 64-byte rows, 64-byte swizzle).  Conflict-free: the eight lanes of a quarter warp
-// land in eight different 16-byte bank groups.
+// 16 float32 values of one row stored straight to global memory as T (two or four 16-byte
+// stores; a warp's 32 rows each take whole 32-byte sectors).
 template <typename T>
-__device__ __forceinline__ void stage_row(uint8_t* box, int row, const float (&v)[16]);
+__device__ __forceinline__ void store_row16(T* dst, const float (&v)[16]);
 template <>
-__device__ __forceinline__ void stage_row<bf16>(uint8_t* box, int row, const float (&v)[16]) {
+__device__ __forceinline__ void store_row16<bf16>(bf16* dst, const float (&v)[16]) {
 #pragma unroll
   for (int c = 0; c < 2; ++c) {
     uint4 q;
@@ -75,49 +73,19 @@ __device__ __forceinline__ void stage_row<bf16>(uint8_t* box, int row, const flo
       const __nv_bfloat162 h = __floats2bfloat162_rn(v[8 * c + 2 * u], v[8 * c + 2 * u + 1]);
       w[u] = *reinterpret_cast<const uint32_t*>(&h);
     }
-    *reinterpret_cast<uint4*>(box + row * 32 + ((c ^ ((row >> 2) & 1)) << 4)) = q;
+    reinterpret_cast<uint4*>(dst)[c] = q;
   }
 }
 template <>
-__device__ __forceinline__ void stage_row<float>(uint8_t* box, int row, const float (&v)[16]) {
+__device__ __forceinline__ void store_row16<float>(float* dst, const float (&v)[16]) {
 #pragma unroll
   for (int c = 0; c < 4; ++c)
-    *reinterpret_cast<float4*>(box + row * 64 + ((c ^ ((row >> 1) & 3)) << 4)) =
-        make_float4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
+    reinterpret_cast<float4*>(dst)[c] = make_float4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
 }
-
-// Output staging of one epilogue warp: NB boxes used in turn, each freed once the TMA store
-// that last read it is done reading.  The stores are small (32 rows x 16 columns), so how many
-// are in flight sets the output bandwidth: the launchers take the deepest NB that fits.
-template <typename T, int NB>
-struct Stager {
-  uint8_t* base;
-  uint32_t n;  // boxes used so far
-  static constexpr uint32_t BOX = 32 * 16 * sizeof(T);
-  __device__ uint8_t* next() {
-    uint8_t* b = base + (n % NB) * BOX;
-    if ((threadIdx.x & 31) == 0 && n >= NB) tc::tma_store_wait_read_n<NB - 1>();
-    __syncwarp();
-    ++n;
-    return b;
-  }
-  // Hands the box just written to the TMA store of rows [row0, row0 + 32), columns [col0, +16).
-  __device__ void store(const CUtensorMap* map, uint8_t* box, int col0, int row0) {
-    tc::fence_proxy_async_smem();
-    __syncwarp();
-    if ((threadIdx.x & 31) == 0) {
-      tc::tma_store_2d(map, box, col0, row0);
-      tc::tma_store_commit();
-    }
-  }
-  __device__ void drain() {
-    if ((threadIdx.x & 31) == 0) tc::tma_store_wait0();
-    __syncwarp();
-  }
-};
 
 struct ProjParams {
   int R, k, nblk, P;     // rows, gate block, blocks, CTAs per (block, matrix group)
+  void* out[4];          // forward: lr, li (split: then their lo planes); dx: out[0]
   const float* bias[2];  // forward: ba, bx (null = zero)
   const void* add;       // dx: the addend (float32 or bf16 [R][W]); may alias the output
   int add_f32;
@@ -130,16 +98,13 @@ struct ProjParams {
 // ================================================================ forward projection
 // CTA (blk, r) keeps Wa[blk], Wx[blk] in shared memory and takes the row tiles r, r + P, ...
 // Per tile the x tile feeds two accumulations, lr then li, each into the next slot of a ring
-// of k-column TMEM buffers; the epilogue warps add the bias, convert and store.  SPLIT: the
-// float32 logits go out as bf16 hi and lo planes (tm_lr2 / tm_li2 map the lo planes).
-template <typename OT, bool SPLIT, int NB>
+// of k-column TMEM buffers; the epilogue warps add the bias, convert and store each row
+// straight to global memory, the next chunk's TMEM load in flight meanwhile.  SPLIT: the
+// float32 logits go out as bf16 hi and lo planes (p.out[2], p.out[3]: the lo planes).
+template <typename OT, bool SPLIT>
 __global__ void __launch_bounds__(NTHREADS, 1)
     k_proj_fwd(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_wa,
-               const __grid_constant__ CUtensorMap tm_wx,
-               const __grid_constant__ CUtensorMap tm_lr,
-               const __grid_constant__ CUtensorMap tm_li,
-               const __grid_constant__ CUtensorMap tm_lr2,
-               const __grid_constant__ CUtensorMap tm_li2, const __grid_constant__ ProjParams p,
+               const __grid_constant__ CUtensorMap tm_wx, const __grid_constant__ ProjParams p,
                int stages) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (tc::smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -150,8 +115,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   const int NS = 512 / (int)KC;  // TMEM ring slots
   uint8_t* s_w[2] = {smem, smem + WB};
   uint8_t* s_x = smem + 2 * WB;
-  uint8_t* s_stage = s_x + stages * TB;
-  float* s_bias = reinterpret_cast<float*>(s_stage + 4 * NB * Stager<OT, NB>::BOX);
+  float* s_bias = reinterpret_cast<float*>(s_x + stages * TB);
   uint64_t* bars = reinterpret_cast<uint64_t*>(s_bias + 2 * k);
   uint64_t* w_full = bars;
   uint64_t* x_full = bars + 1;
@@ -239,33 +203,36 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     }
   } else {
     const int q = warp & 3;  // TMEM lane quadrant = rows 32 q .. 32 q + 31 of a tile
-    Stager<OT, NB> sg{s_stage + (warp - 2) * NB * Stager<OT, NB>::BOX, 0u};
-    const CUtensorMap* out[2] = {&tm_lr, &tm_li};
-    const CUtensorMap* out2[2] = {&tm_lr2, &tm_li2};
+    const int NC = k / 16;
     for (int it = 0; it < my_tiles; ++it) {
-      const int row0 = (rr + it * p.P) * TR + 32 * q;
+      const int row = (rr + it * p.P) * TR + 32 * q + lane;  // this thread's row
+      const bool in = row < p.R;
 #pragma unroll 1
       for (int m = 0; m < 2; ++m) {
         const int u = 2 * it + m, slot = u % NS;
         if (!ctl.wait(&acc_full[slot], (u / NS) & 1)) break;
         tc::tc_fence_after();
         const uint32_t ta = tmem + ((uint32_t)(32 * q) << 16) + slot * KC;
-        for (int c = 0; c < k / 16; ++c) {
-          float v[16];
-          tc::tmem_ld16(ta + 16 * c, v);
-          tc::tmem_ld_wait();
-          tc::reg_fence(v);
+        const size_t at = (size_t)row * p.W + (size_t)blk * k;
+        OT* dst = static_cast<OT*>(p.out[m]) + at;
+        OT* dst2 = SPLIT ? static_cast<OT*>(p.out[2 + m]) + at : nullptr;
+        // the next chunk's accumulator load is in flight while this one is written out
+        float v[2][16];
+        tc::tmem_ld16(ta, v[0]);
 #pragma unroll
-          for (int e = 0; e < 16; ++e) v[e] += s_bias[m * k + 16 * c + e];
-          uint8_t* box = sg.next();
-          stage_row<OT>(box, lane, v);
-          sg.store(out[m], box, blk * k + 16 * c, row0);
+        for (int c = 0; c < NCMAX; ++c) {
+          if (c >= NC) break;
+          tc::tmem_ld_wait();
+          tc::reg_fence(v[c & 1]);
+          if (c + 1 < NC) tc::tmem_ld16(ta + 16 * (c + 1), v[(c + 1) & 1]);
+          float (&vv)[16] = v[c & 1];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) vv[e] += s_bias[m * k + 16 * c + e];
+          if (in) store_row16<OT>(dst + 16 * c, vv);
           if (SPLIT) {  // lo = v - bf16(v), exact in float32, then rounded to bf16
 #pragma unroll
-            for (int e = 0; e < 16; ++e) v[e] -= __bfloat162float(__float2bfloat16_rn(v[e]));
-            uint8_t* box2 = sg.next();
-            stage_row<OT>(box2, lane, v);
-            sg.store(out2[m], box2, blk * k + 16 * c, row0);
+            for (int e = 0; e < 16; ++e) vv[e] -= __bfloat162float(__float2bfloat16_rn(vv[e]));
+            if (in) store_row16<OT>(dst2 + 16 * c, vv);
           }
         }
         tc::tc_fence_before();
@@ -273,7 +240,6 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         if (lane == 0) tc::mbar_arrive(&acc_empty[slot]);
       }
     }
-    sg.drain();
   }
   tc::tc_fence_before();
   __syncthreads();
@@ -330,11 +296,11 @@ struct AddChunk<bf16> {
   }
 };
 
-template <typename OT, typename AT, int NB>
+template <typename OT, typename AT>
 __global__ void __launch_bounds__(NTHREADS, 1)
     k_proj_dx(const __grid_constant__ CUtensorMap tm_dla, const __grid_constant__ CUtensorMap tm_dlx,
               const __grid_constant__ CUtensorMap tm_wa,
-              const __grid_constant__ CUtensorMap tm_wx, const __grid_constant__ CUtensorMap tm_dx,
+              const __grid_constant__ CUtensorMap tm_wx,
               const __grid_constant__ ProjParams p, int stages) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (tc::smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -345,8 +311,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   const int NOP = 2 * p.nplanes;  // operand tiles per row tile
   uint8_t* s_w[2] = {smem, smem + WB};
   uint8_t* s_in = smem + 2 * WB;
-  uint8_t* s_stage = s_in + stages * TB;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(s_stage + 4 * NB * Stager<OT, NB>::BOX);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(s_in + stages * TB);
   uint64_t* w_full = bars;
   uint64_t* in_full = bars + 1;
   uint64_t* in_empty = in_full + stages;
@@ -445,14 +410,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     }
   } else {
     const int q = warp & 3;
-    Stager<OT, NB> sg{s_stage + (warp - 2) * NB * Stager<OT, NB>::BOX, 0u};
     const int NC = k / 16;
     for (int it = 0; it < my_tiles; ++it) {
       const int slot = it & 1;
-      const int rw = (rr + it * p.P) * TR + 32 * q;  // the warp's first row
-      const int row = rw + lane;
+      const int row = (rr + it * p.P) * TR + 32 * q + lane;
       const bool in = row < p.R;
-      const AT* arow = static_cast<const AT*>(p.add) + (size_t)row * p.W + (size_t)blk * k;
+      const size_t at = (size_t)row * p.W + (size_t)blk * k;
+      const AT* arow = static_cast<const AT*>(p.add) + at;
+      OT* dst = static_cast<OT*>(p.out[0]) + at;
       // the addend's whole row is requested before the accumulator is waited for (one memory
       // round trip per tile instead of one per chunk)
       AddChunk<AT> add[NCMAX];
@@ -462,23 +427,22 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       if (!ctl.wait(&acc_full[slot], (it >> 1) & 1)) break;
       tc::tc_fence_after();
       const uint32_t ta = tmem + ((uint32_t)(32 * q) << 16) + slot * KC;
+      float v[2][16];
+      tc::tmem_ld16(ta, v[0]);
 #pragma unroll
       for (int c = 0; c < NCMAX; ++c) {
         if (c >= NC) break;
-        float v[16];
-        tc::tmem_ld16(ta + 16 * c, v);
         tc::tmem_ld_wait();
-        tc::reg_fence(v);
-        add[c].add_to(v);
-        uint8_t* box = sg.next();
-        stage_row<OT>(box, lane, v);
-        sg.store(&tm_dx, box, blk * k + 16 * c, rw);
+        tc::reg_fence(v[c & 1]);
+        if (c + 1 < NC) tc::tmem_ld16(ta + 16 * (c + 1), v[(c + 1) & 1]);
+        float (&vv)[16] = v[c & 1];
+        add[c].add_to(vv);
+        if (in) store_row16<OT>(dst + 16 * c, vv);
       }
       tc::tc_fence_before();
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(&acc_empty[slot]);
     }
-    sg.drain();
   }
   tc::tc_fence_before();
   __syncthreads();
@@ -760,18 +724,6 @@ cudaError_t planes_map(const Dims& d, const void* base, size_t plane_elems, int 
                      CU_TENSOR_MAP_SWIZZLE_32B);
 }
 
-// An output [R][W] of 16-column x 32-row boxes (bf16: 32-byte rows; float32: 64-byte rows).
-cudaError_t out_map(const Dims& d, void* base, int dt, CUtensorMap* m) {
-  const uint64_t R = (uint64_t)d.B * d.T;
-  const uint64_t es = dt == DT_F32 ? 4 : 2;
-  const uint64_t dims[2] = {(uint64_t)d.W, R};
-  const uint64_t str[1] = {(uint64_t)d.W * es};
-  const uint32_t box[2] = {16, 32};
-  return encode_tmap(m, dt == DT_F32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
-                     2, base, dims, str, box,
-                     dt == DT_F32 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B);
-}
-
 size_t bars_bytes(int n) { return 256 + (size_t)n * 8; }
 
 }  // namespace
@@ -792,19 +744,10 @@ cudaError_t launch_proj_fwd(const Dims& d, int ot, const void* x, const void* Wa
   if (!proj_tc_supported(d)) return cudaErrorNotSupported;
   const bool split = ot == DT_SPLIT;
   const int et = split ? DT_BF16 : ot;  // element type of each output plane
-  CUtensorMap mx, mwa, mwx, mlr, mli, mlr2, mli2;
+  CUtensorMap mx, mwa, mwx;
   cudaError_t e = act_map(d, x, &mx);
   if (e == cudaSuccess) e = weight_maps(d, Wa, Wx, &mwa, &mwx);
-  if (e == cudaSuccess) e = out_map(d, lr, et, &mlr);
-  if (e == cudaSuccess) e = out_map(d, li, et, &mli);
   if (e != cudaSuccess) return e;
-  mlr2 = mlr;
-  mli2 = mli;
-  if (split) {  // the lo planes follow the hi planes, N elements later
-    e = out_map(d, static_cast<bf16*>(lr) + d.N, DT_BF16, &mlr2);
-    if (e == cudaSuccess) e = out_map(d, static_cast<bf16*>(li) + d.N, DT_BF16, &mli2);
-    if (e != cudaSuccess) return e;
-  }
   ProjParams p = {};
   p.R = d.B * d.T;
   p.k = d.k;
@@ -813,31 +756,23 @@ cudaError_t launch_proj_fwd(const Dims& d, int ot, const void* x, const void* Wa
   p.P = ctas_per_group(d.nblk);
   p.bias[0] = ba;
   p.bias[1] = bx;
-  const size_t box = 32 * 16 * (et == DT_F32 ? 4 : 2);
-  const int NS = 512 / (int)kcols(d.k);
-  // the deepest output staging (16, 8 or 4 boxes a warp) with at least two x stages, then as
-  // many x stages (up to 4) as fit
-  int nb = 16, stages = 0;
-  size_t fixed = 0;
-  for (; nb >= 4; nb /= 2) {
-    fixed = 1024 + 2 * (size_t)d.k * d.k * 2 + 4 * nb * box + 2 * d.k * 4 + bars_bytes(1 + 2 * NS);
-    if (fixed + 2 * ((size_t)tile_bytes(d.k) + 16) <= SMEM_MAX || nb == 4) break;
+  p.out[0] = lr;
+  p.out[1] = li;
+  if (split) {  // the lo planes follow the hi planes, N elements later
+    p.out[2] = static_cast<bf16*>(lr) + d.N;
+    p.out[3] = static_cast<bf16*>(li) + d.N;
   }
-  stages = 4;
+  const int NS = 512 / (int)kcols(d.k);
+  const size_t fixed = 1024 + 2 * (size_t)d.k * d.k * 2 + 2 * d.k * 4 + bars_bytes(1 + 2 * NS);
+  int stages = 6;
   while (stages > 1 && fixed + stages * (size_t)tile_bytes(d.k) + 16 * stages > SMEM_MAX) --stages;
   const size_t smem = fixed + stages * (size_t)tile_bytes(d.k) + 16 * stages;
   if (smem > SMEM_MAX) return cudaErrorNotSupported;
-  using KF = decltype(&k_proj_fwd<bf16, false, 4>);
-  KF kern;
-  if (split)
-    kern = nb == 16 ? k_proj_fwd<bf16, true, 16> : nb == 8 ? k_proj_fwd<bf16, true, 8> : k_proj_fwd<bf16, true, 4>;
-  else if (ot == DT_F32)
-    kern = nb == 16 ? k_proj_fwd<float, false, 16> : nb == 8 ? k_proj_fwd<float, false, 8> : k_proj_fwd<float, false, 4>;
-  else
-    kern = nb == 16 ? k_proj_fwd<bf16, false, 16> : nb == 8 ? k_proj_fwd<bf16, false, 8> : k_proj_fwd<bf16, false, 4>;
+  auto kern = split ? k_proj_fwd<bf16, true>
+                    : (et == DT_F32 ? k_proj_fwd<float, false> : k_proj_fwd<bf16, false>);
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  kern<<<p.P * d.nblk, NTHREADS, smem, s>>>(mx, mwa, mwx, mlr, mli, mlr2, mli2, p, stages);
+  kern<<<p.P * d.nblk, NTHREADS, smem, s>>>(mx, mwa, mwx, p, stages);
   note_launches(1);
   return cudaGetLastError();
 }
@@ -846,11 +781,10 @@ cudaError_t launch_proj_dx(const Dims& d, int ot, const void* dlr, const void* d
                            size_t plane_elems, int nplanes, const void* Wa, const void* Wx,
                            const void* add, int add_f32, void* dx, cudaStream_t s) {
   if (!proj_tc_supported(d)) return cudaErrorNotSupported;
-  CUtensorMap mdla, mdlx, mwa, mwx, mdx;
+  CUtensorMap mdla, mdlx, mwa, mwx;
   cudaError_t e = planes_map(d, dlr, plane_elems, nplanes, &mdla);
   if (e == cudaSuccess) e = planes_map(d, dli, plane_elems, nplanes, &mdlx);
   if (e == cudaSuccess) e = weight_maps(d, Wa, Wx, &mwa, &mwx);
-  if (e == cudaSuccess) e = out_map(d, dx, ot, &mdx);
   if (e != cudaSuccess) return e;
   ProjParams p = {};
   p.R = d.B * d.T;
@@ -861,29 +795,17 @@ cudaError_t launch_proj_dx(const Dims& d, int ot, const void* dlr, const void* d
   p.add = add;
   p.add_f32 = add_f32;
   p.nplanes = nplanes;
-  const size_t box = 32 * 16 * (ot == DT_F32 ? 4 : 2);
-  int nb = 16;
-  size_t fixed = 0;
-  for (; nb >= 4; nb /= 2) {
-    fixed = 1024 + 2 * (size_t)d.k * d.k * 2 + 4 * nb * box + bars_bytes(5);
-    if (fixed + 2 * ((size_t)tile_bytes(d.k) + 16) <= SMEM_MAX || nb == 4) break;
-  }
-  int stages = 4;
+  p.out[0] = dx;
+  const size_t fixed = 1024 + 2 * (size_t)d.k * d.k * 2 + bars_bytes(5);
+  int stages = 6;
   while (stages > 2 && fixed + stages * (size_t)tile_bytes(d.k) + 16 * stages > SMEM_MAX) --stages;
   const size_t smem = fixed + stages * (size_t)tile_bytes(d.k) + 16 * stages;
   if (smem > SMEM_MAX) return cudaErrorNotSupported;
-  using KD = decltype(&k_proj_dx<bf16, bf16, 4>);
-  KD kern;
-#define RGLRU_DX_KERN(O, A) \
-  (nb == 16 ? k_proj_dx<O, A, 16> : nb == 8 ? k_proj_dx<O, A, 8> : k_proj_dx<O, A, 4>)
-  if (ot == DT_F32)
-    kern = add_f32 ? RGLRU_DX_KERN(float, float) : RGLRU_DX_KERN(float, bf16);
-  else
-    kern = add_f32 ? RGLRU_DX_KERN(bf16, float) : RGLRU_DX_KERN(bf16, bf16);
-#undef RGLRU_DX_KERN
+  auto kern = ot == DT_F32 ? (add_f32 ? k_proj_dx<float, float> : k_proj_dx<float, bf16>)
+                           : (add_f32 ? k_proj_dx<bf16, float> : k_proj_dx<bf16, bf16>);
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  kern<<<p.P * d.nblk, NTHREADS, smem, s>>>(mdla, mdlx, mwa, mwx, mdx, p, stages);
+  kern<<<p.P * d.nblk, NTHREADS, smem, s>>>(mdla, mdlx, mwa, mwx, p, stages);
   note_launches(1);
   return cudaGetLastError();
 }
