@@ -17,9 +17,11 @@
 // Every operand tile is 128 rows of one gate block, loaded by TMA as 16-channel slabs with
 // the 32-byte swizzle (128 rows x 32 bytes = 4 KB a slab): a slab is one K = 16 step of a
 // K-major operand, and 16 consecutive M or N indices of an MN-major one.  One CTA per SM:
-// warp 0 issues the TMA loads, warp 1 the MMAs (one elected lane), warps 2..5 read the
+// warp 0 issues the TMA loads, warp 1 the MMAs (one elected lane), the other warps read the
 // accumulators back (warp w reaches TMEM lanes 32 (w % 4) .. 32 (w % 4) + 31, so it owns those
-// rows of a tile).  Pipeline waits are bounded (2 s); a wait that runs out winds the CTA down.
+// rows of a tile): one set of four in the dW kernel, which writes only its partial sums, and
+// one or two sets (as shared memory allows their box rings) in the forward and dx kernels,
+// whose epilogues write every output element.  Pipeline waits are bounded (2 s); a wait that runs out winds the CTA down.
 #include <cudaTypedefs.h>
 
 #include <algorithm>
@@ -34,7 +36,8 @@ namespace {
 
 constexpr int TR = 128;                   // rows of a tile
 constexpr uint32_t SLAB = TR * 32;        // one 16-channel slab of a tile
-constexpr int NTHREADS = 192;             // TMA, MMA, 4 epilogue warps
+constexpr int NTHREADS = 192;             // TMA, MMA, one set of 4 epilogue warps
+constexpr int NTHREADS_MAX = 320;         // TMA, MMA, two sets of 4 epilogue warps
 constexpr uint64_t WAIT_NS = 2000000000ull;
 constexpr size_t SMEM_MAX = 232448;       // 227 KB of dynamic shared memory per CTA
 constexpr int NCMAX = PROJ_TC_KMAX / 16;   // 16-column chunks of a row, at most
@@ -58,34 +61,89 @@ struct Abort {
   }
 };
 
-// 16 float32 values of one row stored straight to global memory as T (two or four 16-byte
-// stores; a warp's 32 rows each take whole 32-byte sectors).
-template <typename T>
-__device__ __forceinline__ void store_row16(T* dst, const float (&v)[16]);
-template <>
-__device__ __forceinline__ void store_row16<bf16>(bf16* dst, const float (&v)[16]) {
-#pragma unroll
-  for (int c = 0; c < 2; ++c) {
-    uint4 q;
-    uint32_t* w = &q.x;
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const __nv_bfloat162 h = __floats2bfloat162_rn(v[8 * c + 2 * u], v[8 * c + 2 * u + 1]);
-      w[u] = *reinterpret_cast<const uint32_t*>(&h);
-    }
-    reinterpret_cast<uint4*>(dst)[c] = q;
+// ---------------------------------------------------------------- staged row stores
+// An epilogue warp owns 32 rows of a tile, one a lane, and produces each row 16 columns at a
+// time.  Stored straight to global memory, every 16-byte store of the warp would touch 32
+// rows, and those stores run at a fraction of the copy bandwidth.  Instead the warp writes its
+// chunks into shared-memory boxes of 32 rows x bi bytes (bi = 128, 64 or 32: the widest that
+// divides a block row), in the layout the TMA swizzle of that width gives: 16-byte unit u of
+// row r sits at unit u ^ ((r >> shift) & (bi / 16 - 1)), shift = 0, 1, 2 for bi = 128, 64,
+// 32; the same XOR keeps the warp's writes free of bank conflicts.  One lane stores each
+// completed box with a TMA tensor store; a ring of RING boxes (per output plane) lets the
+// stores drain behind the next chunks.
+constexpr int RING = 2;
+
+template <typename OT>
+struct BoxStore {
+  static constexpr int UPC = (int)sizeof(OT);  // 16-byte units of a 16-column chunk
+  uint8_t* ring;  // RING x planes boxes of 32 * bi bytes, 1024-byte aligned
+  int bi, csh, cmask, sw, planes, lane, slot;  // chunks a box = 1 << csh (cmask = that - 1)
+
+  __device__ BoxStore(uint8_t* r, int bi_, int planes_, int lane_)
+      : ring(r), bi(bi_), planes(planes_), lane(lane_), slot(0) {
+    // chunks a box: bi / (16 sizeof(OT)), a power of two; rows swizzled by lane >> shift
+    csh = (bi_ == 128 ? 3 : (bi_ == 64 ? 2 : 1)) - (sizeof(OT) == 4 ? 2 : 1);
+    cmask = (1 << csh) - 1;
+    const int shift = bi_ == 128 ? 0 : (bi_ == 64 ? 1 : 2);
+    sw = (lane_ >> shift) & (bi_ / 16 - 1);
   }
-}
-template <>
-__device__ __forceinline__ void store_row16<float>(float* dst, const float (&v)[16]) {
+  __device__ uint8_t* box(int pl) const { return ring + (size_t)(slot * planes + pl) * 32 * bi; }
+  // Before the first chunk of a box: the ring slot's earlier stores have finished reading it.
+  __device__ void begin(int c) {
+    if ((c & cmask) == 0) {
+      if (lane == 0) tc::tma_store_wait_read_n<RING - 1>();
+      __syncwarp();
+    }
+  }
+  // Chunk c of this lane's row, plane pl.
+  __device__ void put(int c, int pl, const float (&v)[16]) {
+    uint8_t* row = box(pl) + lane * bi;
+    const int u0 = (c & cmask) * UPC;
+    if constexpr (sizeof(OT) == 2) {
 #pragma unroll
-  for (int c = 0; c < 4; ++c)
-    reinterpret_cast<float4*>(dst)[c] = make_float4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
+      for (int j = 0; j < 2; ++j) {
+        uint4 q;
+        uint32_t* w = &q.x;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const __nv_bfloat162 h = __floats2bfloat162_rn(v[8 * j + 2 * e], v[8 * j + 2 * e + 1]);
+          w[e] = *reinterpret_cast<const uint32_t*>(&h);
+        }
+        *reinterpret_cast<uint4*>(row + (((u0 + j) ^ sw) << 4)) = q;
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        *reinterpret_cast<float4*>(row + (((u0 + j) ^ sw) << 4)) =
+            make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+    }
+  }
+  // After chunk c: a completed box goes out to columns x0 + (its first column), rows y0 .. y0 + 31
+  // of every plane (rows past the tensor are clipped by the store).
+  __device__ void end(int c, const CUtensorMap* map, int x0, int y0) {
+    if ((c & cmask) != cmask) return;
+    tc::fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+      const int x = x0 + (c >> csh) * (bi / (int)sizeof(OT));
+      for (int pl = 0; pl < planes; ++pl) tc::tma_store_3d(map, box(pl), x, y0, pl);
+      tc::tma_store_commit();
+    }
+    slot ^= 1;  // RING = 2
+  }
+  __device__ void drain() const {
+    if (lane == 0) tc::tma_store_wait0();
+  }
+};
+static_assert(RING == 2, "BoxStore::end steps a two-slot ring");
+
+// Bytes of one epilogue warp's box ring.
+__host__ __device__ constexpr uint32_t ring_bytes(int bi, int planes) {
+  return (uint32_t)(RING * planes * 32 * bi);
 }
 
 struct ProjParams {
   int R, k, nblk, P;     // rows, gate block, blocks, CTAs per (block, matrix group)
-  void* out[4];          // forward: lr, li (split: then their lo planes); dx: out[0]
   const float* bias[2];  // forward: ba, bx (null = zero)
   const void* add;       // dx: the addend (float32 or bf16 [R][W]); may alias the output
   int add_f32;
@@ -93,18 +151,21 @@ struct ProjParams {
   int nplanes;           // gradient operand planes (1, or 2 for hi + lo)
   int nmat;              // dW: matrices per CTA (2: both; 1: CTA group m handles matrix m)
   float* part;           // dW: partial sums [blk][r][m][k * k + k]
+  int bi;                // forward, dx: row bytes of an output box (128, 64 or 32)
+  int nsets;             // forward, dx: sets of 4 epilogue warps (1 or 2)
 };
 
 // ================================================================ forward projection
 // CTA (blk, r) keeps Wa[blk], Wx[blk] in shared memory and takes the row tiles r, r + P, ...
 // Per tile the x tile feeds two accumulations, lr then li, each into the next slot of a ring
-// of k-column TMEM buffers; the epilogue warps add the bias, convert and store each row
-// straight to global memory, the next chunk's TMEM load in flight meanwhile.  SPLIT: the
-// float32 logits go out as bf16 hi and lo planes (p.out[2], p.out[3]: the lo planes).
+// of k-column TMEM buffers; the epilogue warps add the bias, convert, and stage each row into
+// their box rings for TMA stores (BoxStore), the next chunk's TMEM load in flight meanwhile.
+// SPLIT: the float32 logits go out as bf16 hi and lo planes (the output maps' second plane).
 template <typename OT, bool SPLIT>
-__global__ void __launch_bounds__(NTHREADS, 1)
+__global__ void __launch_bounds__(NTHREADS_MAX, 1)
     k_proj_fwd(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_wa,
-               const __grid_constant__ CUtensorMap tm_wx, const __grid_constant__ ProjParams p,
+               const __grid_constant__ CUtensorMap tm_wx, const __grid_constant__ CUtensorMap tm_lr,
+               const __grid_constant__ CUtensorMap tm_li, const __grid_constant__ ProjParams p,
                int stages) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (tc::smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -113,9 +174,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   const uint32_t WB = (uint32_t)k * k * 2;
   const uint32_t KC = kcols(k);
   const int NS = 512 / (int)KC;  // TMEM ring slots
+  constexpr int PLANES = SPLIT ? 2 : 1;
   uint8_t* s_w[2] = {smem, smem + WB};
   uint8_t* s_x = smem + 2 * WB;
-  float* s_bias = reinterpret_cast<float*>(s_x + stages * TB);
+  uint8_t* s_ring = s_x + stages * TB;  // the epilogue warps' box rings (1024-byte aligned)
+  float* s_bias = reinterpret_cast<float*>(s_ring + 4 * p.nsets * ring_bytes(p.bi, PLANES));
   uint64_t* bars = reinterpret_cast<uint64_t*>(s_bias + 2 * k);
   uint64_t* w_full = bars;
   uint64_t* x_full = bars + 1;
@@ -145,7 +208,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     *abort_flag = 0u;
     tc::fence_barrier_init();
   }
-  for (int j = threadIdx.x; j < 2 * k; j += NTHREADS) {
+  for (int j = threadIdx.x; j < 2 * k; j += blockDim.x) {
     const float* b = p.bias[j >= k];
     s_bias[j] = b ? b[blk * k + (j % k)] : 0.0f;
   }
@@ -204,19 +267,21 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   } else {
     const int q = warp & 3;  // TMEM lane quadrant = rows 32 q .. 32 q + 31 of a tile
     const int NC = k / 16;
+    // one set: every warp writes lr then li; two sets: set 0 writes lr, set 1 li
+    const int set = (warp - 2) >> 2;
+    const int m0 = p.nsets == 2 ? set : 0, m1 = p.nsets == 2 ? set + 1 : 2;
+    BoxStore<OT> bs(s_ring + (warp - 2) * ring_bytes(p.bi, PLANES), p.bi, PLANES, lane);
     for (int it = 0; it < my_tiles; ++it) {
-      const int row = (rr + it * p.P) * TR + 32 * q + lane;  // this thread's row
-      const bool in = row < p.R;
+      const int y0 = (rr + it * p.P) * TR + 32 * q;  // this warp's first row
 #pragma unroll 1
-      for (int m = 0; m < 2; ++m) {
+      for (int m = m0; m < m1; ++m) {
         const int u = 2 * it + m, slot = u % NS;
         if (!ctl.wait(&acc_full[slot], (u / NS) & 1)) break;
         tc::tc_fence_after();
         const uint32_t ta = tmem + ((uint32_t)(32 * q) << 16) + slot * KC;
-        const size_t at = (size_t)row * p.W + (size_t)blk * k;
-        OT* dst = static_cast<OT*>(p.out[m]) + at;
-        OT* dst2 = SPLIT ? static_cast<OT*>(p.out[2 + m]) + at : nullptr;
-        // the next chunk's accumulator load is in flight while this one is written out
+        const CUtensorMap* om = m ? &tm_li : &tm_lr;
+        const float4* b4 = reinterpret_cast<const float4*>(s_bias + m * k);
+        // the next chunk's accumulator load is in flight while this one is staged
         float v[2][16];
         tc::tmem_ld16(ta, v[0]);
 #pragma unroll
@@ -227,19 +292,28 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           if (c + 1 < NC) tc::tmem_ld16(ta + 16 * (c + 1), v[(c + 1) & 1]);
           float (&vv)[16] = v[c & 1];
 #pragma unroll
-          for (int e = 0; e < 16; ++e) vv[e] += s_bias[m * k + 16 * c + e];
-          if (in) store_row16<OT>(dst + 16 * c, vv);
+          for (int e = 0; e < 4; ++e) {
+            const float4 b = b4[4 * c + e];
+            vv[4 * e] += b.x;
+            vv[4 * e + 1] += b.y;
+            vv[4 * e + 2] += b.z;
+            vv[4 * e + 3] += b.w;
+          }
+          bs.begin(c);
+          bs.put(c, 0, vv);
           if (SPLIT) {  // lo = v - bf16(v), exact in float32, then rounded to bf16
 #pragma unroll
             for (int e = 0; e < 16; ++e) vv[e] -= __bfloat162float(__float2bfloat16_rn(vv[e]));
-            if (in) store_row16<OT>(dst2 + 16 * c, vv);
+            bs.put(c, 1, vv);
           }
+          bs.end(c, om, blk * k, y0);
         }
         tc::tc_fence_before();
         __syncwarp();
         if (lane == 0) tc::mbar_arrive(&acc_empty[slot]);
       }
     }
+    bs.drain();
   }
   tc::tc_fence_before();
   __syncthreads();
@@ -253,7 +327,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 // CTA (blk, r) keeps Wa[blk], Wx[blk] in shared memory (the K-major B operand of dx = dl W^T)
 // and takes the row tiles r, r + P, ...  Per tile the 2 x nplanes gradient operand tiles pass
 // through a ring of `stages` buffers, each one K-loop into the tile's accumulator (one of two
-// TMEM buffers); the epilogue adds the addend tile and stores dx.
+// TMEM buffers); the epilogue adds the addend tile and stores dx through its box ring.
 // Loads the 16 addend values of chunk c of this thread's row (zero past the rows).
 template <typename AT>
 struct AddChunk;
@@ -297,10 +371,10 @@ struct AddChunk<bf16> {
 };
 
 template <typename OT, typename AT>
-__global__ void __launch_bounds__(NTHREADS, 1)
+__global__ void __launch_bounds__(NTHREADS_MAX, 1)
     k_proj_dx(const __grid_constant__ CUtensorMap tm_dla, const __grid_constant__ CUtensorMap tm_dlx,
               const __grid_constant__ CUtensorMap tm_wa,
-              const __grid_constant__ CUtensorMap tm_wx,
+              const __grid_constant__ CUtensorMap tm_wx, const __grid_constant__ CUtensorMap tm_dx,
               const __grid_constant__ ProjParams p, int stages) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (tc::smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -311,7 +385,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   const int NOP = 2 * p.nplanes;  // operand tiles per row tile
   uint8_t* s_w[2] = {smem, smem + WB};
   uint8_t* s_in = smem + 2 * WB;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(s_in + stages * TB);
+  uint8_t* s_ring = s_in + stages * TB;  // the epilogue warps' box rings (1024-byte aligned)
+  uint64_t* bars = reinterpret_cast<uint64_t*>(s_ring + 4 * p.nsets * ring_bytes(p.bi, 1));
   uint64_t* w_full = bars;
   uint64_t* in_full = bars + 1;
   uint64_t* in_empty = in_full + stages;
@@ -335,7 +410,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     }
     for (int s = 0; s < 2; ++s) {
       tc::mbar_init(&acc_full[s], 1);
-      tc::mbar_init(&acc_empty[s], 4);
+      tc::mbar_init(&acc_empty[s], 4 * p.nsets);
     }
     *abort_flag = 0u;
     tc::fence_barrier_init();
@@ -411,38 +486,52 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   } else {
     const int q = warp & 3;
     const int NC = k / 16;
+    // with two sets, set h writes the output boxes b = h mod 2 (the chunks c with
+    // (c >> csh) mod 2 = h); the addend is loaded for those chunks only
+    const int set = (warp - 2) >> 2;
+    BoxStore<OT> bs(s_ring + (warp - 2) * ring_bytes(p.bi, 1), p.bi, 1, lane);
+    // the warp's j-th chunk: c = j with one set; with two, chunk j mod (chunks a box) of the
+    // warp's box j / (chunks a box), i.e. of box 2 (that) + set
+    auto chunk = [&](int j) {
+      return p.nsets == 1 ? j : ((((j >> bs.csh) << 1) + set) << bs.csh) | (j & bs.cmask);
+    };
     for (int it = 0; it < my_tiles; ++it) {
       const int slot = it & 1;
-      const int row = (rr + it * p.P) * TR + 32 * q + lane;
+      const int y0 = (rr + it * p.P) * TR + 32 * q;
+      const int row = y0 + lane;
       const bool in = row < p.R;
-      const size_t at = (size_t)row * p.W + (size_t)blk * k;
-      const AT* arow = static_cast<const AT*>(p.add) + at;
-      OT* dst = static_cast<OT*>(p.out[0]) + at;
-      // the addend's whole row is requested before the accumulator is waited for (one memory
-      // round trip per tile instead of one per chunk)
-      AddChunk<AT> add[NCMAX];
+      const AT* arow = static_cast<const AT*>(p.add) + (size_t)row * p.W + (size_t)blk * k;
+      // the addend's first NA chunks of this warp are requested before the accumulator is
+      // waited for, each later one NA chunks ahead of its use (a rolling window of registers)
+      constexpr int NA = sizeof(AT) == 4 ? 3 : 5;
+      AddChunk<AT> add[NA];
 #pragma unroll
-      for (int c = 0; c < NCMAX; ++c)
-        if (c < NC) add[c].load(arow, c, in);
+      for (int j = 0; j < NA; ++j)
+        if (chunk(j) < NC) add[j].load(arow, chunk(j), in);
       if (!ctl.wait(&acc_full[slot], (it >> 1) & 1)) break;
       tc::tc_fence_after();
       const uint32_t ta = tmem + ((uint32_t)(32 * q) << 16) + slot * KC;
       float v[2][16];
-      tc::tmem_ld16(ta, v[0]);
+      if (chunk(0) < NC) tc::tmem_ld16(ta + 16 * chunk(0), v[0]);
 #pragma unroll
-      for (int c = 0; c < NCMAX; ++c) {
+      for (int j = 0; j < NCMAX; ++j) {
+        const int c = chunk(j);
         if (c >= NC) break;
         tc::tmem_ld_wait();
-        tc::reg_fence(v[c & 1]);
-        if (c + 1 < NC) tc::tmem_ld16(ta + 16 * (c + 1), v[(c + 1) & 1]);
-        float (&vv)[16] = v[c & 1];
-        add[c].add_to(vv);
-        if (in) store_row16<OT>(dst + 16 * c, vv);
+        tc::reg_fence(v[j & 1]);
+        if (chunk(j + 1) < NC) tc::tmem_ld16(ta + 16 * chunk(j + 1), v[(j + 1) & 1]);
+        float (&vv)[16] = v[j & 1];
+        add[j % NA].add_to(vv);
+        if (chunk(j + NA) < NC) add[j % NA].load(arow, chunk(j + NA), in);
+        bs.begin(c);
+        bs.put(c, 0, vv);
+        bs.end(c, &tm_dx, blk * k, y0);
       }
       tc::tc_fence_before();
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(&acc_empty[slot]);
     }
+    bs.drain();
   }
   tc::tc_fence_before();
   __syncthreads();
@@ -650,8 +739,18 @@ __global__ void k_proj_dw_reduce(const float* __restrict__ part, int nblk, int P
     const int m = (int)(rem / per);
     const size_t off = rem % per;
     const float* src = part + (blk * P * 2 + m) * per + off;
+    // four partials requested at a time, added in CTA order
     float s = 0.0f;
-    for (int r = 0; r < P; ++r) s += src[(size_t)r * 2 * per];
+    int r = 0;
+    for (; r + 4 <= P; r += 4) {
+      const float a0 = src[(size_t)r * 2 * per], a1 = src[(size_t)(r + 1) * 2 * per];
+      const float a2 = src[(size_t)(r + 2) * 2 * per], a3 = src[(size_t)(r + 3) * 2 * per];
+      s += a0;
+      s += a1;
+      s += a2;
+      s += a3;
+    }
+    for (; r < P; ++r) s += src[(size_t)r * 2 * per];
     if (off < (size_t)k * k) {
       (m ? dWx : dWa)[blk * k * k + off] = s;
     } else {
@@ -724,6 +823,27 @@ cudaError_t planes_map(const Dims& d, const void* base, size_t plane_elems, int 
                      CU_TENSOR_MAP_SWIZZLE_32B);
 }
 
+// Row bytes of an output box: the widest of 128, 64, 32 that divides a block row of k elements.
+int box_row_bytes(int k, int esize) {
+  const int rb = k * esize;
+  return rb % 128 == 0 ? 128 : (rb % 64 == 0 ? 64 : 32);
+}
+
+// An output [R][W] of element type et (planes of N elements apart: split hi + lo) in boxes of
+// 32 rows x bi bytes, with the TMA swizzle of that width (the layout BoxStore writes).
+cudaError_t out_map(const Dims& d, void* base, int et, int planes, int bi, CUtensorMap* m) {
+  const int es = et == DT_F32 ? 4 : 2;
+  const uint64_t dims[3] = {(uint64_t)d.W, (uint64_t)d.B * d.T, (uint64_t)planes};
+  const uint64_t str[2] = {(uint64_t)d.W * es, (uint64_t)d.N * es};
+  const uint32_t box[3] = {(uint32_t)(bi / es), 32, 1};
+  const CUtensorMapSwizzle sw = bi == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
+                                          : (bi == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                                      : CU_TENSOR_MAP_SWIZZLE_32B);
+  return encode_tmap(m, et == DT_F32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                     : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                     3, base, dims, str, box, sw);
+}
+
 size_t bars_bytes(int n) { return 256 + (size_t)n * 8; }
 
 }  // namespace
@@ -756,23 +876,32 @@ cudaError_t launch_proj_fwd(const Dims& d, int ot, const void* x, const void* Wa
   p.P = ctas_per_group(d.nblk);
   p.bias[0] = ba;
   p.bias[1] = bx;
-  p.out[0] = lr;
-  p.out[1] = li;
-  if (split) {  // the lo planes follow the hi planes, N elements later
-    p.out[2] = static_cast<bf16*>(lr) + d.N;
-    p.out[3] = static_cast<bf16*>(li) + d.N;
-  }
+  // split: the lo planes follow the hi planes, N elements later (the maps' second plane)
+  const int planes = split ? 2 : 1;
+  p.bi = box_row_bytes(d.k, et == DT_F32 ? 4 : 2);
+  CUtensorMap mlr, mli;
+  e = out_map(d, lr, et, planes, p.bi, &mlr);
+  if (e == cudaSuccess) e = out_map(d, li, et, planes, p.bi, &mli);
+  if (e != cudaSuccess) return e;
+  // two sets of epilogue warps where their box rings still leave two x stages
   const int NS = 512 / (int)kcols(d.k);
-  const size_t fixed = 1024 + 2 * (size_t)d.k * d.k * 2 + 2 * d.k * 4 + bars_bytes(1 + 2 * NS);
-  int stages = 6;
-  while (stages > 1 && fixed + stages * (size_t)tile_bytes(d.k) + 16 * stages > SMEM_MAX) --stages;
-  const size_t smem = fixed + stages * (size_t)tile_bytes(d.k) + 16 * stages;
-  if (smem > SMEM_MAX) return cudaErrorNotSupported;
+  const size_t TBs = tile_bytes(d.k);
+  size_t smem = 0;
+  int stages = 0;
+  for (p.nsets = 2; p.nsets >= 1; --p.nsets) {
+    const size_t fixed = 1024 + 2 * (size_t)d.k * d.k * 2 +
+                         4 * (size_t)p.nsets * ring_bytes(p.bi, planes) + 2 * d.k * 4 +
+                         bars_bytes(1 + 2 * NS);
+    stages = fixed > SMEM_MAX ? 0 : (int)std::min<size_t>(6, (SMEM_MAX - fixed) / TBs);
+    smem = fixed + stages * TBs;
+    if (stages >= (p.nsets == 2 ? 2 : 1)) break;
+  }
+  if (p.nsets < 1 || stages < 1) return cudaErrorNotSupported;
   auto kern = split ? k_proj_fwd<bf16, true>
                     : (et == DT_F32 ? k_proj_fwd<float, false> : k_proj_fwd<bf16, false>);
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  kern<<<p.P * d.nblk, NTHREADS, smem, s>>>(mx, mwa, mwx, p, stages);
+  kern<<<p.P * d.nblk, 64 + 128 * p.nsets, smem, s>>>(mx, mwa, mwx, mlr, mli, p, stages);
   note_launches(1);
   return cudaGetLastError();
 }
@@ -795,17 +924,27 @@ cudaError_t launch_proj_dx(const Dims& d, int ot, const void* dlr, const void* d
   p.add = add;
   p.add_f32 = add_f32;
   p.nplanes = nplanes;
-  p.out[0] = dx;
-  const size_t fixed = 1024 + 2 * (size_t)d.k * d.k * 2 + bars_bytes(5);
-  int stages = 6;
-  while (stages > 2 && fixed + stages * (size_t)tile_bytes(d.k) + 16 * stages > SMEM_MAX) --stages;
-  const size_t smem = fixed + stages * (size_t)tile_bytes(d.k) + 16 * stages;
-  if (smem > SMEM_MAX) return cudaErrorNotSupported;
+  p.bi = box_row_bytes(d.k, ot == DT_F32 ? 4 : 2);
+  CUtensorMap mdx;
+  e = out_map(d, dx, ot, 1, p.bi, &mdx);
+  if (e != cudaSuccess) return e;
+  // two sets of epilogue warps where their box rings still leave three operand stages
+  const size_t TBs = tile_bytes(d.k);
+  size_t smem = 0;
+  int stages = 0;
+  for (p.nsets = 2; p.nsets >= 1; --p.nsets) {
+    const size_t fixed = 1024 + 2 * (size_t)d.k * d.k * 2 +
+                         4 * (size_t)p.nsets * ring_bytes(p.bi, 1) + bars_bytes(5);
+    stages = fixed > SMEM_MAX ? 0 : (int)std::min<size_t>(6, (SMEM_MAX - fixed) / TBs);
+    smem = fixed + stages * TBs;
+    if (stages >= (p.nsets == 2 ? 3 : 2)) break;
+  }
+  if (p.nsets < 1 || stages < 2) return cudaErrorNotSupported;
   auto kern = ot == DT_F32 ? (add_f32 ? k_proj_dx<float, float> : k_proj_dx<float, bf16>)
                            : (add_f32 ? k_proj_dx<bf16, float> : k_proj_dx<bf16, bf16>);
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  kern<<<p.P * d.nblk, NTHREADS, smem, s>>>(mdla, mdlx, mwa, mwx, p, stages);
+  kern<<<p.P * d.nblk, 64 + 128 * p.nsets, smem, s>>>(mdla, mdlx, mwa, mwx, mdx, p, stages);
   note_launches(1);
   return cudaGetLastError();
 }

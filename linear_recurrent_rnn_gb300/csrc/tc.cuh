@@ -331,15 +331,23 @@ __device__ __forceinline__ void reg_fence(float (&v)[N]) {
 
 // ---------------------------------------------------------------- descriptors
 // Shared-memory matrix descriptor (sm_100 format): start address, leading / stride byte
-// offsets (>> 4), version 1 at bits 46-47, layout type at bits 61-63 (6 = 32-byte swizzle).
-__device__ __forceinline__ uint64_t smem_desc_sw32(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+// offsets (>> 4), version 1 at bits 46-47, layout type at bits 61-63 (2, 4, 6 = 128-, 64-,
+// 32-byte swizzle).  In the swizzled layouts used here SBO is the distance between groups of
+// 8 rows (8 x the swizzle width) and, for an MN-major operand, LBO the distance between the
+// swizzle-wide column slabs along M or N.
+enum : uint32_t { LAYOUT_SW128 = 2, LAYOUT_SW64 = 4, LAYOUT_SW32 = 6 };
+__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo,
+                                              uint32_t layout) {
   uint64_t d = 0;
   d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
   d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
   d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
   d |= (uint64_t)1u << 46;
-  d |= (uint64_t)6u << 61;
+  d |= (uint64_t)layout << 61;
   return d;
+}
+__device__ __forceinline__ uint64_t smem_desc_sw32(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  return smem_desc(saddr, lbo, sbo, LAYOUT_SW32);
 }
 
 // The n x n identity (bf16, n a multiple of 16) as a K-major MMA operand in the slab layout
