@@ -44,9 +44,16 @@ constexpr int NCMAX = PROJ_TC_KMAX / 16;   // 16-column chunks of a row, at most
 
 // Bytes of one operand tile (128 rows x k bf16).
 __host__ __device__ constexpr uint32_t tile_bytes(int k) { return (uint32_t)(k / 16) * SLAB; }
+// Bytes of the addend's identity operand in the dx kernel: the 32 x 32 identity as two
+// 16-column slabs (one per parity of the K step), see k_proj_dx.
+constexpr uint32_t ID_BYTES = 2048;
 // TMEM columns of a k-wide accumulator, rounded up to a multiple of 32.
 __host__ __device__ constexpr uint32_t kcols(int k) { return (uint32_t)((k + 31) / 32 * 32); }
-// Bytes past the dW kernel's operand ring that an x operand may read (see k_proj_dw).
+// TMEM columns of one matrix in the dW kernel: its dW accumulators and 32-column db ones.
+__host__ __device__ constexpr uint32_t dw_mcols(int k) {
+  return (uint32_t)((k + 127) / 128) * (kcols(k) + 32u);
+}
+// Bytes past the dW kernel's operand ring that an MN-major operand may read (see k_proj_dw).
 __host__ __device__ constexpr uint32_t dw_pad(int k) {
   return (uint32_t)((k + 127) / 128) * 8 * SLAB - tile_bytes(k);
 }
@@ -119,14 +126,14 @@ struct BoxStore {
     }
   }
   // After chunk c: a completed box goes out to columns x0 + (its first column), rows y0 .. y0 + 31
-  // of every plane (rows past the tensor are clipped by the store).
-  __device__ void end(int c, const CUtensorMap* map, int x0, int y0) {
+  // of planes z0, z0 + 1, ... (rows past the tensor are clipped by the store).
+  __device__ void end(int c, const CUtensorMap* map, int x0, int y0, int z0 = 0) {
     if ((c & cmask) != cmask) return;
     tc::fence_proxy_async_smem();
     __syncwarp();
     if (lane == 0) {
       const int x = x0 + (c >> csh) * (bi / (int)sizeof(OT));
-      for (int pl = 0; pl < planes; ++pl) tc::tma_store_3d(map, box(pl), x, y0, pl);
+      for (int pl = 0; pl < planes; ++pl) tc::tma_store_3d(map, box(pl), x, y0, z0 + pl);
       tc::tma_store_commit();
     }
     slot ^= 1;  // RING = 2
@@ -375,16 +382,25 @@ __global__ void __launch_bounds__(NTHREADS_MAX, 1)
     k_proj_dx(const __grid_constant__ CUtensorMap tm_dla, const __grid_constant__ CUtensorMap tm_dlx,
               const __grid_constant__ CUtensorMap tm_wa,
               const __grid_constant__ CUtensorMap tm_wx, const __grid_constant__ CUtensorMap tm_dx,
-              const __grid_constant__ ProjParams p, int stages) {
+              const __grid_constant__ CUtensorMap tm_add, const __grid_constant__ ProjParams p,
+              int stages) {
+  // a bf16 addend is one more operand tile, added by MMAs against the identity: K step kk (input
+  // channels 16 kk .. 16 kk + 15) adds into accumulator columns 32 (kk / 2) .. + 31 with N = 32,
+  // B = slab kk % 2 of the 32 x 32 identity (ones at rows 16 (kk % 2) + c), so every element
+  // gains one product with 1.0: the float32 sum of the two terms.  A float32 addend is read by
+  // the epilogue warps.
+  constexpr bool ADD_MMA = sizeof(AT) == 2;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (tc::smem_u32(smem_raw) & 1023u)) & 1023u);
   const int k = p.k;
   const uint32_t TB = tile_bytes(k);
   const uint32_t WB = (uint32_t)k * k * 2;
   const uint32_t KC = kcols(k);
-  const int NOP = 2 * p.nplanes;  // operand tiles per row tile
+  const int NDL = 2 * p.nplanes;          // gradient operand tiles per row tile
+  const int NOP = NDL + (ADD_MMA ? 1 : 0);  // operand tiles per row tile
   uint8_t* s_w[2] = {smem, smem + WB};
-  uint8_t* s_in = smem + 2 * WB;
+  uint8_t* s_id = smem + 2 * WB;  // the identity slabs (ADD_MMA)
+  uint8_t* s_in = s_id + (ADD_MMA ? ID_BYTES : 0u);
   uint8_t* s_ring = s_in + stages * TB;  // the epilogue warps' box rings (1024-byte aligned)
   uint64_t* bars = reinterpret_cast<uint64_t*>(s_ring + 4 * p.nsets * ring_bytes(p.bi, 1));
   uint64_t* w_full = bars;
@@ -402,6 +418,7 @@ __global__ void __launch_bounds__(NTHREADS_MAX, 1)
   int my_tiles = 0;
   for (int n = rr; n < ntiles; n += p.P) ++my_tiles;
 
+  if (ADD_MMA) tc::write_identity_sw32(s_id, 32);
   if (threadIdx.x == 0) {
     tc::mbar_init(w_full, 1);
     for (int s = 0; s < stages; ++s) {
@@ -443,17 +460,23 @@ __global__ void __launch_bounds__(NTHREADS_MAX, 1)
           const int st = u % stages;
           if (!(ok = ctl.wait(&in_empty[st], ((u / stages) & 1) ^ 1u))) break;
           uint8_t* buf = s_in + st * TB;
-          const int m = o / p.nplanes, pl = o % p.nplanes;
           tc::mbar_expect_tx(&in_full[st], TB);
-          for (int s = 0; s < k / 16; ++s)
-            tc::tma_load_3d(buf + s * SLAB, m ? &tm_dlx : &tm_dla, &in_full[st],
-                            blk * k + 16 * s, row0, pl);
+          if (o < NDL) {
+            const int m = o / p.nplanes, pl = o % p.nplanes;
+            for (int s = 0; s < k / 16; ++s)
+              tc::tma_load_3d(buf + s * SLAB, m ? &tm_dlx : &tm_dla, &in_full[st],
+                              blk * k + 16 * s, row0, pl);
+          } else {  // the addend tile
+            for (int s = 0; s < k / 16; ++s)
+              tc::tma_load_2d(buf + s * SLAB, &tm_add, &in_full[st], blk * k + 16 * s, row0);
+          }
         }
       }
     }
   } else if (warp == 1) {
     const bool leader = tc::elect_one();
     const uint32_t idesc = tc::idesc_bf16(TR, k, 0, 0);  // A = dl K-major, B = W K-major
+    const uint32_t idesc32 = tc::idesc_bf16(TR, 32, 0, 0);  // A = addend, B = identity slab
     ctl.wait(w_full, 0);
     int u = 0;
     for (int it = 0; it < my_tiles; ++it) {
@@ -469,12 +492,20 @@ __global__ void __launch_bounds__(NTHREADS_MAX, 1)
         }
         tc::tc_fence_after();
         const uint32_t a0 = tc::smem_u32(s_in + st * TB);
-        const uint32_t w0 = tc::smem_u32(s_w[o / p.nplanes]);
         if (leader) {
-          for (int kk = 0; kk < k / 16; ++kk)
-            tc::mma_bf16(tmem + slot * KC, tc::smem_desc_sw32(a0 + kk * SLAB, 16, 256),
-                         tc::smem_desc_sw32(w0 + kk * (k * 32), 16, 256), idesc,
-                         (o > 0 || kk > 0) ? 1u : 0u);
+          if (o < NDL) {
+            const uint32_t w0 = tc::smem_u32(s_w[o / p.nplanes]);
+            for (int kk = 0; kk < k / 16; ++kk)
+              tc::mma_bf16(tmem + slot * KC, tc::smem_desc_sw32(a0 + kk * SLAB, 16, 256),
+                           tc::smem_desc_sw32(w0 + kk * (k * 32), 16, 256), idesc,
+                           (o > 0 || kk > 0) ? 1u : 0u);
+          } else {  // the addend tile
+            const uint32_t i0 = tc::smem_u32(s_id);
+            for (int kk = 0; kk < k / 16; ++kk)
+              tc::mma_bf16(tmem + slot * KC + 32 * (kk >> 1),
+                           tc::smem_desc_sw32(a0 + kk * SLAB, 16, 256),
+                           tc::smem_desc_sw32(i0 + (kk & 1) * 1024, 16, 256), idesc32, 1u);
+          }
           tc::mma_commit(&in_empty[st]);
         }
         __syncwarp();
@@ -503,11 +534,11 @@ __global__ void __launch_bounds__(NTHREADS_MAX, 1)
       const AT* arow = static_cast<const AT*>(p.add) + (size_t)row * p.W + (size_t)blk * k;
       // the addend's first NA chunks of this warp are requested before the accumulator is
       // waited for, each later one NA chunks ahead of its use (a rolling window of registers)
-      constexpr int NA = sizeof(AT) == 4 ? 3 : 5;
+      constexpr int NA = ADD_MMA ? 1 : 3;
       AddChunk<AT> add[NA];
 #pragma unroll
       for (int j = 0; j < NA; ++j)
-        if (chunk(j) < NC) add[j].load(arow, chunk(j), in);
+        if (!ADD_MMA && chunk(j) < NC) add[j].load(arow, chunk(j), in);
       if (!ctl.wait(&acc_full[slot], (it >> 1) & 1)) break;
       tc::tc_fence_after();
       const uint32_t ta = tmem + ((uint32_t)(32 * q) << 16) + slot * KC;
@@ -521,8 +552,10 @@ __global__ void __launch_bounds__(NTHREADS_MAX, 1)
         tc::reg_fence(v[j & 1]);
         if (chunk(j + 1) < NC) tc::tmem_ld16(ta + 16 * chunk(j + 1), v[(j + 1) & 1]);
         float (&vv)[16] = v[j & 1];
-        add[j % NA].add_to(vv);
-        if (chunk(j + NA) < NC) add[j % NA].load(arow, chunk(j + NA), in);
+        if (!ADD_MMA) {
+          add[j % NA].add_to(vv);
+          if (chunk(j + NA) < NC) add[j % NA].load(arow, chunk(j + NA), in);
+        }
         bs.begin(c);
         bs.put(c, 0, vv);
         bs.end(c, &tm_dx, blk * k, y0);
@@ -544,14 +577,16 @@ __global__ void __launch_bounds__(NTHREADS_MAX, 1)
 // ================================================================ dW, db of the projections
 // CTA (blk, g, r): matrix group g (both matrices when nmat = 2, else matrix g) over the row
 // tiles r, r + P, ...  Per tile the x tile and the group's gradient operand tiles pass through
-// a ring of buffers; dW += x^T dl (M = input channel i in steps of 128, N = j) and db += 1^T dl
-// (an all-ones A operand: every lane of that accumulator holds the column sums) accumulate in
-// TMEM over the CTA's tiles; at the end the epilogue warps write the CTA's partial sums, which
+// a ring of buffers; dW += x^T dl (M = input channel i in steps of 128, N = j) and db += dl^T 1
+// (M = j in steps of 128, N = 16 columns of ones: column 0 of that accumulator holds the column
+// sums of dl) accumulate in TMEM over the CTA's tiles; at the end the epilogue warps write the
+// CTA's partial sums (dW through their box rings in the drained operand buffers), which
 // k_proj_dw_reduce adds over the CTAs in a fixed order.
 __global__ void __launch_bounds__(NTHREADS, 1)
     k_proj_dw(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_dla,
               const __grid_constant__ CUtensorMap tm_dlx,
-              const __grid_constant__ ProjParams p, int stages) {
+              const __grid_constant__ CUtensorMap tm_part, const __grid_constant__ ProjParams p,
+              int stages) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (tc::smem_u32(smem_raw) & 1023u)) & 1023u);
   const int k = p.k;
@@ -560,9 +595,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   const uint32_t KC = kcols(k);
   const int NDL = p.nmat * p.nplanes;      // gradient operand tiles per row tile
   uint8_t* s_ones = smem;                  // 128 x 16 bf16 ones, one K-major slab
-  // `stages` operand buffers of TB bytes, then a pad: the x operand of the last 128-channel
-  // row block reads MB * 8 slabs from its buffer's start, past the k / 16 loaded ones (those
-  // lanes of the accumulator are never read), so every such read stays in shared memory
+  // `stages` operand buffers of TB bytes, then a pad: an MN-major operand with M = 128 (x for
+  // dW, dl for db) reads, for the last 128-channel block, MB * 8 slabs from its buffer's start,
+  // past the k / 16 loaded ones (those lanes of the accumulator are never read), so every such
+  // read stays in shared memory
   uint8_t* s_in = smem + SLAB;
   uint64_t* bars = reinterpret_cast<uint64_t*>(s_in + stages * TB + dw_pad(k));
   uint64_t* in_full = bars;
@@ -580,8 +616,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   const int ntiles = (p.R + TR - 1) / TR;
   int my_tiles = 0;
   for (int n = rr; n < ntiles; n += p.P) ++my_tiles;
-  // TMEM per matrix of the group: MB dW accumulators (lanes = i - 128 mb) and one db
-  const uint32_t MCOLS = (uint32_t)(MB + 1) * KC;
+  // TMEM per matrix of the group: MB dW accumulators (lanes = i - 128 mb), then MB db
+  // accumulators of 32 columns (lanes = j - 128 mb, the sums in column 0)
+  const uint32_t MCOLS = dw_mcols(k);
 
   for (int e = threadIdx.x; e < (int)(SLAB / 4); e += NTHREADS)
     reinterpret_cast<uint32_t*>(s_ones)[e] = 0x3F803F80u;  // bf16 1.0 pairs
@@ -634,7 +671,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   } else if (warp == 1) {
     const bool leader = tc::elect_one();
     const uint32_t id_dw = tc::idesc_bf16(TR, k, 1, 1);  // A = x MN-major, B = dl MN-major
-    const uint32_t id_db = tc::idesc_bf16(TR, k, 0, 1);  // A = ones K-major
+    const uint32_t id_db = tc::idesc_bf16(TR, 16, 1, 0);  // A = dl MN-major, B = ones K-major
     const uint32_t ones = tc::smem_u32(s_ones);
     int u = 0;
     bool ok = true;
@@ -657,11 +694,15 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           for (int kk = 0; kk < TR / 16; ++kk) {
             const uint32_t first = (it == 0 && o % p.nplanes == 0 && kk == 0) ? 0u : 1u;
             const uint64_t bdesc = tc::smem_desc_sw32(dl + kk * 512, SLAB, 256);
-            for (int mb = 0; mb < MB; ++mb)
+            const uint64_t odesc = tc::smem_desc_sw32(ones, 16, 256);
+            for (int mb = 0; mb < MB; ++mb) {
               tc::mma_bf16(acc + mb * KC,
                            tc::smem_desc_sw32(xs + mb * 8 * SLAB + kk * 512, SLAB, 256), bdesc,
                            id_dw, first);
-            tc::mma_bf16(acc + MB * KC, tc::smem_desc_sw32(ones, 16, 256), bdesc, id_db, first);
+              tc::mma_bf16(acc + MB * KC + 32 * mb,
+                           tc::smem_desc_sw32(dl + mb * 8 * SLAB + kk * 512, SLAB, 256), odesc,
+                           id_db, first);
+            }
           }
           tc::mma_commit(&in_empty[st]);
         }
@@ -673,52 +714,52 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     if (leader) tc::mma_commit(done);
     __syncwarp();
   } else {
-    // partial sums of this CTA: dW rows i = 32 q + lane (+ 128 mb), then db from lane 0
+    // partial sums of this CTA: dW rows i = 128 mb + 32 q + lane staged in box rings laid
+    // over the drained operand buffers and stored by TMA (plane (blk P + r) 2 + m of the
+    // partials map; rows past k are clipped), then db[j = 128 mb + 32 q + lane]
     const int q = warp & 3;
     const bool ok = my_tiles == 0 || ctl.wait(done, 0);
     tc::tc_fence_after();
+    BoxStore<float> bs(s_in + (warp - 2) * ring_bytes(p.bi, 1), p.bi, 1, lane);
+    const int NC = k / 16;
     for (int mi = 0; mi < p.nmat; ++mi) {
       const int m = p.nmat == 2 ? mi : g;
-      float* dst = p.part + (((size_t)blk * p.P + rr) * 2 + m) * ((size_t)k * k + k);
+      const int z = (blk * p.P + rr) * 2 + m;
+      float* dst = p.part + (size_t)z * ((size_t)k * k + k);
       for (int mb = 0; mb < MB; ++mb) {
-        const int i = 128 * mb + 32 * q + lane;
         const uint32_t ta = tmem + ((uint32_t)(32 * q) << 16) + mi * MCOLS + mb * KC;
-        for (int c = 0; c < k / 16; ++c) {
-          float v[16];
-          if (my_tiles > 0 && ok) {
-            tc::tmem_ld16(ta + 16 * c, v);
-            tc::tmem_ld_wait();
-            tc::reg_fence(v);
-          } else {
+        float v[2][16];
+        if (my_tiles > 0 && ok) tc::tmem_ld16(ta, v[0]);
+#pragma unroll 1
+        for (int c = 0; c < NC; c += 2) {  // two chunks a step: the TMEM buffers stay static
 #pragma unroll
-            for (int e = 0; e < 16; ++e) v[e] = 0.0f;
-          }
-          if (i < k) {
-            float4* o4 = reinterpret_cast<float4*>(dst + (size_t)i * k + 16 * c);
+          for (int h = 0; h < 2; ++h) {
+            if (c + h >= NC) break;
+            if (my_tiles > 0 && ok) {
+              tc::tmem_ld_wait();
+              tc::reg_fence(v[h]);
+              if (c + h + 1 < NC) tc::tmem_ld16(ta + 16 * (c + h + 1), v[h ^ 1]);
+            } else {
 #pragma unroll
-            for (int e = 0; e < 4; ++e)
-              o4[e] = make_float4(v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
+              for (int e = 0; e < 16; ++e) v[h][e] = 0.0f;
+            }
+            bs.begin(c + h);
+            bs.put(c + h, 0, v[h]);
+            bs.end(c + h, &tm_part, 0, 128 * mb + 32 * q, z);
           }
         }
-      }
-      if (q == 0) {  // the db accumulator: every lane holds the sums; lane l writes j = l mod 32
-        const uint32_t ta = tmem + mi * MCOLS + MB * KC;
-        for (int c = 0; c < k / 16; ++c) {
-          float v[16];
-          if (my_tiles > 0 && ok) {
-            tc::tmem_ld16(ta + 16 * c, v);
-            tc::tmem_ld_wait();
-            tc::reg_fence(v);
-          } else {
-#pragma unroll
-            for (int e = 0; e < 16; ++e) v[e] = 0.0f;
-          }
-#pragma unroll
-          for (int e = 0; e < 16; ++e)
-            if (((16 * c + e) & 31) == lane) dst[(size_t)k * k + 16 * c + e] = v[e];
+        const int j = 128 * mb + 32 * q + lane;
+        float sb = 0.0f;
+        if (my_tiles > 0 && ok) {
+          float t[2];
+          tc::tmem_ld2(tmem + ((uint32_t)(32 * q) << 16) + mi * MCOLS + MB * KC + 32 * mb, t);
+          tc::tmem_ld_wait();
+          sb = t[0];
         }
+        if (j < k) dst[(size_t)k * k + j] = sb;
       }
     }
+    bs.drain();
   }
   tc::tc_fence_before();
   __syncthreads();
@@ -729,33 +770,42 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 }
 
 // dW and db: the P partial sums of every (block, matrix) added in CTA order (deterministic).
+// A thread takes four consecutive elements (k (k + 1) is a multiple of 4, and so is the
+// dW / db boundary at k k): 16-byte loads, four partials requested at a time.
 __global__ void k_proj_dw_reduce(const float* __restrict__ part, int nblk, int P, int k,
                                  float* dWa, float* dWx, float* dba, float* dbx) {
   const size_t per = (size_t)k * k + k;
-  const size_t total = (size_t)nblk * 2 * per;
-  for (size_t e = (size_t)blockIdx.x * blockDim.x + threadIdx.x; e < total;
-       e += (size_t)gridDim.x * blockDim.x) {
+  const size_t total4 = (size_t)nblk * 2 * per / 4;
+  for (size_t e4 = (size_t)blockIdx.x * blockDim.x + threadIdx.x; e4 < total4;
+       e4 += (size_t)gridDim.x * blockDim.x) {
+    const size_t e = 4 * e4;
     const size_t blk = e / (2 * per), rem = e % (2 * per);
     const int m = (int)(rem / per);
     const size_t off = rem % per;
-    const float* src = part + (blk * P * 2 + m) * per + off;
-    // four partials requested at a time, added in CTA order
-    float s = 0.0f;
+    const float4* src = reinterpret_cast<const float4*>(part + (blk * P * 2 + m) * per + off);
+    const size_t step = 2 * per / 4;  // float4s from one CTA's partials to the next
+    float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
+    auto add = [&](const float4& v) {
+      s.x += v.x;
+      s.y += v.y;
+      s.z += v.z;
+      s.w += v.w;
+    };
     int r = 0;
     for (; r + 4 <= P; r += 4) {
-      const float a0 = src[(size_t)r * 2 * per], a1 = src[(size_t)(r + 1) * 2 * per];
-      const float a2 = src[(size_t)(r + 2) * 2 * per], a3 = src[(size_t)(r + 3) * 2 * per];
-      s += a0;
-      s += a1;
-      s += a2;
-      s += a3;
+      const float4 a0 = src[r * step], a1 = src[(r + 1) * step];
+      const float4 a2 = src[(r + 2) * step], a3 = src[(r + 3) * step];
+      add(a0);
+      add(a1);
+      add(a2);
+      add(a3);
     }
-    for (; r < P; ++r) s += src[(size_t)r * 2 * per];
+    for (; r < P; ++r) add(src[r * step]);
     if (off < (size_t)k * k) {
-      (m ? dWx : dWa)[blk * k * k + off] = s;
+      *reinterpret_cast<float4*>((m ? dWx : dWa) + blk * k * k + off) = s;
     } else {
       float* db = m ? dbx : dba;
-      if (db) db[blk * k + (off - (size_t)k * k)] = s;
+      if (db) *reinterpret_cast<float4*>(db + blk * k + (off - (size_t)k * k)) = s;
     }
   }
 }
@@ -787,7 +837,7 @@ int dw_ctas_per_group(const Dims& d, int groups) {
   return std::max(1, std::min(P, ntiles));
 }
 
-int dw_nmat(const Dims& d) { return 2 * ((d.k + 127) / 128 + 1) * (int)kcols(d.k) <= 512 ? 2 : 1; }
+int dw_nmat(const Dims& d) { return 2 * dw_mcols(d.k) <= 512 ? 2 : 1; }
 
 cudaError_t weight_maps(const Dims& d, const void* Wa, const void* Wx, CUtensorMap* ma,
                         CUtensorMap* mx) {
@@ -925,15 +975,19 @@ cudaError_t launch_proj_dx(const Dims& d, int ot, const void* dlr, const void* d
   p.add_f32 = add_f32;
   p.nplanes = nplanes;
   p.bi = box_row_bytes(d.k, ot == DT_F32 ? 4 : 2);
-  CUtensorMap mdx;
+  CUtensorMap mdx, madd;
   e = out_map(d, dx, ot, 1, p.bi, &mdx);
+  // a bf16 addend enters as an operand tile (the kernel's identity product); a float32 one
+  // through the epilogue, and its map is unused
+  if (e == cudaSuccess) e = act_map(d, add_f32 ? dx : add, &madd);
   if (e != cudaSuccess) return e;
+  const size_t idb = add_f32 ? 0 : ID_BYTES;
   // two sets of epilogue warps where their box rings still leave three operand stages
   const size_t TBs = tile_bytes(d.k);
   size_t smem = 0;
   int stages = 0;
   for (p.nsets = 2; p.nsets >= 1; --p.nsets) {
-    const size_t fixed = 1024 + 2 * (size_t)d.k * d.k * 2 +
+    const size_t fixed = 1024 + 2 * (size_t)d.k * d.k * 2 + idb +
                          4 * (size_t)p.nsets * ring_bytes(p.bi, 1) + bars_bytes(5);
     stages = fixed > SMEM_MAX ? 0 : (int)std::min<size_t>(6, (SMEM_MAX - fixed) / TBs);
     smem = fixed + stages * TBs;
@@ -944,7 +998,7 @@ cudaError_t launch_proj_dx(const Dims& d, int ot, const void* dlr, const void* d
                            : (add_f32 ? k_proj_dx<bf16, float> : k_proj_dx<bf16, bf16>);
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  kern<<<p.P * d.nblk, 64 + 128 * p.nsets, smem, s>>>(mdla, mdlx, mwa, mwx, mdx, p, stages);
+  kern<<<p.P * d.nblk, 64 + 128 * p.nsets, smem, s>>>(mdla, mdlx, mwa, mwx, mdx, madd, p, stages);
   note_launches(1);
   return cudaGetLastError();
 }
@@ -968,6 +1022,18 @@ cudaError_t launch_proj_dw(const Dims& d, const void* x, const void* dlr, const 
   const int groups = 2 / p.nmat;
   p.P = dw_ctas_per_group(d, d.nblk * groups);
   p.part = part;
+  // the partial sums [nblk P 2 planes][k + 1 rows][k]: dW in the first k rows of a plane,
+  // stored in boxes of 32 rows (rows past k clipped); db in the last row, by plain stores
+  p.bi = box_row_bytes(d.k, 4);
+  CUtensorMap mpart;
+  {
+    const uint64_t dims[3] = {(uint64_t)d.k, (uint64_t)d.k, (uint64_t)d.nblk * p.P * 2};
+    const uint64_t str[2] = {(uint64_t)d.k * 4, ((uint64_t)d.k * d.k + d.k) * 4};
+    const uint32_t box[3] = {(uint32_t)(p.bi / 4), 32, 1};
+    e = encode_tmap(&mpart, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, part, dims, str, box,
+                    p.bi == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B);
+    if (e != cudaSuccess) return e;
+  }
   const size_t TB = tile_bytes(d.k);
   const size_t fixed = 1024 + SLAB + dw_pad(d.k) + bars_bytes(1);
   // all operands of one row tile (x and the group's gradient planes) are held at once
@@ -976,14 +1042,16 @@ cudaError_t launch_proj_dw(const Dims& d, const void* x, const void* dlr, const 
   while (stages > need && fixed + stages * TB + 16 * stages > SMEM_MAX) --stages;
   const size_t smem = fixed + stages * TB + 16 * stages;
   if (smem > SMEM_MAX) return cudaErrorNotSupported;
+  // the epilogue's box rings lie over the drained operand buffers
+  if (4 * (size_t)ring_bytes(p.bi, 1) > stages * TB) return cudaErrorNotSupported;
   e = cudaFuncSetAttribute(k_proj_dw, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  k_proj_dw<<<p.P * d.nblk * groups, NTHREADS, smem, s>>>(mx, mdla, mdlx, p, stages);
+  k_proj_dw<<<p.P * d.nblk * groups, NTHREADS, smem, s>>>(mx, mdla, mdlx, mpart, p, stages);
   note_launches(1);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  const size_t total = (size_t)d.nblk * 2 * ((size_t)d.k * d.k + d.k);
-  const int rgrid = (int)std::min<size_t>((total + 255) / 256, 4096);
+  const size_t total4 = (size_t)d.nblk * 2 * ((size_t)d.k * d.k + d.k) / 4;
+  const int rgrid = (int)std::min<size_t>((total4 + 255) / 256, 4096);
   k_proj_dw_reduce<<<rgrid, 256, 0, s>>>(part, d.nblk, p.P, d.k, dWa, dWx, dba, dbx);
   note_launches(1);
   return cudaGetLastError();
