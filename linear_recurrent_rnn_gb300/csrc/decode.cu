@@ -18,9 +18,10 @@
 // Large batches (bf16, B >= STEP_TC_MIN_B, k a multiple of 32) take k_step_tc instead: the step
 // is then a [B x k] x [k x k] product per gate block and matrix, which goes to the tcgen05
 // tensor cores.  CTA = (128-row tile, gate block, 32-channel slice): TMA brings the x tile
-// (16-channel slabs, 32-byte swizzle) and the two 32-column weight slices, one thread issues
-// the k / 16 MMAs of M = 128 rows x N = 32 channels per matrix into TMEM, and each of the four
-// warps then takes its 32 rows (its TMEM lane quadrant): lr, li from TMEM, x from the staged
+// (16-channel slabs, 32-byte swizzle) and the two 32-column weight slices, issued by the thread
+// that initialises the barriers before anything else; one thread issues the k / 16 MMAs of
+// M = 128 rows x N = 32 channels per matrix into TMEM, and each of the eight warps then takes
+// 32 rows (its TMEM lane quadrant) and 16 of the channels: lr, li from TMEM, x from the staged
 // tile, the state row requested before the MMA wait, and the same gate arithmetic as k_step.
 #include <cudaTypedefs.h>
 
@@ -219,10 +220,11 @@ __global__ void __launch_bounds__(DEC_WARPS * 32) k_step(DecArgs a) {
 
 // ---------------------------------------------------------------- tensor-core step
 constexpr int STC_ROWS = 128;
-constexpr int STC_N = 32;  // channels per CTA
+constexpr int STC_N = 32;                     // channels per CTA
+constexpr int STC_THREADS = 256;              // 8 warps: 4 lane quadrants x 2 channel halves
 constexpr uint32_t STC_SLAB = STC_ROWS * 32;  // 16 channels x 128 rows of x
 
-__global__ void __launch_bounds__(128, 1)
+__global__ void __launch_bounds__(STC_THREADS, 1)
     k_step_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_wa,
               const __grid_constant__ CUtensorMap tm_wx, const __grid_constant__ DecArgs a) {
   extern __shared__ uint8_t smem_raw[];
@@ -242,26 +244,11 @@ __global__ void __launch_bounds__(128, 1)
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 2);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
+  // the operand loads go out first: thread 0 initialises the barriers and issues them at once
   if (threadIdx.x == 0) {
     tc::mbar_init(full, 1);
     tc::mbar_init(done, 1);
     tc::fence_barrier_init();
-  }
-  if (warp == 0) {
-    tc::tmem_alloc(tmem_holder, 2 * STC_N);
-    tc::tmem_relinquish();
-  }
-  if (threadIdx.x < STC_N) {
-    const int w = blk * k + j0 + threadIdx.x;
-    s_c[threadIdx.x] = -8.0f * softplus_f(a.Lambda[w]);
-    s_c[STC_N + threadIdx.x] = a.ba ? a.ba[w] : 0.0f;
-    s_c[2 * STC_N + threadIdx.x] = a.bx ? a.bx[w] : 0.0f;
-  }
-  tc::tc_fence_before();
-  __syncthreads();
-  tc::tc_fence_after();
-  const uint32_t tmem = *tmem_holder;
-  if (threadIdx.x == 0) {
     tc::mbar_expect_tx(full, XB + 4 * WS);
     for (int s = 0; s < k / 16; ++s)
       tc::tma_load_2d(s_x + s * STC_SLAB, &tm_x, full, blk * k + 16 * s, row0);
@@ -269,17 +256,32 @@ __global__ void __launch_bounds__(128, 1)
       for (int s = 0; s < 2; ++s)
         tc::tma_load_2d(s_w[m] + s * WS, m ? &tm_wx : &tm_wa, full, j0 + 16 * s, blk * k);
   }
-  // this thread's row: its state segment and reset flag, requested before any wait
-  const int q = warp & 3;
+  if (warp == 1) {
+    tc::tmem_alloc(tmem_holder, 2 * STC_N);
+    tc::tmem_relinquish();
+  }
+  // this thread's row and 16 channels: state segment, reset flag, and (warp 2) the channel
+  // constants, all requested before any wait
+  const int q = warp & 3, hf = warp >> 2;
   const int row = row0 + 32 * q + lane;
   const bool live = row < a.B;
-  const size_t o = (size_t)row * a.W + (size_t)blk * k + j0;
-  float4 hp[STC_N / 4];
+  const size_t o = (size_t)row * a.W + (size_t)blk * k + j0 + 16 * hf;
+  float4 hp[4];
 #pragma unroll
-  for (int e = 0; e < STC_N / 4; ++e)
+  for (int e = 0; e < 4; ++e)
     hp[e] = (live && a.h_in) ? reinterpret_cast<const float4*>(a.h_in + o)[e]
                              : make_float4(0.f, 0.f, 0.f, 0.f);
   const bool rst = live && a.canonical && a.reset && a.reset[row] != 0;
+  if (warp == 2) {
+    const int w = blk * k + j0 + lane;
+    s_c[lane] = -8.0f * softplus_f(a.Lambda[w]);
+    s_c[STC_N + lane] = a.ba ? a.ba[w] : 0.0f;
+    s_c[2 * STC_N + lane] = a.bx ? a.bx[w] : 0.0f;
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
   if (warp == 0) {
     const bool leader = tc::elect_one();
     const bool ok = tc::mbar_wait(full, 0, 2000000000ull);
@@ -299,48 +301,39 @@ __global__ void __launch_bounds__(128, 1)
   }
   const bool ok = tc::mbar_wait(done, 0, 2000000000ull);
   tc::tc_fence_after();
-  float lr[STC_N], li[STC_N];
+  float lr[16], li[16];
   {
-    float t[16];
-    const uint32_t ta = tmem + ((uint32_t)(32 * q) << 16);
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      tc::tmem_ld16(ta + 16 * h, t);
-      tc::tmem_ld_wait();
-#pragma unroll
-      for (int e = 0; e < 16; ++e) lr[16 * h + e] = t[e];
-      tc::tmem_ld16(ta + STC_N + 16 * h, t);
-      tc::tmem_ld_wait();
-#pragma unroll
-      for (int e = 0; e < 16; ++e) li[16 * h + e] = t[e];
-    }
+    const uint32_t ta = tmem + ((uint32_t)(32 * q) << 16) + 16 * hf;
+    tc::tmem_ld16(ta, lr);
+    tc::tmem_ld16(ta + STC_N, li);
+    tc::tmem_ld_wait();
+    tc::reg_fence(lr);
+    tc::reg_fence(li);
   }
   if (live && ok) {
-    // x of the row's 32 channels from the staged tile: two slabs, 32-byte rows whose 16-byte
+    // x of the row's 16 channels from the staged tile: one slab, a 32-byte row whose 16-byte
     // halves are swapped on rows 4..7 of every 8
     const int r = 32 * q + lane;
-    float xv[STC_N];
+    float xv[16];
 #pragma unroll
-    for (int s = 0; s < 2; ++s) {
+    for (int hh = 0; hh < 2; ++hh) {
+      const uint4 u = *reinterpret_cast<const uint4*>(
+          s_x + (j0 / 16 + hf) * STC_SLAB + r * 32 + ((hh ^ ((r >> 2) & 1)) << 4));
+      const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-        const uint4 u = *reinterpret_cast<const uint4*>(
-            s_x + (j0 / 16 + s) * STC_SLAB + r * 32 + ((hh ^ ((r >> 2) & 1)) << 4));
-        const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          xv[16 * s + 8 * hh + 2 * e] = __uint_as_float(w4[e] << 16);
-          xv[16 * s + 8 * hh + 2 * e + 1] = __uint_as_float(w4[e] & 0xffff0000u);
-        }
+      for (int e = 0; e < 4; ++e) {
+        xv[8 * hh + 2 * e] = __uint_as_float(w4[e] << 16);
+        xv[8 * hh + 2 * e + 1] = __uint_as_float(w4[e] & 0xffff0000u);
       }
     }
     const float* hpf = reinterpret_cast<const float*>(hp);
-    float hn[STC_N];
+    float hn[16];
 #pragma unroll
-    for (int c = 0; c < STC_N; ++c) {
-      const float rg = sigmoid_f(lr[c] + s_c[STC_N + c]);
-      const float ig = sigmoid_f(li[c] + s_c[2 * STC_N + c]);
-      const float la = s_c[c] * rg;
+    for (int c = 0; c < 16; ++c) {
+      const int cc = 16 * hf + c;
+      const float rg = sigmoid_f(lr[c] + s_c[STC_N + cc]);
+      const float ig = sigmoid_f(li[c] + s_c[2 * STC_N + cc]);
+      const float la = s_c[cc] * rg;
       float abar = expf(la);
       float m = sqrtf(one_minus_a2(la));
       if (rst) {
@@ -350,11 +343,11 @@ __global__ void __launch_bounds__(128, 1)
       hn[c] = fmaf(abar, hpf[c], m * (ig * xv[c]));
     }
 #pragma unroll
-    for (int e = 0; e < STC_N / 4; ++e)
+    for (int e = 0; e < 4; ++e)
       reinterpret_cast<float4*>(a.h_out + o)[e] =
           make_float4(hn[4 * e], hn[4 * e + 1], hn[4 * e + 2], hn[4 * e + 3]);
 #pragma unroll
-    for (int e = 0; e < STC_N / 8; ++e) {
+    for (int e = 0; e < 2; ++e) {
       uint4 u;
       uint32_t* pu = &u.x;
 #pragma unroll
@@ -367,7 +360,7 @@ __global__ void __launch_bounds__(128, 1)
   }
   tc::tc_fence_before();
   __syncthreads();
-  if (warp == 0) {
+  if (warp == 1) {
     tc::tc_fence_after();
     tc::tmem_dealloc(tmem, 2 * STC_N);
   }
@@ -425,7 +418,7 @@ cudaError_t launch_step(const Dims& d, const void* x, const void* Wa, const floa
     e = cudaFuncSetAttribute(k_step_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     const dim3 grid((unsigned)(d.nblk * (d.k / STC_N)), (unsigned)((d.B + STC_ROWS - 1) / STC_ROWS));
-    k_step_tc<<<grid, 128, smem, s>>>(mx, mwa, mwx, a);
+    k_step_tc<<<grid, STC_THREADS, smem, s>>>(mx, mwa, mwx, a);
     note_launches(1);
     return cudaGetLastError();
   }
