@@ -296,11 +296,14 @@ rglru_status rglru_gate_proj_backward(const rglru_shape* shape, const void* dlr,
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   if (proj_tc_supported(d) && d.grad == RGLRU_BF16) {
     // one bf16 plane per gradient; dx accumulates in place
-    cudaError_t e = launch_proj_dx(d, DT_BF16, dlr, dli, d.N, 1, Wa, Wx, dx, 0, dx, stream);
+    // dx and dW side by side where one wave of CTAs holds both grids
+    const ProjBwdSplit sp = proj_bwd_split(d);
+    cudaError_t e =
+        launch_proj_dx(d, DT_BF16, dlr, dli, d.N, 1, Wa, Wx, dx, 0, dx, stream, sp.P_dx);
     if (e == cudaSuccess)
       e = launch_proj_dw(d, x, dlr, dli, d.N, 1,
                          reinterpret_cast<float*>(ws + PROJ_PART_OFFSET), dWa, dba, dWx, dbx,
-                         stream);
+                         stream, sp.P_dw);
     return cuda_status(e);
   }
   cudaError_t e =

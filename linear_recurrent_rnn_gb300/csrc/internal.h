@@ -325,15 +325,22 @@ cudaError_t launch_step(const Dims& d, const void* x, const void* Wa, const floa
 constexpr int PROJ_TC_KMAX = 160;
 bool proj_tc_supported(const Dims& d);
 size_t proj_dw_part_bytes(const Dims& d);
+// CTAs per gate block of the dx and dW kernels when the two run side by side (the dW kernel
+// launched as a programmatic dependent of the dx one); {0, 0}: not on one wave, run them one
+// after the other with the default P.
+struct ProjBwdSplit {
+  int P_dx, P_dw;
+};
+ProjBwdSplit proj_bwd_split(const Dims& d);
 cudaError_t launch_proj_fwd(const Dims& d, int ot, const void* x, const void* Wa,
                             const float* ba, const void* Wx, const float* bx, void* lr, void* li,
                             cudaStream_t s);
 cudaError_t launch_proj_dx(const Dims& d, int ot, const void* dlr, const void* dli,
                            size_t plane_elems, int nplanes, const void* Wa, const void* Wx,
-                           const void* add, int add_f32, void* dx, cudaStream_t s);
+                           const void* add, int add_f32, void* dx, cudaStream_t s, int P = 0);
 cudaError_t launch_proj_dw(const Dims& d, const void* x, const void* dlr, const void* dli,
                            size_t plane_elems, int nplanes, float* part, float* dWa, float* dba,
-                           float* dWx, float* dbx, cudaStream_t s);
+                           float* dWx, float* dbx, cudaStream_t s, int P = 0);
 
 // SIMT projections (float32 accumulation).
 cudaError_t launch_gate_proj_simt(const Dims& d, int xt, int ot, const void* x, const void* Wa,

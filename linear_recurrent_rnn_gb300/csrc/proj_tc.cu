@@ -418,6 +418,9 @@ __global__ void __launch_bounds__(NTHREADS_MAX, 1)
   int my_tiles = 0;
   for (int n = rr; n < ntiles; n += p.P) ++my_tiles;
 
+  // the dW kernel launched after this one reads none of its outputs: it may start at once on
+  // the SMs this grid leaves free (programmatic dependent launch)
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (ADD_MMA) tc::write_identity_sw32(s_id, 32);
   if (threadIdx.x == 0) {
     tc::mbar_init(w_full, 1);
@@ -903,6 +906,21 @@ bool proj_tc_supported(const Dims& d) {
          sm_count() > 0;
 }
 
+ProjBwdSplit proj_bwd_split(const Dims& d) {
+  // dx and dW side by side on one wave of CTAs: the P_dx + groups P_dw CTAs of a gate block fit
+  // the SMs, dW's share near its share of the bytes moved (~45 %), and no dW accumulator takes
+  // more than DW_TILES_MAX row tiles
+  ProjBwdSplit sp = {0, 0};
+  const int groups = 2 / dw_nmat(d);
+  const int q = sm_count() / d.nblk;
+  const int ntiles = (d.B * d.T + TR - 1) / TR;
+  const int pmin = (ntiles + DW_TILES_MAX - 1) / DW_TILES_MAX;
+  const int pdw = std::max(pmin, (int)(0.45 * q) / groups);
+  const int pdx = q - groups * pdw;
+  if (pdw >= 1 && pdx >= 1 && pdw <= dw_ctas_per_group(d, d.nblk * groups)) sp = {pdx, pdw};
+  return sp;
+}
+
 size_t proj_dw_part_bytes(const Dims& d) {
   const int P = dw_ctas_per_group(d, d.nblk * (2 / dw_nmat(d)));
   return (size_t)d.nblk * P * 2 * ((size_t)d.k * d.k + d.k) * 4;
@@ -958,7 +976,7 @@ cudaError_t launch_proj_fwd(const Dims& d, int ot, const void* x, const void* Wa
 
 cudaError_t launch_proj_dx(const Dims& d, int ot, const void* dlr, const void* dli,
                            size_t plane_elems, int nplanes, const void* Wa, const void* Wx,
-                           const void* add, int add_f32, void* dx, cudaStream_t s) {
+                           const void* add, int add_f32, void* dx, cudaStream_t s, int P) {
   if (!proj_tc_supported(d)) return cudaErrorNotSupported;
   CUtensorMap mdla, mdlx, mwa, mwx;
   cudaError_t e = planes_map(d, dlr, plane_elems, nplanes, &mdla);
@@ -970,7 +988,7 @@ cudaError_t launch_proj_dx(const Dims& d, int ot, const void* dlr, const void* d
   p.k = d.k;
   p.nblk = d.nblk;
   p.W = d.W;
-  p.P = ctas_per_group(d.nblk);
+  p.P = P > 0 ? P : ctas_per_group(d.nblk);
   p.add = add;
   p.add_f32 = add_f32;
   p.nplanes = nplanes;
@@ -1005,7 +1023,7 @@ cudaError_t launch_proj_dx(const Dims& d, int ot, const void* dlr, const void* d
 
 cudaError_t launch_proj_dw(const Dims& d, const void* x, const void* dlr, const void* dli,
                            size_t plane_elems, int nplanes, float* part, float* dWa, float* dba,
-                           float* dWx, float* dbx, cudaStream_t s) {
+                           float* dWx, float* dbx, cudaStream_t s, int P) {
   if (!proj_tc_supported(d)) return cudaErrorNotSupported;
   CUtensorMap mx, mdla, mdlx;
   cudaError_t e = act_map(d, x, &mx);
@@ -1020,7 +1038,9 @@ cudaError_t launch_proj_dw(const Dims& d, const void* x, const void* dlr, const 
   p.nplanes = nplanes;
   p.nmat = dw_nmat(d);
   const int groups = 2 / p.nmat;
-  p.P = dw_ctas_per_group(d, d.nblk * groups);
+  // P given: the split of proj_bwd_split, next to a running dx grid (programmatic launch)
+  const bool beside = P > 0;
+  p.P = beside ? P : dw_ctas_per_group(d, d.nblk * groups);
   p.part = part;
   // the partial sums [nblk P 2 planes][k + 1 rows][k]: dW in the first k rows of a plane,
   // stored in boxes of 32 rows (rows past k clipped); db in the last row, by plain stores
@@ -1046,10 +1066,24 @@ cudaError_t launch_proj_dw(const Dims& d, const void* x, const void* dlr, const 
   if (4 * (size_t)ring_bytes(p.bi, 1) > stages * TB) return cudaErrorNotSupported;
   e = cudaFuncSetAttribute(k_proj_dw, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  k_proj_dw<<<p.P * d.nblk * groups, NTHREADS, smem, s>>>(mx, mdla, mdlx, mpart, p, stages);
-  note_launches(1);
-  e = cudaGetLastError();
+  if (beside) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(p.P * d.nblk * groups);
+    cfg.blockDim = dim3(NTHREADS);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, k_proj_dw, mx, mdla, mdlx, mpart, p, stages);
+  } else {
+    k_proj_dw<<<p.P * d.nblk * groups, NTHREADS, smem, s>>>(mx, mdla, mdlx, mpart, p, stages);
+    e = cudaGetLastError();
+  }
   if (e != cudaSuccess) return e;
+  note_launches(1);
   const size_t total4 = (size_t)d.nblk * 2 * ((size_t)d.k * d.k + d.k) / 4;
   const int rgrid = (int)std::min<size_t>((total4 + 255) / 256, 4096);
   k_proj_dw_reduce<<<rgrid, 256, 0, s>>>(part, d.nblk, p.P, d.k, dWa, dWx, dba, dbx);
