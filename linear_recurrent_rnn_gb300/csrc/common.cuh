@@ -220,6 +220,33 @@ __device__ __forceinline__ void gates_any2(float2 lr, float2 li, const GateK& k,
   }
 }
 
+// One channel's gates by the same arithmetic, scalar (the decode step: one token a channel,
+// each channel with its own constants).
+__device__ __forceinline__ void gates_any1(float lr, float li, const GateK& k, float& a,
+                                           float& mi, float& i) {
+  const float zr = fminf(fmaf(lr, -LOG2E, k.nbr), GATE_ZR_MAX);
+  const float zi = fminf(fmaf(li, -LOG2E, k.nbi), GATE_ZI_MAX);
+  const float pr = ex2_approx(zr) + 1.0f, pi = ex2_approx(zi) + 1.0f;
+  const float t = rsqrt_approx(pr * pi * pi);
+  const float s = t * pi;
+  const float r = s * s;
+  i = t * s * pr;
+  const float la = k.nk * r;
+  if (la > NEAR_LA) {
+    float p = fmaf(la, DECAY_P3, DECAY_P2);
+    p = fmaf(la, p, DECAY_P1);
+    p = fmaf(la, p, 1.0f);
+    a = fmaf(la, p, 1.0f);
+    float q = fmaf(la, MULT_Q3, MULT_Q2);
+    q = fmaf(la, q, MULT_Q1);
+    q = fmaf(la, q, 1.0f);
+    mi = k.cm * t * q;
+  } else {
+    a = ex2_approx(la * LOG2E);
+    mi = sqrt_approx(fmaf(-a, a, 1.0f)) * i;
+  }
+}
+
 // ---------------------------------------------------------------- staged bf16 tiles
 // A [token][channel] bf16 tile staged by TMA as slabs of 16 channels x 32-byte token rows with
 // the 32-byte swizzle (the row's two 16-byte halves swap on rows 4..7 of every 8).  b0 / b1

@@ -22,7 +22,8 @@
 // that initialises the barriers before anything else; one thread issues the k / 16 MMAs of
 // M = 128 rows x N = 32 channels per matrix into TMEM, and each of the eight warps then takes
 // 32 rows (its TMEM lane quadrant) and 16 of the channels: lr, li from TMEM, x from the staged
-// tile, the state row requested before the MMA wait, and the same gate arithmetic as k_step.
+// tile, the state row requested before the MMA wait, and the gate arithmetic of the fused bf16
+// kernels (two ex2 and one rsqrt a channel, gates_any1).
 #include <cudaTypedefs.h>
 
 #include "common.cuh"
@@ -237,8 +238,8 @@ __global__ void __launch_bounds__(STC_THREADS, 1)
   const uint32_t WS = (uint32_t)k * 32;                // one 16-column weight slab
   uint8_t* s_x = smem;
   uint8_t* s_w[2] = {smem + XB, smem + XB + 2 * WS};
-  float* s_c = reinterpret_cast<float*>(smem + XB + 4 * WS);  // per channel: nk, ba, bx
-  uint64_t* bars = reinterpret_cast<uint64_t*>(s_c + 3 * STC_N);
+  GateK* s_c = reinterpret_cast<GateK*>(smem + XB + 4 * WS);  // per channel
+  uint64_t* bars = reinterpret_cast<uint64_t*>(s_c + STC_N);
   uint64_t* full = bars;
   uint64_t* done = bars + 1;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 2);
@@ -274,9 +275,12 @@ __global__ void __launch_bounds__(STC_THREADS, 1)
   const bool rst = live && a.canonical && a.reset && a.reset[row] != 0;
   if (warp == 2) {
     const int w = blk * k + j0 + lane;
-    s_c[lane] = -8.0f * softplus_f(a.Lambda[w]);
-    s_c[STC_N + lane] = a.ba ? a.ba[w] : 0.0f;
-    s_c[2 * STC_N + lane] = a.bx ? a.bx[w] : 0.0f;
+    GateK g;
+    g.nk = -8.0f * softplus_f(a.Lambda[w]);
+    g.cm = sqrtf(-2.0f * g.nk);
+    g.nbr = a.ba ? -a.ba[w] * LOG2E : 0.0f;  // the biases folded into the exponents
+    g.nbi = a.bx ? -a.bx[w] * LOG2E : 0.0f;
+    s_c[lane] = g;
   }
   tc::tc_fence_before();
   __syncthreads();
@@ -330,17 +334,13 @@ __global__ void __launch_bounds__(STC_THREADS, 1)
     float hn[16];
 #pragma unroll
     for (int c = 0; c < 16; ++c) {
-      const int cc = 16 * hf + c;
-      const float rg = sigmoid_f(lr[c] + s_c[STC_N + cc]);
-      const float ig = sigmoid_f(li[c] + s_c[2 * STC_N + cc]);
-      const float la = s_c[cc] * rg;
-      float abar = expf(la);
-      float m = sqrtf(one_minus_a2(la));
-      if (rst) {
+      float abar, mi, ig;
+      gates_any1(lr[c], li[c], s_c[16 * hf + c], abar, mi, ig);
+      if (rst) {  // canonical reset row: abar = 0, m = 1
         abar = 0.0f;
-        m = 1.0f;
+        mi = ig;
       }
-      hn[c] = fmaf(abar, hpf[c], m * (ig * xv[c]));
+      hn[c] = fmaf(abar, hpf[c], mi * xv[c]);
     }
 #pragma unroll
     for (int e = 0; e < 4; ++e)
@@ -414,7 +414,7 @@ cudaError_t launch_step(const Dims& d, const void* x, const void* Wa, const floa
                       CU_TENSOR_MAP_SWIZZLE_32B);
     if (e != cudaSuccess) return e;
     const size_t smem = 1024 + (size_t)(d.k / 16) * STC_SLAB + 4 * (size_t)d.k * 32 +
-                        3 * STC_N * 4 + 64;
+                        STC_N * sizeof(GateK) + 64;
     e = cudaFuncSetAttribute(k_step_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     const dim3 grid((unsigned)(d.nblk * (d.k / STC_N)), (unsigned)((d.B + STC_ROWS - 1) / STC_ROWS));
