@@ -170,7 +170,7 @@ def measured_peaks():
 # dram__bytes_write.sum from one ncu capture; writes still resident in L2 when the kernel
 # ends are not counted).  It holds for the kernel sources whose hash is recorded beside it;
 # when they have changed since, the line reports null until the counters are taken again.
-TRAFFIC = {"bytes": 70504192 + 9548032, "sources_sha16": "67423dbcd90582de"}
+TRAFFIC = {"bytes": 70508800 + 12798976, "sources_sha16": "cab2b1edac0e3e7d"}
 KERNEL_SOURCES = ("fused_bwd.cu", "tc.cuh", "common.cuh", "lookback.cuh", "internal.h")
 
 
