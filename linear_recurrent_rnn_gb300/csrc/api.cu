@@ -98,11 +98,17 @@ ComposedLayout composed_saved(const Dims& d) {
 // Scratch of the projection backward inside a workspace: the SIMT kernels' partial sums, or
 // the tensor-core kernels' per-CTA dW / db partials, both after a 256-byte header (a scan
 // backward run on the same workspace keeps its status word there).
+// With float32 gradients the tensor-core route first splits dlr and dli into bf16 hi + lo
+// planes, kept after the partials.
 constexpr size_t PROJ_PART_OFFSET = 256;
+size_t gate_planes_offset(const Dims& d) {
+  return align_up(PROJ_PART_OFFSET + proj_dw_part_bytes(d), 256);
+}
 size_t gate_bwd_ws_bytes(const Dims& d) {
   size_t a = gate_bwd_layout(d).total;
   if (proj_tc_supported(d)) {
-    const size_t b = PROJ_PART_OFFSET + proj_dw_part_bytes(d);
+    size_t b = PROJ_PART_OFFSET + proj_dw_part_bytes(d);
+    if (d.grad == RGLRU_F32) b = gate_planes_offset(d) + 2 * (size_t)d.N * 4;
     if (b > a) a = b;
   }
   return a;
@@ -294,16 +300,26 @@ rglru_status rglru_gate_proj_backward(const rglru_shape* shape, const void* dlr,
       !req(dWx) || !opt(dba) || !opt(dbx) || !req(workspace))
     return RGLRU_ERR_INVALID_ARG;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
-  if (proj_tc_supported(d) && d.grad == RGLRU_BF16) {
-    // one bf16 plane per gradient; dx accumulates in place
-    // dx and dW side by side where one wave of CTAs holds both grids
+  if (proj_tc_supported(d)) {
+    // dx accumulates in place; dx and dW run side by side where one wave of CTAs holds both
+    // grids.  bf16 gradients: one plane each; float32: split into bf16 hi + lo planes first.
     const ProjBwdSplit sp = proj_bwd_split(d);
-    cudaError_t e =
-        launch_proj_dx(d, DT_BF16, dlr, dli, d.N, 1, Wa, Wx, dx, 0, dx, stream, sp.P_dx);
-    if (e == cudaSuccess)
-      e = launch_proj_dw(d, x, dlr, dli, d.N, 1,
-                         reinterpret_cast<float*>(ws + PROJ_PART_OFFSET), dWa, dba, dWx, dbx,
-                         stream, sp.P_dw);
+    float* part = reinterpret_cast<float*>(ws + PROJ_PART_OFFSET);
+    cudaError_t e = cudaSuccess;
+    if (d.grad == RGLRU_BF16) {
+      e = launch_proj_dx(d, DT_BF16, dlr, dli, d.N, 1, Wa, Wx, dx, 0, dx, stream, sp.P_dx);
+      if (e == cudaSuccess)
+        e = launch_proj_dw(d, x, dlr, dli, d.N, 1, part, dWa, dba, dWx, dbx, stream, sp.P_dw);
+    } else {
+      uint8_t* pr = ws + gate_planes_offset(d);  // dlr hi, lo, then dli hi, lo
+      uint8_t* pi = pr + 4 * (size_t)d.N;
+      e = launch_split_planes(d, static_cast<const float*>(dlr), pr, stream);
+      if (e == cudaSuccess) e = launch_split_planes(d, static_cast<const float*>(dli), pi, stream);
+      if (e == cudaSuccess)
+        e = launch_proj_dx(d, DT_F32, pr, pi, d.N, 2, Wa, Wx, dx, 1, dx, stream, sp.P_dx);
+      if (e == cudaSuccess)
+        e = launch_proj_dw(d, x, pr, pi, d.N, 2, part, dWa, dba, dWx, dbx, stream, sp.P_dw);
+    }
     return cuda_status(e);
   }
   cudaError_t e =

@@ -7,9 +7,9 @@
 // dli Wx^T, dW = x^T dl, db = sum_n dl.
 //
 // These kernels serve the shapes the tensor-core projections (proj_tc.cu) do not take: float32
-// I/O, whose 1e-5 parity bound a bf16 tensor-core product cannot meet; the standalone
-// projection backward with float32-stored gradients; and gate blocks that are not a multiple
-// of 16 or wider than 160 channels.  Every kernel computes a 64 x 64 output tile per 256-thread block
+// I/O, whose 1e-5 parity bound a bf16 tensor-core product cannot meet, and gate blocks that
+// are not a multiple of 16 or wider than 160 channels.  Every kernel computes a 64 x 64 output
+// tile per 256-thread block
 // (4 x 4 per thread) through 16-deep shared-memory slabs; tails in k and in the token count
 // are guarded.
 #include "common.cuh"

@@ -332,6 +332,8 @@ struct ProjBwdSplit {
   int P_dx, P_dw;
 };
 ProjBwdSplit proj_bwd_split(const Dims& d);
+// float32 [N] -> bf16 hi plane [N] then lo plane [N] at `planes` (N = B T W).
+cudaError_t launch_split_planes(const Dims& d, const float* src, void* planes, cudaStream_t s);
 cudaError_t launch_proj_fwd(const Dims& d, int ot, const void* x, const void* Wa,
                             const float* ba, const void* Wx, const float* bx, void* lr, void* li,
                             cudaStream_t s);

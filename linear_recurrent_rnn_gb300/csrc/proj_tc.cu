@@ -813,6 +813,22 @@ __global__ void k_proj_dw_reduce(const float* __restrict__ part, int nblk, int P
   }
 }
 
+// float32 values as bf16 hi + lo planes (hi = bf16(v), lo = bf16(v - hi): v to ~2^-16), four
+// values a thread: the gradient operands of the projection backward when the caller's
+// gradients are float32.
+__global__ void k_split_planes(const float4* __restrict__ src, uint2* hi, uint2* lo, size_t n4) {
+  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n4;
+       i += (size_t)gridDim.x * blockDim.x) {
+    const float4 v = src[i];
+    const __nv_bfloat162 h0 = __floats2bfloat162_rn(v.x, v.y), h1 = __floats2bfloat162_rn(v.z, v.w);
+    const float2 f0 = __bfloat1622float2(h0), f1 = __bfloat1622float2(h1);
+    const __nv_bfloat162 l0 = __floats2bfloat162_rn(v.x - f0.x, v.y - f0.y);
+    const __nv_bfloat162 l1 = __floats2bfloat162_rn(v.z - f1.x, v.w - f1.y);
+    hi[i] = make_uint2(*reinterpret_cast<const uint32_t*>(&h0), *reinterpret_cast<const uint32_t*>(&h1));
+    lo[i] = make_uint2(*reinterpret_cast<const uint32_t*>(&l0), *reinterpret_cast<const uint32_t*>(&l1));
+  }
+}
+
 // ---------------------------------------------------------------- host side
 int ctas_per_group(int groups) {
   const int sms = sm_count();
@@ -924,6 +940,17 @@ ProjBwdSplit proj_bwd_split(const Dims& d) {
 size_t proj_dw_part_bytes(const Dims& d) {
   const int P = dw_ctas_per_group(d, d.nblk * (2 / dw_nmat(d)));
   return (size_t)d.nblk * P * 2 * ((size_t)d.k * d.k + d.k) * 4;
+}
+
+cudaError_t launch_split_planes(const Dims& d, const float* src, void* planes, cudaStream_t s) {
+  const size_t n4 = (size_t)d.N / 4;  // W is a multiple of 16
+  const int grid = (int)std::min<size_t>((n4 + 255) / 256, (size_t)8 * std::max(1, sm_count()));
+  bf16* hi = static_cast<bf16*>(planes);
+  k_split_planes<<<std::max(grid, 1), 256, 0, s>>>(reinterpret_cast<const float4*>(src),
+                                                  reinterpret_cast<uint2*>(hi),
+                                                  reinterpret_cast<uint2*>(hi + d.N), n4);
+  note_launches(1);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_proj_fwd(const Dims& d, int ot, const void* x, const void* Wa,
