@@ -209,6 +209,26 @@ const char* rglru_status_string(rglru_status s) {
   return "unknown status";
 }
 
+// Where a packed call keeps its token indices in `saved`: in the fused layout on the
+// tensor-core routes, after the logits on the CUDA-core one (whose scan slots are wider).
+struct VarlenIndex {
+  size_t seq_start, seq_end, total;
+};
+static VarlenIndex varlen_index(const Dims& d) {
+  VarlenIndex v;
+  if (fused_supported(d) || composed_tc(d)) {
+    const FusedFwdLayout FL = fused_fwd_layout(d);
+    v.seq_start = FL.seq_start;
+    v.seq_end = FL.seq_end;
+    v.total = FL.total;
+  } else {
+    v.seq_start = composed_saved(d).total;
+    v.seq_end = align_up(v.seq_start + (size_t)d.T * 4, 256);
+    v.total = align_up(v.seq_end + (size_t)d.T * 4, 256);
+  }
+  return v;
+}
+
 size_t rglru_saved_bytes(const rglru_shape* shape) {
   Dims d;
   if (make_dims(shape, &d) != RGLRU_OK) return 0;
@@ -216,7 +236,8 @@ size_t rglru_saved_bytes(const rglru_shape* shape) {
   // take the shape, else the composed path's (which keeps float32 logits)
   size_t a = scan_layout(d, false).total;
   if (logits_scan_supported(d) && fused_fwd_layout(d).total > a) a = fused_fwd_layout(d).total;
-  const size_t f = fused_supported(d) ? fused_fwd_layout(d).total : composed_saved(d).total;
+  size_t f = fused_supported(d) ? fused_fwd_layout(d).total : composed_saved(d).total;
+  if (d.B == 1 && varlen_index(d).total > f) f = varlen_index(d).total;  // packed calls
   return a > f ? a : f;
 }
 
@@ -428,11 +449,11 @@ static rglru_status varlen_setup(const rglru_shape* shape, const int32_t* cu, in
   if (st != RGLRU_OK) return st;
   if (d->B != 1 || d->mode != RGLRU_CANONICAL || S < 1 || !req(cu) || !req(saved))
     return RGLRU_ERR_INVALID_ARG;
-  const FusedFwdLayout FL = fused_fwd_layout(*d);
+  const VarlenIndex VI = varlen_index(*d);
   v->cu_seqlens = cu;
   v->S = S;
-  v->seq_start = reinterpret_cast<const int32_t*>(static_cast<const uint8_t*>(saved) + FL.seq_start);
-  v->seq_end = reinterpret_cast<const int32_t*>(static_cast<const uint8_t*>(saved) + FL.seq_end);
+  v->seq_start = reinterpret_cast<const int32_t*>(static_cast<const uint8_t*>(saved) + VI.seq_start);
+  v->seq_end = reinterpret_cast<const int32_t*>(static_cast<const uint8_t*>(saved) + VI.seq_end);
   v->h0 = nullptr;
   v->hT = nullptr;
   v->dhT = nullptr;
@@ -452,11 +473,30 @@ rglru_status rglru_fused_forward_varlen(const rglru_shape* shape, const void* x,
   if (!req(x) || !req(Wa) || !req(Wx) || !opt(ba) || !opt(bx) || !req(Lambda) || !opt(h0) ||
       !req(y) || !opt(hT))
     return RGLRU_ERR_INVALID_ARG;
-  if (!fused_supported(d) && !composed_tc(d)) return RGLRU_ERR_UNSUPPORTED;
+  // the tensor-core routes (bf16 I/O, k a multiple of 16 up to 160), or float32 I/O on the
+  // CUDA cores
+  if (!fused_supported(d) && !composed_tc(d) && d.io != RGLRU_F32) return RGLRU_ERR_UNSUPPORTED;
   v.h0 = h0;
   v.hT = hT;
   cudaError_t e = launch_seq_index(v, d.T, d.W, const_cast<int32_t*>(v.seq_start),
                                    const_cast<int32_t*>(v.seq_end), stream);
+  if (!fused_supported(d) && !composed_tc(d)) {
+    // float32 I/O (and other shapes off the tensor cores): the SIMT projections, then the
+    // CUDA-core scan over the packed sequences
+    uint8_t* sv = static_cast<uint8_t*>(saved);
+    const ComposedLayout C = composed_saved(d);
+    if (e == cudaSuccess)
+      e = launch_gate_proj_simt(d, d.io, DT_F32, x, Wa, ba, Wx, bx, sv + C.lr, sv + C.li, stream);
+    ScanFwdArgs a = fwd_args(d, x, sv + C.lr, sv + C.li, Lambda, nullptr, nullptr, nullptr, y,
+                             nullptr, saved);
+    a.seq_start = v.seq_start;
+    a.seq_end = v.seq_end;
+    a.h0s = h0;
+    a.hTs = hT;
+    if (e == cudaSuccess) e = cudaMemsetAsync(saved, 0, a.L.zero_bytes, stream);
+    if (e == cudaSuccess) e = launch_scan_fwd(a, d.io, DT_F32, true, stream);
+    return cuda_status(e);
+  }
   if (fused_supported(d)) {
     if (e == cudaSuccess)
       e = launch_fused_fwd(d, x, Wa, ba, Wx, bx, Lambda, nullptr, nullptr, nullptr, y, nullptr,
@@ -490,13 +530,38 @@ rglru_status rglru_fused_backward_varlen(const rglru_shape* shape, const void* d
       !req(Lambda) || !opt(h0) || !req(dx) || !req(dWa) || !req(dWx) || !opt(dba) ||
       !opt(dbx) || !req(dLambda) || !opt(dh0) || !req(workspace))
     return RGLRU_ERR_INVALID_ARG;
-  if (!fused_supported(d) && !composed_tc(d)) return RGLRU_ERR_UNSUPPORTED;
+  if (!fused_supported(d) && !composed_tc(d) && d.io != RGLRU_F32) return RGLRU_ERR_UNSUPPORTED;
   v.h0 = h0;
   v.dhT = dhT;
   v.dh0 = dh0;
   // the token indices were written by the forward into `saved`; empty sequences' dh0 here
   cudaError_t e = cudaSuccess;
   if (dh0) e = launch_seq_empty_dh0(v, d.W, stream);
+  if (!fused_supported(d) && !composed_tc(d)) {
+    // float32 I/O: the CUDA-core scan backward over the packed sequences on the saved float32
+    // logits, then the SIMT projection backward
+    const uint8_t* sv = static_cast<const uint8_t*>(saved);
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    const ComposedLayout C = composed_saved(d);
+    const ComposedWs CW = composed_ws(d);
+    ScanBwdArgs a = bwd_args(d, dy, nullptr, x, sv + C.lr, sv + C.li, Lambda, nullptr, nullptr,
+                             nullptr, saved, ws + CW.dxd, ws + CW.dlr, ws + CW.dli, dLambda,
+                             nullptr, workspace);
+    a.seq_start = v.seq_start;
+    a.seq_end = v.seq_end;
+    a.h0s = h0;
+    a.dhTs = dhT;
+    a.dh0s = dh0;
+    if (e == cudaSuccess) e = cudaMemsetAsync(workspace, 0, a.L.zero_bytes, stream);
+    if (e == cudaSuccess) e = launch_scan_bwd(a, d.io, DT_F32, DT_F32, DT_F32, true, stream);
+    if (e == cudaSuccess)
+      e = launch_gate_dx_simt(d, d.io, DT_F32, d.grad, ws + CW.dlr, ws + CW.dli, Wa, Wx,
+                              reinterpret_cast<const float*>(ws + CW.dxd), dx, stream);
+    if (e == cudaSuccess)
+      e = launch_gate_dw_simt(d, d.io, DT_F32, x, ws + CW.dlr, ws + CW.dli, dWa, dba, dWx, dbx,
+                              ws + CW.gate, stream);
+    return cuda_status(e);
+  }
   if (fused_supported(d)) {
     if (e == cudaSuccess)
       e = launch_fused_bwd(d, dy, nullptr, x, Wa, ba, Wx, bx, Lambda, nullptr, nullptr, nullptr,

@@ -205,6 +205,11 @@ struct ScanFwdArgs {
   uint8_t* scratch;  // `saved`
   ScanLayout L;
   int spin_limit, drop_tile;
+  // packed sequences (Varlen; null seq_start: none): token indices, per-sequence states
+  const int32_t* seq_start = nullptr;
+  const int32_t* seq_end = nullptr;
+  const float* h0s = nullptr;
+  float* hTs = nullptr;
 };
 
 struct ScanBwdArgs {
@@ -228,6 +233,12 @@ struct ScanBwdArgs {
   uint8_t* scratch;  // `workspace`
   ScanLayout L;
   int spin_limit, drop_tile;
+  // packed sequences (Varlen; null seq_start: none)
+  const int32_t* seq_start = nullptr;
+  const int32_t* seq_end = nullptr;
+  const float* h0s = nullptr;
+  const float* dhTs = nullptr;
+  float* dh0s = nullptr;
 };
 
 // Adds n to the process-wide count of kernels enqueued (rglru_kernel_launches).

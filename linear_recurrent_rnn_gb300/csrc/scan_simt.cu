@@ -138,7 +138,10 @@ __device__ __forceinline__ void lb_compose(const float2* agg, size_t row_c0, int
 // The scan kernels are bound by the latency of short tiles, so resident warps matter more
 // than a few spilled registers: 7 CTAs per SM (72 registers) for the forward, 4 (128) for
 // the backward, each measured faster than the spill-free 5 and 3.
-template <typename XT, typename LT, bool CANON>
+// VARLEN (packed sequences, one row): at the first token of sequence s the chain restarts from
+// h0[s] (h -> abar h0[s] + m i x, the carry dropped), and the state after the last token of
+// sequence s is its hT[s].
+template <typename XT, typename LT, bool CANON, bool VARLEN>
 __global__ void __launch_bounds__(128, 7) k_scan_fwd(ScanFwdArgs a) {
   uint32_t* status = reinterpret_cast<uint32_t*>(a.scratch);
   uint32_t* ticket = status + 1;
@@ -164,6 +167,7 @@ __global__ void __launch_bounds__(128, 7) k_scan_fwd(ScanFwdArgs a) {
   // Local scan from a zero carry: hl = state after each token, Ac = product of abar.
   float hl[2][SUB], Ac[2][SUB];
   float rh[2] = {0.0f, 0.0f}, rA[2] = {1.0f, 1.0f};
+  int ens[SUB];  // VARLEN: the sequence ending at each token (-1: none)
 #pragma unroll
   for (int s = 0; s < SUB; ++s) {
     const int t = t0 + s;
@@ -171,11 +175,17 @@ __global__ void __launch_bounds__(128, 7) k_scan_fwd(ScanFwdArgs a) {
     const size_t idx = ((size_t)tl.b * a.T + t) * a.W + w;
     float2 xv = make_float2(0.f, 0.f), rv = xv, iv = xv;
     bool rst = false;
+    int st = -1;
+    ens[s] = -1;
     if (ok) {
       xv = Pair<XT>::load(x + idx);
       rv = Pair<LT>::load(lr + idx);
       iv = Pair<LT>::load(li + idx);
       if (CANON) rst = is_reset(a.reset_mask, a.segment_pos, (size_t)tl.b * a.T + t);
+      if (VARLEN) {
+        st = a.seq_start[(size_t)tl.b * a.T + t];
+        ens[s] = a.seq_end[(size_t)tl.b * a.T + t];
+      }
     }
     const float xs[2] = {xv.x, xv.y}, rs[2] = {rv.x, rv.y}, is[2] = {iv.x, iv.y};
 #pragma unroll
@@ -193,8 +203,13 @@ __global__ void __launch_bounds__(128, 7) k_scan_fwd(ScanFwdArgs a) {
         abar = 1.0f;
         m = 0.0f;
       }
-      rh[j] = fmaf(abar, rh[j], m * (i * xs[j]));
-      rA[j] *= abar;
+      float ach = abar, bv = m * (i * xs[j]);  // the chain's decay and input
+      if (VARLEN && st >= 0) {
+        bv = fmaf(abar, a.h0s ? a.h0s[(size_t)st * a.W + w + j] : 0.0f, bv);
+        ach = 0.0f;
+      }
+      rh[j] = fmaf(ach, rh[j], bv);
+      rA[j] *= ach;
       hl[j][s] = rh[j];
       Ac[j][s] = rA[j];
     }
@@ -269,7 +284,10 @@ __global__ void __launch_bounds__(128, 7) k_scan_fwd(ScanFwdArgs a) {
     const int t = t0 + s;
     if (wok && t < a.T) {
       const size_t idx = ((size_t)tl.b * a.T + t) * a.W + w;
-      Pair<XT>::store(y + idx, fmaf(Ac[0][s], hs[0], hl[0][s]), fmaf(Ac[1][s], hs[1], hl[1][s]));
+      const float y0 = fmaf(Ac[0][s], hs[0], hl[0][s]), y1 = fmaf(Ac[1][s], hs[1], hl[1][s]);
+      Pair<XT>::store(y + idx, y0, y1);
+      if (VARLEN && ens[s] >= 0 && a.hTs)
+        *reinterpret_cast<float2*>(a.hTs + (size_t)ens[s] * a.W + w) = make_float2(y0, y1);
     }
   }
 }
@@ -280,7 +298,10 @@ __global__ void __launch_bounds__(128, 7) k_scan_fwd(ScanFwdArgs a) {
 // dla = abar g (h_{t-1} - u abar / m) (u = i x; zero at reset tokens):
 //   dlr = dla (-8 softplus) r (1 - r),  dx = g m i,  dli = g m u (1 - i),
 //   dLambda partial = sum dla (-8 r)   (times sigmoid(Lambda) in the reduction).
-template <typename XT, typename LT, typename DXT, typename DLT, bool CANON>
+// VARLEN: at a sequence's first token the chain's decay is 0 (no gradient flows to the
+// sequence before) while abar keeps its value for the derivatives, h_{t-1} is h0[s], and
+// dh0[s] = abar g; at its last token dhT[s] joins dy.
+template <typename XT, typename LT, typename DXT, typename DLT, bool CANON, bool VARLEN>
 __global__ void __launch_bounds__(128, 4) k_scan_bwd(ScanBwdArgs a) {
   uint32_t* status = reinterpret_cast<uint32_t*>(a.scratch);
   uint32_t* ticket = status + 1;
@@ -314,6 +335,8 @@ __global__ void __launch_bounds__(128, 4) k_scan_bwd(ScanBwdArgs a) {
   // Phase A: recompute the gates and the local forward scan of this half.
   float hp[2][SUB], ab[2][SUB], uu[2][SUB], mm[2][SUB], rr[2][SUB], ii[2][SUB], gy[2][SUB];
   float rh[2] = {0.0f, 0.0f}, rA[2] = {1.0f, 1.0f};
+  int sts[SUB];          // VARLEN: the sequence starting at each token (-1: none)
+  uint32_t smask = 0u;   // VARLEN: bit s = a sequence starts at token s of this half
 #pragma unroll
   for (int s = 0; s < SUB; ++s) {
     const int t = t0 + s;
@@ -321,12 +344,22 @@ __global__ void __launch_bounds__(128, 4) k_scan_bwd(ScanBwdArgs a) {
     const size_t idx = ((size_t)tl.b * a.T + t) * a.W + w;
     float2 xv = make_float2(0.f, 0.f), rv = xv, iv = xv, dv = xv;
     bool rst = false;
+    sts[s] = -1;
     if (ok) {
       xv = Pair<XT>::load(x + idx);
       dv = Pair<XT>::load(dy + idx);
       rv = Pair<LT>::load(lr + idx);
       iv = Pair<LT>::load(li + idx);
       if (CANON) rst = is_reset(a.reset_mask, a.segment_pos, (size_t)tl.b * a.T + t);
+      if (VARLEN) {
+        sts[s] = a.seq_start[(size_t)tl.b * a.T + t];
+        const int en = a.seq_end[(size_t)tl.b * a.T + t];
+        if (en >= 0 && a.dhTs) {
+          dv.x += a.dhTs[(size_t)en * a.W + w];
+          dv.y += a.dhTs[(size_t)en * a.W + w + 1];
+        }
+        if (sts[s] >= 0) smask |= 1u << s;
+      }
     }
     const float xs[2] = {xv.x, xv.y}, rs[2] = {rv.x, rv.y}, is[2] = {iv.x, iv.y},
                 ds[2] = {dv.x, dv.y};
@@ -347,8 +380,15 @@ __global__ void __launch_bounds__(128, 4) k_scan_bwd(ScanBwdArgs a) {
       }
       const float u = i * xs[j];
       hp[j][s] = rh[j];  // local state before token s
-      rh[j] = fmaf(abar, rh[j], m * u);
-      rA[j] *= abar;
+      float ach = abar, bv = m * u;  // the chain's decay and input
+      if (VARLEN && sts[s] >= 0) {
+        const float h0v = a.h0s ? a.h0s[(size_t)sts[s] * a.W + w + j] : 0.0f;
+        hp[j][s] = h0v;  // the true h_{t-1} of a sequence's first token
+        bv = fmaf(abar, h0v, bv);
+        ach = 0.0f;
+      }
+      rh[j] = fmaf(ach, rh[j], bv);
+      rA[j] *= ach;
       ab[j][s] = abar;
       uu[j][s] = u;
       mm[j][s] = m;
@@ -373,8 +413,9 @@ __global__ void __launch_bounds__(128, 4) k_scan_bwd(ScanBwdArgs a) {
     float P = 1.0f;
 #pragma unroll
     for (int s = 0; s < SUB; ++s) {
-      const float hprev = fmaf(P, hs[j], hp[j][s]);
-      P *= ab[j][s];
+      const bool start = VARLEN && ((smask >> s) & 1u);
+      const float hprev = start ? hp[j][s] : fmaf(P, hs[j], hp[j][s]);
+      P *= start ? 0.0f : ab[j][s];
       const float abar = ab[j][s], m = mm[j][s], u = uu[j][s], r = rr[j][s], i = ii[j][s];
       // dla / g = abar (h_{t-1} - u abar / m); zero at reset tokens since abar = 0 there.
       // (Tokens past T carry m = 0 and take no part.)
@@ -389,8 +430,9 @@ __global__ void __launch_bounds__(128, 4) k_scan_bwd(ScanBwdArgs a) {
 #pragma unroll
     for (int s = SUB - 1; s >= 0; --s) {
       if (s < SUB - 1) {
-        g *= ab[j][s + 1];
-        q *= ab[j][s + 1];
+        const float ach = (VARLEN && ((smask >> (s + 1)) & 1u)) ? 0.0f : ab[j][s + 1];
+        g *= ach;
+        q *= ach;
       }
       g += gy[j][s];
       gl[j][s] = g;
@@ -401,8 +443,9 @@ __global__ void __launch_bounds__(128, 4) k_scan_bwd(ScanBwdArgs a) {
   float Ah[2], Bh[2], A1[2], B1[2], At[2], Bt[2];
 #pragma unroll
   for (int j = 0; j < 2; ++j) {
-    Ah[j] = ab[j][0] * Q[j][0];
-    Bh[j] = ab[j][0] * gl[j][0];
+    const float ach0 = (VARLEN && (smask & 1u)) ? 0.0f : ab[j][0];
+    Ah[j] = ach0 * Q[j][0];
+    Bh[j] = ach0 * gl[j][0];
     A1[j] = __shfl_sync(0xffffffffu, Ah[j], pair + 16);
     B1[j] = __shfl_sync(0xffffffffu, Bh[j], pair + 16);
     const float A0 = __shfl_sync(0xffffffffu, Ah[j], pair);
@@ -476,6 +519,9 @@ __global__ void __launch_bounds__(128, 4) k_scan_bwd(ScanBwdArgs a) {
     }
     if (wok && t < a.T) {
       const size_t idx = ((size_t)tl.b * a.T + t) * a.W + w;
+      if (VARLEN && sts[s] >= 0 && a.dh0s)  // d h0[s] = abar g at the sequence's first token
+        *reinterpret_cast<float2*>(a.dh0s + (size_t)sts[s] * a.W + w) =
+            make_float2(ab[0][s] * g[0], ab[1][s] * g[1]);
       Pair<DXT>::store(dx + idx, g[0] * cx[0][s], g[1] * cx[1][s]);
       OutPair<DLT>::store(dlr + idx, a.dl_plane, g[0] * cr[0][s], g[1] * cr[1][s]);
       OutPair<DLT>::store(dli + idx, a.dl_plane, g[0] * ci[0][s], g[1] * ci[1][s]);
@@ -508,26 +554,30 @@ __global__ void __launch_bounds__(512) k_reduce_dlambda(const float* part, int r
   }
 }
 
-template <typename XT, typename LT>
+template <typename XT, typename LT, bool WITH_VARLEN = false>
 cudaError_t fwd_dispatch_mode(const ScanFwdArgs& a, bool canonical, cudaStream_t s) {
   const size_t ntiles = (size_t)a.B * a.nC * a.ng;
   const unsigned grid = (unsigned)((ntiles + 3) / 4);
-  if (canonical)
-    k_scan_fwd<XT, LT, true><<<grid, 128, 0, s>>>(a);
+  if (WITH_VARLEN && a.seq_start)  // packed sequences: canonical, one row
+    k_scan_fwd<XT, LT, true, WITH_VARLEN><<<grid, 128, 0, s>>>(a);
+  else if (canonical)
+    k_scan_fwd<XT, LT, true, false><<<grid, 128, 0, s>>>(a);
   else
-    k_scan_fwd<XT, LT, false><<<grid, 128, 0, s>>>(a);
+    k_scan_fwd<XT, LT, false, false><<<grid, 128, 0, s>>>(a);
   note_launches(1);
   return cudaGetLastError();
 }
 
-template <typename XT, typename LT, typename DXT, typename DLT>
+template <typename XT, typename LT, typename DXT, typename DLT, bool WITH_VARLEN = false>
 cudaError_t bwd_dispatch_mode(const ScanBwdArgs& a, bool canonical, cudaStream_t s) {
   const size_t ntiles = (size_t)a.B * a.nC * a.ng;
   const unsigned grid = (unsigned)((ntiles + 3) / 4);
-  if (canonical)
-    k_scan_bwd<XT, LT, DXT, DLT, true><<<grid, 128, 0, s>>>(a);
+  if (WITH_VARLEN && a.seq_start)
+    k_scan_bwd<XT, LT, DXT, DLT, true, WITH_VARLEN><<<grid, 128, 0, s>>>(a);
+  else if (canonical)
+    k_scan_bwd<XT, LT, DXT, DLT, true, false><<<grid, 128, 0, s>>>(a);
   else
-    k_scan_bwd<XT, LT, DXT, DLT, false><<<grid, 128, 0, s>>>(a);
+    k_scan_bwd<XT, LT, DXT, DLT, false, false><<<grid, 128, 0, s>>>(a);
   note_launches(1);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
@@ -541,7 +591,8 @@ cudaError_t bwd_dispatch_mode(const ScanBwdArgs& a, bool canonical, cudaStream_t
 
 cudaError_t launch_scan_fwd(const ScanFwdArgs& a, int xt, int lt, bool canonical,
                             cudaStream_t s) {
-  if (xt == DT_F32 && lt == DT_F32) return fwd_dispatch_mode<float, float>(a, canonical, s);
+  if (xt == DT_F32 && lt == DT_F32) return fwd_dispatch_mode<float, float, true>(a, canonical, s);
+  if (a.seq_start) return cudaErrorInvalidValue;  // packed sequences: float32 only here
   if (xt == DT_BF16 && lt == DT_BF16) return fwd_dispatch_mode<bf16, bf16>(a, canonical, s);
   if (xt == DT_BF16 && lt == DT_F32) return fwd_dispatch_mode<bf16, float>(a, canonical, s);
   return cudaErrorInvalidValue;
@@ -550,7 +601,8 @@ cudaError_t launch_scan_fwd(const ScanFwdArgs& a, int xt, int lt, bool canonical
 cudaError_t launch_scan_bwd(const ScanBwdArgs& a, int xt, int lt, int dxt, int dlt,
                             bool canonical, cudaStream_t s) {
   if (xt == DT_F32 && lt == DT_F32 && dxt == DT_F32 && dlt == DT_F32)
-    return bwd_dispatch_mode<float, float, float, float>(a, canonical, s);
+    return bwd_dispatch_mode<float, float, float, float, true>(a, canonical, s);
+  if (a.seq_start) return cudaErrorInvalidValue;  // packed sequences: float32 only here
   if (xt == DT_BF16 && lt == DT_BF16 && dxt == DT_BF16 && dlt == DT_BF16)
     return bwd_dispatch_mode<bf16, bf16, bf16, bf16>(a, canonical, s);
   if (xt == DT_BF16 && lt == DT_BF16 && dxt == DT_F32 && dlt == DT_F32)

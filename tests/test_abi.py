@@ -111,7 +111,7 @@ def test_step_host_validation(lib):
 def test_varlen_host_validation(lib):
     """The packed-sequence entry points check on the host (fake, never dereferenced
     addresses): one row, canonical mode, at least one sequence, the offsets array present,
-    and tensor-core shapes only (bf16, gate blocks a multiple of 16 up to 160)."""
+    and a supported shape (bf16 with gate blocks a multiple of 16 up to 160, or float32 I/O)."""
     A = 1 << 20
     P = lambda v: None if v is None else ctypes.c_void_p(v)
 
@@ -129,9 +129,8 @@ def test_varlen_host_validation(lib):
         assert call(R.make_shape(1, 256, 256, 2, R.BF16, R.BF16, R.RESTRICTED)) == R.ERR_INVALID_ARG
         assert call(good, S=0) == R.ERR_INVALID_ARG
         assert call(good, cu=None) == R.ERR_INVALID_ARG
-        # gate blocks of 24 (not a multiple of 16) and float32 I/O have no packed path
+        # bf16 with gate blocks off the tensor-core routes (k = 24) has no packed path
         assert call(R.make_shape(1, 256, 192, 8, R.BF16, R.BF16, R.CANONICAL)) == R.ERR_UNSUPPORTED
-        assert call(R.make_shape(1, 256, 256, 2, R.F32, R.F32, R.CANONICAL)) == R.ERR_UNSUPPORTED
     assert fwd(good, saved=None) == R.ERR_INVALID_ARG
     assert bwd(good, ws=None) == R.ERR_INVALID_ARG
 

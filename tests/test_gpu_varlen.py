@@ -3,7 +3,8 @@ float64 oracle run on every sequence as a row of its own: sequence s continues f
 without a reset, its final state is hT[s], dhT[s] joins the gradient at its last token and
 dh0[s] is its initial-state gradient; the parameter gradients are the sums over sequences.
 Lengths include empty sequences (hT = h0, dh0 = dhT), a leading empty one (the next sequence
-starts at token 0), a sequence of one token, and starts inside and across 64-token chunks."""
+starts at token 0), a sequence of one token, and starts inside and across 64-token chunks;
+bf16 I/O on the tensor-core kernels, float32 I/O on the CUDA-core scan."""
 import numpy as np
 import pytest
 import torch
@@ -24,15 +25,21 @@ CASES = [
     # slice of W = 320 is partial) and of 48
     ([0, 1, 0, 70, 64, 33, 0, 130, 5, 1], (0.9, 0.999), 44, "bf16", 320, 160),
     ([95, 0, 3, 200], (0.5, 0.999), 45, "f32", 192, 48),
+    # float32 I/O: the CUDA-core scan over the packed sequences (16-token chunks, so starts
+    # fall at every offset within a chunk and inside both of its halves)
+    ([0, 1, 0, 70, 64, 33, 0, 130, 5, 1], (0.9, 0.999), 46, "f32", 256, 128, "f32"),
+    ([17, 8, 9, 1, 40, 0, 3], (0.05, 0.999), 47, "f32", 96, 24, "f32"),
 ]
+CASES = [c if len(c) == 7 else c + ("bf16",) for c in CASES]
 
 
-@pytest.mark.parametrize("lengths,u_range,seed,grad,W,k", CASES,
-                         ids=["mixed", "far", "f32grad", "k160", "k48-f32grad"])
-def test_varlen_matches_per_sequence_oracle(lengths, u_range, seed, grad, W, k):
+@pytest.mark.parametrize("lengths,u_range,seed,grad,W,k,io", CASES,
+                         ids=["mixed", "far", "f32grad", "k160", "k48-f32grad", "f32io",
+                              "f32io-k24-far"])
+def test_varlen_matches_per_sequence_oracle(lengths, u_range, seed, grad, W, k, io):
     T = int(sum(lengths))
     S = len(lengths)
-    wl = Workload("varlen", 1, T, W, k, "bf16", "canonical", u_range, h0_std=1.0)
+    wl = Workload("varlen", 1, T, W, k, io, "canonical", u_range, h0_std=1.0)
     inp = generate(wl, seed)
     rng = np.random.default_rng(seed)
     h0s = torch.from_numpy(rng.standard_normal((S, W))).float()
@@ -43,7 +50,7 @@ def test_varlen_matches_per_sequence_oracle(lengths, u_range, seed, grad, W, k):
 
     d = {n: dev(v) for n, v in inp.items() if isinstance(v, torch.Tensor)}
     gdt = R.BF16 if grad == "bf16" else R.F32
-    sh = R.make_shape(1, T, W, W // k, R.BF16, gdt, R.CANONICAL)
+    sh = R.make_shape(1, T, W, W // k, R.BF16 if io == "bf16" else R.F32, gdt, R.CANONICAL)
     cu_d = torch.from_numpy(cu).cuda()
     y = torch.empty_like(d["x"])
     hT = torch.empty(S, W, device="cuda")
@@ -85,12 +92,12 @@ def test_varlen_matches_per_sequence_oracle(lengths, u_range, seed, grad, W, k):
         g_ref["dx"][:, a:b] = g["dx"]
         for n in ("dWa", "dWx", "dba", "dbx", "dLambda"):
             g_ref[n] = g_ref[n] + g[n]
-    assert_close("y", host(y), y_ref, io="bf16", kind="out")
-    assert_close("hT", host(hT), hT_ref, io="bf16", kind="out")
-    assert_close("dx", host(dx), g_ref["dx"], io="bf16", kind="grad", stored=grad)
+    assert_close("y", host(y), y_ref, io=io, kind="out")
+    assert_close("hT", host(hT), hT_ref, io=io, kind="out")
+    assert_close("dx", host(dx), g_ref["dx"], io=io, kind="grad", stored=grad)
     for n, got in (("dWa", dWa), ("dWx", dWx), ("dba", dba), ("dbx", dbx), ("dLambda", dL)):
-        assert_close(n, host(got), g_ref[n], io="bf16", kind="grad")
-    assert_close("dh0", host(dh0), dh0_ref, io="bf16", kind="grad")
+        assert_close(n, host(got), g_ref[n], io=io, kind="grad")
+    assert_close("dh0", host(dh0), dh0_ref, io=io, kind="grad")
 
 
 def test_varlen_full_size_sampled_blocks():
