@@ -186,8 +186,8 @@ rglru_status rglru_fused_backward(const rglru_shape *shape, const void *dy, cons
  * last token; an empty sequence has hT[s] = h0[s].  Same computation as rglru_fused_forward on
  * each sequence as a row of its own.  bf16 I/O on the tensor cores (k a multiple of 16 up to
  * 160; k = 128 in one fused kernel, other k through the tensor-core projections), float32 I/O
- * on the CUDA cores (any k); other bf16 shapes give RGLRU_ERR_UNSUPPORTED.  `saved` (rglru_saved_bytes of the shape) also keeps the token
- * indices for the backward. */
+ * on the CUDA cores (any k); other bf16 shapes give RGLRU_ERR_UNSUPPORTED.  `saved`
+ * (rglru_saved_bytes of the shape) also keeps the token indices for the backward. */
 rglru_status rglru_fused_forward_varlen(const rglru_shape *shape, const void *x, const void *Wa,
                                         const float *ba, const void *Wx, const float *bx,
                                         const float *Lambda, const int32_t *cu_seqlens,
