@@ -156,7 +156,11 @@ __global__ void __launch_bounds__(256) k_dw_part(int BT, int W, int k, int nblk,
   const long per = (BT + splits - 1) / splits;
   const long nb = split * per, ne = min((long)BT, nb + per);
   const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
-  float acc[4][4] = {};
+  // Each TK-row slab is summed on its own, then added to the running sums with a compensation
+  // term (Kahan): a plain float32 running sum over a split's hundreds to thousands of rows
+  // drifts by up to (rows x 2^-24) of the result where the products share a sign (the
+  // diagonal of dW), beyond the float32 bound of 1e-5.
+  float acc[4][4] = {}, cmp[4][4] = {};
   for (long nn = nb; nn < ne; nn += TK) {
     for (int e = threadIdx.x; e < TK * 64; e += 256) {
       const int r = e / 64, c = e % 64;
@@ -167,6 +171,7 @@ __global__ void __launch_bounds__(256) k_dw_part(int BT, int W, int k, int nblk,
       Gs[r][c] = (okn && j < k) ? to_f32(g[(size_t)n * W + (size_t)blk * k + j]) : 0.0f;
     }
     __syncthreads();
+    float sl[4][4] = {};
 #pragma unroll
     for (int q = 0; q < TK; ++q) {
       float xa[4], gb[4];
@@ -178,8 +183,17 @@ __global__ void __launch_bounds__(256) k_dw_part(int BT, int W, int k, int nblk,
 #pragma unroll
       for (int u = 0; u < 4; ++u)
 #pragma unroll
-        for (int v = 0; v < 4; ++v) acc[u][v] = fmaf(xa[u], gb[v], acc[u][v]);
+        for (int v = 0; v < 4; ++v) sl[u][v] = fmaf(xa[u], gb[v], sl[u][v]);
     }
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+#pragma unroll
+      for (int v = 0; v < 4; ++v) {
+        const float yv = __fsub_rn(sl[u][v], cmp[u][v]);
+        const float t = __fadd_rn(acc[u][v], yv);
+        cmp[u][v] = __fsub_rn(__fsub_rn(t, acc[u][v]), yv);
+        acc[u][v] = t;
+      }
     __syncthreads();
   }
   float* P = part + (((size_t)split * 2 + gate) * nblk + blk) * (size_t)k * k;

@@ -107,6 +107,9 @@ GEMM_CASES = [
     (W_("bf16-k48", 1, 300, 192, 48, "bf16", "restricted"), 27, None),
     (W_("bf16-k128-multi", 1, 1500, 2048, 128, "bf16", "restricted"), 28, None),
     (W_("bf16-k160-multi", 2, 4000, 480, 160, "bf16", "restricted"), 29, None),
+    # float32-stored gradients on the tensor cores (split into bf16 hi + lo planes), with the
+    # dx and dW kernels side by side
+    (W_("bf16-k128-multi-g32", 1, 1500, 2048, 128, "bf16", "restricted"), 30, "f32"),
 ]
 
 
