@@ -83,14 +83,15 @@ const char *rglru_status_string(rglru_status s);
 
 /* Bytes of the `saved` buffer a forward call fills and the matching backward reads
  * (float32 chunk-boundary states plus the forward's look-back scratch; for a fused call on a
- * shape the tensor-core kernels do not take, also the float32 gate logits).  A buffer filled
+ * shape the one-kernel fused path does not take, also the gate logits, as float32 or as bf16
+ * hi + lo planes; for a packed-sequence call, also its token indices).  A buffer filled
  * by rglru_forward is read by rglru_backward; one filled by rglru_fused_forward by
  * rglru_fused_backward.  Sized for the current device.  0 on an invalid shape. */
 size_t rglru_saved_bytes(const rglru_shape *shape);
 
-/* Bytes of the `workspace` scratch taken by rglru_backward, rglru_gate_proj_backward and
- * rglru_fused_backward (the maximum over the three).  Sized for the current device.  0 on an
- * invalid shape. */
+/* Bytes of the `workspace` scratch taken by rglru_backward, rglru_gate_proj_backward,
+ * rglru_fused_backward and rglru_fused_backward_varlen (the maximum over them).  Sized for the
+ * current device.  0 on an invalid shape. */
 size_t rglru_workspace_bytes(const rglru_shape *shape);
 
 /* Block-diagonal gate projections [P1 first paragraph; P2 "protocol.scope"]:
