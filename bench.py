@@ -5,11 +5,12 @@ a float32 carry, restricted protocol (zero initial state, no resets), 16 gate bl
 One step = rglru_fused_forward + rglru_fused_backward over one batch of seeded synthetic
 input already resident in HBM: the gate projections, gates, decay, multiplier, write and
 scan, then the reverse scan, pointwise gradients, the on-device Lambda reduction and the
-projection gradients (dx, dWa, dWx, dba, dbx).  L2 is flushed (a 256 MiB write) before every
-timed step; two CUDA events bracket each step on the launching stream, with nothing else
-recorded between them.  A second pass records the forward / backward split and the backward
-kernel's own duration (for the roofline); a third replays the step captured in a CUDA graph
-(`graph`).
+projection gradients (dx, dWa, dWx, dba, dbx).  The two calls are captured once in a CUDA
+graph and the graph is replayed once a step, as a training loop on one GPU runs them.  L2 is
+flushed (a 256 MiB write) before every timed step; two CUDA events bracket each step on the
+launching stream, with nothing else recorded between them.  A second pass times the same
+step with the calls issued directly (`eager`), a third records the forward / backward split
+and the backward kernel's own duration (for the roofline).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -232,22 +233,36 @@ def run_ours(args, rank, world, local):
     if R.rglru_sync_status(saved) != R.OK or R.rglru_sync_status(ws) != R.OK:
         raise RuntimeError("look-back timeout during warm-up")
 
-    # The step: each timed between two events on the launching stream (nothing else recorded
-    # inside it), the L2 flushed before each.
+    # The step as a training loop on this GPU runs it: the forward and backward calls captured
+    # once in a CUDA graph (the library's calls enqueue only stream-ordered work: the slot
+    # clears and the two kernels), replayed once a step.  Each step is timed between two
+    # events on the launching stream (nothing else recorded inside), the L2 flushed before
+    # each.  Our kernels per step: counted while capturing.
+    gs = torch.cuda.Stream()
+    gs.wait_stream(stream)
+    g = torch.cuda.CUDAGraph()
+    nc0 = R.rglru_kernel_launches()
+    with torch.cuda.graph(g, stream=gs):
+        R.rglru_fused_forward(sh, x, Wa, ba, Wx, bx, L, None, None, None, y, hT, saved, gs)
+        R.rglru_fused_backward(sh, dy, None, x, Wa, ba, Wx, bx, L, None, None, None, saved,
+                               dx, dWa, dba, dWx, dbx, dL, None, ws, gs)
+    per_step_launches = R.rglru_kernel_launches() - nc0
+    stream.wait_stream(gs)
+    for _ in range(args.warmup):
+        g.replay()
+    torch.cuda.synchronize()
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
     clocks = ClockSampler(local)
     dist_barrier(world)
     torch.cuda.synchronize()
     clocks.start()
-    n0 = R.rglru_kernel_launches()
     for k in range(args.steps):
         flush.zero_()
         ev[k][0].record(stream)
-        fwd()
-        bwd()
+        g.replay()
         ev[k][1].record(stream)
     torch.cuda.synchronize()
-    launches = R.rglru_kernel_launches() - n0
+    launches = per_step_launches * args.steps
     clk = clocks.stop()
     dist_barrier(world)
     if R.rglru_sync_status(saved) != R.OK or R.rglru_sync_status(ws) != R.OK:
@@ -256,6 +271,24 @@ def run_ours(args, rank, world, local):
     total_ms = dist_max(sum(step_list), world, device="cuda")
     tokens = wl.B * wl.T
     value = tokens * world * args.steps / (total_ms / 1e3)
+    del g
+
+    # The same step with the two calls issued directly each time (no graph).
+    dev_ = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
+    for k in range(args.steps):
+        flush.zero_()
+        dev_[k][0].record(stream)
+        fwd()
+        bwd()
+        dev_[k][1].record(stream)
+    torch.cuda.synchronize()
+    if R.rglru_sync_status(saved) != R.OK or R.rglru_sync_status(ws) != R.OK:
+        raise RuntimeError("look-back timeout in the direct calls")
+    d_ms = dist_max(sum(e[0].elapsed_time(e[1]) for e in dev_), world, device="cuda")
+    eager = {"ms_per_step": d_ms / args.steps,
+             "value": tokens * world * args.steps / (d_ms / 1e3), "unit": UNIT,
+             "how": "the forward and backward calls issued directly every step (no graph); "
+                    "L2 flushed before every step"}
 
     # A second pass for the split: the forward call, and the backward's tensor-core kernel
     # alone between events the library records around its launch (the call also runs the
@@ -276,37 +309,6 @@ def run_ours(args, rank, world, local):
     torch.cuda.synchronize()
     fwd_ms = [e[0].elapsed_time(e[1]) for e in sev]
     bwd_ms = [e[1].elapsed_time(e[2]) for e in sev]
-
-    # The same step captured once in a CUDA graph (the library's calls enqueue only stream-
-    # ordered work, so they capture as they are) and replayed.
-    graph = None
-    if world == 1:
-        gs = torch.cuda.Stream()
-        gs.wait_stream(stream)
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=gs):
-            R.rglru_fused_forward(sh, x, Wa, ba, Wx, bx, L, None, None, None, y, hT, saved, gs)
-            R.rglru_fused_backward(sh, dy, None, x, Wa, ba, Wx, bx, L, None, None, None, saved,
-                                   dx, dWa, dba, dWx, dbx, dL, None, ws, gs)
-        stream.wait_stream(gs)
-        for _ in range(args.warmup):
-            g.replay()
-        torch.cuda.synchronize()
-        gev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
-        for k in range(args.steps):
-            flush.zero_()
-            gev[k][0].record(stream)
-            g.replay()
-            gev[k][1].record(stream)
-        torch.cuda.synchronize()
-        if R.rglru_sync_status(saved) != R.OK or R.rglru_sync_status(ws) != R.OK:
-            raise RuntimeError("look-back timeout in the graph replays")
-        g_ms = sum(e[0].elapsed_time(e[1]) for e in gev)
-        graph = {"ms_per_step": g_ms / args.steps,
-                 "value": tokens * args.steps / (g_ms / 1e3), "unit": UNIT,
-                 "how": "forward + backward calls captured once in a CUDA graph, replayed; "
-                        "L2 flushed before every replay"}
-        del g
 
     # end to end through the C ABI with host buffers: H2D of x and dy from pinned memory, the
     # step, D2H of every result (y, dx and the parameter gradients), all inside the events
@@ -353,6 +355,8 @@ def run_ours(args, rank, world, local):
                    "k": wl.k, "nblk": wl.nblk, "mode": wl.mode, "grad": "bf16",
                    "carry": "f32", "seed": "2 + rank",
                    "l2": "flushed by a 256 MiB write before every timed step",
+                   "launch": "the fwd + bwd calls captured once in a CUDA graph, replayed once "
+                             "a step (key eager: the calls issued directly)",
                    "parallelism": f"dp{world} (independent batches, no collective)"},
         "fwd_ms": {"median": statistics.median(fwd_ms), "min": min(fwd_ms), "max": max(fwd_ms),
                    "mean": statistics.fmean(fwd_ms)},
@@ -383,7 +387,7 @@ def run_ours(args, rank, world, local):
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": launches,
         "clocks": clk,
-        "graph": graph,
+        "eager": eager,
         "memory": memory_footprint(sh, wl),
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
