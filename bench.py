@@ -457,7 +457,67 @@ def decode_step(flush, peak, W=2048, k=128, reps=20):
             out["roofline_B256"] = {"bound": "hbm", "unit": "GB/s", "achieved": gbs, "peak": peak,
                                     "frac": (gbs / peak) if peak else None,
                                     "algorithmic_bytes": nbytes}
+    out["stack_B256"] = decode_stack(flush, peak, W, k)
     return out
+
+
+def decode_stack(flush, peak, W=2048, k=128, B=256, L=48, reps=10):
+    """One decode token through a stack of L layers at batch B: each layer has its own weights,
+    constants and carried states, and layer l's y is layer l + 1's x.  The L steps are captured
+    once in a CUDA graph and replayed, the L2 flushed before each replay, so the steps follow
+    one another on the GPU as in a graph-captured serving loop.  Weights and states of all
+    layers (L x 4 MB) exceed the L2, so each step reads its operands from HBM.  Reports
+    microseconds per layer step and its bytes against the measured copy bandwidth."""
+    import torch
+    from linear_recurrent_rnn_gb300 import librglru as R
+    from linear_recurrent_rnn_gb300.inputs import Workload, generate
+    sh = R.make_shape(B, 1, W, W // k, R.BF16, R.BF16, R.CANONICAL)
+    layers, xs = [], []
+    for l in range(L):
+        inp = generate(Workload("decode", B, 1, W, k, "bf16", "canonical", h0_std=1.0), 100 + l)
+        d = {n: (v.cuda() if isinstance(v, torch.Tensor) else v) for n, v in inp.items()}
+        layers.append((d["Wa"], d["ba"], d["Wx"], d["bx"], d["Lambda"], d["h0"].clone()))
+        if l == 0:
+            xs.append(d["x"].reshape(B, W).contiguous())
+        xs.append(torch.empty(B, W, dtype=xs[0].dtype, device="cuda"))
+
+    def run(s):
+        for l, (Wa, ba, Wx, bx, Lam, h) in enumerate(layers):
+            R.rglru_step(sh, xs[l], Wa, ba, Wx, bx, Lam, None, h, xs[l + 1], h, s)
+
+    stream = torch.cuda.current_stream()
+    run(stream)
+    torch.cuda.synchronize()
+    gs = torch.cuda.Stream()
+    gs.wait_stream(stream)
+    g = torch.cuda.CUDAGraph()
+    nc0 = R.rglru_kernel_launches()
+    with torch.cuda.graph(g, stream=gs):
+        run(gs)
+    launches = R.rglru_kernel_launches() - nc0
+    stream.wait_stream(gs)
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    ts = []
+    for _ in range(reps):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        g.replay()
+        b.record(stream)
+        torch.cuda.synchronize()
+        ts.append(a.elapsed_time(b))
+    del g
+    us = statistics.median(ts) * 1e3 / L
+    nbytes = 2 * (W // k) * k * k * 2 + B * W * (2 + 4 + 4 + 2)
+    gbs = nbytes / (us / 1e6) / 1e9
+    return {"layers": L, "launches_per_token": launches, "us_per_layer_step": us,
+            "tokens_per_s_per_layer": B / (us / 1e6),
+            "roofline": {"bound": "hbm", "unit": "GB/s", "achieved": gbs, "peak": peak,
+                         "frac": (gbs / peak) if peak else None, "algorithmic_bytes": nbytes},
+            "how": "L layer steps captured once in a CUDA graph, replayed; L2 flushed before "
+                   "each replay; weights and states of all layers exceed the L2"}
 
 
 def varlen_measure(flush, peak, reps=10, W=2048, k=128, T=8192, seed=5):

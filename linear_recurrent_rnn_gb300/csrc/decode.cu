@@ -245,21 +245,32 @@ __global__ void __launch_bounds__(STC_THREADS, 1)
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 2);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-  // the operand loads go out first: thread 0 initialises the barriers and issues them at once
+  // Launched with programmatic stream serialisation: up to griddep_wait nothing touches
+  // global memory (barrier set-up, the TMEM allocation, the tensor-map prefetch), so this part
+  // overlaps the end of the kernel before it on the stream; every read and write of the step's
+  // operands comes after the wait.
   if (threadIdx.x == 0) {
     tc::mbar_init(full, 1);
     tc::mbar_init(done, 1);
     tc::fence_barrier_init();
+    tc::prefetch_tmap(&tm_x);
+    tc::prefetch_tmap(&tm_wa);
+    tc::prefetch_tmap(&tm_wx);
+  }
+  if (warp == 1) {
+    tc::tmem_alloc(tmem_holder, 2 * STC_N);
+    tc::tmem_relinquish();
+  }
+  tc::griddep_wait();
+  tc::griddep_launch_dependents();
+  // the operand loads go out first: thread 0 issues them at once
+  if (threadIdx.x == 0) {
     tc::mbar_expect_tx(full, XB + 4 * WS);
     for (int s = 0; s < k / 16; ++s)
       tc::tma_load_2d(s_x + s * STC_SLAB, &tm_x, full, blk * k + 16 * s, row0);
     for (int m = 0; m < 2; ++m)
       for (int s = 0; s < 2; ++s)
         tc::tma_load_2d(s_w[m] + s * WS, m ? &tm_wx : &tm_wa, full, j0 + 16 * s, blk * k);
-  }
-  if (warp == 1) {
-    tc::tmem_alloc(tmem_holder, 2 * STC_N);
-    tc::tmem_relinquish();
   }
   // this thread's row and 16 channels: state segment, reset flag, and (warp 2) the channel
   // constants, all requested before any wait
@@ -418,7 +429,20 @@ cudaError_t launch_step(const Dims& d, const void* x, const void* Wa, const floa
     e = cudaFuncSetAttribute(k_step_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     const dim3 grid((unsigned)(d.nblk * (d.k / STC_N)), (unsigned)((d.B + STC_ROWS - 1) / STC_ROWS));
-    k_step_tc<<<grid, STC_THREADS, smem, s>>>(mx, mwa, mwx, a);
+    // programmatic stream serialisation: the kernel's set-up overlaps the end of the kernel
+    // before it on the stream (a decode loop's previous step or layer)
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(STC_THREADS);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, k_step_tc, mx, mwa, mwx, a);
+    if (e != cudaSuccess) return e;
     note_launches(1);
     return cudaGetLastError();
   }

@@ -166,6 +166,18 @@ __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 
+// ---------------------------------------------------------------- programmatic launch
+// In a kernel launched with programmatic stream serialisation: griddep_wait returns once the
+// grids before it on the stream have completed and their memory is visible (at once without
+// such a dependency); griddep_launch_dependents lets the next grid on the stream start its
+// launch before this one ends.
+__device__ __forceinline__ void griddep_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- named barriers
 // bar.sync / bar.arrive are the warp-aligned forms: the warp is reconverged first.
 __device__ __forceinline__ void named_bar(int id, int threads) {
