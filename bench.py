@@ -360,9 +360,10 @@ def run_ours(args, rank, world, local):
                    "parallelism": f"dp{world} (independent batches, no collective)"},
         "fwd_ms": {"median": statistics.median(fwd_ms), "min": min(fwd_ms), "max": max(fwd_ms),
                    "mean": statistics.fmean(fwd_ms)},
-        "bwd_ms": {"median": statistics.median(bwd_ms), "min": min(bwd_ms), "max": max(bwd_ms)},
+        "bwd_ms": {"median": statistics.median(bwd_ms), "min": min(bwd_ms), "max": max(bwd_ms),
+                   "mean": statistics.fmean(bwd_ms)},
         "fwd_bwd_ms": {"median": statistics.median(step_list), "min": min(step_list),
-                       "max": max(step_list)},
+                       "max": max(step_list), "mean": statistics.fmean(step_list)},
         "hbm_fraction_of_8TBps": (fwd_b + bwd_b) / (step_ms / 1e3) / 8e12,
         "roofline": {"bound": "hbm", "unit": "GB/s", "kernel": "k_fused_bwd",
                      "achieved": achieved, "peak": peak,
