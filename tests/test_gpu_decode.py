@@ -75,3 +75,45 @@ def test_decode_loop_reproduces_forward(B):
                                   o["Lambda"], o["reset_mask"], None, o["h0"])
     assert_close("y", np.stack([host(y) for y in ys], axis=1), yr, io="bf16", kind="out")
     assert_close("hT", host(h), hr, io="bf16", kind="out")
+
+
+@pytest.mark.parametrize("graph", [False, True], ids=["eager", "graph"])
+def test_decode_steps_back_to_back(graph):
+    """The steps of a decode loop with nothing launched between them (every token's x, reset
+    flags and y prepared beforehand, the state updated in place), issued directly or captured
+    in a CUDA graph and replayed: each step reads the state the step before it wrote, so the
+    loop equals the forward over the whole sequence."""
+    wl = Workload("decode-back-to-back", 96, 24, 256, 128, "bf16", "canonical", reset_p=0.05,
+                  h0_std=1.0)
+    inp = generate(wl, 12)
+    d = {k: dev(v) if isinstance(v, torch.Tensor) else v for k, v in inp.items()}
+    sh = R.make_shape(wl.B, 1, wl.W, wl.nblk, R.BF16, R.BF16, R.CANONICAL)
+    xs = [d["x"][:, t, :].contiguous() for t in range(wl.T)]
+    rs = [d["reset_mask"][:, t].contiguous() for t in range(wl.T)]
+    ys = [torch.empty(wl.B, wl.W, dtype=torch.bfloat16, device="cuda") for _ in range(wl.T)]
+    h = d["h0"].clone()
+
+    def loop(s=None):
+        for t in range(wl.T):
+            R.rglru_step(sh, xs[t], d["Wa"], d["ba"], d["Wx"], d["bx"], d["Lambda"], rs[t], h,
+                         ys[t], h, s)
+
+    torch.cuda.synchronize()
+    if graph:
+        gs = torch.cuda.Stream()
+        gs.wait_stream(torch.cuda.current_stream())
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=gs):
+            loop(gs)
+        torch.cuda.current_stream().wait_stream(gs)
+        h.copy_(d["h0"])
+        torch.cuda.synchronize()
+        g.replay()
+    else:
+        loop()
+    torch.cuda.synchronize()
+    o = oracle_inputs(inp)
+    yr, hr = oracle.fused_forward(R.CANONICAL, o["x"], o["Wa"], o["ba"], o["Wx"], o["bx"],
+                                  o["Lambda"], o["reset_mask"], None, o["h0"])
+    assert_close("y", np.stack([host(y) for y in ys], axis=1), yr, io="bf16", kind="out")
+    assert_close("hT", host(h), hr, io="bf16", kind="out")
