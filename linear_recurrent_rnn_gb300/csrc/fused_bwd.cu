@@ -30,8 +30,8 @@
 //      gradients; dlr, dli go to shared memory as bf16 hi + lo pairs (v = hi + lo to ~2^-16),
 //      the direct dx term into the TMEM dx accumulator.
 //   5. MMA: dx^T += Wa (dlr_hi + dlr_lo)^T + Wx (dli_hi + dli_lo)^T on top of the direct term;
-//      dWa += x^T (dlr_hi + dlr_lo), dWx += x^T (dli_hi + dli_lo) accumulated in TMEM over the
-//      CTA's tiles.  The lo halves keep both products at float32-like accuracy: dl can be O(1)
+//      dWa += x^T (dlr_hi + dlr_lo), dWx += x^T (dli_hi + dli_lo) (both in one N = 256
+//      product per 16 tokens) accumulated in TMEM over the CTA's tiles.  The lo halves keep both products at float32-like accuracy: dl can be O(1)
 //      and a bf16-rounded dl alone would cost ~2^-9 |dl| in dx.
 //   6. dx TMEM -> bf16/f32 -> smem -> TMA store, done after pass 1 of the next tile, so the
 //      step-5 MMAs run while the scan warps work on that pass.
@@ -62,10 +62,14 @@ constexpr uint32_t T_BYTES = FUSED_C * FUSED_K * 2;  // one 64 x 128 bf16 tile
 constexpr uint32_t SLAB_X = FUSED_C * 32;            // 16 channels x 64 tokens
 constexpr uint32_t SLAB_W = FUSED_K * 32;            // 16 out-channels x 128 in-rows
 constexpr uint32_t SLAB_D = FUSED_K * 32;            // 16 tokens x 128 channels (dl buffers)
+// The dl buffers (hi, then lo): per 16-token group the dlr slab, then the dli slab, so that a
+// group's 256 rows are one K-major operand of the dW products (N = 256: dWa and dWx at once).
+constexpr uint32_t DL_GSTR = 2 * SLAB_D;
 constexpr uint32_t DY_ROW = FUSED_K * 2;             // dy tiles: [token][channel], unswizzled
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t COL_LR = 0, COL_LI = 64, COL_DX = 128, COL_HP = 192, COL_DWA = 256,
                    COL_DWX = 384;
+static_assert(COL_DWX == COL_DWA + FUSED_K, "the dW products write dWa and dWx as one N = 256");
 constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;  // 2 s: a pipeline wait never lasts this
 constexpr uint32_t XCH_BYTES = NPART * FUSED_K * 16 + FUSED_K * 4;  // part aggregates + carry
 // W (2) + x/dy stages (2 x 2) + dl buffers (4) + bf16 dx staging (1) tiles, exchange, barriers
@@ -152,7 +156,7 @@ __device__ __forceinline__ void store_dl8(uint8_t* hi_buf, uint8_t* lo_buf, int 
   split_hi_lo(v[1], hi.y, lo.y);
   split_hi_lo(v[2], hi.z, lo.z);
   split_hi_lo(v[3], hi.w, lo.w);
-  const uint32_t at = (tu >> 4) * SLAB_D + j * 32 + ((((tu >> 3) & 1) ^ ((j >> 2) & 1)) << 4);
+  const uint32_t at = (tu >> 4) * DL_GSTR + j * 32 + ((((tu >> 3) & 1) ^ ((j >> 2) & 1)) << 4);
   *reinterpret_cast<uint4*>(hi_buf + at) = hi;
   *reinterpret_cast<uint4*>(lo_buf + at) = lo;
 }
@@ -441,8 +445,8 @@ __device__ __forceinline__ void bwd_pass2b(uint32_t tcol, int tb, int j,
     }
     static_assert(GRP == 8, "the dl stores take 8 tokens");
     if (LGM == LGM_NONE) {
-      store_dl8(s_dl, s_dl + T_BYTES, tb + g * GRP, j, o_r);
-      store_dl8(s_dl + 2 * T_BYTES, s_dl + 3 * T_BYTES, tb + g * GRP, j, o_i);
+      store_dl8(s_dl, s_dl + 2 * T_BYTES, tb + g * GRP, j, o_r);
+      store_dl8(s_dl + SLAB_D, s_dl + 2 * T_BYTES + SLAB_D, tb + g * GRP, j, o_i);
     } else {
 #pragma unroll
       for (int q = 0; q < GRP / 2; ++q) {
@@ -498,7 +502,7 @@ __global__ void __maxnreg__(MAXREG)
   uint8_t* s_wa = smem;                             // LG: the identity
   uint8_t* s_wx = smem + W_BYTES;
   uint8_t* s_in = smem + (LG ? ID_BYTES : 2 * W_BYTES);  // stage s: x, dy (+ LG: logit planes)
-  uint8_t* s_dl = s_in + STAGES * STB;              // r_hi, r_lo, i_hi, i_lo (none in LG)
+  uint8_t* s_dl = s_in + STAGES * STB;              // dl hi, dl lo (none in LG)
   uint8_t* s_dx = s_dl + (LG ? 0 : 4 * T_BYTES);    // dx staging [token][channel]
   float4* s_agg = reinterpret_cast<float4*>(s_dx + T_BYTES);       // [part][k]
   float* s_cin = reinterpret_cast<float*>(s_agg + NPART * FUSED_K);  // [k]
@@ -589,7 +593,7 @@ __global__ void __maxnreg__(MAXREG)
     const bool leader = tc::elect_one();
     constexpr uint32_t id_lg = tc::idesc_bf16(128, FUSED_C, 1, 0);  // W^T x^T
     constexpr uint32_t id_dx = tc::idesc_bf16(128, FUSED_C, 0, 1);  // W dl^T
-    constexpr uint32_t id_dw = tc::idesc_bf16(128, FUSED_K, 1, 0);  // x^T dl
+    constexpr uint32_t id_dw = tc::idesc_bf16(128, 2 * FUSED_K, 1, 0);  // x^T [dlr dli]
     ctl.wait(w_full, 0);
     const uint32_t wa = tc::smem_u32(s_wa), wx = tc::smem_u32(s_wx);
     const uint32_t dl0 = tc::smem_u32(s_dl);
@@ -637,7 +641,7 @@ __global__ void __maxnreg__(MAXREG)
       tc::tc_fence_after();
       if (leader) {
         // dx^T[in][tok] += W[in][out] dl^T[out][tok]: A = W K-major (one 16-column slab per K
-        // step), B = dl buffer MN-major (16-token groups 4 KB apart, 8-row groups 256 B).
+        // step), B = dl buffer MN-major (16-token groups 8 KB apart, 8-row groups 256 B).
 #pragma unroll
         for (int kk = 0; kk < FUSED_K / 16; ++kk) {
           const uint64_t a_a = tc::smem_desc_sw32(wa + kk * SLAB_W, 16, 256);
@@ -645,29 +649,27 @@ __global__ void __maxnreg__(MAXREG)
 #pragma unroll
           for (int h = 0; h < 2; ++h) {  // hi, then lo halves of dl
             tc::mma_bf16(tmem + COL_DX, a_a,
-                         tc::smem_desc_sw32(dl0 + (0 + h) * T_BYTES + kk * 512, SLAB_D, 256),
+                         tc::smem_desc_sw32(dl0 + 2 * h * T_BYTES + kk * 512, DL_GSTR, 256),
                          id_dx, 1);
             tc::mma_bf16(tmem + COL_DX, a_x,
-                         tc::smem_desc_sw32(dl0 + (2 + h) * T_BYTES + kk * 512, SLAB_D, 256),
+                         tc::smem_desc_sw32(dl0 + 2 * h * T_BYTES + SLAB_D + kk * 512, DL_GSTR,
+                                            256),
                          id_dx, 1);
           }
         }
         tc::mma_commit(dx_full);
-        // dW[in][out] += x^T[in][tok] dl[tok][out]: A = x tile MN-major (16-channel slabs 2 KB
-        // apart), B = dl buffer K-major (one 16-token group per K step).
+        // [dWa dWx][in][out] += x^T[in][tok] [dlr dli][tok][out]: A = x tile MN-major
+        // (16-channel slabs 2 KB apart), B = a 16-token group of the dl buffer K-major (dlr
+        // rows, then dli rows), D = the 256 columns of dWa and dWx.
         const uint32_t xs = tc::smem_u32(s_in + st * 2 * T_BYTES);
 #pragma unroll
         for (int kk = 0; kk < FUSED_C / 16; ++kk) {
           const uint64_t adesc = tc::smem_desc_sw32(xs + kk * 512, SLAB_X, 256);
           const uint32_t acc0 = (it > 0 || kk > 0) ? 1u : 0u;
           tc::mma_bf16(tmem + COL_DWA, adesc,
-                       tc::smem_desc_sw32(dl0 + 0 * T_BYTES + kk * SLAB_D, 16, 256), id_dw, acc0);
+                       tc::smem_desc_sw32(dl0 + kk * DL_GSTR, 16, 256), id_dw, acc0);
           tc::mma_bf16(tmem + COL_DWA, adesc,
-                       tc::smem_desc_sw32(dl0 + 1 * T_BYTES + kk * SLAB_D, 16, 256), id_dw, 1);
-          tc::mma_bf16(tmem + COL_DWX, adesc,
-                       tc::smem_desc_sw32(dl0 + 2 * T_BYTES + kk * SLAB_D, 16, 256), id_dw, acc0);
-          tc::mma_bf16(tmem + COL_DWX, adesc,
-                       tc::smem_desc_sw32(dl0 + 3 * T_BYTES + kk * SLAB_D, 16, 256), id_dw, 1);
+                       tc::smem_desc_sw32(dl0 + 2 * T_BYTES + kk * DL_GSTR, 16, 256), id_dw, 1);
         }
         tc::mma_commit(dl_empty);
         tc::mma_commit(&in_empty[st]);
