@@ -218,12 +218,26 @@ __device__ __forceinline__ void bwd_pass1(uint32_t tcol, uint32_t xb0, uint32_t 
       tc::tmem_ld(tcol + COL_LR + (g + 1) * GRP, nr);
       tc::tmem_ld(tcol + COL_LI + (g + 1) * GRP, ni);
     }
+    // Packed-sequence kernels: the group's x and dy requested together before any is used
+    // (their register allocation spills less so); the others load each token pair where it
+    // is used.
+    float dyg[GRP];
+    if (VARLEN) {
+#pragma unroll
+      for (int q = 0; q < GRP / 2; ++q) {
+        const int u = g * GRP + 2 * q;
+        xr[u / 2] = tok_raw(xb0, xb1, u) | (tok_raw(xb0, xb1, u + 1) << 16);
+        dyg[2 * q] = lds_bf16(dyb + u * DY_ROW);
+        dyg[2 * q + 1] = lds_bf16(dyb + (u + 1) * DY_ROW);
+      }
+    }
 #pragma unroll
     for (int q = 0; q < GRP / 2; ++q) {
       const int u = g * GRP + 2 * q;
-      xr[u / 2] = tok_raw(xb0, xb1, u) | (tok_raw(xb0, xb1, u + 1) << 16);
+      if (!VARLEN) xr[u / 2] = tok_raw(xb0, xb1, u) | (tok_raw(xb0, xb1, u + 1) << 16);
       const float2 xv = bf16x2_unpack(xr[u / 2]);
-      float2 dyv = make_float2(lds_bf16(dyb + u * DY_ROW), lds_bf16(dyb + (u + 1) * DY_ROW));
+      float2 dyv = VARLEN ? make_float2(dyg[2 * q], dyg[2 * q + 1])
+                          : make_float2(lds_bf16(dyb + u * DY_ROW), lds_bf16(dyb + (u + 1) * DY_ROW));
       const float2 lr = make_float2(vr[2 * q], vr[2 * q + 1]);
       const float2 li = make_float2(vi[2 * q], vi[2 * q + 1]);
       float2 abar, mi, r, i;
@@ -398,11 +412,21 @@ __device__ __forceinline__ void bwd_pass2b(uint32_t tcol, int tb, int j,
       tc::tmem_ld(tcol + COL_DX + (g - 1) * GRP, nh);
     }
     float2 o_r[GRP / 2], o_i[GRP / 2];  // tokens (u, u + 1) of the two pairs
+    float dyg[GRP];  // packed-sequence kernels: the group's dy first, as in pass 1
+    if (VARLEN) {
+#pragma unroll
+      for (int q = GRP / 2 - 1; q >= 0; --q) {
+        const int u = g * GRP + 2 * q;
+        dyg[2 * q + 1] = lds_bf16(dyb + (u + 1) * DY_ROW);
+        dyg[2 * q] = lds_bf16(dyb + u * DY_ROW);
+      }
+    }
 #pragma unroll
     for (int q = GRP / 2 - 1; q >= 0; --q) {
       const int u = g * GRP + 2 * q;
       const float2 xv = bf16x2_unpack(xr[u / 2]);
-      float2 dyv = make_float2(lds_bf16(dyb + u * DY_ROW), lds_bf16(dyb + (u + 1) * DY_ROW));
+      float2 dyv = VARLEN ? make_float2(dyg[2 * q], dyg[2 * q + 1])
+                          : make_float2(lds_bf16(dyb + u * DY_ROW), lds_bf16(dyb + (u + 1) * DY_ROW));
       if (GENERAL) {
         if (VARLEN) {
           if ((sq.emask >> u) & 1u) dyv.x += seqb_dhT(sq, u);
