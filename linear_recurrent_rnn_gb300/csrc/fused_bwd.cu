@@ -512,6 +512,226 @@ __device__ __forceinline__ void bwd_pass2b(uint32_t tcol, int tb, int j,
   tc::tmem_st_wait();
 }
 
+// The general passes: tiles with a reset, a packed-sequence start or end, tokens past T or a
+// channel outside the near regime, a few tiles a launch.  They walk the part's token groups in
+// a loop (not unrolled) and keep no per-token registers across passes: x comes from the
+// staged tile and the decay is recomputed from the parked r (bitwise as pass 1 computed it),
+// so their code stays small and leaves the fast passes' code compact (inlined fully unrolled,
+// the packed-sequence variants alone slowed every tile of their kernel by a quarter).
+// The decay of a token pair from its r, as gates_any2 computes it, then the token masks:
+// 0 at a reset, 1 past T.
+__device__ __forceinline__ float2 gen_decay(float2 r, const GateK& k, uint32_t rmask, int u,
+                                            int valid) {
+  const float2 la = mul2(bc2(k.nk), r);
+  float2 p = fma2(la, bc2(DECAY_P3), bc2(DECAY_P2));
+  p = fma2(la, p, bc2(DECAY_P1));
+  p = fma2(la, p, bc2(1.0f));
+  float2 a = fma2(la, p, bc2(1.0f));
+  if (!(la.x > NEAR_LA)) a.x = ex2_approx(la.x * LOG2E);
+  if (!(la.y > NEAR_LA)) a.y = ex2_approx(la.y * LOG2E);
+  if ((rmask >> u) & 1u) a.x = 0.0f;
+  if ((rmask >> (u + 1)) & 1u) a.y = 0.0f;
+  if (u >= valid) a.x = 1.0f;
+  if (u + 1 >= valid) a.y = 1.0f;
+  return a;
+}
+
+// General pass 1: as the fast one (gates once, m i / r / i parked, the part's maps), with the
+// token masks and packed-sequence starts and ends.
+template <bool VARLEN>
+__device__ __forceinline__ void bwd_pass1_gen(uint32_t tcol, uint32_t xb0, uint32_t xb1,
+                                              uint32_t dyb, const GateK& gk, uint32_t rmask,
+                                              int valid, const SeqB& sq, float& P, float& fB,
+                                              float& S) {
+  P = 1.0f;
+  fB = 0.0f;
+  S = 0.0f;
+#pragma unroll 1
+  for (int g = 0; g < PT / GRP; ++g) {
+    float vr[GRP], vi[GRP], m4[GRP];
+    tc::tmem_ld(tcol + COL_LR + g * GRP, vr);
+    tc::tmem_ld(tcol + COL_LI + g * GRP, vi);
+    tc::tmem_ld_wait();
+    tc::reg_fence(vr);
+    tc::reg_fence(vi);
+#pragma unroll
+    for (int q = 0; q < GRP / 2; ++q) {
+      const int u = g * GRP + 2 * q;
+      const float2 xv =
+          bf16x2_unpack(tok_raw(xb0, xb1, u) | (tok_raw(xb0, xb1, u + 1) << 16));
+      float2 dyv = make_float2(lds_bf16(dyb + u * DY_ROW), lds_bf16(dyb + (u + 1) * DY_ROW));
+      float2 abar, mi, r, i;
+      gates_any2(make_float2(vr[2 * q], vr[2 * q + 1]), make_float2(vi[2 * q], vi[2 * q + 1]),
+                 gk, abar, mi, r, i);
+      if ((rmask >> u) & 1u) {
+        abar.x = 0.0f;
+        mi.x = i.x;
+      }
+      if ((rmask >> (u + 1)) & 1u) {
+        abar.y = 0.0f;
+        mi.y = i.y;
+      }
+      if (u >= valid) {
+        abar.x = 1.0f;
+        mi.x = 0.0f;
+        dyv.x = 0.0f;
+      }
+      if (u + 1 >= valid) {
+        abar.y = 1.0f;
+        mi.y = 0.0f;
+        dyv.y = 0.0f;
+      }
+      float2 bv = mul2(mi, xv);
+      float2 ach = abar;  // the chains' decay
+      if (VARLEN && (sq.smask | sq.emask)) {
+        if ((sq.smask >> u) & 1u) bv.x = fmaf(abar.x, seqb_h0(sq, u), bv.x);
+        if ((sq.smask >> (u + 1)) & 1u) bv.y = fmaf(abar.y, seqb_h0(sq, u + 1), bv.y);
+        ach = chain_decay(sq, u, abar);
+        if ((sq.emask >> u) & 1u) dyv.x += seqb_dhT(sq, u);
+        if ((sq.emask >> (u + 1)) & 1u) dyv.y += seqb_dhT(sq, u + 1);
+      }
+      fB = fmaf(ach.x, fB, bv.x);
+      P *= ach.x;
+      S = fmaf(P, dyv.x, S);
+      fB = fmaf(ach.y, fB, bv.y);
+      P *= ach.y;
+      S = fmaf(P, dyv.y, S);
+      m4[2 * q] = mi.x;
+      m4[2 * q + 1] = mi.y;
+      vr[2 * q] = r.x;
+      vr[2 * q + 1] = r.y;
+      vi[2 * q] = i.x;
+      vi[2 * q + 1] = i.y;
+    }
+    tc::tmem_st(tcol + COL_LR + g * GRP, m4);
+    tc::tmem_st(tcol + COL_LI + g * GRP, vr);
+    tc::tmem_st(tcol + COL_HP + g * GRP, vi);
+  }
+  tc::tmem_st_wait();
+}
+
+// General pass 2a: h_{t-1} of every token, from the decay recomputed from r.
+template <bool VARLEN>
+__device__ __forceinline__ void bwd_pass2a_gen(uint32_t tcol, uint32_t xb0, uint32_t xb1,
+                                               const GateK& gk, uint32_t rmask, int valid,
+                                               const SeqB& sq, float h) {
+#pragma unroll 1
+  for (int g = 0; g < PT / GRP; ++g) {
+    float m4[GRP], r4[GRP], h4[GRP];
+    tc::tmem_ld(tcol + COL_LR + g * GRP, m4);
+    tc::tmem_ld(tcol + COL_LI + g * GRP, r4);
+    tc::tmem_ld_wait();
+    tc::reg_fence(m4);
+    tc::reg_fence(r4);
+#pragma unroll
+    for (int q = 0; q < GRP / 2; ++q) {
+      const int u = g * GRP + 2 * q;
+      const float2 xv =
+          bf16x2_unpack(tok_raw(xb0, xb1, u) | (tok_raw(xb0, xb1, u + 1) << 16));
+      const float2 ab = gen_decay(make_float2(r4[2 * q], r4[2 * q + 1]), gk, rmask, u, valid);
+      const float2 bv = mul2(make_float2(m4[2 * q], m4[2 * q + 1]), xv);
+      // at a sequence start the state before the token is the sequence's initial state
+      if (VARLEN && ((sq.smask >> u) & 1u)) h = seqb_h0(sq, u);
+      h4[2 * q] = h;
+      h = fmaf(ab.x, h, bv.x);
+      if (VARLEN && ((sq.smask >> (u + 1)) & 1u)) h = seqb_h0(sq, u + 1);
+      h4[2 * q + 1] = h;
+      h = fmaf(ab.y, h, bv.y);
+    }
+    tc::tmem_st(tcol + COL_DX + g * GRP, h4);
+  }
+  tc::tmem_st_wait();
+}
+
+// General pass 2b: as the fast one, the decay recomputed from r, with the token masks and the
+// packed-sequence ends (dy += dhT) and starts (dh0 = a g).
+template <bool VARLEN, typename GT, int LGM>
+__device__ __forceinline__ void bwd_pass2b_gen(uint32_t tcol, int tb, int j, uint32_t xb0,
+                                               uint32_t xb1, uint32_t dyb, const GateK& gk,
+                                               uint32_t rmask, int valid, const SeqB& sq,
+                                               float cin, uint64_t* lg_free, uint8_t* s_dl,
+                                               float2& dsp, float2& dba, float2& dbx,
+                                               const DlOut& dlo) {
+  float gnext = cin, anext = 1.0f;
+#pragma unroll 1
+  for (int g = PT / GRP - 1; g >= 0; --g) {
+    float m4[GRP], r4[GRP], i4[GRP], h4[GRP];
+    tc::tmem_ld(tcol + COL_LR + g * GRP, m4);
+    tc::tmem_ld(tcol + COL_LI + g * GRP, r4);
+    tc::tmem_ld(tcol + COL_HP + g * GRP, i4);
+    tc::tmem_ld(tcol + COL_DX + g * GRP, h4);
+    tc::tmem_ld_wait();
+    tc::reg_fence(m4);
+    tc::reg_fence(r4);
+    tc::reg_fence(i4);
+    tc::reg_fence(h4);
+    if (g == 0) {  // every read of the logits columns has landed
+      tc::tc_fence_before();
+      __syncwarp();
+      if ((threadIdx.x & 31) == 0) tc::mbar_arrive(lg_free);
+    }
+    float2 o_r[GRP / 2], o_i[GRP / 2];
+#pragma unroll
+    for (int q = GRP / 2 - 1; q >= 0; --q) {
+      const int u = g * GRP + 2 * q;
+      const float2 xv =
+          bf16x2_unpack(tok_raw(xb0, xb1, u) | (tok_raw(xb0, xb1, u + 1) << 16));
+      float2 dyv = make_float2(lds_bf16(dyb + u * DY_ROW), lds_bf16(dyb + (u + 1) * DY_ROW));
+      if (VARLEN) {
+        if ((sq.emask >> u) & 1u) dyv.x += seqb_dhT(sq, u);
+        if ((sq.emask >> (u + 1)) & 1u) dyv.y += seqb_dhT(sq, u + 1);
+      }
+      if (u >= valid) dyv.x = 0.0f;
+      if (u + 1 >= valid) dyv.y = 0.0f;
+      const float2 r = make_float2(r4[2 * q], r4[2 * q + 1]);
+      const float2 abar = gen_decay(r, gk, rmask, u, valid);
+      const float2 ach = VARLEN ? chain_decay(sq, u, abar) : abar;  // 0 at starts
+      const float2 mi = make_float2(m4[2 * q], m4[2 * q + 1]);
+      const float2 i = make_float2(i4[2 * q], i4[2 * q + 1]);
+      float2 gv;
+      gv.y = fmaf(anext, gnext, dyv.y);
+      gv.x = fmaf(ach.y, gv.y, dyv.x);
+      gnext = gv.x;
+      anext = ach.x;
+      if (VARLEN && sq.p.dh0s) {  // d h0[s] = a g at the sequence's first token
+        float* dh0 = sq.p.dh0s + sq.w;
+        const int32_t* st = sq.p.seq_start + sq.t0;
+        if (((sq.smask >> u) & 1u) && sq.ok) dh0[(size_t)st[u] * sq.p.W] = abar.x * gv.x;
+        if (((sq.smask >> (u + 1)) & 1u) && sq.ok) dh0[(size_t)st[u + 1] * sq.p.W] = abar.y * gv.y;
+      }
+      const float2 nw = mul2(mul2(i, i), make_float2(rcp_approx(-mi.x), rcp_approx(-mi.y)));
+      float2 alpha = mul2(abar, fma2(mul2(abar, xv), nw, make_float2(h4[2 * q], h4[2 * q + 1])));
+      if (abar.x == 0.0f || mi.x == 0.0f) alpha.x = 0.0f;
+      if (abar.y == 0.0f || mi.y == 0.0f) alpha.y = 0.0f;
+      const float2 dla = mul2(gv, alpha);
+      const float2 dd = mul2(gv, mi);  // direct dx term
+      o_r[q] = mul2(mul2(dla, bc2(gk.nk)), mul2(r, fma2(r, bc2(-1.0f), bc2(1.0f))));
+      o_i[q] = mul2(mul2(dd, xv), fma2(i, bc2(-1.0f), bc2(1.0f)));
+      dsp = fma2(dla, r, dsp);
+      dba = add2(dba, o_r[q]);
+      dbx = add2(dbx, o_i[q]);
+      h4[2 * q] = dd.x;
+      h4[2 * q + 1] = dd.y;
+    }
+    if (LGM == LGM_NONE) {
+      store_dl8(s_dl, s_dl + 2 * T_BYTES, tb + g * GRP, j, o_r);
+      store_dl8(s_dl + SLAB_D, s_dl + 2 * T_BYTES + SLAB_D, tb + g * GRP, j, o_i);
+    } else {
+#pragma unroll
+      for (int q = 0; q < GRP / 2; ++q) {
+        const int u = g * GRP + 2 * q;
+        const size_t idx = dlo.idx0 + (size_t)u * dlo.W;
+        store_dl_pair<GT, LGM>(dlo.dlr, dlo.plane, idx, dlo.W, o_r[q], u < dlo.valid,
+                               u + 1 < dlo.valid);
+        store_dl_pair<GT, LGM>(dlo.dli, dlo.plane, idx, dlo.W, o_i[q], u < dlo.valid,
+                               u + 1 < dlo.valid);
+      }
+    }
+    tc::tmem_st(tcol + COL_DX + g * GRP, h4);
+  }
+  tc::tmem_st_wait();
+}
+
 template <typename GT, bool VARLEN, int LGM>
 __global__ void __maxnreg__(MAXREG)
     k_fused_bwd(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_dy,
@@ -796,8 +1016,8 @@ __global__ void __maxnreg__(MAXREG)
         if (fast)
           bwd_pass1<false, VARLEN>(tcol, xb0, xb1, dyb, gk, 0u, PT, ab, xr, SeqB{p, 0u, 0u, 0, 0}, P, fB, S);
         else
-          bwd_pass1<true, VARLEN>(tcol, xb0, xb1, dyb, gk, rmask, valid, ab, xr,
-                                  seqb(smask, emask, b, c), P, fB, S);
+          bwd_pass1_gen<VARLEN>(tcol, xb0, xb1, dyb, gk, rmask, valid, seqb(smask, emask, b, c),
+                                P, fB, S);
       }
 
       if (have) s_agg[part * FUSED_K + j] = make_float4(P, fB, P, S);  // the part's maps
@@ -877,8 +1097,9 @@ __global__ void __maxnreg__(MAXREG)
 
       // Pass 2a: h_{t-1} through the part, from the earlier parts' map applied to the tile's
       // entry state.
-      if (VARLEN && !fast)
-        bwd_pass2a<true, VARLEN>(tcol, xr, ab, seqb(smask, emask, b, c), fmaf(Fa, hin_tile, Fb));
+      if (!fast)
+        bwd_pass2a_gen<VARLEN>(tcol, xb0, xb1, gk, rmask, valid, seqb(smask, emask, b, c),
+                               fmaf(Fa, hin_tile, Fb));
       else
         bwd_pass2a<false, VARLEN>(tcol, xr, ab, SeqB{p, 0u, 0u, 0, 0}, fmaf(Fa, hin_tile, Fb));
 
@@ -908,9 +1129,9 @@ __global__ void __maxnreg__(MAXREG)
                                            SeqB{p, 0u, 0u, 0, 0}, cin, lg_empty, s_dl, dsp, dba,
                                            dbx, dlo);
       else
-        bwd_pass2b<true, VARLEN, GT, LGM>(tcol, tb, j, xr, dyb, gk.nk, valid, ab,
-                                          seqb(smask, emask, b, c), cin, lg_empty, s_dl, dsp,
-                                          dba, dbx, dlo);
+        bwd_pass2b_gen<VARLEN, GT, LGM>(tcol, tb, j, xb0, xb1, dyb, gk, rmask, valid,
+                                        seqb(smask, emask, b, c), cin, lg_empty, s_dl, dsp, dba,
+                                        dbx, dlo);
       tc::fence_proxy_async_smem();
       tc::tc_fence_before();
       __syncwarp();
