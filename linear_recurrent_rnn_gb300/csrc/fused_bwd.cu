@@ -167,15 +167,14 @@ __device__ __forceinline__ void store_dl8(uint8_t* hi_buf, uint8_t* lo_buf, int 
 // column = token of the part; the thread's columns of each region start at tcol.
 constexpr int GRP = 8;  // tokens per TMEM load / store group
 
-// Pass 1 (tokens ascending): the gates once; abar stays in registers, m i -> COL_LR and r ->
-// COL_LI (over the logits, already read), i -> COL_HP; returns the part's maps: forward
-// h -> P h + fB and reverse c -> P c + S, with P = prod abar and S = sum_t (prod of abar up
-// to t) dy_t.  GENERAL = false is the warp-uniform fast path: every token valid, no reset,
-// every decay in the near regime.
+// Pass 1, fast (tokens ascending; every token valid, no reset or packed-sequence boundary,
+// every decay in the near regime, a warp-uniform condition): the gates once; abar stays in
+// registers, m i -> COL_LR and r -> COL_LI (over the logits, already read), i -> COL_HP;
+// returns the part's maps: forward h -> P h + fB and reverse c -> P c + S, with P = prod abar
+// and S = sum_t (prod of abar up to t) dy_t.  The other tiles take the general passes below.
 // Packed sequences in a part: at a start token (smask) the token continues from its
 // sequence's initial state, h -> a h0[s] + m i x, so the recurrences take 0 for its decay while
-// ab keeps the true a (for the derivatives and dh0[s] = a g); at an end token (emask) dhT[s]
-// joins dy.
+// the derivatives keep the true a (and dh0[s] = a g); at an end token (emask) dhT[s] joins dy.
 struct SeqB {
   const BwdParams& p;  // the sequence arrays (seq_start, seq_end, h0s, dhTs, dh0s)
   uint32_t smask, emask;
@@ -196,11 +195,9 @@ __device__ __forceinline__ float2 chain_decay(const SeqB& sq, int u, float2 a) {
   return a;
 }
 
-template <bool GENERAL, bool VARLEN>
 __device__ __forceinline__ void bwd_pass1(uint32_t tcol, uint32_t xb0, uint32_t xb1, uint32_t dyb,
-                                          const GateK& gk, uint32_t rmask, int valid,
-                                          float2 (&ab)[PT / 2], uint32_t (&xr)[PT / 2],
-                                          const SeqB& sq, float& P, float& fB, float& S) {
+                                          const GateK& gk, float2 (&ab)[PT / 2],
+                                          uint32_t (&xr)[PT / 2], float& P, float& fB, float& S) {
   P = 1.0f;
   fB = 0.0f;
   S = 0.0f;
@@ -218,66 +215,22 @@ __device__ __forceinline__ void bwd_pass1(uint32_t tcol, uint32_t xb0, uint32_t 
       tc::tmem_ld(tcol + COL_LR + (g + 1) * GRP, nr);
       tc::tmem_ld(tcol + COL_LI + (g + 1) * GRP, ni);
     }
-    // Packed-sequence kernels: the group's x and dy requested together before any is used
-    // (their register allocation spills less so); the others load each token pair where it
-    // is used.
-    float dyg[GRP];
-    if (VARLEN) {
-#pragma unroll
-      for (int q = 0; q < GRP / 2; ++q) {
-        const int u = g * GRP + 2 * q;
-        xr[u / 2] = tok_raw(xb0, xb1, u) | (tok_raw(xb0, xb1, u + 1) << 16);
-        dyg[2 * q] = lds_bf16(dyb + u * DY_ROW);
-        dyg[2 * q + 1] = lds_bf16(dyb + (u + 1) * DY_ROW);
-      }
-    }
 #pragma unroll
     for (int q = 0; q < GRP / 2; ++q) {
       const int u = g * GRP + 2 * q;
-      if (!VARLEN) xr[u / 2] = tok_raw(xb0, xb1, u) | (tok_raw(xb0, xb1, u + 1) << 16);
+      xr[u / 2] = tok_raw(xb0, xb1, u) | (tok_raw(xb0, xb1, u + 1) << 16);
       const float2 xv = bf16x2_unpack(xr[u / 2]);
-      float2 dyv = VARLEN ? make_float2(dyg[2 * q], dyg[2 * q + 1])
-                          : make_float2(lds_bf16(dyb + u * DY_ROW), lds_bf16(dyb + (u + 1) * DY_ROW));
-      const float2 lr = make_float2(vr[2 * q], vr[2 * q + 1]);
-      const float2 li = make_float2(vi[2 * q], vi[2 * q + 1]);
+      const float2 dyv =
+          make_float2(lds_bf16(dyb + u * DY_ROW), lds_bf16(dyb + (u + 1) * DY_ROW));
       float2 abar, mi, r, i;
-      if (GENERAL) {
-        gates_any2(lr, li, gk, abar, mi, r, i);
-        if ((rmask >> u) & 1u) {
-          abar.x = 0.0f;
-          mi.x = i.x;
-        }
-        if ((rmask >> (u + 1)) & 1u) {
-          abar.y = 0.0f;
-          mi.y = i.y;
-        }
-        if (u >= valid) {
-          abar.x = 1.0f;
-          mi.x = 0.0f;
-          dyv.x = 0.0f;
-        }
-        if (u + 1 >= valid) {
-          abar.y = 1.0f;
-          mi.y = 0.0f;
-          dyv.y = 0.0f;
-        }
-      } else {
-        gates_near2_i(lr, li, gk, abar, mi, r, i);
-      }
-      float2 bv = mul2(mi, xv);
-      float2 ach = abar;  // the chains' decay
-      if (VARLEN && GENERAL && (sq.smask | sq.emask)) {
-        if ((sq.smask >> u) & 1u) bv.x = fmaf(abar.x, seqb_h0(sq, u), bv.x);
-        if ((sq.smask >> (u + 1)) & 1u) bv.y = fmaf(abar.y, seqb_h0(sq, u + 1), bv.y);
-        ach = chain_decay(sq, u, abar);
-        if ((sq.emask >> u) & 1u) dyv.x += seqb_dhT(sq, u);
-        if ((sq.emask >> (u + 1)) & 1u) dyv.y += seqb_dhT(sq, u + 1);
-      }
-      fB = fmaf(ach.x, fB, bv.x);
-      P *= ach.x;
+      gates_near2_i(make_float2(vr[2 * q], vr[2 * q + 1]), make_float2(vi[2 * q], vi[2 * q + 1]),
+                    gk, abar, mi, r, i);
+      const float2 bv = mul2(mi, xv);
+      fB = fmaf(abar.x, fB, bv.x);
+      P *= abar.x;
       S = fmaf(P, dyv.x, S);
-      fB = fmaf(ach.y, fB, bv.y);
-      P *= ach.y;
+      fB = fmaf(abar.y, fB, bv.y);
+      P *= abar.y;
       S = fmaf(P, dyv.y, S);
       ab[u / 2] = abar;
       m4[2 * q] = mi.x;
@@ -304,11 +257,10 @@ __device__ __forceinline__ void bwd_pass1(uint32_t tcol, uint32_t xb0, uint32_t 
   tc::tmem_st_wait();
 }
 
-// Pass 2a (tokens ascending): h_{t-1} of every token from the state h entering the part,
+// Pass 2a, fast (tokens ascending): h_{t-1} of every token from the state h entering the part,
 // parked in the dx columns (free once the previous tile's dx has been written out).
-template <bool GENERAL, bool VARLEN>
 __device__ __forceinline__ void bwd_pass2a(uint32_t tcol, const uint32_t (&xr)[PT / 2],
-                                           const float2 (&ab)[PT / 2], const SeqB& sq, float h) {
+                                           const float2 (&ab)[PT / 2], float h) {
   float m4[GRP];
   tc::tmem_ld(tcol + COL_LR, m4);
   tc::tmem_ld_wait();
@@ -322,11 +274,8 @@ __device__ __forceinline__ void bwd_pass2a(uint32_t tcol, const uint32_t (&xr)[P
       const int u = g * GRP + 2 * q;
       const float2 xv = bf16x2_unpack(xr[u / 2]);
       const float2 bv = mul2(make_float2(m4[2 * q], m4[2 * q + 1]), xv);
-      // at a sequence start the state before the token is the sequence's initial state
-      if (VARLEN && GENERAL && ((sq.smask >> u) & 1u)) h = seqb_h0(sq, u);
       h4[2 * q] = h;
       h = fmaf(ab[u / 2].x, h, bv.x);
-      if (VARLEN && GENERAL && ((sq.smask >> (u + 1)) & 1u)) h = seqb_h0(sq, u + 1);
       h4[2 * q + 1] = h;
       h = fmaf(ab[u / 2].y, h, bv.y);
     }
@@ -378,13 +327,12 @@ struct DlOut {
   int valid;    // tokens of the part before T (and a real channel: else 0)
 };
 
-template <bool GENERAL, bool VARLEN, typename GT = float, int LGM = LGM_NONE>
+template <typename GT = float, int LGM = LGM_NONE>
 __device__ __forceinline__ void bwd_pass2b(uint32_t tcol, int tb, int j,
                                            const uint32_t (&xr)[PT / 2], uint32_t dyb, float nk,
-                                           int valid, const float2 (&ab)[PT / 2], const SeqB& sq,
-                                           float cin, uint64_t* lg_free,
-                                           uint8_t* s_dl, float2& dsp, float2& dba, float2& dbx,
-                                           const DlOut& dlo = DlOut{}) {
+                                           const float2 (&ab)[PT / 2], float cin,
+                                           uint64_t* lg_free, uint8_t* s_dl, float2& dsp,
+                                           float2& dba, float2& dbx, const DlOut& dlo = DlOut{}) {
   static_assert(PT / GRP >= 2, "the logits columns are released after the second-to-last group");
   float gnext = cin, anext = 1.0f;
   constexpr int G0 = PT / GRP - 1;
@@ -398,65 +346,36 @@ __device__ __forceinline__ void bwd_pass2b(uint32_t tcol, int tb, int j,
   tc::reg_fence(r4);
   tc::reg_fence(i4);
   tc::reg_fence(h4);
-  // The general packed-sequence variant loads each group when it needs it (no prefetch of
-  // the next): its extra loads and addresses would otherwise raise the register peak of the
-  // whole kernel.
-  constexpr bool PREF = !(VARLEN && GENERAL);
 #pragma unroll
   for (int g = G0; g >= 0; --g) {
     float nm[GRP], nr[GRP], ni[GRP], nh[GRP];
-    if (PREF && g > 0) {
+    if (g > 0) {
       tc::tmem_ld(tcol + COL_LR + (g - 1) * GRP, nm);
       tc::tmem_ld(tcol + COL_LI + (g - 1) * GRP, nr);
       tc::tmem_ld(tcol + COL_HP + (g - 1) * GRP, ni);
       tc::tmem_ld(tcol + COL_DX + (g - 1) * GRP, nh);
     }
     float2 o_r[GRP / 2], o_i[GRP / 2];  // tokens (u, u + 1) of the two pairs
-    float dyg[GRP];  // packed-sequence kernels: the group's dy first, as in pass 1
-    if (VARLEN) {
-#pragma unroll
-      for (int q = GRP / 2 - 1; q >= 0; --q) {
-        const int u = g * GRP + 2 * q;
-        dyg[2 * q + 1] = lds_bf16(dyb + (u + 1) * DY_ROW);
-        dyg[2 * q] = lds_bf16(dyb + u * DY_ROW);
-      }
-    }
 #pragma unroll
     for (int q = GRP / 2 - 1; q >= 0; --q) {
       const int u = g * GRP + 2 * q;
       const float2 xv = bf16x2_unpack(xr[u / 2]);
-      float2 dyv = VARLEN ? make_float2(dyg[2 * q], dyg[2 * q + 1])
-                          : make_float2(lds_bf16(dyb + u * DY_ROW), lds_bf16(dyb + (u + 1) * DY_ROW));
-      if (GENERAL) {
-        if (VARLEN) {
-          if ((sq.emask >> u) & 1u) dyv.x += seqb_dhT(sq, u);
-          if ((sq.emask >> (u + 1)) & 1u) dyv.y += seqb_dhT(sq, u + 1);
-        }
-        if (u >= valid) dyv.x = 0.0f;
-        if (u + 1 >= valid) dyv.y = 0.0f;
-      }
+      const float2 dyv =
+          make_float2(lds_bf16(dyb + u * DY_ROW), lds_bf16(dyb + (u + 1) * DY_ROW));
       const float2 abar = ab[u / 2];
-      const float2 ach = (VARLEN && GENERAL) ? chain_decay(sq, u, abar) : abar;  // 0 at starts
       const float2 mi = make_float2(m4[2 * q], m4[2 * q + 1]);
       const float2 r = make_float2(r4[2 * q], r4[2 * q + 1]);
       const float2 i = make_float2(i4[2 * q], i4[2 * q + 1]);
       float2 gv;
       gv.y = fmaf(anext, gnext, dyv.y);
-      gv.x = fmaf(ach.y, gv.y, dyv.x);
+      gv.x = fmaf(abar.y, gv.y, dyv.x);
       gnext = gv.x;
-      anext = ach.x;
-      if (VARLEN && GENERAL && sq.p.dh0s) {  // d h0[s] = a g at the sequence's first token
-        float* dh0 = sq.p.dh0s + sq.w;
-        const int32_t* st = sq.p.seq_start + sq.t0;
-        if (((sq.smask >> u) & 1u) && sq.ok) dh0[(size_t)st[u] * sq.p.W] = abar.x * gv.x;
-        if (((sq.smask >> (u + 1)) & 1u) && sq.ok) dh0[(size_t)st[u + 1] * sq.p.W] = abar.y * gv.y;
-      }
-      // d h_t / d la = abar (h_{t-1} - abar x i / m) with i / m = i^2 / (m i); zero at reset
-      // tokens (abar = 0), past T and where the decay is exactly 1 (m = 0)
+      anext = abar.x;
+      // d h_t / d la = abar (h_{t-1} - abar x i / m) with i / m = i^2 / (m i) (m i > 0 on the
+      // fast path)
       const float2 nw = mul2(mul2(i, i), make_float2(rcp_approx(-mi.x), rcp_approx(-mi.y)));
-      float2 alpha = mul2(abar, fma2(mul2(abar, xv), nw, make_float2(h4[2 * q], h4[2 * q + 1])));
-      if (GENERAL && (abar.x == 0.0f || mi.x == 0.0f)) alpha.x = 0.0f;
-      if (GENERAL && (abar.y == 0.0f || mi.y == 0.0f)) alpha.y = 0.0f;
+      const float2 alpha =
+          mul2(abar, fma2(mul2(abar, xv), nw, make_float2(h4[2 * q], h4[2 * q + 1])));
       const float2 dla = mul2(gv, alpha);
       const float2 dd = mul2(gv, mi);  // direct dx term
       o_r[q] = mul2(mul2(dla, bc2(nk)), mul2(r, fma2(r, bc2(-1.0f), bc2(1.0f))));
@@ -483,12 +402,6 @@ __device__ __forceinline__ void bwd_pass2b(uint32_t tcol, int tb, int j,
       }
     }
     tc::tmem_st(tcol + COL_DX + g * GRP, h4);
-    if (!PREF && g > 0) {
-      tc::tmem_ld(tcol + COL_LR + (g - 1) * GRP, nm);
-      tc::tmem_ld(tcol + COL_LI + (g - 1) * GRP, nr);
-      tc::tmem_ld(tcol + COL_HP + (g - 1) * GRP, ni);
-      tc::tmem_ld(tcol + COL_DX + (g - 1) * GRP, nh);
-    }
     if (g > 0) {
       tc::tmem_ld_wait();
       tc::reg_fence(nm);
@@ -1014,7 +927,7 @@ __global__ void __maxnreg__(MAXREG)
         valid = min(FUSED_C, p.T - c * FUSED_C) - tb;
         fast = near_all && rmask == 0u && (smask | emask) == 0u && valid >= PT;
         if (fast)
-          bwd_pass1<false, VARLEN>(tcol, xb0, xb1, dyb, gk, 0u, PT, ab, xr, SeqB{p, 0u, 0u, 0, 0}, P, fB, S);
+          bwd_pass1(tcol, xb0, xb1, dyb, gk, ab, xr, P, fB, S);
         else
           bwd_pass1_gen<VARLEN>(tcol, xb0, xb1, dyb, gk, rmask, valid, seqb(smask, emask, b, c),
                                 P, fB, S);
@@ -1101,7 +1014,7 @@ __global__ void __maxnreg__(MAXREG)
         bwd_pass2a_gen<VARLEN>(tcol, xb0, xb1, gk, rmask, valid, seqb(smask, emask, b, c),
                                fmaf(Fa, hin_tile, Fb));
       else
-        bwd_pass2a<false, VARLEN>(tcol, xr, ab, SeqB{p, 0u, 0u, 0, 0}, fmaf(Fa, hin_tile, Fb));
+        bwd_pass2a(tcol, xr, ab, fmaf(Fa, hin_tile, Fb));
 
       if (part == 0) {
         const float cin =
@@ -1125,9 +1038,8 @@ __global__ void __maxnreg__(MAXREG)
                       ((size_t)b * p.T + (size_t)c * FUSED_C + tb) * p.W + w, p.W,
                       wok ? valid : 0};
       if (fast)
-        bwd_pass2b<false, VARLEN, GT, LGM>(tcol, tb, j, xr, dyb, gk.nk, PT, ab,
-                                           SeqB{p, 0u, 0u, 0, 0}, cin, lg_empty, s_dl, dsp, dba,
-                                           dbx, dlo);
+        bwd_pass2b<GT, LGM>(tcol, tb, j, xr, dyb, gk.nk, ab, cin, lg_empty, s_dl, dsp, dba, dbx,
+                            dlo);
       else
         bwd_pass2b_gen<VARLEN, GT, LGM>(tcol, tb, j, xb0, xb1, dyb, gk, rmask, valid,
                                         seqb(smask, emask, b, c), cin, lg_empty, s_dl, dsp, dba,
