@@ -113,8 +113,9 @@ struct Ctl {
 // token pairs (u, u + 1) in the two lanes of f32x2 operations (adjacent TMEM columns land in
 // adjacent registers); the recurrence itself is a scalar chain.  The state after each token
 // (hl) and the product of abar up to it (Ac) are parked in TMEM as they are made, over the
-// logits just read (hl over lr, Ac over li); (rA, rh) = the part's map.  GENERAL handles resets, tokens past
-// T and decays with la <= -1/8; the fast variant (chosen warp-uniformly) has none.
+// logits just read (hl over lr, Ac over li); (rA, rh) = the part's map.  This is the fast
+// variant (chosen warp-uniformly): no reset, every token before T, every decay with la > -1/8;
+// local_scan_gen below handles the others.
 constexpr int GRP = 8;  // tokens per TMEM load / store group
 // Sequence starts (smask): the token continues from its sequence's initial state instead of
 // the carried one, h -> a h0[s] + m i x.
@@ -127,11 +128,8 @@ struct SeqStarts {
 __device__ __forceinline__ float seq_h0(const SeqStarts& sq, int u) {
   return sq.h0 ? sq.h0[(size_t)sq.seq[u] * sq.W] : 0.0f;
 }
-template <bool GENERAL, bool VARLEN>
 __device__ __forceinline__ void local_scan(uint32_t t_lr, uint32_t t_li, uint32_t xb0,
-                                           uint32_t xb1, const GateK& gk,
-                                           uint32_t rmask, int valid, const SeqStarts& sq,
-                                           float& rh, float& rA) {
+                                           uint32_t xb1, const GateK& gk, float& rh, float& rA) {
   rh = 0.0f;
   rA = 1.0f;
   // the logits of group g + 1 are requested before group g is computed
@@ -155,39 +153,8 @@ __device__ __forceinline__ void local_scan(uint32_t t_lr, uint32_t t_li, uint32_
       const float2 lr = make_float2(vr[2 * q], vr[2 * q + 1]);
       const float2 li = make_float2(vi[2 * q], vi[2 * q + 1]);
       float2 abar, mi, r;
-      if (GENERAL) {
-        float2 i;
-        gates_any2(lr, li, gk, abar, mi, r, i);
-        if ((rmask >> u) & 1u) {
-          abar.x = 0.0f;
-          mi.x = i.x;
-        }
-        if ((rmask >> (u + 1)) & 1u) {
-          abar.y = 0.0f;
-          mi.y = i.y;
-        }
-        if (u >= valid) {
-          abar.x = 1.0f;
-          mi.x = 0.0f;
-        }
-        if (u + 1 >= valid) {
-          abar.y = 1.0f;
-          mi.y = 0.0f;
-        }
-      } else {
-        gates_near2(lr, li, gk, abar, mi, r);
-      }
-      float2 bv = mul2(mi, xv);
-      if (VARLEN && GENERAL && sq.smask) {
-        if ((sq.smask >> u) & 1u) {
-          bv.x = fmaf(abar.x, seq_h0(sq, u), bv.x);
-          abar.x = 0.0f;
-        }
-        if ((sq.smask >> (u + 1)) & 1u) {
-          bv.y = fmaf(abar.y, seq_h0(sq, u + 1), bv.y);
-          abar.y = 0.0f;
-        }
-      }
+      gates_near2(lr, li, gk, abar, mi, r);
+      const float2 bv = mul2(mi, xv);
       rh = fmaf(abar.x, rh, bv.x);
       rA *= abar.x;
       oh[2 * q] = rh;
@@ -209,6 +176,73 @@ __device__ __forceinline__ void local_scan(uint32_t t_lr, uint32_t t_li, uint32_
         vi[u] = ni[u];
       }
     }
+  }
+  tc::tmem_st_wait();
+}
+
+// The general variant of the local scan (resets, tokens past T, far decays, sequence starts),
+// on a few tiles a launch: the same arithmetic, walking the token groups in a loop rather
+// than unrolled, which keeps the kernel's code around the fast variant small.
+template <bool VARLEN>
+__device__ __forceinline__ void local_scan_gen(uint32_t t_lr, uint32_t t_li, uint32_t xb0,
+                                               uint32_t xb1, const GateK& gk, uint32_t rmask,
+                                               int valid, const SeqStarts& sq, float& rh,
+                                               float& rA) {
+  rh = 0.0f;
+  rA = 1.0f;
+#pragma unroll 1
+  for (int g = 0; g < PT / GRP; ++g) {
+    float vr[GRP], vi[GRP], oh[GRP], oa[GRP];
+    tc::tmem_ld8(t_lr + g * GRP, vr);
+    tc::tmem_ld8(t_li + g * GRP, vi);
+    tc::tmem_ld_wait();
+    tc::reg_fence(vr);
+    tc::reg_fence(vi);
+#pragma unroll
+    for (int q = 0; q < GRP / 2; ++q) {
+      const int u = g * GRP + 2 * q;  // tokens u, u + 1 of the part
+      const float2 xv = make_float2(tok_elem(xb0, xb1, u), tok_elem(xb0, xb1, u + 1));
+      float2 abar, mi, r, i;
+      gates_any2(make_float2(vr[2 * q], vr[2 * q + 1]), make_float2(vi[2 * q], vi[2 * q + 1]),
+                 gk, abar, mi, r, i);
+      if ((rmask >> u) & 1u) {
+        abar.x = 0.0f;
+        mi.x = i.x;
+      }
+      if ((rmask >> (u + 1)) & 1u) {
+        abar.y = 0.0f;
+        mi.y = i.y;
+      }
+      if (u >= valid) {
+        abar.x = 1.0f;
+        mi.x = 0.0f;
+      }
+      if (u + 1 >= valid) {
+        abar.y = 1.0f;
+        mi.y = 0.0f;
+      }
+      float2 bv = mul2(mi, xv);
+      if (VARLEN && sq.smask) {
+        if ((sq.smask >> u) & 1u) {
+          bv.x = fmaf(abar.x, seq_h0(sq, u), bv.x);
+          abar.x = 0.0f;
+        }
+        if ((sq.smask >> (u + 1)) & 1u) {
+          bv.y = fmaf(abar.y, seq_h0(sq, u + 1), bv.y);
+          abar.y = 0.0f;
+        }
+      }
+      rh = fmaf(abar.x, rh, bv.x);
+      rA *= abar.x;
+      oh[2 * q] = rh;
+      oa[2 * q] = rA;
+      rh = fmaf(abar.y, rh, bv.y);
+      rA *= abar.y;
+      oh[2 * q + 1] = rh;
+      oa[2 * q + 1] = rA;
+    }
+    tc::tmem_st8(t_lr + g * GRP, oh);
+    tc::tmem_st8(t_li + g * GRP, oa);
   }
   tc::tmem_st_wait();
 }
@@ -420,9 +454,9 @@ __global__ void __maxnreg__(MAXREG)
       const uint32_t t_lr = tmem + lane_base + a * 128 + tb;
       float rh, rA;
       if (near_all && rmask == 0u && sq.smask == 0u && valid >= PT)
-        local_scan<false, VARLEN>(t_lr, t_lr + 64, xb0, xb1, gk, 0u, PT, sq, rh, rA);
+        local_scan(t_lr, t_lr + 64, xb0, xb1, gk, rh, rA);
       else
-        local_scan<true, VARLEN>(t_lr, t_lr + 64, xb0, xb1, gk, rmask, valid, sq, rh, rA);
+        local_scan_gen<VARLEN>(t_lr, t_lr + 64, xb0, xb1, gk, rmask, valid, sq, rh, rA);
       s_agg[(a * NPART + part) * FUSED_K + j] = make_float2(rA, rh);  // the part's map
       tc::tc_fence_before();
       __syncwarp();
