@@ -984,6 +984,7 @@ __global__ void __maxnreg__(MAXREG)
           float v[8];
           tc::tmem_ld8(tcol + COL_DX + sub * 8, v);
           tc::tmem_ld_wait();
+          tc::reg_fence(v);  // no use of v moves above the wait
 #pragma unroll
           for (int u = 0; u < 8; ++u) {
             const int tl = tb + sub * 8 + u;
@@ -1077,6 +1078,7 @@ __global__ void __maxnreg__(MAXREG)
         if (my_tiles > 0) {
           tc::tmem_ld16(tcol - tb + (mtx ? COL_DWX : COL_DWA) + col, v);
           tc::tmem_ld_wait();
+          tc::reg_fence(v);
         } else {
 #pragma unroll
           for (int u = 0; u < 16; ++u) v[u] = 0.0f;

@@ -553,6 +553,8 @@ __global__ void __maxnreg__(MAXREG)
             tc::tmem_ld16(park + c16, hl);
             tc::tmem_ld16(park + 64 + c16, Ac);
             tc::tmem_ld_wait();
+            tc::reg_fence(hl);
+            tc::reg_fence(Ac);
 #pragma unroll
             for (int u = 0; u < 16; u += 2) {
               const float2 yv =
@@ -575,9 +577,11 @@ __global__ void __maxnreg__(MAXREG)
             while (m != 0u) {
               const int u = __ffs(m) - 1;
               m &= m - 1u;
-              const float hl = tc::tmem_ld1(park + u);
-              const float Ac = tc::tmem_ld1(park + 64 + u);
+              float hl = tc::tmem_ld1(park + u);
+              float Ac = tc::tmem_ld1(park + 64 + u);
               tc::tmem_ld_wait();
+              tc::reg_fence(hl);
+              tc::reg_fence(Ac);
               const int sidx = __shfl_sync(0xffffffffu, pp == 0 ? e0 : e1, u);
               if (p.hTs && wok) p.hTs[(size_t)sidx * p.W + w] = fmaf(Ac, hin, hl);
             }

@@ -757,6 +757,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           float t[2];
           tc::tmem_ld2(tmem + ((uint32_t)(32 * q) << 16) + mi * MCOLS + MB * KC + 32 * mb, t);
           tc::tmem_ld_wait();
+          tc::reg_fence(t);
           sb = t[0];
         }
         if (j < k) dst[(size_t)k * k + j] = sb;

@@ -340,6 +340,7 @@ __device__ __forceinline__ void reg_fence(float (&v)[N]) {
 #pragma unroll
   for (int i = 0; i < N; ++i) asm volatile("" : "+f"(v[i]));
 }
+__device__ __forceinline__ void reg_fence(float& v) { asm volatile("" : "+f"(v)); }
 
 // ---------------------------------------------------------------- descriptors
 // Shared-memory matrix descriptor (sm_100 format): start address, leading / stride byte
