@@ -19,7 +19,7 @@
 // value slots in `saved` (lookback.cuh), which keeps the result bitwise deterministic.
 //
 // Roles (448 threads, one CTA per SM, launched cooperatively so that all CTAs are resident):
-//   warp 0       TMA producer: Wa[blk], Wx[blk] once, then the x tile ring (3 stages)
+//   warp 0       TMA producer: Wa[blk], Wx[blk] once, then the x tile ring (7 stages)
 //   warp 1       MMA issuer: 2 x 8 tcgen05.mma (K = 16 each) per tile into a 4-deep TMEM ring
 //   warps 2..9   scan: warps 2+4p .. 5+4p take tokens 32p .. 32p+31 (lane quadrant warp % 4),
 //                tile after tile, parking each over its own logits, with no barrier
@@ -47,7 +47,10 @@ constexpr int NTHREADS = 64 + (NSCAN + NOUT) * 32;
 // The warps share the SM's four 16 K-register sub-partitions: registers per thread <= 16384 /
 // (32 x warps per sub-partition), rounded down to a multiple of 8.
 constexpr int MAXREG = (16384 / (((NSCAN + NOUT + 2 + 3) / 4) * 32)) / 8 * 8;
-constexpr int XSTAGES = 3;
+// x tiles in flight: the deepest ring the shared memory holds (the x reads of a tile wait on
+// DRAM under the load of every SM; 3 -> 6 -> 7 stages took the forward call 41.1 -> 39.2 ->
+// 38.6 us)
+constexpr int XSTAGES = 7;
 constexpr uint32_t W_BYTES = FUSED_K * FUSED_K * 2;  // one weight block, bf16
 constexpr uint32_t X_BYTES = FUSED_C * FUSED_K * 2;  // one x tile, bf16
 constexpr uint32_t YSTRIP_BYTES = FUSED_C * 32 * 2;  // y of 64 tokens x 32 channels, bf16
