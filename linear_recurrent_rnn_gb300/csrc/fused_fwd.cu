@@ -69,12 +69,19 @@ constexpr size_t SMEM_BYTES =
 // Given-logits mode (the scan of rglru_forward and of the composed layer): no weights; each
 // stage holds the x tile and up to two bf16 planes of each logit tile, and a 64 x 64 identity
 // takes the place of W in the MMA that lays the logits out in TMEM.
+// A stage holds x and the planes actually given, so one plane a logit (48 KB a stage) gets
+// three stages in the region that two planes (80 KB a stage) fill with two.
 constexpr int LG_PLANES = 2;
-constexpr int LG_STAGES = 2;
-constexpr uint32_t LG_STAGE_BYTES = (1 + 2 * LG_PLANES) * X_BYTES;
+constexpr int LG_STAGES_MAX = 3;
+__host__ __device__ constexpr uint32_t lg_stage_bytes(int nplanes) {
+  return (1 + 2 * nplanes) * X_BYTES;
+}
+__host__ __device__ constexpr int lg_stages(int nplanes) { return nplanes == 1 ? 3 : 2; }
+constexpr uint32_t LG_REGION = 2 * lg_stage_bytes(LG_PLANES);
+static_assert(lg_stages(1) * lg_stage_bytes(1) <= LG_REGION, "one-plane stages fit the region");
+static_assert(lg_stages(1) <= LG_STAGES_MAX && lg_stages(2) <= LG_STAGES_MAX, "barriers");
 constexpr uint32_t ID_BYTES = FUSED_C * FUSED_C * 2;
-constexpr size_t LG_SMEM_BYTES =
-    ID_BYTES + LG_STAGES * LG_STAGE_BYTES + Y_BYTES + XCH_BYTES + 256 + 1024;
+constexpr size_t LG_SMEM_BYTES = ID_BYTES + LG_REGION + Y_BYTES + XCH_BYTES + 256 + 1024;
 constexpr uint32_t STATUS_PIPE = 2u;
 
 struct FwdParams {
@@ -258,21 +265,22 @@ __global__ void __maxnreg__(MAXREG)
     k_fused_fwd(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_wa,
                 const __grid_constant__ CUtensorMap tm_wx, const __grid_constant__ CUtensorMap tm_y,
                 FwdParams p) {
-  constexpr int XS = LG ? LG_STAGES : XSTAGES;
-  constexpr uint32_t STB = LG ? LG_STAGE_BYTES : X_BYTES;
+  const int XS = LG ? lg_stages(p.nplanes) : XSTAGES;           // stages in use
+  const uint32_t STB = LG ? lg_stage_bytes(p.nplanes) : X_BYTES;  // bytes a stage
+  constexpr int XSB = LG ? LG_STAGES_MAX : XSTAGES;               // stage barriers
   extern __shared__ uint8_t smem_raw[];
   // 1024-byte aligned base, formed by pointer arithmetic so that it stays a shared pointer
   uint8_t* smem = smem_raw + ((1024u - (tc::smem_u32(smem_raw) & 1023u)) & 1023u);
   uint8_t* s_wa = smem;            // LG: the identity
   uint8_t* s_wx = smem + W_BYTES;  // (unused in LG)
   uint8_t* s_x = smem + (LG ? ID_BYTES : 2 * W_BYTES);
-  uint8_t* s_y = s_x + XS * STB;
+  uint8_t* s_y = s_x + (LG ? LG_REGION : XSTAGES * X_BYTES);
   float2* s_agg = reinterpret_cast<float2*>(s_y + Y_BYTES);  // [buffer][part][channel]
   uint64_t* bars = reinterpret_cast<uint64_t*>(s_agg + NBUF * NPART * FUSED_K);
   uint64_t* w_full = bars;
   uint64_t* x_full = bars + 1;
-  uint64_t* x_empty = bars + 1 + XS;
-  uint64_t* acc_full = bars + 1 + 2 * XS;
+  uint64_t* x_empty = bars + 1 + XSB;
+  uint64_t* acc_full = bars + 1 + 2 * XSB;
   uint64_t* acc_empty = acc_full + NBUF;  // buffer read out by the output warps
   uint64_t* park_full = acc_empty + NBUF;  // a tile parked in its buffer (scan -> output)
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(park_full + NBUF);
@@ -341,7 +349,7 @@ __global__ void __maxnreg__(MAXREG)
           for (int g = 0; g < 2; ++g)
             for (int pl = 0; pl < p.nplanes; ++pl)
               for (int s = 0; s < FUSED_K / 16; ++s)
-                tc::tma_load_4d(sb + (1 + g * LG_PLANES + pl) * X_BYTES + s * SLAB_X,
+                tc::tma_load_4d(sb + (1 + g * p.nplanes + pl) * X_BYTES + s * SLAB_X,
                                 g ? &tm_wx : &tm_wa, &x_full[st], blk * FUSED_K + 16 * s,
                                 tw.c * FUSED_C, tw.b, pl);
         }
@@ -384,7 +392,7 @@ __global__ void __maxnreg__(MAXREG)
 #pragma unroll
               for (int kk = 0; kk < FUSED_C / 16; ++kk)
                 tc::mma_bf16(g ? d_i : d_r,
-                             tc::smem_desc_sw32(xs + (1 + g * LG_PLANES + pl) * X_BYTES + kk * 512,
+                             tc::smem_desc_sw32(xs + (1 + g * p.nplanes + pl) * X_BYTES + kk * 512,
                                                 SLAB_X, 256),
                              tc::smem_desc_sw32(wa + kk * SLAB_X, 16, 256), idesc,
                              (pl > 0 || kk > 0) ? 1u : 0u);
