@@ -472,6 +472,7 @@ def decode_step(flush, peak, W=2048, k=128, reps=20):
                                     "frac": (gbs / peak) if peak else None,
                                     "algorithmic_bytes": nbytes}
     out["stack_B256"] = decode_stack(flush, peak, W, k)
+    out["stack_B1"] = decode_stack(flush, peak, W, k, B=1, L=160)
     return out
 
 
@@ -480,8 +481,9 @@ def decode_stack(flush, peak, W=2048, k=128, B=256, L=48, reps=10):
     constants and carried states, and layer l's y is layer l + 1's x.  The L steps are captured
     once in a CUDA graph and replayed, the L2 flushed before each replay, so the steps follow
     one another on the GPU as in a graph-captured serving loop.  Weights and states of all
-    layers (L x 4 MB) exceed the L2, so each step reads its operands from HBM.  Reports
-    microseconds per layer step and its bytes against the measured copy bandwidth."""
+    layers exceed the L2 (48 x 4 MB at batch 256, 160 x 1 MB at batch 1), so each step reads
+    its operands from HBM.  Reports microseconds per layer step and its bytes against the
+    measured copy bandwidth."""
     import torch
     from linear_recurrent_rnn_gb300 import librglru as R
     from linear_recurrent_rnn_gb300.inputs import Workload, generate

@@ -219,10 +219,10 @@ rglru_status rglru_fused_backward_varlen(const rglru_shape *shape, const void *d
  * x, y [B, W] and Wa, Wx in shape.io; h_in, h_out [B, W] float32 (h_in NULL = zeros; h_out
  * may be h_in, updated in place); reset uint8 [B] (nonzero = the token starts a segment; NULL
  * = none; canonical mode only); ba, bx may be NULL.  k = W / nblk <= 512 (else
- * RGLRU_ERR_UNSUPPORTED).  One kernel, no scratch.  From batch 64 (bf16, k a multiple of 32)
- * the kernel is launched with programmatic stream serialisation: its set-up may overlap the
- * end of the kernel before it on the stream, but it reads and writes no memory before that
- * kernel has completed, so stream order holds for every argument. */
+ * RGLRU_ERR_UNSUPPORTED).  One kernel, no scratch, launched with programmatic stream
+ * serialisation: its launch and set-up may overlap the end of the kernel before it on the
+ * stream, but it reads and writes no memory before that kernel has completed, so stream order
+ * holds for every argument. */
 rglru_status rglru_step(const rglru_shape *shape, const void *x, const void *Wa,
                         const float *ba, const void *Wx, const float *bx, const float *Lambda,
                         const uint8_t *reset, const float *h_in, void *y, float *h_out,

@@ -61,6 +61,10 @@ __device__ __forceinline__ float ld_elem(const void* p, size_t i) {
 template <typename T>
 __global__ void __launch_bounds__(DEC_WARPS * 32) k_step(DecArgs a) {
   extern __shared__ float sm[];
+  // launched with programmatic stream serialisation: the launch overlaps the end of the kernel
+  // before it on the stream; every read and write of the step comes after the wait
+  tc::griddep_wait();
+  tc::griddep_launch_dependents();
   const int k = a.k;
   const int nsl = (k + 31) / 32;
   const int blk = blockIdx.x / nsl, j0 = (blockIdx.x % nsl) * 32;
@@ -449,12 +453,22 @@ cudaError_t launch_step(const Dims& d, const void* x, const void* Wa, const floa
   const size_t smem = step_smem_bytes(d.k);
   const dim3 grid((unsigned)(d.nblk * ((d.k + 31) / 32)), (unsigned)((d.B + DEC_ROWS - 1) / DEC_ROWS));
   cudaError_t e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(DEC_WARPS * 32);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
   if (d.io == RGLRU_BF16) {
     e = cudaFuncSetAttribute(k_step<bf16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e == cudaSuccess) k_step<bf16><<<grid, DEC_WARPS * 32, smem, s>>>(a);
+    if (e == cudaSuccess) e = cudaLaunchKernelEx(&cfg, k_step<bf16>, a);
   } else {
     e = cudaFuncSetAttribute(k_step<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e == cudaSuccess) k_step<float><<<grid, DEC_WARPS * 32, smem, s>>>(a);
+    if (e == cudaSuccess) e = cudaLaunchKernelEx(&cfg, k_step<float>, a);
   }
   if (e != cudaSuccess) return e;
   note_launches(1);
